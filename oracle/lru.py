@@ -1,0 +1,161 @@
+"""Shared all-layer LRU expert cache (oracle simulator).
+
+FreeToken write-up, "router-following LRU cache" and "CUDA Graph-compatible LRU
+cache" sections:
+* one GPU expert cache shared by every MoE layer; a slot holds one
+  (layer, expert) pair, addressed by the flat key ``l*E + e``;
+* a hit refreshes the expert's recency, a fill admits the newly selected
+  expert, an eviction removes the expert the model has not asked for for the
+  longest time;
+* per layer one pass deduplicates the routed experts, classifies them against
+  the residency table, picks K victim slots at once (the miss path takes the
+  first q <= K of them) and rewrites logical ids to slot ids.
+"Elastic memory management" section: at a safe point the cache is rebuilt to
+a new slot budget without touching the host pool.
+
+Readings where the pages are silent (each one is a plain deterministic choice):
+* U = the sorted distinct experts routed by the B tokens of the call.  Every
+  member of U is classified against the state *before* the call.
+* Recency is a stamp from a global counter g: the member of U with rank r gets
+  stamp g + r, hit or miss; then g += |U|.  Stamps are unique.
+* Victims: among slots not holding a hit of this call, empty slots come first
+  (lowest index first), then occupied slots by ascending stamp.  The i-th miss
+  in ascending expert order takes the i-th victim.  A miss never evicts an
+  expert routed in the same call.
+* |U| > C is a capacity error and leaves the state unchanged.
+* Resize to C' < C keeps the C' most recently used experts; the others are
+  evicted in ascending slot order; survivors sitting in slots >= C' move, in
+  ascending old-slot order, into the vacant slots < C' in ascending order.
+  Growing appends empty slots.  Stamps, the map and g are preserved.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import numpy as np
+
+HIT, MISS, RESIZE_EVICT = 0, 1, 2
+
+
+class CapacityError(RuntimeError):
+    pass
+
+
+@dataclass(frozen=True)
+class Event:
+    call: int
+    layer: int
+    expert: int
+    kind: int
+    slot: int
+    evicted_key: int  # -1 if none
+
+    def as_tuple(self):
+        return (self.call, self.layer, self.expert, self.kind, self.slot, self.evicted_key)
+
+
+class CacheSim:
+    """Stamp-based simulator of the shared expert cache's bookkeeping."""
+
+    def __init__(self, L: int, E: int, C: int):
+        if C < 0:
+            raise ValueError("C >= 0")
+        self.L, self.E, self.C = L, E, C
+        self.map = np.full(L * E, -1, dtype=np.int64)
+        self.owner = np.full(C, -1, dtype=np.int64)
+        self.stamp = np.zeros(C, dtype=np.uint64)
+        self.g = 0
+        self.calls = 0
+
+    # -- one layer call ------------------------------------------------------
+    def access(self, layer: int, ids: np.ndarray) -> tuple[list[Event], np.ndarray]:
+        """Process the routed ids [B, k] of one layer call.
+
+        Returns the events (one per distinct expert, ascending expert order)
+        and slot_ids [B, k] (the logical ids rewritten to slot ids).
+        """
+        E = self.E
+        ids = np.asarray(ids)
+        U = sorted(set(int(e) for e in ids.reshape(-1)))
+        if len(U) > self.C:
+            raise CapacityError(f"{len(U)} distinct experts > {self.C} slots")
+        call = self.calls
+        keys = [layer * E + e for e in U]
+        hit_slot = {key: int(self.map[key]) for key in keys if self.map[key] >= 0}
+        taken = set(hit_slot.values())
+        misses = [key for key in keys if key not in hit_slot]
+        victims = []
+        if misses:
+            # order the candidate slots by (0, slot) if empty else (1, stamp)
+            slots = np.arange(self.C)
+            cand = slots[~np.isin(slots, list(taken))]
+            occupied = (self.owner[cand] >= 0).astype(np.int64)
+            secondary = np.where(occupied == 1, self.stamp[cand].astype(np.int64), cand)
+            order = np.lexsort((secondary, occupied))
+            victims = [int(s) for s in cand[order][:len(misses)]]
+        events, slot_of = [], {}
+        mi = 0
+        for r, (e, key) in enumerate(zip(U, keys)):
+            if key in hit_slot:
+                s = hit_slot[key]
+                self.stamp[s] = np.uint64(self.g + r)
+                events.append(Event(call, layer, e, HIT, s, -1))
+            else:
+                s = victims[mi]
+                mi += 1
+                ev = int(self.owner[s])
+                if ev >= 0:
+                    self.map[ev] = -1
+                self.map[key] = s
+                self.owner[s] = key
+                self.stamp[s] = np.uint64(self.g + r)
+                events.append(Event(call, layer, e, MISS, s, ev))
+            slot_of[e] = s
+        self.g += len(U)
+        self.calls += 1
+        slot_ids = np.vectorize(lambda e: slot_of[int(e)], otypes=[np.int64])(ids) if ids.size else ids
+        return events, slot_ids
+
+    # -- safe-point resize ---------------------------------------------------
+    def resize(self, C_new: int) -> list[Event]:
+        """Rebuild the cache with C_new slots; returns RESIZE_EVICT events (ascending slot)."""
+        C = self.C
+        events = []
+        if C_new >= C:
+            self.owner = np.concatenate([self.owner, np.full(C_new - C, -1, dtype=np.int64)])
+            self.stamp = np.concatenate([self.stamp, np.zeros(C_new - C, dtype=np.uint64)])
+            self.C = C_new
+            return events
+        occupied = [s for s in range(C) if self.owner[s] >= 0]
+        by_recency = sorted(occupied, key=lambda s: -int(self.stamp[s]))
+        keep = set(by_recency[:C_new])
+        for s in sorted(occupied):
+            if s not in keep:
+                key = int(self.owner[s])
+                events.append(Event(self.calls, key // self.E, key % self.E, RESIZE_EVICT, s, key))
+                self.map[key] = -1
+                self.owner[s] = -1
+                self.stamp[s] = 0
+        movers = sorted(s for s in keep if s >= C_new)
+        vacant = sorted(s for s in range(C_new) if self.owner[s] < 0)
+        assert len(vacant) >= len(movers)
+        for src, dst in zip(movers, vacant):
+            key = int(self.owner[src])
+            self.owner[dst] = key
+            self.stamp[dst] = self.stamp[src]
+            self.map[key] = dst
+            self.owner[src] = -1
+        self.owner = self.owner[:C_new].copy()
+        self.stamp = self.stamp[:C_new].copy()
+        self.C = C_new
+        return events
+
+    def resident_keys(self) -> set[int]:
+        return {int(k) for k in self.owner if k >= 0}
+
+
+def hit_rate(events: list[Event]) -> float:
+    """hits / (hits + misses) over distinct (call, layer, expert) accesses."""
+    h = sum(1 for e in events if e.kind == HIT)
+    m = sum(1 for e in events if e.kind == MISS)
+    return h / (h + m) if h + m else float("nan")

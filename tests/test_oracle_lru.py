@@ -1,0 +1,208 @@
+"""Pins for the oracle's cache simulator (oracle.lru).
+
+The simulator picks victims for a whole call in one pass over stamps.  It is
+checked against an independently written ordered-list LRU that processes the
+call's distinct experts one by one (the classic move-to-front formulation of
+"evict the expert not requested for the longest time"), exhaustively on tiny
+traces and on random ones, plus the invariants the pages fix: a hit never
+misses while resident, a cache that holds every (layer, expert) pair never
+evicts, and GPU memory changes performance only.
+"""
+import itertools
+import random
+
+import numpy as np
+import pytest
+
+from oracle import lru
+
+
+class ListLRU:
+    """Brute-force LRU: an ordered list of keys, least recent first."""
+
+    def __init__(self, L, E, C):
+        self.L, self.E, self.C = L, E, C
+        self.order = []
+        self.slot = {}
+        self.calls = 0
+
+    def access(self, layer, ids):
+        U = sorted(set(int(e) for e in np.asarray(ids).reshape(-1)))
+        if len(U) > self.C:
+            raise lru.CapacityError()
+        keys = [layer * self.E + e for e in U]
+        call_keys = set(keys)
+        out = []
+        for e, key in zip(U, keys):
+            if key in self.slot:
+                self.order.remove(key)
+                self.order.append(key)
+                out.append((self.calls, layer, e, lru.HIT, self.slot[key], -1))
+                continue
+            used = set(self.slot.values())
+            free = [s for s in range(self.C) if s not in used]
+            if free:
+                s, ev = free[0], -1
+            else:
+                ev = next(k for k in self.order if k not in call_keys)
+                self.order.remove(ev)
+                s = self.slot.pop(ev)
+            self.slot[key] = s
+            self.order.append(key)
+            out.append((self.calls, layer, e, lru.MISS, s, ev))
+        self.calls += 1
+        return out
+
+    def resize(self, C_new):
+        if C_new >= self.C:
+            self.C = C_new
+            return []
+        keep = set(self.order[-C_new:]) if C_new > 0 else set()
+        out = []
+        for key, s in sorted(self.slot.items(), key=lambda kv: kv[1]):
+            if key not in keep:
+                out.append((self.calls, key // self.E, key % self.E, lru.RESIZE_EVICT, s, key))
+        for _, _, _, _, s, key in out:
+            del self.slot[key]
+            self.order.remove(key)
+        used = set(self.slot.values())
+        vacant = [s for s in range(C_new) if s not in used]
+        movers = sorted((s, k) for k, s in self.slot.items() if s >= C_new)
+        for (s, k), d in zip(movers, vacant):
+            self.slot[k] = d
+        self.C = C_new
+        return out
+
+
+def run_both(L, E, C, trace):
+    a, b = lru.CacheSim(L, E, C), ListLRU(L, E, C)
+    ea, eb = [], []
+    for layer, ids in trace:
+        try:
+            ev, _ = a.access(layer, ids)
+            ea += [e.as_tuple() for e in ev]
+        except lru.CapacityError:
+            ea.append("cap")
+        try:
+            eb += b.access(layer, ids)
+        except lru.CapacityError:
+            eb.append("cap")
+    return ea, eb
+
+
+def test_exhaustive_single_layer_k1():
+    # every trace of length 6 over 3 experts, one expert per call, C = 1..3
+    for C in (1, 2, 3):
+        for seq in itertools.product(range(3), repeat=6):
+            trace = [(0, np.array([[e]])) for e in seq]
+            ea, eb = run_both(1, 3, C, trace)
+            assert ea == eb, (C, seq)
+
+
+def test_exhaustive_two_layers_k2():
+    # two layers alternating, two experts routed per call out of 3, C = 2..4
+    pairs = [(0, 1), (0, 2), (1, 2), (1, 1), (2, 0)]
+    for C in (2, 3, 4):
+        for seq in itertools.product(range(len(pairs)), repeat=4):
+            trace = [(i % 2, np.array([pairs[p]])) for i, p in enumerate(seq)]
+            ea, eb = run_both(2, 3, C, trace)
+            assert ea == eb, (C, seq)
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_random_traces(seed):
+    rng = random.Random(seed)
+    L, E = 3, 10
+    C = rng.choice([4, 7, 12, 30])
+    trace = []
+    for _ in range(300):
+        B, k = rng.choice([(1, 2), (2, 2), (3, 1), (2, 3)])
+        trace.append((rng.randrange(L), np.array([[rng.randrange(E) for _ in range(k)] for _ in range(B)])))
+    ea, eb = run_both(L, E, C, trace)
+    assert ea == eb
+
+
+def test_resize_matches_list_truncation():
+    rng = random.Random(3)
+    L, E, C = 2, 12, 10
+    a, b = lru.CacheSim(L, E, C), ListLRU(L, E, C)
+    for phase, C_new in enumerate([10, 4, 9, 3, 3, 11]):
+        if phase:
+            ra = [e.as_tuple() for e in a.resize(C_new)]
+            rb = b.resize(C_new)
+            assert ra == rb
+            assert {k: s for s, k in enumerate(a.owner) if k >= 0} == b.slot
+        for _ in range(60):
+            layer = rng.randrange(L)
+            ids = np.array([[rng.randrange(E), rng.randrange(E)]])
+            ev, _ = a.access(layer, ids)
+            assert [e.as_tuple() for e in ev] == b.access(layer, ids)
+
+
+def test_resize_keeps_most_recent_and_preserves_stamps():
+    sim = lru.CacheSim(1, 8, 6)
+    for e in [0, 1, 2, 3, 4, 5, 1, 3]:
+        sim.access(0, np.array([[e]]))
+    stamps = {int(k): int(sim.stamp[s]) for s, k in enumerate(sim.owner) if k >= 0}
+    g = sim.g
+    ev = sim.resize(3)
+    assert sim.resident_keys() == {3, 1, 5}
+    assert [e.expert for e in ev] == [0, 2, 4]  # ascending slot order: slots 0, 2, 4
+    assert sim.g == g
+    for s, k in enumerate(sim.owner):
+        if k >= 0:
+            assert int(sim.stamp[s]) == stamps[int(k)]
+            assert sim.map[k] == s
+
+
+def test_all_resident_means_no_miss():
+    rng = np.random.default_rng(0)
+    sim = lru.CacheSim(2, 16, 10)
+    for _ in range(200):
+        layer = int(rng.integers(2))
+        ids = rng.integers(0, 16, size=(2, 2))
+        resident = set(int(k) for k in sim.owner if k >= 0)
+        keys = {layer * 16 + int(e) for e in ids.reshape(-1)}
+        ev, _ = sim.access(layer, ids)
+        if keys <= resident:
+            assert all(e.kind == lru.HIT for e in ev)
+
+
+def test_full_capacity_never_evicts():
+    rng = np.random.default_rng(1)
+    L, E = 3, 8
+    sim = lru.CacheSim(L, E, L * E)
+    for _ in range(400):
+        ev, _ = sim.access(int(rng.integers(L)), rng.integers(0, E, size=(3, 2)))
+        assert all(e.evicted_key == -1 for e in ev)
+
+
+def test_capacity_error_leaves_state_unchanged():
+    sim = lru.CacheSim(1, 8, 2)
+    sim.access(0, np.array([[1, 2]]))
+    snap = (sim.map.copy(), sim.owner.copy(), sim.stamp.copy(), sim.g, sim.calls)
+    with pytest.raises(lru.CapacityError):
+        sim.access(0, np.array([[3, 4], [5, 3]]))
+    assert (sim.map == snap[0]).all() and (sim.owner == snap[1]).all() and (sim.stamp == snap[2]).all()
+    assert (sim.g, sim.calls) == snap[3:]
+
+
+def test_hand_worked_trace():
+    # C = 2, one layer, experts: 0, 1, 0, 2, 1.
+    # call0: 0 miss -> slot 0; call1: 1 miss -> slot 1; call2: 0 hit;
+    # call3: 2 miss, LRU is 1 (slot 1); call4: 1 miss, LRU is 0 (slot 0).
+    sim = lru.CacheSim(1, 4, 2)
+    got = []
+    for e in [0, 1, 0, 2, 1]:
+        ev, slots = sim.access(0, np.array([[e]]))
+        got += [(x.kind, x.slot, x.evicted_key) for x in ev]
+    assert got == [(1, 0, -1), (1, 1, -1), (0, 0, -1), (1, 1, 1), (1, 0, 0)]
+    assert lru.hit_rate([lru.Event(0, 0, 0, k, 0, -1) for k in (0, 0, 1, 0)]) == 0.75
+
+
+def test_slot_ids_rewrite():
+    sim = lru.CacheSim(1, 8, 4)
+    ids = np.array([[5, 2], [2, 7]])
+    ev, slots = sim.access(0, ids)
+    slot_of = {e.expert: e.slot for e in ev}
+    assert (slots == np.vectorize(slot_of.get)(ids)).all()
