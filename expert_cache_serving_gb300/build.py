@@ -1,0 +1,76 @@
+"""In-tree build of the CUDA library (sm_103a) and of the C input generator.
+
+Every translation unit is compiled in parallel and linked into
+``expert_cache_serving_gb300/_lib/libmoecache.so`` (CUDA runtime linked
+statically, so the library loads without a GPU driver) and
+``synth/_lib/libsynth.so``.
+"""
+from __future__ import annotations
+
+import concurrent.futures as cf
+import glob
+import os
+import shutil
+import subprocess
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+ROOT = os.path.dirname(PKG)
+CSRC = os.path.join(PKG, "csrc")
+LIBDIR = os.path.join(PKG, "_lib")
+OBJDIR = os.path.join(LIBDIR, "obj")
+LIB = os.path.join(LIBDIR, "libmoecache.so")
+SYNTH_SRC = os.path.join(ROOT, "synth", "synth.c")
+SYNTH_LIB = os.path.join(ROOT, "synth", "_lib", "libsynth.so")
+
+ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
+NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2", "--expt-relaxed-constexpr",
+              "-I" + os.path.join(ROOT, "include"), "-I" + CSRC]
+
+
+def _nvcc() -> str:
+    for cand in (os.environ.get("NVCC"), shutil.which("nvcc"), "/usr/local/cuda/bin/nvcc"):
+        if cand and os.path.exists(cand):
+            return cand
+    raise RuntimeError("nvcc not found")
+
+
+def _run(cmd, verbose):
+    if verbose:
+        print(" ".join(cmd), flush=True)
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError(f"build step failed: {' '.join(cmd)}\n{r.stdout}\n{r.stderr}")
+    return r
+
+
+def build_synth(verbose=False) -> str:
+    os.makedirs(os.path.dirname(SYNTH_LIB), exist_ok=True)
+    _run(["gcc", "-O3", "-fPIC", "-shared", "-ffp-contract=off", "-pthread", SYNTH_SRC, "-o", SYNTH_LIB], verbose)
+    return SYNTH_LIB
+
+
+def build_cuda(verbose=False) -> str:
+    os.makedirs(OBJDIR, exist_ok=True)
+    nvcc = _nvcc()
+    srcs = sorted(glob.glob(os.path.join(CSRC, "*.cu")) + glob.glob(os.path.join(CSRC, "*.cpp")))
+    if not srcs:
+        raise RuntimeError("no CUDA sources")
+    objs = []
+    jobs = []
+    with cf.ThreadPoolExecutor(max_workers=min(16, len(srcs))) as ex:
+        for s in srcs:
+            o = os.path.join(OBJDIR, os.path.basename(s) + ".o")
+            objs.append(o)
+            cmd = [nvcc] + ARCH + NVCC_FLAGS + ["-c", s, "-o", o]
+            if s.endswith(".cpp"):
+                cmd = [nvcc] + NVCC_FLAGS + ["-x", "cu", "-c", s, "-o", o] + ARCH
+            jobs.append(ex.submit(_run, cmd, verbose))
+        for j in jobs:
+            j.result()
+    _run([nvcc] + ARCH + ["-shared", "-cudart", "static", "-o", LIB] + objs + ["-lpthread", "-ldl", "-lrt"], verbose)
+    return LIB
+
+
+def build_all(verbose=False) -> None:
+    build_synth(verbose)
+    build_cuda(verbose)

@@ -1,0 +1,726 @@
+// Host side of the moecache C ABI: the shared expert cache (slot memory,
+// residency state), the per-call orchestration of control kernel, fills and
+// expert-FFN launches, safe-point resize, statistics and tracing.
+//
+// FreeToken write-up, "FreeToken's design": the host expert pool is the source
+// of truth and the remaining GPU memory becomes one elastic expert cache shared
+// by every MoE layer; "elastic memory management": the cache is rebuilt to a
+// new budget at a safe point without reloading the pool.  Slot memory is one
+// reserved virtual range mapped in physical chunks, so a resize maps or
+// unmaps the tail while the resident prefix stays where it is.
+#include <cuda.h>
+
+#include <algorithm>
+#include <atomic>
+#include <chrono>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <new>
+#include <string>
+#include <thread>
+#include <vector>
+
+#include "params.cuh"
+
+using namespace moe;
+
+// ------------------------------------------------------------------ errors --
+static thread_local std::string g_err;
+
+static moe_status fail(moe_status st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_err = buf;
+  return st;
+}
+
+#define CU_TRY(expr)                                                                      \
+  do {                                                                                    \
+    cudaError_t _e = (expr);                                                              \
+    if (_e != cudaSuccess) return fail(MOE_ERR_CUDA, "%s: %s", #expr, cudaGetErrorString(_e)); \
+  } while (0)
+
+// --------------------------------------------------------- driver entry points --
+namespace {
+struct Drv {
+  CUresult (*memAddressReserve)(CUdeviceptr*, size_t, size_t, CUdeviceptr, unsigned long long) = nullptr;
+  CUresult (*memAddressFree)(CUdeviceptr, size_t) = nullptr;
+  CUresult (*memCreate)(CUmemGenericAllocationHandle*, size_t, const CUmemAllocationProp*, unsigned long long) = nullptr;
+  CUresult (*memRelease)(CUmemGenericAllocationHandle) = nullptr;
+  CUresult (*memMap)(CUdeviceptr, size_t, size_t, CUmemGenericAllocationHandle, unsigned long long) = nullptr;
+  CUresult (*memUnmap)(CUdeviceptr, size_t) = nullptr;
+  CUresult (*memSetAccess)(CUdeviceptr, size_t, const CUmemAccessDesc*, size_t) = nullptr;
+  CUresult (*memGetAllocationGranularity)(size_t*, const CUmemAllocationProp*, CUmemAllocationGranularity_flags) = nullptr;
+  bool ok = false;
+};
+
+template <typename F>
+static bool get_entry(const char* name, F* fn) {
+  void* p = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion(name, &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess || !p)
+    return false;
+  *fn = reinterpret_cast<F>(p);
+  return true;
+}
+
+static Drv& drv() {
+  static Drv d;
+  static bool init = false;
+  if (!init) {
+    init = true;
+    d.ok = get_entry("cuMemAddressReserve", &d.memAddressReserve) && get_entry("cuMemAddressFree", &d.memAddressFree) &&
+           get_entry("cuMemCreate", &d.memCreate) && get_entry("cuMemRelease", &d.memRelease) &&
+           get_entry("cuMemMap", &d.memMap) && get_entry("cuMemUnmap", &d.memUnmap) &&
+           get_entry("cuMemSetAccess", &d.memSetAccess) &&
+           get_entry("cuMemGetAllocationGranularity", &d.memGetAllocationGranularity);
+  }
+  return d;
+}
+
+// Slot memory: one virtual range for max_slots records, physically backed in
+// fixed chunks from the start up to the current capacity.
+struct SlotMemory {
+  CUdeviceptr base = 0;
+  size_t reserved = 0, chunk = 0;
+  int device = 0;
+  std::vector<CUmemGenericAllocationHandle> handles;
+
+  moe_status init(int dev, size_t max_bytes) {
+    Drv& d = drv();
+    if (!d.ok) return fail(MOE_ERR_CUDA, "CUDA driver virtual-memory entry points unavailable");
+    device = dev;
+    CUmemAllocationProp prop = {};
+    prop.type = CU_MEM_ALLOCATION_TYPE_PINNED;
+    prop.location.type = CU_MEM_LOCATION_TYPE_DEVICE;
+    prop.location.id = dev;
+    size_t gran = 0;
+    if (d.memGetAllocationGranularity(&gran, &prop, CU_MEM_ALLOC_GRANULARITY_RECOMMENDED) != CUDA_SUCCESS || !gran)
+      return fail(MOE_ERR_CUDA, "cuMemGetAllocationGranularity failed");
+    chunk = ((size_t(256) << 20) + gran - 1) / gran * gran;
+    reserved = std::max<size_t>(chunk, (max_bytes + chunk - 1) / chunk * chunk);
+    if (d.memAddressReserve(&base, reserved, 0, 0, 0) != CUDA_SUCCESS)
+      return fail(MOE_ERR_OOM, "cuMemAddressReserve(%zu) failed", reserved);
+    return MOE_OK;
+  }
+
+  // Make [0, bytes) backed by physical memory (mapping or unmapping chunks).
+  moe_status resize(size_t bytes) {
+    Drv& d = drv();
+    const size_t want = (bytes + chunk - 1) / chunk;
+    if (want * chunk > reserved) return fail(MOE_ERR_INVALID_ARG, "slot memory beyond the reserved range");
+    while (handles.size() > want) {
+      const size_t off = (handles.size() - 1) * chunk;
+      d.memUnmap(base + off, chunk);
+      d.memRelease(handles.back());
+      handles.pop_back();
+    }
+    while (handles.size() < want) {
+      CUmemAllocationProp prop = {};
+      prop.type = CU_MEM_ALLOCATION_TYPE_PINNED;
+      prop.location.type = CU_MEM_LOCATION_TYPE_DEVICE;
+      prop.location.id = device;
+      CUmemGenericAllocationHandle h;
+      if (d.memCreate(&h, chunk, &prop, 0) != CUDA_SUCCESS)
+        return fail(MOE_ERR_OOM, "cuMemCreate: no device memory for %zu more slot bytes", (want - handles.size()) * chunk);
+      const size_t off = handles.size() * chunk;
+      if (d.memMap(base + off, chunk, 0, h, 0) != CUDA_SUCCESS) {
+        d.memRelease(h);
+        return fail(MOE_ERR_CUDA, "cuMemMap failed");
+      }
+      CUmemAccessDesc acc = {};
+      acc.location.type = CU_MEM_LOCATION_TYPE_DEVICE;
+      acc.location.id = device;
+      acc.flags = CU_MEM_ACCESS_FLAGS_PROT_READWRITE;
+      if (d.memSetAccess(base + off, chunk, &acc, 1) != CUDA_SUCCESS) {
+        d.memUnmap(base + off, chunk);
+        d.memRelease(h);
+        return fail(MOE_ERR_CUDA, "cuMemSetAccess failed");
+      }
+      handles.push_back(h);
+    }
+    return MOE_OK;
+  }
+
+  void release() {
+    if (!base) return;
+    resize(0);
+    drv().memAddressFree(base, reserved);
+    base = 0;
+  }
+};
+}  // namespace
+
+// ------------------------------------------------------------------- cache --
+struct moe_cache {
+  moe_model_desc d{};
+  int64_t S = 0, C = 0, C_max = 0;
+  const uint8_t* host_pool = nullptr;
+  const uint8_t* shared_dev = nullptr;
+  int device = 0;
+  SlotMemory slots;
+  // device state
+  int32_t* d_map = nullptr;
+  int32_t* d_owner = nullptr;
+  uint64_t* d_stamp = nullptr;
+  uint64_t* d_g = nullptr;
+  Plan* d_plan = nullptr;
+  float* d_h = nullptr;
+  float* d_partial = nullptr;
+  float* d_logits = nullptr;
+  unsigned* d_bar = nullptr;
+  int* d_err = nullptr;
+  int32_t* d_moves = nullptr;
+  int64_t moves_cap = 0;
+  HostWork* h_work = nullptr;
+  HostWork* d_work = nullptr;
+  cudaStream_t copy = nullptr;
+  bool own_copy = false;
+  cudaStream_t last_stream = nullptr;
+  cudaEvent_t e_ctrl = nullptr, e_fill = nullptr, e_done = nullptr;
+  bool have_done = false;
+  uint32_t seq = 0;
+  int64_t call_index = 0;  // successful forward calls (trace numbering; not reset with the stats)
+  int ffn_grid = 0;
+  size_t ffn_smem = 0;
+  int smem_h_floats = 0, rows_per_cta_max = 0;
+  // accounting
+  moe_stats st{};
+  bool profiling = false, tracing = false;
+  std::vector<moe_event> trace;
+  int64_t trace_total = 0;
+  std::vector<cudaEvent_t> ev_pool;
+  std::vector<std::pair<cudaEvent_t, cudaEvent_t>> pending;
+  int inject_after = -1;
+};
+
+static const char* kNotFound = "";
+
+static size_t record_bytes(const moe_model_desc* d) {
+  const size_t HI = (size_t)d->H * d->I;
+  switch (d->wdtype) {
+    case MOE_FP32: return 12 * HI;
+    case MOE_BF16: return 6 * HI;
+    case MOE_FP4: return 3 * HI / 2 + 3 * HI / 16;
+  }
+  return 0;
+}
+
+static moe_status check_desc(const moe_model_desc* d) {
+  if (!d) return fail(MOE_ERR_INVALID_ARG, "desc is NULL");
+  if (d->L < 1 || d->E < 1 || d->E > kMaxE) return fail(MOE_ERR_INVALID_ARG, "need L >= 1 and 1 <= E <= %d", kMaxE);
+  if (d->k < 1 || d->k > kMaxK || d->k > d->E) return fail(MOE_ERR_INVALID_ARG, "need 1 <= k <= min(E, %d)", kMaxK);
+  if (d->max_tokens < 1 || d->max_tokens > kMaxB) return fail(MOE_ERR_INVALID_ARG, "need 1 <= max_tokens <= %d", kMaxB);
+  if (d->wdtype != MOE_FP32 && d->wdtype != MOE_BF16 && d->wdtype != MOE_FP4)
+    return fail(MOE_ERR_INVALID_ARG, "unknown wdtype %d", d->wdtype);
+  const int m = d->wdtype == MOE_FP4 ? 256 : 64;
+  if (d->H < m || d->I < m || d->H % m || d->I % m)
+    return fail(MOE_ERR_INVALID_ARG, "H and I must be positive multiples of %d for this format", m);
+  if (d->has_shared != 0 && d->has_shared != 1) return fail(MOE_ERR_INVALID_ARG, "has_shared must be 0 or 1");
+  if ((int64_t)d->L * d->E > (int64_t)1 << 30) return fail(MOE_ERR_INVALID_ARG, "L*E too large");
+  return MOE_OK;
+}
+
+static bool is_pinned(const void* p) {
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return a.type == cudaMemoryTypeHost;
+}
+
+static void free_all(moe_cache* c) {
+  if (!c) return;
+  cudaDeviceSynchronize();
+  for (void* p : {(void*)c->d_map, (void*)c->d_owner, (void*)c->d_stamp, (void*)c->d_g, (void*)c->d_plan,
+                  (void*)c->d_h, (void*)c->d_partial, (void*)c->d_logits, (void*)c->d_bar, (void*)c->d_err,
+                  (void*)c->d_moves})
+    if (p) cudaFree(p);
+  if (c->h_work) cudaFreeHost(c->h_work);
+  for (cudaEvent_t e : {c->e_ctrl, c->e_fill, c->e_done})
+    if (e) cudaEventDestroy(e);
+  for (auto& pr : c->pending) {
+    cudaEventDestroy(pr.first);
+    cudaEventDestroy(pr.second);
+  }
+  for (cudaEvent_t e : c->ev_pool) cudaEventDestroy(e);
+  if (c->own_copy && c->copy) cudaStreamDestroy(c->copy);
+  c->slots.release();
+  delete c;
+}
+
+extern "C" size_t moe_record_bytes(const moe_model_desc* desc) {
+  if (check_desc(desc) != MOE_OK) return 0;
+  return record_bytes(desc);
+}
+
+extern "C" int32_t moe_version(void) { return 1; }
+
+extern "C" const char* moe_last_error(void) { return g_err.empty() ? kNotFound : g_err.c_str(); }
+
+extern "C" moe_status moe_cache_create(const moe_model_desc* desc, const void* host_pool, const void* shared_dev,
+                                       int64_t n_slots, int64_t max_slots, void* copy_stream, moe_cache_t* out) {
+  g_err.clear();
+  if (!out) return fail(MOE_ERR_INVALID_ARG, "out is NULL");
+  *out = nullptr;
+  if (moe_status s = check_desc(desc)) return s;
+  const int64_t LE = (int64_t)desc->L * desc->E;
+  if (!host_pool) return fail(MOE_ERR_INVALID_ARG, "host_pool is NULL");
+  if (desc->has_shared && !shared_dev) return fail(MOE_ERR_INVALID_ARG, "has_shared set but shared_dev is NULL");
+  if (max_slots == 0) max_slots = LE;
+  if (n_slots < 0 || max_slots < 0 || n_slots > max_slots || max_slots > (int64_t)INT32_MAX)
+    return fail(MOE_ERR_INVALID_ARG, "need 0 <= n_slots <= max_slots < 2^31");
+  const size_t S = record_bytes(desc);
+  const uint8_t* pool = (const uint8_t*)host_pool;
+  if (!is_pinned(pool) || !is_pinned(pool + (size_t)LE * S - 1))
+    return fail(MOE_ERR_INVALID_ARG, "host_pool must be page-locked (cudaHostAlloc / cudaHostRegister) over all L*E records");
+
+  moe_cache* c = new (std::nothrow) moe_cache();
+  if (!c) return fail(MOE_ERR_OOM, "host allocation failed");
+  c->d = *desc;
+  c->S = (int64_t)S;
+  c->C = n_slots;
+  c->C_max = max_slots;
+  c->host_pool = pool;
+  c->shared_dev = (const uint8_t*)shared_dev;
+  auto bail = [&](moe_status s) {
+    std::string keep = g_err;
+    free_all(c);
+    g_err = keep;
+    return s;
+  };
+  auto cu = [&](cudaError_t e, const char* what) -> moe_status {
+    if (e == cudaSuccess) return MOE_OK;
+    cudaGetLastError();
+    return fail(e == cudaErrorMemoryAllocation ? MOE_ERR_OOM : MOE_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+  };
+  if (cudaGetDevice(&c->device) != cudaSuccess) return bail(fail(MOE_ERR_CUDA, "no CUDA device"));
+  if (moe_status s = c->slots.init(c->device, (size_t)max_slots * S)) return bail(s);
+  if (moe_status s = c->slots.resize((size_t)n_slots * S)) return bail(s);
+
+  const int Bm = desc->max_tokens, k = desc->k, H = desc->H, I = desc->I, E = desc->E;
+  moe_status s = MOE_OK;
+  if ((s = cu(cudaMalloc(&c->d_map, sizeof(int32_t) * LE), "map")) ||
+      (s = cu(cudaMalloc(&c->d_owner, sizeof(int32_t) * std::max<int64_t>(1, max_slots)), "owner")) ||
+      (s = cu(cudaMalloc(&c->d_stamp, sizeof(uint64_t) * std::max<int64_t>(1, max_slots)), "stamp")) ||
+      (s = cu(cudaMalloc(&c->d_g, sizeof(uint64_t)), "counter")) ||
+      (s = cu(cudaMalloc(&c->d_plan, sizeof(Plan)), "plan")) ||
+      (s = cu(cudaMalloc(&c->d_h, sizeof(float) * (size_t)(Bm * k + Bm) * I), "h")) ||
+      (s = cu(cudaMalloc(&c->d_partial, sizeof(float) * (size_t)Bm * (k + 1) * H), "partial")) ||
+      (s = cu(cudaMalloc(&c->d_logits, sizeof(float) * (size_t)Bm * E), "logits")) ||
+      (s = cu(cudaMalloc(&c->d_bar, sizeof(unsigned) * 4), "barrier")) ||
+      (s = cu(cudaMalloc(&c->d_err, sizeof(int)), "err")))
+    return bail(s);
+  if ((s = cu(cudaMemset(c->d_map, 0xFF, sizeof(int32_t) * LE), "memset")) ||
+      (s = cu(cudaMemset(c->d_owner, 0xFF, sizeof(int32_t) * std::max<int64_t>(1, max_slots)), "memset")) ||
+      (s = cu(cudaMemset(c->d_stamp, 0, sizeof(uint64_t) * std::max<int64_t>(1, max_slots)), "memset")) ||
+      (s = cu(cudaMemset(c->d_g, 0, sizeof(uint64_t)), "memset")) ||
+      (s = cu(cudaMemset(c->d_bar, 0, sizeof(unsigned) * 4), "memset")) ||
+      (s = cu(cudaMemset(c->d_err, 0, sizeof(int)), "memset")))
+    return bail(s);
+  if ((s = cu(cudaHostAlloc((void**)&c->h_work, sizeof(HostWork), cudaHostAllocMapped), "pinned summary")))
+    return bail(s);
+  memset((void*)c->h_work, 0, sizeof(HostWork));
+  if ((s = cu(cudaHostGetDevicePointer((void**)&c->d_work, c->h_work, 0), "mapped summary"))) return bail(s);
+  if ((s = cu(cudaEventCreateWithFlags(&c->e_ctrl, cudaEventDisableTiming), "event")) ||
+      (s = cu(cudaEventCreateWithFlags(&c->e_fill, cudaEventDisableTiming), "event")) ||
+      (s = cu(cudaEventCreateWithFlags(&c->e_done, cudaEventDisableTiming), "event")))
+    return bail(s);
+  if (copy_stream) {
+    c->copy = (cudaStream_t)copy_stream;
+  } else {
+    if ((s = cu(cudaStreamCreateWithFlags(&c->copy, cudaStreamNonBlocking), "copy stream"))) return bail(s);
+    c->own_copy = true;
+  }
+
+  // expert-FFN launch shape: one CTA per SM; shared memory for the tokens, an
+  // h buffer and the CTA's output rows
+  int sms = 0;
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, c->device);
+  c->rows_per_cta_max = (H + sms - 1) / sms;
+  const size_t xbytes = (((size_t)Bm * H * (desc->wdtype == MOE_FP32 ? 4 : 2)) + 15) & ~(size_t)15;
+  const size_t obytes = (size_t)c->rows_per_cta_max * Bm * (k + 1) * 4;
+  const size_t budget = 200 * 1024;
+  const size_t need_h = (size_t)Bm * I * 4;  // one expert with every token
+  if (xbytes + obytes + need_h > budget)
+    return bail(fail(MOE_ERR_INVALID_ARG, "max_tokens * (H, I) too large for the decode kernel's shared memory"));
+  c->smem_h_floats = (int)std::min<size_t>((budget - xbytes - obytes) / 4, (size_t)(Bm * k + Bm) * I);
+  c->smem_h_floats &= ~3;
+  c->ffn_smem = ffn_smem_bytes(desc->wdtype, Bm, H, k, c->smem_h_floats, c->rows_per_cta_max);
+  c->ffn_grid = ffn_max_grid(desc->wdtype, c->ffn_smem);
+  if (c->ffn_grid != sms)  // the per-CTA row split above assumes one CTA on every SM
+    return bail(fail(MOE_ERR_CUDA, "decode kernel cannot keep one CTA resident on every SM (%d of %d)", c->ffn_grid, sms));
+  if (cudaDeviceSynchronize() != cudaSuccess) return bail(fail(MOE_ERR_CUDA, "initialisation failed"));
+  *out = c;
+  return MOE_OK;
+}
+
+extern "C" moe_status moe_cache_destroy(moe_cache_t c) {
+  if (!c) return fail(MOE_ERR_INVALID_ARG, "cache is NULL");
+  free_all(c);
+  return MOE_OK;
+}
+
+// ----------------------------------------------------------- profiling events --
+static cudaEvent_t take_event(moe_cache* c) {
+  if (!c->ev_pool.empty()) {
+    cudaEvent_t e = c->ev_pool.back();
+    c->ev_pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  cudaEventCreate(&e);
+  return e;
+}
+
+static void drain_pending(moe_cache* c, bool wait) {
+  size_t keep = 0;
+  for (size_t i = 0; i < c->pending.size(); ++i) {
+    auto pr = c->pending[i];
+    if (wait) cudaEventSynchronize(pr.second);
+    float ms = 0.f;
+    if (cudaEventElapsedTime(&ms, pr.first, pr.second) == cudaSuccess) {
+      c->st.ffn_ms += ms;
+      c->st.ffn_timed += 1;
+      c->ev_pool.push_back(pr.first);
+      c->ev_pool.push_back(pr.second);
+    } else {
+      cudaGetLastError();
+      c->pending[keep++] = pr;
+    }
+  }
+  c->pending.resize(keep);
+}
+
+static cudaError_t run_ffn(moe_cache* c, const FfnParams& fp, cudaStream_t s) {
+  cudaEvent_t a = nullptr, b = nullptr;
+  if (c->profiling) {
+    a = take_event(c);
+    b = take_event(c);
+    cudaEventRecord(a, s);
+  }
+  cudaError_t e = launch_ffn(c->d.wdtype, fp, c->ffn_grid, c->ffn_smem, s);
+  if (c->profiling) {
+    cudaEventRecord(b, s);
+    c->pending.emplace_back(a, b);
+    if (c->pending.size() > 4096) drain_pending(c, false);
+  }
+  c->st.ffn_launches += 1;
+  return e;
+}
+
+// Wait until the control kernel of call `seq` has published its summary.
+static moe_status wait_summary(moe_cache* c, uint32_t seq) {
+  const auto t0 = std::chrono::steady_clock::now();
+  for (uint64_t spin = 0;; ++spin) {
+    if (__atomic_load_n(&c->h_work->seq, __ATOMIC_ACQUIRE) == seq) return MOE_OK;
+    if ((spin & 1023) == 1023) {
+      cudaError_t q = cudaEventQuery(c->e_ctrl);
+      if (q != cudaSuccess && q != cudaErrorNotReady)
+        return fail(MOE_ERR_CUDA, "control kernel failed: %s", cudaGetErrorString(q));
+      if (std::chrono::steady_clock::now() - t0 > std::chrono::seconds(30))
+        return fail(MOE_ERR_TIMEOUT, "control kernel summary not seen after 30 s");
+      if (spin > (1u << 20)) std::this_thread::yield();
+    }
+  }
+}
+
+extern "C" moe_status moe_layer_forward_ex(moe_cache_t c, int32_t layer, const void* x, const float* logits,
+                                           const float* router_w, int32_t B, void* y, void* stream,
+                                           const moe_layer_aux* aux) {
+  g_err.clear();
+  if (!c) return fail(MOE_ERR_INVALID_ARG, "cache is NULL");
+  const moe_model_desc& d = c->d;
+  if (layer < 0 || layer >= d.L) return fail(MOE_ERR_INVALID_ARG, "layer %d out of range", layer);
+  if (B < 1 || B > d.max_tokens) return fail(MOE_ERR_INVALID_ARG, "B=%d outside 1..%d", B, d.max_tokens);
+  if (!x || !y) return fail(MOE_ERR_INVALID_ARG, "x and y must be device pointers");
+  if (!logits && !router_w) return fail(MOE_ERR_INVALID_ARG, "need logits or router_w");
+  cudaStream_t s = (cudaStream_t)stream;
+  if (c->have_done && s != c->last_stream) CU_TRY(cudaStreamWaitEvent(s, c->e_done, 0));
+  c->last_stream = s;
+
+  const float* lg = logits;
+  if (!lg) {
+    CU_TRY(launch_router_logits(x, d.wdtype != MOE_FP32, router_w, B, d.E, d.H, c->d_logits, s));
+    lg = c->d_logits;
+  }
+  const uint32_t seq = ++c->seq;
+  CtrlParams cp{};
+  cp.L = d.L; cp.E = d.E; cp.k = d.k; cp.B = B; cp.layer = layer; cp.C = c->C;
+  cp.logits = lg;
+  cp.st = CacheDev{c->d_map, c->d_owner, c->d_stamp, c->d_g};
+  cp.plan = c->d_plan;
+  cp.work = c->d_work;
+  cp.seq = seq;
+  cp.bar_reset = c->d_bar;
+  cp.n_bar_reset = 4;
+  cp.has_shared = d.has_shared;
+  if (aux) {
+    cp.aux_ids = aux->ids; cp.aux_w = aux->weights; cp.aux_slots = aux->slots;
+    cp.aux_perm = aux->perm; cp.aux_offsets = aux->offsets; cp.aux_logits = aux->logits;
+  }
+  CU_TRY(launch_ctrl(cp, s));
+  CU_TRY(cudaEventRecord(c->e_ctrl, s));
+
+  FfnParams fp{};
+  fp.H = d.H; fp.I = d.I; fp.k = d.k; fp.B = B;
+  fp.which = 0;
+  fp.has_shared = d.has_shared;
+  fp.slots = (const uint8_t*)c->slots.base;
+  fp.S = c->S;
+  fp.shared_rec = d.has_shared ? c->shared_dev + (int64_t)layer * c->S : nullptr;
+  fp.x = x;
+  fp.plan = c->d_plan;
+  fp.h = c->d_h;
+  fp.h_shared_row0 = d.max_tokens * d.k;
+  fp.partial = c->d_partial;
+  fp.y = y;
+  fp.bar = c->d_bar;
+  fp.err = c->d_err;
+  fp.smem_h_floats = c->smem_h_floats;
+  fp.rows_per_cta_max = c->rows_per_cta_max;
+  CU_TRY(run_ffn(c, fp, s));
+
+  if (moe_status w = wait_summary(c, seq)) return w;
+  const HostWork& w = *c->h_work;
+  if (w.err == MOE_ERR_CUDA) {
+    cudaEventRecord(c->e_done, s);
+    c->have_done = true;
+    return fail(MOE_ERR_CUDA, "internal error: victim selection found an inconsistent cache state");
+  }
+  if (w.err == MOE_ERR_CAPACITY) {
+    cudaEventRecord(c->e_done, s);
+    c->have_done = true;
+    return fail(MOE_ERR_CAPACITY, "layer %d routes %d distinct experts but the cache has %lld slots", layer, w.n_u,
+                (long long)c->C);
+  }
+  const int n_u = w.n_u, n_miss = w.n_miss;
+  if (n_miss > 0) {
+    CU_TRY(cudaStreamWaitEvent(c->copy, c->e_ctrl, 0));
+    cudaError_t ce = cudaSuccess;
+    int issued = 0;
+    for (int r = 0; r < n_u && ce == cudaSuccess; ++r) {
+      if (!w.fill[r]) continue;
+      if (c->inject_after >= 0 && issued >= c->inject_after) {
+        ce = cudaErrorInvalidValue;
+        g_err = "injected fill failure";
+        break;
+      }
+      ce = cudaMemcpyAsync((uint8_t*)c->slots.base + (int64_t)w.slot[r] * c->S, c->host_pool + (int64_t)w.key[r] * c->S,
+                           c->S, cudaMemcpyHostToDevice, c->copy);
+      if (ce == cudaSuccess) ++issued;
+    }
+    if (ce != cudaSuccess) {
+      const std::string why = c->inject_after >= 0 ? std::string("injected fill failure") : cudaGetErrorString(ce);
+      c->inject_after = -1;
+      cudaGetLastError();
+      UndoParams up{CacheDev{c->d_map, c->d_owner, c->d_stamp, c->d_g}, c->d_work};
+      cudaEventRecord(c->e_fill, c->copy);
+      cudaStreamWaitEvent(s, c->e_fill, 0);
+      launch_undo(up, s);
+      cudaEventRecord(c->e_done, s);
+      c->have_done = true;
+      return fail(MOE_ERR_CUDA, "fill copy %d of %d could not be issued (%s); cache rolled back", issued + 1, n_miss,
+                  why.c_str());
+    }
+    CU_TRY(cudaEventRecord(c->e_fill, c->copy));
+    CU_TRY(cudaStreamWaitEvent(s, c->e_fill, 0));
+    fp.which = 1;
+    CU_TRY(run_ffn(c, fp, s));
+  }
+  CU_TRY(cudaEventRecord(c->e_done, s));
+  c->have_done = true;
+
+  // accounting
+  moe_stats& st = c->st;
+  const int64_t call_id = c->call_index++;
+  st.calls += 1;
+  st.tokens += B;
+  st.hits += n_u - n_miss;
+  st.misses += n_miss;
+  st.routed_pairs += (int64_t)B * d.k;
+  st.bytes_filled += (int64_t)n_miss * c->S;
+  st.ffn_records += n_u + d.has_shared;
+  for (int r = 0; r < n_u; ++r) {
+    if (w.fill[r] && w.evicted[r] >= 0) st.evictions += 1;
+    if (!w.fill[r]) st.routed_pair_hits += w.pairs[r];
+  }
+  if (c->tracing) {
+    for (int r = 0; r < n_u; ++r) {
+      moe_event ev{};
+      ev.call = call_id;
+      ev.layer = layer;
+      ev.expert = w.key[r] - layer * d.E;
+      ev.kind = w.fill[r] ? MOE_EV_MISS : MOE_EV_HIT;
+      ev.slot = w.slot[r];
+      ev.evicted_key = w.evicted[r];
+      c->trace.push_back(ev);
+    }
+  }
+  return MOE_OK;
+}
+
+extern "C" moe_status moe_layer_forward(moe_cache_t c, int32_t layer, const void* x, const float* logits,
+                                        const float* router_w, int32_t B, void* y, void* stream) {
+  return moe_layer_forward_ex(c, layer, x, logits, router_w, B, y, stream, nullptr);
+}
+
+// --------------------------------------------------------------------- resize --
+extern "C" moe_status moe_cache_resize(moe_cache_t c, int64_t n_slots, void* stream) {
+  g_err.clear();
+  if (!c) return fail(MOE_ERR_INVALID_ARG, "cache is NULL");
+  if (n_slots < 0 || n_slots > c->C_max)
+    return fail(MOE_ERR_INVALID_ARG, "n_slots %lld outside 0..%lld", (long long)n_slots, (long long)c->C_max);
+  if (c->have_done && cudaEventQuery(c->e_done) == cudaErrorNotReady)
+    return fail(MOE_ERR_BUSY, "a forward of this cache is still running on the GPU");
+  if (cudaStreamQuery(c->copy) == cudaErrorNotReady) return fail(MOE_ERR_BUSY, "fills still in flight");
+  cudaGetLastError();
+  cudaStream_t s = (cudaStream_t)stream;
+  const int64_t C = c->C, LE = (int64_t)c->d.L * c->d.E;
+  std::vector<int32_t> owner(std::max<int64_t>(C, n_slots), -1);
+  std::vector<uint64_t> stamp(std::max<int64_t>(C, n_slots), 0);
+  if (C > 0) {
+    CU_TRY(cudaMemcpy(owner.data(), c->d_owner, sizeof(int32_t) * C, cudaMemcpyDeviceToHost));
+    CU_TRY(cudaMemcpy(stamp.data(), c->d_stamp, sizeof(uint64_t) * C, cudaMemcpyDeviceToHost));
+  }
+  if (n_slots < C) {
+    // survivors: the n_slots most recent experts
+    std::vector<int64_t> occ;
+    for (int64_t i = 0; i < C; ++i)
+      if (owner[i] >= 0) occ.push_back(i);
+    std::vector<int64_t> by_recency = occ;
+    std::sort(by_recency.begin(), by_recency.end(), [&](int64_t a, int64_t b) { return stamp[a] > stamp[b]; });
+    std::vector<char> keep(C, 0);
+    for (int64_t i = 0; i < (int64_t)by_recency.size() && i < n_slots; ++i) keep[by_recency[i]] = 1;
+    for (int64_t i : occ) {  // ascending slot order
+      if (keep[i]) continue;
+      if (c->tracing) {
+        moe_event ev{};
+        ev.call = c->call_index;
+        ev.layer = owner[i] / c->d.E;
+        ev.expert = owner[i] % c->d.E;
+        ev.kind = MOE_EV_RESIZE_EVICT;
+        ev.slot = (int32_t)i;
+        ev.evicted_key = owner[i];
+        c->trace.push_back(ev);
+      }
+      owner[i] = -1;
+      stamp[i] = 0;
+      c->st.resize_evictions += 1;
+    }
+    std::vector<int32_t> moves;
+    int64_t vac = 0;
+    for (int64_t src = n_slots; src < C; ++src) {
+      if (!keep[src]) continue;
+      while (owner[vac] >= 0) ++vac;  // a vacancy below n_slots always exists here
+      moves.push_back((int32_t)src);
+      moves.push_back((int32_t)vac);
+      owner[vac] = owner[src];
+      stamp[vac] = stamp[src];
+      owner[src] = -1;
+      stamp[src] = 0;
+      ++vac;
+    }
+    const int n_moves = (int)(moves.size() / 2);
+    if (n_moves > 0) {
+      if (c->moves_cap < (int64_t)moves.size()) {
+        if (c->d_moves) cudaFree(c->d_moves);
+        c->d_moves = nullptr;
+        c->moves_cap = 0;
+        CU_TRY(cudaMalloc(&c->d_moves, sizeof(int32_t) * moves.size()));
+        c->moves_cap = (int64_t)moves.size();
+      }
+      CU_TRY(cudaMemcpyAsync(c->d_moves, moves.data(), sizeof(int32_t) * moves.size(), cudaMemcpyHostToDevice, s));
+      CU_TRY(launch_slot_moves((uint8_t*)c->slots.base, c->S, c->d_moves, n_moves, s));
+    }
+    c->st.resize_moves += n_moves;
+    CU_TRY(cudaStreamSynchronize(s));
+    if (moe_status st = c->slots.resize((size_t)n_slots * c->S)) return st;
+  } else if (n_slots > C) {
+    if (moe_status st = c->slots.resize((size_t)n_slots * c->S)) return st;
+  }
+  // rebuild the residency table from the slot owners
+  std::vector<int32_t> map(LE, -1);
+  for (int64_t i = 0; i < n_slots; ++i)
+    if (owner[i] >= 0) map[owner[i]] = (int32_t)i;
+  if (n_slots > 0) {
+    CU_TRY(cudaMemcpyAsync(c->d_owner, owner.data(), sizeof(int32_t) * n_slots, cudaMemcpyHostToDevice, s));
+    CU_TRY(cudaMemcpyAsync(c->d_stamp, stamp.data(), sizeof(uint64_t) * n_slots, cudaMemcpyHostToDevice, s));
+  }
+  CU_TRY(cudaMemcpyAsync(c->d_map, map.data(), sizeof(int32_t) * LE, cudaMemcpyHostToDevice, s));
+  CU_TRY(cudaStreamSynchronize(s));
+  c->C = n_slots;
+  c->st.resize_calls += 1;
+  return MOE_OK;
+}
+
+// -------------------------------------------------------------- introspection --
+extern "C" moe_status moe_cache_stats(moe_cache_t c, moe_stats* out) {
+  if (!c || !out) return fail(MOE_ERR_INVALID_ARG, "NULL argument");
+  drain_pending(c, true);
+  *out = c->st;
+  return MOE_OK;
+}
+
+extern "C" moe_status moe_cache_reset_stats(moe_cache_t c) {
+  if (!c) return fail(MOE_ERR_INVALID_ARG, "cache is NULL");
+  drain_pending(c, true);
+  c->st = moe_stats{};
+  return MOE_OK;
+}
+
+extern "C" moe_status moe_cache_set_profiling(moe_cache_t c, int32_t on) {
+  if (!c) return fail(MOE_ERR_INVALID_ARG, "cache is NULL");
+  c->profiling = on != 0;
+  return MOE_OK;
+}
+
+extern "C" moe_status moe_cache_set_trace(moe_cache_t c, int32_t on) {
+  if (!c) return fail(MOE_ERR_INVALID_ARG, "cache is NULL");
+  c->tracing = on != 0;
+  return MOE_OK;
+}
+
+extern "C" moe_status moe_cache_trace(moe_cache_t c, moe_event* buf, int64_t cap, int64_t* n) {
+  if (!c || !n || (cap > 0 && !buf)) return fail(MOE_ERR_INVALID_ARG, "NULL argument");
+  *n = (int64_t)c->trace.size();
+  const int64_t m = std::min<int64_t>(cap, *n);
+  if (m > 0) memcpy(buf, c->trace.data(), sizeof(moe_event) * m);
+  return MOE_OK;
+}
+
+extern "C" moe_status moe_cache_state(moe_cache_t c, int32_t* owner, uint64_t* stamp, int64_t cap, int64_t* n_slots,
+                                      uint64_t* counter) {
+  if (!c) return fail(MOE_ERR_INVALID_ARG, "cache is NULL");
+  CU_TRY(cudaDeviceSynchronize());
+  const int64_t m = std::min<int64_t>(cap, c->C);
+  if (owner && m > 0) CU_TRY(cudaMemcpy(owner, c->d_owner, sizeof(int32_t) * m, cudaMemcpyDeviceToHost));
+  if (stamp && m > 0) CU_TRY(cudaMemcpy(stamp, c->d_stamp, sizeof(uint64_t) * m, cudaMemcpyDeviceToHost));
+  if (n_slots) *n_slots = c->C;
+  if (counter) CU_TRY(cudaMemcpy(counter, c->d_g, sizeof(uint64_t), cudaMemcpyDeviceToHost));
+  return MOE_OK;
+}
+
+extern "C" const void* moe_cache_slot_ptr(moe_cache_t c, int64_t s) {
+  if (!c || s < 0 || s >= c->C) return nullptr;
+  return (const uint8_t*)c->slots.base + s * c->S;
+}
+
+extern "C" moe_status moe_cache_inject_fill_failure(moe_cache_t c, int32_t after) {
+  if (!c) return fail(MOE_ERR_INVALID_ARG, "cache is NULL");
+  c->inject_after = after;
+  return MOE_OK;
+}
+
+extern "C" moe_status moe_prefill_stream(moe_cache_t c, int32_t layer_begin, int32_t layer_end, const void* x,
+                                         const float* logits, int32_t T, void* y, void* stream) {
+  (void)layer_begin; (void)layer_end; (void)x; (void)logits; (void)T; (void)y; (void)stream;
+  if (!c) return fail(MOE_ERR_INVALID_ARG, "cache is NULL");
+  return fail(MOE_ERR_INVALID_ARG, "prefill path not available in this build");
+}

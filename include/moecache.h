@@ -1,0 +1,229 @@
+/*
+ * moecache — a routed Mixture-of-Experts layer served from one GPU-resident
+ * expert cache shared by all layers, backed by a pinned host expert pool.
+ *
+ * Method (FreeToken, "Efficient Edge-Native MoE Serving with Bandwidth-
+ * Adaptive Execution", as summarised on discuss.pytorch.kr "FreeToken:
+ * 프론티어급 MoE 모델을 게이밍 데스크톱 수준에서 서빙하기 위한 Edge-Serving에
+ * 대한 연구" and read on qqtang-code.github.io):
+ *  - "FreeToken's design": a host expert pool is the source of truth; the
+ *    free GPU memory is one elastic expert cache shared by every MoE layer,
+ *    each slot holding every tensor of one (layer, expert) pair.
+ *  - "Router-following LRU cache": hits refresh recency, fills admit the
+ *    newly selected expert, eviction removes the expert not requested for
+ *    the longest time.
+ *  - "CUDA Graph-compatible LRU cache": per layer one GPU kernel deduplicates
+ *    the routed experts, classifies them against the residency table, picks
+ *    K victims in one pass and rewrites logical ids to slot ids.
+ *  - "Measured bandwidths decide the split": the GPU evaluates G = H ∪ F as
+ *    one grouped FFN after the batched copy of the fills; partial sums merge
+ *    exactly.
+ *  - "Full-layer double buffering" (prefill): two full-layer buffers from
+ *    the global slot pool; a transfer stream loads layer l+1 while layer l
+ *    computes.
+ *  - "Elastic memory management": at a scheduler safe point the cache is
+ *    rebuilt to a new budget without reloading the host pool.
+ *
+ * Conventions for every entry point:
+ *  - Returns a moe_status; nothing throws or aborts across this boundary.
+ *    On failure moe_last_error() returns a message (thread-local).
+ *  - "device" pointers are CUDA device addresses on the device that was
+ *    current at moe_cache_create; "host" pointers are ordinary process
+ *    memory.  Streams are cudaStream_t values passed as void* (NULL = the
+ *    legacy default stream).
+ *  - One cache is driven by one host thread at a time.
+ *  - Expert key of (layer l, expert e) is l*E + e.
+ *
+ * Expert record (one host-pool row, one cache slot), row-major [out][in]:
+ *  MOE_FP32, MOE_BF16: W_gate[I][H] | W_up[I][H] | W_down[H][I]
+ *  MOE_FP4: gate codes[I][H/2] | up codes[I][H/2] | down codes[H][I/2] |
+ *           gate scales[I][H/16] | up scales[I][H/16] | down scales[H][I/16]
+ *    (e2m1 codes, element 2c in the low nibble of byte c; one e4m3 scale per
+ *     16 consecutive elements of a row; no per-tensor scale)
+ *  Expert FFN: h = SiLU(x W_gate^T) * (x W_up^T), o = h W_down^T.
+ */
+#ifndef MOECACHE_H
+#define MOECACHE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int32_t moe_status;
+enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1, /* bad pointer, size, shape or state */
+  MOE_ERR_OOM = 2,         /* device or pinned memory could not be obtained */
+  MOE_ERR_CAPACITY = 3,    /* a call routes more distinct experts than there are slots */
+  MOE_ERR_BUSY = 4,        /* resize while work of this cache is still in flight */
+  MOE_ERR_CUDA = 5,        /* a CUDA call failed; see moe_last_error() */
+  MOE_ERR_TIMEOUT = 6      /* a bounded wait gave up */
+};
+
+/* weight formats */
+enum { MOE_FP32 = 0, MOE_BF16 = 1, MOE_FP4 = 2 };
+
+/* event kinds in the cache trace */
+enum { MOE_EV_HIT = 0, MOE_EV_MISS = 1, MOE_EV_RESIZE_EVICT = 2 };
+
+typedef struct {
+  int32_t L;          /* MoE layers */
+  int32_t E;          /* routed experts per layer (1 .. 1024) */
+  int32_t k;          /* experts per token (1 .. 16, <= E) */
+  int32_t H;          /* hidden size */
+  int32_t I;          /* per-expert SwiGLU intermediate size */
+  int32_t wdtype;     /* MOE_FP32 | MOE_BF16 | MOE_FP4 */
+  int32_t has_shared; /* 1: every layer also runs one always-resident, ungated shared expert */
+  int32_t max_tokens; /* largest B passed to moe_layer_forward (1 .. 16) */
+} moe_model_desc;
+/* Shape rules: MOE_FP32/MOE_BF16 need H and I multiples of 64; MOE_FP4 needs
+ * multiples of 256.  Activations x and outputs y are float32 for MOE_FP32
+ * models and bf16 otherwise. */
+
+typedef struct {
+  int64_t calls;             /* moe_layer_forward calls that completed */
+  int64_t tokens;            /* tokens over those calls */
+  int64_t hits, misses;      /* distinct (call, expert) accesses */
+  int64_t evictions;         /* misses that displaced a resident expert */
+  int64_t routed_pairs;      /* (token, rank) pairs */
+  int64_t routed_pair_hits;  /* pairs whose expert was resident before the call */
+  int64_t bytes_filled;      /* host -> device bytes copied by fills */
+  int64_t ffn_launches;      /* expert-FFN kernel launches */
+  int64_t ffn_records;       /* expert records streamed by those launches (incl. shared) */
+  double ffn_ms;             /* summed device time of those launches (profiling on) */
+  int64_t ffn_timed;         /* launches included in ffn_ms */
+  int64_t resize_calls, resize_moves, resize_evictions;
+  int64_t prefill_layers;
+  double prefill_ms, prefill_copy_ms, prefill_compute_ms; /* profiling on */
+} moe_stats;
+
+typedef struct {
+  int64_t call;        /* index of the moe_layer_forward call (resize: calls so far) */
+  int32_t layer;
+  int32_t expert;
+  int32_t kind;        /* MOE_EV_* */
+  int32_t slot;
+  int32_t evicted_key; /* key displaced by a miss or resize eviction, -1 if none */
+  int32_t pad;
+} moe_event;
+
+/* Optional device outputs of one forward call, for inspection.  Every field
+ * may be NULL.  Sizes are for B tokens. */
+typedef struct {
+  int32_t* ids;      /* [B][k] selected experts, descending logit, ties -> lower id */
+  float* weights;    /* [B][k] routing weights (softmax over the k selected logits) */
+  int32_t* slots;    /* [B][k] cache slot of each selected expert after the call */
+  int32_t* perm;     /* [B*k] flat pair indices t*k+j grouped by expert (stable) */
+  int32_t* offsets;  /* [E+1] start of each expert's group in perm */
+  float* logits;     /* [B][E] router logits actually used (float32) */
+} moe_layer_aux;
+
+typedef struct moe_cache* moe_cache_t;
+
+/* Bytes of one expert record for desc (0 if desc is invalid). */
+size_t moe_record_bytes(const moe_model_desc* desc);
+
+/* Create a cache.
+ * host_pool: host memory holding L*E records back to back (row l*E+e).  It
+ *   must be page-locked (cudaHostAlloc or cudaHostRegister), stay valid and
+ *   unchanged until moe_cache_destroy, and is never written by the library.
+ * shared_dev: device memory with L records (shared expert of layer l at row
+ *   l), required iff desc->has_shared; owned by the caller.
+ * n_slots: initial capacity C (>= 0).  max_slots: upper bound for resizes
+ *   (0 means L*E); device virtual address space for max_slots records is
+ *   reserved up front and physical memory is mapped for the first C only.
+ * copy_stream: stream for fills (NULL: the library creates one).
+ * Errors: MOE_ERR_INVALID_ARG (shapes, pointers, unpinned pool),
+ *   MOE_ERR_OOM, MOE_ERR_CUDA.  On error *out is NULL. */
+moe_status moe_cache_create(const moe_model_desc* desc, const void* host_pool, const void* shared_dev,
+                            int64_t n_slots, int64_t max_slots, void* copy_stream, moe_cache_t* out);
+
+/* Rebuild the cache with n_slots slots at a safe point ("elastic memory
+ * management").  Shrinking keeps the n_slots most recently used experts,
+ * evicts the rest (logged as MOE_EV_RESIZE_EVICT in ascending slot order)
+ * and moves survivors sitting in slots >= n_slots into the vacant low slots
+ * (ascending old slot -> ascending vacant slot), then unmaps the tail.
+ * Growing maps more slots, empty.  Recency and the host pool are untouched.
+ * stream: where the device copies run; the call returns after they finish.
+ * Errors: MOE_ERR_BUSY if a forward of this cache has not finished on the
+ * GPU, MOE_ERR_INVALID_ARG if n_slots > max_slots, MOE_ERR_OOM, MOE_ERR_CUDA. */
+moe_status moe_cache_resize(moe_cache_t cache, int64_t n_slots, void* stream);
+
+/* One decode-size MoE layer call (1 <= B <= desc->max_tokens).
+ * x: device [B][H] (bf16, or float32 for MOE_FP32).  y: device [B][H], same
+ *   type, written.
+ * logits: device float32 [B][E], or NULL to compute logits = x W_r^T from
+ *   router_w: device float32 [E][H] (then router_w must not be NULL).
+ * The call routes (top-k softmax), updates the LRU cache (one control kernel),
+ * copies each miss's record from the host pool into its victim slot with
+ * cudaMemcpyAsync on the copy stream while the resident experts already run,
+ * evaluates every selected expert (and the shared expert) straight from the
+ * cache slots, and writes y_t = sum_j w_tj * o_tj (+ shared) in rank order.
+ * The host waits once per call for the control kernel (it needs the miss
+ * list to issue the copies); the rest stays asynchronous on `stream`.
+ * Errors: MOE_ERR_INVALID_ARG, MOE_ERR_CAPACITY (more distinct experts than
+ *   slots; cache unchanged, y unspecified), MOE_ERR_CUDA (a fill could not be
+ *   issued: recency is rolled back and this call's victim slots are left
+ *   empty; y unspecified), MOE_ERR_TIMEOUT. */
+moe_status moe_layer_forward(moe_cache_t cache, int32_t layer, const void* x, const float* logits,
+                             const float* router_w, int32_t B, void* y, void* stream);
+
+/* moe_layer_forward with optional inspection outputs (aux may be NULL). */
+moe_status moe_layer_forward_ex(moe_cache_t cache, int32_t layer, const void* x, const float* logits,
+                                const float* router_w, int32_t B, void* y, void* stream,
+                                const moe_layer_aux* aux);
+
+/* Prefill of T tokens through layers [layer_begin, layer_end) with full-layer
+ * double buffering: two buffers of E slots each are carved from the slot
+ * pool; while layer l runs on one, all E records of layer l+1 stream into the
+ * other on the copy stream.  x: device [n_layers][T][H] bf16 (each layer's
+ * input), logits: device float32 [n_layers][T][E], y: device
+ * [n_layers][T][H] bf16.  Only MOE_BF16 / MOE_FP4 models.
+ * Errors: MOE_ERR_CAPACITY if the pool has fewer than 2*E slots,
+ * MOE_ERR_INVALID_ARG, MOE_ERR_OOM, MOE_ERR_CUDA. */
+moe_status moe_prefill_stream(moe_cache_t cache, int32_t layer_begin, int32_t layer_end, const void* x,
+                              const float* logits, int32_t T, void* y, void* stream);
+
+/* Counters since creation (or the last reset).  Synchronises the events of
+ * profiled launches. */
+moe_status moe_cache_stats(moe_cache_t cache, moe_stats* out);
+moe_status moe_cache_reset_stats(moe_cache_t cache);
+
+/* on != 0: time every expert-FFN and prefill launch with CUDA events. */
+moe_status moe_cache_set_profiling(moe_cache_t cache, int32_t on);
+
+/* on != 0: record one moe_event per distinct expert access and per resize
+ * eviction.  moe_cache_trace copies up to cap recorded events to buf (host)
+ * and sets *n to the number recorded in total. */
+moe_status moe_cache_set_trace(moe_cache_t cache, int32_t on);
+moe_status moe_cache_trace(moe_cache_t cache, moe_event* buf, int64_t cap, int64_t* n);
+
+/* Copy of the cache state to host buffers (each may be NULL): owner key of
+ * every slot (-1 empty) and its recency stamp (cap entries at most), the
+ * current slot count and the global recency counter.  Synchronises. */
+moe_status moe_cache_state(moe_cache_t cache, int32_t* owner, uint64_t* stamp, int64_t cap, int64_t* n_slots,
+                           uint64_t* counter);
+
+/* Device address of slot s (for inspection); NULL if s is out of range. */
+const void* moe_cache_slot_ptr(moe_cache_t cache, int64_t s);
+
+/* Test hook: the next fill copies of this cache fail after `after` successful
+ * copies (-1 disables).  Used to check the rollback path without a GPU fault. */
+moe_status moe_cache_inject_fill_failure(moe_cache_t cache, int32_t after);
+
+/* Free everything the library allocated.  Synchronises. */
+moe_status moe_cache_destroy(moe_cache_t cache);
+
+/* Message of the last error on this thread ("" if none). */
+const char* moe_last_error(void);
+
+/* Library ABI version. */
+int32_t moe_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOECACHE_H */
