@@ -171,6 +171,24 @@ def run_reference(args, w):
 
 
 # ------------------------------------------------------------ native leg --
+def measure_link(dev, pool, S, reps=24):
+    """B_P: host->device bandwidth of cudaMemcpyAsync of one expert record
+    from the pinned pool (best of reps), GB/s."""
+    import torch
+
+    dst = torch.empty(S, dtype=torch.uint8, device=dev)
+    best = 0.0
+    for r in range(reps):
+        src = pool[(r * 37) % pool.shape[0]]
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        dst.copy_(src, non_blocking=True)
+        b.record()
+        b.synchronize()
+        best = max(best, S / (a.elapsed_time(b) / 1e3) / 1e9)
+    return best
+
+
 def run_native(args, w):
     import torch
 
@@ -217,7 +235,7 @@ def run_native(args, w):
         step(s, x_dev, lg_dev, y_dev)
     torch.cuda.synchronize()
     mc.moe_cache_reset_stats(cache.handle)
-    mc.moe_cache_set_profiling(cache.handle, True)
+    mc.moe_cache_set_profiling(cache.handle, args.profile)
     clk = ClockSampler(os.path.join(out_dir, f"clocks_rank{rank}.csv"), local)
     clk.start()
     if dist:
@@ -235,6 +253,7 @@ def run_native(args, w):
     ms = ev0.elapsed_time(ev1)
     mc.moe_cache_set_profiling(cache.handle, False)
     stats = mc.moe_cache_stats(cache.handle)
+    phases = mc.moe_cache_phase_times(cache.handle) if args.profile >= 2 else None
     if dist:
         t = torch.tensor([ms], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
@@ -272,12 +291,19 @@ def run_native(args, w):
         e2e_ms = float(t.item())
     e2e_value = w.B * K_e2e * world / (e2e_ms / 1e3) if K_e2e else None
 
-    # roofline of the dominant kernel (expert FFN): algorithmic bytes = every
-    # record it streams once (S bytes each) over its summed launch time
-    ffn_bytes = stats["ffn_records"] * S
-    ffn_s = stats["ffn_ms"] / 1e3
-    achieved = ffn_bytes / ffn_s / 1e9 if ffn_s > 0 else None
+    # roofline of the dominant kernel (the layer kernel): algorithmic bytes =
+    # every expert record it streams once (S bytes each).  Calls with fills
+    # also wait for the host link inside the kernel, so the HBM figure is
+    # taken over the launches of calls without fills; the link-inclusive
+    # bound covers every call.
+    hit_bytes = stats["hit_only_records"] * S
+    hit_s = stats["hit_only_ms"] / 1e3
+    achieved = hit_bytes / hit_s / 1e9 if hit_s > 0 else None
     peak = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
+    b_p = measure_link(dev, pool, S)
+    hbm_s = stats["records_streamed"] * S / (peak * 1e9)
+    link_s = stats["bytes_filled"] / (b_p * 1e9)
+    roof_tok_s = w.B * K / max(hbm_s, link_s) if max(hbm_s, link_s) > 0 else None
     hits, misses = stats["hits"], stats["misses"]
     line = {
         "metric": METRIC, "value": value, "unit": "tok/s (decode)", "n_gpus": world, "steps": K, "warmup": W,
@@ -293,11 +319,20 @@ def run_native(args, w):
         "fill_GB_per_token": stats["bytes_filled"] / 1e9 / (w.B * K),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak if achieved else None, "traffic": None,
-                     "kernel": "ffn_decode_kernel", "peak_kind": peak_kind + " hbm_gbs (copy)",
-                     "launches": stats["ffn_timed"], "avg_launch_us": stats["ffn_ms"] * 1e3 / max(1, stats["ffn_timed"])},
+                     "kernel": "layer_kernel (calls without fills)", "peak_kind": peak_kind + " hbm_gbs (copy)",
+                     "launches": stats["hit_only_timed"],
+                     "avg_launch_us": stats["hit_only_ms"] * 1e3 / max(1, stats["hit_only_timed"]),
+                     "all_launches_avg_us": stats["layer_ms"] * 1e3 / max(1, stats["layer_timed"])},
+        "link": {"B_P_GBps": b_p, "fill_bytes": stats["bytes_filled"],
+                 "roofline_tok_s": roof_tok_s,
+                 "frac": value / roof_tok_s if roof_tok_s else None,
+                 "note": "tok/s bound = max(expert bytes / HBM peak, fill bytes / B_P) over the timed steps"},
         "e2e": {"value": e2e_value, "unit": "tok/s (decode)", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "steps": K_e2e},
-        "gpu_launches": stats["calls"] + stats["ffn_launches"],
+        "gpu_launches": stats["layer_launches"],
+        "phase_us": phases,
+        "host_us_per_call": {"wait_for_miss_list": stats["host_wait_us"] / max(1, stats["calls"]),
+                             "issue_fills": stats["host_issue_us"] / max(1, stats["calls"])},
         "clocks": clocks,
         "setup_s": round(setup_s, 1),
     }
@@ -326,6 +361,7 @@ def main():
     ap.add_argument("--workload", default="c2", choices=["c2", "small"])
     ap.add_argument("--cpu-tokens", type=int, default=3)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile", type=int, default=1, help="1: CUDA events per launch; 2: also phase timestamps")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

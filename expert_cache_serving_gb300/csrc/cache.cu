@@ -55,6 +55,7 @@ struct Drv {
   CUresult (*memUnmap)(CUdeviceptr, size_t) = nullptr;
   CUresult (*memSetAccess)(CUdeviceptr, size_t, const CUmemAccessDesc*, size_t) = nullptr;
   CUresult (*memGetAllocationGranularity)(size_t*, const CUmemAllocationProp*, CUmemAllocationGranularity_flags) = nullptr;
+  CUresult (*streamWriteValue32)(CUstream, CUdeviceptr, cuuint32_t, unsigned int) = nullptr;
   bool ok = false;
 };
 
@@ -78,7 +79,8 @@ static Drv& drv() {
            get_entry("cuMemCreate", &d.memCreate) && get_entry("cuMemRelease", &d.memRelease) &&
            get_entry("cuMemMap", &d.memMap) && get_entry("cuMemUnmap", &d.memUnmap) &&
            get_entry("cuMemSetAccess", &d.memSetAccess) &&
-           get_entry("cuMemGetAllocationGranularity", &d.memGetAllocationGranularity);
+           get_entry("cuMemGetAllocationGranularity", &d.memGetAllocationGranularity) &&
+           get_entry("cuStreamWriteValue32", &d.streamWriteValue32);
   }
   return d;
 }
@@ -171,9 +173,13 @@ struct moe_cache {
   uint64_t* d_g = nullptr;
   Plan* d_plan = nullptr;
   float* d_h = nullptr;
-  float* d_partial = nullptr;
   float* d_logits = nullptr;
-  unsigned* d_bar = nullptr;
+  unsigned long long* d_bar = nullptr;
+  unsigned long long bar_base = 0;
+  unsigned* d_flags = nullptr;  // [0]: plan flag, [1 ..]: fill flags [2][kMaxU]
+  int32_t* d_oldest = nullptr;
+  int* d_oldest_n = nullptr;
+  int* h_err = nullptr;  // pinned, mapped: error word the kernels record timeouts in
   int* d_err = nullptr;
   int32_t* d_moves = nullptr;
   int64_t moves_cap = 0;
@@ -182,12 +188,12 @@ struct moe_cache {
   cudaStream_t copy = nullptr;
   bool own_copy = false;
   cudaStream_t last_stream = nullptr;
-  cudaEvent_t e_ctrl = nullptr, e_fill = nullptr, e_done = nullptr;
+  cudaEvent_t e_pre = nullptr, e_done = nullptr;
   bool have_done = false;
   uint32_t seq = 0;
   int64_t call_index = 0;  // successful forward calls (trace numbering; not reset with the stats)
-  int ffn_grid = 0;
-  size_t ffn_smem = 0;
+  int grid = 0;
+  size_t smem = 0;
   int smem_h_floats = 0, rows_per_cta_max = 0;
   // accounting
   moe_stats st{};
@@ -195,9 +201,23 @@ struct moe_cache {
   std::vector<moe_event> trace;
   int64_t trace_total = 0;
   std::vector<cudaEvent_t> ev_pool;
-  std::vector<std::pair<cudaEvent_t, cudaEvent_t>> pending;
+  struct Timed {
+    cudaEvent_t a, b;
+    bool hit_only;
+    int64_t records;
+  };
+  std::vector<Timed> pending;
   int inject_after = -1;
+  // phase timeline (profiling level 2): ring of [kTlRing][12] GPU timestamps
+  int profile_level = 0;
+  unsigned long long* d_tl = nullptr;
+  std::vector<std::pair<int, int>> tl_calls;  // (ring row, had fills) not yet read
+  int tl_next = 0;
+  moe_phase_times pt{};
 };
+
+static constexpr int kTlRing = 1024;
+static constexpr int kTlStamps = 12;
 
 static const char* kNotFound = "";
 
@@ -239,15 +259,16 @@ static void free_all(moe_cache* c) {
   if (!c) return;
   cudaDeviceSynchronize();
   for (void* p : {(void*)c->d_map, (void*)c->d_owner, (void*)c->d_stamp, (void*)c->d_g, (void*)c->d_plan,
-                  (void*)c->d_h, (void*)c->d_partial, (void*)c->d_logits, (void*)c->d_bar, (void*)c->d_err,
-                  (void*)c->d_moves})
+                  (void*)c->d_h, (void*)c->d_logits, (void*)c->d_bar, (void*)c->d_flags, (void*)c->d_oldest,
+                  (void*)c->d_oldest_n, (void*)c->d_moves, (void*)c->d_tl})
     if (p) cudaFree(p);
   if (c->h_work) cudaFreeHost(c->h_work);
-  for (cudaEvent_t e : {c->e_ctrl, c->e_fill, c->e_done})
+  if (c->h_err) cudaFreeHost(c->h_err);
+  for (cudaEvent_t e : {c->e_pre, c->e_done})
     if (e) cudaEventDestroy(e);
-  for (auto& pr : c->pending) {
-    cudaEventDestroy(pr.first);
-    cudaEventDestroy(pr.second);
+  for (auto& t : c->pending) {
+    cudaEventDestroy(t.a);
+    cudaEventDestroy(t.b);
   }
   for (cudaEvent_t e : c->ev_pool) cudaEventDestroy(e);
   if (c->own_copy && c->copy) cudaStreamDestroy(c->copy);
@@ -263,6 +284,16 @@ extern "C" size_t moe_record_bytes(const moe_model_desc* desc) {
 extern "C" int32_t moe_version(void) { return 1; }
 
 extern "C" const char* moe_last_error(void) { return g_err.empty() ? kNotFound : g_err.c_str(); }
+
+// bytes of the first part of a record (everything the gate/up rows read)
+static int64_t first_part_bytes(const moe_model_desc& d) {
+  const int64_t HI = (int64_t)d.H * d.I;
+  switch (d.wdtype) {
+    case MOE_FP32: return 8 * HI;
+    case MOE_BF16: return 4 * HI;
+    default: return HI + HI / 8;
+  }
+}
 
 extern "C" moe_status moe_cache_create(const moe_model_desc* desc, const void* host_pool, const void* shared_dev,
                                        int64_t n_slots, int64_t max_slots, void* copy_stream, moe_cache_t* out) {
@@ -305,31 +336,38 @@ extern "C" moe_status moe_cache_create(const moe_model_desc* desc, const void* h
   if (moe_status s = c->slots.resize((size_t)n_slots * S)) return bail(s);
 
   const int Bm = desc->max_tokens, k = desc->k, H = desc->H, I = desc->I, E = desc->E;
+  const int M = Bm * k;
+  const size_t nslot_alloc = (size_t)std::max<int64_t>(1, max_slots);
   moe_status s = MOE_OK;
   if ((s = cu(cudaMalloc(&c->d_map, sizeof(int32_t) * LE), "map")) ||
-      (s = cu(cudaMalloc(&c->d_owner, sizeof(int32_t) * std::max<int64_t>(1, max_slots)), "owner")) ||
-      (s = cu(cudaMalloc(&c->d_stamp, sizeof(uint64_t) * std::max<int64_t>(1, max_slots)), "stamp")) ||
+      (s = cu(cudaMalloc(&c->d_owner, sizeof(int32_t) * nslot_alloc), "owner")) ||
+      (s = cu(cudaMalloc(&c->d_stamp, sizeof(uint64_t) * nslot_alloc), "stamp")) ||
       (s = cu(cudaMalloc(&c->d_g, sizeof(uint64_t)), "counter")) ||
       (s = cu(cudaMalloc(&c->d_plan, sizeof(Plan)), "plan")) ||
       (s = cu(cudaMalloc(&c->d_h, sizeof(float) * (size_t)(Bm * k + Bm) * I), "h")) ||
-      (s = cu(cudaMalloc(&c->d_partial, sizeof(float) * (size_t)Bm * (k + 1) * H), "partial")) ||
       (s = cu(cudaMalloc(&c->d_logits, sizeof(float) * (size_t)Bm * E), "logits")) ||
-      (s = cu(cudaMalloc(&c->d_bar, sizeof(unsigned) * 4), "barrier")) ||
-      (s = cu(cudaMalloc(&c->d_err, sizeof(int)), "err")))
+      (s = cu(cudaMalloc(&c->d_bar, sizeof(unsigned long long)), "barrier")) ||
+      (s = cu(cudaMalloc(&c->d_flags, sizeof(unsigned) * (1 + 2 * kMaxU)), "flags")) ||
+      (s = cu(cudaMalloc(&c->d_oldest, sizeof(int32_t) * M), "victim order")) ||
+      (s = cu(cudaMalloc(&c->d_oldest_n, sizeof(int)), "victim order")))
     return bail(s);
   if ((s = cu(cudaMemset(c->d_map, 0xFF, sizeof(int32_t) * LE), "memset")) ||
-      (s = cu(cudaMemset(c->d_owner, 0xFF, sizeof(int32_t) * std::max<int64_t>(1, max_slots)), "memset")) ||
-      (s = cu(cudaMemset(c->d_stamp, 0, sizeof(uint64_t) * std::max<int64_t>(1, max_slots)), "memset")) ||
+      (s = cu(cudaMemset(c->d_owner, 0xFF, sizeof(int32_t) * nslot_alloc), "memset")) ||
+      (s = cu(cudaMemset(c->d_stamp, 0, sizeof(uint64_t) * nslot_alloc), "memset")) ||
       (s = cu(cudaMemset(c->d_g, 0, sizeof(uint64_t)), "memset")) ||
-      (s = cu(cudaMemset(c->d_bar, 0, sizeof(unsigned) * 4), "memset")) ||
-      (s = cu(cudaMemset(c->d_err, 0, sizeof(int)), "memset")))
+      (s = cu(cudaMemset(c->d_bar, 0, sizeof(unsigned long long)), "memset")) ||
+      (s = cu(cudaMemset(c->d_flags, 0, sizeof(unsigned) * (1 + 2 * kMaxU)), "memset")) ||
+      (s = cu(cudaMemset(c->d_oldest_n, 0xFF, sizeof(int)), "memset")))
     return bail(s);
-  if ((s = cu(cudaHostAlloc((void**)&c->h_work, sizeof(HostWork), cudaHostAllocMapped), "pinned summary")))
+  if ((s = cu(cudaHostAlloc((void**)&c->h_work, sizeof(HostWork), cudaHostAllocMapped), "pinned summary")) ||
+      (s = cu(cudaHostAlloc((void**)&c->h_err, sizeof(int), cudaHostAllocMapped), "pinned error word")))
     return bail(s);
   memset((void*)c->h_work, 0, sizeof(HostWork));
-  if ((s = cu(cudaHostGetDevicePointer((void**)&c->d_work, c->h_work, 0), "mapped summary"))) return bail(s);
-  if ((s = cu(cudaEventCreateWithFlags(&c->e_ctrl, cudaEventDisableTiming), "event")) ||
-      (s = cu(cudaEventCreateWithFlags(&c->e_fill, cudaEventDisableTiming), "event")) ||
+  *c->h_err = 0;
+  if ((s = cu(cudaHostGetDevicePointer((void**)&c->d_work, c->h_work, 0), "mapped summary")) ||
+      (s = cu(cudaHostGetDevicePointer((void**)&c->d_err, c->h_err, 0), "mapped error word")))
+    return bail(s);
+  if ((s = cu(cudaEventCreateWithFlags(&c->e_pre, cudaEventDisableTiming), "event")) ||
       (s = cu(cudaEventCreateWithFlags(&c->e_done, cudaEventDisableTiming), "event")))
     return bail(s);
   if (copy_stream) {
@@ -338,24 +376,39 @@ extern "C" moe_status moe_cache_create(const moe_model_desc* desc, const void* h
     if ((s = cu(cudaStreamCreateWithFlags(&c->copy, cudaStreamNonBlocking), "copy stream"))) return bail(s);
     c->own_copy = true;
   }
+  // the copy stream signals landed fills with stream memory writes: check they work here
+  {
+    Drv& dr = drv();
+    if (!dr.streamWriteValue32) return bail(fail(MOE_ERR_CUDA, "cuStreamWriteValue32 unavailable"));
+    if (dr.streamWriteValue32((CUstream)c->copy, (CUdeviceptr)(c->d_flags), 0x5A5Au, 0) != CUDA_SUCCESS)
+      return bail(fail(MOE_ERR_CUDA, "stream memory operations are not supported on this device"));
+    unsigned probe = 0;
+    if ((s = cu(cudaStreamSynchronize(c->copy), "probe")) ||
+        (s = cu(cudaMemcpy(&probe, c->d_flags, sizeof(unsigned), cudaMemcpyDeviceToHost), "probe")))
+      return bail(s);
+    if (probe != 0x5A5Au) return bail(fail(MOE_ERR_CUDA, "stream memory write did not land"));
+    if ((s = cu(cudaMemset(c->d_flags, 0, sizeof(unsigned)), "memset"))) return bail(s);
+  }
 
-  // expert-FFN launch shape: one CTA per SM; shared memory for the tokens, an
-  // h buffer and the CTA's output rows
-  int sms = 0;
+  // layer-kernel launch shape: one CTA per SM; dynamic shared memory for the
+  // tokens, an h buffer and the CTA's output rows
+  int sms = 0, smem_optin = 0;
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, c->device);
+  cudaDeviceGetAttribute(&smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, c->device);
   c->rows_per_cta_max = (H + sms - 1) / sms;
   const size_t xbytes = (((size_t)Bm * H * (desc->wdtype == MOE_FP32 ? 4 : 2)) + 15) & ~(size_t)15;
   const size_t obytes = (size_t)c->rows_per_cta_max * Bm * (k + 1) * 4;
-  const size_t budget = 200 * 1024;
+  const size_t static_smem = layer_static_smem(desc->wdtype);
+  const size_t budget = (size_t)smem_optin > static_smem + 1024 ? (size_t)smem_optin - static_smem - 1024 : 0;
   const size_t need_h = (size_t)Bm * I * 4;  // one expert with every token
   if (xbytes + obytes + need_h > budget)
-    return bail(fail(MOE_ERR_INVALID_ARG, "max_tokens * (H, I) too large for the decode kernel's shared memory"));
+    return bail(fail(MOE_ERR_INVALID_ARG, "max_tokens * (H, I) too large for the layer kernel's shared memory"));
   c->smem_h_floats = (int)std::min<size_t>((budget - xbytes - obytes) / 4, (size_t)(Bm * k + Bm) * I);
   c->smem_h_floats &= ~3;
-  c->ffn_smem = ffn_smem_bytes(desc->wdtype, Bm, H, k, c->smem_h_floats, c->rows_per_cta_max);
-  c->ffn_grid = ffn_max_grid(desc->wdtype, c->ffn_smem);
-  if (c->ffn_grid != sms)  // the per-CTA row split above assumes one CTA on every SM
-    return bail(fail(MOE_ERR_CUDA, "decode kernel cannot keep one CTA resident on every SM (%d of %d)", c->ffn_grid, sms));
+  c->smem = layer_smem_bytes(desc->wdtype, Bm, H, k, c->smem_h_floats, c->rows_per_cta_max);
+  c->grid = layer_max_grid(desc->wdtype, c->smem);
+  if (c->grid != sms)  // the per-CTA row split assumes one CTA on every SM
+    return bail(fail(MOE_ERR_CUDA, "layer kernel cannot keep one CTA resident on every SM (%d of %d)", c->grid, sms));
   if (cudaDeviceSynchronize() != cudaSuccess) return bail(fail(MOE_ERR_CUDA, "initialisation failed"));
   *out = c;
   return MOE_OK;
@@ -382,53 +435,77 @@ static cudaEvent_t take_event(moe_cache* c) {
 static void drain_pending(moe_cache* c, bool wait) {
   size_t keep = 0;
   for (size_t i = 0; i < c->pending.size(); ++i) {
-    auto pr = c->pending[i];
-    if (wait) cudaEventSynchronize(pr.second);
+    const auto t = c->pending[i];
+    if (wait) cudaEventSynchronize(t.b);
     float ms = 0.f;
-    if (cudaEventElapsedTime(&ms, pr.first, pr.second) == cudaSuccess) {
-      c->st.ffn_ms += ms;
-      c->st.ffn_timed += 1;
-      c->ev_pool.push_back(pr.first);
-      c->ev_pool.push_back(pr.second);
+    if (cudaEventElapsedTime(&ms, t.a, t.b) == cudaSuccess) {
+      c->st.layer_ms += ms;
+      c->st.layer_timed += 1;
+      if (t.hit_only) {
+        c->st.hit_only_ms += ms;
+        c->st.hit_only_timed += 1;
+        c->st.hit_only_records += t.records;
+      }
+      c->ev_pool.push_back(t.a);
+      c->ev_pool.push_back(t.b);
     } else {
       cudaGetLastError();
-      c->pending[keep++] = pr;
+      c->pending[keep++] = t;
     }
   }
   c->pending.resize(keep);
 }
 
-static cudaError_t run_ffn(moe_cache* c, const FfnParams& fp, cudaStream_t s) {
-  cudaEvent_t a = nullptr, b = nullptr;
-  if (c->profiling) {
-    a = take_event(c);
-    b = take_event(c);
-    cudaEventRecord(a, s);
+// Fold the recorded phase stamps into the running means.
+static void drain_timeline(moe_cache* c) {
+  if (c->tl_calls.empty()) return;
+  cudaDeviceSynchronize();
+  std::vector<unsigned long long> tl((size_t)kTlRing * kTlStamps);
+  if (cudaMemcpy(tl.data(), c->d_tl, tl.size() * sizeof(unsigned long long), cudaMemcpyDeviceToHost) != cudaSuccess) {
+    cudaGetLastError();
+    c->tl_calls.clear();
+    return;
   }
-  cudaError_t e = launch_ffn(c->d.wdtype, fp, c->ffn_grid, c->ffn_smem, s);
-  if (c->profiling) {
-    cudaEventRecord(b, s);
-    c->pending.emplace_back(a, b);
-    if (c->pending.size() > 4096) drain_pending(c, false);
+  for (auto [row, fills] : c->tl_calls) {
+    const unsigned long long* t = &tl[(size_t)row * kTlStamps];
+    int64_t& n = fills ? c->pt.calls_with_fills : c->pt.calls_hit_only;
+    double* acc = fills ? c->pt.with_fills_us : c->pt.hit_only_us;
+    // running mean per stamp (stamps never reached stay 0 and are skipped)
+    for (int i = 0; i < kTlStamps; ++i) {
+      if (!t[i] || !t[0]) continue;
+      const double us = ((double)t[i] - (double)t[0]) / 1e3;
+      acc[i] += (us - acc[i]) / (double)(n + 1);
+    }
+    n += 1;
   }
-  c->st.ffn_launches += 1;
-  return e;
+  c->tl_calls.clear();
 }
 
-// Wait until the control kernel of call `seq` has published its summary.
-static moe_status wait_summary(moe_cache* c, uint32_t seq) {
+// Wait until the layer kernel of call `seq` has published its summary.
+static moe_status wait_summary(moe_cache* c, uint32_t seq, cudaStream_t s) {
   const auto t0 = std::chrono::steady_clock::now();
   for (uint64_t spin = 0;; ++spin) {
     if (__atomic_load_n(&c->h_work->seq, __ATOMIC_ACQUIRE) == seq) return MOE_OK;
     if ((spin & 1023) == 1023) {
-      cudaError_t q = cudaEventQuery(c->e_ctrl);
+      cudaError_t q = cudaStreamQuery(s);
       if (q != cudaSuccess && q != cudaErrorNotReady)
-        return fail(MOE_ERR_CUDA, "control kernel failed: %s", cudaGetErrorString(q));
+        return fail(MOE_ERR_CUDA, "layer kernel failed: %s", cudaGetErrorString(q));
       if (std::chrono::steady_clock::now() - t0 > std::chrono::seconds(30))
-        return fail(MOE_ERR_TIMEOUT, "control kernel summary not seen after 30 s");
+        return fail(MOE_ERR_TIMEOUT, "layer kernel summary not seen after 30 s");
       if (spin > (1u << 20)) std::this_thread::yield();
     }
   }
+}
+
+// A previous launch recorded a timeout: wait for the stream, re-align the
+// barrier counter and drop the precomputed victim order.
+static moe_status recover_after_timeout(moe_cache* c, cudaStream_t s) {
+  CU_TRY(cudaStreamSynchronize(s));
+  CU_TRY(cudaStreamSynchronize(c->copy));
+  CU_TRY(cudaMemcpy(&c->bar_base, c->d_bar, sizeof(unsigned long long), cudaMemcpyDeviceToHost));
+  CU_TRY(cudaMemset(c->d_oldest_n, 0xFF, sizeof(int)));
+  *(volatile int*)c->h_err = 0;
+  return fail(MOE_ERR_TIMEOUT, "a previous layer call timed out waiting on the GPU; its results were not used");
 }
 
 extern "C" moe_status moe_layer_forward_ex(moe_cache_t c, int32_t layer, const void* x, const float* logits,
@@ -442,6 +519,7 @@ extern "C" moe_status moe_layer_forward_ex(moe_cache_t c, int32_t layer, const v
   if (!x || !y) return fail(MOE_ERR_INVALID_ARG, "x and y must be device pointers");
   if (!logits && !router_w) return fail(MOE_ERR_INVALID_ARG, "need logits or router_w");
   cudaStream_t s = (cudaStream_t)stream;
+  if (*(volatile int*)c->h_err != 0) return recover_after_timeout(c, s);
   if (c->have_done && s != c->last_stream) CU_TRY(cudaStreamWaitEvent(s, c->e_done, 0));
   c->last_stream = s;
 
@@ -451,94 +529,129 @@ extern "C" moe_status moe_layer_forward_ex(moe_cache_t c, int32_t layer, const v
     lg = c->d_logits;
   }
   const uint32_t seq = ++c->seq;
-  CtrlParams cp{};
-  cp.L = d.L; cp.E = d.E; cp.k = d.k; cp.B = B; cp.layer = layer; cp.C = c->C;
-  cp.logits = lg;
-  cp.st = CacheDev{c->d_map, c->d_owner, c->d_stamp, c->d_g};
-  cp.plan = c->d_plan;
-  cp.work = c->d_work;
-  cp.seq = seq;
-  cp.bar_reset = c->d_bar;
-  cp.n_bar_reset = 4;
-  cp.has_shared = d.has_shared;
+  LayerParams p{};
+  p.L = d.L; p.E = d.E; p.k = d.k; p.B = B; p.layer = layer; p.H = d.H; p.I = d.I;
+  p.C = c->C;
+  p.M = d.max_tokens * d.k;
+  p.logits = lg;
+  p.st = CacheDev{c->d_map, c->d_owner, c->d_stamp, c->d_g};
+  p.plan = c->d_plan;
+  p.work = c->d_work;
+  p.seq = seq;
+  p.plan_flag = c->d_flags;
+  p.fill_flags = c->d_flags + 1;
+  p.bar = c->d_bar;
+  p.bar_base = c->bar_base;
+  p.err = c->d_err;
+  p.has_shared = d.has_shared;
+  p.slots = (const uint8_t*)c->slots.base;
+  p.S = c->S;
+  p.shared_rec = d.has_shared ? c->shared_dev + (int64_t)layer * c->S : nullptr;
+  p.x = x;
+  p.h = c->d_h;
+  p.h_shared_row0 = d.max_tokens * d.k;
+  p.y = y;
+  p.smem_h_floats = c->smem_h_floats;
+  p.rows_per_cta_max = c->rows_per_cta_max;
+  p.oldest = c->d_oldest;
+  p.oldest_n = c->d_oldest_n;
+  int tl_row = -1;
+  if (c->profile_level >= 2 && c->d_tl) {
+    if ((int)c->tl_calls.size() >= kTlRing) drain_timeline(c);
+    tl_row = c->tl_next;
+    c->tl_next = (c->tl_next + 1) % kTlRing;
+    p.tl = c->d_tl + (size_t)tl_row * kTlStamps;
+    CU_TRY(cudaMemsetAsync(p.tl, 0, kTlStamps * sizeof(unsigned long long), s));
+  }
   if (aux) {
-    cp.aux_ids = aux->ids; cp.aux_w = aux->weights; cp.aux_slots = aux->slots;
-    cp.aux_perm = aux->perm; cp.aux_offsets = aux->offsets; cp.aux_logits = aux->logits;
+    p.aux_ids = aux->ids; p.aux_w = aux->weights; p.aux_slots = aux->slots;
+    p.aux_perm = aux->perm; p.aux_offsets = aux->offsets; p.aux_logits = aux->logits;
   }
-  CU_TRY(launch_ctrl(cp, s));
-  CU_TRY(cudaEventRecord(c->e_ctrl, s));
-
-  FfnParams fp{};
-  fp.H = d.H; fp.I = d.I; fp.k = d.k; fp.B = B;
-  fp.which = 0;
-  fp.has_shared = d.has_shared;
-  fp.slots = (const uint8_t*)c->slots.base;
-  fp.S = c->S;
-  fp.shared_rec = d.has_shared ? c->shared_dev + (int64_t)layer * c->S : nullptr;
-  fp.x = x;
-  fp.plan = c->d_plan;
-  fp.h = c->d_h;
-  fp.h_shared_row0 = d.max_tokens * d.k;
-  fp.partial = c->d_partial;
-  fp.y = y;
-  fp.bar = c->d_bar;
-  fp.err = c->d_err;
-  fp.smem_h_floats = c->smem_h_floats;
-  fp.rows_per_cta_max = c->rows_per_cta_max;
-  CU_TRY(run_ffn(c, fp, s));
-
-  if (moe_status w = wait_summary(c, seq)) return w;
-  const HostWork& w = *c->h_work;
-  if (w.err == MOE_ERR_CUDA) {
-    cudaEventRecord(c->e_done, s);
-    c->have_done = true;
-    return fail(MOE_ERR_CUDA, "internal error: victim selection found an inconsistent cache state");
+  // everything before this call (earlier layers may still read victim slots)
+  CU_TRY(cudaEventRecord(c->e_pre, s));
+  cudaEvent_t ta = nullptr, tb = nullptr;
+  if (c->profiling) {
+    ta = take_event(c);
+    tb = take_event(c);
+    cudaEventRecord(ta, s);
   }
-  if (w.err == MOE_ERR_CAPACITY) {
-    cudaEventRecord(c->e_done, s);
-    c->have_done = true;
-    return fail(MOE_ERR_CAPACITY, "layer %d routes %d distinct experts but the cache has %lld slots", layer, w.n_u,
-                (long long)c->C);
-  }
-  const int n_u = w.n_u, n_miss = w.n_miss;
-  if (n_miss > 0) {
-    CU_TRY(cudaStreamWaitEvent(c->copy, c->e_ctrl, 0));
-    cudaError_t ce = cudaSuccess;
-    int issued = 0;
-    for (int r = 0; r < n_u && ce == cudaSuccess; ++r) {
-      if (!w.fill[r]) continue;
-      if (c->inject_after >= 0 && issued >= c->inject_after) {
-        ce = cudaErrorInvalidValue;
-        g_err = "injected fill failure";
-        break;
-      }
-      ce = cudaMemcpyAsync((uint8_t*)c->slots.base + (int64_t)w.slot[r] * c->S, c->host_pool + (int64_t)w.key[r] * c->S,
-                           c->S, cudaMemcpyHostToDevice, c->copy);
-      if (ce == cudaSuccess) ++issued;
-    }
-    if (ce != cudaSuccess) {
-      const std::string why = c->inject_after >= 0 ? std::string("injected fill failure") : cudaGetErrorString(ce);
-      c->inject_after = -1;
-      cudaGetLastError();
-      UndoParams up{CacheDev{c->d_map, c->d_owner, c->d_stamp, c->d_g}, c->d_work};
-      cudaEventRecord(c->e_fill, c->copy);
-      cudaStreamWaitEvent(s, c->e_fill, 0);
-      launch_undo(up, s);
-      cudaEventRecord(c->e_done, s);
-      c->have_done = true;
-      return fail(MOE_ERR_CUDA, "fill copy %d of %d could not be issued (%s); cache rolled back", issued + 1, n_miss,
-                  why.c_str());
-    }
-    CU_TRY(cudaEventRecord(c->e_fill, c->copy));
-    CU_TRY(cudaStreamWaitEvent(s, c->e_fill, 0));
-    fp.which = 1;
-    CU_TRY(run_ffn(c, fp, s));
-  }
+  CU_TRY(launch_layer(d.wdtype, p, c->grid, c->smem, s));
+  if (c->profiling) cudaEventRecord(tb, s);
   CU_TRY(cudaEventRecord(c->e_done, s));
   c->have_done = true;
+  c->st.layer_launches += 1;
+
+  const auto t_launch = std::chrono::steady_clock::now();
+  if (moe_status w = wait_summary(c, seq, s)) return w;
+  const auto t_seen = std::chrono::steady_clock::now();
+  c->st.host_wait_us += std::chrono::duration<double, std::micro>(t_seen - t_launch).count();
+  const HostWork& w = *c->h_work;
+  if (w.err != MOE_OK) {
+    if (c->profiling) c->pending.push_back({ta, tb, false, 0});
+    if (w.err == MOE_ERR_CAPACITY)
+      return fail(MOE_ERR_CAPACITY, "layer %d routes %d distinct experts but the cache has %lld slots", layer, w.n_u,
+                  (long long)c->C);
+    return fail(MOE_ERR_CUDA, "internal error: victim selection found an inconsistent cache state");
+  }
+  const int n_u = w.n_u, n_miss = w.n_miss;
+  c->bar_base += (unsigned long long)c->grid * (n_miss > 0 ? 2 : 1);
+  if (tl_row >= 0) c->tl_calls.emplace_back(tl_row, n_miss > 0 ? 1 : 0);
+  if (c->profiling) {
+    c->pending.push_back({ta, tb, n_miss == 0, (int64_t)n_u + d.has_shared});
+    if (c->pending.size() > 4096) drain_pending(c, false);
+  }
+  if (n_miss > 0) {
+    // one copy per half record on the copy stream, each followed by a flag the
+    // kernel waits on; the copies start once every earlier call has finished
+    Drv& dr = drv();
+    CU_TRY(cudaStreamWaitEvent(c->copy, c->e_pre, 0));
+    const int64_t part1 = first_part_bytes(d), part2 = c->S - part1;
+    unsigned* flags = c->d_flags + 1;
+    int f = 0, half = 0;
+    bool failed = false;
+    std::string why;
+    for (f = 0; f < n_miss && !failed; ++f) {
+      const int r = w.fill_order[f];
+      uint8_t* dst = (uint8_t*)c->slots.base + (int64_t)w.slot[r] * c->S;
+      const uint8_t* src = c->host_pool + (int64_t)w.key[r] * c->S;
+      for (half = 0; half < 2; ++half) {
+        if (c->inject_after >= 0 && 2 * f + half >= 2 * c->inject_after) {
+          failed = true;
+          why = "injected fill failure";
+          break;
+        }
+        const int64_t off = half ? part1 : 0, len = half ? part2 : part1;
+        cudaError_t ce = cudaMemcpyAsync(dst + off, src + off, len, cudaMemcpyHostToDevice, c->copy);
+        if (ce != cudaSuccess) {
+          failed = true;
+          why = cudaGetErrorString(ce);
+          cudaGetLastError();
+          break;
+        }
+        if (dr.streamWriteValue32((CUstream)c->copy, (CUdeviceptr)(flags + half * kMaxU + f), seq, 0) !=
+            CUDA_SUCCESS) {
+          failed = true;
+          why = "cuStreamWriteValue32 failed";
+          break;
+        }
+      }
+      if (failed) break;
+    }
+    if (failed) {
+      // release the kernel: this and every later half carries the error bit
+      c->inject_after = -1;
+      for (int g = f; g < n_miss; ++g)
+        for (int hh = (g == f ? half : 0); hh < 2; ++hh)
+          dr.streamWriteValue32((CUstream)c->copy, (CUdeviceptr)(flags + hh * kMaxU + g), seq | kFlagError, 0);
+      return fail(MOE_ERR_CUDA, "fill %d of %d could not be issued (%s); cache rolled back", f + 1, n_miss,
+                  why.c_str());
+    }
+  }
 
   // accounting
   moe_stats& st = c->st;
+  if (n_miss > 0)
+    st.host_issue_us += std::chrono::duration<double, std::micro>(std::chrono::steady_clock::now() - t_seen).count();
   const int64_t call_id = c->call_index++;
   st.calls += 1;
   st.tokens += B;
@@ -546,7 +659,7 @@ extern "C" moe_status moe_layer_forward_ex(moe_cache_t c, int32_t layer, const v
   st.misses += n_miss;
   st.routed_pairs += (int64_t)B * d.k;
   st.bytes_filled += (int64_t)n_miss * c->S;
-  st.ffn_records += n_u + d.has_shared;
+  st.records_streamed += n_u + d.has_shared;
   for (int r = 0; r < n_u; ++r) {
     if (w.fill[r] && w.evicted[r] >= 0) st.evictions += 1;
     if (!w.fill[r]) st.routed_pair_hits += w.pairs[r];
@@ -654,6 +767,7 @@ extern "C" moe_status moe_cache_resize(moe_cache_t c, int64_t n_slots, void* str
     CU_TRY(cudaMemcpyAsync(c->d_stamp, stamp.data(), sizeof(uint64_t) * n_slots, cudaMemcpyHostToDevice, s));
   }
   CU_TRY(cudaMemcpyAsync(c->d_map, map.data(), sizeof(int32_t) * LE, cudaMemcpyHostToDevice, s));
+  CU_TRY(cudaMemsetAsync(c->d_oldest_n, 0xFF, sizeof(int), s));
   CU_TRY(cudaStreamSynchronize(s));
   c->C = n_slots;
   c->st.resize_calls += 1;
@@ -671,13 +785,25 @@ extern "C" moe_status moe_cache_stats(moe_cache_t c, moe_stats* out) {
 extern "C" moe_status moe_cache_reset_stats(moe_cache_t c) {
   if (!c) return fail(MOE_ERR_INVALID_ARG, "cache is NULL");
   drain_pending(c, true);
+  drain_timeline(c);
   c->st = moe_stats{};
+  c->pt = moe_phase_times{};
   return MOE_OK;
 }
 
 extern "C" moe_status moe_cache_set_profiling(moe_cache_t c, int32_t on) {
   if (!c) return fail(MOE_ERR_INVALID_ARG, "cache is NULL");
   c->profiling = on != 0;
+  c->profile_level = on;
+  if (on >= 2 && !c->d_tl)
+    CU_TRY(cudaMalloc(&c->d_tl, sizeof(unsigned long long) * kTlRing * kTlStamps));
+  return MOE_OK;
+}
+
+extern "C" moe_status moe_cache_phase_times(moe_cache_t c, moe_phase_times* out) {
+  if (!c || !out) return fail(MOE_ERR_INVALID_ARG, "NULL argument");
+  drain_timeline(c);
+  *out = c->pt;
   return MOE_OK;
 }
 

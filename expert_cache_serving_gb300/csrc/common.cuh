@@ -14,9 +14,9 @@ constexpr int kMaxB = 16;            // tokens per decode call
 constexpr int kMaxPairs = kMaxB * kMaxK;
 constexpr int kMaxU = kMaxPairs;     // distinct experts per call
 constexpr int kMaxItems = kMaxU + 1; // + shared expert
-constexpr int kCtrlThreads = 1024;
-constexpr int kFfnThreads = 512;
-constexpr int kFfnWarps = kFfnThreads / 32;
+constexpr int kThreads = 512;  // layer kernel CTA size
+constexpr int kWarps = kThreads / 32;
+constexpr unsigned kFlagError = 0x80000000u;  // fill flag: the copy was not issued
 
 // Per-call plan written by the control kernel into device memory and read by
 // the expert-FFN kernels of the same call.
@@ -32,6 +32,9 @@ struct Plan {
   int32_t perm[kMaxPairs];        // flat pair t*k+j grouped by expert (stable)
   int32_t pair_rank[kMaxPairs];   // rank in U of each flat pair
   float pair_w[kMaxPairs];        // routing weight of each flat pair
+  int32_t u_key[kMaxU];           // undo log: key of each member of U
+  uint64_t u_old_stamp[kMaxU];    // undo log: stamp of its slot before the call
+  uint64_t g_before;              // undo log: counter before the call
 };
 
 // Host-visible (pinned, mapped) summary of one call: the miss list the host
@@ -46,7 +49,7 @@ struct HostWork {
   int32_t evicted[kMaxU];
   int32_t fill[kMaxU];
   int32_t pairs[kMaxU];        // routed pairs of this expert
-  uint64_t old_stamp[kMaxU];   // stamp of the slot before the call
+  int32_t fill_order[kMaxU];   // f-th fill the kernel consumes -> rank in U
 };
 
 struct CacheDev {
@@ -97,42 +100,78 @@ __device__ __forceinline__ int block_excl_scan(int v, int* scratch, int* total) 
   return before;
 }
 
-// Grid-wide barrier for a cooperative launch.  The spin gives up after
-// ~`limit_ns` nanoseconds, records MOE_ERR_TIMEOUT in *err and returns false.
-__device__ __forceinline__ bool grid_barrier(unsigned* count, unsigned* gen, int* err,
+__device__ __forceinline__ unsigned long long globaltimer_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ unsigned ld_acquire_sys_u32(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.sys.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void st_release_u32(unsigned* p, unsigned v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Grid-wide barrier of a cooperative launch over a counter that only grows:
+// barrier number b of a launch completes when the counter reaches
+// base + (b + 1) * gridDim.x.  The wait gives up after limit_ns, records
+// MOE_ERR_TIMEOUT in *err and returns false.
+__device__ __forceinline__ bool grid_barrier(unsigned long long* count, unsigned long long target, int* err,
                                              unsigned long long limit_ns = 2000000000ull) {
   __shared__ int s_ok;
   __threadfence();  // publish this thread's global writes before arriving
   __syncthreads();
   if (threadIdx.x == 0) {
     s_ok = 1;
-    const unsigned nblocks = gridDim.x * gridDim.y * gridDim.z;
-    volatile unsigned* vgen = gen;
-    unsigned my_gen = *vgen;
-    __threadfence();
-    unsigned arrived = atomicAdd(count, 1u);
-    if (arrived == nblocks - 1) {
-      atomicExch(count, 0u);
-      __threadfence();
-      atomicAdd(gen, 1u);
-    } else {
-      unsigned long long t0;
-      asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
-      while (*vgen == my_gen) {
-        __nanosleep(64);
-        unsigned long long t;
-        asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-        if (t - t0 > limit_ns) {
-          atomicExch(err, MOE_ERR_TIMEOUT);
-          s_ok = 0;
-          break;
-        }
+    atomicAdd(count, 1ull);
+    const unsigned long long t0 = globaltimer_ns();
+    while (ld_acquire_u64(count) < target) {
+      __nanosleep(32);
+      if (globaltimer_ns() - t0 > limit_ns) {
+        atomicExch(err, MOE_ERR_TIMEOUT);
+        s_ok = 0;
+        break;
       }
     }
     __threadfence();
   }
   __syncthreads();
   return s_ok != 0;
+}
+
+// Wait until *flag == want (returns 0) or want | kFlagError (returns 1); 2 on
+// timeout (MOE_ERR_TIMEOUT recorded).  Thread 0 spins, the CTA waits on it.
+__device__ __forceinline__ int wait_flag(const unsigned* flag, unsigned want, int* err,
+                                         unsigned long long limit_ns = 5000000000ull) {
+  __shared__ int s_res;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int res = 2;
+    const unsigned long long t0 = globaltimer_ns();
+    for (;;) {
+      const unsigned v = ld_acquire_sys_u32(flag);
+      if (v == want) { res = 0; break; }
+      if (v == (want | kFlagError)) { res = 1; break; }
+      if (globaltimer_ns() - t0 > limit_ns) {
+        atomicExch(err, MOE_ERR_TIMEOUT);
+        break;
+      }
+      __nanosleep(64);
+    }
+    s_res = res;
+  }
+  __syncthreads();
+  return s_res;
 }
 
 }  // namespace moe

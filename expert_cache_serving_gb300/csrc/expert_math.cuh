@@ -1,0 +1,207 @@
+// Row access and dot products of the SwiGLU expert, per weight format.
+// A "chunk" is 16 bytes of a row's element stream: fp32 4 elements, bf16 8,
+// FP4 32 (plus the 2 e4m3 scale bytes of its two 16-element blocks).
+#pragma once
+#include <cuda_fp16.h>
+
+#include "common.cuh"
+
+namespace moe {
+
+// 16-byte load of read-only data (resident slots, shared experts).
+__device__ __forceinline__ uint4 ld_ro16(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+__device__ __forceinline__ unsigned short ld_ro2(const void* p) {
+  unsigned short r;
+  asm volatile("ld.global.nc.L1::no_allocate.u16 %0, [%1];" : "=h"(r) : "l"(p));
+  return r;
+}
+// Loads of slots being filled while the kernel runs: bypass L1 and the
+// read-only path, read at L2.
+__device__ __forceinline__ uint4 ld_cg16(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.cg.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
+  return r;
+}
+__device__ __forceinline__ unsigned short ld_cg2(const void* p) {
+  unsigned short r;
+  asm volatile("ld.global.cg.u16 %0, [%1];" : "=h"(r) : "l"(p));
+  return r;
+}
+template <bool FRESH>
+__device__ __forceinline__ uint4 ld_w16(const void* p) {
+  if constexpr (FRESH) return ld_cg16(p); else return ld_ro16(p);
+}
+template <bool FRESH>
+__device__ __forceinline__ unsigned short ld_w2(const void* p) {
+  if constexpr (FRESH) return ld_cg2(p); else return ld_ro2(p);
+}
+
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
+// two e2m1 codes (low nibble = first element) -> two floats (exact)
+__device__ __forceinline__ float2 e2m1x2_to_float2(uint32_t byte) {
+  uint32_t h2;
+  asm("{ .reg .b8 t; cvt.u8.u32 t, %1; cvt.rn.f16x2.e2m1x2 %0, t; }" : "=r"(h2) : "r"(byte));
+  __half2 hv = *reinterpret_cast<__half2*>(&h2);
+  return __half22float2(hv);
+}
+
+// two e4m3 bytes (low byte first) -> two floats (exact)
+__device__ __forceinline__ float2 e4m3x2_to_float2(unsigned short two) {
+  uint32_t h2;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(two));
+  __half2 hv = *reinterpret_cast<__half2*>(&h2);
+  return __half22float2(hv);
+}
+
+template <int WD>
+struct Fmt;
+template <>
+struct Fmt<MOE_FP32> {
+  static constexpr int kElemsPerChunk = 4;
+  static constexpr int kUnroll = 4;
+  __device__ static int64_t row_bytes(int K) { return (int64_t)K * 4; }
+};
+template <>
+struct Fmt<MOE_BF16> {
+  static constexpr int kElemsPerChunk = 8;
+  static constexpr int kUnroll = 4;
+  __device__ static int64_t row_bytes(int K) { return (int64_t)K * 2; }
+};
+template <>
+struct Fmt<MOE_FP4> {
+  static constexpr int kElemsPerChunk = 32;
+  static constexpr int kUnroll = 2;
+  __device__ static int64_t row_bytes(int K) { return (int64_t)K / 2; }
+};
+
+// Byte offsets of the matrices inside a record (see include/moecache.h).
+struct RecView {
+  const uint8_t* gate;
+  const uint8_t* up;
+  const uint8_t* down;
+  const uint8_t* gate_sc;
+  const uint8_t* up_sc;
+  const uint8_t* down_sc;
+};
+
+template <int WD>
+__device__ __forceinline__ RecView rec_view(const uint8_t* rec, int H, int I) {
+  RecView v;
+  const int64_t HI = (int64_t)H * I;
+  if (WD == MOE_FP32) {
+    v.gate = rec; v.up = rec + HI * 4; v.down = rec + 2 * HI * 4;
+    v.gate_sc = v.up_sc = v.down_sc = nullptr;
+  } else if (WD == MOE_BF16) {
+    v.gate = rec; v.up = rec + HI * 2; v.down = rec + 2 * HI * 2;
+    v.gate_sc = v.up_sc = v.down_sc = nullptr;
+  } else {
+    v.gate = rec;
+    v.up = rec + HI / 2;
+    v.gate_sc = rec + HI;
+    v.up_sc = rec + HI + HI / 16;
+    v.down = rec + HI + HI / 8;
+    v.down_sc = rec + HI + HI / 8 + HI / 2;
+  }
+  return v;
+}
+
+// ---- dot of one chunk with activations ---------------------------------------
+template <int WD, typename VT>
+__device__ __forceinline__ float chunk_dot(uint4 w, unsigned short sc2, const VT* xs);
+
+template <>
+__device__ __forceinline__ float chunk_dot<MOE_FP32, float>(uint4 w, unsigned short, const float* xs) {
+  float4 a = *reinterpret_cast<const float4*>(xs);
+  float acc = __uint_as_float(w.x) * a.x;
+  acc = fmaf(__uint_as_float(w.y), a.y, acc);
+  acc = fmaf(__uint_as_float(w.z), a.z, acc);
+  acc = fmaf(__uint_as_float(w.w), a.w, acc);
+  return acc;
+}
+
+__device__ __forceinline__ float dot8_bf16w(uint4 w, float4 a, float4 b) {
+  float acc = bf16lo(w.x) * a.x;
+  acc = fmaf(bf16hi(w.x), a.y, acc);
+  acc = fmaf(bf16lo(w.y), a.z, acc);
+  acc = fmaf(bf16hi(w.y), a.w, acc);
+  acc = fmaf(bf16lo(w.z), b.x, acc);
+  acc = fmaf(bf16hi(w.z), b.y, acc);
+  acc = fmaf(bf16lo(w.w), b.z, acc);
+  acc = fmaf(bf16hi(w.w), b.w, acc);
+  return acc;
+}
+
+template <>
+__device__ __forceinline__ float chunk_dot<MOE_BF16, __nv_bfloat16>(uint4 w, unsigned short, const __nv_bfloat16* xs) {
+  uint4 xv = *reinterpret_cast<const uint4*>(xs);
+  float4 a = make_float4(bf16lo(xv.x), bf16hi(xv.x), bf16lo(xv.y), bf16hi(xv.y));
+  float4 b = make_float4(bf16lo(xv.z), bf16hi(xv.z), bf16lo(xv.w), bf16hi(xv.w));
+  return dot8_bf16w(w, a, b);
+}
+
+template <>
+__device__ __forceinline__ float chunk_dot<MOE_BF16, float>(uint4 w, unsigned short, const float* xs) {
+  float4 a = *reinterpret_cast<const float4*>(xs);
+  float4 b = *reinterpret_cast<const float4*>(xs + 4);
+  return dot8_bf16w(w, a, b);
+}
+
+// 16 e2m1 codes (8 bytes) against 16 activation values
+template <typename VT>
+__device__ __forceinline__ float block16_dot(uint32_t c0, uint32_t c1, const VT* xs);
+
+template <>
+__device__ __forceinline__ float block16_dot<__nv_bfloat16>(uint32_t c0, uint32_t c1, const __nv_bfloat16* xs) {
+  uint4 xa = *reinterpret_cast<const uint4*>(xs);
+  uint4 xb = *reinterpret_cast<const uint4*>(xs + 8);
+  const uint32_t xw[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
+  float acc = 0.f;
+#pragma unroll
+  for (int b = 0; b < 8; ++b) {
+    const uint32_t byte = ((b < 4 ? c0 : c1) >> (8 * (b & 3))) & 0xFFu;
+    float2 w2 = e2m1x2_to_float2(byte);
+    acc = fmaf(w2.x, bf16lo(xw[b]), acc);
+    acc = fmaf(w2.y, bf16hi(xw[b]), acc);
+  }
+  return acc;
+}
+
+template <>
+__device__ __forceinline__ float block16_dot<float>(uint32_t c0, uint32_t c1, const float* xs) {
+  float acc = 0.f;
+#pragma unroll
+  for (int b = 0; b < 8; ++b) {
+    const uint32_t byte = ((b < 4 ? c0 : c1) >> (8 * (b & 3))) & 0xFFu;
+    float2 w2 = e2m1x2_to_float2(byte);
+    acc = fmaf(w2.x, xs[2 * b], acc);
+    acc = fmaf(w2.y, xs[2 * b + 1], acc);
+  }
+  return acc;
+}
+
+template <>
+__device__ __forceinline__ float chunk_dot<MOE_FP4, __nv_bfloat16>(uint4 w, unsigned short sc2, const __nv_bfloat16* xs) {
+  float2 s = e4m3x2_to_float2(sc2);
+  float a0 = block16_dot<__nv_bfloat16>(w.x, w.y, xs);
+  float a1 = block16_dot<__nv_bfloat16>(w.z, w.w, xs + 16);
+  return fmaf(a1, s.y, a0 * s.x);
+}
+
+template <>
+__device__ __forceinline__ float chunk_dot<MOE_FP4, float>(uint4 w, unsigned short sc2, const float* xs) {
+  float2 s = e4m3x2_to_float2(sc2);
+  float a0 = block16_dot<float>(w.x, w.y, xs);
+  float a1 = block16_dot<float>(w.z, w.w, xs + 16);
+  return fmaf(a1, s.y, a0 * s.x);
+}
+
+}  // namespace moe

@@ -1,0 +1,488 @@
+// One decode-size routed-MoE layer call as a single cooperative launch.
+//
+// FreeToken write-up: the router and the cache lookup run on the GPU ("decode
+// co-design"); one GPU step per layer deduplicates, classifies, picks victims
+// and rewrites ids ("CUDA Graph-compatible LRU cache"); the GPU evaluates the
+// set G = H ∪ F as a grouped FFN once the batched copy of F has landed, and
+// the partial sums merge exactly ("measured bandwidths decide the split",
+// Fig. 2 caption); decode is memory-bound, each routed expert's weights being
+// read once per token.
+//
+// CTA 0 runs the control step and publishes the miss list to the host, which
+// issues one cudaMemcpyAsync per half record (gate/up part, then W_down) on
+// the copy stream, each followed by a stream write of a per-fill flag.  The
+// other CTAs meanwhile load the activations and run the shared expert's
+// gate/up rows.  Then, all CTAs together (512 threads, one CTA per SM):
+//  1. gate/up rows of the resident experts: h = SiLU(x W_gate^T) * (x W_up^T);
+//     a warp streams one gate row and one up row with 16-byte loads (FP4
+//     dequantised in registers) and serves every token routed to the expert;
+//     CTA 0 meanwhile ranks the oldest slots for the next call;
+//  2. grid barrier, then W_down rows: each CTA owns a contiguous range of
+//     output rows n for every expert and keeps o[t][j][n] in shared memory;
+//  3. fills, in order, each as soon as its flag says the copy landed: gate/up
+//     rows, one grid barrier, then W_down rows into the same shared buffer;
+//  4. y_t[n] = sum_j w_tj o_tj[n] (+ shared) in rank order, in float32.
+// Every dot product has a fixed summation order independent of which phase
+// computes it, so outputs are bitwise identical whatever the residency.
+#include "control.cuh"
+#include "expert_math.cuh"
+
+namespace moe {
+
+struct ItemTable {
+  const uint8_t* rec[kMaxItems];
+  int ntok[kMaxItems];
+  int pair0[kMaxItems];      // -1 for the shared expert
+  int hbase[kMaxItems + 1];  // running token count in item order
+};
+
+// Items of plan list `which` into tb; returns the count.  All threads call.
+__device__ int load_items(const LayerParams& p, const Plan* pl, int which, ItemTable& tb) {
+  const int n = pl->n_items[which];
+  for (int i = threadIdx.x; i < n; i += blockDim.x) {
+    const int r = pl->items[which][i];
+    if (r == pl->n_u) {
+      tb.rec[i] = p.shared_rec;
+      tb.ntok[i] = p.B;
+      tb.pair0[i] = -1;
+    } else {
+      tb.rec[i] = p.slots + (int64_t)pl->u_slot[r] * p.S;
+      tb.pair0[i] = pl->u_off[r];
+      tb.ntok[i] = pl->u_off[r + 1] - pl->u_off[r];
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int run = 0;
+    for (int i = 0; i < n; ++i) { tb.hbase[i] = run; run += tb.ntok[i]; }
+    tb.hbase[n] = run;
+  }
+  __syncthreads();
+  return n;
+}
+
+// token, h row and rank slot of the q-th token of item `it`
+__device__ __forceinline__ void item_token(const LayerParams& p, const Plan* pl, const ItemTable& tb, int it, int q,
+                                           int* t, int* hrow, int* j) {
+  const int p0 = tb.pair0[it];
+  if (p0 < 0) {
+    *t = q;
+    *hrow = p.h_shared_row0 + q;
+    *j = p.k;
+  } else {
+    const int pair = pl->perm[p0 + q];
+    *t = pair / p.k;
+    *hrow = pair;
+    *j = pair % p.k;
+  }
+}
+
+// Gate/up rows of items [ib, ie), spread over CTAs [cta0, cta0 + ncta).
+template <int WD, int MAXT, bool FRESH, typename XT>
+__device__ void phase1(const LayerParams& p, const Plan* pl, const ItemTable& tb, int ib, int ie, int cta0, int ncta,
+                       const XT* xs) {
+  using F = Fmt<WD>;
+  constexpr int EPC = F::kElemsPerChunk, UNR = F::kUnroll;
+  const int rel = (int)blockIdx.x - cta0;
+  if (rel < 0 || rel >= ncta || ie <= ib) return;
+  const int H = p.H, I = p.I, lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int64_t total = (int64_t)(ie - ib) * I;
+  const int64_t t0 = (int64_t)rel * total / ncta, t1 = (int64_t)(rel + 1) * total / ncta;
+  const int nchunks = H / EPC;
+  const int64_t rb = F::row_bytes(H);
+  for (int64_t task = t0 + warp; task < t1; task += kWarps) {
+    const int it = ib + (int)(task / I), i = (int)(task % I);
+    const int ntok = tb.ntok[it];
+    const RecView v = rec_view<WD>(tb.rec[it], H, I);
+    const uint8_t* grow = v.gate + (int64_t)i * rb;
+    const uint8_t* urow = v.up + (int64_t)i * rb;
+    const uint8_t* gsc = (WD == MOE_FP4) ? v.gate_sc + (int64_t)i * (H / 16) : nullptr;
+    const uint8_t* usc = (WD == MOE_FP4) ? v.up_sc + (int64_t)i * (H / 16) : nullptr;
+    int tok[MAXT];
+#pragma unroll
+    for (int q = 0; q < MAXT; ++q) {
+      int t = 0, hr, j;
+      if (q < ntok) item_token(p, pl, tb, it, q, &t, &hr, &j);
+      tok[q] = t;
+    }
+    float ag[MAXT], au[MAXT];
+#pragma unroll
+    for (int q = 0; q < MAXT; ++q) { ag[q] = 0.f; au[q] = 0.f; }
+    for (int c0 = 0; c0 < nchunks; c0 += 32 * UNR) {
+      uint4 wg[UNR], wu[UNR];
+      unsigned short sg[UNR], su[UNR];
+#pragma unroll
+      for (int u = 0; u < UNR; ++u) {
+        const int c = c0 + lane + 32 * u;
+        if (c < nchunks) {
+          wg[u] = ld_w16<FRESH>(grow + (int64_t)c * 16);
+          wu[u] = ld_w16<FRESH>(urow + (int64_t)c * 16);
+          if (WD == MOE_FP4) {
+            sg[u] = ld_w2<FRESH>(gsc + 2 * c);
+            su[u] = ld_w2<FRESH>(usc + 2 * c);
+          } else {
+            sg[u] = su[u] = 0;
+          }
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < UNR; ++u) {
+        const int c = c0 + lane + 32 * u;
+        if (c < nchunks) {
+#pragma unroll
+          for (int q = 0; q < MAXT; ++q) {
+            if (q < ntok) {
+              const XT* xr = xs + (size_t)tok[q] * H + (size_t)c * EPC;
+              ag[q] += chunk_dot<WD, XT>(wg[u], sg[u], xr);
+              au[q] += chunk_dot<WD, XT>(wu[u], su[u], xr);
+            }
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < MAXT; ++q) {
+      if (q < ntok) {
+        const float g = warp_sum(ag[q]);
+        const float u = warp_sum(au[q]);
+        if (lane == 0) {
+          int t, hr, j;
+          item_token(p, pl, tb, it, q, &t, &hr, &j);
+          p.h[(int64_t)hr * I + i] = g / (1.0f + expf(-g)) * u;
+        }
+      }
+    }
+  }
+}
+
+// W_down rows [n0, n0 + nrows) of items [ib, ie) -> os[row][t][j].
+template <int WD, int MAXT, bool FRESH>
+__device__ void phase2(const LayerParams& p, const Plan* pl, const ItemTable& tb, int ib, int ie, int n0, int nrows,
+                       float* hs, float* os) {
+  using F = Fmt<WD>;
+  constexpr int EPC = F::kElemsPerChunk;
+  constexpr int R2 = 4;    // rows in flight per warp
+  constexpr int UNR2 = 2;  // 16-byte chunks per lane held in registers
+  const int H = p.H, I = p.I, B = p.B, k = p.k, lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int ostride = B * (k + 1);
+  const int nchunks = I / EPC;
+  const int64_t rb = F::row_bytes(I);
+  int g0 = ib;
+  while (g0 < ie) {
+    int g1 = g0, used = 0;
+    while (g1 < ie) {
+      const int nt = tb.ntok[g1];
+      if (used + nt * I > p.smem_h_floats && g1 > g0) break;
+      used += nt * I;
+      ++g1;
+    }
+    __syncthreads();
+    {  // h rows of the group, item-major, in one flat pass (all loads in flight together)
+      __shared__ int s_hrow[kMaxPairs + kMaxB];
+      const int rows = tb.hbase[g1] - tb.hbase[g0];
+      for (int rr = threadIdx.x; rr < rows; rr += blockDim.x) {
+        int g = g0;
+        while (tb.hbase[g + 1] - tb.hbase[g0] <= rr) ++g;
+        int t, hr, j;
+        item_token(p, pl, tb, g, rr - (tb.hbase[g] - tb.hbase[g0]), &t, &hr, &j);
+        s_hrow[rr] = hr;
+      }
+      __syncthreads();
+      const int per = I / 4;
+      for (int e = threadIdx.x; e < rows * per; e += blockDim.x) {
+        const int rr = e / per, c4 = e % per;
+        reinterpret_cast<float4*>(hs + (int64_t)rr * I)[c4] =
+            __ldcg(reinterpret_cast<const float4*>(p.h + (int64_t)s_hrow[rr] * I) + c4);
+      }
+    }
+    __syncthreads();
+    const int nunits = (g1 - g0) * nrows;
+    for (int u0 = warp * R2; u0 < nunits; u0 += kWarps * R2) {
+      uint4 w[R2][UNR2];
+      unsigned short sc[R2][UNR2];
+#pragma unroll
+      for (int r = 0; r < R2; ++r) {
+        const int unit = u0 + r;
+        if (unit < nunits) {
+          const int gi = g0 + unit / nrows, row = n0 + unit % nrows;
+          const RecView v = rec_view<WD>(tb.rec[gi], H, I);
+          const uint8_t* drow = v.down + (int64_t)row * rb;
+          const uint8_t* dsc = (WD == MOE_FP4) ? v.down_sc + (int64_t)row * (I / 16) : nullptr;
+#pragma unroll
+          for (int u = 0; u < UNR2; ++u) {
+            const int c = lane + 32 * u;
+            if (c < nchunks) {
+              w[r][u] = ld_w16<FRESH>(drow + (int64_t)c * 16);
+              sc[r][u] = (WD == MOE_FP4) ? ld_w2<FRESH>(dsc + 2 * c) : (unsigned short)0;
+            }
+          }
+        }
+      }
+#pragma unroll
+      for (int r = 0; r < R2; ++r) {
+        const int unit = u0 + r;
+        if (unit >= nunits) continue;
+        const int gi = g0 + unit / nrows, row = n0 + unit % nrows;
+        const int hbase = tb.hbase[gi] - tb.hbase[g0];
+        const int ntok = tb.ntok[gi];
+#pragma unroll
+        for (int q = 0; q < MAXT; ++q) {
+          if (q < ntok) {
+            const float* hrow = hs + (int64_t)(hbase + q) * I;
+            float acc = 0.f;
+#pragma unroll
+            for (int u = 0; u < UNR2; ++u) {
+              const int c = lane + 32 * u;
+              if (c < nchunks) acc += chunk_dot<WD, float>(w[r][u], sc[r][u], hrow + (int64_t)c * EPC);
+            }
+            for (int c = lane + 32 * UNR2; c < nchunks; c += 32) {  // rows longer than 32*UNR2 chunks
+              const RecView v = rec_view<WD>(tb.rec[gi], H, I);
+              const uint4 ww = ld_w16<FRESH>(v.down + (int64_t)row * rb + (int64_t)c * 16);
+              const unsigned short ss =
+                  (WD == MOE_FP4) ? ld_w2<FRESH>(v.down_sc + (int64_t)row * (I / 16) + 2 * c) : (unsigned short)0;
+              acc += chunk_dot<WD, float>(ww, ss, hrow + (int64_t)c * EPC);
+            }
+            acc = warp_sum(acc);
+            if (lane == 0) {
+              int t, hr, j;
+              item_token(p, pl, tb, gi, q, &t, &hr, &j);
+              os[(row - n0) * ostride + t * (k + 1) + j] = acc;
+            }
+          }
+        }
+      }
+    }
+    g0 = g1;
+  }
+  __syncthreads();
+}
+
+template <int WD, int MAXT>
+__global__ void __launch_bounds__(kThreads, 1) layer_kernel(LayerParams p) {
+  using XT = typename std::conditional<WD == MOE_FP32, float, __nv_bfloat16>::type;
+  extern __shared__ __align__(16) uint8_t smem[];
+  __shared__ CtrlSmem cs;
+  __shared__ ItemTable tb;
+  const int H = p.H, B = p.B, k = p.k;
+  const int G = gridDim.x;
+  const bool ctrl = blockIdx.x == 0;
+  XT* xs = reinterpret_cast<XT*>(smem);
+  float* hs = reinterpret_cast<float*>(smem + (((size_t)B * H * sizeof(XT) + 15) & ~(size_t)15));
+  float* os = hs + p.smem_h_floats;
+  const int n0 = (int)((int64_t)blockIdx.x * H / G), n1 = (int)((int64_t)(blockIdx.x + 1) * H / G);
+  const int nrows = n1 - n0;
+
+  // ---- 0. control | activations and the shared expert's gate/up rows --------
+  if (p.tl && blockIdx.x == 1 && threadIdx.x == 0) p.tl[0] = globaltimer_ns();
+  if (ctrl) {
+    const int cst = control_step(p, cs);
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      st_release_u32(p.plan_flag, p.seq);
+      if (p.tl) p.tl[10] = globaltimer_ns();
+    }
+    if (cst == MOE_OK) compact_oldest(p, cs);
+    if (p.tl && threadIdx.x == 0) p.tl[11] = globaltimer_ns();
+  }
+  {
+    const int nvec = (int)((size_t)B * H * sizeof(XT) / 16);
+    const uint4* src = reinterpret_cast<const uint4*>(p.x);
+    uint4* dst = reinterpret_cast<uint4*>(xs);
+    for (int i = threadIdx.x; i < nvec; i += blockDim.x) dst[i] = src[i];
+  }
+  if (!ctrl && p.has_shared) {
+    if (threadIdx.x == 0) {
+      tb.rec[0] = p.shared_rec;
+      tb.ntok[0] = B;
+      tb.pair0[0] = -1;
+      tb.hbase[0] = 0;
+      tb.hbase[1] = B;
+    }
+    __syncthreads();
+    phase1<WD, MAXT, false>(p, p.plan, tb, 0, 1, 1, G - 1, xs);
+  }
+  if (!ctrl && wait_flag(p.plan_flag, p.seq, p.err) != 0) return;
+  __syncthreads();
+  const bool rec = p.tl && blockIdx.x == 1 && threadIdx.x == 0;
+  if (rec) p.tl[1] = globaltimer_ns();
+  const Plan* pl = p.plan;
+  if (pl->err != MOE_OK) return;
+
+  // ---- 1. gate/up rows of the resident routed experts --------------------------
+  const int n_res = load_items(p, pl, 0, tb);
+  if (threadIdx.x < n_res && nrows > 0) {  // this CTA's W_down rows of every resident expert -> L2
+    const RecView v = rec_view<WD>(tb.rec[threadIdx.x], H, p.I);
+    const int64_t rb = Fmt<WD>::row_bytes(p.I);
+    prefetch_l2(v.down + (int64_t)n0 * rb, (uint32_t)(nrows * rb));
+    if (WD == MOE_FP4) prefetch_l2(v.down_sc + (int64_t)n0 * (p.I / 16), (uint32_t)(nrows * (p.I / 16)));
+  }
+  if (!ctrl) phase1<WD, MAXT, false>(p, pl, tb, 0, n_res - p.has_shared, 1, G - 1, xs);
+  if (rec) p.tl[2] = globaltimer_ns();
+  if (!grid_barrier(p.bar, p.bar_base + (unsigned long long)G, p.err)) return;
+  if (rec) p.tl[3] = globaltimer_ns();
+
+  // ---- 2. W_down rows of the resident experts --------------------------------------
+  const int ostride = B * (k + 1);
+  for (int i = threadIdx.x; i < nrows * ostride; i += blockDim.x) os[i] = 0.f;
+  phase2<WD, MAXT, false>(p, pl, tb, 0, n_res, n0, nrows, hs, os);
+  if (rec) p.tl[4] = globaltimer_ns();
+
+  // ---- 3. fills, each as soon as its copy has landed -------------------------------
+  const int nf = pl->n_items[1];
+  int fill_err = 0;
+  if (nf > 0) {
+    load_items(p, pl, 1, tb);
+    for (int f = 0; f < nf && !fill_err; ++f) {
+      if (wait_flag(&p.fill_flags[f], p.seq, p.err) != 0) {
+        fill_err = 1;
+        break;
+      }
+      if (rec && f == 0) p.tl[5] = globaltimer_ns();
+      phase1<WD, MAXT, true>(p, pl, tb, f, f + 1, 0, G, xs);
+    }
+    if (rec) p.tl[6] = globaltimer_ns();
+    if (!grid_barrier(p.bar, p.bar_base + 2ull * G, p.err)) return;
+    if (rec) p.tl[7] = globaltimer_ns();
+    for (int f = 0; f < nf && !fill_err; ++f) {
+      if (wait_flag(&p.fill_flags[kMaxU + f], p.seq, p.err) != 0) {
+        fill_err = 1;
+        break;
+      }
+      if (rec && f == nf - 1) p.tl[8] = globaltimer_ns();
+      phase2<WD, MAXT, true>(p, pl, tb, f, f + 1, n0, nrows, hs, os);
+    }
+    if (fill_err) {
+      if (ctrl) undo_call(p);
+      return;
+    }
+  }
+
+  // ---- 4. weighted combine in rank order --------------------------------------------
+  for (int e = threadIdx.x; e < nrows * B; e += blockDim.x) {
+    const int nl = e / B, t = e % B, n = n0 + nl;
+    const float* o = os + nl * ostride + t * (k + 1);
+    float acc = 0.f;
+    for (int j = 0; j < k; ++j) acc = fmaf(pl->pair_w[t * k + j], o[j], acc);
+    if (p.has_shared) acc += o[k];
+    if constexpr (WD == MOE_FP32)
+      reinterpret_cast<float*>(p.y)[(int64_t)t * H + n] = acc;
+    else
+      reinterpret_cast<__nv_bfloat16*>(p.y)[(int64_t)t * H + n] = __float2bfloat16_rn(acc);
+  }
+  if (rec) p.tl[9] = globaltimer_ns();
+}
+
+// ---- router logits (when the caller passes W_r instead of logits) ------------------
+template <typename XT>
+__global__ void router_logits_kernel(const XT* __restrict__ x, const float* __restrict__ wr, int B, int E, int H,
+                                     float* __restrict__ logits) {
+  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+  if (warp >= B * E) return;
+  const int t = warp / E, e = warp % E;
+  const XT* xr = x + (size_t)t * H;
+  const float* w = wr + (size_t)e * H;
+  float acc = 0.f;
+  for (int h = lane; h < H; h += 32) {
+    float xv;
+    if constexpr (sizeof(XT) == 2)
+      xv = __bfloat162float(xr[h]);
+    else
+      xv = xr[h];
+    acc = fmaf(xv, w[h], acc);
+  }
+  acc = warp_sum(acc);
+  if (lane == 0) logits[warp] = acc;
+}
+
+cudaError_t launch_router_logits(const void* x, bool x_bf16, const float* wr, int B, int E, int H, float* logits,
+                                 cudaStream_t s) {
+  const int warps = B * E, threads = 256, blocks = (warps * 32 + threads - 1) / threads;
+  if (x_bf16)
+    router_logits_kernel<__nv_bfloat16><<<blocks, threads, 0, s>>>((const __nv_bfloat16*)x, wr, B, E, H, logits);
+  else
+    router_logits_kernel<float><<<blocks, threads, 0, s>>>((const float*)x, wr, B, E, H, logits);
+  return cudaGetLastError();
+}
+
+// ---- launch ------------------------------------------------------------------------------
+size_t layer_smem_bytes(int wdtype, int B, int H, int k, int smem_h_floats, int rows_per_cta_max) {
+  const size_t xbytes = (((size_t)B * H * (wdtype == MOE_FP32 ? 4 : 2)) + 15) & ~(size_t)15;
+  return xbytes + (size_t)smem_h_floats * 4 + (size_t)rows_per_cta_max * B * (k + 1) * 4;
+}
+
+template <int WD, int MAXT>
+static cudaError_t launch_t(const LayerParams& p, int grid, size_t smem, cudaStream_t s) {
+  auto fn = layer_kernel<WD, MAXT>;
+  static size_t smem_set = 0;  // largest dynamic shared memory already allowed for this instantiation
+  if (smem > smem_set) {
+    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    smem_set = smem;
+  }
+  void* args[] = {const_cast<LayerParams*>(&p)};
+  return cudaLaunchCooperativeKernel((const void*)fn, dim3(grid), dim3(kThreads), args, smem, s);
+}
+
+template <int WD>
+static cudaError_t launch_w(const LayerParams& p, int grid, size_t smem, cudaStream_t s) {
+  if (p.B <= 1) return launch_t<WD, 1>(p, grid, smem, s);
+  if (p.B <= 2) return launch_t<WD, 2>(p, grid, smem, s);
+  if (p.B <= 4) return launch_t<WD, 4>(p, grid, smem, s);
+  if (p.B <= 8) return launch_t<WD, 8>(p, grid, smem, s);
+  return launch_t<WD, 16>(p, grid, smem, s);
+}
+
+cudaError_t launch_layer(int wdtype, const LayerParams& p, int grid, size_t smem, cudaStream_t s) {
+  switch (wdtype) {
+    case MOE_FP32: return launch_w<MOE_FP32>(p, grid, smem, s);
+    case MOE_BF16: return launch_w<MOE_BF16>(p, grid, smem, s);
+    case MOE_FP4: return launch_w<MOE_FP4>(p, grid, smem, s);
+  }
+  return cudaErrorInvalidValue;
+}
+
+template <int WD>
+static void kernel_list(const void** out) {
+  out[0] = (const void*)layer_kernel<WD, 1>;
+  out[1] = (const void*)layer_kernel<WD, 2>;
+  out[2] = (const void*)layer_kernel<WD, 4>;
+  out[3] = (const void*)layer_kernel<WD, 8>;
+  out[4] = (const void*)layer_kernel<WD, 16>;
+}
+
+static void kernels_of(int wdtype, const void** out) {
+  if (wdtype == MOE_FP32) kernel_list<MOE_FP32>(out);
+  else if (wdtype == MOE_BF16) kernel_list<MOE_BF16>(out);
+  else kernel_list<MOE_FP4>(out);
+}
+
+size_t layer_static_smem(int wdtype) {
+  const void* fns[5];
+  kernels_of(wdtype, fns);
+  size_t mx = 0;
+  for (const void* f : fns) {
+    cudaFuncAttributes a;
+    if (cudaFuncGetAttributes(&a, f) == cudaSuccess) mx = a.sharedSizeBytes > mx ? a.sharedSizeBytes : mx;
+  }
+  return mx;
+}
+
+// Largest cooperative grid every instantiation supports with `smem` dynamic
+// shared memory, capped at one CTA per SM.
+int layer_max_grid(int wdtype, size_t smem) {
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const void* fns[5];
+  kernels_of(wdtype, fns);
+  int per_sm = 1;
+  for (const void* f : fns) {
+    int n = 0;
+    if (cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) return 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, f, kThreads, smem) != cudaSuccess) return 0;
+    per_sm = n < per_sm ? n : per_sm;
+  }
+  return sms * per_sm;
+}
+
+}  // namespace moe

@@ -30,8 +30,11 @@ class moe_stats(ctypes.Structure):
     _fields_ = [("calls", ctypes.c_int64), ("tokens", ctypes.c_int64), ("hits", ctypes.c_int64),
                 ("misses", ctypes.c_int64), ("evictions", ctypes.c_int64), ("routed_pairs", ctypes.c_int64),
                 ("routed_pair_hits", ctypes.c_int64), ("bytes_filled", ctypes.c_int64),
-                ("ffn_launches", ctypes.c_int64), ("ffn_records", ctypes.c_int64), ("ffn_ms", ctypes.c_double),
-                ("ffn_timed", ctypes.c_int64), ("resize_calls", ctypes.c_int64), ("resize_moves", ctypes.c_int64),
+                ("layer_launches", ctypes.c_int64), ("records_streamed", ctypes.c_int64),
+                ("layer_ms", ctypes.c_double), ("layer_timed", ctypes.c_int64), ("hit_only_ms", ctypes.c_double),
+                ("hit_only_timed", ctypes.c_int64), ("hit_only_records", ctypes.c_int64),
+                ("host_wait_us", ctypes.c_double), ("host_issue_us", ctypes.c_double),
+                ("resize_calls", ctypes.c_int64), ("resize_moves", ctypes.c_int64),
                 ("resize_evictions", ctypes.c_int64), ("prefill_layers", ctypes.c_int64),
                 ("prefill_ms", ctypes.c_double), ("prefill_copy_ms", ctypes.c_double),
                 ("prefill_compute_ms", ctypes.c_double)]
@@ -51,6 +54,15 @@ class moe_layer_aux(ctypes.Structure):
                 ("perm", ctypes.c_void_p), ("offsets", ctypes.c_void_p), ("logits", ctypes.c_void_p)]
 
 
+class moe_phase_times(ctypes.Structure):
+    _fields_ = [("calls_hit_only", ctypes.c_int64), ("calls_with_fills", ctypes.c_int64),
+                ("hit_only_us", ctypes.c_double * 12), ("with_fills_us", ctypes.c_double * 12)]
+
+    def as_dict(self):
+        return {"calls_hit_only": self.calls_hit_only, "calls_with_fills": self.calls_with_fills,
+                "hit_only_us": list(self.hit_only_us), "with_fills_us": list(self.with_fills_us)}
+
+
 _P = ctypes.c_void_p
 _I32, _I64 = ctypes.c_int32, ctypes.c_int64
 
@@ -65,6 +77,7 @@ SIGNATURES = {
     "moe_cache_stats": (_I32, [_P, ctypes.POINTER(moe_stats)]),
     "moe_cache_reset_stats": (_I32, [_P]),
     "moe_cache_set_profiling": (_I32, [_P, _I32]),
+    "moe_cache_phase_times": (_I32, [_P, ctypes.POINTER(moe_phase_times)]),
     "moe_cache_set_trace": (_I32, [_P, _I32]),
     "moe_cache_trace": (_I32, [_P, ctypes.POINTER(moe_event), _I64, ctypes.POINTER(_I64)]),
     "moe_cache_state": (_I32, [_P, _P, _P, _I64, ctypes.POINTER(_I64), ctypes.POINTER(ctypes.c_uint64)]),
@@ -161,8 +174,14 @@ def moe_cache_reset_stats(cache: int) -> None:
     check(lib.moe_cache_reset_stats(cache), "moe_cache_reset_stats")
 
 
-def moe_cache_set_profiling(cache: int, on: bool) -> None:
-    check(lib.moe_cache_set_profiling(cache, int(on)), "moe_cache_set_profiling")
+def moe_cache_set_profiling(cache: int, level: int) -> None:
+    check(lib.moe_cache_set_profiling(cache, int(level)), "moe_cache_set_profiling")
+
+
+def moe_cache_phase_times(cache: int) -> dict:
+    pt = moe_phase_times()
+    check(lib.moe_cache_phase_times(cache, ctypes.byref(pt)), "moe_cache_phase_times")
+    return pt.as_dict()
 
 
 def moe_cache_set_trace(cache: int, on: bool) -> None:

@@ -36,8 +36,10 @@
  *
  * Expert record (one host-pool row, one cache slot), row-major [out][in]:
  *  MOE_FP32, MOE_BF16: W_gate[I][H] | W_up[I][H] | W_down[H][I]
- *  MOE_FP4: gate codes[I][H/2] | up codes[I][H/2] | down codes[H][I/2] |
- *           gate scales[I][H/16] | up scales[I][H/16] | down scales[H][I/16]
+ *  MOE_FP4: gate codes[I][H/2] | up codes[I][H/2] | gate scales[I][H/16] |
+ *           up scales[I][H/16] | down codes[H][I/2] | down scales[H][I/16]
+ *  In every format the first part (everything the gate/up projections read)
+ *  and the second part (W_down) are each contiguous.
  *    (e2m1 codes, element 2c in the low nibble of byte c; one e4m3 scale per
  *     16 consecutive elements of a row; no per-tensor scale)
  *  Expert FFN: h = SiLU(x W_gate^T) * (x W_up^T), o = h W_down^T.
@@ -91,10 +93,15 @@ typedef struct {
   int64_t routed_pairs;      /* (token, rank) pairs */
   int64_t routed_pair_hits;  /* pairs whose expert was resident before the call */
   int64_t bytes_filled;      /* host -> device bytes copied by fills */
-  int64_t ffn_launches;      /* expert-FFN kernel launches */
-  int64_t ffn_records;       /* expert records streamed by those launches (incl. shared) */
-  double ffn_ms;             /* summed device time of those launches (profiling on) */
-  int64_t ffn_timed;         /* launches included in ffn_ms */
+  int64_t layer_launches;    /* layer-kernel launches (one per call) */
+  int64_t records_streamed;  /* expert records read by the completed calls (incl. shared) */
+  double layer_ms;           /* summed device time of timed launches (profiling on) */
+  int64_t layer_timed;       /* launches included in layer_ms */
+  double hit_only_ms;        /* ... of those, launches of calls without fills */
+  int64_t hit_only_timed;
+  int64_t hit_only_records;  /* records those calls read */
+  double host_wait_us;       /* host time from launch to seeing the call's miss list */
+  double host_issue_us;      /* host time spent issuing fills */
   int64_t resize_calls, resize_moves, resize_evictions;
   int64_t prefill_layers;
   double prefill_ms, prefill_copy_ms, prefill_compute_ms; /* profiling on */
@@ -192,8 +199,25 @@ moe_status moe_prefill_stream(moe_cache_t cache, int32_t layer_begin, int32_t la
 moe_status moe_cache_stats(moe_cache_t cache, moe_stats* out);
 moe_status moe_cache_reset_stats(moe_cache_t cache);
 
-/* on != 0: time every expert-FFN and prefill launch with CUDA events. */
+/* on >= 1: time every layer-kernel and prefill launch with CUDA events.
+ * on >= 2: also record GPU timestamps at the phases of every layer call
+ * (see moe_phase_times). */
 moe_status moe_cache_set_profiling(moe_cache_t cache, int32_t on);
+
+/* Mean time, in microseconds after the layer kernel starts, at which a call
+ * reaches each phase, over the calls profiled at level 2 (split by whether
+ * the call had fills).  Stamps: 0 start, 1 plan visible to all CTAs, 2 gate/up
+ * rows of resident experts done, 3 first grid barrier passed, 4 W_down rows of
+ * resident experts done, 5 first fill's first half landed, 6 gate/up rows of
+ * the fills done, 7 second grid barrier passed, 8 last fill's second half
+ * landed, 9 end, 10 control step done, 11 victim list maintained.  A call that
+ * never reaches a stamp does not count towards it. */
+typedef struct {
+  int64_t calls_hit_only, calls_with_fills;
+  double hit_only_us[12];
+  double with_fills_us[12];
+} moe_phase_times;
+moe_status moe_cache_phase_times(moe_cache_t cache, moe_phase_times* out);
 
 /* on != 0: record one moe_event per distinct expert access and per resize
  * eviction.  moe_cache_trace copies up to cap recorded events to buf (host)

@@ -9,8 +9,8 @@ copies three weight tensors).
 
 Layout (row-major, [out][in]):
 * fp32 / bf16: ``W_gate[I][H] | W_up[I][H] | W_down[H][I]``.
-* FP4: ``gate codes[I][H/2] | up codes[I][H/2] | down codes[H][I/2] |
-  gate scales[I][H/16] | up scales[I][H/16] | down scales[H][I/16]``.
+* FP4: ``gate codes[I][H/2] | up codes[I][H/2] | gate scales[I][H/16] |
+  up scales[I][H/16] | down codes[H][I/2] | down scales[H][I/16]``.
 """
 from __future__ import annotations
 
@@ -46,10 +46,12 @@ def parse(record: np.ndarray, H: int, I: int, wdtype: int):
     elif wdtype == BF16:
         v = _bf16_to_f64(rec.view(np.uint16))
     else:
-        c = rec[:3 * HI // 2]
-        s = rec[3 * HI // 2:]
-        g = fp4.dequant_rows(c[:HI // 2].reshape(I, H // 2), s[:HI // 16].reshape(I, H // 16))
-        u = fp4.dequant_rows(c[HI // 2:HI].reshape(I, H // 2), s[HI // 16:2 * HI // 16].reshape(I, H // 16))
-        d = fp4.dequant_rows(c[HI:].reshape(H, I // 2), s[2 * HI // 16:].reshape(H, I // 16))
+        q, e = HI // 2, HI // 16  # code and scale bytes of one matrix
+        gc, uc = rec[0:q], rec[q:2 * q]
+        gs, us = rec[2 * q:2 * q + e], rec[2 * q + e:2 * q + 2 * e]
+        dc, ds = rec[2 * q + 2 * e:3 * q + 2 * e], rec[3 * q + 2 * e:]
+        g = fp4.dequant_rows(gc.reshape(I, H // 2), gs.reshape(I, H // 16))
+        u = fp4.dequant_rows(uc.reshape(I, H // 2), us.reshape(I, H // 16))
+        d = fp4.dequant_rows(dc.reshape(H, I // 2), ds.reshape(H, I // 16))
         return g, u, d
     return v[:HI].reshape(I, H), v[HI:2 * HI].reshape(I, H), v[2 * HI:].reshape(H, I)

@@ -35,10 +35,11 @@ Record layout (one record per (layer, expert) key ``l*E + e``; the shared
 expert of layer ``l`` uses key ``L*E + l``):
 
 * fp32 / bf16: ``W_gate[I][H] | W_up[I][H] | W_down[H][I]`` row-major.
-* FP4: ``gate codes[I][H/2] | up codes[I][H/2] | down codes[H][I/2] |
-  gate scales[I][H/16] | up scales[I][H/16] | down scales[H][I/16]``; code
-  byte ``c`` of a row holds element ``2c`` in its low nibble and ``2c+1`` in
-  its high nibble; scale byte ``b`` covers elements ``16b .. 16b+15``.
+* FP4: ``gate codes[I][H/2] | up codes[I][H/2] | gate scales[I][H/16] |
+  up scales[I][H/16] | down codes[H][I/2] | down scales[H][I/16]`` (the
+  gate/up half and the down half are each contiguous); code byte ``c`` of a
+  row holds element ``2c`` in its low nibble and ``2c+1`` in its high
+  nibble; scale byte ``b`` covers elements ``16b .. 16b+15``.
 """
 from __future__ import annotations
 
@@ -169,14 +170,14 @@ def expert_record(seed: int, key: int, H: int, I: int, wdtype: int, sigma: float
     if wdtype != WD_FP4:
         raise ValueError(wdtype)
     out = np.empty(record_bytes(H, I, wdtype), dtype=np.uint8)
-    shapes = [(I, H), (I, H), (H, I)]
-    code_off, scale_off = 0, 3 * HI // 2
-    for t, (R, K) in enumerate(shapes):
-        codes, scales = quantise_fp4_rows(v[t * HI:(t + 1) * HI].reshape(R, K))
-        out[code_off:code_off + codes.size] = codes.reshape(-1)
-        out[scale_off:scale_off + scales.size] = scales.reshape(-1)
-        code_off += codes.size
-        scale_off += scales.size
+    parts = []
+    for t, (R, K) in enumerate([(I, H), (I, H), (H, I)]):
+        parts.append(quantise_fp4_rows(v[t * HI:(t + 1) * HI].reshape(R, K)))
+    (gc, gs), (uc, us), (dc, ds) = parts
+    off = 0
+    for arr in (gc, uc, gs, us, dc, ds):
+        out[off:off + arr.size] = arr.reshape(-1)
+        off += arr.size
     return out
 
 

@@ -106,8 +106,17 @@ static void do_row(const job_t* j, int64_t unit) {
   } else {
     int64_t S = 3 * HI / 2 + 3 * HI / 16;
     uint8_t* rec = j->dst + kidx * S;
-    uint8_t* codes = rec + (n0 >> 1);
-    uint8_t* scales = rec + 3 * HI / 2 + (n0 >> 4);
+    /* gate codes | up codes | gate scales | up scales | down codes | down scales */
+    const int64_t in_t = (int64_t)row * K; /* element offset inside tensor t */
+    uint8_t* codes;
+    uint8_t* scales;
+    if (t < 2) {
+      codes = rec + t * (HI / 2) + (in_t >> 1);
+      scales = rec + HI + t * (HI / 16) + (in_t >> 4);
+    } else {
+      codes = rec + HI + HI / 8 + (in_t >> 1);
+      scales = rec + HI + HI / 8 + HI / 2 + (in_t >> 4);
+    }
     for (int64_t b = 0; b < K / 16; ++b) {
       float v[16];
       float amax = 0.0f;
