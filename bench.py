@@ -222,6 +222,7 @@ def run_native(args, w):
     x_dev = x_host.to(dev)
     y_dev = torch.empty_like(x_dev)
     cache = runner.Cache(w, pool, shared)
+    mc.moe_cache_set_fill_mode(cache.handle, mc.MOE_FILL_DEVICE if args.fill_mode == "device" else mc.MOE_FILL_COPY)
     setup_s = time.perf_counter() - t_setup
     stream = torch.cuda.current_stream()
 
@@ -311,7 +312,7 @@ def run_native(args, w):
         "data": "synthetic",
         "config": {"workload": w.name, "layers": w.L, "experts": w.E, "top_k": w.k, "hidden": w.H,
                    "intermediate": w.I, "shared_expert": w.shared, "batch": w.B, "cache_slots": w.C,
-                   "record_bytes": S, "host_pool_GB": round(w.LE * S / 1e9, 2),
+                   "record_bytes": S, "host_pool_GB": round(w.LE * S / 1e9, 2), "fill_mode": args.fill_mode,
                    "trace": "AR(1) logits rho=0.8 sd=0.6, cold cache at warm-up start",
                    "l2": "per-step expert stream >> 129 MB L2 (no reuse across layers); no flush"},
         "hit_rate": hits / (hits + misses) if hits + misses else None,
@@ -362,6 +363,8 @@ def main():
     ap.add_argument("--cpu-tokens", type=int, default=3)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile", type=int, default=1, help="1: CUDA events per launch; 2: also phase timestamps")
+    ap.add_argument("--fill-mode", default="copy", choices=["copy", "device"],
+                    help="copy: host-issued cudaMemcpyAsync fills (default); device: the kernel pulls misses itself")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

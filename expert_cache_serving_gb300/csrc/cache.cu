@@ -208,6 +208,7 @@ struct moe_cache {
   };
   std::vector<Timed> pending;
   int inject_after = -1;
+  int fill_mode = MOE_FILL_COPY;
   // phase timeline (profiling level 2): ring of [kTlRing][12] GPU timestamps
   int profile_level = 0;
   unsigned long long* d_tl = nullptr;
@@ -544,6 +545,8 @@ extern "C" moe_status moe_layer_forward_ex(moe_cache_t c, int32_t layer, const v
   p.bar_base = c->bar_base;
   p.err = c->d_err;
   p.has_shared = d.has_shared;
+  p.device_fill = c->fill_mode == MOE_FILL_DEVICE;
+  p.pool = c->host_pool;  // pinned pages are mapped at the same address under unified addressing
   p.slots = (const uint8_t*)c->slots.base;
   p.S = c->S;
   p.shared_rec = d.has_shared ? c->shared_dev + (int64_t)layer * c->S : nullptr;
@@ -594,13 +597,13 @@ extern "C" moe_status moe_layer_forward_ex(moe_cache_t c, int32_t layer, const v
     return fail(MOE_ERR_CUDA, "internal error: victim selection found an inconsistent cache state");
   }
   const int n_u = w.n_u, n_miss = w.n_miss;
-  c->bar_base += (unsigned long long)c->grid * (n_miss > 0 ? 2 : 1);
+  c->bar_base += (unsigned long long)c->grid * (n_miss > 0 && !p.device_fill ? 2 : 1);
   if (tl_row >= 0) c->tl_calls.emplace_back(tl_row, n_miss > 0 ? 1 : 0);
   if (c->profiling) {
     c->pending.push_back({ta, tb, n_miss == 0, (int64_t)n_u + d.has_shared});
     if (c->pending.size() > 4096) drain_pending(c, false);
   }
-  if (n_miss > 0) {
+  if (n_miss > 0 && !p.device_fill) {
     // one copy per half record on the copy stream, each followed by a flag the
     // kernel waits on; the copies start once every earlier call has finished
     Drv& dr = drv();
@@ -836,6 +839,20 @@ extern "C" moe_status moe_cache_state(moe_cache_t c, int32_t* owner, uint64_t* s
 extern "C" const void* moe_cache_slot_ptr(moe_cache_t c, int64_t s) {
   if (!c || s < 0 || s >= c->C) return nullptr;
   return (const uint8_t*)c->slots.base + s * c->S;
+}
+
+extern "C" moe_status moe_cache_set_fill_mode(moe_cache_t c, int32_t mode) {
+  if (!c) return fail(MOE_ERR_INVALID_ARG, "cache is NULL");
+  if (mode != MOE_FILL_COPY && mode != MOE_FILL_DEVICE) return fail(MOE_ERR_INVALID_ARG, "unknown fill mode %d", mode);
+  if (mode == MOE_FILL_DEVICE) {
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, c->host_pool) != cudaSuccess || a.devicePointer != (void*)c->host_pool) {
+      cudaGetLastError();
+      return fail(MOE_ERR_INVALID_ARG, "the host pool is not mapped at the same device address");
+    }
+  }
+  c->fill_mode = mode;
+  return MOE_OK;
 }
 
 extern "C" moe_status moe_cache_inject_fill_failure(moe_cache_t c, int32_t after) {

@@ -112,12 +112,6 @@ __device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long
   return v;
 }
 
-__device__ __forceinline__ unsigned ld_acquire_sys_u32(const unsigned* p) {
-  unsigned v;
-  asm volatile("ld.acquire.sys.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-
 __device__ __forceinline__ void st_release_u32(unsigned* p, unsigned v) {
   asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
@@ -159,14 +153,20 @@ __device__ __forceinline__ int wait_flag(const unsigned* flag, unsigned want, in
     int res = 2;
     const unsigned long long t0 = globaltimer_ns();
     for (;;) {
-      const unsigned v = ld_acquire_sys_u32(flag);
-      if (v == want) { res = 0; break; }
-      if (v == (want | kFlagError)) { res = 1; break; }
+      // relaxed polling at GPU scope, one acquire fence once the value is seen
+      // (system-scope acquires from every CTA slowed the copy engine down)
+      unsigned v;
+      asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
+      if (v == want || v == (want | kFlagError)) {
+        asm volatile("fence.acq_rel.gpu;" ::: "memory");
+        res = v == want ? 0 : 1;
+        break;
+      }
       if (globaltimer_ns() - t0 > limit_ns) {
         atomicExch(err, MOE_ERR_TIMEOUT);
         break;
       }
-      __nanosleep(64);
+      __nanosleep(256);
     }
     s_res = res;
   }

@@ -30,35 +30,60 @@
 namespace moe {
 
 struct ItemTable {
-  const uint8_t* rec[kMaxItems];
+  const uint8_t* rec[kMaxItems];  // where the record is read (slot, shared expert, or host pool)
+  uint8_t* dst[kMaxItems];        // slot a device-driven fill writes the record to (else null)
   int ntok[kMaxItems];
   int pair0[kMaxItems];      // -1 for the shared expert
   int hbase[kMaxItems + 1];  // running token count in item order
 };
 
-// Items of plan list `which` into tb; returns the count.  All threads call.
-__device__ int load_items(const LayerParams& p, const Plan* pl, int which, ItemTable& tb) {
+// Items of plan list `which` into tb at position `at` (list 1 from the host
+// pool when `from_pool`); returns the new item count.  All threads call.
+__device__ int load_items(const LayerParams& p, const Plan* pl, int which, ItemTable& tb, int at = 0,
+                          bool from_pool = false) {
   const int n = pl->n_items[which];
   for (int i = threadIdx.x; i < n; i += blockDim.x) {
     const int r = pl->items[which][i];
     if (r == pl->n_u) {
-      tb.rec[i] = p.shared_rec;
-      tb.ntok[i] = p.B;
-      tb.pair0[i] = -1;
+      tb.rec[at + i] = p.shared_rec;
+      tb.dst[at + i] = nullptr;
+      tb.ntok[at + i] = p.B;
+      tb.pair0[at + i] = -1;
     } else {
-      tb.rec[i] = p.slots + (int64_t)pl->u_slot[r] * p.S;
-      tb.pair0[i] = pl->u_off[r];
-      tb.ntok[i] = pl->u_off[r + 1] - pl->u_off[r];
+      uint8_t* slot = const_cast<uint8_t*>(p.slots) + (int64_t)pl->u_slot[r] * p.S;
+      tb.rec[at + i] = from_pool ? p.pool + (int64_t)pl->u_key[r] * p.S : slot;
+      tb.dst[at + i] = from_pool ? slot : nullptr;
+      tb.pair0[at + i] = pl->u_off[r];
+      tb.ntok[at + i] = pl->u_off[r + 1] - pl->u_off[r];
     }
   }
   __syncthreads();
   if (threadIdx.x == 0) {
-    int run = 0;
-    for (int i = 0; i < n; ++i) { tb.hbase[i] = run; run += tb.ntok[i]; }
-    tb.hbase[n] = run;
+    int run = at ? tb.hbase[at] : 0;
+    for (int i = at; i < at + n; ++i) { tb.hbase[i] = run; run += tb.ntok[i]; }
+    tb.hbase[at + n] = run;
   }
   __syncthreads();
-  return n;
+  return at + n;
+}
+
+// Device-driven fill of the W_down rows [n0, n0 + nrows) of item `it`: copy
+// them from the host pool into the item's slot (each CTA copies its own rows).
+template <int WD>
+__device__ void copy_down_rows(const LayerParams& p, const ItemTable& tb, int it, int n0, int nrows) {
+  const RecView src = rec_view<WD>(tb.rec[it], p.H, p.I);
+  const RecView dst = rec_view<WD>(tb.dst[it], p.H, p.I);
+  const int64_t rb = Fmt<WD>::row_bytes(p.I);
+  const int nv = (int)(nrows * rb / 16);
+  const uint4* s0 = reinterpret_cast<const uint4*>(src.down + (int64_t)n0 * rb);
+  uint4* d0 = reinterpret_cast<uint4*>(const_cast<uint8_t*>(dst.down) + (int64_t)n0 * rb);
+  for (int v = threadIdx.x; v < nv; v += blockDim.x) d0[v] = ld_ro16(s0 + v);
+  if (WD == MOE_FP4) {
+    const int ns = nrows * (p.I / 16) / 16;
+    const uint4* s1 = reinterpret_cast<const uint4*>(src.down_sc + (int64_t)n0 * (p.I / 16));
+    uint4* d1 = reinterpret_cast<uint4*>(const_cast<uint8_t*>(dst.down_sc) + (int64_t)n0 * (p.I / 16));
+    for (int v = threadIdx.x; v < ns; v += blockDim.x) d1[v] = ld_ro16(s1 + v);
+  }
 }
 
 // token, h row and rank slot of the q-th token of item `it`
@@ -78,7 +103,8 @@ __device__ __forceinline__ void item_token(const LayerParams& p, const Plan* pl,
 }
 
 // Gate/up rows of items [ib, ie), spread over CTAs [cta0, cta0 + ncta).
-template <int WD, int MAXT, bool FRESH, typename XT>
+// WB: the rows are read from the host pool and also written to the slot.
+template <int WD, int MAXT, bool FRESH, bool WB = false, typename XT>
 __device__ void phase1(const LayerParams& p, const Plan* pl, const ItemTable& tb, int ib, int ie, int cta0, int ncta,
                        const XT* xs) {
   using F = Fmt<WD>;
@@ -122,6 +148,21 @@ __device__ void phase1(const LayerParams& p, const Plan* pl, const ItemTable& tb
             su[u] = ld_w2<FRESH>(usc + 2 * c);
           } else {
             sg[u] = su[u] = 0;
+          }
+        }
+      }
+      if constexpr (WB) {
+        const RecView dv = rec_view<WD>(tb.dst[it], H, I);
+#pragma unroll
+        for (int u = 0; u < UNR; ++u) {
+          const int c = c0 + lane + 32 * u;
+          if (c < nchunks) {
+            *reinterpret_cast<uint4*>(const_cast<uint8_t*>(dv.gate) + (int64_t)i * rb + (int64_t)c * 16) = wg[u];
+            *reinterpret_cast<uint4*>(const_cast<uint8_t*>(dv.up) + (int64_t)i * rb + (int64_t)c * 16) = wu[u];
+            if (WD == MOE_FP4) {
+              *reinterpret_cast<unsigned short*>(const_cast<uint8_t*>(dv.gate_sc) + (int64_t)i * (H / 16) + 2 * c) = sg[u];
+              *reinterpret_cast<unsigned short*>(const_cast<uint8_t*>(dv.up_sc) + (int64_t)i * (H / 16) + 2 * c) = su[u];
+            }
           }
         }
       }
@@ -310,6 +351,13 @@ __global__ void __launch_bounds__(kThreads, 1) layer_kernel(LayerParams p) {
 
   // ---- 1. gate/up rows of the resident routed experts --------------------------
   const int n_res = load_items(p, pl, 0, tb);
+  if (p.device_fill && pl->n_items[1] > 0) {
+    // device-driven fills: pull each missed record from the host pool, use it
+    // for this call and store it in its slot; W_down rows by the CTA that owns them
+    const int n_all = load_items(p, pl, 1, tb, n_res, true);
+    for (int it = n_res; it < n_all; ++it) copy_down_rows<WD>(p, tb, it, n0, nrows);
+    if (!ctrl) phase1<WD, MAXT, false, true>(p, pl, tb, n_res, n_all, 1, G - 1, xs);
+  }
   if (threadIdx.x < n_res && nrows > 0) {  // this CTA's W_down rows of every resident expert -> L2
     const RecView v = rec_view<WD>(tb.rec[threadIdx.x], H, p.I);
     const int64_t rb = Fmt<WD>::row_bytes(p.I);
@@ -330,7 +378,10 @@ __global__ void __launch_bounds__(kThreads, 1) layer_kernel(LayerParams p) {
   // ---- 3. fills, each as soon as its copy has landed -------------------------------
   const int nf = pl->n_items[1];
   int fill_err = 0;
-  if (nf > 0) {
+  if (nf > 0 && p.device_fill) {
+    // device-driven fills were pulled from the pool in phase 1 (see below)
+    phase2<WD, MAXT, true>(p, pl, tb, n_res, n_res + nf, n0, nrows, hs, os);
+  } else if (nf > 0) {
     load_items(p, pl, 1, tb);
     for (int f = 0; f < nf && !fill_err; ++f) {
       if (wait_flag(&p.fill_flags[f], p.seq, p.err) != 0) {

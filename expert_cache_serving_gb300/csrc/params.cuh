@@ -20,6 +20,8 @@ struct LayerParams {
   unsigned long long bar_base;
   int* err;
   int has_shared;
+  int device_fill;            // 1: the kernel pulls each fill from the pool itself
+  const uint8_t* pool;        // device-visible address of the pinned host pool (device_fill)
   const uint8_t* slots;       // slot s at slots + s * S
   int64_t S;
   const uint8_t* shared_rec;  // shared expert record of this layer (or null)

@@ -16,6 +16,7 @@ _LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib", "li
 MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_OOM, MOE_ERR_CAPACITY, MOE_ERR_BUSY, MOE_ERR_CUDA, MOE_ERR_TIMEOUT = range(7)
 MOE_FP32, MOE_BF16, MOE_FP4 = 0, 1, 2
 MOE_EV_HIT, MOE_EV_MISS, MOE_EV_RESIZE_EVICT = 0, 1, 2
+MOE_FILL_COPY, MOE_FILL_DEVICE = 0, 1
 STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_OOM", 3: "MOE_ERR_CAPACITY",
                 4: "MOE_ERR_BUSY", 5: "MOE_ERR_CUDA", 6: "MOE_ERR_TIMEOUT"}
 
@@ -82,6 +83,7 @@ SIGNATURES = {
     "moe_cache_trace": (_I32, [_P, ctypes.POINTER(moe_event), _I64, ctypes.POINTER(_I64)]),
     "moe_cache_state": (_I32, [_P, _P, _P, _I64, ctypes.POINTER(_I64), ctypes.POINTER(ctypes.c_uint64)]),
     "moe_cache_slot_ptr": (_P, [_P, _I64]),
+    "moe_cache_set_fill_mode": (_I32, [_P, _I32]),
     "moe_cache_inject_fill_failure": (_I32, [_P, _I32]),
     "moe_cache_destroy": (_I32, [_P]),
     "moe_last_error": (ctypes.c_char_p, []),
@@ -211,6 +213,10 @@ def moe_cache_state(cache: int, cap: int):
 
 def moe_cache_slot_ptr(cache: int, s: int) -> int | None:
     return lib.moe_cache_slot_ptr(cache, s)
+
+
+def moe_cache_set_fill_mode(cache: int, mode: int) -> None:
+    check(lib.moe_cache_set_fill_mode(cache, mode), "moe_cache_set_fill_mode")
 
 
 def moe_cache_inject_fill_failure(cache: int, after: int) -> None:

@@ -234,6 +234,20 @@ moe_status moe_cache_state(moe_cache_t cache, int32_t* owner, uint64_t* stamp, i
 /* Device address of slot s (for inspection); NULL if s is out of range. */
 const void* moe_cache_slot_ptr(moe_cache_t cache, int64_t s);
 
+/* How misses are filled.
+ * MOE_FILL_COPY (default): the host issues cudaMemcpyAsync of each missed
+ *   record from the pinned pool into its victim slot on the copy stream, and
+ *   the layer kernel consumes each half as its stream-written flag arrives.
+ * MOE_FILL_DEVICE: the layer kernel reads each missed record from the pinned
+ *   pool itself (the pool must be mapped at the same device address, as on
+ *   unified-addressing systems), uses it for the call and stores it in its
+ *   victim slot: the fused, fixed-shape, device-driven transfer of the
+ *   "CUDA Graph-compatible LRU cache" section, with no host step on the fill
+ *   path.  Results are identical in both modes.
+ * Errors: MOE_ERR_INVALID_ARG (unknown mode, pool not mapped). */
+enum { MOE_FILL_COPY = 0, MOE_FILL_DEVICE = 1 };
+moe_status moe_cache_set_fill_mode(moe_cache_t cache, int32_t mode);
+
 /* Test hook: the next fill copies of this cache fail after `after` successful
  * copies (-1 disables).  Used to check the rollback path without a GPU fault. */
 moe_status moe_cache_inject_fill_failure(moe_cache_t cache, int32_t after);

@@ -93,7 +93,7 @@ def run_oracle(w: Workload, calls, logits=None, router_w=None, C=None, y_for=Non
 
 
 def run_gpu(w: Workload, calls, logits=None, router_w=None, C=None, max_slots=0, resize=None, keep_y=True,
-            pool=None, shared=None, inject=None):
+            pool=None, shared=None, inject=None, fill_mode=0):
     """GPU side through the C ABI; returns (RunOut, final cache state, stats).
     inject: {call index: number of fills that succeed before the injected failure}."""
     import torch
@@ -106,6 +106,7 @@ def run_gpu(w: Workload, calls, logits=None, router_w=None, C=None, max_slots=0,
     shared = runner.build_shared(w) if shared is None else shared
     cache = runner.Cache(w, pool, shared, C=C, max_slots=max_slots)
     mc.moe_cache_set_trace(cache.handle, True)
+    mc.moe_cache_set_fill_mode(cache.handle, fill_mode)
     B, k, E, H = w.B, w.k, w.E, w.H
     xdt = runner.x_dtype(w)
     ids = torch.empty((B, k), dtype=torch.int32, device=dev)

@@ -202,3 +202,71 @@ def test_resize_schedule_parity_and_output_identity():
     # the host pool is never written
     fresh = runner.build_pool(w)
     assert torch.equal(pool, fresh)
+
+
+# ---- device-driven fills (the layer kernel pulls misses from the pool) ------
+
+@pytest.mark.parametrize("B", [1, 3])
+def test_device_fill_bf16_parity(B):
+    w = configs.SMALL_BF16.with_(B=B, C=40 if B == 1 else 80)
+    calls = H.decode_calls(w)
+    lg = H.trace_logits(w)
+    ref = H.run_oracle(w, calls, logits=lg)
+    gpu, _, stats = H.run_gpu(w, calls, logits=lg, fill_mode=1)
+    compare(gpu, ref)
+    assert stats["misses"] > 0
+
+
+@pytest.mark.parametrize("B,C", [(1, 11), (8, 30)])
+def test_device_fill_fp4_parity(B, C):
+    w = configs.SMALL_FP4_NARROW.with_(B=B, C=C)
+    calls = H.decode_calls(w)
+    lg = H.trace_logits(w)
+    ref = H.run_oracle(w, calls, logits=lg)
+    gpu, _, _ = H.run_gpu(w, calls, logits=lg, fill_mode=1)
+    compare(gpu, ref)
+
+
+def test_fill_modes_bitwise_identical_and_slots_hold_records():
+    from expert_cache_serving_gb300 import moecache as mc
+    from expert_cache_serving_gb300 import runner
+
+    w = configs.SMALL_FP4.with_(steps=6)
+    calls = H.decode_calls(w)
+    lg = H.trace_logits(w)
+    pool, shared = runner.build_pool(w), runner.build_shared(w)
+    a, sa, _ = H.run_gpu(w, calls, logits=lg, pool=pool, shared=shared, fill_mode=0)
+    b, sb, _ = H.run_gpu(w, calls, logits=lg, pool=pool, shared=shared, fill_mode=1)
+    for ca, cb in zip(a.calls, b.calls):
+        assert (ca.y == cb.y).all()
+    assert [tuple(e) for e in a.events] == [tuple(e) for e in b.events]
+    # after a device-driven run every occupied slot holds its expert's record byte for byte
+    cache = runner.Cache(w, pool, shared)
+    mc.moe_cache_set_fill_mode(cache.handle, 1)
+    dev = torch.device("cuda")
+    y = torch.empty((w.B, w.H), dtype=torch.bfloat16, device=dev)
+    for (s, l) in calls:
+        assert cache.forward(l, runner.activations(w, s, l).to(dev), torch.from_numpy(lg[s, l]).to(dev), y, w.B) == 0
+    torch.cuda.synchronize()
+    owner, _, n, _ = mc.moe_cache_state(cache.handle, w.C)
+    S = synth.record_bytes(w.H, w.I, w.wdtype)
+    class SlotView:  # zero-copy device view of one slot
+        def __init__(self, ptr):
+            self.__cuda_array_interface__ = {"shape": (S,), "typestr": "|u1", "data": (ptr, False), "version": 3}
+
+    for slot, key in enumerate(owner):
+        if key < 0:
+            continue
+        got = torch.as_tensor(SlotView(mc.moe_cache_slot_ptr(cache.handle, slot)), device=dev)
+        assert torch.equal(got.cpu(), pool[key]), f"slot {slot} does not hold record {key}"
+    cache.close()
+
+
+def test_device_fill_with_resize():
+    w = configs.SMALL_BF16.with_(B=2, C=40, steps=12)
+    calls = H.decode_calls(w)
+    lg = H.trace_logits(w)
+    resize = {10: 19, 20: 60}
+    ref = H.run_oracle(w, calls, logits=lg, resize=resize, y_for=set())
+    gpu, _, _ = H.run_gpu(w, calls, logits=lg, max_slots=w.LE, resize=resize, fill_mode=1)
+    compare(gpu, ref, check_y=False)
