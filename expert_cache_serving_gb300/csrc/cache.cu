@@ -38,6 +38,8 @@ static moe_status fail(moe_status st, const char* fmt, ...) {
   return st;
 }
 
+void moe::set_last_error(const char* msg) { g_err = msg; }
+
 #define CU_TRY(expr)                                                                      \
   do {                                                                                    \
     cudaError_t _e = (expr);                                                              \

@@ -50,5 +50,6 @@ size_t layer_static_smem(int wdtype);
 cudaError_t launch_layer(int wdtype, const LayerParams& p, int grid, size_t smem, cudaStream_t s);
 int layer_max_grid(int wdtype, size_t smem);
 cudaError_t launch_slot_moves(uint8_t* base, int64_t S, const int32_t* moves, int n_moves, cudaStream_t s);
+void set_last_error(const char* msg);  // message returned by moe_last_error() on this thread
 
 }  // namespace moe

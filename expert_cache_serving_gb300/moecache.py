@@ -85,6 +85,7 @@ SIGNATURES = {
     "moe_cache_slot_ptr": (_P, [_P, _I64]),
     "moe_cache_set_fill_mode": (_I32, [_P, _I32]),
     "moe_cache_inject_fill_failure": (_I32, [_P, _I32]),
+    "moe_layer_forward_resident_noalloc": (_I32, [ctypes.POINTER(moe_model_desc), _P, _P, _P, _P, _I32, _P, _P]),
     "moe_cache_destroy": (_I32, [_P]),
     "moe_last_error": (ctypes.c_char_p, []),
     "moe_version": (_I32, []),
@@ -221,6 +222,13 @@ def moe_cache_set_fill_mode(cache: int, mode: int) -> None:
 
 def moe_cache_inject_fill_failure(cache: int, after: int) -> None:
     check(lib.moe_cache_inject_fill_failure(cache, after), "moe_cache_inject_fill_failure")
+
+
+def moe_layer_forward_resident_noalloc(desc: moe_model_desc, bank, shared_rec, x, logits, B: int, y,
+                                       stream=None) -> int:
+    """Layer over a caller-owned bank of resident experts; allocates nothing (see include/moecache.h)."""
+    return lib.moe_layer_forward_resident_noalloc(ctypes.byref(desc), _ptr(bank), _ptr(shared_rec), _ptr(x),
+                                                  _ptr(logits), B, _ptr(y), _stream(stream))
 
 
 def moe_cache_destroy(cache: int) -> None:

@@ -252,6 +252,28 @@ moe_status moe_cache_set_fill_mode(moe_cache_t cache, int32_t mode);
  * copies (-1 disables).  Used to check the rollback path without a GPU fault. */
 moe_status moe_cache_inject_fill_failure(moe_cache_t cache, int32_t after);
 
+/* Routed MoE layer for callers that cannot allocate device memory (their
+ * device memory is owned by another allocator or a fixed budget, or a
+ * synchronising cudaMalloc/cudaFree is not acceptable on their path).  The
+ * pages have no counterpart: it is the same layer as moe_layer_forward with
+ * every expert resident, without a cache.
+ * desc: E, k, H, I, wdtype, has_shared are used (L, max_tokens ignored).
+ * bank: device, the E expert records of the layer back to back (record
+ *   layout as above); shared_rec: device record of the shared expert, required
+ *   iff desc->has_shared.  x: device [B][H], logits: device float32 [B][E],
+ *   y: device [B][H] written; 1 <= B <= 16.  All owned by the caller.
+ * Scratch: a 4 MiB + 16 KiB array inside the library, held by every GPU that
+ *   loads it until the process exits; (B*k + B) * I * 4 bytes must fit in
+ *   4 MiB, otherwise MOE_ERR_INVALID_ARG.  The first call on a device looks the
+ *   array's device address up (cudaGetSymbolAddress) and should come before
+ *   any stream capture.  Nothing in the scratch needs to start at zero; every
+ *   call overwrites it, so calls that overlap on the GPU (different streams,
+ *   different threads) race and must be serialised by the caller.
+ * Never calls cudaMalloc, cudaFree or any allocating routine.
+ * Errors: MOE_ERR_INVALID_ARG, MOE_ERR_CUDA (launch failure). */
+moe_status moe_layer_forward_resident_noalloc(const moe_model_desc* desc, const void* bank, const void* shared_rec,
+                                              const void* x, const float* logits, int32_t B, void* y, void* stream);
+
 /* Free everything the library allocated.  Synchronises. */
 moe_status moe_cache_destroy(moe_cache_t cache);
 
