@@ -58,6 +58,9 @@ struct Drv {
   CUresult (*memSetAccess)(CUdeviceptr, size_t, const CUmemAccessDesc*, size_t) = nullptr;
   CUresult (*memGetAllocationGranularity)(size_t*, const CUmemAllocationProp*, CUmemAllocationGranularity_flags) = nullptr;
   CUresult (*streamWriteValue32)(CUstream, CUdeviceptr, cuuint32_t, unsigned int) = nullptr;
+  CUresult (*tensorMapEncodeTiled)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill) = nullptr;
   bool ok = false;
 };
 
@@ -82,7 +85,8 @@ static Drv& drv() {
            get_entry("cuMemMap", &d.memMap) && get_entry("cuMemUnmap", &d.memUnmap) &&
            get_entry("cuMemSetAccess", &d.memSetAccess) &&
            get_entry("cuMemGetAllocationGranularity", &d.memGetAllocationGranularity) &&
-           get_entry("cuStreamWriteValue32", &d.streamWriteValue32);
+           get_entry("cuStreamWriteValue32", &d.streamWriteValue32) &&
+           get_entry("cuTensorMapEncodeTiled", &d.tensorMapEncodeTiled);
   }
   return d;
 }
@@ -217,6 +221,22 @@ struct moe_cache {
   std::vector<std::pair<int, int>> tl_calls;  // (ring row, had fills) not yet read
   int tl_next = 0;
   moe_phase_times pt{};
+  // prefill scratch (allocated at the first moe_prefill_stream call, grown on demand)
+  struct Prefill {
+    int T_cap = 0;
+    int32_t *ids = nullptr, *cnt = nullptr, *base = nullptr, *offsets = nullptr, *pos = nullptr, *perm = nullptr;
+    float* w = nullptr;
+    void *xp = nullptr, *hp = nullptr;
+    float* op = nullptr;
+    uint8_t* wb = nullptr;  // bf16 staging of a layer's FP4 records (+ shared expert)
+    cudaEvent_t loaded[2] = {nullptr, nullptr}, consumed[2] = {nullptr, nullptr}, start = nullptr;
+    struct Timed {
+      cudaEvent_t a, b;
+      int kind;  // 0 whole call, 1 copy, 2 compute, 3 gemm
+      double flop;
+    };
+    std::vector<Timed> timed;
+  } pf;
 };
 
 static constexpr int kTlRing = 1024;
@@ -274,6 +294,15 @@ static void free_all(moe_cache* c) {
     cudaEventDestroy(t.b);
   }
   for (cudaEvent_t e : c->ev_pool) cudaEventDestroy(e);
+  for (void* p : {(void*)c->pf.ids, (void*)c->pf.cnt, (void*)c->pf.base, (void*)c->pf.offsets, (void*)c->pf.pos,
+                  (void*)c->pf.perm, (void*)c->pf.w, c->pf.xp, c->pf.hp, (void*)c->pf.op, (void*)c->pf.wb})
+    if (p) cudaFree(p);
+  for (cudaEvent_t e : {c->pf.loaded[0], c->pf.loaded[1], c->pf.consumed[0], c->pf.consumed[1], c->pf.start})
+    if (e) cudaEventDestroy(e);
+  for (auto& t : c->pf.timed) {
+    cudaEventDestroy(t.a);
+    cudaEventDestroy(t.b);
+  }
   if (c->own_copy && c->copy) cudaStreamDestroy(c->copy);
   c->slots.release();
   delete c;
@@ -780,9 +809,30 @@ extern "C" moe_status moe_cache_resize(moe_cache_t c, int64_t n_slots, void* str
 }
 
 // -------------------------------------------------------------- introspection --
+static void drain_prefill(moe_cache* c) {
+  for (auto& t : c->pf.timed) {
+    cudaEventSynchronize(t.b);
+    float ms = 0.f;
+    if (cudaEventElapsedTime(&ms, t.a, t.b) == cudaSuccess) {
+      if (t.kind == 0) c->st.prefill_ms += ms;
+      else if (t.kind == 1) c->st.prefill_copy_ms += ms;
+      else if (t.kind == 2) c->st.prefill_compute_ms += ms;
+      else {
+        c->st.prefill_gemm_ms += ms;
+        c->st.prefill_gemm_flop += t.flop;
+      }
+    }
+    cudaGetLastError();
+    c->ev_pool.push_back(t.a);
+    c->ev_pool.push_back(t.b);
+  }
+  c->pf.timed.clear();
+}
+
 extern "C" moe_status moe_cache_stats(moe_cache_t c, moe_stats* out) {
   if (!c || !out) return fail(MOE_ERR_INVALID_ARG, "NULL argument");
   drain_pending(c, true);
+  drain_prefill(c);
   *out = c->st;
   return MOE_OK;
 }
@@ -791,6 +841,7 @@ extern "C" moe_status moe_cache_reset_stats(moe_cache_t c) {
   if (!c) return fail(MOE_ERR_INVALID_ARG, "cache is NULL");
   drain_pending(c, true);
   drain_timeline(c);
+  drain_prefill(c);
   c->st = moe_stats{};
   c->pt = moe_phase_times{};
   return MOE_OK;
@@ -863,9 +914,184 @@ extern "C" moe_status moe_cache_inject_fill_failure(moe_cache_t c, int32_t after
   return MOE_OK;
 }
 
+// ---------------------------------------------------------------------- prefill --
+static moe_status encode_map(CUtensorMap* m, const void* base, int rank, const uint64_t* dims, const uint64_t* strides,
+                             const uint32_t* box) {
+  Drv& d = drv();
+  cuuint64_t gd[3], gs[2];
+  cuuint32_t bx[3], es[3] = {1, 1, 1};
+  for (int i = 0; i < rank; ++i) { gd[i] = dims[i]; bx[i] = box[i]; }
+  for (int i = 0; i + 1 < rank; ++i) gs[i] = strides[i];
+  const CUresult r = d.tensorMapEncodeTiled(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), gd, gs,
+                                            bx, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? MOE_OK : fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+}
+
+// [rows][K] bf16 activations, boxes of 128 rows x 64 elements
+static moe_status map_rows(CUtensorMap* m, const void* base, int64_t rows, int K) {
+  const uint64_t dims[2] = {(uint64_t)K, (uint64_t)rows}, strides[1] = {(uint64_t)K * 2};
+  const uint32_t box[2] = {64, 128};
+  return encode_map(m, base, 2, dims, strides, box);
+}
+
+// [n][rows][K] bf16 matrices n records apart, boxes of 128 rows x 64 elements
+static moe_status map_weights(CUtensorMap* m, const void* base, int n, int rows, int K, int64_t rec_stride) {
+  const uint64_t dims[3] = {(uint64_t)K, (uint64_t)rows, (uint64_t)n};
+  const uint64_t strides[2] = {(uint64_t)K * 2, (uint64_t)rec_stride};
+  const uint32_t box[3] = {64, 128, 1};
+  return encode_map(m, base, 3, dims, strides, box);
+}
+
+static moe_status prefill_scratch(moe_cache* c, int T) {
+  auto& pf = c->pf;
+  if (T <= pf.T_cap) return MOE_OK;
+  const moe_model_desc& d = c->d;
+  for (void* p : {(void*)pf.ids, (void*)pf.cnt, (void*)pf.base, (void*)pf.offsets, (void*)pf.pos, (void*)pf.perm,
+                  (void*)pf.w, pf.xp, pf.hp, (void*)pf.op})
+    if (p) cudaFree(p);
+  pf.T_cap = 0;
+  const int64_t n_pairs = (int64_t)T * d.k + (d.has_shared ? T : 0);
+  const int G = d.E + (d.has_shared ? 1 : 0);
+  const int64_t n_chunks = (n_pairs + 1023) / 1024;
+  auto al = [&](void** p, size_t bytes) { return cudaMalloc(p, bytes); };
+  if (al((void**)&pf.ids, sizeof(int32_t) * T * d.k) || al((void**)&pf.w, sizeof(float) * T * d.k) ||
+      al((void**)&pf.cnt, sizeof(int32_t) * n_chunks * G) || al((void**)&pf.base, sizeof(int32_t) * n_chunks * G) ||
+      al((void**)&pf.offsets, sizeof(int32_t) * (G + 1)) || al((void**)&pf.pos, sizeof(int32_t) * n_pairs) ||
+      al((void**)&pf.perm, sizeof(int32_t) * n_pairs) || al(&pf.xp, (size_t)n_pairs * d.H * 2) ||
+      al(&pf.hp, (size_t)n_pairs * d.I * 2) || al((void**)&pf.op, (size_t)n_pairs * d.H * 4)) {
+    cudaGetLastError();
+    return fail(MOE_ERR_OOM, "prefill scratch for T=%d does not fit", T);
+  }
+  if (d.wdtype == MOE_FP4 && !pf.wb) {
+    const size_t s16 = (size_t)6 * d.H * d.I;
+    if (cudaMalloc((void**)&pf.wb, s16 * (d.E + 1)) != cudaSuccess) {
+      cudaGetLastError();
+      return fail(MOE_ERR_OOM, "prefill bf16 staging of one layer does not fit");
+    }
+  }
+  for (int b = 0; b < 2; ++b) {
+    if (!pf.loaded[b]) CU_TRY(cudaEventCreateWithFlags(&pf.loaded[b], cudaEventDisableTiming));
+    if (!pf.consumed[b]) CU_TRY(cudaEventCreateWithFlags(&pf.consumed[b], cudaEventDisableTiming));
+  }
+  if (!pf.start) CU_TRY(cudaEventCreateWithFlags(&pf.start, cudaEventDisableTiming));
+  pf.T_cap = T;
+  return MOE_OK;
+}
+
 extern "C" moe_status moe_prefill_stream(moe_cache_t c, int32_t layer_begin, int32_t layer_end, const void* x,
                                          const float* logits, int32_t T, void* y, void* stream) {
-  (void)layer_begin; (void)layer_end; (void)x; (void)logits; (void)T; (void)y; (void)stream;
+  g_err.clear();
   if (!c) return fail(MOE_ERR_INVALID_ARG, "cache is NULL");
-  return fail(MOE_ERR_INVALID_ARG, "prefill path not available in this build");
+  const moe_model_desc& d = c->d;
+  if (d.wdtype != MOE_BF16 && d.wdtype != MOE_FP4) return fail(MOE_ERR_INVALID_ARG, "prefill needs a bf16 or FP4 model");
+  if (layer_begin < 0 || layer_end > d.L || layer_begin >= layer_end)
+    return fail(MOE_ERR_INVALID_ARG, "layer range [%d, %d) invalid", layer_begin, layer_end);
+  if (T < 1 || (int64_t)T * d.k > (int64_t)1 << 30) return fail(MOE_ERR_INVALID_ARG, "T=%d invalid", T);
+  if (!x || !logits || !y) return fail(MOE_ERR_INVALID_ARG, "x, logits and y must be device pointers");
+  if (d.I % 128 || d.H % 256) return fail(MOE_ERR_INVALID_ARG, "prefill needs I % 128 == 0 and H % 256 == 0");
+  const int64_t E = d.E;
+  if (c->C < 2 * E)
+    return fail(MOE_ERR_CAPACITY, "prefill needs two full-layer buffers (%lld slots), the cache has %lld",
+                (long long)(2 * E), (long long)c->C);
+  cudaStream_t s = (cudaStream_t)stream;
+  if (*(volatile int*)c->h_err != 0) return recover_after_timeout(c, s);
+  if (moe_status st = prefill_scratch(c, T)) return st;
+  auto& pf = c->pf;
+  if (c->have_done && s != c->last_stream) CU_TRY(cudaStreamWaitEvent(s, c->e_done, 0));
+  c->last_stream = s;
+
+  const int H = d.H, I = d.I, k = d.k, sh = d.has_shared;
+  const int Tk = T * k, n_pairs = Tk + (sh ? T : 0);
+  const int64_t S = c->S, s16 = (int64_t)6 * H * I;
+  const int64_t buf0 = c->C - 2 * E;  // buffers: slots [C-2E, C-E) and [C-E, C)
+  uint8_t* slots = (uint8_t*)c->slots.base;
+  const CacheDev st{c->d_map, c->d_owner, c->d_stamp, c->d_g};
+
+  // the buffer slots stop holding decode experts
+  CU_TRY(prefill_evict_range(st, buf0, c->C, c->d_oldest_n, s));
+  CU_TRY(cudaEventRecord(pf.start, s));
+  CU_TRY(cudaStreamWaitEvent(c->copy, pf.start, 0));
+
+  CUtensorMap map_xp, map_hp, map_gu, map_dn, map_sgu, map_sdn;
+  if (moe_status e = map_rows(&map_xp, pf.xp, n_pairs, H)) return e;
+  if (moe_status e = map_rows(&map_hp, pf.hp, n_pairs, I)) return e;
+  if (d.wdtype == MOE_FP4) {
+    if (moe_status e = map_weights(&map_gu, pf.wb, (int)E, 2 * I, H, s16)) return e;
+    if (moe_status e = map_weights(&map_dn, pf.wb + (int64_t)4 * H * I, (int)E, H, I, s16)) return e;
+    if (sh) {
+      if (moe_status e = map_weights(&map_sgu, pf.wb + E * s16, 1, 2 * I, H, s16)) return e;
+      if (moe_status e = map_weights(&map_sdn, pf.wb + E * s16 + (int64_t)4 * H * I, 1, H, I, s16)) return e;
+    }
+  }
+  auto timed = [&](cudaStream_t on, int kind, double flop) -> std::pair<cudaEvent_t, cudaEvent_t> {
+    if (!c->profiling) return {nullptr, nullptr};
+    cudaEvent_t a = take_event(c), b = take_event(c);
+    cudaEventRecord(a, on);
+    pf.timed.push_back({a, b, kind, flop});
+    return {a, b};
+  };
+  auto done = [&](std::pair<cudaEvent_t, cudaEvent_t> ev, cudaStream_t on) {
+    if (ev.second) cudaEventRecord(ev.second, on);
+  };
+  const auto whole = timed(s, 0, 0.0);
+  const double gemm_flop = 2.0 * n_pairs * (2.0 * I * H) + 2.0 * n_pairs * ((double)H * I);
+
+  for (int li = 0; li < layer_end - layer_begin; ++li) {
+    const int l = layer_begin + li, b = li & 1;
+    uint8_t* buf = slots + (buf0 + b * E) * S;
+    // stream layer l's experts into buffer b once layer l-2 released it
+    if (li >= 2) CU_TRY(cudaStreamWaitEvent(c->copy, pf.consumed[b], 0));
+    const auto cp = timed(c->copy, 1, 0.0);
+    CU_TRY(cudaMemcpyAsync(buf, c->host_pool + (int64_t)l * E * S, E * S, cudaMemcpyHostToDevice, c->copy));
+    done(cp, c->copy);
+    CU_TRY(cudaEventRecord(pf.loaded[b], c->copy));
+
+    // routing, grouping and gather need no weights: they run while the copy lands
+    const float* lg = logits + (int64_t)li * T * E;
+    const uint8_t* xl = (const uint8_t*)x + (int64_t)li * T * H * 2;
+    uint8_t* yl = (uint8_t*)y + (int64_t)li * T * H * 2;
+    CU_TRY(prefill_route(lg, T, (int)E, k, pf.ids, pf.w, s));
+    CU_TRY(prefill_group(pf.ids, T, k, (int)E, sh, pf.cnt, pf.base, pf.offsets, pf.pos, pf.perm, s));
+    CU_TRY(prefill_gather(xl, T, k, H, n_pairs, pf.perm, pf.xp, s));
+    CU_TRY(cudaStreamWaitEvent(s, pf.loaded[b], 0));
+    const auto comp = timed(s, 2, 0.0);
+    const CUtensorMap* gu = &map_gu;
+    const CUtensorMap* dn = &map_dn;
+    CUtensorMap bgu, bdn, bsgu, bsdn;
+    if (d.wdtype == MOE_FP4) {
+      CU_TRY(prefill_dequant(buf, S, pf.wb, s16, (int)E, H, I, s));
+      if (sh) CU_TRY(prefill_dequant(c->shared_dev + (int64_t)l * S, S, pf.wb + E * s16, s16, 1, H, I, s));
+      CU_TRY(cudaEventRecord(pf.consumed[b], s));  // the GEMMs read the staging copy
+    } else {
+      if (moe_status e = map_weights(&bgu, buf, (int)E, 2 * I, H, S)) return e;
+      if (moe_status e = map_weights(&bdn, buf + (int64_t)4 * H * I, (int)E, H, I, S)) return e;
+      gu = &bgu;
+      dn = &bdn;
+      if (sh) {
+        const uint8_t* srec = c->shared_dev + (int64_t)l * S;
+        if (moe_status e = map_weights(&bsgu, srec, 1, 2 * I, H, S)) return e;
+        if (moe_status e = map_weights(&bsdn, srec + (int64_t)4 * H * I, 1, H, I, S)) return e;
+      }
+    }
+    const CUtensorMap* sgu = d.wdtype == MOE_FP4 ? &map_sgu : &bsgu;
+    const CUtensorMap* sdn = d.wdtype == MOE_FP4 ? &map_sdn : &bsdn;
+    const auto gm = timed(s, 3, gemm_flop);
+    CU_TRY(prefill_gemm_gate_up(map_xp, *gu, pf.offsets, (int)E, n_pairs, H, I, pf.hp, c->d_err, s));
+    if (sh) CU_TRY(prefill_gemm_gate_up(map_xp, *sgu, pf.offsets + E, 1, n_pairs, H, I, pf.hp, c->d_err, s));
+    CU_TRY(prefill_gemm_down(map_hp, *dn, pf.offsets, (int)E, n_pairs, H, I, pf.op, c->d_err, s));
+    if (sh) CU_TRY(prefill_gemm_down(map_hp, *sdn, pf.offsets + E, 1, n_pairs, H, I, pf.op, c->d_err, s));
+    done(gm, s);
+    if (d.wdtype != MOE_FP4) CU_TRY(cudaEventRecord(pf.consumed[b], s));
+    CU_TRY(prefill_combine(pf.op, pf.pos, pf.w, T, k, H, sh, yl, s));
+    done(comp, s);
+  }
+  done(whole, s);
+  // later calls must not start before the copies finished with the buffers
+  CU_TRY(cudaStreamWaitEvent(s, pf.loaded[(layer_end - layer_begin - 1) & 1], 0));
+  CU_TRY(cudaEventRecord(c->e_done, s));
+  c->have_done = true;
+  c->st.prefill_layers += layer_end - layer_begin;
+  c->st.prefill_tokens += (int64_t)T * (layer_end - layer_begin);
+  return MOE_OK;
 }

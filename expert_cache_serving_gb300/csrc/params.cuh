@@ -1,5 +1,7 @@
 // Kernel parameter blocks and launch entry points shared by the host code.
 #pragma once
+#include <cuda.h>
+
 #include "common.cuh"
 
 namespace moe {
@@ -51,5 +53,21 @@ cudaError_t launch_layer(int wdtype, const LayerParams& p, int grid, size_t smem
 int layer_max_grid(int wdtype, size_t smem);
 cudaError_t launch_slot_moves(uint8_t* base, int64_t S, const int32_t* moves, int n_moves, cudaStream_t s);
 void set_last_error(const char* msg);  // message returned by moe_last_error() on this thread
+
+// prefill (prefill.cu)
+cudaError_t prefill_route(const float* logits, int T, int E, int k, int32_t* ids, float* w, cudaStream_t s);
+cudaError_t prefill_group(const int32_t* ids, int T, int k, int E, int has_shared, int32_t* cnt, int32_t* base,
+                          int32_t* offsets, int32_t* pos, int32_t* perm, cudaStream_t s);
+cudaError_t prefill_gather(const void* x, int T, int k, int H, int n_pairs, const int32_t* perm, void* xp,
+                           cudaStream_t s);
+cudaError_t prefill_dequant(const uint8_t* src, int64_t S4, uint8_t* dst, int64_t S16, int n_rec, int H, int I,
+                            cudaStream_t s);
+cudaError_t prefill_gemm_gate_up(const CUtensorMap& a, const CUtensorMap& b, const int32_t* offsets, int n_groups,
+                                 int n_rows, int H, int I, void* hp, int* err, cudaStream_t s);
+cudaError_t prefill_gemm_down(const CUtensorMap& a, const CUtensorMap& b, const int32_t* offsets, int n_groups,
+                              int n_rows, int H, int I, float* op, int* err, cudaStream_t s);
+cudaError_t prefill_combine(const float* op, const int32_t* pos, const float* w, int T, int k, int H, int has_shared,
+                            void* y, cudaStream_t s);
+cudaError_t prefill_evict_range(const CacheDev& st, int64_t s0, int64_t s1, int* oldest_n, cudaStream_t s);
 
 }  // namespace moe

@@ -1,0 +1,318 @@
+// Prefill-size routed-MoE layer: routing of T tokens, stable grouping of the
+// (token, rank) pairs by expert, gather of the activations per expert, FP4 ->
+// bf16 staging of the layer's experts, the two grouped GEMMs on tcgen05/TMEM
+// (gate/up with the SwiGLU epilogue, then down) and the weighted combine.
+//
+// FreeToken write-up, "전층 이중 버퍼링": prefill activates almost every expert
+// of a layer, so the layer's full expert set is streamed into one of two
+// full-layer buffers carved from the slot pool while the previous layer
+// computes on the other; the host-side orchestration is in cache.cu.
+#include "expert_math.cuh"
+#include "params.cuh"
+#include "tc_gemm.cuh"
+
+namespace moe {
+namespace pf {
+
+// ---- 1. routing: one warp per token, same rule as the decode control step ----
+__global__ void route_kernel(const float* __restrict__ logits, int T, int E, int k, int32_t* __restrict__ ids,
+                             float* __restrict__ w) {
+  const int lane = threadIdx.x & 31;
+  const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  if (t >= T) return;
+  const float* lg = logits + (size_t)t * E;
+  float v[kMaxE / 32];
+#pragma unroll
+  for (int q = 0; q < kMaxE / 32; ++q) {
+    const int e = lane + 32 * q;
+    float x = -INFINITY;
+    if (e < E) {
+      x = lg[e];
+      if (x != x) x = -INFINITY;
+    }
+    v[q] = x;
+  }
+  unsigned taken = 0u;
+  float m0 = 0.f, sum = 0.f, mine = 0.f;
+  int my_id = 0;
+  for (int r = 0; r < k; ++r) {
+    float bv = -INFINITY;
+    int bi = 0x7FFFFFFF;
+#pragma unroll
+    for (int q = 0; q < kMaxE / 32; ++q) {
+      const int e = lane + 32 * q;
+      if (e < E && !(taken & (1u << q)) && (v[q] > bv || (v[q] == bv && e < bi))) { bv = v[q]; bi = e; }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xFFFFFFFFu, bv, o);
+      const int oi = __shfl_xor_sync(0xFFFFFFFFu, bi, o);
+      if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
+    }
+    if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+    if (r == 0) m0 = bv;
+    const float ex = expf(bv - m0);
+    sum += ex;
+    if (lane == r) { my_id = bi; mine = ex; }
+  }
+  if (lane < k) {
+    ids[(size_t)t * k + lane] = my_id;
+    w[(size_t)t * k + lane] = mine / sum;
+  }
+}
+
+// Group of flat pair p: routed pairs t*k+j -> their expert; with a shared
+// expert, pairs T*k + t form group E.
+__device__ __forceinline__ int pair_group(const int32_t* ids, int Tk, int E, int p) { return p < Tk ? ids[p] : E; }
+
+// ---- 2. stable counting sort of the pairs by group ---------------------------------
+// chunk c = pairs [c*1024, (c+1)*1024): per-chunk histogram
+__global__ void __launch_bounds__(1024) group_count_kernel(const int32_t* ids, int Tk, int n_pairs, int E, int G,
+                                                           int32_t* cnt) {
+  extern __shared__ int32_t h[];
+  for (int g = threadIdx.x; g < G; g += blockDim.x) h[g] = 0;
+  __syncthreads();
+  const int p = blockIdx.x * 1024 + threadIdx.x;
+  if (p < n_pairs) atomicAdd(&h[pair_group(ids, Tk, E, p)], 1);
+  __syncthreads();
+  for (int g = threadIdx.x; g < G; g += blockDim.x) cnt[(size_t)blockIdx.x * G + g] = h[g];
+}
+
+// one block: base[c][g] = start of chunk c's pairs of group g; offsets[g] = group starts
+__global__ void __launch_bounds__(1024) group_scan_kernel(const int32_t* cnt, int n_chunks, int G, int32_t* base,
+                                                          int32_t* offsets) {
+  __shared__ int scratch[33];
+  __shared__ int s_run;
+  if (threadIdx.x == 0) s_run = 0;
+  __syncthreads();
+  const int total = G * n_chunks;  // group-major, chunk-minor
+  for (int i0 = 0; i0 < total; i0 += blockDim.x) {
+    const int i = i0 + threadIdx.x;
+    const int g = i / n_chunks, c = i % n_chunks;
+    const int v = i < total ? cnt[(size_t)c * G + g] : 0;
+    int tot;
+    const int ex = block_excl_scan(v, scratch, &tot);
+    const int run = s_run;
+    if (i < total) {
+      base[(size_t)c * G + g] = run + ex;
+      if (c == 0) offsets[g] = run + ex;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) s_run = run + tot;
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) offsets[G] = s_run;
+}
+
+// place the chunk's pairs in order: warps one after the other, ranks within a
+// warp from the peer mask of equal groups
+__global__ void __launch_bounds__(1024) group_place_kernel(const int32_t* ids, int Tk, int n_pairs, int E, int G,
+                                                           const int32_t* base, int32_t* pos, int32_t* perm) {
+  extern __shared__ int32_t run[];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (int g = threadIdx.x; g < G; g += blockDim.x) run[g] = base[(size_t)blockIdx.x * G + g];
+  __syncthreads();
+  const int p = blockIdx.x * 1024 + threadIdx.x;
+  const bool valid = p < n_pairs;
+  const int g = valid ? pair_group(ids, Tk, E, p) : -1 - lane;  // invalid lanes never match
+  const unsigned peers = __match_any_sync(0xFFFFFFFFu, g);
+  const int rank = __popc(peers & ((1u << lane) - 1u));
+  const bool leader = rank == 0;
+  for (int w = 0; w < 32; ++w) {
+    if (warp == w && valid) {
+      const int at = run[g] + rank;
+      pos[p] = at;
+      perm[at] = p;
+      __syncwarp(peers);
+      if (leader) run[g] += __popc(peers);
+    }
+    __syncthreads();
+  }
+}
+
+// ---- 3. gather of the activations in group order -------------------------------------
+__global__ void gather_kernel(const __nv_bfloat16* __restrict__ x, int Tk, int k, int H, int n_pairs,
+                              const int32_t* __restrict__ perm, __nv_bfloat16* __restrict__ xp) {
+  const int per = H / 8;  // 16-byte vectors per row
+  const int64_t total = (int64_t)n_pairs * per;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+    const int row = (int)(i / per), v = (int)(i % per);
+    const int p = perm[row];
+    const int t = p < Tk ? p / k : p - Tk;
+    reinterpret_cast<uint4*>(xp + (int64_t)row * H)[v] = reinterpret_cast<const uint4*>(x + (int64_t)t * H)[v];
+  }
+}
+
+// ---- 4. FP4 -> bf16 staging of expert records (exact) ----------------------------------
+// one thread per 16-element block of one matrix row
+__global__ void dequant_kernel(const uint8_t* __restrict__ src, int64_t S4, uint8_t* __restrict__ dst, int64_t S16,
+                               int n_rec, int H, int I) {
+  const int64_t HI = (int64_t)H * I;
+  const int64_t blocks_per_rec = 3 * HI / 16;
+  const int64_t total = blocks_per_rec * n_rec;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t rec = i / blocks_per_rec, b = i % blocks_per_rec;
+    const int mat = (int)(b / (HI / 16));
+    const int64_t bb = b % (HI / 16);  // block within the matrix (row-major, 16 elements per block)
+    const uint8_t* r4 = src + rec * S4;
+    const uint8_t* codes = mat == 0 ? r4 : mat == 1 ? r4 + HI / 2 : r4 + HI + HI / 8;
+    const uint8_t* scales = mat == 0 ? r4 + HI : mat == 1 ? r4 + HI + HI / 16 : r4 + HI + HI / 8 + HI / 2;
+    const uint2 c = *reinterpret_cast<const uint2*>(codes + bb * 8);
+    const float2 s2 = e4m3x2_to_float2((unsigned short)scales[bb]);
+    const float s = s2.x;
+    uint32_t out[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const uint32_t byte = ((q < 4 ? c.x : c.y) >> (8 * (q & 3))) & 0xFFu;
+      const float2 f = e2m1x2_to_float2(byte);
+      __nv_bfloat162 b2 = __floats2bfloat162_rn(f.x * s, f.y * s);
+      out[q] = *reinterpret_cast<uint32_t*>(&b2);
+    }
+    uint4* d = reinterpret_cast<uint4*>(dst + rec * S16 + (int64_t)mat * HI * 2 + bb * 32);
+    d[0] = make_uint4(out[0], out[1], out[2], out[3]);
+    d[1] = make_uint4(out[4], out[5], out[6], out[7]);
+  }
+}
+
+// ---- 5/6. grouped GEMMs ----------------------------------------------------------------------
+struct BRowGateUp {
+  int I;
+  __device__ int operator()(int nb, int half) const { return half ? I + nb * 128 : nb * 128; }
+};
+struct BRowDown {
+  __device__ int operator()(int nb, int half) const { return nb * 256 + half * 128; }
+};
+
+__global__ void __launch_bounds__(tc::kThreads, 1)
+    gemm_gate_up_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
+                        const int32_t* offsets, int n_groups, int H, int I, __nv_bfloat16* hp, int* err) {
+  tc::grouped_gemm_cta(&map_a, &map_b, offsets, n_groups, I / 128, H, tc::EpiSwiGLU{hp, I}, BRowGateUp{I}, err);
+}
+
+__global__ void __launch_bounds__(tc::kThreads, 1)
+    gemm_down_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
+                     const int32_t* offsets, int n_groups, int H, int I, float* op, int* err) {
+  tc::grouped_gemm_cta(&map_a, &map_b, offsets, n_groups, H / 256, I, tc::EpiStoreF32{op, H}, BRowDown{}, err);
+}
+
+// ---- 7. combine ------------------------------------------------------------------------------
+__global__ void combine_kernel(const float* __restrict__ op, const int32_t* __restrict__ pos, const float* __restrict__ w,
+                               int T, int k, int H, int has_shared, __nv_bfloat16* __restrict__ y) {
+  const int per = H / 4;
+  const int64_t total = (int64_t)T * per;
+  const int Tk = T * k;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+    const int t = (int)(i / per), v = (int)(i % per);
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int j = 0; j < k; ++j) {
+      const float wj = w[(int64_t)t * k + j];
+      const float4 o = reinterpret_cast<const float4*>(op + (int64_t)pos[(int64_t)t * k + j] * H)[v];
+      acc.x = fmaf(wj, o.x, acc.x);
+      acc.y = fmaf(wj, o.y, acc.y);
+      acc.z = fmaf(wj, o.z, acc.z);
+      acc.w = fmaf(wj, o.w, acc.w);
+    }
+    if (has_shared) {
+      const float4 o = reinterpret_cast<const float4*>(op + (int64_t)pos[Tk + t] * H)[v];
+      acc.x += o.x; acc.y += o.y; acc.z += o.z; acc.w += o.w;
+    }
+    __nv_bfloat162 a = __floats2bfloat162_rn(acc.x, acc.y), b = __floats2bfloat162_rn(acc.z, acc.w);
+    uint2 out = make_uint2(*reinterpret_cast<uint32_t*>(&a), *reinterpret_cast<uint32_t*>(&b));
+    reinterpret_cast<uint2*>(y + (int64_t)t * H)[v] = out;
+  }
+}
+
+// Empty the slots [s0, s1) (the prefill buffers): their experts are no longer resident.
+__global__ void evict_range_kernel(CacheDev st, int64_t s0, int64_t s1, int* oldest_n) {
+  for (int64_t s = s0 + blockIdx.x * blockDim.x + threadIdx.x; s < s1; s += (int64_t)gridDim.x * blockDim.x) {
+    const int own = st.owner[s];
+    if (own >= 0) st.map[own] = -1;
+    st.owner[s] = -1;
+    st.stamp[s] = 0;
+  }
+  if (blockIdx.x == 0 && threadIdx.x == 0) *oldest_n = -1;
+}
+
+}  // namespace pf
+
+// ---- launchers ----------------------------------------------------------------------------
+static int g_sms = 0;
+static int sms() {
+  if (!g_sms) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&g_sms, cudaDevAttrMultiProcessorCount, dev);
+  }
+  return g_sms;
+}
+
+cudaError_t prefill_route(const float* logits, int T, int E, int k, int32_t* ids, float* w, cudaStream_t s) {
+  const int warps_per_block = 8;
+  pf::route_kernel<<<(T + warps_per_block - 1) / warps_per_block, 32 * warps_per_block, 0, s>>>(logits, T, E, k, ids, w);
+  return cudaGetLastError();
+}
+
+cudaError_t prefill_group(const int32_t* ids, int T, int k, int E, int has_shared, int32_t* cnt, int32_t* base,
+                          int32_t* offsets, int32_t* pos, int32_t* perm, cudaStream_t s) {
+  const int Tk = T * k, n_pairs = Tk + (has_shared ? T : 0), G = E + (has_shared ? 1 : 0);
+  const int n_chunks = (n_pairs + 1023) / 1024;
+  pf::group_count_kernel<<<n_chunks, 1024, G * sizeof(int32_t), s>>>(ids, Tk, n_pairs, E, G, cnt);
+  pf::group_scan_kernel<<<1, 1024, 0, s>>>(cnt, n_chunks, G, base, offsets);
+  pf::group_place_kernel<<<n_chunks, 1024, G * sizeof(int32_t), s>>>(ids, Tk, n_pairs, E, G, base, pos, perm);
+  return cudaGetLastError();
+}
+
+cudaError_t prefill_gather(const void* x, int T, int k, int H, int n_pairs, const int32_t* perm, void* xp,
+                           cudaStream_t s) {
+  pf::gather_kernel<<<sms() * 8, 256, 0, s>>>((const __nv_bfloat16*)x, T * k, k, H, n_pairs, perm, (__nv_bfloat16*)xp);
+  return cudaGetLastError();
+}
+
+cudaError_t prefill_dequant(const uint8_t* src, int64_t S4, uint8_t* dst, int64_t S16, int n_rec, int H, int I,
+                            cudaStream_t s) {
+  pf::dequant_kernel<<<sms() * 8, 256, 0, s>>>(src, S4, dst, S16, n_rec, H, I);
+  return cudaGetLastError();
+}
+
+static bool g_gemm_attr = false;
+static cudaError_t gemm_attr() {
+  if (g_gemm_attr) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(pf::gemm_gate_up_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)tc::kSmemBytes);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(pf::gemm_down_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tc::kSmemBytes);
+  g_gemm_attr = e == cudaSuccess;
+  return e;
+}
+
+// grid: enough CTAs for every tile of n_rows rows over n_groups groups
+static int gemm_grid(int n_rows, int n_groups, int nblocks_n) { return (n_rows / tc::kBM + n_groups) * nblocks_n; }
+
+cudaError_t prefill_gemm_gate_up(const CUtensorMap& a, const CUtensorMap& b, const int32_t* offsets, int n_groups,
+                                 int n_rows, int H, int I, void* hp, int* err, cudaStream_t s) {
+  if (cudaError_t e = gemm_attr()) return e;
+  pf::gemm_gate_up_kernel<<<gemm_grid(n_rows, n_groups, I / 128), tc::kThreads, tc::kSmemBytes, s>>>(
+      a, b, offsets, n_groups, H, I, (__nv_bfloat16*)hp, err);
+  return cudaGetLastError();
+}
+
+cudaError_t prefill_gemm_down(const CUtensorMap& a, const CUtensorMap& b, const int32_t* offsets, int n_groups,
+                              int n_rows, int H, int I, float* op, int* err, cudaStream_t s) {
+  if (cudaError_t e = gemm_attr()) return e;
+  pf::gemm_down_kernel<<<gemm_grid(n_rows, n_groups, H / 256), tc::kThreads, tc::kSmemBytes, s>>>(
+      a, b, offsets, n_groups, H, I, op, err);
+  return cudaGetLastError();
+}
+
+cudaError_t prefill_combine(const float* op, const int32_t* pos, const float* w, int T, int k, int H, int has_shared,
+                            void* y, cudaStream_t s) {
+  pf::combine_kernel<<<sms() * 8, 256, 0, s>>>(op, pos, w, T, k, H, has_shared, (__nv_bfloat16*)y);
+  return cudaGetLastError();
+}
+
+cudaError_t prefill_evict_range(const CacheDev& st, int64_t s0, int64_t s1, int* oldest_n, cudaStream_t s) {
+  pf::evict_range_kernel<<<64, 256, 0, s>>>(st, s0, s1, oldest_n);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

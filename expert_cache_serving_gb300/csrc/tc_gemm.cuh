@@ -1,0 +1,300 @@
+// Grouped bf16 GEMM on the 5th-generation tensor cores (tcgen05 + TMEM), fed
+// by TMA, for the prefill-size expert FFN.
+//
+// FreeToken write-up, "전층 이중 버퍼링": in prefill a layer's routed tokens
+// cover almost every expert, so each expert's FFN is a dense contraction over
+// the ~T*k/E tokens routed to it.
+//
+// One CTA computes one 128 x 256 output tile of one expert:
+//   rows    = 128 consecutive (token, rank) pairs of the expert in the grouped
+//             activation matrix A [rows][K] (bf16, K-major), rows beyond the
+//             expert's group are computed but never stored;
+//   columns = 256 rows of the expert's weight matrix B [E][N][K] (bf16,
+//             K-major), loaded as two 128-row boxes (b_row0, b_row1) so the
+//             gate/up GEMM can place gate rows j.. and up rows I+j.. side by side.
+// Warp roles (192 threads): warp 0 issues TMA loads into a 4-stage ring of
+// 48 KB stages (128B swizzle), warp 1 owns TMEM (256 fp32 columns) and issues
+// tcgen05.mma (M=128, N=256, K=16) from one elected thread, warps 2..5 read
+// the accumulator back with tcgen05.ld (each warp its 32 TMEM lanes) and run
+// the epilogue.  Every mbarrier wait is bounded: on time-out the kernel
+// records MOE_ERR_TIMEOUT, stops issuing work and still frees its TMEM.
+#pragma once
+#include <cuda.h>
+
+#include "common.cuh"
+
+namespace moe {
+namespace tc {
+
+constexpr int kBM = 128, kBN = 256, kBK = 64;  // tile; kBK bf16 = 128 bytes = one swizzle row
+constexpr int kStages = 4;
+constexpr int kAStage = kBM * kBK * 2;          // 16 KB
+constexpr int kBStage = kBN * kBK * 2;          // 32 KB
+constexpr int kStageBytes = kAStage + kBStage;  // 48 KB
+constexpr int kThreads = 192;
+constexpr int kTmemCols = 256;
+constexpr size_t kSmemBytes = (size_t)kStages * kStageBytes + 1024 /*align*/ + 256 /*barriers*/;
+
+// ---- PTX wrappers --------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
+
+// Wait for the phase with the given parity; false on time-out (~limit_ns).
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsigned long long limit_ns = 2000000000ull) {
+  const uint32_t a = smem_u32(bar);
+  unsigned long long t0 = 0;
+  for (uint32_t it = 0;; ++it) {
+    uint32_t done;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(done)
+        : "r"(a), "r"(parity)
+        : "memory");
+    if (done) return true;
+    if ((it & 255) == 0) {
+      const unsigned long long t = globaltimer_ns();
+      if (t0 == 0) t0 = t;
+      else if (t - t0 > limit_ns) return false;
+    }
+  }
+}
+
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];" ::"r"(
+          smem_u32(dst)),
+      "l"(map), "r"(smem_u32(bar)), "r"(c0), "r"(c1)
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1, int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(
+          smem_u32(dst)),
+      "l"(map), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+
+// K-major operand tile in shared memory written by TMA with 128-byte swizzle:
+// rows of 128 bytes, 8-row (1024-byte) swizzle atoms.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((addr & 0x3FFFF) >> 4);       // start address
+  d |= (uint64_t)0 << 16;                         // leading byte offset (unused for swizzled K-major)
+  d |= (uint64_t)(1024 >> 4) << 32;               // stride byte offset: one 8-row atom
+  d |= (uint64_t)1 << 46;                         // descriptor version for tcgen05
+  d |= (uint64_t)2 << 61;                         // 128-byte swizzle
+  return d;
+}
+
+// kind::f16 instruction descriptor: bf16 x bf16 -> f32, both K-major, M x N.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
+  return (1u << 4)                  // D format f32
+         | (1u << 7)                // A format bf16
+         | (1u << 10)               // B format bf16
+         | ((uint32_t)(N >> 3) << 17)
+         | ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_bf16(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t accum) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.u32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(tmem_d),
+      "l"(a), "l"(b), "r"(idesc), "r"(accum)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+
+__device__ __forceinline__ void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst_smem)),
+               "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+// 32 lanes x 32 bits, 16 consecutive columns -> 16 registers per thread.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+
+// ---- tile scheduling -----------------------------------------------------------
+// Work item of one CTA: expert e, rows [row0, row0 + 128) of A (clipped to
+// row_end for stores), output column block nb.
+struct Tile {
+  int e, row0, row_end, nb;
+};
+
+// Tiles are enumerated expert-major, then row block, then column block; the
+// grid is sized for the worst case and CTAs past the last tile exit.
+__device__ __forceinline__ bool find_tile(const int32_t* offsets, int E, int nblocks_n, int cta, Tile* t) {
+  int base = 0;
+  for (int e = 0; e < E; ++e) {
+    const int n = offsets[e + 1] - offsets[e];
+    const int mt = (n + kBM - 1) / kBM;
+    const int cnt = mt * nblocks_n;
+    if (cta < base + cnt) {
+      const int r = cta - base;
+      t->e = e;
+      t->row0 = offsets[e] + (r / nblocks_n) * kBM;
+      t->row_end = offsets[e + 1];
+      t->nb = r % nblocks_n;
+      return true;
+    }
+    base += cnt;
+  }
+  return false;
+}
+
+// Epilogues --------------------------------------------------------------------
+// gate/up: columns [0,128) gate, [128,256) up of output block nb -> bf16 h.
+struct EpiSwiGLU {
+  __nv_bfloat16* h;  // [rows][I]
+  int I;
+  __device__ void operator()(uint32_t tmem, int row, bool valid, int nb) const {
+    for (int c = 0; c < 128; c += 16) {
+      float g[16], u[16];
+      tmem_ld16(tmem + c, g);
+      tmem_ld16(tmem + 128 + c, u);
+      if (!valid) continue;
+      uint32_t packed[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float h0 = g[2 * i] / (1.0f + expf(-g[2 * i])) * u[2 * i];
+        const float h1 = g[2 * i + 1] / (1.0f + expf(-g[2 * i + 1])) * u[2 * i + 1];
+        __nv_bfloat162 p2 = __floats2bfloat162_rn(h0, h1);
+        packed[i] = *reinterpret_cast<uint32_t*>(&p2);
+      }
+      uint4* dst = reinterpret_cast<uint4*>(h + (int64_t)row * I + (int64_t)nb * 128 + c);
+      dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+      dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+    }
+  }
+};
+
+// down: 256 fp32 columns of output block nb -> o [rows][N].
+struct EpiStoreF32 {
+  float* o;
+  int N;
+  __device__ void operator()(uint32_t tmem, int row, bool valid, int nb) const {
+    for (int c = 0; c < 256; c += 16) {
+      float v[16];
+      tmem_ld16(tmem + c, v);
+      if (!valid) continue;
+      float4* dst = reinterpret_cast<float4*>(o + (int64_t)row * N + (int64_t)nb * 256 + c);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+    }
+  }
+};
+
+// A: 2D map over [rows][K]; B: 3D map over [E][Nrows][K].  b_row(nb, half)
+// gives the first weight row of each 128-row half of the 256-column block.
+template <typename Epi, typename BRow>
+__device__ void grouped_gemm_cta(const CUtensorMap* map_a, const CUtensorMap* map_b, const int32_t* offsets, int E,
+                                 int nblocks_n, int K, Epi epi, BRow b_row, int* err) {
+  extern __shared__ __align__(1024) uint8_t tc_smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(tc_smem_raw) + 1023) & ~(uintptr_t)1023);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
+  uint64_t* empty = full + kStages;
+  uint64_t* acc_full = empty + kStages;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_full + 1);
+  __shared__ Tile s_tile;
+  __shared__ int s_has;
+  __shared__ int s_fail;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    s_has = find_tile(offsets, E, nblocks_n, blockIdx.x, &s_tile) ? 1 : 0;
+    s_fail = 0;
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(acc_full, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  if (!s_has) return;
+  const Tile t = s_tile;
+  if (warp == 1) tmem_alloc(tmem_slot, kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const int ksteps = K / kBK;
+
+  if (warp == 0 && lane == 0) {
+    // TMA producer
+    for (int ks = 0; ks < ksteps; ++ks) {
+      const int s = ks % kStages;
+      if (ks >= kStages && !mbar_wait(&empty[s], ((ks / kStages) - 1) & 1)) { s_fail = 1; break; }
+      if (s_fail) break;
+      uint8_t* a_dst = smem + s * kStageBytes;
+      uint8_t* b_dst = a_dst + kAStage;
+      mbar_expect_tx(&full[s], kStageBytes);
+      tma_load_2d(a_dst, map_a, &full[s], ks * kBK, t.row0);
+      tma_load_3d(b_dst, map_b, &full[s], ks * kBK, b_row(t.nb, 0), t.e);
+      tma_load_3d(b_dst + kBStage / 2, map_b, &full[s], ks * kBK, b_row(t.nb, 1), t.e);
+    }
+  } else if (warp == 1 && lane == 0) {
+    // MMA issuer
+    constexpr uint32_t idesc = idesc_bf16(kBM, kBN);
+    for (int ks = 0; ks < ksteps; ++ks) {
+      const int s = ks % kStages;
+      if (s_fail || !mbar_wait(&full[s], (ks / kStages) & 1)) { s_fail = 1; break; }
+      tc_fence_after();
+      const uint32_t a0 = smem_u32(smem + s * kStageBytes);
+      const uint32_t b0 = a0 + kAStage;
+#pragma unroll
+      for (int kk = 0; kk < kBK / 16; ++kk)
+        mma_bf16(tmem, smem_desc_sw128(a0 + kk * 32), smem_desc_sw128(b0 + kk * 32), idesc, (ks | kk) != 0);
+      mma_commit(&empty[s]);
+    }
+    mma_commit(acc_full);
+  } else if (warp >= 2) {
+    // epilogue: warp w reads TMEM lanes 32*(w%4) .. +31, i.e. tile rows
+    const int q = warp & 3;
+    const bool ok = mbar_wait(acc_full, 0, 4000000000ull);
+    tc_fence_after();
+    const int r = q * 32 + lane;
+    const int row = t.row0 + r;
+    if (ok && !s_fail) epi(tmem + ((uint32_t)(q * 32) << 16), row, row < t.row_end, t.nb);
+    if (!ok) s_fail = 1;
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (s_fail && threadIdx.x == 0) atomicExch(err, MOE_ERR_TIMEOUT);
+  if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+}
+
+}  // namespace tc
+}  // namespace moe

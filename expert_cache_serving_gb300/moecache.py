@@ -37,8 +37,9 @@ class moe_stats(ctypes.Structure):
                 ("host_wait_us", ctypes.c_double), ("host_issue_us", ctypes.c_double),
                 ("resize_calls", ctypes.c_int64), ("resize_moves", ctypes.c_int64),
                 ("resize_evictions", ctypes.c_int64), ("prefill_layers", ctypes.c_int64),
-                ("prefill_ms", ctypes.c_double), ("prefill_copy_ms", ctypes.c_double),
-                ("prefill_compute_ms", ctypes.c_double)]
+                ("prefill_tokens", ctypes.c_int64), ("prefill_ms", ctypes.c_double),
+                ("prefill_copy_ms", ctypes.c_double), ("prefill_compute_ms", ctypes.c_double),
+                ("prefill_gemm_ms", ctypes.c_double), ("prefill_gemm_flop", ctypes.c_double)]
 
     def as_dict(self):
         return {name: getattr(self, name) for name, _ in self._fields_}

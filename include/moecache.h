@@ -104,7 +104,12 @@ typedef struct {
   double host_issue_us;      /* host time spent issuing fills */
   int64_t resize_calls, resize_moves, resize_evictions;
   int64_t prefill_layers;
-  double prefill_ms, prefill_copy_ms, prefill_compute_ms; /* profiling on */
+  int64_t prefill_tokens;    /* tokens x layers processed by moe_prefill_stream */
+  double prefill_ms;         /* device time of whole moe_prefill_stream calls (profiling on) */
+  double prefill_copy_ms;    /* summed duration of the per-layer host -> device expert streams */
+  double prefill_compute_ms; /* summed per-layer compute time after each layer's experts landed */
+  double prefill_gemm_ms;    /* summed time of the grouped GEMM launches */
+  double prefill_gemm_flop;  /* useful flops of those launches (2 * rows * N * K) */
 } moe_stats;
 
 typedef struct {
