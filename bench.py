@@ -352,6 +352,83 @@ def run_native(args, w):
     return 0
 
 
+# ------------------------------------------------------------ prefill leg --
+def run_prefill(args, w):
+    """Config 4: one T-token prompt through every layer of the config-3 model
+    per step, layer l+1's experts streamed host->device while layer l runs."""
+    import torch
+
+    from expert_cache_serving_gb300 import moecache as mc
+    from expert_cache_serving_gb300 import runner
+
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    peaks, peak_kind = load_peaks()
+    T, L = w.B, w.L
+    t0 = time.perf_counter()
+    pool = runner.build_pool(w)
+    xs = np.stack([synth.activations_bf16(w.seed, 0, l, T, w.H) for l in range(L)])
+    x = torch.from_numpy(xs.view(np.int16)).view(torch.bfloat16).to(dev)
+    del xs
+    logits = torch.from_numpy(synth.iid_logits(w.seed, L, T, w.E)).to(dev)
+    y = torch.empty_like(x)
+    cache = runner.Cache(w, pool, None, C=w.C, max_tokens=1)
+    setup_s = time.perf_counter() - t0
+    stream = torch.cuda.current_stream()
+
+    def step():
+        st = mc.moe_prefill_stream(cache.handle, 0, L, x, logits, T, y, stream)
+        if st != mc.MOE_OK:
+            raise mc.MoeError(st, "moe_prefill_stream")
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    mc.moe_cache_reset_stats(cache.handle)
+    mc.moe_cache_set_profiling(cache.handle, 1)
+    clk = ClockSampler(os.path.join(ROOT, "gpurun_out", "clocks_prefill.csv"))
+    os.makedirs(os.path.join(ROOT, "gpurun_out"), exist_ok=True)
+    clk.start()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    clocks = clk.stop()
+    ms = e0.elapsed_time(e1)
+    st = mc.moe_cache_stats(cache.handle)
+    S = synth.record_bytes(w.H, w.I, w.wdtype)
+    b_p = measure_link(dev, pool, S)
+    value = T * args.steps / (ms / 1e3)
+    gemm_tflops = st["prefill_gemm_flop"] / (st["prefill_gemm_ms"] / 1e3) / 1e12 if st["prefill_gemm_ms"] else None
+    peak_tf = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops", 1700.0)))
+    copy_bytes = L * w.E * S * args.steps
+    line = {
+        "metric": METRIC, "value": value, "unit": "tok/s (prefill)", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16 (FP4 weights dequantised exactly)", "data": "synthetic",
+        "config": {"workload": w.name, "layers": L, "experts": w.E, "top_k": w.k, "hidden": w.H,
+                   "intermediate": w.I, "prompt_tokens": T, "cache_slots": w.C, "record_bytes": S,
+                   "host_pool_GB": round(w.LE * S / 1e9, 1), "step": "one prompt through all layers",
+                   "l2": "each layer streams 3.6 GB of experts >> 129 MB L2; no flush"},
+        "roofline": {"bound": "tensor", "achieved": gemm_tflops, "peak": peak_tf, "unit": "TFLOP/s",
+                     "frac": gemm_tflops / peak_tf if gemm_tflops else None, "traffic": None,
+                     "kernel": "grouped tcgen05 GEMMs (gate/up + down)", "peak_kind": peak_kind + " bf16 sustained",
+                     "gemm_ms_per_step": st["prefill_gemm_ms"] / args.steps},
+        "link": {"B_P_GBps": b_p, "copy_ms_per_step": st["prefill_copy_ms"] / args.steps,
+                 "compute_ms_per_step": st["prefill_compute_ms"] / args.steps,
+                 "exposed_copy_ms_per_step": ms / args.steps - st["prefill_compute_ms"] / args.steps,
+                 "bound_ms_per_step": max(st["prefill_copy_ms"], st["prefill_compute_ms"]) / args.steps,
+                 "frac_of_bound": max(st["prefill_copy_ms"], st["prefill_compute_ms"]) / ms,
+                 "stream_GBps": copy_bytes / (st["prefill_copy_ms"] / 1e3) / 1e9 if st["prefill_copy_ms"] else None},
+        "gpu_launches": None, "clocks": clocks, "setup_s": round(setup_s, 1),
+    }
+    print(json.dumps(line), flush=True)
+    cache.close()
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -359,7 +436,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=16)
     ap.add_argument("--e2e-steps", type=int, default=None)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
-    ap.add_argument("--workload", default="c2", choices=["c2", "small"])
+    ap.add_argument("--workload", default="c2", choices=["c2", "c4", "small"])
     ap.add_argument("--cpu-tokens", type=int, default=3)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile", type=int, default=1, help="1: CUDA events per launch; 2: also phase timestamps")
@@ -368,6 +445,8 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.workload == "c4":
+        return run_prefill(args, configs.C4)
     w = configs.C2 if args.workload == "c2" else configs.SMALL_BF16
     if args.impl == "reference":
         return run_reference(args, w)

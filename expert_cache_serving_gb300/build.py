@@ -43,9 +43,15 @@ def _run(cmd, verbose):
     return r
 
 
+SYNTH_GPU_SRC = os.path.join(ROOT, "synth", "synth_gpu.cu")
+SYNTH_GPU_LIB = os.path.join(ROOT, "synth", "_lib", "libsynth_gpu.so")
+
+
 def build_synth(verbose=False) -> str:
     os.makedirs(os.path.dirname(SYNTH_LIB), exist_ok=True)
     _run(["gcc", "-O3", "-fPIC", "-shared", "-ffp-contract=off", "-pthread", SYNTH_SRC, "-o", SYNTH_LIB], verbose)
+    _run([_nvcc()] + ARCH + ["-O3", "-fmad=false", "-Xcompiler", "-fPIC", "-shared", "-cudart", "static",
+                             SYNTH_GPU_SRC, "-o", SYNTH_GPU_LIB], verbose)
     return SYNTH_LIB
 
 

@@ -18,11 +18,9 @@ def model_desc(w: Workload, max_tokens: int | None = None) -> mc.moe_model_desc:
 
 
 def build_pool(w: Workload, threads: int | None = None) -> torch.Tensor:
-    """Pinned host tensor u8 [L*E, S] with every routed expert record (C generator)."""
-    S = synth.record_bytes(w.H, w.I, w.wdtype)
-    pool = torch.empty((w.LE, S), dtype=torch.uint8, pin_memory=True)
-    synth.fill_records(pool.data_ptr(), w.seed, 0, w.LE, w.H, w.I, w.wdtype, w.sigma, threads)
-    return pool
+    """Host tensor u8 [L*E, S] over exact-size pinned memory holding every routed
+    expert record, generated on the GPU (the seeded generator's CUDA twin)."""
+    return torch.from_numpy(synth.pinned_pool(w.seed, w.LE, w.H, w.I, w.wdtype, w.sigma))
 
 
 def build_shared(w: Workload, device="cuda") -> torch.Tensor | None:

@@ -212,6 +212,78 @@ def fill_records(dst_ptr: int, seed: int, key0: int, n_keys: int, H: int, I: int
         raise RuntimeError(f"synth_records failed ({rc})")
 
 
+# --- GPU twin (synth_gpu.cu) and exact-size pinned buffers -------------------------
+
+_GLIB = None
+
+
+def _gpu_lib():
+    global _GLIB
+    if _GLIB is None:
+        path = os.path.join(os.path.dirname(__file__), "_lib", "libsynth_gpu.so")
+        if not os.path.exists(path):
+            raise RuntimeError(f"{path} missing: run __graft_entry__.build() first")
+        lib = ctypes.CDLL(path)
+        lib.synth_gpu_records.argtypes = [ctypes.c_uint64, ctypes.c_float, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                          ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p]
+        lib.synth_gpu_fill_host.argtypes = [ctypes.c_uint64, ctypes.c_float, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                            ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p, ctypes.c_int64]
+        lib.synth_host_alloc.argtypes = [ctypes.c_size_t]
+        lib.synth_host_alloc.restype = ctypes.c_void_p
+        lib.synth_host_free.argtypes = [ctypes.c_void_p]
+        _GLIB = lib
+    return _GLIB
+
+
+def records_gpu(dst_dev_ptr: int, seed: int, key0: int, n_keys: int, H: int, I: int, wdtype: int,
+                sigma: float = 0.02) -> None:
+    """Records key0 .. key0+n_keys-1 written back to back at a device address."""
+    rc = _gpu_lib().synth_gpu_records(seed, float(sigma_scale(sigma)), H, I, wdtype, key0, n_keys,
+                                      ctypes.c_void_p(dst_dev_ptr))
+    if rc:
+        raise RuntimeError(f"synth_gpu_records failed ({rc})")
+
+
+def mem_available_bytes() -> int:
+    with open("/proc/meminfo") as f:
+        for line in f:
+            if line.startswith("MemAvailable:"):
+                return int(line.split()[1]) * 1024
+    return 0
+
+
+class PinnedBuffer:
+    """Exact-size page-locked host buffer; freed when the last view of it goes away."""
+
+    def __init__(self, nbytes: int, reserve: int = 16 << 30):
+        avail = mem_available_bytes()
+        if avail and nbytes + reserve > avail:
+            raise MemoryError(f"{nbytes / 1e9:.1f} GB pinned pool would leave less than "
+                              f"{reserve / 1e9:.0f} GB of the {avail / 1e9:.1f} GB available host memory")
+        self.nbytes = nbytes
+        self.ptr = _gpu_lib().synth_host_alloc(nbytes)
+        if not self.ptr:
+            raise MemoryError(f"cudaHostAlloc of {nbytes} bytes failed")
+        self.__array_interface__ = {"shape": (nbytes,), "typestr": "|u1", "data": (self.ptr, False), "version": 3}
+
+    def __del__(self):
+        if getattr(self, "ptr", None):
+            _gpu_lib().synth_host_free(ctypes.c_void_p(self.ptr))
+            self.ptr = None
+
+
+def pinned_pool(seed: int, n_keys: int, H: int, I: int, wdtype: int, sigma: float = 0.02,
+                chunk_bytes: int = 1 << 30) -> np.ndarray:
+    """u8 [n_keys, S] numpy view of an exact-size pinned buffer filled on the GPU."""
+    S = record_bytes(H, I, wdtype)
+    buf = PinnedBuffer(n_keys * S)
+    rc = _gpu_lib().synth_gpu_fill_host(seed, float(sigma_scale(sigma)), H, I, wdtype, 0, n_keys,
+                                        ctypes.c_void_p(buf.ptr), chunk_bytes)
+    if rc:
+        raise RuntimeError(f"synth_gpu_fill_host failed ({rc})")
+    return np.asarray(buf).reshape(n_keys, S)
+
+
 def records_array(seed: int, key0: int, n_keys: int, H: int, I: int, wdtype: int,
                   sigma: float = 0.02) -> np.ndarray:
     """Records as a fresh numpy u8 [n_keys, S] array, filled by the C generator."""
