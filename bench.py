@@ -436,7 +436,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=16)
     ap.add_argument("--e2e-steps", type=int, default=None)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
-    ap.add_argument("--workload", default="c2", choices=["c2", "c4", "small"])
+    ap.add_argument("--workload", default="c2", choices=["c2", "c4", "small", "small-prefill"],
+                    help="c2: Qwen3.6-shaped decode (default); c4: 4096-token FP4 prefill over 43 layers; "
+                         "small / small-prefill: 3-layer bf16 decode / 2-layer FP4 prefill for profiler captures")
     ap.add_argument("--cpu-tokens", type=int, default=3)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile", type=int, default=1, help="1: CUDA events per launch; 2: also phase timestamps")
@@ -447,6 +449,8 @@ def main():
         ap.error("--warmup must be >= 3")
     if args.workload == "c4":
         return run_prefill(args, configs.C4)
+    if args.workload == "small-prefill":
+        return run_prefill(args, configs.C4.with_(name="small-fp4-prefill-256", L=2, E=16, C=32, B=256))
     w = configs.C2 if args.workload == "c2" else configs.SMALL_BF16
     if args.impl == "reference":
         return run_reference(args, w)
