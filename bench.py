@@ -171,22 +171,23 @@ def run_reference(args, w):
 
 
 # ------------------------------------------------------------ native leg --
-def measure_link(dev, pool, S, reps=24):
-    """B_P: host->device bandwidth of cudaMemcpyAsync of one expert record
-    from the pinned pool (best of reps), GB/s."""
+def measure_link(dev, pool, S, n=96):
+    """B_P: sustained host->device bandwidth of back-to-back cudaMemcpyAsync of
+    expert records spread evenly over the whole pinned pool, GB/s (the link
+    rate varies across the pool's pages, so one record is not representative)."""
     import torch
 
     dst = torch.empty(S, dtype=torch.uint8, device=dev)
-    best = 0.0
-    for r in range(reps):
-        src = pool[(r * 37) % pool.shape[0]]
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record()
-        dst.copy_(src, non_blocking=True)
-        b.record()
-        b.synchronize()
-        best = max(best, S / (a.elapsed_time(b) / 1e3) / 1e9)
-    return best
+    rows = [(r * pool.shape[0]) // n for r in range(n)]
+    dst.copy_(pool[rows[0]], non_blocking=True)
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for r in rows:
+        dst.copy_(pool[r], non_blocking=True)
+    b.record()
+    b.synchronize()
+    return n * S / (a.elapsed_time(b) / 1e3) / 1e9
 
 
 def run_native(args, w):

@@ -380,7 +380,7 @@ extern "C" moe_status moe_cache_create(const moe_model_desc* desc, const void* h
       (s = cu(cudaMalloc(&c->d_logits, sizeof(float) * (size_t)Bm * E), "logits")) ||
       (s = cu(cudaMalloc(&c->d_bar, sizeof(unsigned long long)), "barrier")) ||
       (s = cu(cudaMalloc(&c->d_flags, sizeof(unsigned) * (1 + 2 * kMaxU)), "flags")) ||
-      (s = cu(cudaMalloc(&c->d_oldest, sizeof(int32_t) * M), "victim order")) ||
+      (s = cu(cudaMalloc(&c->d_oldest, sizeof(int32_t) * kMaxU), "victim order")) ||
       (s = cu(cudaMalloc(&c->d_oldest_n, sizeof(int)), "victim order")))
     return bail(s);
   if ((s = cu(cudaMemset(c->d_map, 0xFF, sizeof(int32_t) * LE), "memset")) ||

@@ -93,9 +93,11 @@ def run_oracle(w: Workload, calls, logits=None, router_w=None, C=None, y_for=Non
 
 
 def run_gpu(w: Workload, calls, logits=None, router_w=None, C=None, max_slots=0, resize=None, keep_y=True,
-            pool=None, shared=None, inject=None, fill_mode=0):
+            pool=None, shared=None, inject=None, fill_mode=0, y_for=None, light=False):
     """GPU side through the C ABI; returns (RunOut, final cache state, stats).
-    inject: {call index: number of fills that succeed before the injected failure}."""
+    inject: {call index: number of fills that succeed before the injected failure}.
+    y_for: call indices whose output to keep (None = all, when keep_y).
+    light: only ids and slots are read back per call (full-size runs)."""
     import torch
 
     from expert_cache_serving_gb300 import moecache as mc
@@ -126,18 +128,20 @@ def run_gpu(w: Workload, calls, logits=None, router_w=None, C=None, max_slots=0,
         if inject and ci in inject:
             mc.moe_cache_inject_fill_failure(cache.handle, inject[ci])
         x = runner.activations(w, s, l).to(dev)
-        aux = {"ids": ids, "weights": wts, "slots": slots, "perm": perm, "offsets": offs}
+        aux = {"ids": ids, "slots": slots} if light else \
+            {"ids": ids, "weights": wts, "slots": slots, "perm": perm, "offsets": offs}
         lg = lg_dev[s, l] if lg_dev is not None else None
         st = cache.forward(l, x, lg, y, B, router_w=(wr_dev[l] if wr_dev is not None else None), stream=stream,
                            aux=aux)
         co = CallOut(s, l, status=st)
         if st == mc.MOE_OK:
             co.ids = ids.cpu().numpy().copy()
-            co.w = wts.cpu().numpy().astype(np.float64)
             co.slots = slots.cpu().numpy().copy()
-            co.perm = perm.cpu().numpy().copy()
-            co.offsets = offs.cpu().numpy().copy()
-            if keep_y:
+            if not light:
+                co.w = wts.cpu().numpy().astype(np.float64)
+                co.perm = perm.cpu().numpy().copy()
+                co.offsets = offs.cpu().numpy().copy()
+            if keep_y and (y_for is None or ci in y_for):
                 co.y = y.float().cpu().numpy().astype(np.float64)
         out.calls.append(co)
     torch.cuda.synchronize()
