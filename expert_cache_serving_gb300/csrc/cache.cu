@@ -201,6 +201,7 @@ struct moe_cache {
   int grid = 0;
   size_t smem = 0;
   int smem_h_floats = 0, rows_per_cta_max = 0;
+  int stage_items = 0, stage_pitch = 0, stage_off = 0;  // W_down rows staged in shared memory
   // accounting
   moe_stats st{};
   bool profiling = false, tracing = false;
@@ -437,7 +438,17 @@ extern "C" moe_status moe_cache_create(const moe_model_desc* desc, const void* h
     return bail(fail(MOE_ERR_INVALID_ARG, "max_tokens * (H, I) too large for the layer kernel's shared memory"));
   c->smem_h_floats = (int)std::min<size_t>((budget - xbytes - obytes) / 4, (size_t)(Bm * k + Bm) * I);
   c->smem_h_floats &= ~3;
-  c->smem = layer_smem_bytes(desc->wdtype, Bm, H, k, c->smem_h_floats, c->rows_per_cta_max);
+  // what is left holds this CTA's W_down rows of as many resident experts as fit
+  const int64_t down_row_bytes = desc->wdtype == MOE_FP32   ? 4LL * I
+                                 : desc->wdtype == MOE_BF16 ? 2LL * I
+                                                            : I / 2 + I / 16;
+  const size_t stage_off = (layer_smem_bytes(desc->wdtype, Bm, H, k, c->smem_h_floats, c->rows_per_cta_max) + 15) &
+                           ~(size_t)15;
+  c->stage_pitch = (int)(c->rows_per_cta_max * down_row_bytes);
+  c->stage_off = (int)stage_off;
+  c->stage_items =
+      stage_off < budget ? (int)std::min<size_t>((budget - stage_off) / (size_t)c->stage_pitch, (size_t)kMaxItems) : 0;
+  c->smem = stage_off + (size_t)c->stage_items * c->stage_pitch;
   c->grid = layer_max_grid(desc->wdtype, c->smem);
   if (c->grid != sms)  // the per-CTA row split assumes one CTA on every SM
     return bail(fail(MOE_ERR_CUDA, "layer kernel cannot keep one CTA resident on every SM (%d of %d)", c->grid, sms));
@@ -587,6 +598,9 @@ extern "C" moe_status moe_layer_forward_ex(moe_cache_t c, int32_t layer, const v
   p.y = y;
   p.smem_h_floats = c->smem_h_floats;
   p.rows_per_cta_max = c->rows_per_cta_max;
+  p.stage_items = c->stage_items;
+  p.stage_pitch = c->stage_pitch;
+  p.stage_off = c->stage_off;
   p.oldest = c->d_oldest;
   p.oldest_n = c->d_oldest_n;
   int tl_row = -1;

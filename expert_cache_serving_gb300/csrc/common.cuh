@@ -116,6 +116,52 @@ __device__ __forceinline__ void st_release_u32(unsigned* p, unsigned v) {
   asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
+// ---- shared-memory addresses, mbarriers and 1-D bulk copies ------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
+
+// Wait for the phase with the given parity; false on time-out (~limit_ns).
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsigned long long limit_ns = 2000000000ull) {
+  const uint32_t a = smem_u32(bar);
+  unsigned long long t0 = 0;
+  for (uint32_t it = 0;; ++it) {
+    uint32_t done;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(done)
+        : "r"(a), "r"(parity)
+        : "memory");
+    if (done) return true;
+    if ((it & 255) == 0) {
+      const unsigned long long t = globaltimer_ns();
+      if (t0 == 0) t0 = t;
+      else if (t - t0 > limit_ns) return false;
+    }
+  }
+}
+
+// 1-D bulk copy global -> shared (the async proxy), completing `bytes` on the
+// mbarrier, L2 evict-first (streamed weights).  dst, src and bytes must be
+// multiples of 16.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "{\n .reg .b64 pol;\n createpolicy.fractional.L2::evict_first.b64 pol, 1.0;\n"
+      " cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], pol;\n}\n"
+      ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() { asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory"); }
+
 // Grid-wide barrier of a cooperative launch over a counter that only grows:
 // barrier number b of a launch completes when the counter reaches
 // base + (b + 1) * gridDim.x.  The wait gives up after limit_ns, records
@@ -146,7 +192,7 @@ __device__ __forceinline__ bool grid_barrier(unsigned long long* count, unsigned
 // Wait until *flag == want (returns 0) or want | kFlagError (returns 1); 2 on
 // timeout (MOE_ERR_TIMEOUT recorded).  Thread 0 spins, the CTA waits on it.
 __device__ __forceinline__ int wait_flag(const unsigned* flag, unsigned want, int* err,
-                                         unsigned long long limit_ns = 5000000000ull) {
+                                         unsigned long long limit_ns = 5000000000ull, unsigned sleep_ns = 256) {
   __shared__ int s_res;
   __syncthreads();
   if (threadIdx.x == 0) {
@@ -166,7 +212,7 @@ __device__ __forceinline__ int wait_flag(const unsigned* flag, unsigned want, in
         atomicExch(err, MOE_ERR_TIMEOUT);
         break;
       }
-      __nanosleep(256);
+      __nanosleep(sleep_ns);
     }
     s_res = res;
   }

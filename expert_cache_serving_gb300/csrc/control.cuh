@@ -38,7 +38,7 @@ struct CtrlSmem {
   unsigned bits[kMaxE / 32];
   int wpre[kMaxE / 32];
   int U[kMaxU];
-  int slot[kMaxU];
+  int slot[kMaxU];  // slot of U[r] after the call (hit: its slot; miss: its victim)
   int fill[kMaxU];
   int mrank[kMaxU];
   int cnt[kMaxU];
@@ -46,14 +46,74 @@ struct CtrlSmem {
   int sel_slot[kMaxU];
   unsigned long long sel_key[kMaxU];
   int victim[kMaxU];
+  int victim_owner[kMaxU];  // key held by each victim before the call (-1: empty)
   int scan[33];
   unsigned hist[2048];
   int nu, nmiss, nsel, err, remaining, bin;
   unsigned long long g, kmin, kmax, prefix;
 };
 
-__device__ __forceinline__ bool better_logit(float a, int ia, float b, int ib) {
-  return a > b || (a == b && ia < ib);
+// Order-preserving 32-bit key of a logit for the router's max-reductions: NaN
+// counts as -inf and -0 as +0, so equal logits give equal keys and the
+// lower expert id wins the tie.  Real logits map to keys > 0; 0 marks "none".
+__device__ __forceinline__ unsigned logit_key(float x) {
+  unsigned u = __float_as_uint(x);
+  if ((u & 0x7FFFFFFFu) > 0x7F800000u) u = 0xFF800000u;  // NaN -> -inf
+  if ((u & 0x7FFFFFFFu) == 0u) u = 0u;                   // -0 -> +0
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float key_logit(unsigned key) {
+  return __uint_as_float((key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key);
+}
+
+// Top-k of one token's E logits by one warp: lane l holds experts l + 32q
+// (q < NQ) as keys, keeps its own best, and each round the warp takes the
+// largest key (redux max) and, among equal keys, the lowest expert id (redux
+// min); only the winning lane rescans.  Weights = softmax over the k taken
+// logits, exp(l_r - l_0) / sum, in the order taken.
+template <int NQ>
+__device__ __forceinline__ void route_token(const float* lg, int E, int k, int lane, float* aux, int* ids, float* w) {
+  unsigned key[NQ];
+#pragma unroll
+  for (int q = 0; q < NQ; ++q) {
+    const int e = lane + 32 * q;
+    key[q] = 0u;
+    if (e < E) {
+      const float x = lg[e];
+      if (aux) aux[e] = x;
+      key[q] = logit_key(x);
+    }
+  }
+  unsigned bk = 0u;
+  int bq = 0;
+#pragma unroll
+  for (int q = 0; q < NQ; ++q)
+    if (key[q] > bk) { bk = key[q]; bq = q; }
+  float m0 = 0.f, sum = 0.f;
+  for (int r = 0; r < k; ++r) {
+    const unsigned m = __reduce_max_sync(0xFFFFFFFFu, bk);
+    const int e = (int)__reduce_min_sync(0xFFFFFFFFu, bk == m ? (unsigned)(lane + 32 * bq) : 0xFFFFFFFFu);
+    const float x = key_logit(m);
+    if (r == 0) m0 = x;
+    const float ex = expf(x - m0);
+    sum += ex;
+    if (lane == 0) {
+      ids[r] = e;
+      w[r] = ex;
+    }
+    if ((e & 31) == lane) {
+      const int taken = e >> 5;
+      bk = 0u;
+      bq = 0;
+#pragma unroll
+      for (int q = 0; q < NQ; ++q) {
+        if (q == taken) key[q] = 0u;
+        if (key[q] > bk) { bk = key[q]; bq = q; }
+      }
+    }
+  }
+  if (lane == 0)
+    for (int r = 0; r < k; ++r) w[r] = w[r] / sum;
 }
 
 // Rank key of slot s for victim selection; false if s is excluded (a slot
@@ -172,9 +232,24 @@ __device__ int select_oldest(CtrlSmem& cs, const CacheDev& st, int64_t C, int wa
   return nsel == want ? want : -1;
 }
 
-// Routing, deduplication, lookup, victim choice, state update and grouping.
-// Writes the plan (device), the host summary (pinned) and the inspection
-// outputs.  Returns the status (MOE_OK or an error) to every thread.
+// Publish the host summary of the call (its fields are already written):
+// system-scope fences by every writer, then the sequence number last.
+__device__ __forceinline__ void publish_summary(const LayerParams& p) {
+  __threadfence_system();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence_system();
+    p.work->seq = p.seq;
+  }
+}
+
+// Routing, deduplication, residency lookup, victim choice and grouping: the
+// plan the other CTAs need, written to device memory (and, when the host must
+// issue copies for this call, the host summary too, before anything else).
+// Recency, the residency table and the undo log are written afterwards by
+// control_commit, off the other CTAs' critical path.  Returns the status
+// (MOE_OK or an error) to every thread; on an error the plan and the host
+// summary carry it and nothing is changed.
 __device__ int control_step(const LayerParams& p, CtrlSmem& cs) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarp = blockDim.x >> 5;
   const int E = p.E, k = p.k, B = p.B, npairs = B * k;
@@ -182,54 +257,34 @@ __device__ int control_step(const LayerParams& p, CtrlSmem& cs) {
   Plan* plan = p.plan;
   HostWork* work = p.work;
 
-  // ---- router: one warp per token, logits held in registers ---------------
-  for (int t = warp; t < B; t += nwarp) {
-    const float* lg = p.logits + (size_t)t * E;
-    float v[kMaxE / 32];
-#pragma unroll
-    for (int q = 0; q < kMaxE / 32; ++q) {
-      const int e = lane + 32 * q;
-      float x = -INFINITY;
-      if (e < E) {
-        x = lg[e];
-        if (p.aux_logits) p.aux_logits[(size_t)t * E + e] = x;
-        if (x != x) x = -INFINITY;
-      }
-      v[q] = x;
-    }
-    unsigned taken = 0u;  // bit q: element lane+32q already selected
-    float m0 = 0.f, sum = 0.f;
-    for (int r = 0; r < k; ++r) {
-      float bv = -INFINITY;
-      int bi = 0x7FFFFFFF;
-#pragma unroll
-      for (int q = 0; q < kMaxE / 32; ++q) {
-        const int e = lane + 32 * q;
-        if (e < E && !(taken & (1u << q)) && better_logit(v[q], e, bv, bi)) { bv = v[q]; bi = e; }
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const float ov = __shfl_xor_sync(0xFFFFFFFFu, bv, o);
-        const int oi = __shfl_xor_sync(0xFFFFFFFFu, bi, o);
-        if (better_logit(ov, oi, bv, bi)) { bv = ov; bi = oi; }
-      }
-      if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-      if (r == 0) m0 = bv;
-      const float ex = expf(bv - m0);
-      sum += ex;
-      if (lane == 0) {
-        cs.ids[t * k + r] = bi;
-        cs.w[t * k + r] = ex;
-      }
-    }
-    if (lane == 0)
-      for (int r = 0; r < k; ++r) cs.w[t * k + r] = cs.w[t * k + r] / sum;
+  // ---- loads that depend on nothing, issued first: this thread's entry of the
+  // oldest-slot list (its owner is read next to the residency lookups), the
+  // recency counter and the list length
+  const int my_listed = tid < kMaxU ? p.oldest[tid] : -1;
+  if (tid == 0) {
+    cs.err = MOE_OK;
+    cs.g = *p.st.g;
+    cs.nsel = *p.oldest_n;
   }
   for (int i = tid; i < kMaxE / 32; i += blockDim.x) cs.bits[i] = 0u;
-  if (tid == 0) { cs.err = MOE_OK; cs.g = *p.st.g; }
+
+  // ---- router: one warp per token ------------------------------------------------
+  const int nq = (E + 31) >> 5;
+  for (int t = warp; t < B; t += nwarp) {
+    const float* lg = p.logits + (size_t)t * E;
+    float* aux = p.aux_logits ? p.aux_logits + (size_t)t * E : nullptr;
+    int* ids = cs.ids + t * k;
+    float* w = cs.w + t * k;
+    if (nq <= 1) route_token<1>(lg, E, k, lane, aux, ids, w);
+    else if (nq <= 2) route_token<2>(lg, E, k, lane, aux, ids, w);
+    else if (nq <= 4) route_token<4>(lg, E, k, lane, aux, ids, w);
+    else if (nq <= 8) route_token<8>(lg, E, k, lane, aux, ids, w);
+    else if (nq <= 16) route_token<16>(lg, E, k, lane, aux, ids, w);
+    else route_token<32>(lg, E, k, lane, aux, ids, w);
+  }
   __syncthreads();
 
-  // ---- dedup: U = sorted distinct routed experts ----------------------------
+  // ---- dedup: U = sorted distinct routed experts ----------------------------------
   if (tid < npairs) atomicOr(&cs.bits[cs.ids[tid] >> 5], 1u << (cs.ids[tid] & 31));
   __syncthreads();
   const int nwords = (E + 31) / 32;
@@ -258,45 +313,64 @@ __device__ int control_step(const LayerParams& p, CtrlSmem& cs) {
   if (tid == 0 && n_u > C) cs.err = MOE_ERR_CAPACITY;
   __syncthreads();
 
-  // ---- classify against the residency table ---------------------------------
+  // ---- residency lookups and the owners of the listed slots, in flight together ----
+  const bool state_ok = cs.err == MOE_OK;
+  const int listed0 = cs.nsel;  // -1: the list must be rebuilt
+  int my_slot = -1, my_owner = -1;
+  if (state_ok && tid < n_u) my_slot = p.st.map[p.layer * E + cs.U[tid]];
+  if (state_ok && tid < listed0 && my_listed >= 0 && my_listed < C) my_owner = p.st.owner[my_listed];
+  // one scan for both the grouping offsets (pairs per expert, high half) and
+  // the miss ranks (low half); both totals are at most 256
   int is_miss = 0;
-  if (cs.err == MOE_OK && tid < n_u) {
-    const int s = p.st.map[p.layer * E + cs.U[tid]];
-    cs.slot[tid] = s;
-    is_miss = s < 0;
+  if (state_ok && tid < n_u) {
+    cs.slot[tid] = my_slot;
+    is_miss = my_slot < 0;
     cs.fill[tid] = is_miss;
   }
-  int nmiss;
-  const int mr = block_excl_scan(is_miss, cs.scan, &nmiss);
-  if (tid < n_u) cs.mrank[tid] = mr;
+  int packed_tot;
+  const int packed = block_excl_scan(((tid < n_u ? cs.cnt[tid] : 0) << 16) | is_miss, cs.scan, &packed_tot);
+  const int nmiss = packed_tot & 0xFFFF, mr = packed & 0xFFFF;
+  if (tid < n_u) {
+    cs.off[tid] = packed >> 16;
+    cs.mrank[tid] = mr;
+  }
+  if (tid == 0) cs.off[n_u] = npairs;
+  __syncthreads();
 
-  // ---- victims: first nmiss entries of the oldest-slot list that are no hits --
-  if (cs.err == MOE_OK && nmiss > 0) {
-    int listed = *p.oldest_n;
+  // ---- victims: first nmiss entries of the oldest-slot list that are no hits ------
+  if (state_ok && nmiss > 0) {
+    int listed = listed0;
     const int full = (int)(C < (int64_t)kMaxU ? C : (int64_t)kMaxU);
+    bool rebuilt = false;
     if (listed < 0 || (listed < n_u && listed < full)) {  // rank all C slots again
       const int got = select_oldest(cs, p.st, C, full, E, -1, nullptr);
       listed = got == full ? full : 0;
       for (int i = tid; i < listed; i += blockDim.x) p.oldest[i] = cs.sel_slot[i];
       if (tid == 0) cs.err = got == full ? MOE_OK : MOE_ERR_CUDA;
+      rebuilt = true;
       __syncthreads();
     }
-    int ok = 0, slot = -1;
+    int ok = 0, slot = -1, own = -1;
     if (tid < listed) {
-      slot = p.oldest[tid];
-      unsigned long long kk;
-      ok = slot_key(p.st, C, slot, E, p.layer, cs.bits, &kk) ? 1 : 0;
+      slot = rebuilt ? cs.sel_slot[tid] : my_listed;
+      own = rebuilt ? p.st.owner[slot] : my_owner;
+      ok = 1;
+      if (own >= 0 && own / E == p.layer) {
+        const int e = own % E;
+        if (cs.bits[e >> 5] & (1u << (e & 31))) ok = 0;  // holds one of this call's hits
+      }
     }
-    int tot;
-    const int pos = block_excl_scan(ok, cs.scan, &tot);
-    if (ok && pos < nmiss) cs.victim[pos] = slot;
+    int navail;
+    const int pos = block_excl_scan(ok, cs.scan, &navail);
+    if (ok && pos < nmiss) {
+      cs.victim[pos] = slot;
+      cs.victim_owner[pos] = own;
+    }
     if (tid == 0) {
       cs.nsel = listed;
-      if (tot < nmiss) cs.err = MOE_ERR_CUDA;  // cannot happen with a consistent list
+      if (navail < nmiss) cs.err = MOE_ERR_CUDA;  // cannot happen with a consistent list
     }
     __syncthreads();
-  } else if (tid == 0) {
-    cs.nsel = *p.oldest_n;
   }
   if (cs.err != MOE_OK) {
     if (tid == 0) {
@@ -314,43 +388,26 @@ __device__ int control_step(const LayerParams& p, CtrlSmem& cs) {
     return cs.err;
   }
 
-  // ---- apply: restamp hits, assign victims, keep the undo log --------------------
-  const unsigned long long g0 = cs.g;
+  // ---- the plan (and the fields of the host summary) ----------------------------------
+  const bool host_first = nmiss > 0 && !p.device_fill;
   if (tid < n_u) {
     const int key = p.layer * E + cs.U[tid];
+    const int fill = cs.fill[tid];
+    const int s = fill ? cs.victim[cs.mrank[tid]] : cs.slot[tid];
+    cs.slot[tid] = s;
     plan->u_key[tid] = key;
+    plan->u_expert[tid] = cs.U[tid];
+    plan->u_slot[tid] = s;
+    plan->u_fill[tid] = fill;
     work->key[tid] = key;
+    work->slot[tid] = s;
+    work->fill[tid] = fill;
+    work->evicted[tid] = fill ? cs.victim_owner[cs.mrank[tid]] : -1;
     work->pairs[tid] = cs.cnt[tid];
-    if (!cs.fill[tid]) {
-      const int s = cs.slot[tid];
-      plan->u_old_stamp[tid] = p.st.stamp[s];
-      p.st.stamp[s] = g0 + tid;
-      work->slot[tid] = s;
-      work->evicted[tid] = -1;
-      work->fill[tid] = 0;
-    } else {
-      const int v = cs.victim[cs.mrank[tid]];
-      const int ev = p.st.owner[v];
-      plan->u_old_stamp[tid] = p.st.stamp[v];
-      if (ev >= 0) p.st.map[ev] = -1;
-      p.st.map[key] = v;
-      p.st.owner[v] = key;
-      p.st.stamp[v] = g0 + tid;
-      cs.slot[tid] = v;
-      work->slot[tid] = v;
-      work->evicted[tid] = ev;
-      work->fill[tid] = 1;
-    }
+    if (fill) work->fill_order[cs.mrank[tid]] = tid;
   }
-  if (tid == 0) *p.st.g = g0 + n_u;
-
-  // ---- stable grouping of (token, rank) pairs by expert (block-scan histogram)
-  int tot;
-  const int off = block_excl_scan(tid < n_u ? cs.cnt[tid] : 0, cs.scan, &tot);
-  if (tid < n_u) cs.off[tid] = off;
-  if (tid == 0) cs.off[n_u] = npairs;
-  __syncthreads();
-  if (tid < npairs) {
+  if (tid <= n_u) plan->u_off[tid] = cs.off[tid];
+  if (tid < npairs) {  // stable grouping of the (token, rank) pairs by expert
     const int r = cs.prank[tid];
     int before = 0;
     for (int q = 0; q < tid; ++q) before += (cs.prank[q] == r);
@@ -361,7 +418,7 @@ __device__ int control_step(const LayerParams& p, CtrlSmem& cs) {
     if (p.aux_perm) p.aux_perm[pos] = tid;
     if (p.aux_ids) p.aux_ids[tid] = cs.ids[tid];
     if (p.aux_w) p.aux_w[tid] = cs.w[tid];
-    if (p.aux_slots) p.aux_slots[tid] = cs.slot[r];
+    if (p.aux_slots) p.aux_slots[tid] = cs.fill[r] ? cs.victim[cs.mrank[r]] : cs.slot[r];
   }
   if (p.aux_offsets) {
     for (int e = tid; e <= E; e += blockDim.x) {
@@ -369,20 +426,9 @@ __device__ int control_step(const LayerParams& p, CtrlSmem& cs) {
       p.aux_offsets[e] = r < n_u ? cs.off[r] : npairs;
     }
   }
-  if (tid < n_u) {
-    plan->u_expert[tid] = cs.U[tid];
-    plan->u_slot[tid] = cs.slot[tid];
-    plan->u_fill[tid] = cs.fill[tid];
-  }
-  if (tid <= n_u) plan->u_off[tid] = cs.off[tid];
-  const int is_res = tid < n_u && !cs.fill[tid];
-  int nres;
-  const int rpos = block_excl_scan(is_res, cs.scan, &nres);
-  if (is_res) plan->items[0][rpos] = tid;
-  if (tid < n_u && cs.fill[tid]) {
-    plan->items[1][cs.mrank[tid]] = tid;
-    work->fill_order[cs.mrank[tid]] = tid;
-  }
+  const int nres = n_u - nmiss;  // hits before rank r: r minus the misses before it
+  if (tid < n_u && !cs.fill[tid]) plan->items[0][tid - cs.mrank[tid]] = tid;
+  if (tid < n_u && cs.fill[tid]) plan->items[1][cs.mrank[tid]] = tid;
   if (tid == 0) {
     if (p.has_shared) plan->items[0][nres] = n_u;  // the shared expert is item index n_u
     plan->err = MOE_OK;
@@ -392,19 +438,44 @@ __device__ int control_step(const LayerParams& p, CtrlSmem& cs) {
     plan->n_miss = nmiss;
     plan->n_items[0] = nres + (p.has_shared ? 1 : 0);
     plan->n_items[1] = nmiss;
-    plan->g_before = g0;
+    plan->g_before = cs.g;
     work->err = MOE_OK;
     work->n_u = n_u;
     work->n_miss = nmiss;
-    work->g_before = g0;
+    work->g_before = cs.g;
+    cs.nmiss = nmiss;
   }
-  __threadfence_system();  // each writer publishes its part of the host summary
+  if (host_first) publish_summary(p);  // the host issues this call's copies from it
+  // the CTA barrier orders every thread's plan writes before thread 0's
+  // release store of the plan flag (GPU scope), which the other CTAs acquire
   __syncthreads();
-  if (tid == 0) {
-    __threadfence_system();
-    work->seq = p.seq;
-  }
   return MOE_OK;
+}
+
+// Recency, residency table and undo log of a planned call, written after the
+// other CTAs have been released: hits and fills take stamps g + r in U order,
+// each victim's previous key leaves the table, g advances by |U|.  Then the
+// host summary, unless control_step already published it.
+__device__ void control_commit(const LayerParams& p, CtrlSmem& cs) {
+  const int tid = threadIdx.x, n_u = cs.nu;
+  const unsigned long long g0 = cs.g;
+  if (tid < n_u) {
+    const int s = cs.slot[tid];
+    const int key = p.layer * p.E + cs.U[tid];
+    p.plan->u_old_stamp[tid] = p.st.stamp[s];
+    if (cs.fill[tid]) {
+      const int ev = cs.victim_owner[cs.mrank[tid]];
+      if (ev >= 0) p.st.map[ev] = -1;
+      p.st.map[key] = s;
+      p.st.owner[s] = key;
+    }
+    p.st.stamp[s] = g0 + tid;
+  }
+  if (tid == 0) *p.st.g = g0 + n_u;
+  if (!(cs.nmiss > 0 && !p.device_fill))
+    publish_summary(p);
+  else
+    __syncthreads();
 }
 
 // Drop from the oldest-slot list every slot this call touched (hits and

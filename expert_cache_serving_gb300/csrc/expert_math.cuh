@@ -8,17 +8,25 @@
 
 namespace moe {
 
-// 16-byte load of read-only data (resident slots, shared experts).
+// 16-byte load of read-only streamed weights (resident slots, shared experts,
+// host pool): no L1 allocation and L2 evict-first, so the weight stream does
+// not push the kernel's code and the small cache state out of L2.
 __device__ __forceinline__ uint4 ld_ro16(const void* p) {
   uint4 r;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-               : "l"(p));
+  asm volatile(
+      "{\n .reg .b64 pol;\n createpolicy.fractional.L2::evict_first.b64 pol, 1.0;\n"
+      " ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], pol;\n}\n"
+      : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+      : "l"(p));
   return r;
 }
 __device__ __forceinline__ unsigned short ld_ro2(const void* p) {
   unsigned short r;
-  asm volatile("ld.global.nc.L1::no_allocate.u16 %0, [%1];" : "=h"(r) : "l"(p));
+  asm volatile(
+      "{\n .reg .b64 pol;\n createpolicy.fractional.L2::evict_first.b64 pol, 1.0;\n"
+      " ld.global.nc.L1::no_allocate.L2::cache_hint.u16 %0, [%1], pol;\n}\n"
+      : "=h"(r)
+      : "l"(p));
   return r;
 }
 // Loads of slots being filled while the kernel runs: bypass L1 and the
@@ -40,6 +48,18 @@ __device__ __forceinline__ uint4 ld_w16(const void* p) {
 template <bool FRESH>
 __device__ __forceinline__ unsigned short ld_w2(const void* p) {
   if constexpr (FRESH) return ld_cg2(p); else return ld_ro2(p);
+}
+
+// Shared-memory loads of staged rows.
+__device__ __forceinline__ uint4 lds16(const void* p) {
+  uint4 r;
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "r"(smem_u32(p)));
+  return r;
+}
+__device__ __forceinline__ unsigned short lds2(const void* p) {
+  unsigned short r;
+  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(r) : "r"(smem_u32(p)));
+  return r;
 }
 
 __device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {

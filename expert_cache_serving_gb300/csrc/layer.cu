@@ -35,6 +35,8 @@ struct ItemTable {
   int ntok[kMaxItems];
   int pair0[kMaxItems];      // -1 for the shared expert
   int hbase[kMaxItems + 1];  // running token count in item order
+  int perm[kMaxPairs];       // the plan's grouped pair order, copied once per call
+  float pair_w[kMaxPairs];   // the plan's routing weights, copied once per call
 };
 
 // Items of plan list `which` into tb at position `at` (list 1 from the host
@@ -42,6 +44,11 @@ struct ItemTable {
 __device__ int load_items(const LayerParams& p, const Plan* pl, int which, ItemTable& tb, int at = 0,
                           bool from_pool = false) {
   const int n = pl->n_items[which];
+  if (at == 0 && which == 0)
+    for (int i = threadIdx.x; i < p.B * p.k; i += blockDim.x) {
+      tb.perm[i] = pl->perm[i];
+      tb.pair_w[i] = pl->pair_w[i];
+    }
   for (int i = threadIdx.x; i < n; i += blockDim.x) {
     const int r = pl->items[which][i];
     if (r == pl->n_u) {
@@ -67,22 +74,40 @@ __device__ int load_items(const LayerParams& p, const Plan* pl, int which, ItemT
   return at + n;
 }
 
-// Device-driven fill of the W_down rows [n0, n0 + nrows) of item `it`: copy
-// them from the host pool into the item's slot (each CTA copies its own rows).
+// 16-byte unit v of the W_down rows [n0, n0 + nrows) of record `rec` (codes
+// or values first, then the FP4 scales).  Row bytes and FP4 scale rows are
+// multiples of 16 for every accepted shape (I % 64 == 0; FP4: I % 256 == 0).
 template <int WD>
-__device__ void copy_down_rows(const LayerParams& p, const ItemTable& tb, int it, int n0, int nrows) {
-  const RecView src = rec_view<WD>(tb.rec[it], p.H, p.I);
-  const RecView dst = rec_view<WD>(tb.dst[it], p.H, p.I);
-  const int64_t rb = Fmt<WD>::row_bytes(p.I);
-  const int nv = (int)(nrows * rb / 16);
-  const uint4* s0 = reinterpret_cast<const uint4*>(src.down + (int64_t)n0 * rb);
-  uint4* d0 = reinterpret_cast<uint4*>(const_cast<uint8_t*>(dst.down) + (int64_t)n0 * rb);
-  for (int v = threadIdx.x; v < nv; v += blockDim.x) d0[v] = ld_ro16(s0 + v);
-  if (WD == MOE_FP4) {
-    const int ns = nrows * (p.I / 16) / 16;
-    const uint4* s1 = reinterpret_cast<const uint4*>(src.down_sc + (int64_t)n0 * (p.I / 16));
-    uint4* d1 = reinterpret_cast<uint4*>(const_cast<uint8_t*>(dst.down_sc) + (int64_t)n0 * (p.I / 16));
-    for (int v = threadIdx.x; v < ns; v += blockDim.x) d1[v] = ld_ro16(s1 + v);
+__device__ __forceinline__ const uint8_t* down_unit(const uint8_t* rec, int H, int I, int n0, int nv, int v) {
+  const RecView r = rec_view<WD>(rec, H, I);
+  if (v < nv) return r.down + (int64_t)n0 * Fmt<WD>::row_bytes(I) + (int64_t)v * 16;
+  return r.down_sc + (int64_t)n0 * (I / 16) + (int64_t)(v - nv) * 16;
+}
+
+// Device-driven fill of this CTA's W_down rows [n0, n0 + nrows) of items
+// [ib, ie): copy them from the host pool into the items' slots, with eight
+// independent 16-byte loads in flight per thread (host-link latency bound).
+template <int WD>
+__device__ void copy_down_rows(const LayerParams& p, const ItemTable& tb, int ib, int ie, int n0, int nrows) {
+  constexpr int U = 8;
+  const int H = p.H, I = p.I;
+  const int nv = (int)(nrows * Fmt<WD>::row_bytes(I) / 16);
+  const int per = nv + (WD == MOE_FP4 ? nrows * (I / 16) / 16 : 0);
+  const int total = (ie - ib) * per;
+  for (int v0 = threadIdx.x; v0 < total; v0 += U * blockDim.x) {
+    uint4 buf[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int v = v0 + u * (int)blockDim.x;
+      if (v < total) buf[u] = ld_ro16(down_unit<WD>(tb.rec[ib + v / per], H, I, n0, nv, v % per));
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int v = v0 + u * (int)blockDim.x;
+      if (v < total)
+        *reinterpret_cast<uint4*>(const_cast<uint8_t*>(down_unit<WD>(tb.dst[ib + v / per], H, I, n0, nv, v % per))) =
+            buf[u];
+    }
   }
 }
 
@@ -95,7 +120,7 @@ __device__ __forceinline__ void item_token(const LayerParams& p, const Plan* pl,
     *hrow = p.h_shared_row0 + q;
     *j = p.k;
   } else {
-    const int pair = pl->perm[p0 + q];
+    const int pair = tb.perm[p0 + q];
     *t = pair / p.k;
     *hrow = pair;
     *j = pair % p.k;
@@ -196,18 +221,43 @@ __device__ void phase1(const LayerParams& p, const Plan* pl, const ItemTable& tb
   }
 }
 
+// Where W_down row `row` (and its FP4 scales) of item gi is read: its record,
+// or, when STAGED, staged item j of this CTA in shared memory.
+template <int WD, bool STAGED>
+__device__ __forceinline__ void down_row(const ItemTable& tb, int j, int gi, int row, int n0, int nrows, int H, int I,
+                                         const uint8_t* stage, int pitch, const uint8_t** drow, const uint8_t** dsc) {
+  const int64_t rb = Fmt<WD>::row_bytes(I);
+  if constexpr (STAGED) {
+    const uint8_t* base = stage + (int64_t)j * pitch;
+    *drow = base + (int64_t)(row - n0) * rb;
+    *dsc = base + (int64_t)nrows * rb + (int64_t)(row - n0) * (I / 16);
+  } else {
+    const RecView v = rec_view<WD>(tb.rec[gi], H, I);
+    *drow = v.down + (int64_t)row * rb;
+    *dsc = (WD == MOE_FP4) ? v.down_sc + (int64_t)row * (I / 16) : nullptr;
+  }
+}
+template <bool FRESH, bool STAGED>
+__device__ __forceinline__ uint4 ld_down16(const uint8_t* q) {
+  if constexpr (STAGED) return lds16(q); else return ld_w16<FRESH>(q);
+}
+template <bool FRESH, bool STAGED>
+__device__ __forceinline__ unsigned short ld_down2(const uint8_t* q) {
+  if constexpr (STAGED) return lds2(q); else return ld_w2<FRESH>(q);
+}
+
 // W_down rows [n0, n0 + nrows) of items [ib, ie) -> os[row][t][j].
-template <int WD, int MAXT, bool FRESH>
+// STAGED: the rows of item ib + j sit in shared memory at stage + j * pitch
+// (rows n0.., then their FP4 scales), copied there during phase 1.
+template <int WD, int MAXT, bool FRESH, bool STAGED = false>
 __device__ void phase2(const LayerParams& p, const Plan* pl, const ItemTable& tb, int ib, int ie, int n0, int nrows,
-                       float* hs, float* os) {
+                       float* hs, float* os, const uint8_t* stage = nullptr, int pitch = 0) {
   using F = Fmt<WD>;
   constexpr int EPC = F::kElemsPerChunk;
-  constexpr int R2 = 4;    // rows in flight per warp
-  constexpr int UNR2 = 2;  // 16-byte chunks per lane held in registers
+  constexpr int kLanesPerRow = 8, kRowsPerWarp = 32 / kLanesPerRow, kChunksPerLane = MAXT >= 16 ? 4 : 8;
   const int H = p.H, I = p.I, B = p.B, k = p.k, lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int ostride = B * (k + 1);
   const int nchunks = I / EPC;
-  const int64_t rb = F::row_bytes(I);
   int g0 = ib;
   while (g0 < ie) {
     int g1 = g0, used = 0;
@@ -229,67 +279,69 @@ __device__ void phase2(const LayerParams& p, const Plan* pl, const ItemTable& tb
         s_hrow[rr] = hr;
       }
       __syncthreads();
-      const int per = I / 4;
-      for (int e = threadIdx.x; e < rows * per; e += blockDim.x) {
-        const int rr = e / per, c4 = e % per;
-        reinterpret_cast<float4*>(hs + (int64_t)rr * I)[c4] =
-            __ldcg(reinterpret_cast<const float4*>(p.h + (int64_t)s_hrow[rr] * I) + c4);
+      const int per = I / 4, n4 = rows * per;
+      for (int e0 = threadIdx.x; e0 < n4; e0 += 4 * blockDim.x) {  // four loads in flight per thread
+        float4 v[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int e = e0 + u * (int)blockDim.x;
+          if (e < n4) v[u] = __ldcg(reinterpret_cast<const float4*>(p.h + (int64_t)s_hrow[e / per] * I) + e % per);
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int e = e0 + u * (int)blockDim.x;
+          if (e < n4) reinterpret_cast<float4*>(hs + (int64_t)(e / per) * I)[e % per] = v[u];
+        }
       }
     }
     __syncthreads();
+    // 8 lanes per row, 4 rows per warp: lane l of row group g reads chunks
+    // l, l + 8, l + 16, ... of unit u0 + g in increasing order (8 in flight),
+    // then the group's 8 partial sums reduce by a fixed butterfly
+    const int grp = lane / kLanesPerRow, gl = lane % kLanesPerRow;
     const int nunits = (g1 - g0) * nrows;
-    for (int u0 = warp * R2; u0 < nunits; u0 += kWarps * R2) {
-      uint4 w[R2][UNR2];
-      unsigned short sc[R2][UNR2];
+    for (int u0 = warp * kRowsPerWarp; u0 < nunits; u0 += kWarps * kRowsPerWarp) {
+      const int unit = u0 + grp;
+      const bool live = unit < nunits;
+      const int gi = live ? g0 + unit / nrows : g0, row = live ? n0 + unit % nrows : n0;
+      const uint8_t *drow = nullptr, *dsc = nullptr;
+      if (live) down_row<WD, STAGED>(tb, gi - ib, gi, row, n0, nrows, H, I, stage, pitch, &drow, &dsc);
+      const int hbase = tb.hbase[gi] - tb.hbase[g0];
+      const int ntok = live ? tb.ntok[gi] : 0;
+      float acc[MAXT];
 #pragma unroll
-      for (int r = 0; r < R2; ++r) {
-        const int unit = u0 + r;
-        if (unit < nunits) {
-          const int gi = g0 + unit / nrows, row = n0 + unit % nrows;
-          const RecView v = rec_view<WD>(tb.rec[gi], H, I);
-          const uint8_t* drow = v.down + (int64_t)row * rb;
-          const uint8_t* dsc = (WD == MOE_FP4) ? v.down_sc + (int64_t)row * (I / 16) : nullptr;
+      for (int q = 0; q < MAXT; ++q) acc[q] = 0.f;
+      for (int c0 = 0; c0 < nchunks; c0 += kLanesPerRow * kChunksPerLane) {
+        uint4 w[kChunksPerLane];
+        unsigned short sc[kChunksPerLane];
 #pragma unroll
-          for (int u = 0; u < UNR2; ++u) {
-            const int c = lane + 32 * u;
-            if (c < nchunks) {
-              w[r][u] = ld_w16<FRESH>(drow + (int64_t)c * 16);
-              sc[r][u] = (WD == MOE_FP4) ? ld_w2<FRESH>(dsc + 2 * c) : (unsigned short)0;
-            }
+        for (int u = 0; u < kChunksPerLane; ++u) {
+          const int c = c0 + gl + kLanesPerRow * u;
+          if (live && c < nchunks) {
+            w[u] = ld_down16<FRESH, STAGED>(drow + (int64_t)c * 16);
+            sc[u] = (WD == MOE_FP4) ? ld_down2<FRESH, STAGED>(dsc + 2 * c) : (unsigned short)0;
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < kChunksPerLane; ++u) {
+          const int c = c0 + gl + kLanesPerRow * u;
+          if (live && c < nchunks) {
+#pragma unroll
+            for (int q = 0; q < MAXT; ++q)
+              if (q < ntok) acc[q] += chunk_dot<WD, float>(w[u], sc[u], hs + (int64_t)(hbase + q) * I + (int64_t)c * EPC);
           }
         }
       }
 #pragma unroll
-      for (int r = 0; r < R2; ++r) {
-        const int unit = u0 + r;
-        if (unit >= nunits) continue;
-        const int gi = g0 + unit / nrows, row = n0 + unit % nrows;
-        const int hbase = tb.hbase[gi] - tb.hbase[g0];
-        const int ntok = tb.ntok[gi];
-#pragma unroll
-        for (int q = 0; q < MAXT; ++q) {
-          if (q < ntok) {
-            const float* hrow = hs + (int64_t)(hbase + q) * I;
-            float acc = 0.f;
-#pragma unroll
-            for (int u = 0; u < UNR2; ++u) {
-              const int c = lane + 32 * u;
-              if (c < nchunks) acc += chunk_dot<WD, float>(w[r][u], sc[r][u], hrow + (int64_t)c * EPC);
-            }
-            for (int c = lane + 32 * UNR2; c < nchunks; c += 32) {  // rows longer than 32*UNR2 chunks
-              const RecView v = rec_view<WD>(tb.rec[gi], H, I);
-              const uint4 ww = ld_w16<FRESH>(v.down + (int64_t)row * rb + (int64_t)c * 16);
-              const unsigned short ss =
-                  (WD == MOE_FP4) ? ld_w2<FRESH>(v.down_sc + (int64_t)row * (I / 16) + 2 * c) : (unsigned short)0;
-              acc += chunk_dot<WD, float>(ww, ss, hrow + (int64_t)c * EPC);
-            }
-            acc = warp_sum(acc);
-            if (lane == 0) {
-              int t, hr, j;
-              item_token(p, pl, tb, gi, q, &t, &hr, &j);
-              os[(row - n0) * ostride + t * (k + 1) + j] = acc;
-            }
-          }
+      for (int q = 0; q < MAXT; ++q) {
+        float a = acc[q];
+        a += __shfl_xor_sync(0xFFFFFFFFu, a, 4);
+        a += __shfl_xor_sync(0xFFFFFFFFu, a, 2);
+        a += __shfl_xor_sync(0xFFFFFFFFu, a, 1);
+        if (live && gl == 0 && q < ntok) {
+          int t, hr, j;
+          item_token(p, pl, tb, gi, q, &t, &hr, &j);
+          os[(row - n0) * ostride + t * (k + 1) + j] = a;
         }
       }
     }
@@ -316,13 +368,15 @@ __global__ void __launch_bounds__(kThreads, 1) layer_kernel(LayerParams p) {
   // ---- 0. control | activations and the shared expert's gate/up rows --------
   if (p.tl && blockIdx.x == 1 && threadIdx.x == 0) p.tl[0] = globaltimer_ns();
   if (ctrl) {
-    const int cst = control_step(p, cs);
-    __syncthreads();
+    const int cst = control_step(p, cs);  // ends with a CTA barrier after the plan writes
     if (threadIdx.x == 0) {
       st_release_u32(p.plan_flag, p.seq);
       if (p.tl) p.tl[10] = globaltimer_ns();
     }
-    if (cst == MOE_OK) compact_oldest(p, cs);
+    if (cst == MOE_OK) {
+      control_commit(p, cs);
+      compact_oldest(p, cs);
+    }
     if (p.tl && threadIdx.x == 0) p.tl[11] = globaltimer_ns();
   }
   {
@@ -342,7 +396,7 @@ __global__ void __launch_bounds__(kThreads, 1) layer_kernel(LayerParams p) {
     __syncthreads();
     phase1<WD, MAXT, false>(p, p.plan, tb, 0, 1, 1, G - 1, xs);
   }
-  if (!ctrl && wait_flag(p.plan_flag, p.seq, p.err) != 0) return;
+  if (!ctrl && wait_flag(p.plan_flag, p.seq, p.err, 5000000000ull, 32) != 0) return;
   __syncthreads();
   const bool rec = p.tl && blockIdx.x == 1 && threadIdx.x == 0;
   if (rec) p.tl[1] = globaltimer_ns();
@@ -355,31 +409,59 @@ __global__ void __launch_bounds__(kThreads, 1) layer_kernel(LayerParams p) {
     // device-driven fills: pull each missed record from the host pool, use it
     // for this call and store it in its slot; W_down rows by the CTA that owns them
     const int n_all = load_items(p, pl, 1, tb, n_res, true);
-    for (int it = n_res; it < n_all; ++it) copy_down_rows<WD>(p, tb, it, n0, nrows);
+    copy_down_rows<WD>(p, tb, n_res, n_all, n0, nrows);
     if (!ctrl) phase1<WD, MAXT, false, true>(p, pl, tb, n_res, n_all, 1, G - 1, xs);
   }
-  if (threadIdx.x < n_res && nrows > 0) {  // this CTA's W_down rows of every resident expert -> L2
-    const RecView v = rec_view<WD>(tb.rec[threadIdx.x], H, p.I);
-    const int64_t rb = Fmt<WD>::row_bytes(p.I);
-    prefetch_l2(v.down + (int64_t)n0 * rb, (uint32_t)(nrows * rb));
-    if (WD == MOE_FP4) prefetch_l2(v.down_sc + (int64_t)n0 * (p.I / 16), (uint32_t)(nrows * (p.I / 16)));
+  // this CTA's W_down rows of the resident experts: the first n_stage items
+  // into shared memory by bulk copies completing on s_stage, the rest into L2
+  __shared__ __align__(8) uint64_t s_stage;
+  const int n_stage = nrows > 0 ? min(n_res, p.stage_items) : 0;
+  const uint8_t* stage = smem + p.stage_off;
+  {
+    const int64_t rb = Fmt<WD>::row_bytes(p.I), sb = (WD == MOE_FP4) ? p.I / 16 : 0;
+    if (threadIdx.x == 0 && n_stage > 0) {
+      mbar_init(&s_stage, 1);
+      fence_mbar_init();
+      mbar_expect_tx(&s_stage, (uint32_t)(n_stage * nrows * (rb + sb)));
+      for (int j = 0; j < n_stage; ++j) {
+        const RecView v = rec_view<WD>(tb.rec[j], H, p.I);
+        uint8_t* dst = smem + p.stage_off + (int64_t)j * p.stage_pitch;
+        bulk_g2s(dst, v.down + (int64_t)n0 * rb, (uint32_t)(nrows * rb), &s_stage);
+        if (WD == MOE_FP4) bulk_g2s(dst + nrows * rb, v.down_sc + (int64_t)n0 * sb, (uint32_t)(nrows * sb), &s_stage);
+      }
+    }
+    if ((int)threadIdx.x >= n_stage && (int)threadIdx.x < n_res && nrows > 0) {
+      const RecView v = rec_view<WD>(tb.rec[threadIdx.x], H, p.I);
+      prefetch_l2(v.down + (int64_t)n0 * rb, (uint32_t)(nrows * rb));
+      if (WD == MOE_FP4) prefetch_l2(v.down_sc + (int64_t)n0 * sb, (uint32_t)(nrows * sb));
+    }
   }
   if (!ctrl) phase1<WD, MAXT, false>(p, pl, tb, 0, n_res - p.has_shared, 1, G - 1, xs);
   if (rec) p.tl[2] = globaltimer_ns();
-  if (!grid_barrier(p.bar, p.bar_base + (unsigned long long)G, p.err)) return;
+  const bool bar_ok = grid_barrier(p.bar, p.bar_base + (unsigned long long)G, p.err);
+  if (n_stage > 0 && !mbar_wait(&s_stage, 0)) {  // the staging copies never leave this CTA in flight
+    if (threadIdx.x == 0) atomicExch(p.err, MOE_ERR_TIMEOUT);
+    mbar_wait(&s_stage, 0);
+    return;
+  }
+  if (!bar_ok) return;
   if (rec) p.tl[3] = globaltimer_ns();
 
   // ---- 2. W_down rows of the resident experts --------------------------------------
   const int ostride = B * (k + 1);
   for (int i = threadIdx.x; i < nrows * ostride; i += blockDim.x) os[i] = 0.f;
-  phase2<WD, MAXT, false>(p, pl, tb, 0, n_res, n0, nrows, hs, os);
+  phase2<WD, MAXT, false, true>(p, pl, tb, 0, n_stage, n0, nrows, hs, os, stage, p.stage_pitch);
+  phase2<WD, MAXT, false>(p, pl, tb, n_stage, n_res, n0, nrows, hs, os);
   if (rec) p.tl[4] = globaltimer_ns();
 
   // ---- 3. fills, each as soon as its copy has landed -------------------------------
   const int nf = pl->n_items[1];
   int fill_err = 0;
   if (nf > 0 && p.device_fill) {
-    // device-driven fills were pulled from the pool in phase 1 (see below)
+    // device-driven fills: this CTA copied its own W_down rows of every fill
+    // into the slots in phase 1, so they are read there, not over the link
+    for (int it = n_res + (int)threadIdx.x; it < n_res + nf; it += blockDim.x) tb.rec[it] = tb.dst[it];
+    __syncthreads();
     phase2<WD, MAXT, true>(p, pl, tb, n_res, n_res + nf, n0, nrows, hs, os);
   } else if (nf > 0) {
     load_items(p, pl, 1, tb);
@@ -413,7 +495,7 @@ __global__ void __launch_bounds__(kThreads, 1) layer_kernel(LayerParams p) {
     const int nl = e / B, t = e % B, n = n0 + nl;
     const float* o = os + nl * ostride + t * (k + 1);
     float acc = 0.f;
-    for (int j = 0; j < k; ++j) acc = fmaf(pl->pair_w[t * k + j], o[j], acc);
+    for (int j = 0; j < k; ++j) acc = fmaf(tb.pair_w[t * k + j], o[j], acc);
     if (p.has_shared) acc += o[k];
     if constexpr (WD == MOE_FP32)
       reinterpret_cast<float*>(p.y)[(int64_t)t * H + n] = acc;

@@ -10,7 +10,7 @@ namespace moe {
 struct LayerParams {
   int L, E, k, B, layer, H, I;
   int64_t C;
-  int M;                      // length of the precomputed victim order (max_tokens * k)
+  int M;                      // max_tokens * k
   const float* logits;        // [B][E]
   CacheDev st;
   Plan* plan;
@@ -33,6 +33,9 @@ struct LayerParams {
   void* y;                    // [B][H]
   int smem_h_floats;          // capacity of the shared-memory h buffer
   int rows_per_cta_max;
+  int stage_items;            // resident items whose W_down rows a CTA stages in shared memory
+  int stage_pitch;            // bytes per staged item (rows_per_cta_max rows, then their FP4 scales)
+  int stage_off;              // byte offset of the staging area in dynamic shared memory
   int32_t* oldest;            // [kMaxU] oldest slots, ascending key
   int* oldest_n;              // entries in it, -1 if invalid
   unsigned long long* tl;     // optional phase timestamps of this call [12] (profiling)
