@@ -293,12 +293,55 @@ def run_native(args, w):
         e2e_ms = float(t.item())
     e2e_value = w.B * K_e2e * world / (e2e_ms / 1e3) if K_e2e else None
 
+    # ablation: the same timed steps with the other fill mechanism (copy
+    # engine + stream flags vs the kernel pulling misses over the host link)
+    ablation = None
+    if not args.no_ablation:
+        other = "device" if args.fill_mode == "copy" else "copy"
+        cache.close()
+        cache_b = runner.Cache(w, pool, shared)
+        mc.moe_cache_set_fill_mode(cache_b.handle, mc.MOE_FILL_DEVICE if other == "device" else mc.MOE_FILL_COPY)
+
+        def step_b(s):
+            for l in range(w.L):
+                st = cache_b.forward(l, x_dev[s, l], lg_dev[s, l], y_dev[s, l], w.B, stream=stream)
+                if st != mc.MOE_OK:
+                    raise mc.MoeError(st, "moe_layer_forward")
+
+        for s in range(W):
+            step_b(s)
+        torch.cuda.synchronize()
+        mc.moe_cache_reset_stats(cache_b.handle)
+        mc.moe_cache_set_profiling(cache_b.handle, 1)
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a0.record(stream)
+        for s in range(W, W + K):
+            step_b(s)
+        a1.record(stream)
+        torch.cuda.synchronize()
+        ms_b = a0.elapsed_time(a1)
+        mc.moe_cache_set_profiling(cache_b.handle, False)
+        sb = mc.moe_cache_stats(cache_b.handle)
+        ablation = {"fill_mode": other, "value": w.B * K * world / (ms_b / 1e3), "unit": "tok/s (decode)",
+                    "ms_per_step": ms_b / K,
+                    "hit_only_avg_launch_us": sb["hit_only_ms"] * 1e3 / max(1, sb["hit_only_timed"]),
+                    "all_launches_avg_us": sb["layer_ms"] * 1e3 / max(1, sb["layer_timed"]),
+                    "hit_rate": sb["hits"] / max(1, sb["hits"] + sb["misses"]),
+                    "note": "same trace steps and pool, measured after the main leg in the same process"}
+        cache = cache_b
+
     # roofline of the dominant kernel (the layer kernel): algorithmic bytes =
     # every expert record it streams once (S bytes each).  Calls with fills
     # also wait for the host link inside the kernel, so the HBM figure is
     # taken over the launches of calls without fills; the link-inclusive
     # bound covers every call.
     hit_bytes = stats["hit_only_records"] * S
+    # DRAM traffic of the layer kernel from the committed ncu capture
+    # (profiles/decode_layer_kernel_small_full.md: same expert shape, 8
+    # resident records read 50.508 MB + wrote 0.321 MB), scaled per record to
+    # this run's records per hit-only launch; valid for this expert shape only
+    recs_per_launch = stats["hit_only_records"] / max(1, stats["hit_only_timed"])
+    traffic = (50.508288e6 + 0.320512e6) / 8 * recs_per_launch if S == 6291456 else None
     hit_s = stats["hit_only_ms"] / 1e3
     achieved = hit_bytes / hit_s / 1e9 if hit_s > 0 else None
     peak = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
@@ -320,7 +363,8 @@ def run_native(args, w):
         "routed_pair_hit_rate": stats["routed_pair_hits"] / stats["routed_pairs"] if stats["routed_pairs"] else None,
         "fill_GB_per_token": stats["bytes_filled"] / 1e9 / (w.B * K),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak if achieved else None, "traffic": None,
+                     "frac": achieved / peak if achieved else None, "traffic": traffic,
+                     "algorithmic_bytes_per_launch": recs_per_launch * S,
                      "kernel": "layer_kernel (calls without fills)", "peak_kind": peak_kind + " hbm_gbs (copy)",
                      "launches": stats["hit_only_timed"],
                      "avg_launch_us": stats["hit_only_ms"] * 1e3 / max(1, stats["hit_only_timed"]),
@@ -331,6 +375,7 @@ def run_native(args, w):
                  "note": "tok/s bound = max(expert bytes / HBM peak, fill bytes / B_P) over the timed steps"},
         "e2e": {"value": e2e_value, "unit": "tok/s (decode)", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "steps": K_e2e},
+        "ablation": ablation,
         "gpu_launches": stats["layer_launches"],
         "phase_us": phases,
         "host_us_per_call": {"wait_for_miss_list": stats["host_wait_us"] / max(1, stats["calls"]),
@@ -443,6 +488,7 @@ def main():
     ap.add_argument("--cpu-tokens", type=int, default=3)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile", type=int, default=1, help="1: CUDA events per launch; 2: also phase timestamps")
+    ap.add_argument("--no-ablation", action="store_true", help="skip the timed pass with the other fill mode")
     ap.add_argument("--fill-mode", default="copy", choices=["copy", "device"],
                     help="copy: host-issued cudaMemcpyAsync fills (default); device: the kernel pulls misses itself")
     args = ap.parse_args()

@@ -192,6 +192,7 @@ struct moe_cache {
   HostWork* h_work = nullptr;
   HostWork* d_work = nullptr;
   cudaStream_t copy = nullptr;
+  cudaStream_t copy2 = nullptr;  // internal second copy stream: fills alternate between the two
   bool own_copy = false;
   cudaStream_t last_stream = nullptr;
   cudaEvent_t e_pre = nullptr, e_done = nullptr;
@@ -305,6 +306,7 @@ static void free_all(moe_cache* c) {
     cudaEventDestroy(t.b);
   }
   if (c->own_copy && c->copy) cudaStreamDestroy(c->copy);
+  if (c->copy2) cudaStreamDestroy(c->copy2);
   c->slots.release();
   delete c;
 }
@@ -409,6 +411,7 @@ extern "C" moe_status moe_cache_create(const moe_model_desc* desc, const void* h
     if ((s = cu(cudaStreamCreateWithFlags(&c->copy, cudaStreamNonBlocking), "copy stream"))) return bail(s);
     c->own_copy = true;
   }
+  if ((s = cu(cudaStreamCreateWithFlags(&c->copy2, cudaStreamNonBlocking), "copy stream"))) return bail(s);
   // the copy stream signals landed fills with stream memory writes: check they work here
   {
     Drv& dr = drv();
@@ -545,6 +548,7 @@ static moe_status wait_summary(moe_cache* c, uint32_t seq, cudaStream_t s) {
 static moe_status recover_after_timeout(moe_cache* c, cudaStream_t s) {
   CU_TRY(cudaStreamSynchronize(s));
   CU_TRY(cudaStreamSynchronize(c->copy));
+  CU_TRY(cudaStreamSynchronize(c->copy2));
   CU_TRY(cudaMemcpy(&c->bar_base, c->d_bar, sizeof(unsigned long long), cudaMemcpyDeviceToHost));
   CU_TRY(cudaMemset(c->d_oldest_n, 0xFF, sizeof(int)));
   *(volatile int*)c->h_err = 0;
@@ -649,10 +653,13 @@ extern "C" moe_status moe_layer_forward_ex(moe_cache_t c, int32_t layer, const v
     if (c->pending.size() > 4096) drain_pending(c, false);
   }
   if (n_miss > 0 && !p.device_fill) {
-    // one copy per half record on the copy stream, each followed by a flag the
-    // kernel waits on; the copies start once every earlier call has finished
+    // one copy per half record, each followed by a flag the kernel waits on;
+    // records alternate between two copy streams so that one stream's flag
+    // write and next-copy start overlap the other's transfer; the copies start
+    // once every earlier call has finished
     Drv& dr = drv();
     CU_TRY(cudaStreamWaitEvent(c->copy, c->e_pre, 0));
+    if (n_miss > 1) CU_TRY(cudaStreamWaitEvent(c->copy2, c->e_pre, 0));
     const int64_t part1 = first_part_bytes(d), part2 = c->S - part1;
     unsigned* flags = c->d_flags + 1;
     int f = 0, half = 0;
@@ -669,14 +676,15 @@ extern "C" moe_status moe_layer_forward_ex(moe_cache_t c, int32_t layer, const v
           break;
         }
         const int64_t off = half ? part1 : 0, len = half ? part2 : part1;
-        cudaError_t ce = cudaMemcpyAsync(dst + off, src + off, len, cudaMemcpyHostToDevice, c->copy);
+        cudaStream_t cs = (f & 1) ? c->copy2 : c->copy;
+        cudaError_t ce = cudaMemcpyAsync(dst + off, src + off, len, cudaMemcpyHostToDevice, cs);
         if (ce != cudaSuccess) {
           failed = true;
           why = cudaGetErrorString(ce);
           cudaGetLastError();
           break;
         }
-        if (dr.streamWriteValue32((CUstream)c->copy, (CUdeviceptr)(flags + half * kMaxU + f), seq, 0) !=
+        if (dr.streamWriteValue32((CUstream)cs, (CUdeviceptr)(flags + half * kMaxU + f), seq, 0) !=
             CUDA_SUCCESS) {
           failed = true;
           why = "cuStreamWriteValue32 failed";
@@ -740,7 +748,8 @@ extern "C" moe_status moe_cache_resize(moe_cache_t c, int64_t n_slots, void* str
     return fail(MOE_ERR_INVALID_ARG, "n_slots %lld outside 0..%lld", (long long)n_slots, (long long)c->C_max);
   if (c->have_done && cudaEventQuery(c->e_done) == cudaErrorNotReady)
     return fail(MOE_ERR_BUSY, "a forward of this cache is still running on the GPU");
-  if (cudaStreamQuery(c->copy) == cudaErrorNotReady) return fail(MOE_ERR_BUSY, "fills still in flight");
+  if (cudaStreamQuery(c->copy) == cudaErrorNotReady || cudaStreamQuery(c->copy2) == cudaErrorNotReady)
+    return fail(MOE_ERR_BUSY, "fills still in flight");
   cudaGetLastError();
   cudaStream_t s = (cudaStream_t)stream;
   const int64_t C = c->C, LE = (int64_t)c->d.L * c->d.E;

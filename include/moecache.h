@@ -147,7 +147,10 @@ size_t moe_record_bytes(const moe_model_desc* desc);
  * n_slots: initial capacity C (>= 0).  max_slots: upper bound for resizes
  *   (0 means L*E); device virtual address space for max_slots records is
  *   reserved up front and physical memory is mapped for the first C only.
- * copy_stream: stream for fills (NULL: the library creates one).
+ * copy_stream: stream for fills (NULL: the library creates one).  The
+ *   library also creates one internal copy stream; copy-mode fill records
+ *   alternate between the two, both ordered after the work that precedes
+ *   each layer call on the compute stream.
  * Errors: MOE_ERR_INVALID_ARG (shapes, pointers, unpinned pool),
  *   MOE_ERR_OOM, MOE_ERR_CUDA.  On error *out is NULL. */
 moe_status moe_cache_create(const moe_model_desc* desc, const void* host_pool, const void* shared_dev,
