@@ -230,7 +230,6 @@ struct moe_cache {
     float* w = nullptr;
     void *xp = nullptr, *hp = nullptr;
     float* op = nullptr;
-    uint8_t* wb = nullptr;  // bf16 staging of a layer's FP4 records (+ shared expert)
     cudaEvent_t loaded[2] = {nullptr, nullptr}, consumed[2] = {nullptr, nullptr}, start = nullptr;
     struct Timed {
       cudaEvent_t a, b;
@@ -297,7 +296,7 @@ static void free_all(moe_cache* c) {
   }
   for (cudaEvent_t e : c->ev_pool) cudaEventDestroy(e);
   for (void* p : {(void*)c->pf.ids, (void*)c->pf.cnt, (void*)c->pf.base, (void*)c->pf.offsets, (void*)c->pf.pos,
-                  (void*)c->pf.perm, (void*)c->pf.w, c->pf.xp, c->pf.hp, (void*)c->pf.op, (void*)c->pf.wb})
+                  (void*)c->pf.perm, (void*)c->pf.w, c->pf.xp, c->pf.hp, (void*)c->pf.op})
     if (p) cudaFree(p);
   for (cudaEvent_t e : {c->pf.loaded[0], c->pf.loaded[1], c->pf.consumed[0], c->pf.consumed[1], c->pf.start})
     if (e) cudaEventDestroy(e);
@@ -939,15 +938,16 @@ extern "C" moe_status moe_cache_inject_fill_failure(moe_cache_t c, int32_t after
 
 // ---------------------------------------------------------------------- prefill --
 static moe_status encode_map(CUtensorMap* m, const void* base, int rank, const uint64_t* dims, const uint64_t* strides,
-                             const uint32_t* box) {
+                             const uint32_t* box, CUtensorMapDataType dtype = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                             CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
   Drv& d = drv();
   cuuint64_t gd[3], gs[2];
   cuuint32_t bx[3], es[3] = {1, 1, 1};
   for (int i = 0; i < rank; ++i) { gd[i] = dims[i]; bx[i] = box[i]; }
   for (int i = 0; i + 1 < rank; ++i) gs[i] = strides[i];
-  const CUresult r = d.tensorMapEncodeTiled(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), gd, gs,
-                                            bx, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  const CUresult r = d.tensorMapEncodeTiled(m, dtype, rank, const_cast<void*>(base), gd, gs, bx, es,
+                                            CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? MOE_OK : fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
 }
 
@@ -964,6 +964,37 @@ static moe_status map_weights(CUtensorMap* m, const void* base, int n, int rows,
   const uint64_t strides[2] = {(uint64_t)K * 2, (uint64_t)rec_stride};
   const uint32_t box[3] = {64, 128, 1};
   return encode_map(m, base, 3, dims, strides, box);
+}
+
+// FP4 weights of n records: e2m1 codes [n][rows][K/2] bytes, boxes of 128
+// rows x 32 bytes (one 64-element K-step); e4m3 scales [n][rows][K/16], boxes
+// of 128 rows x 16 bytes (four K-steps).  Row strides K/2 and K/16 are
+// multiples of 16 for every accepted FP4 shape (H, I multiples of 256).
+static moe_status map_fp4_codes(CUtensorMap* m, const void* base, int n, int rows, int K, int64_t rec_stride) {
+  const uint64_t dims[3] = {(uint64_t)K / 2, (uint64_t)rows, (uint64_t)n};
+  const uint64_t strides[2] = {(uint64_t)K / 2, (uint64_t)rec_stride};
+  const uint32_t box[3] = {32, 128, 1};
+  return encode_map(m, base, 3, dims, strides, box, CU_TENSOR_MAP_DATA_TYPE_UINT8, CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+static moe_status map_fp4_scales(CUtensorMap* m, const void* base, int n, int rows, int K, int64_t rec_stride) {
+  const uint64_t dims[3] = {(uint64_t)K / 16, (uint64_t)rows, (uint64_t)n};
+  const uint64_t strides[2] = {(uint64_t)K / 16, (uint64_t)rec_stride};
+  const uint32_t box[3] = {16, 128, 1};
+  return encode_map(m, base, 3, dims, strides, box, CU_TENSOR_MAP_DATA_TYPE_UINT8, CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+
+// The four weight maps of one FP4 record range (gate/up codes and scales,
+// down codes and scales), record layout gate codes | up codes | gate scales |
+// up scales | down codes | down scales.
+struct Fp4Maps {
+  CUtensorMap gu_c, gu_s, dn_c, dn_s;
+};
+static moe_status map_fp4_layer(Fp4Maps* m, const uint8_t* base, int n, int H, int I, int64_t S) {
+  const int64_t HI = (int64_t)H * I;
+  if (moe_status e = map_fp4_codes(&m->gu_c, base, n, 2 * I, H, S)) return e;
+  if (moe_status e = map_fp4_scales(&m->gu_s, base + HI, n, 2 * I, H, S)) return e;
+  if (moe_status e = map_fp4_codes(&m->dn_c, base + HI + HI / 8, n, H, I, S)) return e;
+  return map_fp4_scales(&m->dn_s, base + HI + HI / 8 + HI / 2, n, H, I, S);
 }
 
 static moe_status prefill_scratch(moe_cache* c, int T) {
@@ -985,13 +1016,6 @@ static moe_status prefill_scratch(moe_cache* c, int T) {
       al(&pf.hp, (size_t)n_pairs * d.I * 2) || al((void**)&pf.op, (size_t)n_pairs * d.H * 4)) {
     cudaGetLastError();
     return fail(MOE_ERR_OOM, "prefill scratch for T=%d does not fit", T);
-  }
-  if (d.wdtype == MOE_FP4 && !pf.wb) {
-    const size_t s16 = (size_t)6 * d.H * d.I;
-    if (cudaMalloc((void**)&pf.wb, s16 * (d.E + 1)) != cudaSuccess) {
-      cudaGetLastError();
-      return fail(MOE_ERR_OOM, "prefill bf16 staging of one layer does not fit");
-    }
   }
   for (int b = 0; b < 2; ++b) {
     if (!pf.loaded[b]) CU_TRY(cudaEventCreateWithFlags(&pf.loaded[b], cudaEventDisableTiming));
@@ -1026,7 +1050,7 @@ extern "C" moe_status moe_prefill_stream(moe_cache_t c, int32_t layer_begin, int
 
   const int H = d.H, I = d.I, k = d.k, sh = d.has_shared;
   const int Tk = T * k, n_pairs = Tk + (sh ? T : 0);
-  const int64_t S = c->S, s16 = (int64_t)6 * H * I;
+  const int64_t S = c->S;
   const int64_t buf0 = c->C - 2 * E;  // buffers: slots [C-2E, C-E) and [C-E, C)
   uint8_t* slots = (uint8_t*)c->slots.base;
   const CacheDev st{c->d_map, c->d_owner, c->d_stamp, c->d_g};
@@ -1036,17 +1060,9 @@ extern "C" moe_status moe_prefill_stream(moe_cache_t c, int32_t layer_begin, int
   CU_TRY(cudaEventRecord(pf.start, s));
   CU_TRY(cudaStreamWaitEvent(c->copy, pf.start, 0));
 
-  CUtensorMap map_xp, map_hp, map_gu, map_dn, map_sgu, map_sdn;
+  CUtensorMap map_xp, map_hp;
   if (moe_status e = map_rows(&map_xp, pf.xp, n_pairs, H)) return e;
   if (moe_status e = map_rows(&map_hp, pf.hp, n_pairs, I)) return e;
-  if (d.wdtype == MOE_FP4) {
-    if (moe_status e = map_weights(&map_gu, pf.wb, (int)E, 2 * I, H, s16)) return e;
-    if (moe_status e = map_weights(&map_dn, pf.wb + (int64_t)4 * H * I, (int)E, H, I, s16)) return e;
-    if (sh) {
-      if (moe_status e = map_weights(&map_sgu, pf.wb + E * s16, 1, 2 * I, H, s16)) return e;
-      if (moe_status e = map_weights(&map_sdn, pf.wb + E * s16 + (int64_t)4 * H * I, 1, H, I, s16)) return e;
-    }
-  }
   auto timed = [&](cudaStream_t on, int kind, double flop) -> std::pair<cudaEvent_t, cudaEvent_t> {
     if (!c->profiling) return {nullptr, nullptr};
     cudaEvent_t a = take_event(c), b = take_event(c);
@@ -1076,36 +1092,40 @@ extern "C" moe_status moe_prefill_stream(moe_cache_t c, int32_t layer_begin, int
     uint8_t* yl = (uint8_t*)y + (int64_t)li * T * H * 2;
     CU_TRY(prefill_route(lg, T, (int)E, k, pf.ids, pf.w, s));
     CU_TRY(prefill_group(pf.ids, T, k, (int)E, sh, pf.cnt, pf.base, pf.offsets, pf.pos, pf.perm, s));
-    CU_TRY(prefill_gather(xl, T, k, H, n_pairs, pf.perm, pf.xp, s));
+    CU_TRY(prefill_gather(xl, T, k, H, n_pairs, pf.perm, pf.xp, d.wdtype == MOE_FP4, s));  // FP4: f16 rows
     CU_TRY(cudaStreamWaitEvent(s, pf.loaded[b], 0));
     const auto comp = timed(s, 2, 0.0);
-    const CUtensorMap* gu = &map_gu;
-    const CUtensorMap* dn = &map_dn;
-    CUtensorMap bgu, bdn, bsgu, bsdn;
-    if (d.wdtype == MOE_FP4) {
-      CU_TRY(prefill_dequant(buf, S, pf.wb, s16, (int)E, H, I, s));
-      if (sh) CU_TRY(prefill_dequant(c->shared_dev + (int64_t)l * S, S, pf.wb + E * s16, s16, 1, H, I, s));
-      CU_TRY(cudaEventRecord(pf.consumed[b], s));  // the GEMMs read the staging copy
+    const uint8_t* srec = sh ? c->shared_dev + (int64_t)l * S : nullptr;
+    const auto gm = timed(s, 3, gemm_flop);
+    if (d.wdtype == MOE_FP4) {  // the GEMMs read the FP4 codes and scales in the buffer
+      Fp4Maps lm, shm;
+      if (moe_status e = map_fp4_layer(&lm, buf, (int)E, H, I, S)) return e;
+      if (sh)
+        if (moe_status e = map_fp4_layer(&shm, srec, 1, H, I, S)) return e;
+      CU_TRY(prefill_gemm_gate_up_fp4(map_xp, lm.gu_c, lm.gu_s, pf.offsets, (int)E, n_pairs, H, I, pf.hp, c->d_err,
+                                      s));
+      if (sh)
+        CU_TRY(prefill_gemm_gate_up_fp4(map_xp, shm.gu_c, shm.gu_s, pf.offsets + E, 1, n_pairs, H, I, pf.hp,
+                                        c->d_err, s));
+      CU_TRY(prefill_gemm_down_fp4(map_hp, lm.dn_c, lm.dn_s, pf.offsets, (int)E, n_pairs, H, I, pf.op, c->d_err, s));
+      if (sh)
+        CU_TRY(prefill_gemm_down_fp4(map_hp, shm.dn_c, shm.dn_s, pf.offsets + E, 1, n_pairs, H, I, pf.op, c->d_err,
+                                     s));
     } else {
+      CUtensorMap bgu, bdn, bsgu, bsdn;
       if (moe_status e = map_weights(&bgu, buf, (int)E, 2 * I, H, S)) return e;
       if (moe_status e = map_weights(&bdn, buf + (int64_t)4 * H * I, (int)E, H, I, S)) return e;
-      gu = &bgu;
-      dn = &bdn;
       if (sh) {
-        const uint8_t* srec = c->shared_dev + (int64_t)l * S;
         if (moe_status e = map_weights(&bsgu, srec, 1, 2 * I, H, S)) return e;
         if (moe_status e = map_weights(&bsdn, srec + (int64_t)4 * H * I, 1, H, I, S)) return e;
       }
+      CU_TRY(prefill_gemm_gate_up(map_xp, bgu, pf.offsets, (int)E, n_pairs, H, I, pf.hp, c->d_err, s));
+      if (sh) CU_TRY(prefill_gemm_gate_up(map_xp, bsgu, pf.offsets + E, 1, n_pairs, H, I, pf.hp, c->d_err, s));
+      CU_TRY(prefill_gemm_down(map_hp, bdn, pf.offsets, (int)E, n_pairs, H, I, pf.op, c->d_err, s));
+      if (sh) CU_TRY(prefill_gemm_down(map_hp, bsdn, pf.offsets + E, 1, n_pairs, H, I, pf.op, c->d_err, s));
     }
-    const CUtensorMap* sgu = d.wdtype == MOE_FP4 ? &map_sgu : &bsgu;
-    const CUtensorMap* sdn = d.wdtype == MOE_FP4 ? &map_sdn : &bsdn;
-    const auto gm = timed(s, 3, gemm_flop);
-    CU_TRY(prefill_gemm_gate_up(map_xp, *gu, pf.offsets, (int)E, n_pairs, H, I, pf.hp, c->d_err, s));
-    if (sh) CU_TRY(prefill_gemm_gate_up(map_xp, *sgu, pf.offsets + E, 1, n_pairs, H, I, pf.hp, c->d_err, s));
-    CU_TRY(prefill_gemm_down(map_hp, *dn, pf.offsets, (int)E, n_pairs, H, I, pf.op, c->d_err, s));
-    if (sh) CU_TRY(prefill_gemm_down(map_hp, *sdn, pf.offsets + E, 1, n_pairs, H, I, pf.op, c->d_err, s));
     done(gm, s);
-    if (d.wdtype != MOE_FP4) CU_TRY(cudaEventRecord(pf.consumed[b], s));
+    CU_TRY(cudaEventRecord(pf.consumed[b], s));  // buffer b may be refilled
     CU_TRY(prefill_combine(pf.op, pf.pos, pf.w, T, k, H, sh, yl, s));
     done(comp, s);
   }

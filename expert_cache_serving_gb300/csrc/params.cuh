@@ -62,13 +62,17 @@ cudaError_t prefill_route(const float* logits, int T, int E, int k, int32_t* ids
 cudaError_t prefill_group(const int32_t* ids, int T, int k, int E, int has_shared, int32_t* cnt, int32_t* base,
                           int32_t* offsets, int32_t* pos, int32_t* perm, cudaStream_t s);
 cudaError_t prefill_gather(const void* x, int T, int k, int H, int n_pairs, const int32_t* perm, void* xp,
-                           cudaStream_t s);
-cudaError_t prefill_dequant(const uint8_t* src, int64_t S4, uint8_t* dst, int64_t S16, int n_rec, int H, int I,
-                            cudaStream_t s);
+                           int to_f16, cudaStream_t s);
 cudaError_t prefill_gemm_gate_up(const CUtensorMap& a, const CUtensorMap& b, const int32_t* offsets, int n_groups,
                                  int n_rows, int H, int I, void* hp, int* err, cudaStream_t s);
 cudaError_t prefill_gemm_down(const CUtensorMap& a, const CUtensorMap& b, const int32_t* offsets, int n_groups,
                               int n_rows, int H, int I, float* op, int* err, cudaStream_t s);
+cudaError_t prefill_gemm_gate_up_fp4(const CUtensorMap& a, const CUtensorMap& codes, const CUtensorMap& scales,
+                                     const int32_t* offsets, int n_groups, int n_rows, int H, int I, void* hp,
+                                     int* err, cudaStream_t s);
+cudaError_t prefill_gemm_down_fp4(const CUtensorMap& a, const CUtensorMap& codes, const CUtensorMap& scales,
+                                  const int32_t* offsets, int n_groups, int n_rows, int H, int I, float* op, int* err,
+                                  cudaStream_t s);
 cudaError_t prefill_combine(const float* op, const int32_t* pos, const float* w, int T, int k, int H, int has_shared,
                             void* y, cudaStream_t s);
 cudaError_t prefill_evict_range(const CacheDev& st, int64_t s0, int64_t s1, int* oldest_n, cudaStream_t s);

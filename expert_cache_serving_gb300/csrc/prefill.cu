@@ -1,7 +1,8 @@
 // Prefill-size routed-MoE layer: routing of T tokens, stable grouping of the
-// (token, rank) pairs by expert, gather of the activations per expert, FP4 ->
-// bf16 staging of the layer's experts, the two grouped GEMMs on tcgen05/TMEM
-// (gate/up with the SwiGLU epilogue, then down) and the weighted combine.
+// (token, rank) pairs by expert, gather of the activations per expert, the two
+// grouped GEMMs on tcgen05/TMEM reading the layer buffer's bf16 weights or its
+// FP4 codes and scales directly (gate/up with the SwiGLU epilogue, then down)
+// and the weighted combine.
 //
 // FreeToken write-up, "전층 이중 버퍼링": prefill activates almost every expert
 // of a layer, so the layer's full expert set is streamed into one of two
@@ -131,6 +132,9 @@ __global__ void __launch_bounds__(1024) group_place_kernel(const int32_t* ids, i
 }
 
 // ---- 3. gather of the activations in group order -------------------------------------
+// TO_F16: rows are written as f16 (the FP4 GEMMs run on f16 operands); bf16 ->
+// f16 is exact for every bf16 value inside the f16 range.
+template <bool TO_F16>
 __global__ void gather_kernel(const __nv_bfloat16* __restrict__ x, int Tk, int k, int H, int n_pairs,
                               const int32_t* __restrict__ perm, __nv_bfloat16* __restrict__ xp) {
   const int per = H / 8;  // 16-byte vectors per row
@@ -139,42 +143,21 @@ __global__ void gather_kernel(const __nv_bfloat16* __restrict__ x, int Tk, int k
     const int row = (int)(i / per), v = (int)(i % per);
     const int p = perm[row];
     const int t = p < Tk ? p / k : p - Tk;
-    reinterpret_cast<uint4*>(xp + (int64_t)row * H)[v] = reinterpret_cast<const uint4*>(x + (int64_t)t * H)[v];
-  }
-}
-
-// ---- 4. FP4 -> bf16 staging of expert records (exact) ----------------------------------
-// one thread per 16-element block of one matrix row
-__global__ void dequant_kernel(const uint8_t* __restrict__ src, int64_t S4, uint8_t* __restrict__ dst, int64_t S16,
-                               int n_rec, int H, int I) {
-  const int64_t HI = (int64_t)H * I;
-  const int64_t blocks_per_rec = 3 * HI / 16;
-  const int64_t total = blocks_per_rec * n_rec;
-  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t rec = i / blocks_per_rec, b = i % blocks_per_rec;
-    const int mat = (int)(b / (HI / 16));
-    const int64_t bb = b % (HI / 16);  // block within the matrix (row-major, 16 elements per block)
-    const uint8_t* r4 = src + rec * S4;
-    const uint8_t* codes = mat == 0 ? r4 : mat == 1 ? r4 + HI / 2 : r4 + HI + HI / 8;
-    const uint8_t* scales = mat == 0 ? r4 + HI : mat == 1 ? r4 + HI + HI / 16 : r4 + HI + HI / 8 + HI / 2;
-    const uint2 c = *reinterpret_cast<const uint2*>(codes + bb * 8);
-    const float2 s2 = e4m3x2_to_float2((unsigned short)scales[bb]);
-    const float s = s2.x;
-    uint32_t out[8];
+    uint4 val = reinterpret_cast<const uint4*>(x + (int64_t)t * H)[v];
+    if constexpr (TO_F16) {
+      uint32_t* w = reinterpret_cast<uint32_t*>(&val);
 #pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      const uint32_t byte = ((q < 4 ? c.x : c.y) >> (8 * (q & 3))) & 0xFFu;
-      const float2 f = e2m1x2_to_float2(byte);
-      __nv_bfloat162 b2 = __floats2bfloat162_rn(f.x * s, f.y * s);
-      out[q] = *reinterpret_cast<uint32_t*>(&b2);
+      for (int i = 0; i < 4; ++i) {
+        const __half2 h2 = __floats2half2_rn(bf16lo(w[i]), bf16hi(w[i]));
+        w[i] = *reinterpret_cast<const uint32_t*>(&h2);
+      }
     }
-    uint4* d = reinterpret_cast<uint4*>(dst + rec * S16 + (int64_t)mat * HI * 2 + bb * 32);
-    d[0] = make_uint4(out[0], out[1], out[2], out[3]);
-    d[1] = make_uint4(out[4], out[5], out[6], out[7]);
+    reinterpret_cast<uint4*>(xp + (int64_t)row * H)[v] = val;
   }
 }
 
-// ---- 5/6. grouped GEMMs ----------------------------------------------------------------------
+
+// ---- 4/5. grouped GEMMs ----------------------------------------------------------------------
 struct BRowGateUp {
   int I;
   __device__ int operator()(int nb, int half) const { return half ? I + nb * 128 : nb * 128; }
@@ -186,7 +169,7 @@ struct BRowDown {
 __global__ void __launch_bounds__(tc::kThreads, 1)
     gemm_gate_up_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                         const int32_t* offsets, int n_groups, int H, int I, __nv_bfloat16* hp, int* err) {
-  tc::grouped_gemm_cta(&map_a, &map_b, offsets, n_groups, I / 128, H, tc::EpiSwiGLU{hp, I}, BRowGateUp{I}, err);
+  tc::grouped_gemm_cta(&map_a, &map_b, offsets, n_groups, I / 128, H, tc::EpiSwiGLU<>{hp, I}, BRowGateUp{I}, err);
 }
 
 __global__ void __launch_bounds__(tc::kThreads, 1)
@@ -195,7 +178,24 @@ __global__ void __launch_bounds__(tc::kThreads, 1)
   tc::grouped_gemm_cta(&map_a, &map_b, offsets, n_groups, H / 256, I, tc::EpiStoreF32{op, H}, BRowDown{}, err);
 }
 
-// ---- 7. combine ------------------------------------------------------------------------------
+// FP4 weights read directly (codes + scales maps over the layer buffer)
+__global__ void __launch_bounds__(tc::fp4::kThreads, 1)
+    gemm_gate_up_fp4_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_c,
+                            const __grid_constant__ CUtensorMap map_s, const int32_t* offsets, int n_groups, int H,
+                            int I, __half* hp, int* err) {
+  tc::grouped_gemm_fp4_cta(&map_a, &map_c, &map_s, offsets, n_groups, I / 128, H, tc::EpiSwiGLU<__half>{hp, I},
+                           BRowGateUp{I}, err);
+}
+
+__global__ void __launch_bounds__(tc::fp4::kThreads, 1)
+    gemm_down_fp4_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_c,
+                         const __grid_constant__ CUtensorMap map_s, const int32_t* offsets, int n_groups, int H, int I,
+                         float* op, int* err) {
+  tc::grouped_gemm_fp4_cta(&map_a, &map_c, &map_s, offsets, n_groups, H / 256, I, tc::EpiStoreF32{op, H}, BRowDown{},
+                           err);
+}
+
+// ---- 6. combine ------------------------------------------------------------------------------
 __global__ void combine_kernel(const float* __restrict__ op, const int32_t* __restrict__ pos, const float* __restrict__ w,
                                int T, int k, int H, int has_shared, __nv_bfloat16* __restrict__ y) {
   const int per = H / 4;
@@ -263,14 +263,13 @@ cudaError_t prefill_group(const int32_t* ids, int T, int k, int E, int has_share
 }
 
 cudaError_t prefill_gather(const void* x, int T, int k, int H, int n_pairs, const int32_t* perm, void* xp,
-                           cudaStream_t s) {
-  pf::gather_kernel<<<sms() * 8, 256, 0, s>>>((const __nv_bfloat16*)x, T * k, k, H, n_pairs, perm, (__nv_bfloat16*)xp);
-  return cudaGetLastError();
-}
-
-cudaError_t prefill_dequant(const uint8_t* src, int64_t S4, uint8_t* dst, int64_t S16, int n_rec, int H, int I,
-                            cudaStream_t s) {
-  pf::dequant_kernel<<<sms() * 8, 256, 0, s>>>(src, S4, dst, S16, n_rec, H, I);
+                           int to_f16, cudaStream_t s) {
+  if (to_f16)
+    pf::gather_kernel<true><<<sms() * 8, 256, 0, s>>>((const __nv_bfloat16*)x, T * k, k, H, n_pairs, perm,
+                                                      (__nv_bfloat16*)xp);
+  else
+    pf::gather_kernel<false><<<sms() * 8, 256, 0, s>>>((const __nv_bfloat16*)x, T * k, k, H, n_pairs, perm,
+                                                       (__nv_bfloat16*)xp);
   return cudaGetLastError();
 }
 
@@ -301,6 +300,36 @@ cudaError_t prefill_gemm_down(const CUtensorMap& a, const CUtensorMap& b, const 
   if (cudaError_t e = gemm_attr()) return e;
   pf::gemm_down_kernel<<<gemm_grid(n_rows, n_groups, H / 256), tc::kThreads, tc::kSmemBytes, s>>>(
       a, b, offsets, n_groups, H, I, op, err);
+  return cudaGetLastError();
+}
+
+static bool g_gemm_fp4_attr = false;
+static cudaError_t gemm_fp4_attr() {
+  if (g_gemm_fp4_attr) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(pf::gemm_gate_up_fp4_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)tc::fp4::kSmemBytes);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(pf::gemm_down_fp4_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)tc::fp4::kSmemBytes);
+  g_gemm_fp4_attr = e == cudaSuccess;
+  return e;
+}
+
+cudaError_t prefill_gemm_gate_up_fp4(const CUtensorMap& a, const CUtensorMap& codes, const CUtensorMap& scales,
+                                     const int32_t* offsets, int n_groups, int n_rows, int H, int I, void* hp,
+                                     int* err, cudaStream_t s) {
+  if (cudaError_t e = gemm_fp4_attr()) return e;
+  pf::gemm_gate_up_fp4_kernel<<<gemm_grid(n_rows, n_groups, I / 128), tc::fp4::kThreads, tc::fp4::kSmemBytes, s>>>(
+      a, codes, scales, offsets, n_groups, H, I, (__half*)hp, err);
+  return cudaGetLastError();
+}
+
+cudaError_t prefill_gemm_down_fp4(const CUtensorMap& a, const CUtensorMap& codes, const CUtensorMap& scales,
+                                  const int32_t* offsets, int n_groups, int n_rows, int H, int I, float* op, int* err,
+                                  cudaStream_t s) {
+  if (cudaError_t e = gemm_fp4_attr()) return e;
+  pf::gemm_down_fp4_kernel<<<gemm_grid(n_rows, n_groups, H / 256), tc::fp4::kThreads, tc::fp4::kSmemBytes, s>>>(
+      a, codes, scales, offsets, n_groups, H, I, op, err);
   return cudaGetLastError();
 }
 

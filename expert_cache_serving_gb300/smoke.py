@@ -1,9 +1,10 @@
-"""One small decode run on cuda:0 checked against the CPU oracle.
+"""Small decode and prefill runs on cuda:0 checked against the CPU oracle.
 
 Runs the tiny fp32 workload (2 layers, 16 experts, top-2, 12 cache slots)
 for a few steps and a small bf16 workload with a shared expert through the C
 ABI, and compares routing, slots, the cache event log and the layer outputs
-with the oracle.  Raises on any mismatch.
+with the oracle; then one 64-token FP4 prefill layer (H 512, I 256, 24
+experts, top-4) through the tcgen05 grouped GEMMs.  Raises on any mismatch.
 """
 from __future__ import annotations
 
@@ -62,4 +63,27 @@ def run() -> None:
         torch.cuda.synchronize()
         assert [tuple(e) for e in mc.moe_cache_trace(cache.handle)] == want_events, "cache event log mismatch"
         cache.close()
+
+    # one FP4 prefill layer (tensor-core grouped GEMMs reading FP4 codes)
+    w = configs.SMALL_FP4_NARROW.with_(C=48)
+    T = 64
+    pool = runner.build_pool(w)
+    cache = runner.Cache(w, pool, None, C=w.C, max_tokens=1)
+    xs = synth.activations_bf16(w.seed + 100, 0, 0, T, w.H)
+    lg = synth.iid_logits(w.seed, 1, T, w.E)
+    x = torch.from_numpy(xs.view(np.int16)).view(torch.bfloat16).to(dev)
+    y = torch.empty_like(x)
+    mc.check(mc.moe_prefill_stream(cache.handle, 0, 1, x, torch.from_numpy(lg).to(dev), T, y,
+                                   torch.cuda.current_stream()), "moe_prefill_stream")
+    torch.cuda.synchronize()
+    ids, wts = router.topk_softmax(lg[0].astype(np.float64), w.k)
+
+    def expert0(e):
+        return records.parse(synth.records_array(w.seed, e, 1, w.H, w.I, w.wdtype)[0], w.H, w.I, w.wdtype)
+
+    ref = ffn.moe_layer(synth.bf16_bits_to_f32(xs).astype(np.float64), ids, wts, expert0, None)
+    got = y.float().cpu().numpy().astype(np.float64)
+    err = np.max(np.abs(got - ref))
+    assert err <= 1e-2 * np.max(np.abs(ref)), f"prefill output error {err}"
+    cache.close()
     print("smoke: ok")
