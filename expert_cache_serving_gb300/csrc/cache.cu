@@ -370,7 +370,6 @@ extern "C" moe_status moe_cache_create(const moe_model_desc* desc, const void* h
   if (moe_status s = c->slots.resize((size_t)n_slots * S)) return bail(s);
 
   const int Bm = desc->max_tokens, k = desc->k, H = desc->H, I = desc->I, E = desc->E;
-  const int M = Bm * k;
   const size_t nslot_alloc = (size_t)std::max<int64_t>(1, max_slots);
   moe_status s = MOE_OK;
   if ((s = cu(cudaMalloc(&c->d_map, sizeof(int32_t) * LE), "map")) ||
@@ -578,7 +577,6 @@ extern "C" moe_status moe_layer_forward_ex(moe_cache_t c, int32_t layer, const v
   LayerParams p{};
   p.L = d.L; p.E = d.E; p.k = d.k; p.B = B; p.layer = layer; p.H = d.H; p.I = d.I;
   p.C = c->C;
-  p.M = d.max_tokens * d.k;
   p.logits = lg;
   p.st = CacheDev{c->d_map, c->d_owner, c->d_stamp, c->d_g};
   p.plan = c->d_plan;

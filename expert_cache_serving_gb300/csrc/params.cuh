@@ -10,7 +10,6 @@ namespace moe {
 struct LayerParams {
   int L, E, k, B, layer, H, I;
   int64_t C;
-  int M;                      // max_tokens * k
   const float* logits;        // [B][E]
   CacheDev st;
   Plan* plan;
