@@ -43,6 +43,7 @@ def _run(cmd, verbose):
     return r
 
 
+LAYER_INST = "layer_inst.cu"  # compiled once per (format, token bound)
 SYNTH_GPU_SRC = os.path.join(ROOT, "synth", "synth_gpu.cu")
 SYNTH_GPU_LIB = os.path.join(ROOT, "synth", "_lib", "libsynth_gpu.so")
 
@@ -58,19 +59,26 @@ def build_synth(verbose=False) -> str:
 def build_cuda(verbose=False) -> str:
     os.makedirs(OBJDIR, exist_ok=True)
     nvcc = _nvcc()
-    srcs = sorted(glob.glob(os.path.join(CSRC, "*.cu")) + glob.glob(os.path.join(CSRC, "*.cpp")))
+    srcs = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
     if not srcs:
         raise RuntimeError("no CUDA sources")
-    objs = []
-    jobs = []
-    with cf.ThreadPoolExecutor(max_workers=min(16, len(srcs))) as ex:
-        for s in srcs:
-            o = os.path.join(OBJDIR, os.path.basename(s) + ".o")
-            objs.append(o)
-            cmd = [nvcc] + ARCH + NVCC_FLAGS + ["-c", s, "-o", o]
-            if s.endswith(".cpp"):
-                cmd = [nvcc] + NVCC_FLAGS + ["-x", "cu", "-c", s, "-o", o] + ARCH
-            jobs.append(ex.submit(_run, cmd, verbose))
+    # (source, extra defines, object): the decode layer kernel's source is
+    # compiled once per (format, token bound) so its 15 instantiations build
+    # in parallel
+    units = []
+    for s in srcs:
+        base = os.path.basename(s)
+        if base == LAYER_INST:
+            for fmt in (0, 1, 2):
+                for maxt in (1, 2, 4, 8, 16):
+                    units.append((s, [f"-DMOE_LAYER_FMT={fmt}", f"-DMOE_LAYER_MAXT={maxt}"],
+                                  os.path.join(OBJDIR, f"{base}.{fmt}.{maxt}.o")))
+        else:
+            units.append((s, [], os.path.join(OBJDIR, base + ".o")))
+    objs = [o for _, _, o in units]
+    workers = max(1, min(len(units), os.cpu_count() or 8))
+    with cf.ThreadPoolExecutor(max_workers=workers) as ex:
+        jobs = [ex.submit(_run, [nvcc] + ARCH + NVCC_FLAGS + defs + ["-c", s, "-o", o], verbose) for s, defs, o in units]
         for j in jobs:
             j.result()
     _run([nvcc] + ARCH + ["-shared", "-cudart", "static", "-o", LIB] + objs + ["-lpthread", "-ldl", "-lrt"], verbose)

@@ -137,7 +137,7 @@ __device__ __forceinline__ bool slot_key(const CacheDev& st, int64_t C, int64_t 
 // ascending into cs.sel_slot / cs.sel_key; returns how many were found.
 // Radix select with 11-bit digits over the span of the keys, then a rank sort
 // of the selected few.  Every thread of the CTA must call.
-__device__ int select_oldest(CtrlSmem& cs, const CacheDev& st, int64_t C, int want, int E, int layer,
+static __device__ int select_oldest(CtrlSmem& cs, const CacheDev& st, int64_t C, int want, int E, int layer,
                              const unsigned* bits) {
   const int tid = threadIdx.x, lane = tid & 31, nt = blockDim.x;
   unsigned long long lmin = ~0ull, lmax = 0ull;
@@ -250,7 +250,7 @@ __device__ __forceinline__ void publish_summary(const LayerParams& p) {
 // control_commit, off the other CTAs' critical path.  Returns the status
 // (MOE_OK or an error) to every thread; on an error the plan and the host
 // summary carry it and nothing is changed.
-__device__ int control_step(const LayerParams& p, CtrlSmem& cs) {
+static __device__ int control_step(const LayerParams& p, CtrlSmem& cs) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarp = blockDim.x >> 5;
   const int E = p.E, k = p.k, B = p.B, npairs = B * k;
   const int64_t C = p.C;
@@ -456,7 +456,7 @@ __device__ int control_step(const LayerParams& p, CtrlSmem& cs) {
 // other CTAs have been released: hits and fills take stamps g + r in U order,
 // each victim's previous key leaves the table, g advances by |U|.  Then the
 // host summary, unless control_step already published it.
-__device__ void control_commit(const LayerParams& p, CtrlSmem& cs) {
+static __device__ void control_commit(const LayerParams& p, CtrlSmem& cs) {
   const int tid = threadIdx.x, n_u = cs.nu;
   const unsigned long long g0 = cs.g;
   if (tid < n_u) {
@@ -481,7 +481,7 @@ __device__ void control_commit(const LayerParams& p, CtrlSmem& cs) {
 // Drop from the oldest-slot list every slot this call touched (hits and
 // victims now own keys of this call).  Run by the control CTA after the plan
 // is published.
-__device__ void compact_oldest(const LayerParams& p, CtrlSmem& cs) {
+static __device__ void compact_oldest(const LayerParams& p, CtrlSmem& cs) {
   __syncthreads();
   const int listed = cs.nsel;
   if (listed < 0) return;
@@ -502,7 +502,7 @@ __device__ void compact_oldest(const LayerParams& p, CtrlSmem& cs) {
 // Undo of a call whose fills did not arrive: recency and the counter go back
 // to their values before the call; the call's victim slots are left empty
 // (their previous contents may already be overwritten).
-__device__ void undo_call(const LayerParams& p) {
+static __device__ void undo_call(const LayerParams& p) {
   const Plan* pl = p.plan;
   for (int r = threadIdx.x; r < pl->n_u; r += blockDim.x) {
     const int s = pl->u_slot[r];

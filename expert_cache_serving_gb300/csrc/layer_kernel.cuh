@@ -1,0 +1,524 @@
+// One decode-size routed-MoE layer call as a single cooperative launch.
+//
+// FreeToken write-up: the router and the cache lookup run on the GPU ("decode
+// co-design"); one GPU step per layer deduplicates, classifies, picks victims
+// and rewrites ids ("CUDA Graph-compatible LRU cache"); the GPU evaluates the
+// set G = H ∪ F as a grouped FFN once the batched copy of F has landed, and
+// the partial sums merge exactly ("measured bandwidths decide the split",
+// Fig. 2 caption); decode is memory-bound, each routed expert's weights being
+// read once per token.
+//
+// CTA 0 runs the control step and publishes the miss list to the host, which
+// issues one cudaMemcpyAsync per half record (gate/up part, then W_down) on
+// the copy stream, each followed by a stream write of a per-fill flag.  The
+// other CTAs meanwhile load the activations and run the shared expert's
+// gate/up rows.  Then, all CTAs together (512 threads, one CTA per SM):
+//  1. gate/up rows of the resident experts: h = SiLU(x W_gate^T) * (x W_up^T);
+//     a warp streams one gate row and one up row with 16-byte loads (FP4
+//     dequantised in registers) and serves every token routed to the expert;
+//     CTA 0 meanwhile ranks the oldest slots for the next call;
+//  2. grid barrier, then W_down rows: each CTA owns a contiguous range of
+//     output rows n for every expert and keeps o[t][j][n] in shared memory;
+//  3. fills, in order, each as soon as its flag says the copy landed: gate/up
+//     rows, one grid barrier, then W_down rows into the same shared buffer;
+//  4. y_t[n] = sum_j w_tj o_tj[n] (+ shared) in rank order, in float32.
+// Every dot product has a fixed summation order independent of which phase
+// computes it, so outputs are bitwise identical whatever the residency.
+#pragma once
+#include "control.cuh"
+#include "expert_math.cuh"
+
+namespace moe {
+
+struct ItemTable {
+  const uint8_t* rec[kMaxItems];  // where the record is read (slot, shared expert, or host pool)
+  uint8_t* dst[kMaxItems];        // slot a device-driven fill writes the record to (else null)
+  int ntok[kMaxItems];
+  int pair0[kMaxItems];      // -1 for the shared expert
+  int hbase[kMaxItems + 1];  // running token count in item order
+  int perm[kMaxPairs];       // the plan's grouped pair order, copied once per call
+  float pair_w[kMaxPairs];   // the plan's routing weights, copied once per call
+};
+
+// Items of plan list `which` into tb at position `at` (list 1 from the host
+// pool when `from_pool`); returns the new item count.  All threads call.
+static __device__ int load_items(const LayerParams& p, const Plan* pl, int which, ItemTable& tb, int at = 0,
+                          bool from_pool = false) {
+  const int n = pl->n_items[which];
+  if (at == 0 && which == 0)
+    for (int i = threadIdx.x; i < p.B * p.k; i += blockDim.x) {
+      tb.perm[i] = pl->perm[i];
+      tb.pair_w[i] = pl->pair_w[i];
+    }
+  for (int i = threadIdx.x; i < n; i += blockDim.x) {
+    const int r = pl->items[which][i];
+    if (r == pl->n_u) {
+      tb.rec[at + i] = p.shared_rec;
+      tb.dst[at + i] = nullptr;
+      tb.ntok[at + i] = p.B;
+      tb.pair0[at + i] = -1;
+    } else {
+      uint8_t* slot = const_cast<uint8_t*>(p.slots) + (int64_t)pl->u_slot[r] * p.S;
+      tb.rec[at + i] = from_pool ? p.pool + (int64_t)pl->u_key[r] * p.S : slot;
+      tb.dst[at + i] = from_pool ? slot : nullptr;
+      tb.pair0[at + i] = pl->u_off[r];
+      tb.ntok[at + i] = pl->u_off[r + 1] - pl->u_off[r];
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int run = at ? tb.hbase[at] : 0;
+    for (int i = at; i < at + n; ++i) { tb.hbase[i] = run; run += tb.ntok[i]; }
+    tb.hbase[at + n] = run;
+  }
+  __syncthreads();
+  return at + n;
+}
+
+// 16-byte unit v of the W_down rows [n0, n0 + nrows) of record `rec` (codes
+// or values first, then the FP4 scales).  Row bytes and FP4 scale rows are
+// multiples of 16 for every accepted shape (I % 64 == 0; FP4: I % 256 == 0).
+template <int WD>
+__device__ __forceinline__ const uint8_t* down_unit(const uint8_t* rec, int H, int I, int n0, int nv, int v) {
+  const RecView r = rec_view<WD>(rec, H, I);
+  if (v < nv) return r.down + (int64_t)n0 * Fmt<WD>::row_bytes(I) + (int64_t)v * 16;
+  return r.down_sc + (int64_t)n0 * (I / 16) + (int64_t)(v - nv) * 16;
+}
+
+// Device-driven fill of this CTA's W_down rows [n0, n0 + nrows) of items
+// [ib, ie): copy them from the host pool into the items' slots, with eight
+// independent 16-byte loads in flight per thread (host-link latency bound).
+template <int WD>
+__device__ void copy_down_rows(const LayerParams& p, const ItemTable& tb, int ib, int ie, int n0, int nrows) {
+  constexpr int U = 8;
+  const int H = p.H, I = p.I;
+  const int nv = (int)(nrows * Fmt<WD>::row_bytes(I) / 16);
+  const int per = nv + (WD == MOE_FP4 ? nrows * (I / 16) / 16 : 0);
+  const int total = (ie - ib) * per;
+  for (int v0 = threadIdx.x; v0 < total; v0 += U * blockDim.x) {
+    uint4 buf[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int v = v0 + u * (int)blockDim.x;
+      if (v < total) buf[u] = ld_ro16(down_unit<WD>(tb.rec[ib + v / per], H, I, n0, nv, v % per));
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int v = v0 + u * (int)blockDim.x;
+      if (v < total)
+        *reinterpret_cast<uint4*>(const_cast<uint8_t*>(down_unit<WD>(tb.dst[ib + v / per], H, I, n0, nv, v % per))) =
+            buf[u];
+    }
+  }
+}
+
+// token, h row and rank slot of the q-th token of item `it`
+__device__ __forceinline__ void item_token(const LayerParams& p, const Plan* pl, const ItemTable& tb, int it, int q,
+                                           int* t, int* hrow, int* j) {
+  const int p0 = tb.pair0[it];
+  if (p0 < 0) {
+    *t = q;
+    *hrow = p.h_shared_row0 + q;
+    *j = p.k;
+  } else {
+    const int pair = tb.perm[p0 + q];
+    *t = pair / p.k;
+    *hrow = pair;
+    *j = pair % p.k;
+  }
+}
+
+// Gate/up rows of items [ib, ie), spread over CTAs [cta0, cta0 + ncta).
+// WB: the rows are read from the host pool and also written to the slot.
+template <int WD, int MAXT, bool FRESH, bool WB = false, typename XT>
+__device__ void phase1(const LayerParams& p, const Plan* pl, const ItemTable& tb, int ib, int ie, int cta0, int ncta,
+                       const XT* xs) {
+  using F = Fmt<WD>;
+  constexpr int EPC = F::kElemsPerChunk, UNR = F::kUnroll;
+  const int rel = (int)blockIdx.x - cta0;
+  if (rel < 0 || rel >= ncta || ie <= ib) return;
+  const int H = p.H, I = p.I, lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int64_t total = (int64_t)(ie - ib) * I;
+  const int64_t t0 = (int64_t)rel * total / ncta, t1 = (int64_t)(rel + 1) * total / ncta;
+  const int nchunks = H / EPC;
+  const int64_t rb = F::row_bytes(H);
+  for (int64_t task = t0 + warp; task < t1; task += kWarps) {
+    const int it = ib + (int)(task / I), i = (int)(task % I);
+    const int ntok = tb.ntok[it];
+    const RecView v = rec_view<WD>(tb.rec[it], H, I);
+    const uint8_t* grow = v.gate + (int64_t)i * rb;
+    const uint8_t* urow = v.up + (int64_t)i * rb;
+    const uint8_t* gsc = (WD == MOE_FP4) ? v.gate_sc + (int64_t)i * (H / 16) : nullptr;
+    const uint8_t* usc = (WD == MOE_FP4) ? v.up_sc + (int64_t)i * (H / 16) : nullptr;
+    int tok[MAXT];
+#pragma unroll
+    for (int q = 0; q < MAXT; ++q) {
+      int t = 0, hr, j;
+      if (q < ntok) item_token(p, pl, tb, it, q, &t, &hr, &j);
+      tok[q] = t;
+    }
+    float ag[MAXT], au[MAXT];
+#pragma unroll
+    for (int q = 0; q < MAXT; ++q) { ag[q] = 0.f; au[q] = 0.f; }
+    for (int c0 = 0; c0 < nchunks; c0 += 32 * UNR) {
+      uint4 wg[UNR], wu[UNR];
+      unsigned short sg[UNR], su[UNR];
+#pragma unroll
+      for (int u = 0; u < UNR; ++u) {
+        const int c = c0 + lane + 32 * u;
+        if (c < nchunks) {
+          wg[u] = ld_w16<FRESH>(grow + (int64_t)c * 16);
+          wu[u] = ld_w16<FRESH>(urow + (int64_t)c * 16);
+          if (WD == MOE_FP4) {
+            sg[u] = ld_w2<FRESH>(gsc + 2 * c);
+            su[u] = ld_w2<FRESH>(usc + 2 * c);
+          } else {
+            sg[u] = su[u] = 0;
+          }
+        }
+      }
+      if constexpr (WB) {
+        const RecView dv = rec_view<WD>(tb.dst[it], H, I);
+#pragma unroll
+        for (int u = 0; u < UNR; ++u) {
+          const int c = c0 + lane + 32 * u;
+          if (c < nchunks) {
+            *reinterpret_cast<uint4*>(const_cast<uint8_t*>(dv.gate) + (int64_t)i * rb + (int64_t)c * 16) = wg[u];
+            *reinterpret_cast<uint4*>(const_cast<uint8_t*>(dv.up) + (int64_t)i * rb + (int64_t)c * 16) = wu[u];
+            if (WD == MOE_FP4) {
+              *reinterpret_cast<unsigned short*>(const_cast<uint8_t*>(dv.gate_sc) + (int64_t)i * (H / 16) + 2 * c) = sg[u];
+              *reinterpret_cast<unsigned short*>(const_cast<uint8_t*>(dv.up_sc) + (int64_t)i * (H / 16) + 2 * c) = su[u];
+            }
+          }
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < UNR; ++u) {
+        const int c = c0 + lane + 32 * u;
+        if (c < nchunks) {
+#pragma unroll
+          for (int q = 0; q < MAXT; ++q) {
+            if (q < ntok) {
+              const XT* xr = xs + (size_t)tok[q] * H + (size_t)c * EPC;
+              ag[q] += chunk_dot<WD, XT>(wg[u], sg[u], xr);
+              au[q] += chunk_dot<WD, XT>(wu[u], su[u], xr);
+            }
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < MAXT; ++q) {
+      if (q < ntok) {
+        const float g = warp_sum(ag[q]);
+        const float u = warp_sum(au[q]);
+        if (lane == 0) {
+          int t, hr, j;
+          item_token(p, pl, tb, it, q, &t, &hr, &j);
+          p.h[(int64_t)hr * I + i] = g / (1.0f + expf(-g)) * u;
+        }
+      }
+    }
+  }
+}
+
+// Where W_down row `row` (and its FP4 scales) of item gi is read: its record,
+// or, when STAGED, staged item j of this CTA in shared memory.
+template <int WD, bool STAGED>
+__device__ __forceinline__ void down_row(const ItemTable& tb, int j, int gi, int row, int n0, int nrows, int H, int I,
+                                         const uint8_t* stage, int pitch, const uint8_t** drow, const uint8_t** dsc) {
+  const int64_t rb = Fmt<WD>::row_bytes(I);
+  if constexpr (STAGED) {
+    const uint8_t* base = stage + (int64_t)j * pitch;
+    *drow = base + (int64_t)(row - n0) * rb;
+    *dsc = base + (int64_t)nrows * rb + (int64_t)(row - n0) * (I / 16);
+  } else {
+    const RecView v = rec_view<WD>(tb.rec[gi], H, I);
+    *drow = v.down + (int64_t)row * rb;
+    *dsc = (WD == MOE_FP4) ? v.down_sc + (int64_t)row * (I / 16) : nullptr;
+  }
+}
+template <bool FRESH, bool STAGED>
+__device__ __forceinline__ uint4 ld_down16(const uint8_t* q) {
+  if constexpr (STAGED) return lds16(q); else return ld_w16<FRESH>(q);
+}
+template <bool FRESH, bool STAGED>
+__device__ __forceinline__ unsigned short ld_down2(const uint8_t* q) {
+  if constexpr (STAGED) return lds2(q); else return ld_w2<FRESH>(q);
+}
+
+// W_down rows [n0, n0 + nrows) of items [ib, ie) -> os[row][t][j].
+// STAGED: the rows of item ib + j sit in shared memory at stage + j * pitch
+// (rows n0.., then their FP4 scales), copied there during phase 1.
+template <int WD, int MAXT, bool FRESH, bool STAGED = false>
+__device__ void phase2(const LayerParams& p, const Plan* pl, const ItemTable& tb, int ib, int ie, int n0, int nrows,
+                       float* hs, float* os, const uint8_t* stage = nullptr, int pitch = 0) {
+  using F = Fmt<WD>;
+  constexpr int EPC = F::kElemsPerChunk;
+  constexpr int kLanesPerRow = 8, kRowsPerWarp = 32 / kLanesPerRow, kChunksPerLane = MAXT >= 16 ? 4 : 8;
+  const int H = p.H, I = p.I, B = p.B, k = p.k, lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int ostride = B * (k + 1);
+  const int nchunks = I / EPC;
+  int g0 = ib;
+  while (g0 < ie) {
+    int g1 = g0, used = 0;
+    while (g1 < ie) {
+      const int nt = tb.ntok[g1];
+      if (used + nt * I > p.smem_h_floats && g1 > g0) break;
+      used += nt * I;
+      ++g1;
+    }
+    __syncthreads();
+    {  // h rows of the group, item-major, in one flat pass (all loads in flight together)
+      __shared__ int s_hrow[kMaxPairs + kMaxB];
+      const int rows = tb.hbase[g1] - tb.hbase[g0];
+      for (int rr = threadIdx.x; rr < rows; rr += blockDim.x) {
+        int g = g0;
+        while (tb.hbase[g + 1] - tb.hbase[g0] <= rr) ++g;
+        int t, hr, j;
+        item_token(p, pl, tb, g, rr - (tb.hbase[g] - tb.hbase[g0]), &t, &hr, &j);
+        s_hrow[rr] = hr;
+      }
+      __syncthreads();
+      const int per = I / 4, n4 = rows * per;
+      for (int e0 = threadIdx.x; e0 < n4; e0 += 4 * blockDim.x) {  // four loads in flight per thread
+        float4 v[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int e = e0 + u * (int)blockDim.x;
+          if (e < n4) v[u] = __ldcg(reinterpret_cast<const float4*>(p.h + (int64_t)s_hrow[e / per] * I) + e % per);
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int e = e0 + u * (int)blockDim.x;
+          if (e < n4) reinterpret_cast<float4*>(hs + (int64_t)(e / per) * I)[e % per] = v[u];
+        }
+      }
+    }
+    __syncthreads();
+    // 8 lanes per row, 4 rows per warp: lane l of row group g reads chunks
+    // l, l + 8, l + 16, ... of unit u0 + g in increasing order (8 in flight),
+    // then the group's 8 partial sums reduce by a fixed butterfly
+    const int grp = lane / kLanesPerRow, gl = lane % kLanesPerRow;
+    const int nunits = (g1 - g0) * nrows;
+    for (int u0 = warp * kRowsPerWarp; u0 < nunits; u0 += kWarps * kRowsPerWarp) {
+      const int unit = u0 + grp;
+      const bool live = unit < nunits;
+      const int gi = live ? g0 + unit / nrows : g0, row = live ? n0 + unit % nrows : n0;
+      const uint8_t *drow = nullptr, *dsc = nullptr;
+      if (live) down_row<WD, STAGED>(tb, gi - ib, gi, row, n0, nrows, H, I, stage, pitch, &drow, &dsc);
+      const int hbase = tb.hbase[gi] - tb.hbase[g0];
+      const int ntok = live ? tb.ntok[gi] : 0;
+      float acc[MAXT];
+#pragma unroll
+      for (int q = 0; q < MAXT; ++q) acc[q] = 0.f;
+      for (int c0 = 0; c0 < nchunks; c0 += kLanesPerRow * kChunksPerLane) {
+        uint4 w[kChunksPerLane];
+        unsigned short sc[kChunksPerLane];
+#pragma unroll
+        for (int u = 0; u < kChunksPerLane; ++u) {
+          const int c = c0 + gl + kLanesPerRow * u;
+          if (live && c < nchunks) {
+            w[u] = ld_down16<FRESH, STAGED>(drow + (int64_t)c * 16);
+            sc[u] = (WD == MOE_FP4) ? ld_down2<FRESH, STAGED>(dsc + 2 * c) : (unsigned short)0;
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < kChunksPerLane; ++u) {
+          const int c = c0 + gl + kLanesPerRow * u;
+          if (live && c < nchunks) {
+#pragma unroll
+            for (int q = 0; q < MAXT; ++q)
+              if (q < ntok) acc[q] += chunk_dot<WD, float>(w[u], sc[u], hs + (int64_t)(hbase + q) * I + (int64_t)c * EPC);
+          }
+        }
+      }
+#pragma unroll
+      for (int q = 0; q < MAXT; ++q) {
+        float a = acc[q];
+        a += __shfl_xor_sync(0xFFFFFFFFu, a, 4);
+        a += __shfl_xor_sync(0xFFFFFFFFu, a, 2);
+        a += __shfl_xor_sync(0xFFFFFFFFu, a, 1);
+        if (live && gl == 0 && q < ntok) {
+          int t, hr, j;
+          item_token(p, pl, tb, gi, q, &t, &hr, &j);
+          os[(row - n0) * ostride + t * (k + 1) + j] = a;
+        }
+      }
+    }
+    g0 = g1;
+  }
+  __syncthreads();
+}
+
+template <int WD, int MAXT>
+__global__ void __launch_bounds__(kThreads, 1) layer_kernel(LayerParams p) {
+  using XT = typename std::conditional<WD == MOE_FP32, float, __nv_bfloat16>::type;
+  extern __shared__ __align__(16) uint8_t smem[];
+  __shared__ CtrlSmem cs;
+  __shared__ ItemTable tb;
+  const int H = p.H, B = p.B, k = p.k;
+  const int G = gridDim.x;
+  const bool ctrl = blockIdx.x == 0;
+  XT* xs = reinterpret_cast<XT*>(smem);
+  float* hs = reinterpret_cast<float*>(smem + (((size_t)B * H * sizeof(XT) + 15) & ~(size_t)15));
+  float* os = hs + p.smem_h_floats;
+  const int n0 = (int)((int64_t)blockIdx.x * H / G), n1 = (int)((int64_t)(blockIdx.x + 1) * H / G);
+  const int nrows = n1 - n0;
+
+  // ---- 0. control | activations and the shared expert's gate/up rows --------
+  if (p.tl && blockIdx.x == 1 && threadIdx.x == 0) p.tl[0] = globaltimer_ns();
+  if (ctrl) {
+    const int cst = control_step(p, cs);  // ends with a CTA barrier after the plan writes
+    if (threadIdx.x == 0) {
+      st_release_u32(p.plan_flag, p.seq);
+      if (p.tl) p.tl[10] = globaltimer_ns();
+    }
+    if (cst == MOE_OK) {
+      control_commit(p, cs);
+      compact_oldest(p, cs);
+    }
+    if (p.tl && threadIdx.x == 0) p.tl[11] = globaltimer_ns();
+  }
+  {
+    const int nvec = (int)((size_t)B * H * sizeof(XT) / 16);
+    const uint4* src = reinterpret_cast<const uint4*>(p.x);
+    uint4* dst = reinterpret_cast<uint4*>(xs);
+    for (int i = threadIdx.x; i < nvec; i += blockDim.x) dst[i] = src[i];
+  }
+  if (!ctrl && p.has_shared) {
+    if (threadIdx.x == 0) {
+      tb.rec[0] = p.shared_rec;
+      tb.ntok[0] = B;
+      tb.pair0[0] = -1;
+      tb.hbase[0] = 0;
+      tb.hbase[1] = B;
+    }
+    __syncthreads();
+    phase1<WD, MAXT, false>(p, p.plan, tb, 0, 1, 1, G - 1, xs);
+  }
+  if (!ctrl && wait_flag(p.plan_flag, p.seq, p.err, 5000000000ull, 32) != 0) return;
+  __syncthreads();
+  const bool rec = p.tl && blockIdx.x == 1 && threadIdx.x == 0;
+  if (rec) p.tl[1] = globaltimer_ns();
+  const Plan* pl = p.plan;
+  if (pl->err != MOE_OK) return;
+
+  // ---- 1. gate/up rows of the resident routed experts --------------------------
+  const int n_res = load_items(p, pl, 0, tb);
+  if (p.device_fill && pl->n_items[1] > 0) {
+    // device-driven fills: pull each missed record from the host pool, use it
+    // for this call and store it in its slot; W_down rows by the CTA that owns them
+    const int n_all = load_items(p, pl, 1, tb, n_res, true);
+    copy_down_rows<WD>(p, tb, n_res, n_all, n0, nrows);
+    if (!ctrl) phase1<WD, MAXT, false, true>(p, pl, tb, n_res, n_all, 1, G - 1, xs);
+  }
+  // this CTA's W_down rows of the resident experts: the first n_stage items
+  // into shared memory by bulk copies completing on s_stage, the rest into L2
+  __shared__ __align__(8) uint64_t s_stage;
+  const int n_stage = nrows > 0 ? min(n_res, p.stage_items) : 0;
+  const uint8_t* stage = smem + p.stage_off;
+  {
+    const int64_t rb = Fmt<WD>::row_bytes(p.I), sb = (WD == MOE_FP4) ? p.I / 16 : 0;
+    if (threadIdx.x == 0 && n_stage > 0) {
+      mbar_init(&s_stage, 1);
+      fence_mbar_init();
+      mbar_expect_tx(&s_stage, (uint32_t)(n_stage * nrows * (rb + sb)));
+      for (int j = 0; j < n_stage; ++j) {
+        const RecView v = rec_view<WD>(tb.rec[j], H, p.I);
+        uint8_t* dst = smem + p.stage_off + (int64_t)j * p.stage_pitch;
+        bulk_g2s(dst, v.down + (int64_t)n0 * rb, (uint32_t)(nrows * rb), &s_stage);
+        if (WD == MOE_FP4) bulk_g2s(dst + nrows * rb, v.down_sc + (int64_t)n0 * sb, (uint32_t)(nrows * sb), &s_stage);
+      }
+    }
+    if ((int)threadIdx.x >= n_stage && (int)threadIdx.x < n_res && nrows > 0) {
+      const RecView v = rec_view<WD>(tb.rec[threadIdx.x], H, p.I);
+      prefetch_l2(v.down + (int64_t)n0 * rb, (uint32_t)(nrows * rb));
+      if (WD == MOE_FP4) prefetch_l2(v.down_sc + (int64_t)n0 * sb, (uint32_t)(nrows * sb));
+    }
+  }
+  if (!ctrl) phase1<WD, MAXT, false>(p, pl, tb, 0, n_res - p.has_shared, 1, G - 1, xs);
+  if (rec) p.tl[2] = globaltimer_ns();
+  const bool bar_ok = grid_barrier(p.bar, p.bar_base + (unsigned long long)G, p.err);
+  if (n_stage > 0 && !mbar_wait(&s_stage, 0)) {  // the staging copies never leave this CTA in flight
+    if (threadIdx.x == 0) atomicExch(p.err, MOE_ERR_TIMEOUT);
+    mbar_wait(&s_stage, 0);
+    return;
+  }
+  if (!bar_ok) return;
+  if (rec) p.tl[3] = globaltimer_ns();
+
+  // ---- 2. W_down rows of the resident experts --------------------------------------
+  const int ostride = B * (k + 1);
+  for (int i = threadIdx.x; i < nrows * ostride; i += blockDim.x) os[i] = 0.f;
+  phase2<WD, MAXT, false, true>(p, pl, tb, 0, n_stage, n0, nrows, hs, os, stage, p.stage_pitch);
+  phase2<WD, MAXT, false>(p, pl, tb, n_stage, n_res, n0, nrows, hs, os);
+  if (rec) p.tl[4] = globaltimer_ns();
+
+  // ---- 3. fills, each as soon as its copy has landed -------------------------------
+  const int nf = pl->n_items[1];
+  int fill_err = 0;
+  if (nf > 0 && p.device_fill) {
+    // device-driven fills: this CTA copied its own W_down rows of every fill
+    // into the slots in phase 1, so they are read there, not over the link
+    for (int it = n_res + (int)threadIdx.x; it < n_res + nf; it += blockDim.x) tb.rec[it] = tb.dst[it];
+    __syncthreads();
+    phase2<WD, MAXT, true>(p, pl, tb, n_res, n_res + nf, n0, nrows, hs, os);
+  } else if (nf > 0) {
+    load_items(p, pl, 1, tb);
+    for (int f = 0; f < nf && !fill_err; ++f) {
+      if (wait_flag(&p.fill_flags[f], p.seq, p.err) != 0) {
+        fill_err = 1;
+        break;
+      }
+      if (rec && f == 0) p.tl[5] = globaltimer_ns();
+      phase1<WD, MAXT, true>(p, pl, tb, f, f + 1, 0, G, xs);
+    }
+    if (rec) p.tl[6] = globaltimer_ns();
+    if (!grid_barrier(p.bar, p.bar_base + 2ull * G, p.err)) return;
+    if (rec) p.tl[7] = globaltimer_ns();
+    for (int f = 0; f < nf && !fill_err; ++f) {
+      if (wait_flag(&p.fill_flags[kMaxU + f], p.seq, p.err) != 0) {
+        fill_err = 1;
+        break;
+      }
+      if (rec && f == nf - 1) p.tl[8] = globaltimer_ns();
+      phase2<WD, MAXT, true>(p, pl, tb, f, f + 1, n0, nrows, hs, os);
+    }
+    if (fill_err) {
+      if (ctrl) undo_call(p);
+      return;
+    }
+  }
+
+  // ---- 4. weighted combine in rank order --------------------------------------------
+  for (int e = threadIdx.x; e < nrows * B; e += blockDim.x) {
+    const int nl = e / B, t = e % B, n = n0 + nl;
+    const float* o = os + nl * ostride + t * (k + 1);
+    float acc = 0.f;
+    for (int j = 0; j < k; ++j) acc = fmaf(tb.pair_w[t * k + j], o[j], acc);
+    if (p.has_shared) acc += o[k];
+    if constexpr (WD == MOE_FP32)
+      reinterpret_cast<float*>(p.y)[(int64_t)t * H + n] = acc;
+    else
+      reinterpret_cast<__nv_bfloat16*>(p.y)[(int64_t)t * H + n] = __float2bfloat16_rn(acc);
+  }
+  if (rec) p.tl[9] = globaltimer_ns();
+}
+
+// Cooperative launch of one instantiation (dynamic shared memory raised once
+// per instantiation to the largest size asked for).
+template <int WD, int MAXT>
+cudaError_t launch_t(const LayerParams& p, int grid, size_t smem, cudaStream_t s) {
+  auto fn = layer_kernel<WD, MAXT>;
+  static size_t smem_set = 0;  // largest dynamic shared memory already allowed for this instantiation
+  if (smem > smem_set) {
+    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    smem_set = smem;
+  }
+  void* args[] = {const_cast<LayerParams*>(&p)};
+  return cudaLaunchCooperativeKernel((const void*)fn, dim3(grid), dim3(kThreads), args, smem, s);
+}
+
+}  // namespace moe
