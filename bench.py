@@ -48,6 +48,21 @@ def load_peaks():
     return {"hbm_gbs": FALLBACK_HBM_GBS}, "fallback"
 
 
+# ------------------------------------------------------------ multi-rank --
+def max_over_ranks(x: float, dist, device) -> float:
+    """The largest x over all ranks (every rank gets it); x itself without a
+    process group.  The timed region of each rank is reduced this way, so a
+    whole-job rate divides the units all ranks processed by the slowest rank's
+    time."""
+    if dist is None:
+        return x
+    import torch
+
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 # --------------------------------------------------------------- clocks --
 class ClockSampler:
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -256,10 +271,7 @@ def run_native(args, w):
     mc.moe_cache_set_profiling(cache.handle, False)
     stats = mc.moe_cache_stats(cache.handle)
     phases = mc.moe_cache_phase_times(cache.handle) if args.profile >= 2 else None
-    if dist:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, dist, dev)
     tokens = w.B * K * world
     value = tokens / (ms / 1e3)
 
@@ -287,10 +299,7 @@ def run_native(args, w):
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1)
-    if dist:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e2e_ms, dist, dev)
     e2e_value = w.B * K_e2e * world / (e2e_ms / 1e3) if K_e2e else None
 
     # ablation: the same timed steps with the other fill mechanism (copy
