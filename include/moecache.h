@@ -196,7 +196,12 @@ moe_status moe_layer_forward_ex(moe_cache_t cache, int32_t layer, const void* x,
  * pool; while layer l runs on one, all E records of layer l+1 stream into the
  * other on the copy stream.  x: device [n_layers][T][H] bf16 (each layer's
  * input), logits: device float32 [n_layers][T][E], y: device
- * [n_layers][T][H] bf16.  Only MOE_BF16 / MOE_FP4 models.
+ * [n_layers][T][H] bf16.  Only MOE_BF16 / MOE_FP4 models; prefill also
+ * needs I % 128 == 0 and H % 256 == 0.  The expert GEMMs accumulate in
+ * float32; their operands are bf16 for MOE_BF16 models and f16 for MOE_FP4
+ * models (the activations convert exactly for |x| <= 65504, the FP4 weights
+ * expand exactly, the SwiGLU intermediate is rounded to f16).  The slots of
+ * the two buffers (the last 2*E slots) hold no decode expert afterwards.
  * Errors: MOE_ERR_CAPACITY if the pool has fewer than 2*E slots,
  * MOE_ERR_INVALID_ARG, MOE_ERR_OOM, MOE_ERR_CUDA. */
 moe_status moe_prefill_stream(moe_cache_t cache, int32_t layer_begin, int32_t layer_end, const void* x,
