@@ -1,34 +1,40 @@
 #!/usr/bin/env python3
-"""Decode benchmark of the routed-MoE layer served from the shared GPU expert cache.
+"""Benchmark of the routed-MoE layer served from the shared GPU expert cache.
 
-Workload (default): Qwen3.6-35B-A3B-shaped decode — 40 MoE layers, hidden
+Headline (``value``): Qwen3.6-35B-A3B-shaped decode — 40 MoE layers, hidden
 2048, per-expert SwiGLU intermediate 512, 256 experts, top-8, one shared
 expert, bf16 weights ~N(0, 0.02) and bf16 activations, batch 1, AR(1) router
 logits (logit_t = 0.8 logit_{t-1} + 0.6 N(0,1)), cache of 5,120 slots (50% of
-the 10,240 layer-experts) backed by a 64.4 GB pinned host pool.  All inputs
-are seeded and synthetic.
+the 10,240 layer-experts) backed by a 64.4 GB pinned host pool, misses filled
+by cudaMemcpyAsync on the copy streams.  One step = one decode token through
+all 40 layers (router, cache control, fills, expert FFN, combine).  W warm-up
+steps start from a cold cache; the K timed steps continue the same trace.
 
-One step = one decode token through all 40 layers (router, cache control,
-fills, expert FFN, combine).  W warm-up steps start from a cold cache; the K
-timed steps continue the same trace.  Prints one JSON line.
+The same JSON line carries the other legs of the metric, each measured the
+same way (one pair of CUDA events around the timed steps, per-launch
+profiling off; per-launch statistics come from a separate pass):
+  decode_c2_device  the headline workload with device-driven fills;
+  decode_c3_b1/b8   DeepSeek-V4-Flash-shaped FP4 decode at batch 1 and 8;
+  prefill_c4        a 4096-token prompt through the 43 FP4 layers;
+  elastic_c5        Qwen3.6-shaped decode with the cache resized 60% -> 25%
+                    -> 80% of the layer-experts at steps 512 and 1280.
+All inputs are seeded and synthetic.  Prints one JSON line.
 
-    python bench.py [--steps K] [--warmup W] [--gpus N] [--impl native|reference]
+    python bench.py [--steps K] [--warmup W] [--gpus N] [--impl native|reference] [--legs ...]
 """
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
-# the oracle leg runs on one host thread: pin BLAS before numpy loads
-for _v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
-    os.environ.setdefault(_v, "1")
-
-import numpy as np  # noqa: E402
+import numpy as np
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
@@ -38,14 +44,32 @@ from synth import configs  # noqa: E402
 
 METRIC = "MoE decode tok/s + prefill tok/s; HBM GB/s (tensor %) vs peak; cache hit rate"
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+ALL_LEGS = ("c2_device", "c3", "c4", "c5")
 
 
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
-        d = json.load(open(p))
-        return d, "measured"
-    return {"hbm_gbs": FALLBACK_HBM_GBS}, "fallback"
+        with open(p) as f:
+            return json.load(f), "measured"
+    return {"hbm_gbs": FALLBACK_HBM_GBS, "bf16_tflops": FALLBACK_BF16_TFLOPS,
+            "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+def blas_threads() -> int | None:
+    """Threads numpy's BLAS uses (None when it cannot be asked)."""
+    try:
+        import threadpoolctl
+
+        info = threadpoolctl.threadpool_info()
+        n = [d.get("num_threads") for d in info if d.get("user_api") == "blas"]
+        return int(n[0]) if n else None
+    except Exception:
+        for v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS"):
+            if os.environ.get(v, "").isdigit():
+                return int(os.environ[v])
+        return None
 
 
 # ------------------------------------------------------------ multi-rank --
@@ -65,23 +89,25 @@ def max_over_ranks(x: float, dist, device) -> float:
 
 # --------------------------------------------------------------- clocks --
 class ClockSampler:
+    """nvidia-smi clock and throttle-reason samples every 200 ms while running."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, path, device_index=0):
-        self.path = path
+    def __init__(self, device_index=0):
         self.proc = None
         self.dev = device_index
+        self.f = None
 
     def start(self):
         try:
-            self.f = open(self.path, "w")
+            self.f = tempfile.TemporaryFile(mode="w+")
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.FIELDS}",
                                           "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.f,
                                          stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
+        return self
 
     def stop(self):
         if self.proc is None:
@@ -91,16 +117,19 @@ class ClockSampler:
             self.proc.wait(timeout=5)
         except Exception:
             self.proc.kill()
+        self.f.seek(0)
+        lines = self.f.read().splitlines()
         self.f.close()
-        sm, mx, reasons = [], 0.0, set()
+        sm, mx, power, reasons = [], 0.0, [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in open(self.path):
+        for line in lines:
             parts = [p.strip() for p in line.split(",")]
             if len(parts) < 9:
                 continue
             try:
                 sm.append(float(parts[1]))
                 mx = max(mx, float(parts[2]))
+                power.append(float(parts[3]))
             except ValueError:
                 continue
             for n, v in zip(names, parts[5:9]):
@@ -108,7 +137,8 @@ class ClockSampler:
                     reasons.add(n)
         if not sm:
             return None
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm),
+                "power_w_max": max(power) if power else None}
 
 
 # ------------------------------------------------------------ oracle leg --
@@ -152,7 +182,7 @@ def oracle_tokens(w, lg, n_tokens, layers=None, pool_np=None):
 
 
 def run_reference(args, w):
-    """The reference arm: the CPU oracle as it stands, on host cores, on a
+    """The reference arm: the CPU oracle as it stands, on the host cores, on a
     bounded sample per step (4 layer calls of one token)."""
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
@@ -161,8 +191,7 @@ def run_reference(args, w):
     T = args.warmup + args.steps
     lg = synth.ar1_logits(w.seed, max(T, 1), w.L, w.B, w.E)
     done = 0
-    # warm-up steps untimed
-    for s in range(args.warmup):
+    for s in range(args.warmup):  # warm-up steps, untimed
         oracle_tokens(w, lg[s:s + 1], 1, layers=[(s * per_step_layers + i) % w.L for i in range(per_step_layers)])
     secs = 0.0
     for s in range(args.warmup, T):
@@ -175,9 +204,9 @@ def run_reference(args, w):
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tok/s (decode)", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs / max(1, args.steps) * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": w.name, "layers": w.L, "experts": w.E, "top_k": w.k, "hidden": w.H,
-                   "intermediate": w.I, "batch": w.B, "cache_slots": w.C},
-        "cpu_baseline": {"value": value, "unit": "tok/s (decode)", "cores": 1, "kind": "oracle",
+        "config": decode_config(w),
+        "cpu_baseline": {"value": value, "unit": "tok/s (decode)", "cores": os.cpu_count(),
+                         "blas_threads": blas_threads(), "kind": "oracle",
                          "sample": f"{per_step_layers} layer calls of one token per step, float64 numpy"},
         "e2e": {"value": value, "unit": "tok/s (decode)", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -185,7 +214,17 @@ def run_reference(args, w):
     return 0
 
 
-# ------------------------------------------------------------ native leg --
+# ------------------------------------------------------------ native legs --
+def decode_config(w):
+    return {"workload": w.name, "layers": w.L, "experts": w.E, "top_k": w.k, "hidden": w.H, "intermediate": w.I,
+            "shared_expert": w.shared, "batch": w.B, "cache_slots": w.C,
+            "weights": synth.WD_NAMES[w.wdtype] + (" (e2m1 + e4m3 per 16)" if w.wdtype == synth.WD_FP4 else ""),
+            "record_bytes": synth.record_bytes(w.H, w.I, w.wdtype),
+            "host_pool_GB": round(w.LE * synth.record_bytes(w.H, w.I, w.wdtype) / 1e9, 2),
+            "trace": "AR(1) logits rho=0.8 sd=0.6 per (layer, sequence, expert), cold cache at warm-up start",
+            "l2": "per-step expert stream >> 129 MB L2 (no reuse across layers); no flush"}
+
+
 def measure_link(dev, pool, S, n=96):
     """B_P: sustained host->device bandwidth of back-to-back cudaMemcpyAsync of
     expert records spread evenly over the whole pinned pool, GB/s (the link
@@ -205,11 +244,265 @@ def measure_link(dev, pool, S, n=96):
     return n * S / (a.elapsed_time(b) / 1e3) / 1e9
 
 
-def run_native(args, w):
+class DecodeInputs:
+    """Pinned pool, shared experts, logits and activations of a decode workload."""
+
+    def __init__(self, w, T, dev, pool=None, x_from_synth=True):
+        import torch
+
+        from expert_cache_serving_gb300 import runner
+
+        t0 = time.perf_counter()
+        self.w, self.T, self.dev = w, T, dev
+        self.pool = runner.build_pool(w) if pool is None else pool
+        self.shared = runner.build_shared(w, dev)
+        self.S = synth.record_bytes(w.H, w.I, w.wdtype)
+        self.lg_host = synth.ar1_logits(w.seed, T, w.L, w.B, w.E)
+        if x_from_synth:
+            self.x_host = torch.stack([torch.stack([runner.activations(w, s, l) for l in range(w.L)])
+                                       for s in range(T)])
+        else:  # long traces: seeded N(0,1) activations drawn on the host by torch
+            g = torch.Generator().manual_seed(w.seed)
+            self.x_host = torch.randn((T, w.L, w.B, w.H), generator=g).to(runner.x_dtype(w))
+        self.lg_dev = torch.from_numpy(self.lg_host).to(dev)
+        self.x_dev = self.x_host.to(dev)
+        self.y_dev = torch.empty_like(self.x_dev[0])
+        self.setup_s = time.perf_counter() - t0
+
+
+def decode_pass(inp, W, K, fill_mode, profile=0, host_io=False, resize=None, max_slots=0):
+    """One fresh cache; W untimed warm-up steps from cold, then K steps timed
+    with one pair of CUDA events on the launching stream (per-launch events
+    only when profile > 0).  host_io: every timed step copies its activations
+    and logits from pinned host memory and its outputs back (end to end).
+    resize: {step: slots}, applied at the safe point before that step; the
+    phases between resizes are timed separately.  Returns a dict."""
     import torch
 
     from expert_cache_serving_gb300 import moecache as mc
     from expert_cache_serving_gb300 import runner
+
+    w, dev = inp.w, inp.dev
+    stream = torch.cuda.current_stream()
+    cache = runner.Cache(w, inp.pool, inp.shared, max_slots=max_slots)
+    mc.moe_cache_set_fill_mode(cache.handle, mc.MOE_FILL_DEVICE if fill_mode == "device" else mc.MOE_FILL_COPY)
+    y = inp.y_dev
+
+    def step(s, x, lg):
+        for l in range(w.L):
+            st = cache.forward(l, x[l], lg[l], y[l], w.B, stream=stream)
+            if st != mc.MOE_OK:
+                raise mc.MoeError(st, "moe_layer_forward")
+
+    for s in range(W):
+        step(s, inp.x_dev[s], inp.lg_dev[s])
+    torch.cuda.synchronize()
+    mc.check(mc.moe_cache_sync(cache.handle, stream), "moe_cache_sync")
+    mc.moe_cache_reset_stats(cache.handle)
+    mc.moe_cache_set_profiling(cache.handle, profile)
+    h2d = d2h = 0
+    if host_io:
+        x_pin = inp.x_host.pin_memory()
+        lg_pin = torch.from_numpy(inp.lg_host).pin_memory()
+        y_pin = torch.empty_like(x_pin[:1]).pin_memory()
+        xs = torch.empty_like(inp.x_dev[0])
+        ls = torch.empty_like(inp.lg_dev[0])
+        h2d = xs.numel() * xs.element_size() + ls.numel() * ls.element_size()
+        d2h = y.numel() * y.element_size()
+    bounds = sorted(set([W] + [s for s in (resize or {}) if W < s < W + K] + [W + K]))
+    phases = []
+    clk = ClockSampler(dev.index or 0).start()
+    for a, b in zip(bounds, bounds[1:]):
+        resize_ms = None
+        if resize and a in resize and a > W:
+            t0 = time.perf_counter()
+            torch.cuda.synchronize()
+            mc.check(mc.moe_cache_sync(cache.handle, stream), "moe_cache_sync")
+            mc.moe_cache_resize(cache.handle, resize[a], stream)
+            resize_ms = (time.perf_counter() - t0) * 1e3
+        mc.moe_cache_reset_stats(cache.handle)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for s in range(a, b):
+            if host_io:
+                xs.copy_(x_pin[s], non_blocking=True)
+                ls.copy_(lg_pin[s], non_blocking=True)
+                step(s, xs, ls)
+                y_pin[0].copy_(y, non_blocking=True)
+            else:
+                step(s, inp.x_dev[s], inp.lg_dev[s])
+        e1.record(stream)
+        torch.cuda.synchronize()
+        mc.check(mc.moe_cache_sync(cache.handle, stream), "moe_cache_sync")
+        ms = e0.elapsed_time(e1)
+        st = mc.moe_cache_stats(cache.handle)
+        phases.append({"steps": [a, b], "ms": ms, "stats": st, "resize_ms": resize_ms,
+                       "slots": mc.moe_cache_state(cache.handle, 0)[2]})
+    clocks = clk.stop()
+    mc.moe_cache_set_profiling(cache.handle, 0)
+    pt = mc.moe_cache_phase_times(cache.handle) if profile >= 2 else None
+    cache.close()
+    ms = sum(p["ms"] for p in phases)
+    tot = {}
+    for p in phases:
+        for k_, v in p["stats"].items():
+            tot[k_] = tot.get(k_, 0) + v
+    return {"ms": ms, "stats": tot, "phases": phases, "clocks": clocks, "h2d": h2d, "d2h": d2h, "phase_us": pt}
+
+
+def hit_rate(st):
+    return st["hits"] / (st["hits"] + st["misses"]) if st["hits"] + st["misses"] else None
+
+
+def kernel_roofline(st, S, peak):
+    """Layer-kernel HBM roofline from a profiled pass: algorithmic bytes (records
+    streamed x record bytes) of the calls without fills over their summed
+    CUDA-event launch time."""
+    n = st["hit_only_timed"]
+    recs = st["hit_only_records"] / n if n else None
+    avg_us = st["hit_only_ms"] * 1e3 / n if n else None
+    achieved = recs * S / (avg_us / 1e6) / 1e9 if n else None
+    return {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+            "frac": achieved / peak if achieved else None, "traffic": None,
+            "algorithmic_bytes_per_launch": recs * S if n else None, "launches": n, "avg_launch_us": avg_us,
+            "all_launches_avg_us": st["layer_ms"] * 1e3 / max(1, st["layer_timed"])}
+
+
+def decode_leg(inp, W, K, peak, b_p, fill_mode="copy", profile=True):
+    """Timed pass (profiling off) plus a profiled pass for the kernel roofline."""
+    w = inp.w
+    main = decode_pass(inp, W, K, fill_mode)
+    st = main["stats"]
+    value = w.B * K / (main["ms"] / 1e3)
+    hbm_s = st["records_streamed"] * inp.S / (peak * 1e9)
+    link_s = st["bytes_filled"] / (b_p * 1e9)
+    roof = w.B * K / max(hbm_s, link_s) if max(hbm_s, link_s) > 0 else None
+    out = {"value": value, "unit": "tok/s (decode)", "ms_per_step": main["ms"] / K, "steps": K, "warmup": W,
+           "fill_mode": fill_mode, "hit_rate": hit_rate(st),
+           "hit_rate_note": f"over the {K} timed steps after {W} warm-up steps from a cold cache",
+           "routed_pair_hit_rate": st["routed_pair_hits"] / st["routed_pairs"] if st["routed_pairs"] else None,
+           "fill_GB_per_token": st["bytes_filled"] / 1e9 / (w.B * K),
+           "link": {"B_P_GBps": b_p, "roofline_tok_s": roof, "frac": value / roof if roof else None,
+                    "note": "bound = max(expert bytes / HBM peak, fill bytes / B_P) over the timed steps"},
+           "deferred_calls": st["deferred_calls"], "gpu_launches": st["layer_launches"] + st["finish_launches"],
+           "host_us_per_call": {"wait_for_miss_list": st["host_wait_us"] / max(1, st["calls"]),
+                                "issue_fills": st["host_issue_us"] / max(1, st["calls"])},
+           "clocks": main["clocks"]}
+    if profile:
+        prof = decode_pass(inp, W, K, "device", profile=1)
+        out["roofline"] = kernel_roofline(prof["stats"], inp.S, peak)
+        out["roofline"]["kernel"] = "layer_kernel, calls without fills (profiled pass, device-fill mode)"
+    return out, main
+
+
+def prefill_leg(w, pool, dev, W, K, peaks, peak_kind):
+    """Config 4: one T-token prompt through every layer of the FP4 model per
+    step, layer l+1's experts streamed host->device while layer l runs."""
+    import torch
+
+    from expert_cache_serving_gb300 import moecache as mc
+    from expert_cache_serving_gb300 import runner
+
+    T, L = w.B, w.L
+    xs = np.stack([synth.activations_bf16(w.seed, 0, l, T, w.H) for l in range(L)])
+    x = torch.from_numpy(xs.view(np.int16)).view(torch.bfloat16).to(dev)
+    del xs
+    logits = torch.from_numpy(synth.iid_logits(w.seed, L, T, w.E)).to(dev)
+    y = torch.empty_like(x)
+    cache = runner.Cache(w, pool, None, C=w.C, max_tokens=1)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        st = mc.moe_prefill_stream(cache.handle, 0, L, x, logits, T, y, stream)
+        if st != mc.MOE_OK:
+            raise mc.MoeError(st, "moe_prefill_stream")
+
+    def timed(n, profile):
+        mc.moe_cache_reset_stats(cache.handle)
+        mc.moe_cache_set_profiling(cache.handle, profile)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(n):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        mc.moe_cache_set_profiling(cache.handle, 0)
+        return e0.elapsed_time(e1), mc.moe_cache_stats(cache.handle)
+
+    for _ in range(W):
+        step()
+    torch.cuda.synchronize()
+    clk = ClockSampler(dev.index or 0).start()
+    ms, _ = timed(K, 0)
+    clocks = clk.stop()
+    pms, st = timed(1, 1)
+    cache.close()
+    S = synth.record_bytes(w.H, w.I, w.wdtype)
+    value = T * K / (ms / 1e3)
+    gemm_tflops = st["prefill_gemm_flop"] / (st["prefill_gemm_ms"] / 1e3) / 1e12 if st["prefill_gemm_ms"] else None
+    peak_tf = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops", FALLBACK_BF16_TFLOPS)))
+    copy_bytes = L * w.E * S
+    return {
+        "value": value, "unit": "tok/s (prefill)", "ms_per_step": ms / K, "steps": K, "warmup": W,
+        "dtype": "f16 operands (FP4 weights expanded exactly), fp32 accumulation",
+        "config": {"workload": w.name, "layers": L, "experts": w.E, "top_k": w.k, "hidden": w.H,
+                   "intermediate": w.I, "prompt_tokens": T, "cache_slots": w.C, "record_bytes": S,
+                   "step": "one prompt through all layers", "logits": "i.i.d. N(0,1) per (token, layer, expert)",
+                   "l2": "each layer streams 3.6 GB of experts >> 129 MB L2; no flush"},
+        "roofline": {"bound": "tensor", "achieved": gemm_tflops, "peak": peak_tf, "unit": "TFLOP/s",
+                     "frac": gemm_tflops / peak_tf if gemm_tflops else None, "traffic": None,
+                     "kernel": "grouped tcgen05 GEMMs (gate/up + down), weights resident in the layer buffer",
+                     "peak_kind": peak_kind + " bf16 sustained (f16 dense rate is the same)",
+                     "gemm_ms_per_step": st["prefill_gemm_ms"], "flop_per_step": st["prefill_gemm_flop"]},
+        "link": {"copy_ms_per_step": st["prefill_copy_ms"], "compute_ms_per_step": st["prefill_compute_ms"],
+                 "profiled_step_ms": pms,
+                 "exposed_copy_ms_per_step": max(0.0, ms / K - st["prefill_compute_ms"]),
+                 "bound_ms_per_step": max(st["prefill_copy_ms"], st["prefill_compute_ms"]),
+                 "frac_of_bound": max(st["prefill_copy_ms"], st["prefill_compute_ms"]) / (ms / K),
+                 "stream_GBps": copy_bytes / (st["prefill_copy_ms"] / 1e3) / 1e9 if st["prefill_copy_ms"] else None,
+                 "note": "copy/compute split from a separate profiled step"},
+        "clocks": clocks,
+    }
+
+
+def elastic_leg(w, dev, batches, fill_mode="copy"):
+    """Config 5: the cache budget resized 60% -> 25% -> 80% at fixed safe-point
+    steps; hit rate and tok/s per phase, the moves, and the host pool's
+    address and checksum before and after."""
+    import torch
+
+    out = {"fill_mode": fill_mode, "schedule": [[s, c] for s, c in w.resize], "initial_slots": w.C, "batches": {}}
+    pool = None
+    for B in batches:
+        wb = w.with_(B=B)
+        inp = DecodeInputs(wb, wb.steps, dev, pool=pool, x_from_synth=False)
+        pool = inp.pool
+        ptr = pool.ctypes.data
+        digest = hashlib.blake2b(np.ascontiguousarray(pool[::997]).tobytes(), digest_size=16).hexdigest()
+        res = decode_pass(inp, 0, wb.steps, fill_mode, resize=dict(wb.resize), max_slots=wb.LE)
+        phases = []
+        for p in res["phases"]:
+            st = p["stats"]
+            n = p["steps"][1] - p["steps"][0]
+            phases.append({"steps": p["steps"], "slots": p["slots"], "tok_s": B * n / (p["ms"] / 1e3),
+                           "hit_rate": hit_rate(st), "misses": st["misses"], "evictions": st["evictions"],
+                           "resize_moves": st["resize_moves"], "resize_evictions": st["resize_evictions"],
+                           "resize_ms": p["resize_ms"]})
+        after = hashlib.blake2b(np.ascontiguousarray(pool[::997]).tobytes(), digest_size=16).hexdigest()
+        out["batches"][str(B)] = {"phases": phases, "tok_s": B * wb.steps / (res["ms"] / 1e3),
+                                  "pool_unchanged": after == digest and pool.ctypes.data == ptr,
+                                  "clocks": res["clocks"]}
+        del inp, res
+    out["note"] = ("whole 2048-step trace from a cold cache; resize time (a synchronising safe point) is "
+                   "reported per phase and excluded from the phase's tok/s")
+    torch.cuda.empty_cache()
+    return out
+
+
+def run_native(args):
+    import torch
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -222,295 +515,129 @@ def run_native(args, w):
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     dev = torch.device("cuda", local)
     peaks, peak_kind = load_peaks()
-    out_dir = os.path.join(ROOT, "gpurun_out")
-    os.makedirs(out_dir, exist_ok=True)
-
+    hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
     W, K = args.warmup, args.steps
-    K_e2e = K if args.e2e_steps is None else args.e2e_steps
-    T = W + K + K_e2e
-    t_setup = time.perf_counter()
-    pool = runner.build_pool(w)
-    shared = runner.build_shared(w, dev)
-    S = synth.record_bytes(w.H, w.I, w.wdtype)
-    lg_host = synth.ar1_logits(w.seed, T, w.L, w.B, w.E)
-    x_host = torch.stack([torch.stack([runner.activations(w, s, l) for l in range(w.L)]) for s in range(T)])
-    lg_dev = torch.from_numpy(lg_host).to(dev)
-    x_dev = x_host.to(dev)
-    y_dev = torch.empty_like(x_dev)
-    cache = runner.Cache(w, pool, shared)
-    mc.moe_cache_set_fill_mode(cache.handle, mc.MOE_FILL_DEVICE if args.fill_mode == "device" else mc.MOE_FILL_COPY)
-    setup_s = time.perf_counter() - t_setup
-    stream = torch.cuda.current_stream()
+    legs = set(ALL_LEGS if args.legs == "all" else [x for x in args.legs.split(",") if x])
+    t_all = time.perf_counter()
 
-    def step(s, x, lg, y):
-        for l in range(w.L):
-            st = cache.forward(l, x[s, l], lg[s, l], y[s, l], w.B, stream=stream)
-            if st != mc.MOE_OK:
-                raise mc.MoeError(st, "moe_layer_forward")
-
-    for s in range(W):
-        step(s, x_dev, lg_dev, y_dev)
-    torch.cuda.synchronize()
-    mc.moe_cache_reset_stats(cache.handle)
-    mc.moe_cache_set_profiling(cache.handle, args.profile)
-    clk = ClockSampler(os.path.join(out_dir, f"clocks_rank{rank}.csv"), local)
-    clk.start()
+    # ---- headline: config 2, copy-mode fills ---------------------------------------
+    w = configs.C2 if args.workload == "c2" else configs.SMALL_BF16
+    inp = DecodeInputs(w, W + K, dev)
+    b_p = measure_link(dev, inp.pool, inp.S)
     if dist:
         dist.barrier()
-    torch.cuda.synchronize()
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    ev0.record(stream)
-    for s in range(W, W + K):
-        step(s, x_dev, lg_dev, y_dev)
-    ev1.record(stream)
-    torch.cuda.synchronize()
+    head = decode_pass(inp, W, K, "copy")
+    ms = max_over_ranks(head["ms"], dist, dev)
+    value = w.B * K * world / (ms / 1e3)
     if dist:
         dist.barrier()
-    clocks = clk.stop()
-    ms = ev0.elapsed_time(ev1)
-    mc.moe_cache_set_profiling(cache.handle, False)
-    stats = mc.moe_cache_stats(cache.handle)
-    phases = mc.moe_cache_phase_times(cache.handle) if args.profile >= 2 else None
-    ms = max_over_ranks(ms, dist, dev)
-    tokens = w.B * K * world
-    value = tokens / (ms / 1e3)
-
-    # end to end through the C ABI with host buffers: per step copy the
-    # step's activations and logits from pinned host memory, run the layers,
-    # copy the outputs back
-    x_pin = x_host.pin_memory()
-    lg_pin = torch.from_numpy(lg_host).pin_memory()
-    y_pin = torch.empty_like(x_pin).pin_memory()
-    xs_dev = torch.empty((1,) + tuple(x_dev.shape[1:]), dtype=x_dev.dtype, device=dev)
-    ls_dev = torch.empty((1,) + tuple(lg_dev.shape[1:]), dtype=lg_dev.dtype, device=dev)
-    ys_dev = torch.empty_like(xs_dev)
-    h2d = xs_dev.numel() * xs_dev.element_size() + ls_dev.numel() * ls_dev.element_size()
-    d2h = ys_dev.numel() * ys_dev.element_size()
-    if dist:
-        dist.barrier()
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for s in range(W + K, T):
-        xs_dev.copy_(x_pin[s:s + 1], non_blocking=True)
-        ls_dev.copy_(lg_pin[s:s + 1], non_blocking=True)
-        step(0, xs_dev, ls_dev, ys_dev)
-        y_pin[s:s + 1].copy_(ys_dev, non_blocking=True)
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1)
-    e2e_ms = max_over_ranks(e2e_ms, dist, dev)
-    e2e_value = w.B * K_e2e * world / (e2e_ms / 1e3) if K_e2e else None
-
-    # ablation: the same timed steps with the other fill mechanism (copy
-    # engine + stream flags vs the kernel pulling misses over the host link)
-    ablation = None
-    if not args.no_ablation:
-        other = "device" if args.fill_mode == "copy" else "copy"
-        cache.close()
-        cache_b = runner.Cache(w, pool, shared)
-        mc.moe_cache_set_fill_mode(cache_b.handle, mc.MOE_FILL_DEVICE if other == "device" else mc.MOE_FILL_COPY)
-
-        def step_b(s):
-            for l in range(w.L):
-                st = cache_b.forward(l, x_dev[s, l], lg_dev[s, l], y_dev[s, l], w.B, stream=stream)
-                if st != mc.MOE_OK:
-                    raise mc.MoeError(st, "moe_layer_forward")
-
-        for s in range(W):
-            step_b(s)
-        torch.cuda.synchronize()
-        mc.moe_cache_reset_stats(cache_b.handle)
-        mc.moe_cache_set_profiling(cache_b.handle, 1)
-        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a0.record(stream)
-        for s in range(W, W + K):
-            step_b(s)
-        a1.record(stream)
-        torch.cuda.synchronize()
-        ms_b = a0.elapsed_time(a1)
-        mc.moe_cache_set_profiling(cache_b.handle, False)
-        sb = mc.moe_cache_stats(cache_b.handle)
-        ablation = {"fill_mode": other, "value": w.B * K * world / (ms_b / 1e3), "unit": "tok/s (decode)",
-                    "ms_per_step": ms_b / K,
-                    "hit_only_avg_launch_us": sb["hit_only_ms"] * 1e3 / max(1, sb["hit_only_timed"]),
-                    "all_launches_avg_us": sb["layer_ms"] * 1e3 / max(1, sb["layer_timed"]),
-                    "hit_rate": sb["hits"] / max(1, sb["hits"] + sb["misses"]),
-                    "note": "same trace steps and pool, measured after the main leg in the same process"}
-        cache = cache_b
-
-    # roofline of the dominant kernel (the layer kernel): algorithmic bytes =
-    # every expert record it streams once (S bytes each).  Calls with fills
-    # also wait for the host link inside the kernel, so the HBM figure is
-    # taken over the launches of calls without fills; the link-inclusive
-    # bound covers every call.
-    hit_bytes = stats["hit_only_records"] * S
-    # DRAM traffic of the layer kernel from the committed ncu capture
-    # (profiles/decode_layer_kernel_small_full.md: same expert shape, 8
-    # resident records read 50.508 MB + wrote 0.321 MB), scaled per record to
-    # this run's records per hit-only launch; valid for this expert shape only
-    recs_per_launch = stats["hit_only_records"] / max(1, stats["hit_only_timed"])
-    traffic = (50.508288e6 + 0.320512e6) / 8 * recs_per_launch if S == 6291456 else None
-    hit_s = stats["hit_only_ms"] / 1e3
-    achieved = hit_bytes / hit_s / 1e9 if hit_s > 0 else None
-    peak = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
-    b_p = measure_link(dev, pool, S)
-    hbm_s = stats["records_streamed"] * S / (peak * 1e9)
-    link_s = stats["bytes_filled"] / (b_p * 1e9)
-    roof_tok_s = w.B * K / max(hbm_s, link_s) if max(hbm_s, link_s) > 0 else None
-    hits, misses = stats["hits"], stats["misses"]
+    e2e = decode_pass(inp, W, K, "copy", host_io=True)
+    e2e_ms = max_over_ranks(e2e["ms"], dist, dev)
+    st = head["stats"]
+    prof = decode_pass(inp, W, K, "device", profile=2 if args.profile >= 2 else 1)
+    hbm_s = st["records_streamed"] * inp.S / (hbm_peak * 1e9)
+    link_s = st["bytes_filled"] / (b_p * 1e9)
+    roof_tok_s = w.B * K / max(hbm_s, link_s)
     line = {
         "metric": METRIC, "value": value, "unit": "tok/s (decode)", "n_gpus": world, "steps": K, "warmup": W,
         "ms_per_step": ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-        "data": "synthetic",
-        "config": {"workload": w.name, "layers": w.L, "experts": w.E, "top_k": w.k, "hidden": w.H,
-                   "intermediate": w.I, "shared_expert": w.shared, "batch": w.B, "cache_slots": w.C,
-                   "record_bytes": S, "host_pool_GB": round(w.LE * S / 1e9, 2), "fill_mode": args.fill_mode,
-                   "trace": "AR(1) logits rho=0.8 sd=0.6, cold cache at warm-up start",
-                   "l2": "per-step expert stream >> 129 MB L2 (no reuse across layers); no flush"},
-        "hit_rate": hits / (hits + misses) if hits + misses else None,
-        "routed_pair_hit_rate": stats["routed_pair_hits"] / stats["routed_pairs"] if stats["routed_pairs"] else None,
-        "fill_GB_per_token": stats["bytes_filled"] / 1e9 / (w.B * K),
-        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak if achieved else None, "traffic": traffic,
-                     "algorithmic_bytes_per_launch": recs_per_launch * S,
-                     "kernel": "layer_kernel (calls without fills)", "peak_kind": peak_kind + " hbm_gbs (copy)",
-                     "launches": stats["hit_only_timed"],
-                     "avg_launch_us": stats["hit_only_ms"] * 1e3 / max(1, stats["hit_only_timed"]),
-                     "all_launches_avg_us": stats["layer_ms"] * 1e3 / max(1, stats["layer_timed"])},
-        "link": {"B_P_GBps": b_p, "fill_bytes": stats["bytes_filled"],
-                 "roofline_tok_s": roof_tok_s,
-                 "frac": value / roof_tok_s if roof_tok_s else None,
+        "data": "synthetic", "config": dict(decode_config(w), fill_mode="copy"),
+        "hit_rate": hit_rate(st),
+        "hit_rate_note": f"distinct (call, expert) accesses over the {K} timed steps, after {W} warm-up steps "
+                         f"from a cold cache",
+        "routed_pair_hit_rate": st["routed_pair_hits"] / st["routed_pairs"] if st["routed_pairs"] else None,
+        "fill_GB_per_token": st["bytes_filled"] / 1e9 / (w.B * K),
+        "roofline": dict(kernel_roofline(prof["stats"], inp.S, hbm_peak),
+                         kernel="layer_kernel, calls without fills (profiled pass, device-fill mode, same steps)",
+                         peak_kind=peak_kind + " hbm_gbs (copy)"),
+        "link": {"B_P_GBps": b_p, "fill_bytes": st["bytes_filled"], "roofline_tok_s": roof_tok_s,
+                 "frac": value / world / roof_tok_s,
                  "note": "tok/s bound = max(expert bytes / HBM peak, fill bytes / B_P) over the timed steps"},
-        "e2e": {"value": e2e_value, "unit": "tok/s (decode)", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "steps": K_e2e},
-        "ablation": ablation,
-        "gpu_launches": stats["layer_launches"],
-        "phase_us": phases,
-        "host_us_per_call": {"wait_for_miss_list": stats["host_wait_us"] / max(1, stats["calls"]),
-                             "issue_fills": stats["host_issue_us"] / max(1, stats["calls"])},
-        "clocks": clocks,
-        "setup_s": round(setup_s, 1),
+        "e2e": {"value": w.B * K * world / (e2e_ms / 1e3), "unit": "tok/s (decode)",
+                "h2d_bytes_per_step": e2e["h2d"] * w.L, "d2h_bytes_per_step": e2e["d2h"] * w.L, "steps": K,
+                "note": "same trace steps and cache history as value; per step the activations and logits of "
+                        "every layer are copied from pinned host memory and the outputs back"},
+        "gpu_launches": st["layer_launches"] + st["finish_launches"],
+        "deferred_calls": st["deferred_calls"],
+        "host_us_per_call": {"wait_for_miss_list": st["host_wait_us"] / max(1, st["calls"]),
+                             "issue_fills": st["host_issue_us"] / max(1, st["calls"])},
+        "phase_us": prof["phase_us"],
+        "clocks": head["clocks"],
+        "legs": {},
     }
     if rank == 0 and not args.no_cpu_baseline:
         n_tok = args.cpu_tokens
-        calls, secs = oracle_tokens(w, lg_host, n_tok, pool_np=pool.numpy())
-        cpu_v = calls / w.L * w.B / secs
-        line["cpu_baseline"] = {"value": cpu_v, "unit": "tok/s (decode)", "cores": 1, "kind": "oracle",
+        calls, secs = oracle_tokens(w, inp.lg_host, n_tok, pool_np=inp.pool)
+        line["cpu_baseline"] = {"value": calls / w.L * w.B / secs, "unit": "tok/s (decode)",
+                                "cores": os.cpu_count(), "blas_threads": blas_threads(), "kind": "oracle",
                                 "sample": f"first {n_tok} tokens x {w.L} layers of the trace, float64 numpy, "
                                           f"{secs:.1f} s"}
+    if "c2_device" in legs:
+        dev_leg, _ = decode_leg(inp, W, K, hbm_peak, b_p, fill_mode="device", profile=False)
+        line["legs"]["decode_c2_device"] = dev_leg
+    del inp
+    torch.cuda.empty_cache()
+
+    # ---- configs 3 and 4: the FP4 model -------------------------------------------
+    if "c3" in legs or "c4" in legs:
+        from expert_cache_serving_gb300 import runner
+
+        pool3 = runner.build_pool(configs.C3)
+        S3 = synth.record_bytes(configs.C3.H, configs.C3.I, configs.C3.wdtype)
+        b_p3 = measure_link(dev, pool3, S3)
+        if "c3" in legs:
+            for B in (1, 8):
+                w3 = configs.C3.with_(B=B, name=configs.C3.name if B == 1 else configs.C3_B8.name)
+                inp3 = DecodeInputs(w3, W + K, dev, pool=pool3)
+                leg, _ = decode_leg(inp3, W, K, hbm_peak, b_p3)
+                leg["config"] = decode_config(w3)
+                line["legs"][f"decode_c3_b{B}"] = leg
+                del inp3
+                torch.cuda.empty_cache()
+        if "c4" in legs:
+            w4 = configs.C4
+            leg = prefill_leg(w4, pool3, dev, args.prefill_warmup, args.prefill_steps, peaks, peak_kind)
+            leg["config"]["weights"] = "the config-3 model's pool (seed 3); prompt activations and logits seed 4"
+            leg["link"]["B_P_GBps"] = b_p3
+            line["legs"]["prefill_c4"] = leg
+        del pool3
+        torch.cuda.empty_cache()
+
+    # ---- config 5: elastic resize --------------------------------------------------
+    if "c5" in legs:
+        bs = [int(b) for b in args.elastic_batches.split(",") if b]
+        line["legs"]["elastic_c5"] = elastic_leg(configs.C5, dev, bs)
+
+    line["wall_s"] = round(time.perf_counter() - t_all, 1)
     if rank == 0:
         print(json.dumps(line), flush=True)
-    cache.close()
     if dist:
         dist.destroy_process_group()
-    return 0
-
-
-# ------------------------------------------------------------ prefill leg --
-def run_prefill(args, w):
-    """Config 4: one T-token prompt through every layer of the config-3 model
-    per step, layer l+1's experts streamed host->device while layer l runs."""
-    import torch
-
-    from expert_cache_serving_gb300 import moecache as mc
-    from expert_cache_serving_gb300 import runner
-
-    torch.cuda.set_device(0)
-    dev = torch.device("cuda", 0)
-    peaks, peak_kind = load_peaks()
-    T, L = w.B, w.L
-    t0 = time.perf_counter()
-    pool = runner.build_pool(w)
-    xs = np.stack([synth.activations_bf16(w.seed, 0, l, T, w.H) for l in range(L)])
-    x = torch.from_numpy(xs.view(np.int16)).view(torch.bfloat16).to(dev)
-    del xs
-    logits = torch.from_numpy(synth.iid_logits(w.seed, L, T, w.E)).to(dev)
-    y = torch.empty_like(x)
-    cache = runner.Cache(w, pool, None, C=w.C, max_tokens=1)
-    setup_s = time.perf_counter() - t0
-    stream = torch.cuda.current_stream()
-
-    def step():
-        st = mc.moe_prefill_stream(cache.handle, 0, L, x, logits, T, y, stream)
-        if st != mc.MOE_OK:
-            raise mc.MoeError(st, "moe_prefill_stream")
-
-    for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize()
-    mc.moe_cache_reset_stats(cache.handle)
-    mc.moe_cache_set_profiling(cache.handle, 1)
-    clk = ClockSampler(os.path.join(ROOT, "gpurun_out", "clocks_prefill.csv"))
-    os.makedirs(os.path.join(ROOT, "gpurun_out"), exist_ok=True)
-    clk.start()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(args.steps):
-        step()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    clocks = clk.stop()
-    ms = e0.elapsed_time(e1)
-    st = mc.moe_cache_stats(cache.handle)
-    S = synth.record_bytes(w.H, w.I, w.wdtype)
-    b_p = measure_link(dev, pool, S)
-    value = T * args.steps / (ms / 1e3)
-    gemm_tflops = st["prefill_gemm_flop"] / (st["prefill_gemm_ms"] / 1e3) / 1e12 if st["prefill_gemm_ms"] else None
-    peak_tf = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops", 1700.0)))
-    copy_bytes = L * w.E * S * args.steps
-    line = {
-        "metric": METRIC, "value": value, "unit": "tok/s (prefill)", "n_gpus": 1, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16 (FP4 weights dequantised exactly)", "data": "synthetic",
-        "config": {"workload": w.name, "layers": L, "experts": w.E, "top_k": w.k, "hidden": w.H,
-                   "intermediate": w.I, "prompt_tokens": T, "cache_slots": w.C, "record_bytes": S,
-                   "host_pool_GB": round(w.LE * S / 1e9, 1), "step": "one prompt through all layers",
-                   "l2": "each layer streams 3.6 GB of experts >> 129 MB L2; no flush"},
-        "roofline": {"bound": "tensor", "achieved": gemm_tflops, "peak": peak_tf, "unit": "TFLOP/s",
-                     "frac": gemm_tflops / peak_tf if gemm_tflops else None, "traffic": None,
-                     "kernel": "grouped tcgen05 GEMMs (gate/up + down)", "peak_kind": peak_kind + " bf16 sustained",
-                     "gemm_ms_per_step": st["prefill_gemm_ms"] / args.steps},
-        "link": {"B_P_GBps": b_p, "copy_ms_per_step": st["prefill_copy_ms"] / args.steps,
-                 "compute_ms_per_step": st["prefill_compute_ms"] / args.steps,
-                 "exposed_copy_ms_per_step": ms / args.steps - st["prefill_compute_ms"] / args.steps,
-                 "bound_ms_per_step": max(st["prefill_copy_ms"], st["prefill_compute_ms"]) / args.steps,
-                 "frac_of_bound": max(st["prefill_copy_ms"], st["prefill_compute_ms"]) / ms,
-                 "stream_GBps": copy_bytes / (st["prefill_copy_ms"] / 1e3) / 1e9 if st["prefill_copy_ms"] else None},
-        "gpu_launches": None, "clocks": clocks, "setup_s": round(setup_s, 1),
-    }
-    print(json.dumps(line), flush=True)
-    cache.close()
     return 0
 
 
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
-    ap.add_argument("--warmup", type=int, default=16)
-    ap.add_argument("--e2e-steps", type=int, default=None)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
-    ap.add_argument("--workload", default="c2", choices=["c2", "c4", "small", "small-prefill"],
-                    help="c2: Qwen3.6-shaped decode (default); c4: 4096-token FP4 prefill over 43 layers; "
-                         "small / small-prefill: 3-layer bf16 decode / 2-layer FP4 prefill for profiler captures")
+    ap.add_argument("--workload", default="c2", choices=["c2", "small"],
+                    help="headline decode workload: c2 (default) or a 3-layer bf16 case for profiler captures")
+    ap.add_argument("--legs", default="all",
+                    help="comma list of extra legs: c2_device, c3, c4, c5 ('all' default, '' for none)")
+    ap.add_argument("--prefill-steps", type=int, default=3)
+    ap.add_argument("--prefill-warmup", type=int, default=2)
+    ap.add_argument("--elastic-batches", default="1,4")
     ap.add_argument("--cpu-tokens", type=int, default=3)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--profile", type=int, default=1, help="1: CUDA events per launch; 2: also phase timestamps")
-    ap.add_argument("--no-ablation", action="store_true", help="skip the timed pass with the other fill mode")
-    ap.add_argument("--fill-mode", default="copy", choices=["copy", "device"],
-                    help="copy: host-issued cudaMemcpyAsync fills (default); device: the kernel pulls misses itself")
+    ap.add_argument("--profile", type=int, default=1, help="2: also record phase timestamps in the profiled pass")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
-    if args.workload == "c4":
-        return run_prefill(args, configs.C4)
-    if args.workload == "small-prefill":
-        return run_prefill(args, configs.C4.with_(name="small-fp4-prefill-256", L=2, E=16, C=32, B=256))
-    w = configs.C2 if args.workload == "c2" else configs.SMALL_BF16
     if args.impl == "reference":
-        return run_reference(args, w)
-    return run_native(args, w)
+        return run_reference(args, configs.C2)
+    return run_native(args)
 
 
 if __name__ == "__main__":

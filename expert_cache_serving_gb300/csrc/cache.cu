@@ -16,6 +16,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <deque>
 #include <new>
 #include <string>
 #include <thread>
@@ -181,23 +182,40 @@ struct moe_cache {
   float* d_h = nullptr;
   float* d_logits = nullptr;
   unsigned long long* d_bar = nullptr;
-  unsigned long long bar_base = 0;
   unsigned* d_flags = nullptr;  // [0]: plan flag, [1 ..]: fill flags [2][kMaxU]
+  CallState* d_cst = nullptr;   // copy-fill completion state of the latest call
+  float* d_o_part = nullptr;    // partial sums handed to the completion kernel
+  int o_part_floats = 0;
+  unsigned long long* d_deferred = nullptr;
+  unsigned long long deferred_base = 0;  // value of the device counter at the last statistics reset
+  unsigned long long wait_gu_ns = 2000000, wait_dn_ns = 2000000;
+  bool pdl = true;              // launch layer kernels as programmatic dependents
   int32_t* d_oldest = nullptr;
   int* d_oldest_n = nullptr;
   int* h_err = nullptr;  // pinned, mapped: error word the kernels record timeouts in
   int* d_err = nullptr;
   int32_t* d_moves = nullptr;
   int64_t moves_cap = 0;
-  HostWork* h_work = nullptr;
+  HostWork* h_work = nullptr;  // ring of kRing call summaries (pinned, mapped), call seq at seq % kRing
   HostWork* d_work = nullptr;
   cudaStream_t copy = nullptr;
   cudaStream_t copy2 = nullptr;  // internal second copy stream: fills alternate between the two
   bool own_copy = false;
   cudaStream_t last_stream = nullptr;
-  cudaEvent_t e_pre = nullptr, e_done = nullptr;
-  bool have_done = false;
+  bool have_last = false;        // work of this cache has been enqueued on last_stream
+  cudaEvent_t e_done = nullptr;  // recorded on last_stream when the stream changes or at a resize
+  cudaEvent_t e_copy[2] = {nullptr, nullptr};  // end of a call's copies on each copy stream
   uint32_t seq = 0;
+  // device-fill calls whose summaries the host has not read yet (oldest first)
+  struct Inflight {
+    uint32_t seq;
+    int layer, B;
+    cudaEvent_t ta, tb;
+    int tl_row;
+  };
+  std::deque<Inflight> inflight;
+  moe_status sticky = MOE_OK;  // first error found while reading summaries, for moe_cache_sync
+  std::string sticky_msg;
   int64_t call_index = 0;  // successful forward calls (trace numbering; not reset with the stats)
   int grid = 0;
   size_t smem = 0;
@@ -242,6 +260,7 @@ struct moe_cache {
 
 static constexpr int kTlRing = 1024;
 static constexpr int kTlStamps = 12;
+static constexpr int kRing = 256;  // call summaries in flight (device-fill calls the host has not read)
 
 static const char* kNotFound = "";
 
@@ -284,12 +303,17 @@ static void free_all(moe_cache* c) {
   cudaDeviceSynchronize();
   for (void* p : {(void*)c->d_map, (void*)c->d_owner, (void*)c->d_stamp, (void*)c->d_g, (void*)c->d_plan,
                   (void*)c->d_h, (void*)c->d_logits, (void*)c->d_bar, (void*)c->d_flags, (void*)c->d_oldest,
-                  (void*)c->d_oldest_n, (void*)c->d_moves, (void*)c->d_tl})
+                  (void*)c->d_oldest_n, (void*)c->d_moves, (void*)c->d_tl, (void*)c->d_cst, (void*)c->d_o_part,
+                  (void*)c->d_deferred})
     if (p) cudaFree(p);
   if (c->h_work) cudaFreeHost(c->h_work);
   if (c->h_err) cudaFreeHost(c->h_err);
-  for (cudaEvent_t e : {c->e_pre, c->e_done})
+  for (cudaEvent_t e : {c->e_done, c->e_copy[0], c->e_copy[1]})
     if (e) cudaEventDestroy(e);
+  for (auto& f : c->inflight) {
+    if (f.ta) cudaEventDestroy(f.ta);
+    if (f.tb) cudaEventDestroy(f.tb);
+  }
   for (auto& t : c->pending) {
     cudaEventDestroy(t.a);
     cudaEventDestroy(t.b);
@@ -382,7 +406,9 @@ extern "C" moe_status moe_cache_create(const moe_model_desc* desc, const void* h
       (s = cu(cudaMalloc(&c->d_bar, sizeof(unsigned long long)), "barrier")) ||
       (s = cu(cudaMalloc(&c->d_flags, sizeof(unsigned) * (1 + 2 * kMaxU)), "flags")) ||
       (s = cu(cudaMalloc(&c->d_oldest, sizeof(int32_t) * kMaxU), "victim order")) ||
-      (s = cu(cudaMalloc(&c->d_oldest_n, sizeof(int)), "victim order")))
+      (s = cu(cudaMalloc(&c->d_oldest_n, sizeof(int)), "victim order")) ||
+      (s = cu(cudaMalloc(&c->d_cst, sizeof(CallState)), "call state")) ||
+      (s = cu(cudaMalloc(&c->d_deferred, sizeof(unsigned long long)), "counter")))
     return bail(s);
   if ((s = cu(cudaMemset(c->d_map, 0xFF, sizeof(int32_t) * LE), "memset")) ||
       (s = cu(cudaMemset(c->d_owner, 0xFF, sizeof(int32_t) * nslot_alloc), "memset")) ||
@@ -390,18 +416,21 @@ extern "C" moe_status moe_cache_create(const moe_model_desc* desc, const void* h
       (s = cu(cudaMemset(c->d_g, 0, sizeof(uint64_t)), "memset")) ||
       (s = cu(cudaMemset(c->d_bar, 0, sizeof(unsigned long long)), "memset")) ||
       (s = cu(cudaMemset(c->d_flags, 0, sizeof(unsigned) * (1 + 2 * kMaxU)), "memset")) ||
-      (s = cu(cudaMemset(c->d_oldest_n, 0xFF, sizeof(int)), "memset")))
+      (s = cu(cudaMemset(c->d_oldest_n, 0xFF, sizeof(int)), "memset")) ||
+      (s = cu(cudaMemset(c->d_cst, 0xFF, sizeof(CallState)), "memset")) ||
+      (s = cu(cudaMemset(c->d_deferred, 0, sizeof(unsigned long long)), "memset")))
     return bail(s);
-  if ((s = cu(cudaHostAlloc((void**)&c->h_work, sizeof(HostWork), cudaHostAllocMapped), "pinned summary")) ||
+  if ((s = cu(cudaHostAlloc((void**)&c->h_work, sizeof(HostWork) * kRing, cudaHostAllocMapped), "pinned summary")) ||
       (s = cu(cudaHostAlloc((void**)&c->h_err, sizeof(int), cudaHostAllocMapped), "pinned error word")))
     return bail(s);
-  memset((void*)c->h_work, 0, sizeof(HostWork));
+  memset((void*)c->h_work, 0, sizeof(HostWork) * kRing);
   *c->h_err = 0;
   if ((s = cu(cudaHostGetDevicePointer((void**)&c->d_work, c->h_work, 0), "mapped summary")) ||
       (s = cu(cudaHostGetDevicePointer((void**)&c->d_err, c->h_err, 0), "mapped error word")))
     return bail(s);
-  if ((s = cu(cudaEventCreateWithFlags(&c->e_pre, cudaEventDisableTiming), "event")) ||
-      (s = cu(cudaEventCreateWithFlags(&c->e_done, cudaEventDisableTiming), "event")))
+  if ((s = cu(cudaEventCreateWithFlags(&c->e_done, cudaEventDisableTiming), "event")) ||
+      (s = cu(cudaEventCreateWithFlags(&c->e_copy[0], cudaEventDisableTiming), "event")) ||
+      (s = cu(cudaEventCreateWithFlags(&c->e_copy[1], cudaEventDisableTiming), "event")))
     return bail(s);
   if (copy_stream) {
     c->copy = (cudaStream_t)copy_stream;
@@ -451,8 +480,11 @@ extern "C" moe_status moe_cache_create(const moe_model_desc* desc, const void* h
       stage_off < budget ? (int)std::min<size_t>((budget - stage_off) / (size_t)c->stage_pitch, (size_t)kMaxItems) : 0;
   c->smem = stage_off + (size_t)c->stage_items * c->stage_pitch;
   c->grid = layer_max_grid(desc->wdtype, c->smem);
-  if (c->grid != sms)  // the per-CTA row split assumes one CTA on every SM
+  if (c->grid != sms || c->grid > kMaxGrid)  // the per-CTA row split assumes one CTA on every SM
     return bail(fail(MOE_ERR_CUDA, "layer kernel cannot keep one CTA resident on every SM (%d of %d)", c->grid, sms));
+  c->o_part_floats = c->rows_per_cta_max * Bm * (k + 1);
+  if ((s = cu(cudaMalloc(&c->d_o_part, sizeof(float) * (size_t)c->o_part_floats * c->grid), "partial sums")))
+    return bail(s);
   if (cudaDeviceSynchronize() != cudaSuccess) return bail(fail(MOE_ERR_CUDA, "initialisation failed"));
   *out = c;
   return MOE_OK;
@@ -527,9 +559,10 @@ static void drain_timeline(moe_cache* c) {
 
 // Wait until the layer kernel of call `seq` has published its summary.
 static moe_status wait_summary(moe_cache* c, uint32_t seq, cudaStream_t s) {
+  const HostWork* w = c->h_work + seq % kRing;
   const auto t0 = std::chrono::steady_clock::now();
   for (uint64_t spin = 0;; ++spin) {
-    if (__atomic_load_n(&c->h_work->seq, __ATOMIC_ACQUIRE) == seq) return MOE_OK;
+    if (__atomic_load_n(&w->seq, __ATOMIC_ACQUIRE) == seq) return MOE_OK;
     if ((spin & 1023) == 1023) {
       cudaError_t q = cudaStreamQuery(s);
       if (q != cudaSuccess && q != cudaErrorNotReady)
@@ -541,16 +574,99 @@ static moe_status wait_summary(moe_cache* c, uint32_t seq, cudaStream_t s) {
   }
 }
 
-// A previous launch recorded a timeout: wait for the stream, re-align the
-// barrier counter and drop the precomputed victim order.
+// A kernel recorded that a bounded wait for the GPU gave up: wait for the
+// streams, put the barrier counter back in step and drop the victim order.
 static moe_status recover_after_timeout(moe_cache* c, cudaStream_t s) {
   CU_TRY(cudaStreamSynchronize(s));
   CU_TRY(cudaStreamSynchronize(c->copy));
   CU_TRY(cudaStreamSynchronize(c->copy2));
-  CU_TRY(cudaMemcpy(&c->bar_base, c->d_bar, sizeof(unsigned long long), cudaMemcpyDeviceToHost));
+  CU_TRY(cudaMemset(c->d_bar, 0, sizeof(unsigned long long)));
   CU_TRY(cudaMemset(c->d_oldest_n, 0xFF, sizeof(int)));
+  CU_TRY(cudaDeviceSynchronize());
   *(volatile int*)c->h_err = 0;
-  return fail(MOE_ERR_TIMEOUT, "a previous layer call timed out waiting on the GPU; its results were not used");
+  return fail(MOE_ERR_TIMEOUT,
+              "a bounded wait inside a kernel of this cache gave up (the rows of that call are NaN); state recovered");
+}
+
+// Counters, profiling records and trace events of one completed call from its summary.
+static void account_call(moe_cache* c, int layer, int B, const HostWork& w, cudaEvent_t ta, cudaEvent_t tb,
+                         int tl_row) {
+  const moe_model_desc& d = c->d;
+  const int n_u = w.n_u, n_miss = w.n_miss;
+  if (tl_row >= 0) c->tl_calls.emplace_back(tl_row, n_miss > 0 ? 1 : 0);
+  if (ta) {
+    c->pending.push_back({ta, tb, n_miss == 0, (int64_t)n_u + d.has_shared});
+    if (c->pending.size() > 4096) drain_pending(c, false);
+  }
+  moe_stats& st = c->st;
+  const int64_t call_id = c->call_index++;
+  st.calls += 1;
+  st.tokens += B;
+  st.hits += n_u - n_miss;
+  st.misses += n_miss;
+  st.routed_pairs += (int64_t)B * d.k;
+  st.bytes_filled += (int64_t)n_miss * c->S;
+  st.records_streamed += n_u + d.has_shared;
+  for (int r = 0; r < n_u; ++r) {
+    if (w.fill[r] && w.evicted[r] >= 0) st.evictions += 1;
+    if (!w.fill[r]) st.routed_pair_hits += w.pairs[r];
+  }
+  if (c->tracing) {
+    for (int r = 0; r < n_u; ++r) {
+      moe_event ev{};
+      ev.call = call_id;
+      ev.layer = layer;
+      ev.expert = w.key[r] - layer * d.E;
+      ev.kind = w.fill[r] ? MOE_EV_MISS : MOE_EV_HIT;
+      ev.slot = w.slot[r];
+      ev.evicted_key = w.evicted[r];
+      c->trace.push_back(ev);
+    }
+  }
+}
+
+// Read the summaries of device-fill calls in flight until at most `keep` remain.
+static moe_status drain_inflight(moe_cache* c, size_t keep) {
+  while (c->inflight.size() > keep) {
+    const auto f = c->inflight.front();
+    if (moe_status e = wait_summary(c, f.seq, c->last_stream)) return e;
+    const HostWork& w = c->h_work[f.seq % kRing];
+    if (w.err != MOE_OK) {
+      if (c->sticky == MOE_OK) {
+        c->sticky = MOE_ERR_CUDA;
+        c->sticky_msg = "internal error: victim selection found an inconsistent cache state";
+      }
+      if (f.ta) {
+        c->ev_pool.push_back(f.ta);
+        c->ev_pool.push_back(f.tb);
+      }
+    } else {
+      account_call(c, f.layer, f.B, w, f.ta, f.tb, f.tl_row);
+    }
+    c->inflight.pop_front();
+  }
+  return MOE_OK;
+}
+
+// Order this call after the cache's earlier work when it comes on another stream.
+static moe_status follow_stream(moe_cache* c, cudaStream_t s) {
+  if (c->have_last && s != c->last_stream) {
+    CU_TRY(cudaEventRecord(c->e_done, c->last_stream));
+    CU_TRY(cudaStreamWaitEvent(s, c->e_done, 0));
+  }
+  c->last_stream = s;
+  c->have_last = true;
+  return MOE_OK;
+}
+
+static cudaError_t launch_k1(moe_cache* c, const LayerParams& p, cudaStream_t s) {
+  if (c->pdl) {
+    cudaError_t e = launch_layer(c->d.wdtype, p, c->grid, c->smem, true, s);
+    if (e == cudaSuccess) return e;
+    cudaGetLastError();  // programmatic dependent launch refused for this launch: launch plainly from now on
+    c->pdl = false;
+  }
+  return launch_layer(c->d.wdtype, p, c->grid, c->smem, false, s);
 }
 
 extern "C" moe_status moe_layer_forward_ex(moe_cache_t c, int32_t layer, const void* x, const float* logits,
@@ -564,9 +680,17 @@ extern "C" moe_status moe_layer_forward_ex(moe_cache_t c, int32_t layer, const v
   if (!x || !y) return fail(MOE_ERR_INVALID_ARG, "x and y must be device pointers");
   if (!logits && !router_w) return fail(MOE_ERR_INVALID_ARG, "need logits or router_w");
   cudaStream_t s = (cudaStream_t)stream;
-  if (*(volatile int*)c->h_err != 0) return recover_after_timeout(c, s);
-  if (c->have_done && s != c->last_stream) CU_TRY(cudaStreamWaitEvent(s, c->e_done, 0));
-  c->last_stream = s;
+  if (*(volatile int*)c->h_err != 0) {
+    drain_inflight(c, 0);
+    return recover_after_timeout(c, s);
+  }
+  // device-fill calls run ahead of the host; a call that could exceed the
+  // capacity (B*k > C) waits for its summary so the error is this call's
+  const bool device = c->fill_mode == MOE_FILL_DEVICE;
+  const bool async = device && (int64_t)B * d.k <= c->C;
+  if (!async || c->inflight.size() >= (size_t)kRing - 1)
+    if (moe_status e = drain_inflight(c, async ? (size_t)kRing / 2 : 0)) return e;
+  if (moe_status e = follow_stream(c, s)) return e;
 
   const float* lg = logits;
   if (!lg) {
@@ -580,15 +704,20 @@ extern "C" moe_status moe_layer_forward_ex(moe_cache_t c, int32_t layer, const v
   p.logits = lg;
   p.st = CacheDev{c->d_map, c->d_owner, c->d_stamp, c->d_g};
   p.plan = c->d_plan;
-  p.work = c->d_work;
+  p.work = c->d_work + seq % kRing;
   p.seq = seq;
   p.plan_flag = c->d_flags;
   p.fill_flags = c->d_flags + 1;
   p.bar = c->d_bar;
-  p.bar_base = c->bar_base;
   p.err = c->d_err;
+  p.cst = c->d_cst;
+  p.o_part = c->d_o_part;
+  p.o_part_floats = c->o_part_floats;
+  p.wait_gu_ns = c->wait_gu_ns;
+  p.wait_dn_ns = c->wait_dn_ns;
+  p.deferred = c->d_deferred;
   p.has_shared = d.has_shared;
-  p.device_fill = c->fill_mode == MOE_FILL_DEVICE;
+  p.device_fill = device;
   p.pool = c->host_pool;  // pinned pages are mapped at the same address under unified addressing
   p.slots = (const uint8_t*)c->slots.base;
   p.S = c->S;
@@ -606,7 +735,10 @@ extern "C" moe_status moe_layer_forward_ex(moe_cache_t c, int32_t layer, const v
   p.oldest_n = c->d_oldest_n;
   int tl_row = -1;
   if (c->profile_level >= 2 && c->d_tl) {
-    if ((int)c->tl_calls.size() >= kTlRing) drain_timeline(c);
+    if ((int)c->tl_calls.size() >= kTlRing / 2) {
+      if (moe_status e = drain_inflight(c, 0)) return e;
+      drain_timeline(c);
+    }
     tl_row = c->tl_next;
     c->tl_next = (c->tl_next + 1) % kTlRing;
     p.tl = c->d_tl + (size_t)tl_row * kTlStamps;
@@ -616,47 +748,44 @@ extern "C" moe_status moe_layer_forward_ex(moe_cache_t c, int32_t layer, const v
     p.aux_ids = aux->ids; p.aux_w = aux->weights; p.aux_slots = aux->slots;
     p.aux_perm = aux->perm; p.aux_offsets = aux->offsets; p.aux_logits = aux->logits;
   }
-  // everything before this call (earlier layers may still read victim slots)
-  CU_TRY(cudaEventRecord(c->e_pre, s));
   cudaEvent_t ta = nullptr, tb = nullptr;
   if (c->profiling) {
     ta = take_event(c);
     tb = take_event(c);
     cudaEventRecord(ta, s);
   }
-  CU_TRY(launch_layer(d.wdtype, p, c->grid, c->smem, s));
+  CU_TRY(launch_k1(c, p, s));
   if (c->profiling) cudaEventRecord(tb, s);
-  CU_TRY(cudaEventRecord(c->e_done, s));
-  c->have_done = true;
   c->st.layer_launches += 1;
+  if (async) {
+    c->inflight.push_back({seq, layer, B, ta, tb, tl_row});
+    return MOE_OK;
+  }
 
   const auto t_launch = std::chrono::steady_clock::now();
   if (moe_status w = wait_summary(c, seq, s)) return w;
   const auto t_seen = std::chrono::steady_clock::now();
   c->st.host_wait_us += std::chrono::duration<double, std::micro>(t_seen - t_launch).count();
-  const HostWork& w = *c->h_work;
+  const HostWork& w = c->h_work[seq % kRing];
   if (w.err != MOE_OK) {
-    if (c->profiling) c->pending.push_back({ta, tb, false, 0});
+    if (ta) {
+      c->ev_pool.push_back(ta);
+      c->ev_pool.push_back(tb);
+    }
     if (w.err == MOE_ERR_CAPACITY)
       return fail(MOE_ERR_CAPACITY, "layer %d routes %d distinct experts but the cache has %lld slots", layer, w.n_u,
                   (long long)c->C);
     return fail(MOE_ERR_CUDA, "internal error: victim selection found an inconsistent cache state");
   }
-  const int n_u = w.n_u, n_miss = w.n_miss;
-  c->bar_base += (unsigned long long)c->grid * (n_miss > 0 && !p.device_fill ? 2 : 1);
-  if (tl_row >= 0) c->tl_calls.emplace_back(tl_row, n_miss > 0 ? 1 : 0);
-  if (c->profiling) {
-    c->pending.push_back({ta, tb, n_miss == 0, (int64_t)n_u + d.has_shared});
-    if (c->pending.size() > 4096) drain_pending(c, false);
-  }
-  if (n_miss > 0 && !p.device_fill) {
-    // one copy per half record, each followed by a flag the kernel waits on;
-    // records alternate between two copy streams so that one stream's flag
-    // write and next-copy start overlap the other's transfer; the copies start
-    // once every earlier call has finished
+  const int n_miss = w.n_miss;
+  if (n_miss > 0 && !device) {
+    // one copy per half record, each followed by a flag the layer kernel waits
+    // on; records alternate between two copy streams so that one stream's
+    // flag write and next-copy start overlap the other's transfer.  No earlier
+    // kernel can still read a victim slot: the summary is written after the
+    // layer kernel's dependency wait, i.e. after everything before this call
+    // on the compute stream has completed.
     Drv& dr = drv();
-    CU_TRY(cudaStreamWaitEvent(c->copy, c->e_pre, 0));
-    if (n_miss > 1) CU_TRY(cudaStreamWaitEvent(c->copy2, c->e_pre, 0));
     const int64_t part1 = first_part_bytes(d), part2 = c->S - part1;
     unsigned* flags = c->d_flags + 1;
     int f = 0, half = 0;
@@ -696,39 +825,28 @@ extern "C" moe_status moe_layer_forward_ex(moe_cache_t c, int32_t layer, const v
       for (int g = f; g < n_miss; ++g)
         for (int hh = (g == f ? half : 0); hh < 2; ++hh)
           dr.streamWriteValue32((CUstream)c->copy, (CUdeviceptr)(flags + hh * kMaxU + g), seq | kFlagError, 0);
+    }
+    // the completion kernel runs after every copy of the call; it finishes
+    // the rows the layer kernel handed over, or undoes the call after a failure
+    CU_TRY(cudaEventRecord(c->e_copy[0], c->copy));
+    CU_TRY(cudaStreamWaitEvent(s, c->e_copy[0], 0));
+    if (n_miss > 1 || failed) {
+      CU_TRY(cudaEventRecord(c->e_copy[1], c->copy2));
+      CU_TRY(cudaStreamWaitEvent(s, c->e_copy[1], 0));
+    }
+    CU_TRY(launch_layer_finish(d.wdtype, p, c->grid, c->smem, s));
+    c->st.finish_launches += 1;
+    if (failed) {
+      if (ta) {
+        c->ev_pool.push_back(ta);
+        c->ev_pool.push_back(tb);
+      }
       return fail(MOE_ERR_CUDA, "fill %d of %d could not be issued (%s); cache rolled back", f + 1, n_miss,
                   why.c_str());
     }
+    c->st.host_issue_us += std::chrono::duration<double, std::micro>(std::chrono::steady_clock::now() - t_seen).count();
   }
-
-  // accounting
-  moe_stats& st = c->st;
-  if (n_miss > 0)
-    st.host_issue_us += std::chrono::duration<double, std::micro>(std::chrono::steady_clock::now() - t_seen).count();
-  const int64_t call_id = c->call_index++;
-  st.calls += 1;
-  st.tokens += B;
-  st.hits += n_u - n_miss;
-  st.misses += n_miss;
-  st.routed_pairs += (int64_t)B * d.k;
-  st.bytes_filled += (int64_t)n_miss * c->S;
-  st.records_streamed += n_u + d.has_shared;
-  for (int r = 0; r < n_u; ++r) {
-    if (w.fill[r] && w.evicted[r] >= 0) st.evictions += 1;
-    if (!w.fill[r]) st.routed_pair_hits += w.pairs[r];
-  }
-  if (c->tracing) {
-    for (int r = 0; r < n_u; ++r) {
-      moe_event ev{};
-      ev.call = call_id;
-      ev.layer = layer;
-      ev.expert = w.key[r] - layer * d.E;
-      ev.kind = w.fill[r] ? MOE_EV_MISS : MOE_EV_HIT;
-      ev.slot = w.slot[r];
-      ev.evicted_key = w.evicted[r];
-      c->trace.push_back(ev);
-    }
-  }
+  account_call(c, layer, B, w, ta, tb, tl_row);
   return MOE_OK;
 }
 
@@ -743,11 +861,16 @@ extern "C" moe_status moe_cache_resize(moe_cache_t c, int64_t n_slots, void* str
   if (!c) return fail(MOE_ERR_INVALID_ARG, "cache is NULL");
   if (n_slots < 0 || n_slots > c->C_max)
     return fail(MOE_ERR_INVALID_ARG, "n_slots %lld outside 0..%lld", (long long)n_slots, (long long)c->C_max);
-  if (c->have_done && cudaEventQuery(c->e_done) == cudaErrorNotReady)
-    return fail(MOE_ERR_BUSY, "a forward of this cache is still running on the GPU");
+  if (c->have_last) {
+    // everything enqueued on the cache's stream so far (its last calls among it)
+    CU_TRY(cudaEventRecord(c->e_done, c->last_stream));
+    if (cudaEventQuery(c->e_done) == cudaErrorNotReady)
+      return fail(MOE_ERR_BUSY, "a forward of this cache is still running on the GPU");
+  }
   if (cudaStreamQuery(c->copy) == cudaErrorNotReady || cudaStreamQuery(c->copy2) == cudaErrorNotReady)
     return fail(MOE_ERR_BUSY, "fills still in flight");
   cudaGetLastError();
+  if (moe_status e = drain_inflight(c, 0)) return e;
   cudaStream_t s = (cudaStream_t)stream;
   const int64_t C = c->C, LE = (int64_t)c->d.L * c->d.E;
   std::vector<int32_t> owner(std::max<int64_t>(C, n_slots), -1);
@@ -849,21 +972,58 @@ static void drain_prefill(moe_cache* c) {
   c->pf.timed.clear();
 }
 
+static unsigned long long read_deferred(moe_cache* c) {
+  unsigned long long v = 0;
+  if (cudaMemcpy(&v, c->d_deferred, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess) cudaGetLastError();
+  return v;
+}
+
 extern "C" moe_status moe_cache_stats(moe_cache_t c, moe_stats* out) {
   if (!c || !out) return fail(MOE_ERR_INVALID_ARG, "NULL argument");
+  if (moe_status e = drain_inflight(c, 0)) return e;
   drain_pending(c, true);
   drain_prefill(c);
   *out = c->st;
+  out->deferred_calls = (int64_t)(read_deferred(c) - c->deferred_base);
   return MOE_OK;
 }
 
 extern "C" moe_status moe_cache_reset_stats(moe_cache_t c) {
   if (!c) return fail(MOE_ERR_INVALID_ARG, "cache is NULL");
+  if (moe_status e = drain_inflight(c, 0)) return e;
   drain_pending(c, true);
   drain_timeline(c);
   drain_prefill(c);
   c->st = moe_stats{};
   c->pt = moe_phase_times{};
+  c->deferred_base = read_deferred(c);
+  return MOE_OK;
+}
+
+extern "C" moe_status moe_cache_sync(moe_cache_t c, void* stream) {
+  g_err.clear();
+  if (!c) return fail(MOE_ERR_INVALID_ARG, "cache is NULL");
+  cudaStream_t s = (cudaStream_t)stream;
+  CU_TRY(cudaStreamSynchronize(s));
+  if (c->have_last && c->last_stream != s) CU_TRY(cudaStreamSynchronize(c->last_stream));
+  CU_TRY(cudaStreamSynchronize(c->copy));
+  CU_TRY(cudaStreamSynchronize(c->copy2));
+  if (moe_status e = drain_inflight(c, 0)) return e;
+  if (*(volatile int*)c->h_err != 0) return recover_after_timeout(c, s);
+  if (c->sticky != MOE_OK) {
+    const moe_status e = c->sticky;
+    c->sticky = MOE_OK;
+    return fail(e, "%s", c->sticky_msg.c_str());
+  }
+  return MOE_OK;
+}
+
+extern "C" moe_status moe_cache_set_wait_limit_ns(moe_cache_t c, int64_t gate_up_ns, int64_t down_ns) {
+  if (!c) return fail(MOE_ERR_INVALID_ARG, "cache is NULL");
+  if (gate_up_ns < 0 || down_ns < 0 || gate_up_ns > 60000000000LL || down_ns > 60000000000LL)
+    return fail(MOE_ERR_INVALID_ARG, "wait limits must lie in 0 .. 60 s");
+  c->wait_gu_ns = (unsigned long long)gate_up_ns;
+  c->wait_dn_ns = (unsigned long long)down_ns;
   return MOE_OK;
 }
 
@@ -878,6 +1038,7 @@ extern "C" moe_status moe_cache_set_profiling(moe_cache_t c, int32_t on) {
 
 extern "C" moe_status moe_cache_phase_times(moe_cache_t c, moe_phase_times* out) {
   if (!c || !out) return fail(MOE_ERR_INVALID_ARG, "NULL argument");
+  if (moe_status e = drain_inflight(c, 0)) return e;
   drain_timeline(c);
   *out = c->pt;
   return MOE_OK;
@@ -891,6 +1052,7 @@ extern "C" moe_status moe_cache_set_trace(moe_cache_t c, int32_t on) {
 
 extern "C" moe_status moe_cache_trace(moe_cache_t c, moe_event* buf, int64_t cap, int64_t* n) {
   if (!c || !n || (cap > 0 && !buf)) return fail(MOE_ERR_INVALID_ARG, "NULL argument");
+  if (moe_status e = drain_inflight(c, 0)) return e;
   *n = (int64_t)c->trace.size();
   const int64_t m = std::min<int64_t>(cap, *n);
   if (m > 0) memcpy(buf, c->trace.data(), sizeof(moe_event) * m);
@@ -901,6 +1063,7 @@ extern "C" moe_status moe_cache_state(moe_cache_t c, int32_t* owner, uint64_t* s
                                       uint64_t* counter) {
   if (!c) return fail(MOE_ERR_INVALID_ARG, "cache is NULL");
   CU_TRY(cudaDeviceSynchronize());
+  if (moe_status e = drain_inflight(c, 0)) return e;
   const int64_t m = std::min<int64_t>(cap, c->C);
   if (owner && m > 0) CU_TRY(cudaMemcpy(owner, c->d_owner, sizeof(int32_t) * m, cudaMemcpyDeviceToHost));
   if (stamp && m > 0) CU_TRY(cudaMemcpy(stamp, c->d_stamp, sizeof(uint64_t) * m, cudaMemcpyDeviceToHost));
@@ -917,6 +1080,7 @@ extern "C" const void* moe_cache_slot_ptr(moe_cache_t c, int64_t s) {
 extern "C" moe_status moe_cache_set_fill_mode(moe_cache_t c, int32_t mode) {
   if (!c) return fail(MOE_ERR_INVALID_ARG, "cache is NULL");
   if (mode != MOE_FILL_COPY && mode != MOE_FILL_DEVICE) return fail(MOE_ERR_INVALID_ARG, "unknown fill mode %d", mode);
+  if (moe_status e = drain_inflight(c, 0)) return e;
   if (mode == MOE_FILL_DEVICE) {
     cudaPointerAttributes a;
     if (cudaPointerGetAttributes(&a, c->host_pool) != cudaSuccess || a.devicePointer != (void*)c->host_pool) {
@@ -1043,8 +1207,8 @@ extern "C" moe_status moe_prefill_stream(moe_cache_t c, int32_t layer_begin, int
   if (*(volatile int*)c->h_err != 0) return recover_after_timeout(c, s);
   if (moe_status st = prefill_scratch(c, T)) return st;
   auto& pf = c->pf;
-  if (c->have_done && s != c->last_stream) CU_TRY(cudaStreamWaitEvent(s, c->e_done, 0));
-  c->last_stream = s;
+  if (moe_status e = drain_inflight(c, 0)) return e;
+  if (moe_status e = follow_stream(c, s)) return e;
 
   const int H = d.H, I = d.I, k = d.k, sh = d.has_shared;
   const int Tk = T * k, n_pairs = Tk + (sh ? T : 0);
@@ -1130,8 +1294,6 @@ extern "C" moe_status moe_prefill_stream(moe_cache_t c, int32_t layer_begin, int
   done(whole, s);
   // later calls must not start before the copies finished with the buffers
   CU_TRY(cudaStreamWaitEvent(s, pf.loaded[(layer_end - layer_begin - 1) & 1], 0));
-  CU_TRY(cudaEventRecord(c->e_done, s));
-  c->have_done = true;
   c->st.prefill_layers += layer_end - layer_begin;
   c->st.prefill_tokens += (int64_t)T * (layer_end - layer_begin);
   return MOE_OK;

@@ -52,6 +52,18 @@ struct HostWork {
   int32_t fill_order[kMaxU];   // f-th fill the kernel consumes -> rank in U
 };
 
+// Completion state of one decode call in copy-fill mode, read by the
+// completion kernel that runs after the call's copies: whether the layer
+// kernel stopped waiting for a fill's gate/up half (then the completion
+// kernel computes every fill), and per CTA how many fills its saved partial
+// sums already hold (-1: the CTA wrote its outputs itself).
+constexpr int kMaxGrid = 1024;
+struct CallState {
+  int gu_stop;             // a CTA gave up waiting for a first (gate/up) half
+  int pad[31];
+  int part[kMaxGrid];      // per CTA: -1 complete, >= 0 fills in its saved sums, -2 failed fill
+};
+
 struct CacheDev {
   int32_t* map;      // [L*E] key -> slot or -1
   int32_t* owner;    // [C_max] slot -> key or -1
@@ -162,18 +174,21 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
 
 __device__ __forceinline__ void fence_mbar_init() { asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory"); }
 
-// Grid-wide barrier of a cooperative launch over a counter that only grows:
-// barrier number b of a launch completes when the counter reaches
-// base + (b + 1) * gridDim.x.  The wait gives up after limit_ns, records
-// MOE_ERR_TIMEOUT in *err and returns false.
-__device__ __forceinline__ bool grid_barrier(unsigned long long* count, unsigned long long target, int* err,
+// Grid-wide barrier of a launch whose CTAs are all resident, over a counter
+// that only grows and that only full grids of gridDim.x CTAs arrive at:
+// arrival number a belongs to the barrier that completes when the counter
+// reaches (a / G + 1) * G, so no base has to be carried from launch to launch.
+// The wait gives up after limit_ns, records MOE_ERR_TIMEOUT in *err and
+// returns false (the counter is then out of step until the host resets it).
+__device__ __forceinline__ bool grid_barrier(unsigned long long* count, int* err,
                                              unsigned long long limit_ns = 2000000000ull) {
   __shared__ int s_ok;
   __threadfence();  // publish this thread's global writes before arriving
   __syncthreads();
   if (threadIdx.x == 0) {
     s_ok = 1;
-    atomicAdd(count, 1ull);
+    const unsigned long long G = gridDim.x;
+    const unsigned long long target = (atomicAdd(count, 1ull) / G + 1) * G;
     const unsigned long long t0 = globaltimer_ns();
     while (ld_acquire_u64(count) < target) {
       __nanosleep(32);
@@ -189,10 +204,12 @@ __device__ __forceinline__ bool grid_barrier(unsigned long long* count, unsigned
   return s_ok != 0;
 }
 
-// Wait until *flag == want (returns 0) or want | kFlagError (returns 1); 2 on
-// timeout (MOE_ERR_TIMEOUT recorded).  Thread 0 spins, the CTA waits on it.
-__device__ __forceinline__ int wait_flag(const unsigned* flag, unsigned want, int* err,
-                                         unsigned long long limit_ns = 5000000000ull, unsigned sleep_ns = 256) {
+// Wait until *flag == want (returns 0) or want | kFlagError (returns 1).
+// Gives up (returns 2) after limit_ns, or as soon as *stop becomes non-zero
+// when stop is given.  Thread 0 polls, the CTA waits on it.  Giving up is
+// not an error here: the caller decides what it means.
+__device__ __forceinline__ int wait_flag(const unsigned* flag, unsigned want, const int* stop,
+                                         unsigned long long limit_ns, unsigned sleep_ns = 256) {
   __shared__ int s_res;
   __syncthreads();
   if (threadIdx.x == 0) {
@@ -208,10 +225,12 @@ __device__ __forceinline__ int wait_flag(const unsigned* flag, unsigned want, in
         res = v == want ? 0 : 1;
         break;
       }
-      if (globaltimer_ns() - t0 > limit_ns) {
-        atomicExch(err, MOE_ERR_TIMEOUT);
-        break;
+      if (stop) {
+        int sv;
+        asm volatile("ld.relaxed.gpu.global.s32 %0, [%1];" : "=r"(sv) : "l"(stop) : "memory");
+        if (sv) break;
       }
+      if (globaltimer_ns() - t0 >= limit_ns) break;
       __nanosleep(sleep_ns);
     }
     s_res = res;
@@ -219,5 +238,11 @@ __device__ __forceinline__ int wait_flag(const unsigned* flag, unsigned want, in
   __syncthreads();
   return s_res;
 }
+
+// Programmatic dependent launch: wait until the previous launch on the stream
+// has completed and its memory is visible (a no-op when the kernel was not
+// launched as a dependent), and let the next launch begin its start-up.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 }  // namespace moe

@@ -1,4 +1,7 @@
-// Per-call cache control, executed by one CTA of the layer kernel.
+// Per-call cache control inside the layer kernel.  Routing, deduplication,
+// residency lookup and grouping run in every CTA (route_lookup); victim
+// choice, the plan, the host summary and the commit of recency and residency
+// run in the control CTA (choose_victims, control_commit, compact_oldest).
 //
 // FreeToken write-up, "CUDA Graph-compatible LRU cache": per MoE layer one GPU
 // step deduplicates the routed experts, classifies them against the residency
@@ -35,6 +38,7 @@ struct CtrlSmem {
   int ids[kMaxPairs];
   float w[kMaxPairs];
   int prank[kMaxPairs];
+  int perm[kMaxPairs];  // flat pair t*k+j grouped by expert (stable)
   unsigned bits[kMaxE / 32];
   int wpre[kMaxE / 32];
   int U[kMaxU];
@@ -95,7 +99,7 @@ __device__ __forceinline__ void route_token(const float* lg, int E, int k, int l
     const int e = (int)__reduce_min_sync(0xFFFFFFFFu, bk == m ? (unsigned)(lane + 32 * bq) : 0xFFFFFFFFu);
     const float x = key_logit(m);
     if (r == 0) m0 = x;
-    const float ex = expf(x - m0);
+    const float ex = x == m0 ? 1.f : expf(x - m0);  // equal to the largest (also +-inf): exp(0)
     sum += ex;
     if (lane == 0) {
       ids[r] = e;
@@ -243,36 +247,26 @@ __device__ __forceinline__ void publish_summary(const LayerParams& p) {
   }
 }
 
-// Routing, deduplication, residency lookup, victim choice and grouping: the
-// plan the other CTAs need, written to device memory (and, when the host must
-// issue copies for this call, the host summary too, before anything else).
-// Recency, the residency table and the undo log are written afterwards by
-// control_commit, off the other CTAs' critical path.  Returns the status
-// (MOE_OK or an error) to every thread; on an error the plan and the host
-// summary carry it and nothing is changed.
-static __device__ int control_step(const LayerParams& p, CtrlSmem& cs) {
+// Routing, deduplication, residency lookup and grouping of one call, run by
+// every CTA of the layer kernel on its own (the inputs are a few KB and the
+// result is deterministic, so every CTA arrives at the same tables without
+// waiting for one another): top-k per token, U = sorted distinct experts,
+// each member's slot (or a miss), the stable grouping of the (token, rank)
+// pairs by expert (offsets and perm) and the miss ranks.  The residency table
+// is only read here; the control CTA writes it after a grid barrier that every
+// CTA reaches after this lookup.  Returns MOE_ERR_CAPACITY (|U| > C) or MOE_OK
+// to every thread.
+static __device__ int route_lookup(const LayerParams& p, CtrlSmem& cs, bool write_aux) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarp = blockDim.x >> 5;
   const int E = p.E, k = p.k, B = p.B, npairs = B * k;
-  const int64_t C = p.C;
-  Plan* plan = p.plan;
-  HostWork* work = p.work;
-
-  // ---- loads that depend on nothing, issued first: this thread's entry of the
-  // oldest-slot list (its owner is read next to the residency lookups), the
-  // recency counter and the list length
-  const int my_listed = tid < kMaxU ? p.oldest[tid] : -1;
-  if (tid == 0) {
-    cs.err = MOE_OK;
-    cs.g = *p.st.g;
-    cs.nsel = *p.oldest_n;
-  }
   for (int i = tid; i < kMaxE / 32; i += blockDim.x) cs.bits[i] = 0u;
+  __syncthreads();
 
   // ---- router: one warp per token ------------------------------------------------
   const int nq = (E + 31) >> 5;
   for (int t = warp; t < B; t += nwarp) {
     const float* lg = p.logits + (size_t)t * E;
-    float* aux = p.aux_logits ? p.aux_logits + (size_t)t * E : nullptr;
+    float* aux = (write_aux && p.aux_logits) ? p.aux_logits + (size_t)t * E : nullptr;
     int* ids = cs.ids + t * k;
     float* w = cs.w + t * k;
     if (nq <= 1) route_token<1>(lg, E, k, lane, aux, ids, w);
@@ -310,35 +304,86 @@ static __device__ int control_step(const LayerParams& p, CtrlSmem& cs) {
     cs.U[r] = e;
     atomicAdd(&cs.cnt[r], 1);
   }
-  if (tid == 0 && n_u > C) cs.err = MOE_ERR_CAPACITY;
   __syncthreads();
+  if (n_u > p.C) return MOE_ERR_CAPACITY;
 
-  // ---- residency lookups and the owners of the listed slots, in flight together ----
-  const bool state_ok = cs.err == MOE_OK;
-  const int listed0 = cs.nsel;  // -1: the list must be rebuilt
-  int my_slot = -1, my_owner = -1;
-  if (state_ok && tid < n_u) my_slot = p.st.map[p.layer * E + cs.U[tid]];
-  if (state_ok && tid < listed0 && my_listed >= 0 && my_listed < C) my_owner = p.st.owner[my_listed];
-  // one scan for both the grouping offsets (pairs per expert, high half) and
-  // the miss ranks (low half); both totals are at most 256
+  // ---- residency lookups, then one scan for the grouping offsets (pairs per
+  // expert, high half) and the miss ranks (low half); both totals are <= 256
   int is_miss = 0;
-  if (state_ok && tid < n_u) {
-    cs.slot[tid] = my_slot;
-    is_miss = my_slot < 0;
+  if (tid < n_u) {
+    const int s = p.st.map[p.layer * E + cs.U[tid]];
+    cs.slot[tid] = s;
+    is_miss = s < 0;
     cs.fill[tid] = is_miss;
   }
   int packed_tot;
   const int packed = block_excl_scan(((tid < n_u ? cs.cnt[tid] : 0) << 16) | is_miss, cs.scan, &packed_tot);
-  const int nmiss = packed_tot & 0xFFFF, mr = packed & 0xFFFF;
   if (tid < n_u) {
     cs.off[tid] = packed >> 16;
-    cs.mrank[tid] = mr;
+    cs.mrank[tid] = packed & 0xFFFF;
   }
-  if (tid == 0) cs.off[n_u] = npairs;
+  if (tid == 0) {
+    cs.off[n_u] = npairs;
+    cs.nmiss = packed_tot & 0xFFFF;
+  }
   __syncthreads();
+  // stable grouping of the (token, rank) pairs by expert
+  if (tid < npairs) {
+    const int r = cs.prank[tid];
+    int before = 0;
+    for (int q = 0; q < tid; ++q) before += (cs.prank[q] == r);
+    cs.perm[cs.off[r] + before] = tid;
+  }
+  __syncthreads();
+  return MOE_OK;
+}
 
-  // ---- victims: first nmiss entries of the oldest-slot list that are no hits ------
-  if (state_ok && nmiss > 0) {
+// The plan's error and the host summary of a call that cannot run (capacity,
+// or an inconsistent victim list); control CTA only.
+static __device__ void publish_error(const LayerParams& p, const CtrlSmem& cs, int err) {
+  if (threadIdx.x != 0) return;
+  Plan* plan = p.plan;
+  HostWork* work = p.work;
+  plan->err = err;
+  plan->n_u = cs.nu;
+  plan->n_miss = 0;
+  plan->n_items[0] = plan->n_items[1] = 0;
+  work->err = err;
+  work->n_u = cs.nu;
+  work->n_miss = 0;
+  work->g_before = *p.st.g;
+  __threadfence_system();
+  work->seq = p.seq;
+  __threadfence();
+  st_release_u32(p.plan_flag, p.seq);
+}
+
+// Victims, the plan and the host summary (control CTA, after route_lookup):
+// the first n_miss entries of the oldest-slot list that hold no hit of this
+// call become the misses' slots (the whole pool is ranked again when the list
+// runs short).  When the host issues this call's copies the summary is
+// published before anything else.  Ends with thread 0's release store of the
+// plan flag, which the other CTAs acquire before they read fill slots.
+// Returns MOE_OK, or MOE_ERR_CUDA if the list was inconsistent (the plan and
+// the summary then carry the error).
+static __device__ int choose_victims(const LayerParams& p, CtrlSmem& cs) {
+  const int tid = threadIdx.x;
+  const int E = p.E, k = p.k, B = p.B, npairs = B * k, n_u = cs.nu, nmiss = cs.nmiss;
+  const int64_t C = p.C;
+  Plan* plan = p.plan;
+  HostWork* work = p.work;
+  const int my_listed = tid < kMaxU ? p.oldest[tid] : -1;
+  if (tid == 0) {
+    cs.err = MOE_OK;
+    cs.g = *p.st.g;
+    cs.nsel = *p.oldest_n;
+  }
+  __syncthreads();
+  const int listed0 = cs.nsel;  // -1: the list must be rebuilt
+  int my_owner = -1;
+  if (tid < listed0 && my_listed >= 0 && my_listed < C) my_owner = p.st.owner[my_listed];
+
+  if (nmiss > 0) {
     int listed = listed0;
     const int full = (int)(C < (int64_t)kMaxU ? C : (int64_t)kMaxU);
     bool rebuilt = false;
@@ -373,23 +418,14 @@ static __device__ int control_step(const LayerParams& p, CtrlSmem& cs) {
     __syncthreads();
   }
   if (cs.err != MOE_OK) {
-    if (tid == 0) {
-      plan->err = cs.err;
-      plan->n_u = n_u;
-      plan->n_miss = 0;
-      plan->n_items[0] = plan->n_items[1] = 0;
-      work->err = cs.err;
-      work->n_u = n_u;
-      work->n_miss = 0;
-      work->g_before = cs.g;
-      __threadfence_system();
-      work->seq = p.seq;
-    }
+    publish_error(p, cs, cs.err);
     return cs.err;
   }
 
   // ---- the plan (and the fields of the host summary) ----------------------------------
-  const bool host_first = nmiss > 0 && !p.device_fill;
+  // copy mode: the host waits for this summary (it issues the fills and must
+  // know there are none); device mode: published after the commit instead
+  const bool host_first = !p.device_fill;
   if (tid < n_u) {
     const int key = p.layer * E + cs.U[tid];
     const int fill = cs.fill[tid];
@@ -407,18 +443,16 @@ static __device__ int control_step(const LayerParams& p, CtrlSmem& cs) {
     if (fill) work->fill_order[cs.mrank[tid]] = tid;
   }
   if (tid <= n_u) plan->u_off[tid] = cs.off[tid];
-  if (tid < npairs) {  // stable grouping of the (token, rank) pairs by expert
+  __syncthreads();
+  if (tid < npairs) {
     const int r = cs.prank[tid];
-    int before = 0;
-    for (int q = 0; q < tid; ++q) before += (cs.prank[q] == r);
-    const int pos = cs.off[r] + before;
-    plan->perm[pos] = tid;
+    plan->perm[tid] = cs.perm[tid];
     plan->pair_rank[tid] = r;
     plan->pair_w[tid] = cs.w[tid];
-    if (p.aux_perm) p.aux_perm[pos] = tid;
+    if (p.aux_perm) p.aux_perm[tid] = cs.perm[tid];
     if (p.aux_ids) p.aux_ids[tid] = cs.ids[tid];
     if (p.aux_w) p.aux_w[tid] = cs.w[tid];
-    if (p.aux_slots) p.aux_slots[tid] = cs.fill[r] ? cs.victim[cs.mrank[r]] : cs.slot[r];
+    if (p.aux_slots) p.aux_slots[tid] = cs.slot[r];
   }
   if (p.aux_offsets) {
     for (int e = tid; e <= E; e += blockDim.x) {
@@ -443,19 +477,20 @@ static __device__ int control_step(const LayerParams& p, CtrlSmem& cs) {
     work->n_u = n_u;
     work->n_miss = nmiss;
     work->g_before = cs.g;
-    cs.nmiss = nmiss;
   }
   if (host_first) publish_summary(p);  // the host issues this call's copies from it
   // the CTA barrier orders every thread's plan writes before thread 0's
   // release store of the plan flag (GPU scope), which the other CTAs acquire
   __syncthreads();
+  if (tid == 0) st_release_u32(p.plan_flag, p.seq);
   return MOE_OK;
 }
 
-// Recency, residency table and undo log of a planned call, written after the
-// other CTAs have been released: hits and fills take stamps g + r in U order,
-// each victim's previous key leaves the table, g advances by |U|.  Then the
-// host summary, unless control_step already published it.
+// Recency, residency table and undo log of a planned call, written once every
+// CTA has done its residency lookups (after the first grid barrier): hits and
+// fills take stamps g + r in U order, each victim's previous key leaves the
+// table, g advances by |U|.  Then the host summary in device-fill mode
+// (choose_victims published it already in copy mode).
 static __device__ void control_commit(const LayerParams& p, CtrlSmem& cs) {
   const int tid = threadIdx.x, n_u = cs.nu;
   const unsigned long long g0 = cs.g;
@@ -472,7 +507,7 @@ static __device__ void control_commit(const LayerParams& p, CtrlSmem& cs) {
     p.st.stamp[s] = g0 + tid;
   }
   if (tid == 0) *p.st.g = g0 + n_u;
-  if (!(cs.nmiss > 0 && !p.device_fill))
+  if (p.device_fill)
     publish_summary(p);
   else
     __syncthreads();
@@ -499,9 +534,10 @@ static __device__ void compact_oldest(const LayerParams& p, CtrlSmem& cs) {
   if (threadIdx.x == 0) *p.oldest_n = tot;
 }
 
-// Undo of a call whose fills did not arrive: recency and the counter go back
-// to their values before the call; the call's victim slots are left empty
-// (their previous contents may already be overwritten).
+// Undo of a call whose fills could not be issued (run by the completion
+// kernel once every copy of the call has ended): recency and the counter go
+// back to their values before the call; the call's victim slots are left
+// empty (their previous contents may already be overwritten).
 static __device__ void undo_call(const LayerParams& p) {
   const Plan* pl = p.plan;
   for (int r = threadIdx.x; r < pl->n_u; r += blockDim.x) {

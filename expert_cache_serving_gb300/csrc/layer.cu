@@ -45,38 +45,55 @@ size_t layer_smem_bytes(int wdtype, int B, int H, int k, int smem_h_floats, int 
 }
 
 // The 15 instantiations (format x token bound 1, 2, 4, 8, 16) are compiled
-// as separate objects from layer_inst.cu; each exports its launcher and its
-// kernel's address.
-#define MOE_LAYER_DECL(F, M)                                                                  \
-  cudaError_t layer_launch_##F##_##M(const LayerParams& p, int grid, size_t smem, cudaStream_t s); \
-  const void* layer_kernel_##F##_##M();
+// as separate objects from layer_inst.cu; each exports the launchers and the
+// addresses of its layer kernel and completion kernel.
+#define MOE_LAYER_DECL(F, M)                                                                                \
+  cudaError_t layer_launch_##F##_##M(const LayerParams& p, int grid, size_t smem, bool pdl, cudaStream_t s); \
+  cudaError_t layer_finish_##F##_##M(const LayerParams& p, int grid, size_t smem, cudaStream_t s);           \
+  const void* layer_kernel_##F##_##M();                                                                     \
+  const void* layer_finish_kernel_##F##_##M();
 #define MOE_LAYER_DECL_F(F) \
   MOE_LAYER_DECL(F, 1) MOE_LAYER_DECL(F, 2) MOE_LAYER_DECL(F, 4) MOE_LAYER_DECL(F, 8) MOE_LAYER_DECL(F, 16)
 MOE_LAYER_DECL_F(0)
 MOE_LAYER_DECL_F(1)
 MOE_LAYER_DECL_F(2)
 
-using LayerLaunch = cudaError_t (*)(const LayerParams&, int, size_t, cudaStream_t);
+using LayerLaunch = cudaError_t (*)(const LayerParams&, int, size_t, bool, cudaStream_t);
+using FinishLaunch = cudaError_t (*)(const LayerParams&, int, size_t, cudaStream_t);
 using LayerKernel = const void* (*)();
-#define MOE_LAYER_ROW(F) {layer_launch_##F##_1, layer_launch_##F##_2, layer_launch_##F##_4, layer_launch_##F##_8, layer_launch_##F##_16}
-#define MOE_KERNEL_ROW(F) {layer_kernel_##F##_1, layer_kernel_##F##_2, layer_kernel_##F##_4, layer_kernel_##F##_8, layer_kernel_##F##_16}
-static const LayerLaunch kLaunch[3][5] = {MOE_LAYER_ROW(0), MOE_LAYER_ROW(1), MOE_LAYER_ROW(2)};
-static const LayerKernel kKernel[3][5] = {MOE_KERNEL_ROW(0), MOE_KERNEL_ROW(1), MOE_KERNEL_ROW(2)};
+#define MOE_ROW(P, F) {P##F##_1, P##F##_2, P##F##_4, P##F##_8, P##F##_16}
+static const LayerLaunch kLaunch[3][5] = {MOE_ROW(layer_launch_, 0), MOE_ROW(layer_launch_, 1),
+                                          MOE_ROW(layer_launch_, 2)};
+static const FinishLaunch kFinish[3][5] = {MOE_ROW(layer_finish_, 0), MOE_ROW(layer_finish_, 1),
+                                           MOE_ROW(layer_finish_, 2)};
+static const LayerKernel kKernel[3][5] = {MOE_ROW(layer_kernel_, 0), MOE_ROW(layer_kernel_, 1),
+                                          MOE_ROW(layer_kernel_, 2)};
+static const LayerKernel kFinishKernel[3][5] = {MOE_ROW(layer_finish_kernel_, 0), MOE_ROW(layer_finish_kernel_, 1),
+                                                MOE_ROW(layer_finish_kernel_, 2)};
 static_assert(MOE_FP32 == 0 && MOE_BF16 == 1 && MOE_FP4 == 2, "table rows follow the format codes");
 
 static int maxt_index(int B) { return B <= 1 ? 0 : B <= 2 ? 1 : B <= 4 ? 2 : B <= 8 ? 3 : 4; }
 
-cudaError_t launch_layer(int wdtype, const LayerParams& p, int grid, size_t smem, cudaStream_t s) {
+cudaError_t launch_layer(int wdtype, const LayerParams& p, int grid, size_t smem, bool pdl, cudaStream_t s) {
   if (wdtype < 0 || wdtype > 2) return cudaErrorInvalidValue;
-  return kLaunch[wdtype][maxt_index(p.B)](p, grid, smem, s);
+  return kLaunch[wdtype][maxt_index(p.B)](p, grid, smem, pdl, s);
 }
 
+cudaError_t launch_layer_finish(int wdtype, const LayerParams& p, int grid, size_t smem, cudaStream_t s) {
+  if (wdtype < 0 || wdtype > 2) return cudaErrorInvalidValue;
+  return kFinish[wdtype][maxt_index(p.B)](p, grid, smem, s);
+}
+
+// every kernel of a format: 5 layer kernels, then 5 completion kernels
 static void kernels_of(int wdtype, const void** out) {
-  for (int i = 0; i < 5; ++i) out[i] = kKernel[wdtype][i]();
+  for (int i = 0; i < 5; ++i) {
+    out[i] = kKernel[wdtype][i]();
+    out[5 + i] = kFinishKernel[wdtype][i]();
+  }
 }
 
 size_t layer_static_smem(int wdtype) {
-  const void* fns[5];
+  const void* fns[10];
   kernels_of(wdtype, fns);
   size_t mx = 0;
   for (const void* f : fns) {
@@ -92,7 +109,7 @@ int layer_max_grid(int wdtype, size_t smem) {
   int dev = 0, sms = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const void* fns[5];
+  const void* fns[10];
   kernels_of(wdtype, fns);
   int per_sm = 1;
   for (const void* f : fns) {

@@ -1,4 +1,5 @@
-// One decode-size routed-MoE layer call as a single cooperative launch.
+// One decode-size routed-MoE layer call as a single cooperative launch (plus,
+// in copy-fill mode, a completion launch after the call's copies).
 //
 // FreeToken write-up: the router and the cache lookup run on the GPU ("decode
 // co-design"); one GPU step per layer deduplicates, classifies, picks victims
@@ -8,22 +9,26 @@
 // Fig. 2 caption); decode is memory-bound, each routed expert's weights being
 // read once per token.
 //
-// CTA 0 runs the control step and publishes the miss list to the host, which
-// issues one cudaMemcpyAsync per half record (gate/up part, then W_down) on
-// the copy stream, each followed by a stream write of a per-fill flag.  The
-// other CTAs meanwhile load the activations and run the shared expert's
-// gate/up rows.  Then, all CTAs together (512 threads, one CTA per SM):
-//  1. gate/up rows of the resident experts: h = SiLU(x W_gate^T) * (x W_up^T);
-//     a warp streams one gate row and one up row with 16-byte loads (FP4
-//     dequantised in registers) and serves every token routed to the expert;
-//     CTA 0 meanwhile ranks the oldest slots for the next call;
-//  2. grid barrier, then W_down rows: each CTA owns a contiguous range of
-//     output rows n for every expert and keeps o[t][j][n] in shared memory;
+// Every CTA (512 threads, one per SM) routes the call and looks its experts up
+// itself; CTA 0 also picks the victims and publishes the miss list to the
+// host, which issues one cudaMemcpyAsync per half record (gate/up part, then
+// W_down) on the copy streams, each followed by a stream write of a per-fill
+// flag.  Then:
+//  1. gate/up rows of the resident experts and the shared expert:
+//     h = SiLU(x W_gate^T) * (x W_up^T); a warp streams one gate row and one up
+//     row with 16-byte loads (FP4 dequantised in registers) and serves every
+//     token routed to the expert; meanwhile each CTA's W_down rows of those
+//     experts are staged in shared memory by bulk copies;
+//  2. grid barrier (CTA 0 then commits recency and residency), then W_down
+//     rows: each CTA owns a contiguous range of output rows n for every expert
+//     and keeps o[t][j][n] in shared memory;
 //  3. fills, in order, each as soon as its flag says the copy landed: gate/up
-//     rows, one grid barrier, then W_down rows into the same shared buffer;
+//     rows, one grid barrier, then W_down rows into the same shared buffer (a
+//     CTA that waits too long hands its rows to the completion kernel);
 //  4. y_t[n] = sum_j w_tj o_tj[n] (+ shared) in rank order, in float32.
 // Every dot product has a fixed summation order independent of which phase
-// computes it, so outputs are bitwise identical whatever the residency.
+// or launch computes it, so outputs are bitwise identical whatever the
+// residency.
 #pragma once
 #include "control.cuh"
 #include "expert_math.cuh"
@@ -113,8 +118,8 @@ __device__ void copy_down_rows(const LayerParams& p, const ItemTable& tb, int ib
 }
 
 // token, h row and rank slot of the q-th token of item `it`
-__device__ __forceinline__ void item_token(const LayerParams& p, const Plan* pl, const ItemTable& tb, int it, int q,
-                                           int* t, int* hrow, int* j) {
+__device__ __forceinline__ void item_token(const LayerParams& p, const ItemTable& tb, int it, int q, int* t,
+                                           int* hrow, int* j) {
   const int p0 = tb.pair0[it];
   if (p0 < 0) {
     *t = q;
@@ -131,8 +136,7 @@ __device__ __forceinline__ void item_token(const LayerParams& p, const Plan* pl,
 // Gate/up rows of items [ib, ie), spread over CTAs [cta0, cta0 + ncta).
 // WB: the rows are read from the host pool and also written to the slot.
 template <int WD, int MAXT, bool FRESH, bool WB = false, typename XT>
-__device__ void phase1(const LayerParams& p, const Plan* pl, const ItemTable& tb, int ib, int ie, int cta0, int ncta,
-                       const XT* xs) {
+__device__ void phase1(const LayerParams& p, const ItemTable& tb, int ib, int ie, int cta0, int ncta, const XT* xs) {
   using F = Fmt<WD>;
   constexpr int EPC = F::kElemsPerChunk, UNR = F::kUnroll;
   const int rel = (int)blockIdx.x - cta0;
@@ -154,7 +158,7 @@ __device__ void phase1(const LayerParams& p, const Plan* pl, const ItemTable& tb
 #pragma unroll
     for (int q = 0; q < MAXT; ++q) {
       int t = 0, hr, j;
-      if (q < ntok) item_token(p, pl, tb, it, q, &t, &hr, &j);
+      if (q < ntok) item_token(p, tb, it, q, &t, &hr, &j);
       tok[q] = t;
     }
     float ag[MAXT], au[MAXT];
@@ -214,7 +218,7 @@ __device__ void phase1(const LayerParams& p, const Plan* pl, const ItemTable& tb
         const float u = warp_sum(au[q]);
         if (lane == 0) {
           int t, hr, j;
-          item_token(p, pl, tb, it, q, &t, &hr, &j);
+          item_token(p, tb, it, q, &t, &hr, &j);
           p.h[(int64_t)hr * I + i] = g / (1.0f + expf(-g)) * u;
         }
       }
@@ -251,8 +255,8 @@ __device__ __forceinline__ unsigned short ld_down2(const uint8_t* q) {
 // STAGED: the rows of item ib + j sit in shared memory at stage + j * pitch
 // (rows n0.., then their FP4 scales), copied there during phase 1.
 template <int WD, int MAXT, bool FRESH, bool STAGED = false>
-__device__ void phase2(const LayerParams& p, const Plan* pl, const ItemTable& tb, int ib, int ie, int n0, int nrows,
-                       float* hs, float* os, const uint8_t* stage = nullptr, int pitch = 0) {
+__device__ void phase2(const LayerParams& p, const ItemTable& tb, int ib, int ie, int n0, int nrows, float* hs,
+                       float* os, const uint8_t* stage = nullptr, int pitch = 0) {
   using F = Fmt<WD>;
   constexpr int EPC = F::kElemsPerChunk;
   constexpr int kLanesPerRow = 8, kRowsPerWarp = 32 / kLanesPerRow, kChunksPerLane = MAXT >= 16 ? 4 : 8;
@@ -276,7 +280,7 @@ __device__ void phase2(const LayerParams& p, const Plan* pl, const ItemTable& tb
         int g = g0;
         while (tb.hbase[g + 1] - tb.hbase[g0] <= rr) ++g;
         int t, hr, j;
-        item_token(p, pl, tb, g, rr - (tb.hbase[g] - tb.hbase[g0]), &t, &hr, &j);
+        item_token(p, tb, g, rr - (tb.hbase[g] - tb.hbase[g0]), &t, &hr, &j);
         s_hrow[rr] = hr;
       }
       __syncthreads();
@@ -341,7 +345,7 @@ __device__ void phase2(const LayerParams& p, const Plan* pl, const ItemTable& tb
         a += __shfl_xor_sync(0xFFFFFFFFu, a, 1);
         if (live && gl == 0 && q < ntok) {
           int t, hr, j;
-          item_token(p, pl, tb, gi, q, &t, &hr, &j);
+          item_token(p, tb, gi, q, &t, &hr, &j);
           os[(row - n0) * ostride + t * (k + 1) + j] = a;
         }
       }
@@ -351,12 +355,96 @@ __device__ void phase2(const LayerParams& p, const Plan* pl, const ItemTable& tb
   __syncthreads();
 }
 
+// Items of the call's resident experts (hits in U order, then the shared
+// expert) and the call's pair order and weights, from this CTA's own control
+// tables; returns the item count.  All threads call.
+static __device__ int local_items(const LayerParams& p, const CtrlSmem& cs, ItemTable& tb) {
+  const int n_u = cs.nu, npairs = p.B * p.k, nres = n_u - cs.nmiss;
+  for (int i = threadIdx.x; i < npairs; i += blockDim.x) {
+    tb.perm[i] = cs.perm[i];
+    tb.pair_w[i] = cs.w[i];
+  }
+  for (int r = threadIdx.x; r < n_u; r += blockDim.x) {
+    if (cs.fill[r]) continue;
+    const int i = r - cs.mrank[r];  // hits before rank r
+    tb.rec[i] = p.slots + (int64_t)cs.slot[r] * p.S;
+    tb.dst[i] = nullptr;
+    tb.pair0[i] = cs.off[r];
+    tb.ntok[i] = cs.off[r + 1] - cs.off[r];
+  }
+  if (threadIdx.x == 0 && p.has_shared) {
+    tb.rec[nres] = p.shared_rec;
+    tb.dst[nres] = nullptr;
+    tb.ntok[nres] = p.B;
+    tb.pair0[nres] = -1;
+  }
+  __syncthreads();
+  const int n = nres + (p.has_shared ? 1 : 0);
+  if (threadIdx.x == 0) {
+    int run = 0;
+    for (int i = 0; i < n; ++i) { tb.hbase[i] = run; run += tb.ntok[i]; }
+    tb.hbase[n] = run;
+  }
+  __syncthreads();
+  return n;
+}
+
+// y_t[n] = sum_j w_tj o_tj[n] (+ shared) in rank order for this CTA's rows.
+template <int WD>
+__device__ __forceinline__ void combine_rows(const LayerParams& p, const ItemTable& tb, const float* os, int n0,
+                                             int nrows) {
+  const int B = p.B, k = p.k, H = p.H, ostride = B * (k + 1);
+  for (int e = threadIdx.x; e < nrows * B; e += blockDim.x) {
+    const int nl = e / B, t = e % B, n = n0 + nl;
+    const float* o = os + nl * ostride + t * (k + 1);
+    float acc = 0.f;
+    for (int j = 0; j < k; ++j) acc = fmaf(tb.pair_w[t * k + j], o[j], acc);
+    if (p.has_shared) acc += o[k];
+    if constexpr (WD == MOE_FP32)
+      reinterpret_cast<float*>(p.y)[(int64_t)t * H + n] = acc;
+    else
+      reinterpret_cast<__nv_bfloat16*>(p.y)[(int64_t)t * H + n] = __float2bfloat16_rn(acc);
+  }
+}
+
+// A bounded wait of this CTA gave up: its output rows become NaN, so a caller
+// that reads y without checking the status still cannot mistake it for a result.
+template <int WD>
+__device__ void poison_rows(const LayerParams& p, int n0, int nrows) {
+  for (int e = threadIdx.x; e < nrows * p.B; e += blockDim.x) {
+    const int t = e % p.B, n = n0 + e / p.B;
+    if constexpr (WD == MOE_FP32)
+      reinterpret_cast<float*>(p.y)[(int64_t)t * p.H + n] = __int_as_float(0x7FC00000);
+    else
+      reinterpret_cast<__nv_bfloat16*>(p.y)[(int64_t)t * p.H + n] = __ushort_as_bfloat16((unsigned short)0x7FC0);
+  }
+}
+
+__device__ __forceinline__ int ld_relaxed_s32(const int* q) {
+  int v;
+  asm volatile("ld.relaxed.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(q) : "memory");
+  return v;
+}
+
+// The layer kernel of one decode call.  Every CTA routes the call and looks
+// its experts up itself, so the resident experts' rows start streaming at
+// once; the control CTA also picks the victims, writes the plan and publishes
+// the host summary (the miss list the host issues copies from), and after the
+// first grid barrier (when every CTA has done its lookups) commits recency
+// and residency.  In copy-fill mode each fill is consumed as its stream flag
+// arrives; a CTA that has waited wait_gu_ns for a gate/up half, or wait_dn_ns
+// for a W_down half, stops waiting: its partial sums go to o_part and the
+// completion kernel, ordered after the call's copies on the stream, finishes
+// its rows.  A call's result never depends on copy-engine work progressing
+// while this kernel holds the SMs.
 template <int WD, int MAXT>
 __global__ void __launch_bounds__(kThreads, 1) layer_kernel(LayerParams p) {
   using XT = typename std::conditional<WD == MOE_FP32, float, __nv_bfloat16>::type;
   extern __shared__ __align__(16) uint8_t smem[];
   __shared__ CtrlSmem cs;
   __shared__ ItemTable tb;
+  __shared__ __align__(8) uint64_t s_stage;
+  __shared__ int s_flag;
   const int H = p.H, B = p.B, k = p.k;
   const int G = gridDim.x;
   const bool ctrl = blockIdx.x == 0;
@@ -365,20 +453,15 @@ __global__ void __launch_bounds__(kThreads, 1) layer_kernel(LayerParams p) {
   float* os = hs + p.smem_h_floats;
   const int n0 = (int)((int64_t)blockIdx.x * H / G), n1 = (int)((int64_t)(blockIdx.x + 1) * H / G);
   const int nrows = n1 - n0;
+  const int ostride = B * (k + 1);
+  const bool rec = p.tl && blockIdx.x == 1 && threadIdx.x == 0;
 
-  // ---- 0. control | activations and the shared expert's gate/up rows --------
-  if (p.tl && blockIdx.x == 1 && threadIdx.x == 0) p.tl[0] = globaltimer_ns();
-  if (ctrl) {
-    const int cst = control_step(p, cs);  // ends with a CTA barrier after the plan writes
-    if (threadIdx.x == 0) {
-      st_release_u32(p.plan_flag, p.seq);
-      if (p.tl) p.tl[10] = globaltimer_ns();
-    }
-    if (cst == MOE_OK) {
-      control_commit(p, cs);
-      compact_oldest(p, cs);
-    }
-    if (p.tl && threadIdx.x == 0) p.tl[11] = globaltimer_ns();
+  grid_dep_wait();  // the previous call's commit and outputs are visible
+  grid_dep_launch();
+  if (rec) p.tl[0] = globaltimer_ns();
+  if (threadIdx.x == 0) {
+    p.cst->part[blockIdx.x] = -1;
+    if (ctrl) p.cst->gu_stop = 0;  // before the first grid barrier, which every later writer passes
   }
   {
     const int nvec = (int)((size_t)B * H * sizeof(XT) / 16);
@@ -386,36 +469,18 @@ __global__ void __launch_bounds__(kThreads, 1) layer_kernel(LayerParams p) {
     uint4* dst = reinterpret_cast<uint4*>(xs);
     for (int i = threadIdx.x; i < nvec; i += blockDim.x) dst[i] = src[i];
   }
-  if (!ctrl && p.has_shared) {
-    if (threadIdx.x == 0) {
-      tb.rec[0] = p.shared_rec;
-      tb.ntok[0] = B;
-      tb.pair0[0] = -1;
-      tb.hbase[0] = 0;
-      tb.hbase[1] = B;
-    }
-    __syncthreads();
-    phase1<WD, MAXT, false>(p, p.plan, tb, 0, 1, 1, G - 1, xs);
-  }
-  if (!ctrl && wait_flag(p.plan_flag, p.seq, p.err, 5000000000ull, 32) != 0) return;
-  __syncthreads();
-  const bool rec = p.tl && blockIdx.x == 1 && threadIdx.x == 0;
-  if (rec) p.tl[1] = globaltimer_ns();
-  const Plan* pl = p.plan;
-  if (pl->err != MOE_OK) return;
 
-  // ---- 1. gate/up rows of the resident routed experts --------------------------
-  const int n_res = load_items(p, pl, 0, tb);
-  if (p.device_fill && pl->n_items[1] > 0) {
-    // device-driven fills: pull each missed record from the host pool, use it
-    // for this call and store it in its slot; W_down rows by the CTA that owns them
-    const int n_all = load_items(p, pl, 1, tb, n_res, true);
-    copy_down_rows<WD>(p, tb, n_res, n_all, n0, nrows);
-    if (!ctrl) phase1<WD, MAXT, false, true>(p, pl, tb, n_res, n_all, 1, G - 1, xs);
-  }
+  // ---- 0. routing and lookup (every CTA); victims, plan, summary (control CTA)
+  int err = route_lookup(p, cs, ctrl);
+  if (ctrl) err = err == MOE_OK ? choose_victims(p, cs) : (publish_error(p, cs, err), err);
+  if (err != MOE_OK) return;  // capacity: every CTA; inconsistent victim list: the control CTA
+  if (ctrl && p.tl) p.tl[10] = globaltimer_ns();
+  if (rec) p.tl[1] = globaltimer_ns();
+
+  // ---- 1. gate/up rows of the resident experts and the shared expert --------------
+  const int n_res = local_items(p, cs, tb);
   // this CTA's W_down rows of the resident experts: the first n_stage items
   // into shared memory by bulk copies completing on s_stage, the rest into L2
-  __shared__ __align__(8) uint64_t s_stage;
   const int n_stage = nrows > 0 ? min(n_res, p.stage_items) : 0;
   const uint8_t* stage = smem + p.stage_off;
   {
@@ -437,88 +502,201 @@ __global__ void __launch_bounds__(kThreads, 1) layer_kernel(LayerParams p) {
       if (WD == MOE_FP4) prefetch_l2(v.down_sc + (int64_t)n0 * sb, (uint32_t)(nrows * sb));
     }
   }
-  if (!ctrl) phase1<WD, MAXT, false>(p, pl, tb, 0, n_res - p.has_shared, 1, G - 1, xs);
+  if (!ctrl) phase1<WD, MAXT, false>(p, tb, 0, n_res, 1, G - 1, xs);
   if (rec) p.tl[2] = globaltimer_ns();
-  const bool bar_ok = grid_barrier(p.bar, p.bar_base + (unsigned long long)G, p.err);
+
+  // the fills' slots come from the control CTA's plan
+  bool ok = true;
+  if (!ctrl && wait_flag(p.plan_flag, p.seq, nullptr, 5000000000ull, 32) != 0) {
+    if (threadIdx.x == 0) atomicExch(p.err, MOE_ERR_TIMEOUT);
+    ok = false;
+  }
+  const Plan* pl = p.plan;
+  if (ok && pl->err != MOE_OK) ok = false;  // the control CTA returned above
+  const int nf = ok ? pl->n_items[1] : 0;
+  if (ok && p.device_fill && nf > 0) {
+    // device-driven fills: pull each missed record from the host pool, use it
+    // for this call and store it in its slot; W_down rows by the CTA that owns them
+    const int n_all = load_items(p, pl, 1, tb, n_res, true);
+    copy_down_rows<WD>(p, tb, n_res, n_all, n0, nrows);
+    if (!ctrl) phase1<WD, MAXT, false, true>(p, tb, n_res, n_all, 1, G - 1, xs);
+  }
+  const bool bar_ok = ok && grid_barrier(p.bar, p.err);
   if (n_stage > 0 && !mbar_wait(&s_stage, 0)) {  // the staging copies never leave this CTA in flight
     if (threadIdx.x == 0) atomicExch(p.err, MOE_ERR_TIMEOUT);
     mbar_wait(&s_stage, 0);
+    poison_rows<WD>(p, n0, nrows);
     return;
   }
-  if (!bar_ok) return;
+  if (!bar_ok) {
+    if (ok) poison_rows<WD>(p, n0, nrows);
+    return;
+  }
   if (rec) p.tl[3] = globaltimer_ns();
+  if (ctrl) {
+    control_commit(p, cs);
+    compact_oldest(p, cs);
+    if (p.tl && threadIdx.x == 0) p.tl[11] = globaltimer_ns();
+  }
 
   // ---- 2. W_down rows of the resident experts --------------------------------------
-  const int ostride = B * (k + 1);
   for (int i = threadIdx.x; i < nrows * ostride; i += blockDim.x) os[i] = 0.f;
-  phase2<WD, MAXT, false, true>(p, pl, tb, 0, n_stage, n0, nrows, hs, os, stage, p.stage_pitch);
-  phase2<WD, MAXT, false>(p, pl, tb, n_stage, n_res, n0, nrows, hs, os);
+  phase2<WD, MAXT, false, true>(p, tb, 0, n_stage, n0, nrows, hs, os, stage, p.stage_pitch);
+  phase2<WD, MAXT, false>(p, tb, n_stage, n_res, n0, nrows, hs, os);
   if (rec) p.tl[4] = globaltimer_ns();
 
-  // ---- 3. fills, each as soon as its copy has landed -------------------------------
-  const int nf = pl->n_items[1];
-  int fill_err = 0;
+  // ---- 3. fills ----------------------------------------------------------------------
   if (nf > 0 && p.device_fill) {
     // device-driven fills: this CTA copied its own W_down rows of every fill
     // into the slots in phase 1, so they are read there, not over the link
     for (int it = n_res + (int)threadIdx.x; it < n_res + nf; it += blockDim.x) tb.rec[it] = tb.dst[it];
     __syncthreads();
-    phase2<WD, MAXT, true>(p, pl, tb, n_res, n_res + nf, n0, nrows, hs, os);
+    phase2<WD, MAXT, true>(p, tb, n_res, n_res + nf, n0, nrows, hs, os);
   } else if (nf > 0) {
+    // copy mode: each fill as soon as its copy has landed
     load_items(p, pl, 1, tb);
-    for (int f = 0; f < nf && !fill_err; ++f) {
-      if (wait_flag(&p.fill_flags[f], p.seq, p.err) != 0) {
-        fill_err = 1;
+    for (int f = 0; f < nf; ++f) {
+      if (wait_flag(&p.fill_flags[f], p.seq, &p.cst->gu_stop, p.wait_gu_ns) != 0) {
+        if (threadIdx.x == 0) atomicExch(&p.cst->gu_stop, 1);  // every CTA stops waiting
         break;
       }
       if (rec && f == 0) p.tl[5] = globaltimer_ns();
-      phase1<WD, MAXT, true>(p, pl, tb, f, f + 1, 0, G, xs);
+      phase1<WD, MAXT, true>(p, tb, f, f + 1, 0, G, xs);
     }
     if (rec) p.tl[6] = globaltimer_ns();
-    if (!grid_barrier(p.bar, p.bar_base + 2ull * G, p.err)) return;
+    if (!grid_barrier(p.bar, p.err)) {
+      poison_rows<WD>(p, n0, nrows);
+      return;
+    }
     if (rec) p.tl[7] = globaltimer_ns();
-    for (int f = 0; f < nf && !fill_err; ++f) {
-      if (wait_flag(&p.fill_flags[kMaxU + f], p.seq, p.err) != 0) {
-        fill_err = 1;
+    if (threadIdx.x == 0) s_flag = ld_relaxed_s32(&p.cst->gu_stop);
+    __syncthreads();
+    int handed = s_flag ? 0 : -1;  // fills whose W_down rows os holds when handing over
+    for (int f = 0; f < nf && handed < 0; ++f) {
+      if (wait_flag(&p.fill_flags[kMaxU + f], p.seq, nullptr, p.wait_dn_ns) != 0) {
+        handed = f;
         break;
       }
       if (rec && f == nf - 1) p.tl[8] = globaltimer_ns();
-      phase2<WD, MAXT, true>(p, pl, tb, f, f + 1, n0, nrows, hs, os);
+      phase2<WD, MAXT, true>(p, tb, f, f + 1, n0, nrows, hs, os);
     }
-    if (fill_err) {
-      if (ctrl) undo_call(p);
+    if (handed >= 0) {
+      // the completion kernel finishes this CTA's rows after the copies
+      float* dst = p.o_part + (int64_t)blockIdx.x * p.o_part_floats;
+      for (int i = threadIdx.x; i < nrows * ostride; i += blockDim.x) dst[i] = os[i];
+      if (threadIdx.x == 0) p.cst->part[blockIdx.x] = handed;
       return;
     }
   }
 
   // ---- 4. weighted combine in rank order --------------------------------------------
-  for (int e = threadIdx.x; e < nrows * B; e += blockDim.x) {
-    const int nl = e / B, t = e % B, n = n0 + nl;
-    const float* o = os + nl * ostride + t * (k + 1);
-    float acc = 0.f;
-    for (int j = 0; j < k; ++j) acc = fmaf(tb.pair_w[t * k + j], o[j], acc);
-    if (p.has_shared) acc += o[k];
-    if constexpr (WD == MOE_FP32)
-      reinterpret_cast<float*>(p.y)[(int64_t)t * H + n] = acc;
-    else
-      reinterpret_cast<__nv_bfloat16*>(p.y)[(int64_t)t * H + n] = __float2bfloat16_rn(acc);
-  }
+  combine_rows<WD>(p, tb, os, n0, nrows);
   if (rec) p.tl[9] = globaltimer_ns();
 }
 
-// Cooperative launch of one instantiation (dynamic shared memory raised once
-// per instantiation to the largest size asked for).
+// Completion kernel of a copy-fill call, launched on the compute stream after
+// the call's copies have ended.  Every fill flag is final by then: if one
+// carries the error bit (the host could not issue a copy), the call is undone.
+// Otherwise the CTAs that handed over finish their rows: the fills' gate/up
+// rows when the layer kernel stopped before them (then every CTA takes part
+// and one grid barrier follows), the remaining W_down rows from the saved
+// partial sums, and the combine, with the layer kernel's code and summation
+// order, so the outputs are bitwise the same as when it finishes alone.
 template <int WD, int MAXT>
-cudaError_t launch_t(const LayerParams& p, int grid, size_t smem, cudaStream_t s) {
-  auto fn = layer_kernel<WD, MAXT>;
-  static size_t smem_set = 0;  // largest dynamic shared memory already allowed for this instantiation
-  if (smem > smem_set) {
+__global__ void __launch_bounds__(kThreads, 1) layer_finish_kernel(LayerParams p) {
+  using XT = typename std::conditional<WD == MOE_FP32, float, __nv_bfloat16>::type;
+  extern __shared__ __align__(16) uint8_t smem[];
+  __shared__ ItemTable tb;
+  __shared__ int s_state[3];
+  const int H = p.H, B = p.B, k = p.k;
+  const int G = gridDim.x;
+  XT* xs = reinterpret_cast<XT*>(smem);
+  float* hs = reinterpret_cast<float*>(smem + (((size_t)B * H * sizeof(XT) + 15) & ~(size_t)15));
+  float* os = hs + p.smem_h_floats;
+  const int n0 = (int)((int64_t)blockIdx.x * H / G), n1 = (int)((int64_t)(blockIdx.x + 1) * H / G);
+  const int nrows = n1 - n0;
+  const int ostride = B * (k + 1);
+  const Plan* pl = p.plan;
+  if (pl->err != MOE_OK) return;
+  const int nf = pl->n_items[1];
+  if (threadIdx.x == 0) {
+    int failed = 0;
+    for (int f = 0; f < nf; ++f)
+      if (p.fill_flags[f] != p.seq || p.fill_flags[kMaxU + f] != p.seq) failed = 1;
+    s_state[0] = failed;
+    s_state[1] = p.cst->gu_stop;
+    s_state[2] = p.cst->part[blockIdx.x];
+  }
+  __syncthreads();
+  if (s_state[0]) {
+    if (blockIdx.x == 0) undo_call(p);
+    return;
+  }
+  const int gu = s_state[1], part = s_state[2];
+  if (!gu && part < 0) return;  // the layer kernel finished this CTA's rows
+  for (int i = threadIdx.x; i < B * k; i += blockDim.x) {
+    tb.perm[i] = pl->perm[i];
+    tb.pair_w[i] = pl->pair_w[i];
+  }
+  load_items(p, pl, 1, tb);
+  if (gu) {
+    const int nvec = (int)((size_t)B * H * sizeof(XT) / 16);
+    const uint4* src = reinterpret_cast<const uint4*>(p.x);
+    uint4* dst = reinterpret_cast<uint4*>(xs);
+    for (int i = threadIdx.x; i < nvec; i += blockDim.x) dst[i] = src[i];
+    __syncthreads();
+    phase1<WD, MAXT, false>(p, tb, 0, nf, 0, G, xs);
+    if (!grid_barrier(p.bar, p.err)) {
+      poison_rows<WD>(p, n0, nrows);
+      return;
+    }
+  }
+  const float* srcp = p.o_part + (int64_t)blockIdx.x * p.o_part_floats;
+  for (int i = threadIdx.x; i < nrows * ostride; i += blockDim.x) os[i] = srcp[i];
+  __syncthreads();
+  phase2<WD, MAXT, false>(p, tb, gu ? 0 : part, nf, n0, nrows, hs, os);
+  combine_rows<WD>(p, tb, os, n0, nrows);
+  if (blockIdx.x == 0 && threadIdx.x == 0) atomicAdd(p.deferred, 1ull);
+}
+
+// Launch of one instantiation as a cooperative grid (every CTA resident, for
+// the grid barriers), optionally as a programmatic dependent of the previous
+// launch on the stream; dynamic shared memory is raised once per kernel to the
+// largest size asked for.
+template <typename K>
+static cudaError_t launch_coop(K fn, size_t* smem_set, const LayerParams& p, int grid, size_t smem, bool pdl,
+                               cudaStream_t s) {
+  if (smem > *smem_set) {
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    smem_set = smem;
+    *smem_set = smem;
   }
   void* args[] = {const_cast<LayerParams*>(&p)};
-  return cudaLaunchCooperativeKernel((const void*)fn, dim3(grid), dim3(kThreads), args, smem, s);
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 2 : 1;
+  return cudaLaunchKernelExC(&cfg, (const void*)fn, args);
+}
+
+template <int WD, int MAXT>
+cudaError_t launch_t(const LayerParams& p, int grid, size_t smem, bool pdl, cudaStream_t s) {
+  static size_t smem_set = 0;
+  return launch_coop(layer_kernel<WD, MAXT>, &smem_set, p, grid, smem, pdl, s);
+}
+
+template <int WD, int MAXT>
+cudaError_t launch_finish_t(const LayerParams& p, int grid, size_t smem, cudaStream_t s) {
+  static size_t smem_set = 0;
+  return launch_coop(layer_finish_kernel<WD, MAXT>, &smem_set, p, grid, smem, false, s);
 }
 
 }  // namespace moe

@@ -69,7 +69,7 @@ __device__ void route_token(const ResidentParams& p, int t, int32_t* ids, float*
     }
     chosen[r] = bi;
     if (r == 0) m0 = bv;
-    const float ex = expf(bv - m0);
+    const float ex = bv == m0 ? 1.f : expf(bv - m0);  // equal to the largest (also +-inf): exp(0)
     sum += ex;
     if (lane == 0) { ids[t * p.k + r] = bi; w[t * p.k + r] = ex; }
   }

@@ -17,9 +17,14 @@ struct LayerParams {
   uint32_t seq;               // call sequence number
   unsigned* plan_flag;        // set to seq by the control CTA once the plan is written
   unsigned* fill_flags;       // [2][kMaxU]: first/second half of fill f landed (seq, or seq|kFlagError)
-  unsigned long long* bar;    // grid barrier counter
-  unsigned long long bar_base;
-  int* err;
+  unsigned long long* bar;    // grid barrier counter (only grows; see grid_barrier)
+  int* err;                   // pinned, mapped: MOE_ERR_TIMEOUT when a bounded wait for the GPU gave up
+  CallState* cst;             // copy-fill completion state of this call
+  float* o_part;              // [gridDim.x][o_part_floats]: saved partial sums of CTAs that handed over
+  int o_part_floats;          // rows_per_cta_max * max_tokens * (k + 1)
+  unsigned long long wait_gu_ns;  // how long the layer kernel waits for a fill's gate/up half
+  unsigned long long wait_dn_ns;  // ... and for its W_down half, before handing the rest over
+  unsigned long long* deferred;   // calls the completion kernel finished (statistics)
   int has_shared;
   int device_fill;            // 1: the kernel pulls each fill from the pool itself
   const uint8_t* pool;        // device-visible address of the pinned host pool (device_fill)
@@ -51,7 +56,11 @@ cudaError_t launch_router_logits(const void* x, bool x_bf16, const float* wr, in
                                  cudaStream_t s);
 size_t layer_smem_bytes(int wdtype, int B, int H, int k, int smem_h_floats, int rows_per_cta_max);
 size_t layer_static_smem(int wdtype);
-cudaError_t launch_layer(int wdtype, const LayerParams& p, int grid, size_t smem, cudaStream_t s);
+// The layer kernel of one call (pdl: launched as a programmatic dependent of
+// the previous launch on the stream), and its completion kernel, which runs
+// after the call's copies and finishes whatever the layer kernel handed over.
+cudaError_t launch_layer(int wdtype, const LayerParams& p, int grid, size_t smem, bool pdl, cudaStream_t s);
+cudaError_t launch_layer_finish(int wdtype, const LayerParams& p, int grid, size_t smem, cudaStream_t s);
 int layer_max_grid(int wdtype, size_t smem);
 cudaError_t launch_slot_moves(uint8_t* base, int64_t S, const int32_t* moves, int n_moves, cudaStream_t s);
 void set_last_error(const char* msg);  // message returned by moe_last_error() on this thread

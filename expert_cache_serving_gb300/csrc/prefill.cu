@@ -52,7 +52,7 @@ __global__ void route_kernel(const float* __restrict__ logits, int T, int E, int
     }
     if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
     if (r == 0) m0 = bv;
-    const float ex = expf(bv - m0);
+    const float ex = bv == m0 ? 1.f : expf(bv - m0);  // equal to the largest (also +-inf): exp(0)
     sum += ex;
     if (lane == r) { my_id = bi; mine = ex; }
   }

@@ -39,7 +39,8 @@ class moe_stats(ctypes.Structure):
                 ("resize_evictions", ctypes.c_int64), ("prefill_layers", ctypes.c_int64),
                 ("prefill_tokens", ctypes.c_int64), ("prefill_ms", ctypes.c_double),
                 ("prefill_copy_ms", ctypes.c_double), ("prefill_compute_ms", ctypes.c_double),
-                ("prefill_gemm_ms", ctypes.c_double), ("prefill_gemm_flop", ctypes.c_double)]
+                ("prefill_gemm_ms", ctypes.c_double), ("prefill_gemm_flop", ctypes.c_double),
+                ("deferred_calls", ctypes.c_int64), ("finish_launches", ctypes.c_int64)]
 
     def as_dict(self):
         return {name: getattr(self, name) for name, _ in self._fields_}
@@ -77,6 +78,8 @@ SIGNATURES = {
     "moe_layer_forward_ex": (_I32, [_P, _I32, _P, _P, _P, _I32, _P, _P, ctypes.POINTER(moe_layer_aux)]),
     "moe_prefill_stream": (_I32, [_P, _I32, _I32, _P, _P, _I32, _P, _P]),
     "moe_cache_stats": (_I32, [_P, ctypes.POINTER(moe_stats)]),
+    "moe_cache_sync": (_I32, [_P, _P]),
+    "moe_cache_set_wait_limit_ns": (_I32, [_P, _I64, _I64]),
     "moe_cache_reset_stats": (_I32, [_P]),
     "moe_cache_set_profiling": (_I32, [_P, _I32]),
     "moe_cache_phase_times": (_I32, [_P, ctypes.POINTER(moe_phase_times)]),
@@ -172,6 +175,15 @@ def moe_cache_stats(cache: int) -> dict:
     st = moe_stats()
     check(lib.moe_cache_stats(cache, ctypes.byref(st)), "moe_cache_stats")
     return st.as_dict()
+
+
+def moe_cache_sync(cache: int, stream=None) -> int:
+    """Waits for the cache's enqueued calls; returns the first error the GPU found after they returned."""
+    return lib.moe_cache_sync(cache, _stream(stream))
+
+
+def moe_cache_set_wait_limit_ns(cache: int, gate_up_ns: int, down_ns: int) -> None:
+    check(lib.moe_cache_set_wait_limit_ns(cache, int(gate_up_ns), int(down_ns)), "moe_cache_set_wait_limit_ns")
 
 
 def moe_cache_reset_stats(cache: int) -> None:

@@ -61,6 +61,7 @@ def run() -> None:
                 err = np.max(np.abs(got - ref))
                 assert err <= 1e-2 * np.max(np.abs(ref)), f"layer output error {err}"
         torch.cuda.synchronize()
+        mc.check(mc.moe_cache_sync(cache.handle, torch.cuda.current_stream()), "moe_cache_sync")
         assert [tuple(e) for e in mc.moe_cache_trace(cache.handle)] == want_events, "cache event log mismatch"
         cache.close()
 

@@ -110,6 +110,8 @@ typedef struct {
   double prefill_compute_ms; /* summed per-layer compute time after each layer's experts landed */
   double prefill_gemm_ms;    /* summed time of the grouped GEMM launches */
   double prefill_gemm_flop;  /* useful flops of those launches (2 * rows * N * K) */
+  int64_t deferred_calls;    /* copy-fill calls finished by the completion kernel (fills landed late) */
+  int64_t finish_launches;   /* completion-kernel launches (one per copy-fill call with misses) */
 } moe_stats;
 
 typedef struct {
@@ -172,17 +174,27 @@ moe_status moe_cache_resize(moe_cache_t cache, int64_t n_slots, void* stream);
  *   type, written.
  * logits: device float32 [B][E], or NULL to compute logits = x W_r^T from
  *   router_w: device float32 [E][H] (then router_w must not be NULL).
- * The call routes (top-k softmax), updates the LRU cache (one control kernel),
- * copies each miss's record from the host pool into its victim slot with
- * cudaMemcpyAsync on the copy stream while the resident experts already run,
- * evaluates every selected expert (and the shared expert) straight from the
- * cache slots, and writes y_t = sum_j w_tj * o_tj (+ shared) in rank order.
- * The host waits once per call for the control kernel (it needs the miss
- * list to issue the copies); the rest stays asynchronous on `stream`.
+ * The call routes (top-k softmax), updates the LRU cache (inside the layer
+ * kernel), copies each miss's record from the host pool into its victim slot
+ * with cudaMemcpyAsync on the copy streams while the resident experts already
+ * run, evaluates every selected expert (and the shared expert) straight from
+ * the cache slots, and writes y_t = sum_j w_tj * o_tj (+ shared) in rank order.
+ * Copy-fill mode (default): the host waits once per call for the layer
+ * kernel's miss list (it issues the copies), then enqueues a small completion
+ * kernel on `stream` after the call's copies; the layer kernel consumes each
+ * fill as it lands, and if a fill is late (see moe_cache_set_wait_limit_ns)
+ * it hands the remaining work to the completion kernel, so y is always this
+ * call's result once `stream` reaches the end of the call.  Device-fill mode:
+ * the call does not wait for the GPU at all when B*k <= n_slots.
  * Errors: MOE_ERR_INVALID_ARG, MOE_ERR_CAPACITY (more distinct experts than
  *   slots; cache unchanged, y unspecified), MOE_ERR_CUDA (a fill could not be
- *   issued: recency is rolled back and this call's victim slots are left
- *   empty; y unspecified), MOE_ERR_TIMEOUT. */
+ *   issued: the completion kernel rolls recency back and leaves this call's
+ *   victim slots empty; y unspecified), MOE_ERR_TIMEOUT (a bounded wait inside
+ *   an earlier kernel of this cache gave up: the outputs of that call are NaN;
+ *   the state has been recovered and this call did nothing).  Errors that the
+ *   GPU finds after the call returned (a bounded wait that gave up, or, in
+ *   device-fill mode, an inconsistent victim list) are reported by
+ *   moe_cache_sync and by the next call. */
 moe_status moe_layer_forward(moe_cache_t cache, int32_t layer, const void* x, const float* logits,
                              const float* router_w, int32_t B, void* y, void* stream);
 
@@ -207,8 +219,24 @@ moe_status moe_layer_forward_ex(moe_cache_t cache, int32_t layer, const void* x,
 moe_status moe_prefill_stream(moe_cache_t cache, int32_t layer_begin, int32_t layer_end, const void* x,
                               const float* logits, int32_t T, void* y, void* stream);
 
+/* Wait for every call of this cache enqueued so far (on `stream` and on the
+ * cache's copy streams), read their summaries, and return the first error
+ * the GPU found after the calls returned: MOE_ERR_TIMEOUT when a bounded
+ * wait inside a kernel gave up (the rows of that call are NaN; the state is
+ * recovered), MOE_ERR_CUDA for an inconsistent victim list in device-fill
+ * mode.  MOE_OK otherwise.  The error is cleared once returned. */
+moe_status moe_cache_sync(moe_cache_t cache, void* stream);
+
+/* How long the layer kernel waits for a fill's gate/up half (gate_up_ns) and
+ * for its W_down half (down_ns) in copy-fill mode before it hands the rest of
+ * the call to the completion kernel (default 2 ms each; 0 hands over at once
+ * whenever a half has not landed yet).  Either way the result is the same,
+ * bit for bit; the limits only trade SM time spent waiting against a second
+ * pass over the fills.  Errors: MOE_ERR_INVALID_ARG (negative or above 60 s). */
+moe_status moe_cache_set_wait_limit_ns(moe_cache_t cache, int64_t gate_up_ns, int64_t down_ns);
+
 /* Counters since creation (or the last reset).  Synchronises the events of
- * profiled launches. */
+ * profiled launches and reads the summaries of calls in flight. */
 moe_status moe_cache_stats(moe_cache_t cache, moe_stats* out);
 moe_status moe_cache_reset_stats(moe_cache_t cache);
 

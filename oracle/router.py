@@ -9,9 +9,15 @@ Readings where the pages are silent:
 * the weights are a softmax over the k selected logits (equivalently the
   full softmax renormalised over the selected experts), so each token's
   weights sum to 1;
-* a NaN logit is treated as -inf (it is never preferred to a real logit).
+* a NaN logit is treated as -inf (it is never preferred to a real logit);
+* the weights use exp(l_j - l_max) with exp taken as 1 for every selected
+  logit equal to the largest one, i.e. the limit of the softmax over equal
+  logits: a token whose selected logits are all -inf (or NaN) gets equal
+  weights 1/k, and the +inf entries of a token share its weight equally.
 """
 from __future__ import annotations
+
+import math
 
 import numpy as np
 
@@ -41,7 +47,9 @@ def topk_softmax(logits: np.ndarray, k: int) -> tuple[np.ndarray, np.ndarray]:
         ids[t] = sel
         z = np.array([logits[t, e] for e in sel], dtype=np.float64)
         z = np.where(np.isnan(z), -np.inf, z)
-        z = np.exp(z - z[0])  # z[0] is the largest selected logit
+        # z[0] is the largest selected logit; equal logits (also -inf == -inf
+        # and +inf == +inf) contribute exp(0) = 1
+        z = np.array([1.0 if zj == z[0] else math.exp(zj - z[0]) for zj in z])
         w[t] = z / z.sum()
     return ids, w
 

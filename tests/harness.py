@@ -93,11 +93,13 @@ def run_oracle(w: Workload, calls, logits=None, router_w=None, C=None, y_for=Non
 
 
 def run_gpu(w: Workload, calls, logits=None, router_w=None, C=None, max_slots=0, resize=None, keep_y=True,
-            pool=None, shared=None, inject=None, fill_mode=0, y_for=None, light=False):
+            pool=None, shared=None, inject=None, fill_mode=0, y_for=None, light=False, wait_ns=None):
     """GPU side through the C ABI; returns (RunOut, final cache state, stats).
     inject: {call index: number of fills that succeed before the injected failure}.
     y_for: call indices whose output to keep (None = all, when keep_y).
-    light: only ids and slots are read back per call (full-size runs)."""
+    light: only ids and slots are read back per call (full-size runs).
+    wait_ns: (gate/up, W_down) fill wait limits of the layer kernel (None: the library's).
+    Ends with moe_cache_sync, which must report no error."""
     import torch
 
     from expert_cache_serving_gb300 import moecache as mc
@@ -109,6 +111,8 @@ def run_gpu(w: Workload, calls, logits=None, router_w=None, C=None, max_slots=0,
     cache = runner.Cache(w, pool, shared, C=C, max_slots=max_slots)
     mc.moe_cache_set_trace(cache.handle, True)
     mc.moe_cache_set_fill_mode(cache.handle, fill_mode)
+    if wait_ns is not None:
+        mc.moe_cache_set_wait_limit_ns(cache.handle, *wait_ns)
     B, k, E, H = w.B, w.k, w.E, w.H
     xdt = runner.x_dtype(w)
     ids = torch.empty((B, k), dtype=torch.int32, device=dev)
@@ -145,6 +149,8 @@ def run_gpu(w: Workload, calls, logits=None, router_w=None, C=None, max_slots=0,
                 co.y = y.float().cpu().numpy().astype(np.float64)
         out.calls.append(co)
     torch.cuda.synchronize()
+    st = mc.moe_cache_sync(cache.handle, stream)
+    assert st == mc.MOE_OK, mc.moe_last_error()
     out.events = mc.moe_cache_trace(cache.handle)
     state = mc.moe_cache_state(cache.handle, cache.w.LE if max_slots == 0 else max_slots)
     stats = mc.moe_cache_stats(cache.handle)

@@ -81,6 +81,25 @@ def test_router_degenerate_cases():
     assert list(ids[0]) == [1, 3]
 
 
+def test_router_non_finite_rows_take_the_equal_logit_limit():
+    # every selected logit -inf (or NaN): the limit of a softmax over equal
+    # logits, i.e. uniform weights over the k lowest ids (library softmax on
+    # equal finite logits gives the same)
+    for row in (np.full((1, 6), -np.inf), np.full((1, 6), np.nan)):
+        ids, w = router.topk_softmax(row, 3)
+        assert list(ids[0]) == [0, 1, 2]
+        assert np.allclose(w[0], scipy.special.softmax(np.zeros(3)), rtol=0, atol=1e-15)
+    # +inf entries share the weight: the limit of softmax([M, M, 0]) as M grows
+    row = np.array([[0.0, np.inf, -1.0, np.inf]])
+    ids, w = router.topk_softmax(row, 3)
+    assert list(ids[0]) == [1, 3, 0]
+    assert np.allclose(w[0], scipy.special.softmax(np.array([800.0, 800.0, 0.0])), rtol=0, atol=1e-15)
+    # a single real logit above -inf: all the weight on it
+    row = np.array([[-np.inf, -np.inf, 0.25, np.nan]])
+    ids, w = router.topk_softmax(row, 3)
+    assert list(ids[0]) == [2, 0, 1] and list(w[0]) == [1.0, 0.0, 0.0]
+
+
 def test_router_logits_brute_force():
     rng = np.random.default_rng(3)
     x = rng.standard_normal((2, 5))
