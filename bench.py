@@ -567,7 +567,7 @@ def run_native(args):
     }
     if rank == 0 and not args.no_cpu_baseline:
         n_tok = args.cpu_tokens
-        calls, secs = oracle_tokens(w, inp.lg_host, n_tok, pool_np=inp.pool)
+        calls, secs = oracle_tokens(w, inp.lg_host, n_tok, pool_np=inp.pool.numpy())
         line["cpu_baseline"] = {"value": calls / w.L * w.B / secs, "unit": "tok/s (decode)",
                                 "cores": os.cpu_count(), "blas_threads": blas_threads(), "kind": "oracle",
                                 "sample": f"first {n_tok} tokens x {w.L} layers of the trace, float64 numpy, "

@@ -249,6 +249,12 @@ struct moe_cache {
     void *xp = nullptr, *hp = nullptr;
     float* op = nullptr;
     cudaEvent_t loaded[2] = {nullptr, nullptr}, consumed[2] = {nullptr, nullptr}, start = nullptr;
+    int32_t* tab = nullptr;   // [steps][E] record slot of each expert per step
+    int tab_steps = 0;
+    int32_t* zero = nullptr;  // {0}: slot table of the shared expert's one-record maps
+    // pinned host copies of the bookkeeping (the state after a prefill is uploaded from them)
+    int32_t *h_owner = nullptr, *h_map = nullptr;
+    uint64_t *h_stamp = nullptr, *h_g = nullptr;
     struct Timed {
       cudaEvent_t a, b;
       int kind;  // 0 whole call, 1 copy, 2 compute, 3 gemm
@@ -320,8 +326,11 @@ static void free_all(moe_cache* c) {
   }
   for (cudaEvent_t e : c->ev_pool) cudaEventDestroy(e);
   for (void* p : {(void*)c->pf.ids, (void*)c->pf.cnt, (void*)c->pf.base, (void*)c->pf.offsets, (void*)c->pf.pos,
-                  (void*)c->pf.perm, (void*)c->pf.w, c->pf.xp, c->pf.hp, (void*)c->pf.op})
+                  (void*)c->pf.perm, (void*)c->pf.w, c->pf.xp, c->pf.hp, (void*)c->pf.op, (void*)c->pf.tab,
+                  (void*)c->pf.zero})
     if (p) cudaFree(p);
+  for (void* p : {(void*)c->pf.h_owner, (void*)c->pf.h_map, (void*)c->pf.h_stamp, (void*)c->pf.h_g})
+    if (p) cudaFreeHost(p);
   for (cudaEvent_t e : {c->pf.loaded[0], c->pf.loaded[1], c->pf.consumed[0], c->pf.consumed[1], c->pf.start})
     if (e) cudaEventDestroy(e);
   for (auto& t : c->pf.timed) {
@@ -662,7 +671,10 @@ static moe_status follow_stream(moe_cache* c, cudaStream_t s) {
 static cudaError_t launch_k1(moe_cache* c, const LayerParams& p, cudaStream_t s) {
   if (c->pdl) {
     cudaError_t e = launch_layer(c->d.wdtype, p, c->grid, c->smem, true, s);
-    if (e == cudaSuccess) return e;
+    if (e == cudaSuccess) {
+      c->st.pdl_launches += 1;
+      return e;
+    }
     cudaGetLastError();  // programmatic dependent launch refused for this launch: launch plainly from now on
     c->pdl = false;
   }
@@ -1159,6 +1171,37 @@ static moe_status map_fp4_layer(Fp4Maps* m, const uint8_t* base, int n, int H, i
   return map_fp4_scales(&m->dn_s, base + HI + HI / 8 + HI / 2, n, H, I, S);
 }
 
+static constexpr int kPrefillChunk = 8192;  // tokens per pass over the layers (the pages' prefill chunk)
+
+static moe_status prefill_staging(moe_cache* c) {
+  auto& pf = c->pf;
+  if (pf.h_owner) return MOE_OK;
+  const int64_t cmax = std::max<int64_t>(1, c->C_max), LE = (int64_t)c->d.L * c->d.E;
+  if (cudaHostAlloc((void**)&pf.h_owner, sizeof(int32_t) * cmax, 0) != cudaSuccess ||
+      cudaHostAlloc((void**)&pf.h_stamp, sizeof(uint64_t) * cmax, 0) != cudaSuccess ||
+      cudaHostAlloc((void**)&pf.h_map, sizeof(int32_t) * LE, 0) != cudaSuccess ||
+      cudaHostAlloc((void**)&pf.h_g, sizeof(uint64_t), 0) != cudaSuccess) {
+    cudaGetLastError();
+    return fail(MOE_ERR_OOM, "pinned prefill staging could not be allocated");
+  }
+  return MOE_OK;
+}
+
+static moe_status prefill_tables(moe_cache* c, int n_steps) {
+  auto& pf = c->pf;
+  if (!pf.zero) {
+    CU_TRY(cudaMalloc(&pf.zero, sizeof(int32_t)));
+    CU_TRY(cudaMemset(pf.zero, 0, sizeof(int32_t)));
+  }
+  if (n_steps <= pf.tab_steps) return MOE_OK;
+  if (pf.tab) cudaFree(pf.tab);
+  pf.tab = nullptr;
+  pf.tab_steps = 0;
+  CU_TRY(cudaMalloc(&pf.tab, sizeof(int32_t) * (size_t)n_steps * c->d.E));
+  pf.tab_steps = n_steps;
+  return MOE_OK;
+}
+
 static moe_status prefill_scratch(moe_cache* c, int T) {
   auto& pf = c->pf;
   if (T <= pf.T_cap) return MOE_OK;
@@ -1188,8 +1231,9 @@ static moe_status prefill_scratch(moe_cache* c, int T) {
   return MOE_OK;
 }
 
-extern "C" moe_status moe_prefill_stream(moe_cache_t c, int32_t layer_begin, int32_t layer_end, const void* x,
-                                         const float* logits, int32_t T, void* y, void* stream) {
+extern "C" moe_status moe_prefill_stream_ex(moe_cache_t c, int32_t layer_begin, int32_t layer_end, const void* x,
+                                            const float* logits, int32_t T, void* y, void* stream,
+                                            const moe_prefill_aux* aux) {
   g_err.clear();
   if (!c) return fail(MOE_ERR_INVALID_ARG, "cache is NULL");
   const moe_model_desc& d = c->d;
@@ -1203,28 +1247,111 @@ extern "C" moe_status moe_prefill_stream(moe_cache_t c, int32_t layer_begin, int
   if (c->C < 2 * E)
     return fail(MOE_ERR_CAPACITY, "prefill needs two full-layer buffers (%lld slots), the cache has %lld",
                 (long long)(2 * E), (long long)c->C);
+  const int Tc = std::min<int>(T, kPrefillChunk), n_chunks = (T + kPrefillChunk - 1) / kPrefillChunk;
+  if (aux && n_chunks > 1 && (aux->perm || aux->offsets || aux->slots))
+    return fail(MOE_ERR_INVALID_ARG, "aux perm, offsets and slots need T <= %d", kPrefillChunk);
   cudaStream_t s = (cudaStream_t)stream;
   if (*(volatile int*)c->h_err != 0) return recover_after_timeout(c, s);
-  if (moe_status st = prefill_scratch(c, T)) return st;
+  if (moe_status st = prefill_scratch(c, Tc)) return st;
   auto& pf = c->pf;
   if (moe_status e = drain_inflight(c, 0)) return e;
   if (moe_status e = follow_stream(c, s)) return e;
 
   const int H = d.H, I = d.I, k = d.k, sh = d.has_shared;
-  const int Tk = T * k, n_pairs = Tk + (sh ? T : 0);
-  const int64_t S = c->S;
-  const int64_t buf0 = c->C - 2 * E;  // buffers: slots [C-2E, C-E) and [C-E, C)
+  const int n_layers = layer_end - layer_begin, n_steps = n_chunks * n_layers;
+  const int64_t S = c->S, C = c->C, LE = (int64_t)d.L * E;
+  const int64_t buf0 = C - 2 * E;  // buffers: slots [C-2E, C-E) and [C-E, C)
   uint8_t* slots = (uint8_t*)c->slots.base;
-  const CacheDev st{c->d_map, c->d_owner, c->d_stamp, c->d_g};
 
-  // the buffer slots stop holding decode experts
-  CU_TRY(prefill_evict_range(st, buf0, c->C, c->d_oldest_n, s));
+  // ---- the cache's bookkeeping for the whole call, on the host: the state
+  // after every earlier call of this cache, the buffers carved out, then per
+  // step (chunk, layer) where each expert is read from and which experts
+  // stream (the rule of the FreeToken write-up's full-layer double buffering:
+  // resident experts are read in place, the rest stream into their buffer
+  // slot, and the buffer contents stay cached afterwards to seed decode)
+  CU_TRY(cudaStreamSynchronize(s));
+  CU_TRY(cudaStreamSynchronize(c->copy));
+  if (moe_status e = prefill_staging(c)) return e;
+  int32_t* owner = pf.h_owner;
+  uint64_t* stamp = pf.h_stamp;
+  int32_t* map = pf.h_map;
+  CU_TRY(cudaMemcpy(owner, c->d_owner, sizeof(int32_t) * C, cudaMemcpyDeviceToHost));
+  CU_TRY(cudaMemcpy(stamp, c->d_stamp, sizeof(uint64_t) * C, cudaMemcpyDeviceToHost));
+  CU_TRY(cudaMemcpy(map, c->d_map, sizeof(int32_t) * LE, cudaMemcpyDeviceToHost));
+  CU_TRY(cudaMemcpy(pf.h_g, c->d_g, sizeof(uint64_t), cudaMemcpyDeviceToHost));
+  for (int64_t sl = buf0; sl < C; ++sl) {
+    const int32_t key = owner[sl];
+    if (key < 0) continue;
+    if (c->tracing) {
+      moe_event ev{};
+      ev.call = c->call_index;
+      ev.layer = key / (int32_t)E;
+      ev.expert = key % (int32_t)E;
+      ev.kind = MOE_EV_PREFILL_EVICT;
+      ev.slot = (int32_t)sl;
+      ev.evicted_key = key;
+      c->trace.push_back(ev);
+    }
+    map[key] = -1;
+    owner[sl] = -1;
+    stamp[sl] = 0;
+  }
+  std::vector<int32_t> tab((size_t)n_steps * E);
+  std::vector<std::vector<std::pair<int, int>>> runs(n_steps);  // streamed expert ranges [e0, e1)
+  std::vector<char> wait_prev(n_steps, 0);
+  int64_t streamed = 0;
+  uint64_t g = *pf.h_g;
+  for (int i = 0; i < n_steps; ++i) {
+    const int l = layer_begin + i % n_layers, b = i & 1;
+    int run0 = -1;
+    for (int e = 0; e < (int)E; ++e) {
+      const int32_t key = (int32_t)(l * E + e);
+      int64_t sl = map[key];
+      const bool stream_it = sl < 0;
+      if (stream_it) {
+        sl = buf0 + b * E + e;
+        if (owner[sl] >= 0) map[owner[sl]] = -1;
+        owner[sl] = key;
+        map[key] = (int32_t)sl;
+        ++streamed;
+        if (run0 < 0) run0 = e;
+      } else if (run0 >= 0) {
+        runs[i].push_back({run0, e});
+        run0 = -1;
+      }
+      stamp[sl] = g + (uint64_t)e;
+      tab[(size_t)i * E + e] = (int32_t)sl;
+    }
+    if (run0 >= 0) runs[i].push_back({run0, (int)E});
+    g += (uint64_t)E;
+    // the copy of step i overwrites buffer slots that step i-1 may still read
+    if (i > 0)
+      for (auto [e0, e1] : runs[i])
+        for (int e = 0; e < (int)E && !wait_prev[i]; ++e) {
+          const int32_t r = tab[(size_t)(i - 1) * E + e];
+          if (r >= buf0 + b * E + e0 && r < buf0 + b * E + e1) wait_prev[i] = 1;
+        }
+  }
+  *pf.h_g = g;
+  if (moe_status e2 = prefill_tables(c, n_steps)) return e2;
+  CU_TRY(cudaMemcpyAsync(pf.tab, tab.data(), sizeof(int32_t) * tab.size(), cudaMemcpyHostToDevice, s));
+
   CU_TRY(cudaEventRecord(pf.start, s));
   CU_TRY(cudaStreamWaitEvent(c->copy, pf.start, 0));
-
+  const int np_c = Tc * k + (sh ? Tc : 0);
   CUtensorMap map_xp, map_hp;
-  if (moe_status e = map_rows(&map_xp, pf.xp, n_pairs, H)) return e;
-  if (moe_status e = map_rows(&map_hp, pf.hp, n_pairs, I)) return e;
+  if (moe_status e = map_rows(&map_xp, pf.xp, np_c, H)) return e;
+  if (moe_status e = map_rows(&map_hp, pf.hp, np_c, I)) return e;
+  // weight maps over the whole slot pool (group e reads record tab[e]) and
+  // over the shared expert's record of each layer
+  Fp4Maps pool_fp4{}, sh_fp4{};
+  CUtensorMap bgu{}, bdn{}, bsgu{}, bsdn{};
+  if (d.wdtype == MOE_FP4) {
+    if (moe_status e = map_fp4_layer(&pool_fp4, slots, (int)C, H, I, S)) return e;
+  } else {
+    if (moe_status e = map_weights(&bgu, slots, (int)C, 2 * I, H, S)) return e;
+    if (moe_status e = map_weights(&bdn, slots + (int64_t)4 * H * I, (int)C, H, I, S)) return e;
+  }
   auto timed = [&](cudaStream_t on, int kind, double flop) -> std::pair<cudaEvent_t, cudaEvent_t> {
     if (!c->profiling) return {nullptr, nullptr};
     cudaEvent_t a = take_event(c), b = take_event(c);
@@ -1236,65 +1363,94 @@ extern "C" moe_status moe_prefill_stream(moe_cache_t c, int32_t layer_begin, int
     if (ev.second) cudaEventRecord(ev.second, on);
   };
   const auto whole = timed(s, 0, 0.0);
-  const double gemm_flop = 2.0 * n_pairs * (2.0 * I * H) + 2.0 * n_pairs * ((double)H * I);
 
-  for (int li = 0; li < layer_end - layer_begin; ++li) {
-    const int l = layer_begin + li, b = li & 1;
-    uint8_t* buf = slots + (buf0 + b * E) * S;
-    // stream layer l's experts into buffer b once layer l-2 released it
-    if (li >= 2) CU_TRY(cudaStreamWaitEvent(c->copy, pf.consumed[b], 0));
+  for (int i = 0; i < n_steps; ++i) {
+    const int li = i % n_layers, ch = i / n_layers, l = layer_begin + li, b = i & 1;
+    const int t0 = ch * kPrefillChunk, Tn = std::min(Tc, T - t0);
+    const int Tk = Tn * k, n_pairs = Tk + (sh ? Tn : 0);
+    // stream the layer's missing experts into buffer b once the computes that
+    // read those slots have finished
+    if (i >= 2) CU_TRY(cudaStreamWaitEvent(c->copy, pf.consumed[b], 0));
+    if (wait_prev[i]) CU_TRY(cudaStreamWaitEvent(c->copy, pf.consumed[b ^ 1], 0));
     const auto cp = timed(c->copy, 1, 0.0);
-    CU_TRY(cudaMemcpyAsync(buf, c->host_pool + (int64_t)l * E * S, E * S, cudaMemcpyHostToDevice, c->copy));
+    for (auto [e0, e1] : runs[i])
+      CU_TRY(cudaMemcpyAsync(slots + (buf0 + b * E + e0) * S, c->host_pool + ((int64_t)l * E + e0) * S,
+                             (int64_t)(e1 - e0) * S, cudaMemcpyHostToDevice, c->copy));
     done(cp, c->copy);
     CU_TRY(cudaEventRecord(pf.loaded[b], c->copy));
 
     // routing, grouping and gather need no weights: they run while the copy lands
-    const float* lg = logits + (int64_t)li * T * E;
-    const uint8_t* xl = (const uint8_t*)x + (int64_t)li * T * H * 2;
-    uint8_t* yl = (uint8_t*)y + (int64_t)li * T * H * 2;
-    CU_TRY(prefill_route(lg, T, (int)E, k, pf.ids, pf.w, s));
-    CU_TRY(prefill_group(pf.ids, T, k, (int)E, sh, pf.cnt, pf.base, pf.offsets, pf.pos, pf.perm, s));
-    CU_TRY(prefill_gather(xl, T, k, H, n_pairs, pf.perm, pf.xp, d.wdtype == MOE_FP4, s));  // FP4: f16 rows
+    const float* lg = logits + ((int64_t)li * T + t0) * E;
+    const uint8_t* xl = (const uint8_t*)x + ((int64_t)li * T + t0) * H * 2;
+    uint8_t* yl = (uint8_t*)y + ((int64_t)li * T + t0) * H * 2;
+    CU_TRY(prefill_route(lg, Tn, (int)E, k, pf.ids, pf.w, s));
+    CU_TRY(prefill_group(pf.ids, Tn, k, (int)E, sh, pf.cnt, pf.base, pf.offsets, pf.pos, pf.perm, s));
+    CU_TRY(prefill_gather(xl, Tn, k, H, n_pairs, pf.perm, pf.xp, d.wdtype == MOE_FP4, s));  // FP4: f16 rows
+    const int32_t* tab_i = pf.tab + (size_t)i * E;
+    if (aux) {
+      const int64_t at = ((int64_t)li * T + t0) * k;
+      if (aux->ids) CU_TRY(cudaMemcpyAsync(aux->ids + at, pf.ids, sizeof(int32_t) * Tk, cudaMemcpyDeviceToDevice, s));
+      if (aux->weights)
+        CU_TRY(cudaMemcpyAsync(aux->weights + at, pf.w, sizeof(float) * Tk, cudaMemcpyDeviceToDevice, s));
+      if (aux->perm)
+        CU_TRY(cudaMemcpyAsync(aux->perm + (int64_t)li * Tk, pf.perm, sizeof(int32_t) * Tk, cudaMemcpyDeviceToDevice,
+                               s));
+      if (aux->offsets)
+        CU_TRY(cudaMemcpyAsync(aux->offsets + (int64_t)li * (E + 1), pf.offsets, sizeof(int32_t) * (E + 1),
+                               cudaMemcpyDeviceToDevice, s));
+      if (aux->slots)
+        CU_TRY(cudaMemcpyAsync(aux->slots + (int64_t)li * E, tab_i, sizeof(int32_t) * E, cudaMemcpyDeviceToDevice,
+                               s));
+    }
     CU_TRY(cudaStreamWaitEvent(s, pf.loaded[b], 0));
     const auto comp = timed(s, 2, 0.0);
     const uint8_t* srec = sh ? c->shared_dev + (int64_t)l * S : nullptr;
+    const double gemm_flop = 2.0 * n_pairs * (2.0 * I * H) + 2.0 * n_pairs * ((double)H * I);
     const auto gm = timed(s, 3, gemm_flop);
-    if (d.wdtype == MOE_FP4) {  // the GEMMs read the FP4 codes and scales in the buffer
-      Fp4Maps lm, shm;
-      if (moe_status e = map_fp4_layer(&lm, buf, (int)E, H, I, S)) return e;
+    if (d.wdtype == MOE_FP4) {  // the GEMMs read the FP4 codes and scales where each expert sits
       if (sh)
-        if (moe_status e = map_fp4_layer(&shm, srec, 1, H, I, S)) return e;
-      CU_TRY(prefill_gemm_gate_up_fp4(map_xp, lm.gu_c, lm.gu_s, pf.offsets, (int)E, n_pairs, H, I, pf.hp, c->d_err,
-                                      s));
+        if (moe_status e = map_fp4_layer(&sh_fp4, srec, 1, H, I, S)) return e;
+      CU_TRY(prefill_gemm_gate_up_fp4(map_xp, pool_fp4.gu_c, pool_fp4.gu_s, pf.offsets, tab_i, (int)E, n_pairs, H, I,
+                                      pf.hp, c->d_err, s));
       if (sh)
-        CU_TRY(prefill_gemm_gate_up_fp4(map_xp, shm.gu_c, shm.gu_s, pf.offsets + E, 1, n_pairs, H, I, pf.hp,
-                                        c->d_err, s));
-      CU_TRY(prefill_gemm_down_fp4(map_hp, lm.dn_c, lm.dn_s, pf.offsets, (int)E, n_pairs, H, I, pf.op, c->d_err, s));
+        CU_TRY(prefill_gemm_gate_up_fp4(map_xp, sh_fp4.gu_c, sh_fp4.gu_s, pf.offsets + E, pf.zero, 1, n_pairs, H, I,
+                                        pf.hp, c->d_err, s));
+      CU_TRY(prefill_gemm_down_fp4(map_hp, pool_fp4.dn_c, pool_fp4.dn_s, pf.offsets, tab_i, (int)E, n_pairs, H, I,
+                                   pf.op, c->d_err, s));
       if (sh)
-        CU_TRY(prefill_gemm_down_fp4(map_hp, shm.dn_c, shm.dn_s, pf.offsets + E, 1, n_pairs, H, I, pf.op, c->d_err,
-                                     s));
+        CU_TRY(prefill_gemm_down_fp4(map_hp, sh_fp4.dn_c, sh_fp4.dn_s, pf.offsets + E, pf.zero, 1, n_pairs, H, I,
+                                     pf.op, c->d_err, s));
     } else {
-      CUtensorMap bgu, bdn, bsgu, bsdn;
-      if (moe_status e = map_weights(&bgu, buf, (int)E, 2 * I, H, S)) return e;
-      if (moe_status e = map_weights(&bdn, buf + (int64_t)4 * H * I, (int)E, H, I, S)) return e;
       if (sh) {
         if (moe_status e = map_weights(&bsgu, srec, 1, 2 * I, H, S)) return e;
         if (moe_status e = map_weights(&bsdn, srec + (int64_t)4 * H * I, 1, H, I, S)) return e;
       }
-      CU_TRY(prefill_gemm_gate_up(map_xp, bgu, pf.offsets, (int)E, n_pairs, H, I, pf.hp, c->d_err, s));
-      if (sh) CU_TRY(prefill_gemm_gate_up(map_xp, bsgu, pf.offsets + E, 1, n_pairs, H, I, pf.hp, c->d_err, s));
-      CU_TRY(prefill_gemm_down(map_hp, bdn, pf.offsets, (int)E, n_pairs, H, I, pf.op, c->d_err, s));
-      if (sh) CU_TRY(prefill_gemm_down(map_hp, bsdn, pf.offsets + E, 1, n_pairs, H, I, pf.op, c->d_err, s));
+      CU_TRY(prefill_gemm_gate_up(map_xp, bgu, pf.offsets, tab_i, (int)E, n_pairs, H, I, pf.hp, c->d_err, s));
+      if (sh)
+        CU_TRY(prefill_gemm_gate_up(map_xp, bsgu, pf.offsets + E, pf.zero, 1, n_pairs, H, I, pf.hp, c->d_err, s));
+      CU_TRY(prefill_gemm_down(map_hp, bdn, pf.offsets, tab_i, (int)E, n_pairs, H, I, pf.op, c->d_err, s));
+      if (sh) CU_TRY(prefill_gemm_down(map_hp, bsdn, pf.offsets + E, pf.zero, 1, n_pairs, H, I, pf.op, c->d_err, s));
     }
     done(gm, s);
     CU_TRY(cudaEventRecord(pf.consumed[b], s));  // buffer b may be refilled
-    CU_TRY(prefill_combine(pf.op, pf.pos, pf.w, T, k, H, sh, yl, s));
+    CU_TRY(prefill_combine(pf.op, pf.pos, pf.w, Tn, k, H, sh, yl, s));
     done(comp, s);
   }
   done(whole, s);
-  // later calls must not start before the copies finished with the buffers
-  CU_TRY(cudaStreamWaitEvent(s, pf.loaded[(layer_end - layer_begin - 1) & 1], 0));
-  c->st.prefill_layers += layer_end - layer_begin;
-  c->st.prefill_tokens += (int64_t)T * (layer_end - layer_begin);
+  // the cache after prefill: buffer contents become ordinary entries
+  CU_TRY(cudaMemcpyAsync(c->d_owner, owner, sizeof(int32_t) * C, cudaMemcpyHostToDevice, s));
+  CU_TRY(cudaMemcpyAsync(c->d_stamp, stamp, sizeof(uint64_t) * C, cudaMemcpyHostToDevice, s));
+  CU_TRY(cudaMemcpyAsync(c->d_map, map, sizeof(int32_t) * LE, cudaMemcpyHostToDevice, s));
+  CU_TRY(cudaMemcpyAsync(c->d_g, pf.h_g, sizeof(uint64_t), cudaMemcpyHostToDevice, s));
+  CU_TRY(cudaMemsetAsync(c->d_oldest_n, 0xFF, sizeof(int), s));
+  c->st.prefill_layers += n_layers;
+  c->st.prefill_tokens += (int64_t)T * n_layers;
+  c->st.prefill_records_streamed += streamed;
+  c->st.prefill_records_in_place += (int64_t)n_steps * E - streamed;
   return MOE_OK;
+}
+
+extern "C" moe_status moe_prefill_stream(moe_cache_t c, int32_t layer_begin, int32_t layer_end, const void* x,
+                                         const float* logits, int32_t T, void* y, void* stream) {
+  return moe_prefill_stream_ex(c, layer_begin, layer_end, x, logits, T, y, stream, nullptr);
 }

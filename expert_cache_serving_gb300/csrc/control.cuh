@@ -39,6 +39,7 @@ struct CtrlSmem {
   float w[kMaxPairs];
   int prank[kMaxPairs];
   int perm[kMaxPairs];  // flat pair t*k+j grouped by expert (stable)
+  int maprow[kMaxE];    // residency table row of this call's layer
   unsigned bits[kMaxE / 32];
   int wpre[kMaxE / 32];
   int U[kMaxU];
@@ -259,8 +260,15 @@ __device__ __forceinline__ void publish_summary(const LayerParams& p) {
 static __device__ int route_lookup(const LayerParams& p, CtrlSmem& cs, bool write_aux) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarp = blockDim.x >> 5;
   const int E = p.E, k = p.k, B = p.B, npairs = B * k;
+  // the layer's residency row is loaded while the router's logits load (the
+  // two latencies overlap); stored to shared memory after the router
+  int mrow[kMaxE / kThreads];
+#pragma unroll
+  for (int j = 0; j < kMaxE / kThreads; ++j) {
+    const int e = tid + j * kThreads;
+    mrow[j] = e < E ? p.st.map[p.layer * E + e] : -1;
+  }
   for (int i = tid; i < kMaxE / 32; i += blockDim.x) cs.bits[i] = 0u;
-  __syncthreads();
 
   // ---- router: one warp per token ------------------------------------------------
   const int nq = (E + 31) >> 5;
@@ -275,6 +283,11 @@ static __device__ int route_lookup(const LayerParams& p, CtrlSmem& cs, bool writ
     else if (nq <= 8) route_token<8>(lg, E, k, lane, aux, ids, w);
     else if (nq <= 16) route_token<16>(lg, E, k, lane, aux, ids, w);
     else route_token<32>(lg, E, k, lane, aux, ids, w);
+  }
+#pragma unroll
+  for (int j = 0; j < kMaxE / kThreads; ++j) {
+    const int e = tid + j * kThreads;
+    if (e < E) cs.maprow[e] = mrow[j];
   }
   __syncthreads();
 
@@ -311,7 +324,7 @@ static __device__ int route_lookup(const LayerParams& p, CtrlSmem& cs, bool writ
   // expert, high half) and the miss ranks (low half); both totals are <= 256
   int is_miss = 0;
   if (tid < n_u) {
-    const int s = p.st.map[p.layer * E + cs.U[tid]];
+    const int s = cs.maprow[cs.U[tid]];
     cs.slot[tid] = s;
     is_miss = s < 0;
     cs.fill[tid] = is_miss;

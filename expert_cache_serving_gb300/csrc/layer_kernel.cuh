@@ -444,6 +444,7 @@ __global__ void __launch_bounds__(kThreads, 1) layer_kernel(LayerParams p) {
   __shared__ CtrlSmem cs;
   __shared__ ItemTable tb;
   __shared__ __align__(8) uint64_t s_stage;
+  __shared__ __align__(8) uint64_t s_xin;
   __shared__ int s_flag;
   const int H = p.H, B = p.B, k = p.k;
   const int G = gridDim.x;
@@ -463,17 +464,29 @@ __global__ void __launch_bounds__(kThreads, 1) layer_kernel(LayerParams p) {
     p.cst->part[blockIdx.x] = -1;
     if (ctrl) p.cst->gu_stop = 0;  // before the first grid barrier, which every later writer passes
   }
-  {
-    const int nvec = (int)((size_t)B * H * sizeof(XT) / 16);
+  // activations into shared memory by one bulk copy (waited for before phase 1),
+  // or by plain loads when the caller's pointer is not 16-byte aligned
+  const uint32_t xbytes = (uint32_t)((size_t)B * H * sizeof(XT));
+  const bool x_bulk = ((uintptr_t)p.x & 15) == 0;
+  if (x_bulk && threadIdx.x == 0) {
+    mbar_init(&s_xin, 1);
+    fence_mbar_init();
+    mbar_expect_tx(&s_xin, xbytes);
+    bulk_g2s(xs, p.x, xbytes, &s_xin);
+  }
+  if (!x_bulk) {
     const uint4* src = reinterpret_cast<const uint4*>(p.x);
     uint4* dst = reinterpret_cast<uint4*>(xs);
-    for (int i = threadIdx.x; i < nvec; i += blockDim.x) dst[i] = src[i];
+    for (int i = threadIdx.x; i < (int)(xbytes / 16); i += blockDim.x) dst[i] = src[i];
   }
 
   // ---- 0. routing and lookup (every CTA); victims, plan, summary (control CTA)
   int err = route_lookup(p, cs, ctrl);
   if (ctrl) err = err == MOE_OK ? choose_victims(p, cs) : (publish_error(p, cs, err), err);
-  if (err != MOE_OK) return;  // capacity: every CTA; inconsistent victim list: the control CTA
+  if (err != MOE_OK) {  // capacity: every CTA; inconsistent victim list: the control CTA
+    if (x_bulk) mbar_wait(&s_xin, 0);  // no bulk copy outlives its CTA
+    return;
+  }
   if (ctrl && p.tl) p.tl[10] = globaltimer_ns();
   if (rec) p.tl[1] = globaltimer_ns();
 
@@ -501,6 +514,13 @@ __global__ void __launch_bounds__(kThreads, 1) layer_kernel(LayerParams p) {
       prefetch_l2(v.down + (int64_t)n0 * rb, (uint32_t)(nrows * rb));
       if (WD == MOE_FP4) prefetch_l2(v.down_sc + (int64_t)n0 * sb, (uint32_t)(nrows * sb));
     }
+  }
+  if (x_bulk && !mbar_wait(&s_xin, 0)) {
+    if (threadIdx.x == 0) atomicExch(p.err, MOE_ERR_TIMEOUT);
+    mbar_wait(&s_xin, 0);
+    if (n_stage > 0) mbar_wait(&s_stage, 0);
+    poison_rows<WD>(p, n0, nrows);
+    return;
   }
   if (!ctrl) phase1<WD, MAXT, false>(p, tb, 0, n_res, 1, G - 1, xs);
   if (rec) p.tl[2] = globaltimer_ns();

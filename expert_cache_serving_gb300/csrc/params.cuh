@@ -71,18 +71,20 @@ cudaError_t prefill_group(const int32_t* ids, int T, int k, int E, int has_share
                           int32_t* offsets, int32_t* pos, int32_t* perm, cudaStream_t s);
 cudaError_t prefill_gather(const void* x, int T, int k, int H, int n_pairs, const int32_t* perm, void* xp,
                            int to_f16, cudaStream_t s);
-cudaError_t prefill_gemm_gate_up(const CUtensorMap& a, const CUtensorMap& b, const int32_t* offsets, int n_groups,
-                                 int n_rows, int H, int I, void* hp, int* err, cudaStream_t s);
-cudaError_t prefill_gemm_down(const CUtensorMap& a, const CUtensorMap& b, const int32_t* offsets, int n_groups,
-                              int n_rows, int H, int I, float* op, int* err, cudaStream_t s);
+// grouped GEMMs: group g's weights are record slot_of[g] of the weight maps
+cudaError_t prefill_gemm_gate_up(const CUtensorMap& a, const CUtensorMap& b, const int32_t* offsets,
+                                 const int32_t* slot_of, int n_groups, int n_rows, int H, int I, void* hp, int* err,
+                                 cudaStream_t s);
+cudaError_t prefill_gemm_down(const CUtensorMap& a, const CUtensorMap& b, const int32_t* offsets,
+                              const int32_t* slot_of, int n_groups, int n_rows, int H, int I, float* op, int* err,
+                              cudaStream_t s);
 cudaError_t prefill_gemm_gate_up_fp4(const CUtensorMap& a, const CUtensorMap& codes, const CUtensorMap& scales,
-                                     const int32_t* offsets, int n_groups, int n_rows, int H, int I, void* hp,
-                                     int* err, cudaStream_t s);
+                                     const int32_t* offsets, const int32_t* slot_of, int n_groups, int n_rows, int H,
+                                     int I, void* hp, int* err, cudaStream_t s);
 cudaError_t prefill_gemm_down_fp4(const CUtensorMap& a, const CUtensorMap& codes, const CUtensorMap& scales,
-                                  const int32_t* offsets, int n_groups, int n_rows, int H, int I, float* op, int* err,
-                                  cudaStream_t s);
+                                  const int32_t* offsets, const int32_t* slot_of, int n_groups, int n_rows, int H,
+                                  int I, float* op, int* err, cudaStream_t s);
 cudaError_t prefill_combine(const float* op, const int32_t* pos, const float* w, int T, int k, int H, int has_shared,
                             void* y, cudaStream_t s);
-cudaError_t prefill_evict_range(const CacheDev& st, int64_t s0, int64_t s1, int* oldest_n, cudaStream_t s);
 
 }  // namespace moe

@@ -168,31 +168,34 @@ struct BRowDown {
 
 __global__ void __launch_bounds__(tc::kThreads, 1)
     gemm_gate_up_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
-                        const int32_t* offsets, int n_groups, int H, int I, __nv_bfloat16* hp, int* err) {
-  tc::grouped_gemm_cta(&map_a, &map_b, offsets, n_groups, I / 128, H, tc::EpiSwiGLU<>{hp, I}, BRowGateUp{I}, err);
+                        const int32_t* offsets, const int32_t* slot_of, int n_groups, int H, int I, __nv_bfloat16* hp,
+                        int* err) {
+  tc::grouped_gemm_cta(&map_a, &map_b, offsets, slot_of, n_groups, I / 128, H, tc::EpiSwiGLU<>{hp, I}, BRowGateUp{I},
+                       err);
 }
 
 __global__ void __launch_bounds__(tc::kThreads, 1)
     gemm_down_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
-                     const int32_t* offsets, int n_groups, int H, int I, float* op, int* err) {
-  tc::grouped_gemm_cta(&map_a, &map_b, offsets, n_groups, H / 256, I, tc::EpiStoreF32{op, H}, BRowDown{}, err);
+                     const int32_t* offsets, const int32_t* slot_of, int n_groups, int H, int I, float* op, int* err) {
+  tc::grouped_gemm_cta(&map_a, &map_b, offsets, slot_of, n_groups, H / 256, I, tc::EpiStoreF32{op, H}, BRowDown{},
+                       err);
 }
 
 // FP4 weights read directly (codes + scales maps over the layer buffer)
 __global__ void __launch_bounds__(tc::fp4::kThreads, 1)
     gemm_gate_up_fp4_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_c,
-                            const __grid_constant__ CUtensorMap map_s, const int32_t* offsets, int n_groups, int H,
-                            int I, __half* hp, int* err) {
-  tc::grouped_gemm_fp4_cta(&map_a, &map_c, &map_s, offsets, n_groups, I / 128, H, tc::EpiSwiGLU<__half>{hp, I},
-                           BRowGateUp{I}, err);
+                            const __grid_constant__ CUtensorMap map_s, const int32_t* offsets,
+                            const int32_t* slot_of, int n_groups, int H, int I, __half* hp, int* err) {
+  tc::grouped_gemm_fp4_cta(&map_a, &map_c, &map_s, offsets, slot_of, n_groups, I / 128, H,
+                           tc::EpiSwiGLU<__half>{hp, I}, BRowGateUp{I}, err);
 }
 
 __global__ void __launch_bounds__(tc::fp4::kThreads, 1)
     gemm_down_fp4_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_c,
-                         const __grid_constant__ CUtensorMap map_s, const int32_t* offsets, int n_groups, int H, int I,
-                         float* op, int* err) {
-  tc::grouped_gemm_fp4_cta(&map_a, &map_c, &map_s, offsets, n_groups, H / 256, I, tc::EpiStoreF32{op, H}, BRowDown{},
-                           err);
+                         const __grid_constant__ CUtensorMap map_s, const int32_t* offsets, const int32_t* slot_of,
+                         int n_groups, int H, int I, float* op, int* err) {
+  tc::grouped_gemm_fp4_cta(&map_a, &map_c, &map_s, offsets, slot_of, n_groups, H / 256, I, tc::EpiStoreF32{op, H},
+                           BRowDown{}, err);
 }
 
 // ---- 6. combine ------------------------------------------------------------------------------
@@ -220,17 +223,6 @@ __global__ void combine_kernel(const float* __restrict__ op, const int32_t* __re
     uint2 out = make_uint2(*reinterpret_cast<uint32_t*>(&a), *reinterpret_cast<uint32_t*>(&b));
     reinterpret_cast<uint2*>(y + (int64_t)t * H)[v] = out;
   }
-}
-
-// Empty the slots [s0, s1) (the prefill buffers): their experts are no longer resident.
-__global__ void evict_range_kernel(CacheDev st, int64_t s0, int64_t s1, int* oldest_n) {
-  for (int64_t s = s0 + blockIdx.x * blockDim.x + threadIdx.x; s < s1; s += (int64_t)gridDim.x * blockDim.x) {
-    const int own = st.owner[s];
-    if (own >= 0) st.map[own] = -1;
-    st.owner[s] = -1;
-    st.stamp[s] = 0;
-  }
-  if (blockIdx.x == 0 && threadIdx.x == 0) *oldest_n = -1;
 }
 
 }  // namespace pf
@@ -287,19 +279,21 @@ static cudaError_t gemm_attr() {
 // grid: enough CTAs for every tile of n_rows rows over n_groups groups
 static int gemm_grid(int n_rows, int n_groups, int nblocks_n) { return (n_rows / tc::kBM + n_groups) * nblocks_n; }
 
-cudaError_t prefill_gemm_gate_up(const CUtensorMap& a, const CUtensorMap& b, const int32_t* offsets, int n_groups,
-                                 int n_rows, int H, int I, void* hp, int* err, cudaStream_t s) {
+cudaError_t prefill_gemm_gate_up(const CUtensorMap& a, const CUtensorMap& b, const int32_t* offsets,
+                                 const int32_t* slot_of, int n_groups, int n_rows, int H, int I, void* hp, int* err,
+                                 cudaStream_t s) {
   if (cudaError_t e = gemm_attr()) return e;
   pf::gemm_gate_up_kernel<<<gemm_grid(n_rows, n_groups, I / 128), tc::kThreads, tc::kSmemBytes, s>>>(
-      a, b, offsets, n_groups, H, I, (__nv_bfloat16*)hp, err);
+      a, b, offsets, slot_of, n_groups, H, I, (__nv_bfloat16*)hp, err);
   return cudaGetLastError();
 }
 
-cudaError_t prefill_gemm_down(const CUtensorMap& a, const CUtensorMap& b, const int32_t* offsets, int n_groups,
-                              int n_rows, int H, int I, float* op, int* err, cudaStream_t s) {
+cudaError_t prefill_gemm_down(const CUtensorMap& a, const CUtensorMap& b, const int32_t* offsets,
+                              const int32_t* slot_of, int n_groups, int n_rows, int H, int I, float* op, int* err,
+                              cudaStream_t s) {
   if (cudaError_t e = gemm_attr()) return e;
   pf::gemm_down_kernel<<<gemm_grid(n_rows, n_groups, H / 256), tc::kThreads, tc::kSmemBytes, s>>>(
-      a, b, offsets, n_groups, H, I, op, err);
+      a, b, offsets, slot_of, n_groups, H, I, op, err);
   return cudaGetLastError();
 }
 
@@ -316,31 +310,26 @@ static cudaError_t gemm_fp4_attr() {
 }
 
 cudaError_t prefill_gemm_gate_up_fp4(const CUtensorMap& a, const CUtensorMap& codes, const CUtensorMap& scales,
-                                     const int32_t* offsets, int n_groups, int n_rows, int H, int I, void* hp,
-                                     int* err, cudaStream_t s) {
+                                     const int32_t* offsets, const int32_t* slot_of, int n_groups, int n_rows, int H,
+                                     int I, void* hp, int* err, cudaStream_t s) {
   if (cudaError_t e = gemm_fp4_attr()) return e;
   pf::gemm_gate_up_fp4_kernel<<<gemm_grid(n_rows, n_groups, I / 128), tc::fp4::kThreads, tc::fp4::kSmemBytes, s>>>(
-      a, codes, scales, offsets, n_groups, H, I, (__half*)hp, err);
+      a, codes, scales, offsets, slot_of, n_groups, H, I, (__half*)hp, err);
   return cudaGetLastError();
 }
 
 cudaError_t prefill_gemm_down_fp4(const CUtensorMap& a, const CUtensorMap& codes, const CUtensorMap& scales,
-                                  const int32_t* offsets, int n_groups, int n_rows, int H, int I, float* op, int* err,
-                                  cudaStream_t s) {
+                                  const int32_t* offsets, const int32_t* slot_of, int n_groups, int n_rows, int H,
+                                  int I, float* op, int* err, cudaStream_t s) {
   if (cudaError_t e = gemm_fp4_attr()) return e;
   pf::gemm_down_fp4_kernel<<<gemm_grid(n_rows, n_groups, H / 256), tc::fp4::kThreads, tc::fp4::kSmemBytes, s>>>(
-      a, codes, scales, offsets, n_groups, H, I, op, err);
+      a, codes, scales, offsets, slot_of, n_groups, H, I, op, err);
   return cudaGetLastError();
 }
 
 cudaError_t prefill_combine(const float* op, const int32_t* pos, const float* w, int T, int k, int H, int has_shared,
                             void* y, cudaStream_t s) {
   pf::combine_kernel<<<sms() * 8, 256, 0, s>>>(op, pos, w, T, k, H, has_shared, (__nv_bfloat16*)y);
-  return cudaGetLastError();
-}
-
-cudaError_t prefill_evict_range(const CacheDev& st, int64_t s0, int64_t s1, int* oldest_n, cudaStream_t s) {
-  pf::evict_range_kernel<<<64, 256, 0, s>>>(st, s0, s1, oldest_n);
   return cudaGetLastError();
 }
 

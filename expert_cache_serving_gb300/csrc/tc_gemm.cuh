@@ -1,5 +1,6 @@
 // Grouped bf16 GEMM on the 5th-generation tensor cores (tcgen05 + TMEM), fed
-// by TMA, for the prefill-size expert FFN.
+// by TMA, for the prefill-size expert FFN.  The weight maps cover a range of
+// records (the whole slot pool); group e's weights are record slot_of[e].
 //
 // FreeToken write-up, "전층 이중 버퍼링": in prefill a layer's routed tokens
 // cover almost every expert, so each expert's FFN is a dense contraction over
@@ -196,8 +197,8 @@ struct EpiStoreF32 {
 // A: 2D map over [rows][K]; B: 3D map over [E][Nrows][K].  b_row(nb, half)
 // gives the first weight row of each 128-row half of the 256-column block.
 template <typename Epi, typename BRow>
-__device__ void grouped_gemm_cta(const CUtensorMap* map_a, const CUtensorMap* map_b, const int32_t* offsets, int E,
-                                 int nblocks_n, int K, Epi epi, BRow b_row, int* err) {
+__device__ void grouped_gemm_cta(const CUtensorMap* map_a, const CUtensorMap* map_b, const int32_t* offsets,
+                                 const int32_t* slot_of, int E, int nblocks_n, int K, Epi epi, BRow b_row, int* err) {
   extern __shared__ __align__(1024) uint8_t tc_smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(tc_smem_raw) + 1023) & ~(uintptr_t)1023);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
@@ -230,7 +231,8 @@ __device__ void grouped_gemm_cta(const CUtensorMap* map_a, const CUtensorMap* ma
   const int ksteps = K / kBK;
 
   if (warp == 0 && lane == 0) {
-    // TMA producer
+    // TMA producer; the weights of group t.e sit in record slot_of[t.e]
+    const int rec = slot_of[t.e];
     for (int ks = 0; ks < ksteps; ++ks) {
       const int s = ks % kStages;
       if (ks >= kStages && !mbar_wait(&empty[s], ((ks / kStages) - 1) & 1)) { s_fail = 1; break; }
@@ -239,8 +241,8 @@ __device__ void grouped_gemm_cta(const CUtensorMap* map_a, const CUtensorMap* ma
       uint8_t* b_dst = a_dst + kAStage;
       mbar_expect_tx(&full[s], kStageBytes);
       tma_load_2d(a_dst, map_a, &full[s], ks * kBK, t.row0);
-      tma_load_3d(b_dst, map_b, &full[s], ks * kBK, b_row(t.nb, 0), t.e);
-      tma_load_3d(b_dst + kBStage / 2, map_b, &full[s], ks * kBK, b_row(t.nb, 1), t.e);
+      tma_load_3d(b_dst, map_b, &full[s], ks * kBK, b_row(t.nb, 0), rec);
+      tma_load_3d(b_dst + kBStage / 2, map_b, &full[s], ks * kBK, b_row(t.nb, 1), rec);
     }
   } else if (warp == 1 && lane == 0) {
     // MMA issuer
@@ -339,8 +341,8 @@ __device__ __forceinline__ uint32_t e4m3_to_f16x2_both(uint32_t scale_byte) {
 // bytes x 128 rows); scales: 3D u8 map over [E][Nrows][K/16] (box 16 x 128).
 template <typename Epi, typename BRow>
 __device__ void grouped_gemm_fp4_cta(const CUtensorMap* map_a, const CUtensorMap* map_codes,
-                                     const CUtensorMap* map_scales, const int32_t* offsets, int E, int nblocks_n, int K,
-                                     Epi epi, BRow b_row, int* err) {
+                                     const CUtensorMap* map_scales, const int32_t* offsets, const int32_t* slot_of,
+                                     int E, int nblocks_n, int K, Epi epi, BRow b_row, int* err) {
   constexpr int kRaw = fp4::kRaw, kBBufs = fp4::kBBufs, kConvWarps = fp4::kConvWarps;
   constexpr int kAStage = fp4::kAStage, kBStage = fp4::kBStage, kCodeStage = fp4::kCodeStage;
   constexpr int kScaleStage = fp4::kScaleStage, kRawBytes = fp4::kRawBytes;
@@ -385,6 +387,8 @@ __device__ void grouped_gemm_fp4_cta(const CUtensorMap* map_a, const CUtensorMap
 
   if (warp == 0 && lane == 0) {
     // TMA producer: A tile, the 256 weight rows' codes, their scale boxes
+    // (the weights of group t.e sit in record slot_of[t.e])
+    const int rec = slot_of[t.e];
     for (int ks = 0; ks < ksteps; ++ks) {
       const int s = ks % kRaw;
       if (ks >= kRaw && !mbar_wait(&empty[s], ((ks / kRaw) - 1) & 1)) { s_fail = 1; break; }
@@ -394,10 +398,10 @@ __device__ void grouped_gemm_fp4_cta(const CUtensorMap* map_a, const CUtensorMap
       uint8_t* scales = codes + kCodeStage;
       mbar_expect_tx(&full[s], fp4::kTxBytes);
       tma_load_2d(a, map_a, &full[s], ks * kBK, t.row0);
-      tma_load_3d(codes, map_codes, &full[s], ks * (kBK / 2), b_row(t.nb, 0), t.e);
-      tma_load_3d(codes + kCodeStage / 2, map_codes, &full[s], ks * (kBK / 2), b_row(t.nb, 1), t.e);
-      tma_load_3d(scales, map_scales, &full[s], (ks >> 2) * 16, b_row(t.nb, 0), t.e);
-      tma_load_3d(scales + kScaleStage / 2, map_scales, &full[s], (ks >> 2) * 16, b_row(t.nb, 1), t.e);
+      tma_load_3d(codes, map_codes, &full[s], ks * (kBK / 2), b_row(t.nb, 0), rec);
+      tma_load_3d(codes + kCodeStage / 2, map_codes, &full[s], ks * (kBK / 2), b_row(t.nb, 1), rec);
+      tma_load_3d(scales, map_scales, &full[s], (ks >> 2) * 16, b_row(t.nb, 0), rec);
+      tma_load_3d(scales + kScaleStage / 2, map_scales, &full[s], (ks >> 2) * 16, b_row(t.nb, 1), rec);
     }
   } else if (warp == 1 && lane == 0) {
     // MMA issuer: A from the raw stage, B from the converted buffer

@@ -15,7 +15,7 @@ _LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib", "li
 
 MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_OOM, MOE_ERR_CAPACITY, MOE_ERR_BUSY, MOE_ERR_CUDA, MOE_ERR_TIMEOUT = range(7)
 MOE_FP32, MOE_BF16, MOE_FP4 = 0, 1, 2
-MOE_EV_HIT, MOE_EV_MISS, MOE_EV_RESIZE_EVICT = 0, 1, 2
+MOE_EV_HIT, MOE_EV_MISS, MOE_EV_RESIZE_EVICT, MOE_EV_PREFILL_EVICT = 0, 1, 2, 3
 MOE_FILL_COPY, MOE_FILL_DEVICE = 0, 1
 STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_OOM", 3: "MOE_ERR_CAPACITY",
                 4: "MOE_ERR_BUSY", 5: "MOE_ERR_CUDA", 6: "MOE_ERR_TIMEOUT"}
@@ -40,7 +40,9 @@ class moe_stats(ctypes.Structure):
                 ("prefill_tokens", ctypes.c_int64), ("prefill_ms", ctypes.c_double),
                 ("prefill_copy_ms", ctypes.c_double), ("prefill_compute_ms", ctypes.c_double),
                 ("prefill_gemm_ms", ctypes.c_double), ("prefill_gemm_flop", ctypes.c_double),
-                ("deferred_calls", ctypes.c_int64), ("finish_launches", ctypes.c_int64)]
+                ("deferred_calls", ctypes.c_int64), ("finish_launches", ctypes.c_int64),
+                ("pdl_launches", ctypes.c_int64), ("prefill_records_streamed", ctypes.c_int64),
+                ("prefill_records_in_place", ctypes.c_int64)]
 
     def as_dict(self):
         return {name: getattr(self, name) for name, _ in self._fields_}
@@ -55,6 +57,11 @@ class moe_event(ctypes.Structure):
 class moe_layer_aux(ctypes.Structure):
     _fields_ = [("ids", ctypes.c_void_p), ("weights", ctypes.c_void_p), ("slots", ctypes.c_void_p),
                 ("perm", ctypes.c_void_p), ("offsets", ctypes.c_void_p), ("logits", ctypes.c_void_p)]
+
+
+class moe_prefill_aux(ctypes.Structure):
+    _fields_ = [("ids", ctypes.c_void_p), ("weights", ctypes.c_void_p), ("perm", ctypes.c_void_p),
+                ("offsets", ctypes.c_void_p), ("slots", ctypes.c_void_p)]
 
 
 class moe_phase_times(ctypes.Structure):
@@ -77,6 +84,7 @@ SIGNATURES = {
     "moe_layer_forward": (_I32, [_P, _I32, _P, _P, _P, _I32, _P, _P]),
     "moe_layer_forward_ex": (_I32, [_P, _I32, _P, _P, _P, _I32, _P, _P, ctypes.POINTER(moe_layer_aux)]),
     "moe_prefill_stream": (_I32, [_P, _I32, _I32, _P, _P, _I32, _P, _P]),
+    "moe_prefill_stream_ex": (_I32, [_P, _I32, _I32, _P, _P, _I32, _P, _P, ctypes.POINTER(moe_prefill_aux)]),
     "moe_cache_stats": (_I32, [_P, ctypes.POINTER(moe_stats)]),
     "moe_cache_sync": (_I32, [_P, _P]),
     "moe_cache_set_wait_limit_ns": (_I32, [_P, _I64, _I64]),
@@ -167,8 +175,14 @@ def moe_layer_forward(cache: int, layer: int, x, logits, router_w, B: int, y, st
                                     _stream(stream), ctypes.byref(a))
 
 
-def moe_prefill_stream(cache: int, layer_begin: int, layer_end: int, x, logits, T: int, y, stream=None) -> int:
-    return lib.moe_prefill_stream(cache, layer_begin, layer_end, _ptr(x), _ptr(logits), T, _ptr(y), _stream(stream))
+def moe_prefill_stream(cache: int, layer_begin: int, layer_end: int, x, logits, T: int, y, stream=None,
+                       aux=None) -> int:
+    if aux is None:
+        return lib.moe_prefill_stream(cache, layer_begin, layer_end, _ptr(x), _ptr(logits), T, _ptr(y),
+                                      _stream(stream))
+    a = moe_prefill_aux(*[_ptr(aux.get(f)) for f, _ in moe_prefill_aux._fields_])
+    return lib.moe_prefill_stream_ex(cache, layer_begin, layer_end, _ptr(x), _ptr(logits), T, _ptr(y),
+                                     _stream(stream), ctypes.byref(a))
 
 
 def moe_cache_stats(cache: int) -> dict:

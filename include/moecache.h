@@ -69,7 +69,7 @@ enum {
 enum { MOE_FP32 = 0, MOE_BF16 = 1, MOE_FP4 = 2 };
 
 /* event kinds in the cache trace */
-enum { MOE_EV_HIT = 0, MOE_EV_MISS = 1, MOE_EV_RESIZE_EVICT = 2 };
+enum { MOE_EV_HIT = 0, MOE_EV_MISS = 1, MOE_EV_RESIZE_EVICT = 2, MOE_EV_PREFILL_EVICT = 3 };
 
 typedef struct {
   int32_t L;          /* MoE layers */
@@ -112,6 +112,9 @@ typedef struct {
   double prefill_gemm_flop;  /* useful flops of those launches (2 * rows * N * K) */
   int64_t deferred_calls;    /* copy-fill calls finished by the completion kernel (fills landed late) */
   int64_t finish_launches;   /* completion-kernel launches (one per copy-fill call with misses) */
+  int64_t pdl_launches;      /* layer-kernel launches made as programmatic dependents of the previous launch */
+  int64_t prefill_records_streamed;  /* expert records moe_prefill_stream copied into its buffers */
+  int64_t prefill_records_in_place;  /* expert records it read where they were already resident */
 } moe_stats;
 
 typedef struct {
@@ -204,20 +207,42 @@ moe_status moe_layer_forward_ex(moe_cache_t cache, int32_t layer, const void* x,
                                 const moe_layer_aux* aux);
 
 /* Prefill of T tokens through layers [layer_begin, layer_end) with full-layer
- * double buffering: two buffers of E slots each are carved from the slot
- * pool; while layer l runs on one, all E records of layer l+1 stream into the
- * other on the copy stream.  x: device [n_layers][T][H] bf16 (each layer's
- * input), logits: device float32 [n_layers][T][E], y: device
- * [n_layers][T][H] bf16.  Only MOE_BF16 / MOE_FP4 models; prefill also
- * needs I % 128 == 0 and H % 256 == 0.  The expert GEMMs accumulate in
- * float32; their operands are bf16 for MOE_BF16 models and f16 for MOE_FP4
- * models (the activations convert exactly for |x| <= 65504, the FP4 weights
- * expand exactly, the SwiGLU intermediate is rounded to f16).  The slots of
- * the two buffers (the last 2*E slots) hold no decode expert afterwards.
+ * double buffering ("전층 이중 버퍼링" in the FreeToken write-up): two buffers
+ * of E slots each are carved from the slot pool (the last 2*E slots; their
+ * entries are evicted, logged as MOE_EV_PREFILL_EVICT in ascending slot
+ * order); while layer l runs on one, layer l+1's experts stream into the
+ * other on the copy stream.  An expert already resident elsewhere in the
+ * cache is read where it is, not streamed.  Every expert of a prefilled layer
+ * counts as used by it (stamps g + e per layer, in layer order), and the
+ * buffers' contents stay cached afterwards: what survives prefill seeds
+ * decode.  Prompts longer than 8192 tokens run as consecutive 8192-token
+ * chunks, each a full pass over the layers.
+ * x: device [n_layers][T][H] bf16 (each layer's input), logits: device float32
+ * [n_layers][T][E], y: device [n_layers][T][H] bf16.  Only MOE_BF16 / MOE_FP4
+ * models; prefill also needs I % 128 == 0 and H % 256 == 0.  The expert GEMMs
+ * accumulate in float32; their operands are bf16 for MOE_BF16 models and f16
+ * for MOE_FP4 models (the activations convert exactly for |x| <= 65504, the
+ * FP4 weights expand exactly, the SwiGLU intermediate is rounded to f16).
+ * The host waits once at the start for the cache's earlier work (it plans the
+ * copies from the residency table); the rest is asynchronous on `stream`.
  * Errors: MOE_ERR_CAPACITY if the pool has fewer than 2*E slots,
  * MOE_ERR_INVALID_ARG, MOE_ERR_OOM, MOE_ERR_CUDA. */
 moe_status moe_prefill_stream(moe_cache_t cache, int32_t layer_begin, int32_t layer_end, const void* x,
                               const float* logits, int32_t T, void* y, void* stream);
+
+/* Optional device outputs of moe_prefill_stream_ex; every field may be NULL.
+ * perm, offsets and slots need T <= 8192 (one chunk). */
+typedef struct {
+  int32_t* ids;      /* [n_layers][T][k] selected experts, descending logit, ties -> lower id */
+  float* weights;    /* [n_layers][T][k] routing weights */
+  int32_t* perm;     /* [n_layers][T*k] flat pairs t*k+j grouped by expert (stable) */
+  int32_t* offsets;  /* [n_layers][E+1] start of each expert's group in perm */
+  int32_t* slots;    /* [n_layers][E] cache slot each expert of the layer was read from */
+} moe_prefill_aux;
+
+/* moe_prefill_stream with optional inspection outputs (aux may be NULL). */
+moe_status moe_prefill_stream_ex(moe_cache_t cache, int32_t layer_begin, int32_t layer_end, const void* x,
+                                 const float* logits, int32_t T, void* y, void* stream, const moe_prefill_aux* aux);
 
 /* Wait for every call of this cache enqueued so far (on `stream` and on the
  * cache's copy streams), read their summaries, and return the first error

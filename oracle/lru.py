@@ -11,7 +11,11 @@ cache" sections:
   the residency table, picks K victim slots at once (the miss path takes the
   first q <= K of them) and rewrites logical ids to slot ids.
 "Elastic memory management" section: at a safe point the cache is rebuilt to
-a new slot budget without touching the host pool.
+a new slot budget without touching the host pool.  "Full-layer double
+buffering" section: prefill carves two full-layer buffers out of the same
+slot pool, streams each layer's whole expert set into one of them while the
+previous layer computes on the other, and whatever survives prefill seeds
+the decode cache (there is no separate prefill cache and no hand-off step).
 
 Readings where the pages are silent (each one is a plain deterministic choice):
 * U = the sorted distinct experts routed by the B tokens of the call.  Every
@@ -27,14 +31,26 @@ Readings where the pages are silent (each one is a plain deterministic choice):
   evicted in ascending slot order; survivors sitting in slots >= C' move, in
   ascending old-slot order, into the vacant slots < C' in ascending order.
   Growing appends empty slots.  Stamps, the map and g are preserved.
+* Prefill over layers l0 .. l1-1 (needs C >= 2E): the buffers are the last
+  2E slots; buffer b = slots C-2E+b*E .. C-2E+b*E+E-1, expert e of a layer
+  in buffer b sits at slot C-2E+b*E+e.  First every entry in the buffers is
+  evicted (PREFILL_EVICT events, ascending slot).  Then step i (layer
+  l0 + i mod (l1-l0); a long prompt repeats the layers once per chunk) uses
+  buffer i mod 2: every expert e of the layer, in ascending order, is either
+  already resident in a slot outside the buffers (read in place, no copy) or
+  streamed into its buffer slot (whatever that slot held is dropped); either
+  way its stamp becomes g + e, then g += E.  The buffer slots keep what was
+  last streamed into them: after prefill they are ordinary cache entries, so
+  the last two layers' streamed experts seed decode.
 """
+
 from __future__ import annotations
 
 from dataclasses import dataclass
 
 import numpy as np
 
-HIT, MISS, RESIZE_EVICT = 0, 1, 2
+HIT, MISS, RESIZE_EVICT, PREFILL_EVICT = 0, 1, 2, 3
 
 
 class CapacityError(RuntimeError):
@@ -149,6 +165,48 @@ class CacheSim:
         self.stamp = self.stamp[:C_new].copy()
         self.C = C_new
         return events
+
+    # -- prefill with full-layer double buffering --------------------------
+    def prefill(self, l0: int, l1: int, chunks: int = 1) -> tuple[list[Event], np.ndarray]:
+        """Layers l0 .. l1-1 through the two full-layer buffers, `chunks`
+        times in a row (a long prompt runs as consecutive chunks, each a full
+        pass over the layers; step i of the passes uses buffer i mod 2).
+
+        Returns the PREFILL_EVICT events of carving the buffers and the slot
+        table int64 [chunks * (l1 - l0), E]: the slot each expert is read from
+        at each step (its buffer slot when streamed, its own slot when
+        resident).
+        """
+        E, C = self.E, self.C
+        if C < 2 * E:
+            raise CapacityError(f"prefill needs two full-layer buffers ({2 * E} slots), the cache has {C}")
+        buf0 = C - 2 * E
+        events = []
+        for s in range(buf0, C):
+            key = int(self.owner[s])
+            if key >= 0:
+                events.append(Event(self.calls, key // E, key % E, PREFILL_EVICT, s, key))
+                self.map[key] = -1
+                self.owner[s] = -1
+                self.stamp[s] = 0
+        n = l1 - l0
+        table = np.zeros((chunks * n, E), dtype=np.int64)
+        for i in range(chunks * n):
+            layer, b = l0 + i % n, i % 2
+            for e in range(E):
+                key = layer * E + e
+                s = int(self.map[key])
+                if s < 0:  # streamed into the buffer
+                    s = buf0 + b * E + e
+                    old = int(self.owner[s])
+                    if old >= 0:
+                        self.map[old] = -1
+                    self.owner[s] = key
+                    self.map[key] = s
+                self.stamp[s] = np.uint64(self.g + e)
+                table[i, e] = s
+            self.g += E
+        return events, table
 
     def resident_keys(self) -> set[int]:
         return {int(k) for k in self.owner if k >= 0}

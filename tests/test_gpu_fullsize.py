@@ -8,6 +8,7 @@ schedule the outputs must also equal, bit for bit, those of a run at full
 residency.  Pools are built on the GPU and freed after each test.
 """
 import gc
+import os
 
 import numpy as np
 import pytest
@@ -97,3 +98,79 @@ def test_elastic_schedule_full(B):
     # the host pool is never written
     assert torch.equal(pool[::997], before)
     free(gpu, ref, full, pool, shared)
+
+
+# ---- prefill at full size: the oracle on a seeded sample of tokens -------------
+
+def _expert_outputs(args):
+    """Oracle worker (spawned process): o = expert(x) of one (layer, expert) for
+    the sampled tokens routed to it."""
+    import numpy as np
+
+    import synth
+    from oracle import ffn, records
+
+    seed, key, H, I, wdtype, x = args
+    rec = synth.records_array(seed, key, 1, H, I, wdtype)[0]
+    return key, ffn.expert(x, *records.parse(rec, H, I, wdtype))
+
+
+def sampled_prefill_reference(w, xs, lg, layers, tokens, workers=16):
+    """y [len(layers), len(tokens), H] from the oracle: routing and combine here,
+    the expert FFNs of the distinct (layer, expert) pairs in a spawned pool."""
+    import multiprocessing as mp
+
+    from oracle import router
+
+    jobs, plan = [], []
+    for li, l in enumerate(layers):
+        x = synth.bf16_bits_to_f32(xs[li][tokens]).astype(np.float64)
+        ids, wts = router.topk_softmax(lg[li][tokens].astype(np.float64), w.k)
+        plan.append((x, ids, wts))
+        for e in sorted(set(ids.reshape(-1).tolist())):
+            jobs.append((w.seed, l * w.E + e, w.H, w.I, w.wdtype, x))
+        if w.shared:
+            jobs.append((w.seed, w.LE + l, w.H, w.I, w.wdtype, x))
+    with mp.get_context("spawn").Pool(min(workers, os.cpu_count() or 1)) as pool:
+        outs = dict(pool.map(_expert_outputs, jobs, chunksize=1))
+    ys = []
+    for li, l in enumerate(layers):
+        x, ids, wts = plan[li]
+        y = np.zeros_like(x)
+        for t in range(len(tokens)):
+            for j in range(w.k):
+                y[t] += wts[t, j] * outs[l * w.E + int(ids[t, j])][t]
+            if w.shared:
+                y[t] += outs[w.LE + l][t]
+        ys.append(y)
+    return ys
+
+
+@pytest.mark.parametrize("w", [configs.C4, configs.C2.with_(name="qwen3.6-shape-prefill-4096", B=4096)],
+                         ids=["dsv4-fp4-4096x43", "qwen36-bf16-4096x40"])
+def test_prefill_full_size_sampled(w):
+    from expert_cache_serving_gb300 import moecache as mc
+    from expert_cache_serving_gb300 import runner
+
+    T, L = w.B, w.L
+    layers = [0, 1, L // 2, L - 1]
+    rng = np.random.default_rng(w.seed)
+    tokens = np.sort(rng.choice(T, size=64, replace=False))
+    xs = np.stack([synth.activations_bf16(w.seed, 0, l, T, w.H) for l in range(L)])
+    lg = synth.iid_logits(w.seed, L, T, w.E)
+    ref = sampled_prefill_reference(w, xs[layers], lg[layers], layers, tokens)
+    dev = torch.device("cuda")
+    pool, shared = runner.build_pool(w), runner.build_shared(w)
+    cache = runner.Cache(w, pool, shared, C=w.C, max_tokens=1)
+    x = torch.from_numpy(xs.view(np.int16)).view(torch.bfloat16).to(dev)
+    del xs
+    y = torch.empty_like(x)
+    st = mc.moe_prefill_stream(cache.handle, 0, L, x, torch.from_numpy(lg).to(dev), T, y, torch.cuda.current_stream())
+    assert st == mc.MOE_OK, mc.moe_last_error()
+    torch.cuda.synchronize()
+    assert mc.moe_cache_sync(cache.handle, torch.cuda.current_stream()) == mc.MOE_OK
+    for li, l in enumerate(layers):
+        got = y[l][torch.from_numpy(tokens).to(dev)].float().cpu().numpy().astype(np.float64)
+        H.assert_layer_close(got, ref[li], f"layer {l}")
+    cache.close()
+    free(x, y, pool, shared)

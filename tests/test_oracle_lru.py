@@ -74,10 +74,51 @@ class ListLRU:
         return out
 
 
+    def prefill(self, l0, l1, chunks=1):
+        """Physical model: the buffers are the last 2E slots; each layer's
+        experts are requested in ascending order, each either read where it
+        is resident or copied into its buffer slot, replacing that slot's
+        content; a requested expert becomes the most recent."""
+        E, C = self.E, self.C
+        buf0 = C - 2 * E
+        out = []
+        for key, s in sorted(self.slot.items(), key=lambda kv: kv[1]):
+            if s >= buf0:
+                out.append((self.calls, key // E, key % E, lru.PREFILL_EVICT, s, key))
+        for _, _, _, _, s, key in out:
+            del self.slot[key]
+            self.order.remove(key)
+        table = []
+        for i in range(chunks * (l1 - l0)):
+            layer = l0 + i % (l1 - l0)
+            row = []
+            for e in range(E):
+                key = layer * E + e
+                if key not in self.slot:
+                    s = buf0 + (i % 2) * E + e
+                    for k in [k for k, v in self.slot.items() if v == s]:
+                        del self.slot[k]
+                        self.order.remove(k)
+                    self.slot[key] = s
+                else:
+                    self.order.remove(key)
+                self.order.append(key)
+                row.append(self.slot[key])
+            table.append(row)
+        return out, table
+
+
 def run_both(L, E, C, trace):
     a, b = lru.CacheSim(L, E, C), ListLRU(L, E, C)
     ea, eb = [], []
     for layer, ids in trace:
+        if layer == "prefill":
+            ev, ta = a.prefill(*ids)
+            evb, tb = b.prefill(*ids)
+            ea += [e.as_tuple() for e in ev]
+            eb += evb
+            assert ta.tolist() == tb
+            continue
         try:
             ev, _ = a.access(layer, ids)
             ea += [e.as_tuple() for e in ev]
@@ -206,3 +247,87 @@ def test_slot_ids_rewrite():
     ev, slots = sim.access(0, ids)
     slot_of = {e.expert: e.slot for e in ev}
     assert (slots == np.vectorize(slot_of.get)(ids)).all()
+
+
+# ------------------------------------------------------------------ prefill --
+
+def recency_order(sim):
+    occ = [s for s in range(sim.C) if sim.owner[s] >= 0]
+    return [int(sim.owner[s]) for s in sorted(occ, key=lambda s: int(sim.stamp[s]))]
+
+
+@pytest.mark.parametrize("seed", range(40))
+def test_prefill_matches_physical_model_inside_random_traces(seed):
+    rng = random.Random(seed)
+    L, E = 4, 3
+    C = rng.randint(2 * E, L * E)
+    trace = []
+    for _ in range(rng.randint(3, 9)):
+        if rng.random() < 0.3:
+            l0 = rng.randint(0, L - 1)
+            trace.append(("prefill", (l0, rng.randint(l0 + 1, L), rng.choice([1, 1, 2, 3]))))
+        else:
+            trace.append((rng.randint(0, L - 1), [[rng.randint(0, E - 1) for _ in range(2)]]))
+    a, b = lru.CacheSim(L, E, C), ListLRU(L, E, C)
+    ea, eb = [], []
+    for layer, ids in trace:
+        if layer == "prefill":
+            ev, ta = a.prefill(*ids)
+            evb, tb = b.prefill(*ids)
+            assert ta.tolist() == tb
+            ea += [e.as_tuple() for e in ev]
+            eb += evb
+        else:
+            ev, _ = a.access(layer, ids)
+            ea += [e.as_tuple() for e in ev]
+            eb += b.access(layer, ids)
+        # same residency, same slots, same recency order after every operation
+        assert {int(a.owner[s]): s for s in range(C) if a.owner[s] >= 0} == b.slot
+        assert recency_order(a) == b.order
+        for key in range(L * E):
+            assert (a.map[key] >= 0) == (key in b.slot)
+    assert ea == eb
+
+
+def test_prefill_survivors_seed_decode():
+    # a full-model prefill on an empty cache leaves the last two layers' whole
+    # expert sets resident in the buffers, so decode on those layers never misses
+    L, E, k = 5, 8, 3
+    sim = lru.CacheSim(L, E, 2 * E + 4)
+    ev, table = sim.prefill(0, L)
+    assert ev == []
+    buf0 = sim.C - 2 * E
+    assert table[L - 1].tolist() == [buf0 + ((L - 1) % 2) * E + e for e in range(E)]
+    assert sim.resident_keys() == {l * E + e for l in (L - 2, L - 1) for e in range(E)}
+    rng = np.random.default_rng(0)
+    for layer in (L - 2, L - 1):
+        ids = rng.choice(E, size=(2, k), replace=True)
+        evs, _ = sim.access(layer, ids)
+        assert all(e.kind == lru.HIT for e in evs)
+
+
+def test_prefill_reads_resident_experts_in_place_and_keeps_one_copy():
+    L, E = 3, 4
+    sim = lru.CacheSim(L, E, 2 * E + 2)
+    sim.access(1, np.array([[2, 3]]))  # layer 1's experts 2 and 3 land in slots 0 and 1
+    assert sim.map[1 * E + 2] == 0 and sim.map[1 * E + 3] == 1
+    ev, table = sim.prefill(0, L)
+    assert table[1].tolist()[2:] == [0, 1]  # read where they are, not streamed
+    keys = [int(k) for k in sim.owner if k >= 0]
+    assert len(keys) == len(set(keys))
+    assert sim.g == 2 + L * E
+
+
+def test_prefill_carves_buffers_and_logs_evictions():
+    L, E = 2, 2
+    sim = lru.CacheSim(L, E, 5)
+    sim.access(0, np.array([[0, 1]]))
+    sim.access(1, np.array([[0, 1]]))
+    sim.access(0, np.array([[0]]))  # hit; slots: 0->key0, 1->key1, 2->key2, 3->key3
+    ev, _ = sim.prefill(1, 2)
+    # buffers are slots 1..4: keys 1, 2, 3 evicted in slot order; key 0 stays
+    assert [(e.slot, e.evicted_key, e.kind) for e in ev] == [(1, 1, lru.PREFILL_EVICT), (2, 2, lru.PREFILL_EVICT),
+                                                             (3, 3, lru.PREFILL_EVICT)]
+    assert sim.map[0] == 0
+    with pytest.raises(lru.CapacityError):
+        lru.CacheSim(L, E, 3).prefill(0, 1)
