@@ -558,6 +558,7 @@ def run_native(args):
                 "note": "same trace steps and cache history as value; per step the activations and logits of "
                         "every layer are copied from pinned host memory and the outputs back"},
         "gpu_launches": st["layer_launches"] + st["finish_launches"],
+        "pdl_launches": st["pdl_launches"],
         "deferred_calls": st["deferred_calls"],
         "host_us_per_call": {"wait_for_miss_list": st["host_wait_us"] / max(1, st["calls"]),
                              "issue_fills": st["host_issue_us"] / max(1, st["calls"])},
@@ -616,14 +617,34 @@ def run_native(args):
     return 0
 
 
+def run_prefill_only(args):
+    """The prefill leg alone, printed as its own line (profiler captures)."""
+    import torch
+
+    from expert_cache_serving_gb300 import runner
+
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    peaks, peak_kind = load_peaks()
+    w = configs.C4 if args.workload == "c4" else configs.C4.with_(name="small-fp4-prefill-256", L=2, E=16, C=32, B=256)
+    pool = runner.build_pool(configs.C3 if args.workload == "c4" else w)
+    leg = prefill_leg(w, pool, dev, args.warmup, args.steps, peaks, peak_kind)
+    line = dict(leg, metric=METRIC, n_gpus=1, higher_is_better=True, scaling="weak", vs_baseline=None,
+                data="synthetic")
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
-    ap.add_argument("--workload", default="c2", choices=["c2", "small"],
-                    help="headline decode workload: c2 (default) or a 3-layer bf16 case for profiler captures")
+    ap.add_argument("--workload", default="c2", choices=["c2", "small", "c4", "small-prefill"],
+                    help="c2: the full benchmark (default); small: a 3-layer bf16 decode headline for profiler "
+                         "captures; c4 / small-prefill: only the prefill leg, at full size or on 2 layers of "
+                         "16 experts with 256 tokens (profiler captures)")
     ap.add_argument("--legs", default="all",
                     help="comma list of extra legs: c2_device, c3, c4, c5 ('all' default, '' for none)")
     ap.add_argument("--prefill-steps", type=int, default=3)
@@ -637,6 +658,8 @@ def main():
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
         return run_reference(args, configs.C2)
+    if args.workload in ("c4", "small-prefill"):
+        return run_prefill_only(args)
     return run_native(args)
 
 

@@ -187,8 +187,10 @@ struct moe_cache {
   float* d_o_part = nullptr;    // partial sums handed to the completion kernel
   int o_part_floats = 0;
   unsigned long long* d_deferred = nullptr;
+  unsigned* d_wave = nullptr;   // [2][kWaveCtrs] per-call counters of the layer kernel, by call parity
   unsigned long long deferred_base = 0;  // value of the device counter at the last statistics reset
   unsigned long long wait_gu_ns = 2000000, wait_dn_ns = 2000000;
+  double split_bp = 0.0, split_bh = 0.0;  // bandwidths for q* (0: not set)
   bool pdl = true;              // launch layer kernels as programmatic dependents
   int32_t* d_oldest = nullptr;
   int* d_oldest_n = nullptr;
@@ -265,7 +267,7 @@ struct moe_cache {
 };
 
 static constexpr int kTlRing = 1024;
-static constexpr int kTlStamps = 12;
+static constexpr int kTlStamps = 16;
 static constexpr int kRing = 256;  // call summaries in flight (device-fill calls the host has not read)
 
 static const char* kNotFound = "";
@@ -310,7 +312,7 @@ static void free_all(moe_cache* c) {
   for (void* p : {(void*)c->d_map, (void*)c->d_owner, (void*)c->d_stamp, (void*)c->d_g, (void*)c->d_plan,
                   (void*)c->d_h, (void*)c->d_logits, (void*)c->d_bar, (void*)c->d_flags, (void*)c->d_oldest,
                   (void*)c->d_oldest_n, (void*)c->d_moves, (void*)c->d_tl, (void*)c->d_cst, (void*)c->d_o_part,
-                  (void*)c->d_deferred})
+                  (void*)c->d_deferred, (void*)c->d_wave})
     if (p) cudaFree(p);
   if (c->h_work) cudaFreeHost(c->h_work);
   if (c->h_err) cudaFreeHost(c->h_err);
@@ -417,7 +419,8 @@ extern "C" moe_status moe_cache_create(const moe_model_desc* desc, const void* h
       (s = cu(cudaMalloc(&c->d_oldest, sizeof(int32_t) * kMaxU), "victim order")) ||
       (s = cu(cudaMalloc(&c->d_oldest_n, sizeof(int)), "victim order")) ||
       (s = cu(cudaMalloc(&c->d_cst, sizeof(CallState)), "call state")) ||
-      (s = cu(cudaMalloc(&c->d_deferred, sizeof(unsigned long long)), "counter")))
+      (s = cu(cudaMalloc(&c->d_deferred, sizeof(unsigned long long)), "counter")) ||
+      (s = cu(cudaMalloc(&c->d_wave, sizeof(unsigned) * 2 * kWaveCtrs), "wave counters")))
     return bail(s);
   if ((s = cu(cudaMemset(c->d_map, 0xFF, sizeof(int32_t) * LE), "memset")) ||
       (s = cu(cudaMemset(c->d_owner, 0xFF, sizeof(int32_t) * nslot_alloc), "memset")) ||
@@ -427,7 +430,8 @@ extern "C" moe_status moe_cache_create(const moe_model_desc* desc, const void* h
       (s = cu(cudaMemset(c->d_flags, 0, sizeof(unsigned) * (1 + 2 * kMaxU)), "memset")) ||
       (s = cu(cudaMemset(c->d_oldest_n, 0xFF, sizeof(int)), "memset")) ||
       (s = cu(cudaMemset(c->d_cst, 0xFF, sizeof(CallState)), "memset")) ||
-      (s = cu(cudaMemset(c->d_deferred, 0, sizeof(unsigned long long)), "memset")))
+      (s = cu(cudaMemset(c->d_deferred, 0, sizeof(unsigned long long)), "memset")) ||
+      (s = cu(cudaMemset(c->d_wave, 0, sizeof(unsigned) * 2 * kWaveCtrs), "memset")))
     return bail(s);
   if ((s = cu(cudaHostAlloc((void**)&c->h_work, sizeof(HostWork) * kRing, cudaHostAllocMapped), "pinned summary")) ||
       (s = cu(cudaHostAlloc((void**)&c->h_err, sizeof(int), cudaHostAllocMapped), "pinned error word")))
@@ -615,6 +619,7 @@ static void account_call(moe_cache* c, int layer, int B, const HostWork& w, cuda
   st.misses += n_miss;
   st.routed_pairs += (int64_t)B * d.k;
   st.bytes_filled += (int64_t)n_miss * c->S;
+  st.qstar_fills += w.qstar;
   st.records_streamed += n_u + d.has_shared;
   for (int r = 0; r < n_u; ++r) {
     if (w.fill[r] && w.evicted[r] >= 0) st.evictions += 1;
@@ -728,6 +733,10 @@ extern "C" moe_status moe_layer_forward_ex(moe_cache_t c, int32_t layer, const v
   p.wait_gu_ns = c->wait_gu_ns;
   p.wait_dn_ns = c->wait_dn_ns;
   p.deferred = c->d_deferred;
+  p.split_bp = c->split_bp;
+  p.split_bh = c->split_bh;
+  p.wave_ctr = c->d_wave + (seq & 1) * kWaveCtrs;
+  p.wave_next = c->d_wave + ((seq + 1) & 1) * kWaveCtrs;
   p.has_shared = d.has_shared;
   p.device_fill = device;
   p.pool = c->host_pool;  // pinned pages are mapped at the same address under unified addressing
@@ -759,6 +768,7 @@ extern "C" moe_status moe_layer_forward_ex(moe_cache_t c, int32_t layer, const v
   if (aux) {
     p.aux_ids = aux->ids; p.aux_w = aux->weights; p.aux_slots = aux->slots;
     p.aux_perm = aux->perm; p.aux_offsets = aux->offsets; p.aux_logits = aux->logits;
+    p.aux_qstar = aux->qstar;
   }
   cudaEvent_t ta = nullptr, tb = nullptr;
   if (c->profiling) {
@@ -1027,6 +1037,15 @@ extern "C" moe_status moe_cache_sync(moe_cache_t c, void* stream) {
     c->sticky = MOE_OK;
     return fail(e, "%s", c->sticky_msg.c_str());
   }
+  return MOE_OK;
+}
+
+extern "C" moe_status moe_cache_set_split_bandwidths(moe_cache_t c, double b_p, double b_h) {
+  if (!c) return fail(MOE_ERR_INVALID_ARG, "cache is NULL");
+  if (!(b_p >= 0.0) || !(b_h >= 0.0)) return fail(MOE_ERR_INVALID_ARG, "bandwidths must be >= 0");
+  if (moe_status e = drain_inflight(c, 0)) return e;
+  c->split_bp = b_p;
+  c->split_bh = b_h;
   return MOE_OK;
 }
 

@@ -17,6 +17,7 @@ constexpr int kMaxItems = kMaxU + 1; // + shared expert
 constexpr int kThreads = 512;  // layer kernel CTA size
 constexpr int kWarps = kThreads / 32;
 constexpr unsigned kFlagError = 0x80000000u;  // fill flag: the copy was not issued
+constexpr int kWaveCtrs = 16;  // per-call counters of the layer kernel (two sets, by call parity)
 
 // Per-call plan written by the control kernel into device memory and read by
 // the expert-FFN kernels of the same call.
@@ -50,6 +51,7 @@ struct HostWork {
   int32_t fill[kMaxU];
   int32_t pairs[kMaxU];        // routed pairs of this expert
   int32_t fill_order[kMaxU];   // f-th fill the kernel consumes -> rank in U
+  int32_t qstar;               // fill count of the bandwidth split for this call's misses
 };
 
 // Completion state of one decode call in copy-fill mode, read by the

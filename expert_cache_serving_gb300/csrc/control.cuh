@@ -259,6 +259,7 @@ __device__ __forceinline__ void publish_summary(const LayerParams& p) {
 // to every thread.
 static __device__ int route_lookup(const LayerParams& p, CtrlSmem& cs, bool write_aux) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarp = blockDim.x >> 5;
+  const bool rec = p.tl && blockIdx.x == 1 && tid == 0;
   const int E = p.E, k = p.k, B = p.B, npairs = B * k;
   // the layer's residency row is loaded while the router's logits load (the
   // two latencies overlap); stored to shared memory after the router
@@ -284,12 +285,14 @@ static __device__ int route_lookup(const LayerParams& p, CtrlSmem& cs, bool writ
     else if (nq <= 16) route_token<16>(lg, E, k, lane, aux, ids, w);
     else route_token<32>(lg, E, k, lane, aux, ids, w);
   }
+  if (rec) p.tl[12] = globaltimer_ns();
 #pragma unroll
   for (int j = 0; j < kMaxE / kThreads; ++j) {
     const int e = tid + j * kThreads;
     if (e < E) cs.maprow[e] = mrow[j];
   }
   __syncthreads();
+  if (rec) p.tl[13] = globaltimer_ns();
 
   // ---- dedup: U = sorted distinct routed experts ----------------------------------
   if (tid < npairs) atomicOr(&cs.bits[cs.ids[tid] >> 5], 1u << (cs.ids[tid] & 31));
@@ -340,6 +343,7 @@ static __device__ int route_lookup(const LayerParams& p, CtrlSmem& cs, bool writ
     cs.nmiss = packed_tot & 0xFFFF;
   }
   __syncthreads();
+  if (rec) p.tl[14] = globaltimer_ns();
   // stable grouping of the (token, rank) pairs by expert
   if (tid < npairs) {
     const int r = cs.prank[tid];
@@ -369,6 +373,19 @@ static __device__ void publish_error(const LayerParams& p, const CtrlSmem& cs, i
   work->seq = p.seq;
   __threadfence();
   st_release_u32(p.plan_flag, p.seq);
+}
+
+// Fill count q* of the bandwidth split for m misses ("measured bandwidths
+// decide the split" in the FreeToken write-up): q/(m-q) ~ B_P/(B_H - B_P), so
+// q* ~ m B_P / B_H, rounded to the nearest integer (halves up), at least one
+// fill, all m when B_H <= B_P or when no bandwidths are set; 0 without misses.
+// Computed in float64 so that the rounding decision is the one the reference
+// computation takes.
+__device__ __forceinline__ int qstar_of(int m, double bp, double bh) {
+  if (m <= 0) return 0;
+  if (!(bp > 0.0) || !(bh > 0.0) || bh <= bp) return m;
+  const int q = (int)floor((double)m * bp / bh + 0.5);
+  return q < 1 ? 1 : (q > m ? m : q);
 }
 
 // Victims, the plan and the host summary (control CTA, after route_lookup):
@@ -490,6 +507,8 @@ static __device__ int choose_victims(const LayerParams& p, CtrlSmem& cs) {
     work->n_u = n_u;
     work->n_miss = nmiss;
     work->g_before = cs.g;
+    work->qstar = qstar_of(nmiss, p.split_bp, p.split_bh);
+    if (p.aux_qstar) *p.aux_qstar = work->qstar;
   }
   if (host_first) publish_summary(p);  // the host issues this call's copies from it
   // the CTA barrier orders every thread's plan writes before thread 0's

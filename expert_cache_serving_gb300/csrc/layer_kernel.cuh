@@ -45,6 +45,21 @@ struct ItemTable {
   float pair_w[kMaxPairs];   // the plan's routing weights, copied once per call
 };
 
+// A group of warps [w0, w0 + nw) of the CTA working together; bar 0 is the
+// CTA-wide barrier, other ids are named barriers of the group's nw * 32 threads.
+struct WarpGroup {
+  int w0, nw, bar;
+  __device__ __forceinline__ int tid() const { return (int)threadIdx.x - 32 * w0; }
+  __device__ __forceinline__ int nthreads() const { return 32 * nw; }
+  __device__ __forceinline__ void sync() const {
+    if (bar == 0)
+      __syncthreads();
+    else
+      asm volatile("bar.sync %0, %1;" ::"r"(bar), "r"(32 * nw) : "memory");
+  }
+};
+__device__ __forceinline__ WarpGroup whole_cta() { return WarpGroup{0, kWarps, 0}; }
+
 // Items of plan list `which` into tb at position `at` (list 1 from the host
 // pool when `from_pool`); returns the new item count.  All threads call.
 static __device__ int load_items(const LayerParams& p, const Plan* pl, int which, ItemTable& tb, int at = 0,
@@ -136,20 +151,36 @@ __device__ __forceinline__ void item_token(const LayerParams& p, const ItemTable
 // Gate/up rows of items [ib, ie), spread over CTAs [cta0, cta0 + ncta).
 // WB: the rows are read from the host pool and also written to the slot.
 template <int WD, int MAXT, bool FRESH, bool WB = false, typename XT>
-__device__ void phase1(const LayerParams& p, const ItemTable& tb, int ib, int ie, int cta0, int ncta, const XT* xs) {
+__device__ void phase1(const LayerParams& p, const ItemTable& tb, int ib, int ie, int cta0, int ncta, const XT* xs,
+                       WarpGroup grp = whole_cta()) {
   using F = Fmt<WD>;
   constexpr int EPC = F::kElemsPerChunk, UNR = F::kUnroll;
   const int rel = (int)blockIdx.x - cta0;
   if (rel < 0 || rel >= ncta || ie <= ib) return;
-  const int H = p.H, I = p.I, lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int H = p.H, I = p.I, lane = threadIdx.x & 31, warp = grp.tid() >> 5;
   const int64_t total = (int64_t)(ie - ib) * I;
   const int64_t t0 = (int64_t)rel * total / ncta, t1 = (int64_t)(rel + 1) * total / ncta;
   const int nchunks = H / EPC;
   const int64_t rb = F::row_bytes(H);
-  for (int64_t task = t0 + warp; task < t1; task += kWarps) {
+  for (int64_t task = t0 + warp; task < t1; task += grp.nw) {
     const int it = ib + (int)(task / I), i = (int)(task % I);
     const int ntok = tb.ntok[it];
     const RecView v = rec_view<WD>(tb.rec[it], H, I);
+    if constexpr (!FRESH && !WB) {
+      // this warp's next rows into L2 while it streams these: more bytes in
+      // flight than its registers hold (resident slots only)
+      const int64_t nx = task + grp.nw;
+      if (lane == 0 && nx < t1) {
+        const int it2 = ib + (int)(nx / I), i2 = (int)(nx % I);
+        const RecView v2 = rec_view<WD>(tb.rec[it2], H, I);
+        prefetch_l2(v2.gate + (int64_t)i2 * rb, (uint32_t)rb);
+        prefetch_l2(v2.up + (int64_t)i2 * rb, (uint32_t)rb);
+        if (WD == MOE_FP4) {
+          prefetch_l2(v2.gate_sc + (int64_t)i2 * (H / 16), (uint32_t)(H / 16));
+          prefetch_l2(v2.up_sc + (int64_t)i2 * (H / 16), (uint32_t)(H / 16));
+        }
+      }
+    }
     const uint8_t* grow = v.gate + (int64_t)i * rb;
     const uint8_t* urow = v.up + (int64_t)i * rb;
     const uint8_t* gsc = (WD == MOE_FP4) ? v.gate_sc + (int64_t)i * (H / 16) : nullptr;
@@ -251,16 +282,17 @@ __device__ __forceinline__ unsigned short ld_down2(const uint8_t* q) {
   if constexpr (STAGED) return lds2(q); else return ld_w2<FRESH>(q);
 }
 
-// W_down rows [n0, n0 + nrows) of items [ib, ie) -> os[row][t][j].
-// STAGED: the rows of item ib + j sit in shared memory at stage + j * pitch
-// (rows n0.., then their FP4 scales), copied there during phase 1.
+// W_down rows [n0, n0 + nrows) of items [ib, ie) -> os[row][t][j], by the
+// warp group grp.  STAGED: the rows of item i sit in shared memory at
+// stage + i * pitch (rows n0.., then their FP4 scales), copied there early.
 template <int WD, int MAXT, bool FRESH, bool STAGED = false>
 __device__ void phase2(const LayerParams& p, const ItemTable& tb, int ib, int ie, int n0, int nrows, float* hs,
-                       float* os, const uint8_t* stage = nullptr, int pitch = 0) {
+                       float* os, const uint8_t* stage = nullptr, int pitch = 0, WarpGroup grp = whole_cta()) {
   using F = Fmt<WD>;
   constexpr int EPC = F::kElemsPerChunk;
   constexpr int kLanesPerRow = 8, kRowsPerWarp = 32 / kLanesPerRow, kChunksPerLane = MAXT >= 16 ? 4 : 8;
-  const int H = p.H, I = p.I, B = p.B, k = p.k, lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int H = p.H, I = p.I, B = p.B, k = p.k, lane = threadIdx.x & 31, warp = grp.tid() >> 5;
+  const int gt = grp.tid(), gn = grp.nthreads();
   const int ostride = B * (k + 1);
   const int nchunks = I / EPC;
   int g0 = ib;
@@ -272,45 +304,45 @@ __device__ void phase2(const LayerParams& p, const ItemTable& tb, int ib, int ie
       used += nt * I;
       ++g1;
     }
-    __syncthreads();
+    grp.sync();
     {  // h rows of the group, item-major, in one flat pass (all loads in flight together)
       __shared__ int s_hrow[kMaxPairs + kMaxB];
       const int rows = tb.hbase[g1] - tb.hbase[g0];
-      for (int rr = threadIdx.x; rr < rows; rr += blockDim.x) {
+      for (int rr = gt; rr < rows; rr += gn) {
         int g = g0;
         while (tb.hbase[g + 1] - tb.hbase[g0] <= rr) ++g;
         int t, hr, j;
         item_token(p, tb, g, rr - (tb.hbase[g] - tb.hbase[g0]), &t, &hr, &j);
         s_hrow[rr] = hr;
       }
-      __syncthreads();
+      grp.sync();
       const int per = I / 4, n4 = rows * per;
-      for (int e0 = threadIdx.x; e0 < n4; e0 += 4 * blockDim.x) {  // four loads in flight per thread
+      for (int e0 = gt; e0 < n4; e0 += 4 * gn) {  // four loads in flight per thread
         float4 v[4];
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-          const int e = e0 + u * (int)blockDim.x;
+          const int e = e0 + u * gn;
           if (e < n4) v[u] = __ldcg(reinterpret_cast<const float4*>(p.h + (int64_t)s_hrow[e / per] * I) + e % per);
         }
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-          const int e = e0 + u * (int)blockDim.x;
+          const int e = e0 + u * gn;
           if (e < n4) reinterpret_cast<float4*>(hs + (int64_t)(e / per) * I)[e % per] = v[u];
         }
       }
     }
-    __syncthreads();
+    grp.sync();
     // 8 lanes per row, 4 rows per warp: lane l of row group g reads chunks
     // l, l + 8, l + 16, ... of unit u0 + g in increasing order (8 in flight),
     // then the group's 8 partial sums reduce by a fixed butterfly
-    const int grp = lane / kLanesPerRow, gl = lane % kLanesPerRow;
+    const int rg = lane / kLanesPerRow, gl = lane % kLanesPerRow;
     const int nunits = (g1 - g0) * nrows;
-    for (int u0 = warp * kRowsPerWarp; u0 < nunits; u0 += kWarps * kRowsPerWarp) {
-      const int unit = u0 + grp;
+    for (int u0 = warp * kRowsPerWarp; u0 < nunits; u0 += grp.nw * kRowsPerWarp) {
+      const int unit = u0 + rg;
       const bool live = unit < nunits;
       const int gi = live ? g0 + unit / nrows : g0, row = live ? n0 + unit % nrows : n0;
       const uint8_t *drow = nullptr, *dsc = nullptr;
-      if (live) down_row<WD, STAGED>(tb, gi - ib, gi, row, n0, nrows, H, I, stage, pitch, &drow, &dsc);
+      if (live) down_row<WD, STAGED>(tb, gi, gi, row, n0, nrows, H, I, stage, pitch, &drow, &dsc);
       const int hbase = tb.hbase[gi] - tb.hbase[g0];
       const int ntok = live ? tb.ntok[gi] : 0;
       float acc[MAXT];
@@ -352,7 +384,7 @@ __device__ void phase2(const LayerParams& p, const ItemTable& tb, int ib, int ie
     }
     g0 = g1;
   }
-  __syncthreads();
+  grp.sync();
 }
 
 // Items of the call's resident experts (hits in U order, then the shared
@@ -420,6 +452,33 @@ __device__ void poison_rows(const LayerParams& p, int n0, int nrows) {
   }
 }
 
+constexpr int kLookupCtr = 0;  // per-call counter of CTAs done with the residency lookups
+
+// Wait (thread 0 of the group polls, the group waits on it) until *c >=
+// target; false after limit_ns (MOE_ERR_TIMEOUT is then recorded).
+static __device__ bool wait_count(const unsigned* c, unsigned target, WarpGroup g, int* err,
+                                  unsigned long long limit_ns = 2000000000ull) {
+  __shared__ int s_ok[3];
+  if (g.tid() == 0) {
+    int ok = 1;
+    const unsigned long long t0 = globaltimer_ns();
+    for (;;) {
+      unsigned v;
+      asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(c) : "memory");
+      if (v >= target) break;
+      if (globaltimer_ns() - t0 > limit_ns) {
+        atomicExch(err, MOE_ERR_TIMEOUT);
+        ok = 0;
+        break;
+      }
+      __nanosleep(32);
+    }
+    s_ok[g.bar] = ok;
+  }
+  g.sync();
+  return s_ok[g.bar] != 0;
+}
+
 __device__ __forceinline__ int ld_relaxed_s32(const int* q) {
   int v;
   asm volatile("ld.relaxed.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(q) : "memory");
@@ -460,15 +519,18 @@ __global__ void __launch_bounds__(kThreads, 1) layer_kernel(LayerParams p) {
   grid_dep_wait();  // the previous call's commit and outputs are visible
   grid_dep_launch();
   if (rec) p.tl[0] = globaltimer_ns();
-  if (threadIdx.x == 0) {
+  if (threadIdx.x == 0) s_flag = 0;  // read only after CTA barriers
+  if (threadIdx.x == kThreads - 64) {
     p.cst->part[blockIdx.x] = -1;
-    if (ctrl) p.cst->gu_stop = 0;  // before the first grid barrier, which every later writer passes
+    if (ctrl) p.cst->gu_stop = 0;  // before the plan flag, which every later writer acquires
   }
+  // counters of the next call (this call's were cleared by the previous one)
+  if (ctrl && threadIdx.x >= kThreads - kWaveCtrs) p.wave_next[threadIdx.x - (kThreads - kWaveCtrs)] = 0u;
   // activations into shared memory by one bulk copy (waited for before phase 1),
   // or by plain loads when the caller's pointer is not 16-byte aligned
   const uint32_t xbytes = (uint32_t)((size_t)B * H * sizeof(XT));
   const bool x_bulk = ((uintptr_t)p.x & 15) == 0;
-  if (x_bulk && threadIdx.x == 0) {
+  if (x_bulk && threadIdx.x == kThreads - 32) {  // the last warp: the router warps start at once
     mbar_init(&s_xin, 1);
     fence_mbar_init();
     mbar_expect_tx(&s_xin, xbytes);
@@ -522,8 +584,40 @@ __global__ void __launch_bounds__(kThreads, 1) layer_kernel(LayerParams p) {
     poison_rows<WD>(p, n0, nrows);
     return;
   }
+  // this CTA has read the residency table: the control CTA may commit
+  if (threadIdx.x == 0) atomicAdd(&p.wave_ctr[kLookupCtr], 1u);
+
+  // ---- 1./2. gate/up rows of the resident experts and the shared expert (CTAs
+  // 1..), one grid barrier, then every CTA's W_down rows; the control CTA
+  // commits recency and residency meanwhile, once every CTA has done its lookups
   if (!ctrl) phase1<WD, MAXT, false>(p, tb, 0, n_res, 1, G - 1, xs);
   if (rec) p.tl[2] = globaltimer_ns();
+  bool bad = false;
+  if (ctrl) {
+    bad = !wait_count(&p.wave_ctr[kLookupCtr], (unsigned)G, whole_cta(), p.err);
+    if (!bad) {
+      control_commit(p, cs);
+      compact_oldest(p, cs);
+    }
+    if (p.tl && threadIdx.x == 0) p.tl[11] = globaltimer_ns();
+  }
+  bad = !grid_barrier(p.bar, p.err) || bad;
+  if (n_stage > 0 && !mbar_wait(&s_stage, 0)) {  // the staging copies never leave this CTA in flight
+    if (threadIdx.x == 0) atomicExch(p.err, MOE_ERR_TIMEOUT);
+    mbar_wait(&s_stage, 0);
+    s_flag = 1;
+  }
+  if (bad) s_flag = 1;
+  __syncthreads();
+  if (s_flag) {  // a bounded wait gave up (recorded in p.err)
+    poison_rows<WD>(p, n0, nrows);
+    return;
+  }
+  if (rec) p.tl[3] = globaltimer_ns();
+  for (int i = threadIdx.x; i < nrows * ostride; i += blockDim.x) os[i] = 0.f;
+  phase2<WD, MAXT, false, true>(p, tb, 0, n_stage, n0, nrows, hs, os, stage, p.stage_pitch);
+  phase2<WD, MAXT, false>(p, tb, n_stage, n_res, n0, nrows, hs, os);
+  if (rec) p.tl[4] = globaltimer_ns();
 
   // the fills' slots come from the control CTA's plan
   bool ok = true;
@@ -532,46 +626,27 @@ __global__ void __launch_bounds__(kThreads, 1) layer_kernel(LayerParams p) {
     ok = false;
   }
   const Plan* pl = p.plan;
-  if (ok && pl->err != MOE_OK) ok = false;  // the control CTA returned above
-  const int nf = ok ? pl->n_items[1] : 0;
-  if (ok && p.device_fill && nf > 0) {
-    // device-driven fills: pull each missed record from the host pool, use it
-    // for this call and store it in its slot; W_down rows by the CTA that owns them
-    const int n_all = load_items(p, pl, 1, tb, n_res, true);
-    copy_down_rows<WD>(p, tb, n_res, n_all, n0, nrows);
-    if (!ctrl) phase1<WD, MAXT, false, true>(p, tb, n_res, n_all, 1, G - 1, xs);
-  }
-  const bool bar_ok = ok && grid_barrier(p.bar, p.err);
-  if (n_stage > 0 && !mbar_wait(&s_stage, 0)) {  // the staging copies never leave this CTA in flight
-    if (threadIdx.x == 0) atomicExch(p.err, MOE_ERR_TIMEOUT);
-    mbar_wait(&s_stage, 0);
-    poison_rows<WD>(p, n0, nrows);
-    return;
-  }
-  if (!bar_ok) {
-    if (ok) poison_rows<WD>(p, n0, nrows);
-    return;
-  }
-  if (rec) p.tl[3] = globaltimer_ns();
-  if (ctrl) {
-    control_commit(p, cs);
-    compact_oldest(p, cs);
-    if (p.tl && threadIdx.x == 0) p.tl[11] = globaltimer_ns();
-  }
-
-  // ---- 2. W_down rows of the resident experts --------------------------------------
-  for (int i = threadIdx.x; i < nrows * ostride; i += blockDim.x) os[i] = 0.f;
-  phase2<WD, MAXT, false, true>(p, tb, 0, n_stage, n0, nrows, hs, os, stage, p.stage_pitch);
-  phase2<WD, MAXT, false>(p, tb, n_stage, n_res, n0, nrows, hs, os);
-  if (rec) p.tl[4] = globaltimer_ns();
+  if (ok && pl->err != MOE_OK) ok = false;
+  if (!ok) return;
+  const int nf = pl->n_items[1];
+  if (rec) p.tl[7] = globaltimer_ns();
 
   // ---- 3. fills ----------------------------------------------------------------------
   if (nf > 0 && p.device_fill) {
-    // device-driven fills: this CTA copied its own W_down rows of every fill
-    // into the slots in phase 1, so they are read there, not over the link
-    for (int it = n_res + (int)threadIdx.x; it < n_res + nf; it += blockDim.x) tb.rec[it] = tb.dst[it];
+    // device-driven fills: pull each missed record from the host pool, use it
+    // for this call and store it in its slot; each CTA copies its own W_down
+    // rows of every fill into the slots and then reads them there, not over
+    // the link
+    const int n_all = load_items(p, pl, 1, tb, n_res, true);
+    copy_down_rows<WD>(p, tb, n_res, n_all, n0, nrows);
+    if (!ctrl) phase1<WD, MAXT, false, true>(p, tb, n_res, n_all, 1, G - 1, xs);
+    if (!grid_barrier(p.bar, p.err)) {
+      poison_rows<WD>(p, n0, nrows);
+      return;
+    }
+    for (int it = n_res + (int)threadIdx.x; it < n_all; it += blockDim.x) tb.rec[it] = tb.dst[it];
     __syncthreads();
-    phase2<WD, MAXT, true>(p, tb, n_res, n_res + nf, n0, nrows, hs, os);
+    phase2<WD, MAXT, true>(p, tb, n_res, n_all, n0, nrows, hs, os);
   } else if (nf > 0) {
     // copy mode: each fill as soon as its copy has landed
     load_items(p, pl, 1, tb);
@@ -588,7 +663,6 @@ __global__ void __launch_bounds__(kThreads, 1) layer_kernel(LayerParams p) {
       poison_rows<WD>(p, n0, nrows);
       return;
     }
-    if (rec) p.tl[7] = globaltimer_ns();
     if (threadIdx.x == 0) s_flag = ld_relaxed_s32(&p.cst->gu_stop);
     __syncthreads();
     int handed = s_flag ? 0 : -1;  // fills whose W_down rows os holds when handing over

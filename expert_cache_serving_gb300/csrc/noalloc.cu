@@ -9,10 +9,13 @@
 // the gate/up intermediate) lives in the file-scope device array below, which
 // every GPU that loads this library holds until the process exits.
 //
-// The computation is the same as moe_layer_forward with every expert
-// resident: top-k softmax routing, h = SiLU(x W_gate^T) * (x W_up^T) per
-// (token, rank), o = h W_down^T, y_t = sum_j w_tj o_tj (+ shared expert), with
-// the same per-row summation order, so the two entry points agree.
+// The computation is the one moe_layer_forward performs with every expert
+// resident: top-k softmax routing (the same tie, NaN and infinity rules),
+// h = SiLU(x W_gate^T) * (x W_up^T) per (token, rank), o = h W_down^T,
+// y_t = sum_j w_tj o_tj (+ shared expert) in rank order.  The dot products are
+// summed in a different order (one warp per row here, 8 lanes per row and a
+// fixed butterfly in the cached layer kernel), so the two entry points agree
+// within the layer tolerance, not bit for bit.
 #include <algorithm>
 #include <cstdio>
 #include <mutex>

@@ -25,6 +25,10 @@ struct LayerParams {
   unsigned long long wait_gu_ns;  // how long the layer kernel waits for a fill's gate/up half
   unsigned long long wait_dn_ns;  // ... and for its W_down half, before handing the rest over
   unsigned long long* deferred;   // calls the completion kernel finished (statistics)
+  double split_bp, split_bh;  // measured B_P and B_H for the fill count q* (0: pure fill, q* = misses)
+  int32_t* aux_qstar;         // optional: q* of this call
+  unsigned* wave_ctr;         // [kWaveCtrs] this call's counters (CTAs done with their lookups)
+  unsigned* wave_next;        // [kWaveCtrs] the next call's counters, cleared by this call
   int has_shared;
   int device_fill;            // 1: the kernel pulls each fill from the pool itself
   const uint8_t* pool;        // device-visible address of the pinned host pool (device_fill)
@@ -42,7 +46,7 @@ struct LayerParams {
   int stage_off;              // byte offset of the staging area in dynamic shared memory
   int32_t* oldest;            // [kMaxU] oldest slots, ascending key
   int* oldest_n;              // entries in it, -1 if invalid
-  unsigned long long* tl;     // optional phase timestamps of this call [12] (profiling)
+  unsigned long long* tl;     // optional phase timestamps of this call [16] (profiling)
   // optional inspection outputs
   int32_t* aux_ids;
   float* aux_w;

@@ -186,16 +186,16 @@ __global__ void __launch_bounds__(tc::fp4::kThreads, 1)
     gemm_gate_up_fp4_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_c,
                             const __grid_constant__ CUtensorMap map_s, const int32_t* offsets,
                             const int32_t* slot_of, int n_groups, int H, int I, __half* hp, int* err) {
-  tc::grouped_gemm_fp4_cta(&map_a, &map_c, &map_s, offsets, slot_of, n_groups, I / 128, H,
-                           tc::EpiSwiGLU<__half>{hp, I}, BRowGateUp{I}, err);
+  tc::grouped_gemm_fp4_persistent(&map_a, &map_c, &map_s, offsets, slot_of, n_groups, I / 128, H,
+                                  tc::EpiSwiGLU<__half>{hp, I}, BRowGateUp{I}, err);
 }
 
 __global__ void __launch_bounds__(tc::fp4::kThreads, 1)
     gemm_down_fp4_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_c,
                          const __grid_constant__ CUtensorMap map_s, const int32_t* offsets, const int32_t* slot_of,
                          int n_groups, int H, int I, float* op, int* err) {
-  tc::grouped_gemm_fp4_cta(&map_a, &map_c, &map_s, offsets, slot_of, n_groups, H / 256, I, tc::EpiStoreF32{op, H},
-                           BRowDown{}, err);
+  tc::grouped_gemm_fp4_persistent(&map_a, &map_c, &map_s, offsets, slot_of, n_groups, H / 256, I,
+                                  tc::EpiStoreF32{op, H}, BRowDown{}, err);
 }
 
 // ---- 6. combine ------------------------------------------------------------------------------
@@ -278,6 +278,11 @@ static cudaError_t gemm_attr() {
 
 // grid: enough CTAs for every tile of n_rows rows over n_groups groups
 static int gemm_grid(int n_rows, int n_groups, int nblocks_n) { return (n_rows / tc::kBM + n_groups) * nblocks_n; }
+// persistent grid: one CTA per SM, at most one per possible tile
+static int persistent_grid(int n_rows, int n_groups, int nblocks_n) {
+  const int most = gemm_grid(n_rows, n_groups, nblocks_n);
+  return most < sms() ? most : sms();
+}
 
 cudaError_t prefill_gemm_gate_up(const CUtensorMap& a, const CUtensorMap& b, const int32_t* offsets,
                                  const int32_t* slot_of, int n_groups, int n_rows, int H, int I, void* hp, int* err,
@@ -313,7 +318,8 @@ cudaError_t prefill_gemm_gate_up_fp4(const CUtensorMap& a, const CUtensorMap& co
                                      const int32_t* offsets, const int32_t* slot_of, int n_groups, int n_rows, int H,
                                      int I, void* hp, int* err, cudaStream_t s) {
   if (cudaError_t e = gemm_fp4_attr()) return e;
-  pf::gemm_gate_up_fp4_kernel<<<gemm_grid(n_rows, n_groups, I / 128), tc::fp4::kThreads, tc::fp4::kSmemBytes, s>>>(
+  pf::gemm_gate_up_fp4_kernel<<<persistent_grid(n_rows, n_groups, I / 128), tc::fp4::kThreads, tc::fp4::kSmemBytes,
+                                s>>>(
       a, codes, scales, offsets, slot_of, n_groups, H, I, (__half*)hp, err);
   return cudaGetLastError();
 }
@@ -322,7 +328,8 @@ cudaError_t prefill_gemm_down_fp4(const CUtensorMap& a, const CUtensorMap& codes
                                   const int32_t* offsets, const int32_t* slot_of, int n_groups, int n_rows, int H,
                                   int I, float* op, int* err, cudaStream_t s) {
   if (cudaError_t e = gemm_fp4_attr()) return e;
-  pf::gemm_down_fp4_kernel<<<gemm_grid(n_rows, n_groups, H / 256), tc::fp4::kThreads, tc::fp4::kSmemBytes, s>>>(
+  pf::gemm_down_fp4_kernel<<<persistent_grid(n_rows, n_groups, H / 256), tc::fp4::kThreads, tc::fp4::kSmemBytes,
+                             s>>>(
       a, codes, scales, offsets, slot_of, n_groups, H, I, op, err);
   return cudaGetLastError();
 }

@@ -275,35 +275,45 @@ __device__ void grouped_gemm_cta(const CUtensorMap* map_a, const CUtensorMap* ma
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 
-// ---- FP4-reading variant ---------------------------------------------------------
-// Same tiles, TMEM accumulator and epilogues, but B is read as FP4 and the GEMM
-// runs on f16 operands: per K-step of 64 elements TMA brings the A tile (f16,
-// 128-byte swizzle), the weight rows' e2m1 codes (256 rows x 32 bytes) and the
-// 16-byte box of e4m3 scales that covers them (reloaded for 4 consecutive
-// K-steps, an L2 hit after the first).  Converter warps expand the codes into
-// the f16 B tile in the 128-byte-swizzled K-major layout the MMA reads (chunk
-// j of row r at position j ^ (r & 7) of the row): cvt.rn.f16x2.e2m1x2 then one
-// f16x2 multiply by the block scale, exact (the product has at most 3 + 4
+// ---- FP4-reading variant, persistent ------------------------------------------------
+// Same tiles and epilogues, but B is read as FP4 and the GEMM runs on f16
+// operands: per K-step of 64 elements TMA brings the A tile (f16, 128-byte
+// swizzle), the weight rows' e2m1 codes (256 rows x 32 bytes) and the 16-byte
+// box of e4m3 scales that covers them (reloaded for 4 consecutive K-steps, an
+// L2 hit after the first).  Converter warps expand the codes into the f16 B
+// tile in the 128-byte-swizzled K-major layout the MMA reads (chunk j of row r
+// at position j ^ (r & 7) of the row): cvt.rn.f16x2.e2m1x2 then one f16x2
+// multiply by the block scale, exact (the product has at most 3 + 4
 // significant bits and its exponent stays within the f16 normal range), so the
 // GEMM equals the one on the dequantised weights.  The weight stream from DRAM
 // is 0.5625 byte per element instead of 2.
+//
+// One CTA per SM walks the tile list (tile t, t + gridDim.x, ...; tiles are
+// enumerated expert-major, then row block, then column block, from a table of
+// per-expert tile counts built in shared memory at the start).  Every ring runs
+// continuously across tiles, and the accumulator is double-buffered in TMEM
+// (2 x 256 columns): the epilogue of tile i overlaps the mainloop of tile i+1.
 // Rings: kRaw stages of (A 16 KB | codes 8 KB | scales 4 KB) filled by TMA and
 // two converted B buffers (32 KB each); barriers full/empty per raw stage,
-// conv/bfree per B buffer.  Warps: 0 TMA producer, 1 MMA issuer, 2..17
-// converters (their count sets the kernel's pace: 4, 8 and 16 converter warps
-// measured 0.46, 0.36 and 0.33 ms on the same GEMMs); 2..5 then run the
-// epilogue.
+// conv/bfree per B buffer, acc_full/acc_empty per accumulator.  Warps: 0 TMA
+// producer, 1 MMA issuer (and TMEM owner), 2..17 converters, 18..21 epilogue
+// (warp w reads TMEM lanes 32 * (w % 4) .. + 31).  Every wait is bounded and
+// also gives up once another role has failed; TMEM is freed on every path.
 namespace fp4 {
 constexpr int kRaw = 5;
 constexpr int kBBufs = 2;
 constexpr int kConvWarps = 16;
-constexpr int kThreads = 64 + 32 * kConvWarps;
+constexpr int kEpiWarps = 4;
+constexpr int kConv0 = 2, kEpi0 = kConv0 + kConvWarps;
+constexpr int kThreads = 32 * (kEpi0 + kEpiWarps);
 constexpr int kAStage = kBM * kBK * 2;      // 16 KB
 constexpr int kBStage = kBN * kBK * 2;      // 32 KB
 constexpr int kCodeStage = kBN * kBK / 2;   // 8 KB
 constexpr int kScaleStage = kBN * 16;       // 4 KB
 constexpr int kRawBytes = kAStage + kCodeStage + kScaleStage;  // 28 KB, 1024-aligned
 constexpr uint32_t kTxBytes = kRawBytes;
+constexpr int kAccCols = 256;               // one accumulator; two of them fill the TMEM
+constexpr int kMaxE = 1024;
 constexpr size_t kSmemBytes = (size_t)kBBufs * kBStage + (size_t)kRaw * kRawBytes + 1024 /*align*/ + 256 /*barriers*/;
 static_assert(kRawBytes % 1024 == 0 && kBStage % 1024 == 0, "tiles must keep the 1024-byte swizzle alignment");
 }  // namespace fp4
@@ -337,15 +347,57 @@ __device__ __forceinline__ uint32_t e4m3_to_f16x2_both(uint32_t scale_byte) {
   return s2;
 }
 
-// A: 2D f16 map over [rows][K]; codes: 3D u8 map over [E][Nrows][K/2] (box 32
-// bytes x 128 rows); scales: 3D u8 map over [E][Nrows][K/16] (box 16 x 128).
+// Bounded wait that also gives up as soon as *fail is set by another role.
+__device__ __forceinline__ bool mbar_wait_or(uint64_t* bar, uint32_t parity, const volatile int* fail,
+                                             unsigned long long limit_ns = 2000000000ull) {
+  const uint32_t a = smem_u32(bar);
+  unsigned long long t0 = 0;
+  for (uint32_t it = 0;; ++it) {
+    uint32_t done;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(done)
+        : "r"(a), "r"(parity)
+        : "memory");
+    if (done) return true;
+    if ((it & 63) == 63) {
+      if (*fail) return false;
+      const unsigned long long t = globaltimer_ns();
+      if (t0 == 0) t0 = t;
+      else if (t - t0 > limit_ns) return false;
+    }
+  }
+}
+
+// Tile t of the list: expert e = the last one whose first tile is <= t.
+__device__ __forceinline__ Tile tile_of(const int* tile_base, const int32_t* offsets, int E, int nblocks_n, int t) {
+  int lo = 0, hi = E;  // tile_base[lo] <= t < tile_base[hi]
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (tile_base[mid] <= t) lo = mid; else hi = mid;
+  }
+  const int r = t - tile_base[lo];
+  Tile tl;
+  tl.e = lo;
+  tl.row0 = offsets[lo] + (r / nblocks_n) * kBM;
+  tl.row_end = offsets[lo + 1];
+  tl.nb = r % nblocks_n;
+  return tl;
+}
+
+// A: 2D f16 map over [rows][K]; codes: 3D u8 map over [records][Nrows][K/2]
+// (box 32 bytes x 128 rows); scales: 3D u8 map over [records][Nrows][K/16]
+// (box 16 x 128); group e's weights are record slot_of[e].
 template <typename Epi, typename BRow>
-__device__ void grouped_gemm_fp4_cta(const CUtensorMap* map_a, const CUtensorMap* map_codes,
-                                     const CUtensorMap* map_scales, const int32_t* offsets, const int32_t* slot_of,
-                                     int E, int nblocks_n, int K, Epi epi, BRow b_row, int* err) {
-  constexpr int kRaw = fp4::kRaw, kBBufs = fp4::kBBufs, kConvWarps = fp4::kConvWarps;
+__device__ void grouped_gemm_fp4_persistent(const CUtensorMap* map_a, const CUtensorMap* map_codes,
+                                            const CUtensorMap* map_scales, const int32_t* offsets,
+                                            const int32_t* slot_of, int E, int nblocks_n, int K, Epi epi, BRow b_row,
+                                            int* err) {
+  constexpr int kRaw = fp4::kRaw, kBBufs = fp4::kBBufs, kConvWarps = fp4::kConvWarps, kEpiWarps = fp4::kEpiWarps;
+  constexpr int kConv0 = fp4::kConv0, kEpi0 = fp4::kEpi0, kAccCols = fp4::kAccCols, kMaxE = fp4::kMaxE;
   constexpr int kAStage = fp4::kAStage, kBStage = fp4::kBStage, kCodeStage = fp4::kCodeStage;
   constexpr int kScaleStage = fp4::kScaleStage, kRawBytes = fp4::kRawBytes;
+  constexpr uint32_t kTxBytes = fp4::kTxBytes;
   extern __shared__ __align__(1024) uint8_t tc_smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(tc_smem_raw) + 1023) & ~(uintptr_t)1023);
   uint8_t* btile = smem;                          // kBBufs converted B tiles
@@ -355,14 +407,29 @@ __device__ void grouped_gemm_fp4_cta(const CUtensorMap* map_a, const CUtensorMap
   uint64_t* conv = empty + kRaw;
   uint64_t* bfree = conv + kBBufs;
   uint64_t* acc_full = bfree + kBBufs;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_full + 1);
-  __shared__ Tile s_tile;
-  __shared__ int s_has;
-  __shared__ int s_fail;
+  uint64_t* acc_empty = acc_full + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 2);
+  __shared__ int tile_base[kMaxE + 1];
+  __shared__ int s_scan[33];
+  __shared__ volatile int s_fail;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
+  // per-expert tile counts -> first tile of each expert (one block scan)
+  int n_tiles;
+  {
+    int base = 0;
+    for (int e0 = 0; e0 < E; e0 += blockDim.x) {
+      const int e = e0 + (int)threadIdx.x;
+      const int cnt = e < E ? (offsets[e + 1] - offsets[e] + kBM - 1) / kBM * nblocks_n : 0;
+      int tot;
+      const int before = block_excl_scan(cnt, s_scan, &tot);
+      if (e < E) tile_base[e] = base + before;
+      base += tot;
+    }
+    n_tiles = base;
+    if (threadIdx.x == 0) tile_base[E] = base;
+  }
   if (threadIdx.x == 0) {
-    s_has = find_tile(offsets, E, nblocks_n, blockIdx.x, &s_tile) ? 1 : 0;
     s_fail = 0;
     for (int i = 0; i < kRaw; ++i) {
       mbar_init(&full[i], 1);
@@ -372,91 +439,116 @@ __device__ void grouped_gemm_fp4_cta(const CUtensorMap* map_a, const CUtensorMap
       mbar_init(&conv[i], kConvWarps);
       mbar_init(&bfree[i], 1);
     }
-    mbar_init(acc_full, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&acc_full[i], 1);
+      mbar_init(&acc_empty[i], kEpiWarps);
+    }
     fence_mbar_init();
   }
   __syncthreads();
-  if (!s_has) return;
-  const Tile t = s_tile;
-  if (warp == 1) tmem_alloc(tmem_slot, kTmemCols);
+  if ((int)blockIdx.x >= n_tiles) return;
+  if (warp == 1) tmem_alloc(tmem_slot, 2 * kAccCols);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const int ksteps = K / kBK;
 
-  if (warp == 0 && lane == 0) {
-    // TMA producer: A tile, the 256 weight rows' codes, their scale boxes
-    // (the weights of group t.e sit in record slot_of[t.e])
-    const int rec = slot_of[t.e];
-    for (int ks = 0; ks < ksteps; ++ks) {
-      const int s = ks % kRaw;
-      if (ks >= kRaw && !mbar_wait(&empty[s], ((ks / kRaw) - 1) & 1)) { s_fail = 1; break; }
-      if (s_fail) break;
-      uint8_t* a = raw + s * kRawBytes;
-      uint8_t* codes = a + kAStage;
-      uint8_t* scales = codes + kCodeStage;
-      mbar_expect_tx(&full[s], fp4::kTxBytes);
-      tma_load_2d(a, map_a, &full[s], ks * kBK, t.row0);
-      tma_load_3d(codes, map_codes, &full[s], ks * (kBK / 2), b_row(t.nb, 0), rec);
-      tma_load_3d(codes + kCodeStage / 2, map_codes, &full[s], ks * (kBK / 2), b_row(t.nb, 1), rec);
-      tma_load_3d(scales, map_scales, &full[s], (ks >> 2) * 16, b_row(t.nb, 0), rec);
-      tma_load_3d(scales + kScaleStage / 2, map_scales, &full[s], (ks >> 2) * 16, b_row(t.nb, 1), rec);
-    }
-  } else if (warp == 1 && lane == 0) {
-    // MMA issuer: A from the raw stage, B from the converted buffer
-    constexpr uint32_t idesc = idesc_f16(kBM, kBN);
-    for (int ks = 0; ks < ksteps; ++ks) {
-      const int s = ks % kRaw, bb = ks % kBBufs;
-      if (s_fail || !mbar_wait(&conv[bb], (ks / kBBufs) & 1)) { s_fail = 1; break; }
-      tc_fence_after();
-      const uint32_t a0 = smem_u32(raw + s * kRawBytes);
-      const uint32_t b0 = smem_u32(btile + bb * kBStage);
-#pragma unroll
-      for (int kk = 0; kk < kBK / 16; ++kk)
-        mma_bf16(tmem, smem_desc_sw128(a0 + kk * 32), smem_desc_sw128(b0 + kk * 32), idesc, (ks | kk) != 0);
-      mma_commit(&empty[s]);
-      mma_commit(&bfree[bb]);
-    }
-    mma_commit(acc_full);
-  } else if (warp >= 2) {
-    // converters: 256 rows x 8 chunks of 8 elements per K-step, 8 per thread
-    const int ct = threadIdx.x - 64;
-    for (int ks = 0; ks < ksteps; ++ks) {
-      const int s = ks % kRaw, bb = ks % kBBufs;
-      if (s_fail || !mbar_wait(&full[s], (ks / kRaw) & 1)) { s_fail = 1; break; }
-      if (ks >= kBBufs && !mbar_wait(&bfree[bb], ((ks / kBBufs) - 1) & 1)) { s_fail = 1; break; }
-      const uint8_t* codes = raw + s * kRawBytes + kAStage;
-      const uint8_t* scales = codes + kCodeStage;
-      uint8_t* bt = btile + bb * kBStage;
-      const int sub = (ks & 3) * 4;  // this K-step's 4 scale bytes in each row's 16-byte box
-#pragma unroll
-      for (int i = 0; i < (kBN * 8) / (32 * kConvWarps); ++i) {
-        const int q = ct + 32 * kConvWarps * i;
-        const int r = q >> 3, j = q & 7;
-        const uint32_t c4 = *reinterpret_cast<const uint32_t*>(codes + r * 32 + j * 4);
-        const uint32_t s2 = e4m3_to_f16x2_both(scales[r * 16 + sub + (j >> 1)]);
-        *reinterpret_cast<uint4*>(bt + r * 128 + ((j ^ (r & 7)) << 4)) = dequant8_f16(c4, s2);
+  if (warp == 0) {
+    if (lane == 0) {  // TMA producer: A tile, the 256 weight rows' codes, their scale boxes
+      int g = 0;  // K-steps issued so far (all tiles)
+      for (int t = blockIdx.x; t < n_tiles && !s_fail; t += gridDim.x) {
+        const Tile tl = tile_of(tile_base, offsets, E, nblocks_n, t);
+        const int rec = slot_of[tl.e];
+        for (int ks = 0; ks < ksteps; ++ks, ++g) {
+          const int s = g % kRaw;
+          if (g >= kRaw && !mbar_wait_or(&empty[s], ((g / kRaw) - 1) & 1, &s_fail)) { s_fail = 1; break; }
+          uint8_t* a = raw + s * kRawBytes;
+          uint8_t* codes = a + kAStage;
+          uint8_t* scales = codes + kCodeStage;
+          mbar_expect_tx(&full[s], kTxBytes);
+          tma_load_2d(a, map_a, &full[s], ks * kBK, tl.row0);
+          tma_load_3d(codes, map_codes, &full[s], ks * (kBK / 2), b_row(tl.nb, 0), rec);
+          tma_load_3d(codes + kCodeStage / 2, map_codes, &full[s], ks * (kBK / 2), b_row(tl.nb, 1), rec);
+          tma_load_3d(scales, map_scales, &full[s], (ks >> 2) * 16, b_row(tl.nb, 0), rec);
+          tma_load_3d(scales + kScaleStage / 2, map_scales, &full[s], (ks >> 2) * 16, b_row(tl.nb, 1), rec);
+        }
       }
-      fence_proxy_async_smem();  // generic-proxy writes -> the tensor core's async-proxy reads
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&conv[bb]);
     }
-    if (warp < 6) {
-      // epilogue: warp w reads TMEM lanes 32*(w%4) .. +31, i.e. tile rows
-      const int q = warp & 3;
-      const bool ok = mbar_wait(acc_full, 0, 4000000000ull);
+  } else if (warp == 1) {
+    if (lane == 0) {  // MMA issuer: A from the raw stage, B from the converted buffer
+      constexpr uint32_t idesc = idesc_f16(kBM, kBN);
+      int g = 0, i = 0;  // K-steps and tiles so far
+      for (int t = blockIdx.x; t < n_tiles && !s_fail; t += gridDim.x, ++i) {
+        const int ab = i & 1;
+        if (i >= 2 && !mbar_wait_or(&acc_empty[ab], ((i >> 1) - 1) & 1, &s_fail)) { s_fail = 1; break; }
+        tc_fence_after();
+        const uint32_t acc = tmem + (uint32_t)(ab * kAccCols);
+        for (int ks = 0; ks < ksteps; ++ks, ++g) {
+          const int s = g % kRaw, bb = g % kBBufs;
+          if (!mbar_wait_or(&conv[bb], (g / kBBufs) & 1, &s_fail)) { s_fail = 1; break; }
+          tc_fence_after();
+          const uint32_t a0 = smem_u32(raw + s * kRawBytes);
+          const uint32_t b0 = smem_u32(btile + bb * kBStage);
+#pragma unroll
+          for (int kk = 0; kk < kBK / 16; ++kk)
+            mma_bf16(acc, smem_desc_sw128(a0 + kk * 32), smem_desc_sw128(b0 + kk * 32), idesc, (ks | kk) != 0);
+          mma_commit(&empty[s]);
+          mma_commit(&bfree[bb]);
+        }
+        if (s_fail) break;
+        mma_commit(&acc_full[ab]);
+      }
+    }
+  } else if (warp < kEpi0) {
+    // converters: 256 rows x 8 chunks of 8 elements per K-step, 8 per thread
+    const int ct = threadIdx.x - 32 * kConv0;
+    int g = 0;
+    for (int t = blockIdx.x; t < n_tiles && !s_fail; t += gridDim.x) {
+      for (int ks = 0; ks < ksteps; ++ks, ++g) {
+        const int s = g % kRaw, bb = g % kBBufs;
+        if (!mbar_wait_or(&full[s], (g / kRaw) & 1, &s_fail)) { s_fail = 1; break; }
+        if (g >= kBBufs && !mbar_wait_or(&bfree[bb], ((g / kBBufs) - 1) & 1, &s_fail)) { s_fail = 1; break; }
+        const uint8_t* codes = raw + s * kRawBytes + kAStage;
+        const uint8_t* scales = codes + kCodeStage;
+        uint8_t* bt = btile + bb * kBStage;
+        const int sub = (ks & 3) * 4;  // this K-step's 4 scale bytes in each row's 16-byte box
+#pragma unroll
+        for (int q8 = 0; q8 < (kBN * 8) / (32 * kConvWarps); ++q8) {
+          const int q = ct + 32 * kConvWarps * q8;
+          const int r = q >> 3, j = q & 7;
+          const uint32_t c4 = *reinterpret_cast<const uint32_t*>(codes + r * 32 + j * 4);
+          const uint32_t s2 = e4m3_to_f16x2_both(scales[r * 16 + sub + (j >> 1)]);
+          *reinterpret_cast<uint4*>(bt + r * 128 + ((j ^ (r & 7)) << 4)) = dequant8_f16(c4, s2);
+        }
+        fence_proxy_async_smem();  // generic-proxy writes -> the tensor core's async-proxy reads
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&conv[bb]);
+      }
+    }
+  } else {
+    // epilogue: warp w reads TMEM lanes 32 * (w % 4) .. + 31, i.e. tile rows
+    const int q = warp & 3;
+    int i = 0;
+    for (int t = blockIdx.x; t < n_tiles && !s_fail; t += gridDim.x, ++i) {
+      const int ab = i & 1;
+      if (!mbar_wait_or(&acc_full[ab], (i >> 1) & 1, &s_fail, 4000000000ull)) { s_fail = 1; break; }
       tc_fence_after();
-      const int r = q * 32 + lane;
-      const int row = t.row0 + r;
-      if (ok && !s_fail) epi(tmem + ((uint32_t)(q * 32) << 16), row, row < t.row_end, t.nb);
-      if (!ok) s_fail = 1;
+      const Tile tl = tile_of(tile_base, offsets, E, nblocks_n, t);
+      const int row = tl.row0 + q * 32 + lane;
+      epi(tmem + (uint32_t)(ab * kAccCols) + ((uint32_t)(q * 32) << 16), row, row < tl.row_end, tl.nb);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_empty[ab]);
     }
   }
   tc_fence_before();
   __syncthreads();
   if (s_fail && threadIdx.x == 0) atomicExch(err, MOE_ERR_TIMEOUT);
-  if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 2 * kAccCols);
+  }
 }
 
 }  // namespace tc

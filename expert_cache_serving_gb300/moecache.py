@@ -42,7 +42,7 @@ class moe_stats(ctypes.Structure):
                 ("prefill_gemm_ms", ctypes.c_double), ("prefill_gemm_flop", ctypes.c_double),
                 ("deferred_calls", ctypes.c_int64), ("finish_launches", ctypes.c_int64),
                 ("pdl_launches", ctypes.c_int64), ("prefill_records_streamed", ctypes.c_int64),
-                ("prefill_records_in_place", ctypes.c_int64)]
+                ("prefill_records_in_place", ctypes.c_int64), ("qstar_fills", ctypes.c_int64)]
 
     def as_dict(self):
         return {name: getattr(self, name) for name, _ in self._fields_}
@@ -56,7 +56,8 @@ class moe_event(ctypes.Structure):
 
 class moe_layer_aux(ctypes.Structure):
     _fields_ = [("ids", ctypes.c_void_p), ("weights", ctypes.c_void_p), ("slots", ctypes.c_void_p),
-                ("perm", ctypes.c_void_p), ("offsets", ctypes.c_void_p), ("logits", ctypes.c_void_p)]
+                ("perm", ctypes.c_void_p), ("offsets", ctypes.c_void_p), ("logits", ctypes.c_void_p),
+                ("qstar", ctypes.c_void_p)]
 
 
 class moe_prefill_aux(ctypes.Structure):
@@ -66,7 +67,7 @@ class moe_prefill_aux(ctypes.Structure):
 
 class moe_phase_times(ctypes.Structure):
     _fields_ = [("calls_hit_only", ctypes.c_int64), ("calls_with_fills", ctypes.c_int64),
-                ("hit_only_us", ctypes.c_double * 12), ("with_fills_us", ctypes.c_double * 12)]
+                ("hit_only_us", ctypes.c_double * 16), ("with_fills_us", ctypes.c_double * 16)]
 
     def as_dict(self):
         return {"calls_hit_only": self.calls_hit_only, "calls_with_fills": self.calls_with_fills,
@@ -88,6 +89,7 @@ SIGNATURES = {
     "moe_cache_stats": (_I32, [_P, ctypes.POINTER(moe_stats)]),
     "moe_cache_sync": (_I32, [_P, _P]),
     "moe_cache_set_wait_limit_ns": (_I32, [_P, _I64, _I64]),
+    "moe_cache_set_split_bandwidths": (_I32, [_P, ctypes.c_double, ctypes.c_double]),
     "moe_cache_reset_stats": (_I32, [_P]),
     "moe_cache_set_profiling": (_I32, [_P, _I32]),
     "moe_cache_phase_times": (_I32, [_P, ctypes.POINTER(moe_phase_times)]),
@@ -198,6 +200,10 @@ def moe_cache_sync(cache: int, stream=None) -> int:
 
 def moe_cache_set_wait_limit_ns(cache: int, gate_up_ns: int, down_ns: int) -> None:
     check(lib.moe_cache_set_wait_limit_ns(cache, int(gate_up_ns), int(down_ns)), "moe_cache_set_wait_limit_ns")
+
+
+def moe_cache_set_split_bandwidths(cache: int, b_p: float, b_h: float) -> None:
+    check(lib.moe_cache_set_split_bandwidths(cache, float(b_p), float(b_h)), "moe_cache_set_split_bandwidths")
 
 
 def moe_cache_reset_stats(cache: int) -> None:

@@ -115,6 +115,7 @@ typedef struct {
   int64_t pdl_launches;      /* layer-kernel launches made as programmatic dependents of the previous launch */
   int64_t prefill_records_streamed;  /* expert records moe_prefill_stream copied into its buffers */
   int64_t prefill_records_in_place;  /* expert records it read where they were already resident */
+  int64_t qstar_fills;       /* sum over calls of q*, the fill count of the bandwidth split */
 } moe_stats;
 
 typedef struct {
@@ -136,6 +137,7 @@ typedef struct {
   int32_t* perm;     /* [B*k] flat pair indices t*k+j grouped by expert (stable) */
   int32_t* offsets;  /* [E+1] start of each expert's group in perm */
   float* logits;     /* [B][E] router logits actually used (float32) */
+  int32_t* qstar;    /* [1] q*: how many of the call's misses the bandwidth split fills */
 } moe_layer_aux;
 
 typedef struct moe_cache* moe_cache_t;
@@ -260,6 +262,17 @@ moe_status moe_cache_sync(moe_cache_t cache, void* stream);
  * pass over the fills.  Errors: MOE_ERR_INVALID_ARG (negative or above 60 s). */
 moe_status moe_cache_set_wait_limit_ns(moe_cache_t cache, int64_t gate_up_ns, int64_t down_ns);
 
+/* Bandwidths of the fill / host-execution split ("measured bandwidths decide
+ * the split" in the FreeToken write-up): with m misses in a call, the layer
+ * kernel derives q* = m * b_p / b_h rounded to the nearest integer (halves
+ * up), clamped to [1, m], q* = m when b_h <= b_p, 0 when m = 0; b_p is the
+ * measured host-to-device expert-transfer bandwidth, b_h the host's expert
+ * execution bandwidth, any unit.  This library has no host execution branch:
+ * every miss is still filled, and q* is reported (moe_layer_aux.qstar,
+ * moe_stats.qstar_fills) for the split a hybrid engine would take.  Both 0
+ * (the default) means q* = m.  Errors: MOE_ERR_INVALID_ARG (negative). */
+moe_status moe_cache_set_split_bandwidths(moe_cache_t cache, double b_p, double b_h);
+
 /* Counters since creation (or the last reset).  Synchronises the events of
  * profiled launches and reads the summaries of calls in flight. */
 moe_status moe_cache_stats(moe_cache_t cache, moe_stats* out);
@@ -272,16 +285,18 @@ moe_status moe_cache_set_profiling(moe_cache_t cache, int32_t on);
 
 /* Mean time, in microseconds after the layer kernel starts, at which a call
  * reaches each phase, over the calls profiled at level 2 (split by whether
- * the call had fills).  Stamps: 0 start, 1 plan visible to all CTAs, 2 gate/up
- * rows of resident experts done, 3 first grid barrier passed, 4 W_down rows of
- * resident experts done, 5 first fill's first half landed, 6 gate/up rows of
- * the fills done, 7 second grid barrier passed, 8 last fill's second half
- * landed, 9 end, 10 control step done, 11 victim list maintained.  A call that
- * never reaches a stamp does not count towards it. */
+ * the call had fills), as seen by CTA 1 unless noted.  Stamps: 0 start, 1
+ * routing and lookup done, 2 gate/up rows of the resident experts streamed, 3
+ * first wave of W_down rows started, 4 W_down rows of the resident experts
+ * done, 5 first fill's first half landed, 6 gate/up rows of the fills done, 7
+ * plan of the fills read, 8 last fill's second half landed, 9 end, 10 control
+ * CTA: victims and plan written, 11 control CTA: recency committed, 12 router
+ * done, 13 residency row in shared memory, 14 lookups and grouping done,
+ * 15 unused.  A call that never reaches a stamp does not count towards it. */
 typedef struct {
   int64_t calls_hit_only, calls_with_fills;
-  double hit_only_us[12];
-  double with_fills_us[12];
+  double hit_only_us[16];
+  double with_fills_us[16];
 } moe_phase_times;
 moe_status moe_cache_phase_times(moe_cache_t cache, moe_phase_times* out);
 

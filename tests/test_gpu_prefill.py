@@ -201,7 +201,7 @@ def test_prefill_seeds_decode_and_reads_resident_experts_in_place():
 def test_long_prompt_runs_in_chunks():
     from expert_cache_serving_gb300 import moecache as mc
 
-    w = configs.SMALL_BF16.with_(L=2, E=16, k=4, C=40)
+    w = configs.SMALL_BF16.with_(L=3, E=16, k=4, C=40)
     T = 8192 + 300
     layers = [0, 1]
     cache, xs, lg, y, _ = run_prefill(w, T, layers, C=w.C)
