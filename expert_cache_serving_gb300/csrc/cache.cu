@@ -1250,6 +1250,62 @@ static moe_status prefill_scratch(moe_cache* c, int T) {
   return MOE_OK;
 }
 
+// Victims for one on-demand prefill chunk on the host copy of the state, with
+// the decode rule: every expert of the chunk (ascending) gets stamp g + r; a
+// miss takes, among slots not holding a hit of the chunk, the empty slots
+// first (lowest index) then the oldest stamps.  Returns (slot, is_miss) per
+// expert and logs the events.
+static void host_access(moe_cache* c, int layer, const std::vector<int>& chunk, int32_t* owner, uint64_t* stamp,
+                        int32_t* map, uint64_t* g, std::vector<std::pair<int32_t, bool>>* out) {
+  const int64_t E = c->d.E, C = c->C;
+  std::vector<char> hit_slot(C, 0);
+  int n_miss = 0;
+  for (int e : chunk) {
+    const int32_t s = map[layer * E + e];
+    if (s >= 0) hit_slot[s] = 1; else ++n_miss;
+  }
+  std::vector<int64_t> victims;
+  if (n_miss > 0) {
+    std::vector<std::pair<std::pair<int, uint64_t>, int64_t>> cand;
+    cand.reserve(C);
+    for (int64_t s = 0; s < C; ++s) {
+      if (hit_slot[s]) continue;
+      cand.push_back(owner[s] < 0 ? std::make_pair(std::make_pair(0, (uint64_t)s), s)
+                                  : std::make_pair(std::make_pair(1, stamp[s]), s));
+    }
+    std::partial_sort(cand.begin(), cand.begin() + n_miss, cand.end());
+    for (int i = 0; i < n_miss; ++i) victims.push_back(cand[i].second);
+  }
+  out->clear();
+  int mi = 0;
+  for (size_t r = 0; r < chunk.size(); ++r) {
+    const int32_t key = (int32_t)(layer * E + chunk[r]);
+    int32_t s = map[key], evicted = -1;
+    const bool miss = s < 0;
+    if (miss) {
+      s = (int32_t)victims[mi++];
+      evicted = owner[s];
+      if (evicted >= 0) map[evicted] = -1;
+      owner[s] = key;
+      map[key] = s;
+    }
+    stamp[s] = *g + r;
+    out->push_back({s, miss});
+    if (c->tracing) {
+      moe_event ev{};
+      ev.call = c->call_index;
+      ev.layer = layer;
+      ev.expert = chunk[r];
+      ev.kind = miss ? MOE_EV_MISS : MOE_EV_HIT;
+      ev.slot = s;
+      ev.evicted_key = evicted;
+      c->trace.push_back(ev);
+    }
+  }
+  *g += chunk.size();
+  c->call_index += 1;
+}
+
 extern "C" moe_status moe_prefill_stream_ex(moe_cache_t c, int32_t layer_begin, int32_t layer_end, const void* x,
                                             const float* logits, int32_t T, void* y, void* stream,
                                             const moe_prefill_aux* aux) {
@@ -1263,9 +1319,9 @@ extern "C" moe_status moe_prefill_stream_ex(moe_cache_t c, int32_t layer_begin, 
   if (!x || !logits || !y) return fail(MOE_ERR_INVALID_ARG, "x, logits and y must be device pointers");
   if (d.I % 128 || d.H % 256) return fail(MOE_ERR_INVALID_ARG, "prefill needs I % 128 == 0 and H % 256 == 0");
   const int64_t E = d.E;
-  if (c->C < 2 * E)
-    return fail(MOE_ERR_CAPACITY, "prefill needs two full-layer buffers (%lld slots), the cache has %lld",
-                (long long)(2 * E), (long long)c->C);
+  if (c->C < 1) return fail(MOE_ERR_CAPACITY, "prefill needs at least one cache slot");
+  // two full-layer buffers when the pool holds them, else on demand
+  const bool on_demand = c->C < 2 * E;
   const int Tc = std::min<int>(T, kPrefillChunk), n_chunks = (T + kPrefillChunk - 1) / kPrefillChunk;
   if (aux && n_chunks > 1 && (aux->perm || aux->offsets || aux->slots))
     return fail(MOE_ERR_INVALID_ARG, "aux perm, offsets and slots need T <= %d", kPrefillChunk);
@@ -1282,12 +1338,8 @@ extern "C" moe_status moe_prefill_stream_ex(moe_cache_t c, int32_t layer_begin, 
   const int64_t buf0 = C - 2 * E;  // buffers: slots [C-2E, C-E) and [C-E, C)
   uint8_t* slots = (uint8_t*)c->slots.base;
 
-  // ---- the cache's bookkeeping for the whole call, on the host: the state
-  // after every earlier call of this cache, the buffers carved out, then per
-  // step (chunk, layer) where each expert is read from and which experts
-  // stream (the rule of the FreeToken write-up's full-layer double buffering:
-  // resident experts are read in place, the rest stream into their buffer
-  // slot, and the buffer contents stay cached afterwards to seed decode)
+  // ---- the cache's bookkeeping for the whole call, on a host copy of the
+  // state after every earlier call of this cache
   CU_TRY(cudaStreamSynchronize(s));
   CU_TRY(cudaStreamSynchronize(c->copy));
   if (moe_status e = prefill_staging(c)) return e;
@@ -1298,62 +1350,74 @@ extern "C" moe_status moe_prefill_stream_ex(moe_cache_t c, int32_t layer_begin, 
   CU_TRY(cudaMemcpy(stamp, c->d_stamp, sizeof(uint64_t) * C, cudaMemcpyDeviceToHost));
   CU_TRY(cudaMemcpy(map, c->d_map, sizeof(int32_t) * LE, cudaMemcpyDeviceToHost));
   CU_TRY(cudaMemcpy(pf.h_g, c->d_g, sizeof(uint64_t), cudaMemcpyDeviceToHost));
-  for (int64_t sl = buf0; sl < C; ++sl) {
-    const int32_t key = owner[sl];
-    if (key < 0) continue;
-    if (c->tracing) {
-      moe_event ev{};
-      ev.call = c->call_index;
-      ev.layer = key / (int32_t)E;
-      ev.expert = key % (int32_t)E;
-      ev.kind = MOE_EV_PREFILL_EVICT;
-      ev.slot = (int32_t)sl;
-      ev.evicted_key = key;
-      c->trace.push_back(ev);
-    }
-    map[key] = -1;
-    owner[sl] = -1;
-    stamp[sl] = 0;
-  }
-  std::vector<int32_t> tab((size_t)n_steps * E);
-  std::vector<std::vector<std::pair<int, int>>> runs(n_steps);  // streamed expert ranges [e0, e1)
-  std::vector<char> wait_prev(n_steps, 0);
-  int64_t streamed = 0;
-  uint64_t g = *pf.h_g;
-  for (int i = 0; i < n_steps; ++i) {
-    const int l = layer_begin + i % n_layers, b = i & 1;
-    int run0 = -1;
-    for (int e = 0; e < (int)E; ++e) {
-      const int32_t key = (int32_t)(l * E + e);
-      int64_t sl = map[key];
-      const bool stream_it = sl < 0;
-      if (stream_it) {
-        sl = buf0 + b * E + e;
-        if (owner[sl] >= 0) map[owner[sl]] = -1;
-        owner[sl] = key;
-        map[key] = (int32_t)sl;
-        ++streamed;
-        if (run0 < 0) run0 = e;
-      } else if (run0 >= 0) {
-        runs[i].push_back({run0, e});
-        run0 = -1;
+  if (moe_status e2 = prefill_tables(c, on_demand ? 1 : n_steps)) return e2;
+
+  // the double-buffered plan (the rule of the FreeToken write-up's full-layer
+  // double buffering): the buffers are carved out, then per step (chunk,
+  // layer) each expert is read in place if resident, else streamed into its
+  // buffer slot; the buffer contents stay cached afterwards to seed decode
+  std::vector<int32_t> tab;
+  std::vector<std::vector<std::pair<int, int>>> runs;  // streamed expert ranges [e0, e1) per step
+  std::vector<char> wait_prev;
+  int64_t streamed = 0, in_place = 0;
+  if (!on_demand) {
+    for (int64_t sl = buf0; sl < C; ++sl) {
+      const int32_t key = owner[sl];
+      if (key < 0) continue;
+      if (c->tracing) {
+        moe_event ev{};
+        ev.call = c->call_index;
+        ev.layer = key / (int32_t)E;
+        ev.expert = key % (int32_t)E;
+        ev.kind = MOE_EV_PREFILL_EVICT;
+        ev.slot = (int32_t)sl;
+        ev.evicted_key = key;
+        c->trace.push_back(ev);
       }
-      stamp[sl] = g + (uint64_t)e;
-      tab[(size_t)i * E + e] = (int32_t)sl;
+      map[key] = -1;
+      owner[sl] = -1;
+      stamp[sl] = 0;
     }
-    if (run0 >= 0) runs[i].push_back({run0, (int)E});
-    g += (uint64_t)E;
-    // the copy of step i overwrites buffer slots that step i-1 may still read
-    if (i > 0)
-      for (auto [e0, e1] : runs[i])
-        for (int e = 0; e < (int)E && !wait_prev[i]; ++e) {
-          const int32_t r = tab[(size_t)(i - 1) * E + e];
-          if (r >= buf0 + b * E + e0 && r < buf0 + b * E + e1) wait_prev[i] = 1;
+    tab.resize((size_t)n_steps * E);
+    runs.resize(n_steps);
+    wait_prev.assign(n_steps, 0);
+    uint64_t g = *pf.h_g;
+    for (int i = 0; i < n_steps; ++i) {
+      const int l = layer_begin + i % n_layers, b = i & 1;
+      int run0 = -1;
+      for (int e = 0; e < (int)E; ++e) {
+        const int32_t key = (int32_t)(l * E + e);
+        int64_t sl = map[key];
+        if (sl < 0) {
+          sl = buf0 + b * E + e;
+          if (owner[sl] >= 0) map[owner[sl]] = -1;
+          owner[sl] = key;
+          map[key] = (int32_t)sl;
+          ++streamed;
+          if (run0 < 0) run0 = e;
+        } else {
+          ++in_place;
+          if (run0 >= 0) {
+            runs[i].push_back({run0, e});
+            run0 = -1;
+          }
         }
+        stamp[sl] = g + (uint64_t)e;
+        tab[(size_t)i * E + e] = (int32_t)sl;
+      }
+      if (run0 >= 0) runs[i].push_back({run0, (int)E});
+      g += (uint64_t)E;
+      // the copy of step i overwrites buffer slots that step i-1 may still read
+      if (i > 0)
+        for (auto [e0, e1] : runs[i])
+          for (int e = 0; e < (int)E && !wait_prev[i]; ++e) {
+            const int32_t r = tab[(size_t)(i - 1) * E + e];
+            if (r >= buf0 + b * E + e0 && r < buf0 + b * E + e1) wait_prev[i] = 1;
+          }
+    }
+    *pf.h_g = g;
+    CU_TRY(cudaMemcpyAsync(pf.tab, tab.data(), sizeof(int32_t) * tab.size(), cudaMemcpyHostToDevice, s));
   }
-  *pf.h_g = g;
-  if (moe_status e2 = prefill_tables(c, n_steps)) return e2;
-  CU_TRY(cudaMemcpyAsync(pf.tab, tab.data(), sizeof(int32_t) * tab.size(), cudaMemcpyHostToDevice, s));
 
   CU_TRY(cudaEventRecord(pf.start, s));
   CU_TRY(cudaStreamWaitEvent(c->copy, pf.start, 0));
@@ -1381,33 +1445,15 @@ extern "C" moe_status moe_prefill_stream_ex(moe_cache_t c, int32_t layer_begin, 
   auto done = [&](std::pair<cudaEvent_t, cudaEvent_t> ev, cudaStream_t on) {
     if (ev.second) cudaEventRecord(ev.second, on);
   };
-  const auto whole = timed(s, 0, 0.0);
-
-  for (int i = 0; i < n_steps; ++i) {
-    const int li = i % n_layers, ch = i / n_layers, l = layer_begin + li, b = i & 1;
-    const int t0 = ch * kPrefillChunk, Tn = std::min(Tc, T - t0);
-    const int Tk = Tn * k, n_pairs = Tk + (sh ? Tn : 0);
-    // stream the layer's missing experts into buffer b once the computes that
-    // read those slots have finished
-    if (i >= 2) CU_TRY(cudaStreamWaitEvent(c->copy, pf.consumed[b], 0));
-    if (wait_prev[i]) CU_TRY(cudaStreamWaitEvent(c->copy, pf.consumed[b ^ 1], 0));
-    const auto cp = timed(c->copy, 1, 0.0);
-    for (auto [e0, e1] : runs[i])
-      CU_TRY(cudaMemcpyAsync(slots + (buf0 + b * E + e0) * S, c->host_pool + ((int64_t)l * E + e0) * S,
-                             (int64_t)(e1 - e0) * S, cudaMemcpyHostToDevice, c->copy));
-    done(cp, c->copy);
-    CU_TRY(cudaEventRecord(pf.loaded[b], c->copy));
-
-    // routing, grouping and gather need no weights: they run while the copy lands
+  // routing, grouping and gather of one step (they need no weights)
+  auto front = [&](int li, int t0, int Tn, int n_pairs) -> moe_status {
     const float* lg = logits + ((int64_t)li * T + t0) * E;
     const uint8_t* xl = (const uint8_t*)x + ((int64_t)li * T + t0) * H * 2;
-    uint8_t* yl = (uint8_t*)y + ((int64_t)li * T + t0) * H * 2;
     CU_TRY(prefill_route(lg, Tn, (int)E, k, pf.ids, pf.w, s));
     CU_TRY(prefill_group(pf.ids, Tn, k, (int)E, sh, pf.cnt, pf.base, pf.offsets, pf.pos, pf.perm, s));
     CU_TRY(prefill_gather(xl, Tn, k, H, n_pairs, pf.perm, pf.xp, d.wdtype == MOE_FP4, s));  // FP4: f16 rows
-    const int32_t* tab_i = pf.tab + (size_t)i * E;
     if (aux) {
-      const int64_t at = ((int64_t)li * T + t0) * k;
+      const int64_t at = ((int64_t)li * T + t0) * k, Tk = (int64_t)Tn * k;
       if (aux->ids) CU_TRY(cudaMemcpyAsync(aux->ids + at, pf.ids, sizeof(int32_t) * Tk, cudaMemcpyDeviceToDevice, s));
       if (aux->weights)
         CU_TRY(cudaMemcpyAsync(aux->weights + at, pf.w, sizeof(float) * Tk, cudaMemcpyDeviceToDevice, s));
@@ -1417,46 +1463,131 @@ extern "C" moe_status moe_prefill_stream_ex(moe_cache_t c, int32_t layer_begin, 
       if (aux->offsets)
         CU_TRY(cudaMemcpyAsync(aux->offsets + (int64_t)li * (E + 1), pf.offsets, sizeof(int32_t) * (E + 1),
                                cudaMemcpyDeviceToDevice, s));
-      if (aux->slots)
-        CU_TRY(cudaMemcpyAsync(aux->slots + (int64_t)li * E, tab_i, sizeof(int32_t) * E, cudaMemcpyDeviceToDevice,
-                               s));
     }
-    CU_TRY(cudaStreamWaitEvent(s, pf.loaded[b], 0));
-    const auto comp = timed(s, 2, 0.0);
-    const uint8_t* srec = sh ? c->shared_dev + (int64_t)l * S : nullptr;
-    const double gemm_flop = 2.0 * n_pairs * (2.0 * I * H) + 2.0 * n_pairs * ((double)H * I);
-    const auto gm = timed(s, 3, gemm_flop);
+    return MOE_OK;
+  };
+  // the expert GEMMs of the groups whose table entry is a slot (and, with
+  // shared, the shared expert of layer l)
+  auto gemms = [&](const int32_t* tab_i, int l, int n_pairs, bool shared) -> moe_status {
+    const uint8_t* srec = shared ? c->shared_dev + (int64_t)l * S : nullptr;
     if (d.wdtype == MOE_FP4) {  // the GEMMs read the FP4 codes and scales where each expert sits
-      if (sh)
+      if (shared)
         if (moe_status e = map_fp4_layer(&sh_fp4, srec, 1, H, I, S)) return e;
       CU_TRY(prefill_gemm_gate_up_fp4(map_xp, pool_fp4.gu_c, pool_fp4.gu_s, pf.offsets, tab_i, (int)E, n_pairs, H, I,
                                       pf.hp, c->d_err, s));
-      if (sh)
+      if (shared)
         CU_TRY(prefill_gemm_gate_up_fp4(map_xp, sh_fp4.gu_c, sh_fp4.gu_s, pf.offsets + E, pf.zero, 1, n_pairs, H, I,
                                         pf.hp, c->d_err, s));
       CU_TRY(prefill_gemm_down_fp4(map_hp, pool_fp4.dn_c, pool_fp4.dn_s, pf.offsets, tab_i, (int)E, n_pairs, H, I,
                                    pf.op, c->d_err, s));
-      if (sh)
+      if (shared)
         CU_TRY(prefill_gemm_down_fp4(map_hp, sh_fp4.dn_c, sh_fp4.dn_s, pf.offsets + E, pf.zero, 1, n_pairs, H, I,
                                      pf.op, c->d_err, s));
     } else {
-      if (sh) {
+      if (shared) {
         if (moe_status e = map_weights(&bsgu, srec, 1, 2 * I, H, S)) return e;
         if (moe_status e = map_weights(&bsdn, srec + (int64_t)4 * H * I, 1, H, I, S)) return e;
       }
       CU_TRY(prefill_gemm_gate_up(map_xp, bgu, pf.offsets, tab_i, (int)E, n_pairs, H, I, pf.hp, c->d_err, s));
-      if (sh)
+      if (shared)
         CU_TRY(prefill_gemm_gate_up(map_xp, bsgu, pf.offsets + E, pf.zero, 1, n_pairs, H, I, pf.hp, c->d_err, s));
       CU_TRY(prefill_gemm_down(map_hp, bdn, pf.offsets, tab_i, (int)E, n_pairs, H, I, pf.op, c->d_err, s));
-      if (sh) CU_TRY(prefill_gemm_down(map_hp, bsdn, pf.offsets + E, pf.zero, 1, n_pairs, H, I, pf.op, c->d_err, s));
+      if (shared)
+        CU_TRY(prefill_gemm_down(map_hp, bsdn, pf.offsets + E, pf.zero, 1, n_pairs, H, I, pf.op, c->d_err, s));
     }
-    done(gm, s);
-    CU_TRY(cudaEventRecord(pf.consumed[b], s));  // buffer b may be refilled
-    CU_TRY(prefill_combine(pf.op, pf.pos, pf.w, Tn, k, H, sh, yl, s));
-    done(comp, s);
+    return MOE_OK;
+  };
+  const auto whole = timed(s, 0, 0.0);
+
+  if (!on_demand) {
+    for (int i = 0; i < n_steps; ++i) {
+      const int li = i % n_layers, ch = i / n_layers, l = layer_begin + li, b = i & 1;
+      const int t0 = ch * kPrefillChunk, Tn = std::min(Tc, T - t0);
+      const int n_pairs = Tn * k + (sh ? Tn : 0);
+      // stream the layer's missing experts into buffer b once the computes that
+      // read those slots have finished
+      if (i >= 2) CU_TRY(cudaStreamWaitEvent(c->copy, pf.consumed[b], 0));
+      if (wait_prev[i]) CU_TRY(cudaStreamWaitEvent(c->copy, pf.consumed[b ^ 1], 0));
+      const auto cp = timed(c->copy, 1, 0.0);
+      for (auto [e0, e1] : runs[i])
+        CU_TRY(cudaMemcpyAsync(slots + (buf0 + b * E + e0) * S, c->host_pool + ((int64_t)l * E + e0) * S,
+                               (int64_t)(e1 - e0) * S, cudaMemcpyHostToDevice, c->copy));
+      done(cp, c->copy);
+      CU_TRY(cudaEventRecord(pf.loaded[b], c->copy));
+      if (moe_status e = front(li, t0, Tn, n_pairs)) return e;
+      const int32_t* tab_i = pf.tab + (size_t)i * E;
+      if (aux && aux->slots)
+        CU_TRY(cudaMemcpyAsync(aux->slots + (int64_t)li * E, tab_i, sizeof(int32_t) * E, cudaMemcpyDeviceToDevice,
+                               s));
+      CU_TRY(cudaStreamWaitEvent(s, pf.loaded[b], 0));
+      const auto comp = timed(s, 2, 0.0);
+      const auto gm = timed(s, 3, 2.0 * n_pairs * (2.0 * I * H) + 2.0 * n_pairs * ((double)H * I));
+      if (moe_status e = gemms(tab_i, l, n_pairs, sh)) return e;
+      done(gm, s);
+      CU_TRY(cudaEventRecord(pf.consumed[b], s));  // buffer b may be refilled
+      CU_TRY(prefill_combine(pf.op, pf.pos, pf.w, Tn, k, H, sh, (uint8_t*)y + ((int64_t)li * T + t0) * H * 2, s));
+      done(comp, s);
+    }
+  } else {
+    // on demand: per step the layer's distinct routed experts, in chunks of
+    // at most C, each accessed like one decode call; a chunk's copies wait
+    // until the previous chunk's GEMMs no longer read the slots
+    std::vector<int32_t> h_off(E + 1), tab1(E);
+    std::vector<std::pair<int32_t, bool>> acc;
+    uint64_t g = *pf.h_g;
+    for (int i = 0; i < n_steps; ++i) {
+      const int li = i % n_layers, ch = i / n_layers, l = layer_begin + li;
+      const int t0 = ch * kPrefillChunk, Tn = std::min(Tc, T - t0);
+      const int n_pairs = Tn * k + (sh ? Tn : 0);
+      if (moe_status e = front(li, t0, Tn, n_pairs)) return e;
+      CU_TRY(cudaMemcpyAsync(h_off.data(), pf.offsets, sizeof(int32_t) * (E + 1), cudaMemcpyDeviceToHost, s));
+      CU_TRY(cudaStreamSynchronize(s));
+      std::vector<int> U;
+      for (int e = 0; e < (int)E; ++e)
+        if (h_off[e + 1] > h_off[e]) U.push_back(e);
+      std::vector<int32_t> layer_slots(E, -1);
+      const auto comp = timed(s, 2, 0.0);
+      for (size_t c0 = 0; c0 < U.size() || (c0 == 0 && sh); c0 += (size_t)C) {
+        std::vector<int> chunk(U.begin() + std::min(c0, U.size()), U.begin() + std::min(c0 + (size_t)C, U.size()));
+        host_access(c, l, chunk, owner, stamp, map, &g, &acc);
+        std::fill(tab1.begin(), tab1.end(), -1);
+        CU_TRY(cudaStreamWaitEvent(c->copy, pf.consumed[0], 0));  // the previous chunk's GEMMs are done
+        const auto cp = timed(c->copy, 1, 0.0);
+        for (size_t r = 0; r < chunk.size(); ++r) {
+          const auto [sl, miss] = acc[r];
+          tab1[chunk[r]] = sl;
+          layer_slots[chunk[r]] = sl;
+          if (miss) {
+            CU_TRY(cudaMemcpyAsync(slots + (int64_t)sl * S, c->host_pool + ((int64_t)l * E + chunk[r]) * S, S,
+                                   cudaMemcpyHostToDevice, c->copy));
+            ++streamed;
+          } else {
+            ++in_place;
+          }
+        }
+        done(cp, c->copy);
+        CU_TRY(cudaEventRecord(pf.loaded[0], c->copy));
+        CU_TRY(cudaMemcpyAsync(pf.tab, tab1.data(), sizeof(int32_t) * E, cudaMemcpyHostToDevice, s));
+        CU_TRY(cudaStreamWaitEvent(s, pf.loaded[0], 0));
+        int rows = 0;
+        for (int e : chunk) rows += h_off[e + 1] - h_off[e];
+        const int shared_rows = c0 == 0 && sh ? Tn : 0;
+        const auto gm = timed(s, 3, 2.0 * (rows + shared_rows) * (3.0 * I * H));
+        if (moe_status e = gemms(pf.tab, l, n_pairs, c0 == 0 && sh)) return e;
+        done(gm, s);
+        CU_TRY(cudaEventRecord(pf.consumed[0], s));
+        if (U.empty()) break;
+      }
+      if (aux && aux->slots)
+        CU_TRY(cudaMemcpyAsync(aux->slots + (int64_t)li * E, layer_slots.data(), sizeof(int32_t) * E,
+                               cudaMemcpyHostToDevice, s));
+      CU_TRY(prefill_combine(pf.op, pf.pos, pf.w, Tn, k, H, sh, (uint8_t*)y + ((int64_t)li * T + t0) * H * 2, s));
+      done(comp, s);
+    }
+    *pf.h_g = g;
   }
   done(whole, s);
-  // the cache after prefill: buffer contents become ordinary entries
+  // the cache after prefill: what the buffers (or the chunks) left stays cached
   CU_TRY(cudaMemcpyAsync(c->d_owner, owner, sizeof(int32_t) * C, cudaMemcpyHostToDevice, s));
   CU_TRY(cudaMemcpyAsync(c->d_stamp, stamp, sizeof(uint64_t) * C, cudaMemcpyHostToDevice, s));
   CU_TRY(cudaMemcpyAsync(c->d_map, map, sizeof(int32_t) * LE, cudaMemcpyHostToDevice, s));
@@ -1465,7 +1596,7 @@ extern "C" moe_status moe_prefill_stream_ex(moe_cache_t c, int32_t layer_begin, 
   c->st.prefill_layers += n_layers;
   c->st.prefill_tokens += (int64_t)T * n_layers;
   c->st.prefill_records_streamed += streamed;
-  c->st.prefill_records_in_place += (int64_t)n_steps * E - streamed;
+  c->st.prefill_records_in_place += in_place;
   return MOE_OK;
 }
 

@@ -14,7 +14,7 @@
 //
 // Deterministic rules (specified identically for the CPU reference simulator):
 //  * top-k by logit, descending, ties to the lower expert id (NaN counts as
-//    -inf); weights = softmax over the k selected logits;
+//    -inf, -0 as +0); weights = softmax over the k selected logits;
 //  * U = sorted distinct routed experts; the member of rank r gets stamp g + r,
 //    then g += |U|;
 //  * victims: among slots not holding a hit of this call, empty slots first by

@@ -166,21 +166,6 @@ __device__ void phase1(const LayerParams& p, const ItemTable& tb, int ib, int ie
     const int it = ib + (int)(task / I), i = (int)(task % I);
     const int ntok = tb.ntok[it];
     const RecView v = rec_view<WD>(tb.rec[it], H, I);
-    if constexpr (!FRESH && !WB) {
-      // this warp's next rows into L2 while it streams these: more bytes in
-      // flight than its registers hold (resident slots only)
-      const int64_t nx = task + grp.nw;
-      if (lane == 0 && nx < t1) {
-        const int it2 = ib + (int)(nx / I), i2 = (int)(nx % I);
-        const RecView v2 = rec_view<WD>(tb.rec[it2], H, I);
-        prefetch_l2(v2.gate + (int64_t)i2 * rb, (uint32_t)rb);
-        prefetch_l2(v2.up + (int64_t)i2 * rb, (uint32_t)rb);
-        if (WD == MOE_FP4) {
-          prefetch_l2(v2.gate_sc + (int64_t)i2 * (H / 16), (uint32_t)(H / 16));
-          prefetch_l2(v2.up_sc + (int64_t)i2 * (H / 16), (uint32_t)(H / 16));
-        }
-      }
-    }
     const uint8_t* grow = v.gate + (int64_t)i * rb;
     const uint8_t* urow = v.up + (int64_t)i * rb;
     const uint8_t* gsc = (WD == MOE_FP4) ? v.gate_sc + (int64_t)i * (H / 16) : nullptr;

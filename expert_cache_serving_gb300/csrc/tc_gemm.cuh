@@ -126,11 +126,13 @@ struct Tile {
 };
 
 // Tiles are enumerated expert-major, then row block, then column block; the
-// grid is sized for the worst case and CTAs past the last tile exit.
-__device__ __forceinline__ bool find_tile(const int32_t* offsets, int E, int nblocks_n, int cta, Tile* t) {
+// grid is sized for the worst case and CTAs past the last tile exit.  Groups
+// whose slot is negative are skipped (not part of this launch).
+__device__ __forceinline__ bool find_tile(const int32_t* offsets, const int32_t* slot_of, int E, int nblocks_n,
+                                          int cta, Tile* t) {
   int base = 0;
   for (int e = 0; e < E; ++e) {
-    const int n = offsets[e + 1] - offsets[e];
+    const int n = slot_of[e] < 0 ? 0 : offsets[e + 1] - offsets[e];
     const int mt = (n + kBM - 1) / kBM;
     const int cnt = mt * nblocks_n;
     if (cta < base + cnt) {
@@ -211,7 +213,7 @@ __device__ void grouped_gemm_cta(const CUtensorMap* map_a, const CUtensorMap* ma
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    s_has = find_tile(offsets, E, nblocks_n, blockIdx.x, &s_tile) ? 1 : 0;
+    s_has = find_tile(offsets, slot_of, E, nblocks_n, blockIdx.x, &s_tile) ? 1 : 0;
     s_fail = 0;
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&full[s], 1);
@@ -299,10 +301,19 @@ __device__ void grouped_gemm_cta(const CUtensorMap* map_a, const CUtensorMap* ma
 // producer, 1 MMA issuer (and TMEM owner), 2..17 converters, 18..21 epilogue
 // (warp w reads TMEM lanes 32 * (w % 4) .. + 31).  Every wait is bounded and
 // also gives up once another role has failed; TMEM is freed on every path.
+#ifndef MOE_FP4_RAW_STAGES
+#define MOE_FP4_RAW_STAGES 5
+#endif
+#ifndef MOE_FP4_B_BUFFERS
+#define MOE_FP4_B_BUFFERS 2
+#endif
+#ifndef MOE_FP4_CONV_WARPS
+#define MOE_FP4_CONV_WARPS 16
+#endif
 namespace fp4 {
-constexpr int kRaw = 5;
-constexpr int kBBufs = 2;
-constexpr int kConvWarps = 16;
+constexpr int kRaw = MOE_FP4_RAW_STAGES;
+constexpr int kBBufs = MOE_FP4_B_BUFFERS;
+constexpr int kConvWarps = MOE_FP4_CONV_WARPS;
 constexpr int kEpiWarps = 4;
 constexpr int kConv0 = 2, kEpi0 = kConv0 + kConvWarps;
 constexpr int kThreads = 32 * (kEpi0 + kEpiWarps);
@@ -316,6 +327,8 @@ constexpr int kAccCols = 256;               // one accumulator; two of them fill
 constexpr int kMaxE = 1024;
 constexpr size_t kSmemBytes = (size_t)kBBufs * kBStage + (size_t)kRaw * kRawBytes + 1024 /*align*/ + 256 /*barriers*/;
 static_assert(kRawBytes % 1024 == 0 && kBStage % 1024 == 0, "tiles must keep the 1024-byte swizzle alignment");
+static_assert(kSmemBytes + 8 * 1024 <= 227 * 1024, "rings must fit the opt-in shared memory");
+static_assert((kBN * 8) % (32 * kConvWarps) == 0, "converter warps must split a B tile evenly");
 }  // namespace fp4
 
 // kind::f16 instruction descriptor: f16 x f16 -> f32, both K-major, M x N.
@@ -387,7 +400,8 @@ __device__ __forceinline__ Tile tile_of(const int* tile_base, const int32_t* off
 
 // A: 2D f16 map over [rows][K]; codes: 3D u8 map over [records][Nrows][K/2]
 // (box 32 bytes x 128 rows); scales: 3D u8 map over [records][Nrows][K/16]
-// (box 16 x 128); group e's weights are record slot_of[e].
+// (box 16 x 128); group e's weights are record slot_of[e] (groups with a
+// negative slot are not part of this launch).
 template <typename Epi, typename BRow>
 __device__ void grouped_gemm_fp4_persistent(const CUtensorMap* map_a, const CUtensorMap* map_codes,
                                             const CUtensorMap* map_scales, const int32_t* offsets,
@@ -420,7 +434,7 @@ __device__ void grouped_gemm_fp4_persistent(const CUtensorMap* map_a, const CUte
     int base = 0;
     for (int e0 = 0; e0 < E; e0 += blockDim.x) {
       const int e = e0 + (int)threadIdx.x;
-      const int cnt = e < E ? (offsets[e + 1] - offsets[e] + kBM - 1) / kBM * nblocks_n : 0;
+      const int cnt = e < E && slot_of[e] >= 0 ? (offsets[e + 1] - offsets[e] + kBM - 1) / kBM * nblocks_n : 0;
       int tot;
       const int before = block_excl_scan(cnt, s_scan, &tot);
       if (e < E) tile_base[e] = base + before;

@@ -227,8 +227,15 @@ moe_status moe_layer_forward_ex(moe_cache_t cache, int32_t layer, const void* x,
  * FP4 weights expand exactly, the SwiGLU intermediate is rounded to f16).
  * The host waits once at the start for the cache's earlier work (it plans the
  * copies from the residency table); the rest is asynchronous on `stream`.
- * Errors: MOE_ERR_CAPACITY if the pool has fewer than 2*E slots,
- * MOE_ERR_INVALID_ARG, MOE_ERR_OOM, MOE_ERR_CUDA. */
+ * When the pool has fewer than 2*E slots the experts are loaded on demand
+ * instead (the pages' fallback, without oversubscribing GPU memory): per
+ * layer the host reads which experts the tokens route to (one wait per
+ * layer), and accesses them in ascending order in chunks of at most n_slots,
+ * each chunk like one decode call (hits refresh recency, misses take victims
+ * and are copied in, logged as MOE_EV_HIT / MOE_EV_MISS), then evaluates the
+ * chunk before the next one may evict it.
+ * Errors: MOE_ERR_CAPACITY (no slots at all), MOE_ERR_INVALID_ARG,
+ * MOE_ERR_OOM, MOE_ERR_CUDA. */
 moe_status moe_prefill_stream(moe_cache_t cache, int32_t layer_begin, int32_t layer_end, const void* x,
                               const float* logits, int32_t T, void* y, void* stream);
 
@@ -239,7 +246,8 @@ typedef struct {
   float* weights;    /* [n_layers][T][k] routing weights */
   int32_t* perm;     /* [n_layers][T*k] flat pairs t*k+j grouped by expert (stable) */
   int32_t* offsets;  /* [n_layers][E+1] start of each expert's group in perm */
-  int32_t* slots;    /* [n_layers][E] cache slot each expert of the layer was read from */
+  int32_t* slots;    /* [n_layers][E] cache slot each expert of the layer was read from (on demand: -1 when
+                        no token routes to it) */
 } moe_prefill_aux;
 
 /* moe_prefill_stream with optional inspection outputs (aux may be NULL). */

@@ -42,6 +42,9 @@ Readings where the pages are silent (each one is a plain deterministic choice):
   way its stamp becomes g + e, then g += E.  The buffer slots keep what was
   last streamed into them: after prefill they are ordinary cache entries, so
   the last two layers' streamed experts seed decode.
+* Prefill with C < 2E (the pages' on-demand fallback, no oversubscription):
+  per layer, the distinct routed experts in ascending order are accessed in
+  consecutive chunks of at most C, each chunk exactly like one decode call.
 """
 
 from __future__ import annotations
@@ -207,6 +210,28 @@ class CacheSim:
                 table[i, e] = s
             self.g += E
         return events, table
+
+    # -- prefill when two full-layer buffers do not fit ----------------------
+    def prefill_on_demand(self, layer: int, ids: np.ndarray) -> tuple[list[Event], dict[int, int]]:
+        """One layer of a prefill whose cache cannot give two full-layer
+        buffers (C < 2E): the layer's distinct routed experts, ascending, are
+        accessed in consecutive chunks of at most C, each chunk exactly like
+        one decode call (hits refresh recency, misses take victims by the
+        usual rule and are loaded); the chunk's experts are evaluated before
+        the next chunk may evict them.  Returns the events and the slot every
+        expert of the layer was read from.
+        """
+        U = sorted(set(int(e) for e in np.asarray(ids).reshape(-1)))
+        if self.C < 1 and U:
+            raise CapacityError("prefill needs at least one slot")
+        events, slot_of = [], {}
+        for c0 in range(0, len(U), max(1, self.C)):
+            chunk = np.array(U[c0:c0 + self.C], dtype=np.int64).reshape(1, -1)
+            ev, slots = self.access(layer, chunk)
+            events += ev
+            for e, s in zip(chunk.reshape(-1), slots.reshape(-1)):
+                slot_of[int(e)] = int(s)
+        return events, slot_of
 
     def resident_keys(self) -> set[int]:
         return {int(k) for k in self.owner if k >= 0}

@@ -144,13 +144,47 @@ def test_prefill_routing_grouping_and_slots_bit_exact():
     cache.close()
 
 
-def test_prefill_needs_two_full_layer_buffers():
+@pytest.mark.parametrize("w,C", [(configs.SMALL_BF16.with_(B=1, steps=4), 20),
+                                 (configs.SMALL_FP4_NARROW.with_(B=1, steps=4), 7)], ids=["bf16", "fp4"])
+def test_prefill_on_demand_when_two_buffers_do_not_fit(w, C):
+    # C < 2E: each layer's routed experts are loaded in chunks of at most C,
+    # each chunk like one decode call, then evaluated
     from expert_cache_serving_gb300 import moecache as mc
+    from expert_cache_serving_gb300 import runner
 
-    w = configs.SMALL_BF16
-    with pytest.raises(AssertionError):
-        run_prefill(w, 16, [0], C=2 * w.E - 1)
-    assert "two full-layer buffers" in mc.moe_last_error()
+    w = w.with_(C=C)
+    pool, shared = runner.build_pool(w), runner.build_shared(w)
+    calls = H.decode_calls(w, 2)
+    lg = H.trace_logits(w, 2)
+    dev = torch.device("cuda")
+    cache = runner.Cache(w, pool, shared)
+    mc.moe_cache_set_trace(cache.handle, True)
+    y = torch.empty((w.B, w.H), dtype=torch.bfloat16, device=dev)
+    sim = lru.CacheSim(w.L, w.E, w.C)
+    events = []
+    for s, l in calls:  # some decode first, so some experts are resident
+        assert cache.forward(l, runner.activations(w, s, l).to(dev), torch.from_numpy(lg[s, l]).to(dev), y, 1) == 0
+        ev, _ = sim.access(l, router.topk_softmax(lg[s, l].astype(np.float64), w.k)[0])
+        events += [e.as_tuple() for e in ev]
+    layers = [0, 1]
+    _, xs, plg, yp, got = run_prefill(w, 48, layers, C=w.C, aux=True, cache=cache)
+    for li, l in enumerate(layers):
+        ids, _ = router.topk_softmax(plg[li].astype(np.float64), w.k)
+        ev, slot_of = sim.prefill_on_demand(l, ids)
+        events += [e.as_tuple() for e in ev]
+        want = np.full(w.E, -1)
+        for e, s in slot_of.items():
+            want[e] = s
+        assert (got["slots"][li] == want).all(), f"layer {l}: slots"
+    ref = oracle_prefill(w, xs, plg, layers, H.ExpertBank(w))
+    for li in range(len(layers)):
+        H.assert_layer_close(yp[li], ref[li], f"prefill layer {layers[li]}")
+    assert [tuple(e) for e in mc.moe_cache_trace(cache.handle)] == events
+    owner, stamp, n, g = mc.moe_cache_state(cache.handle, w.C)
+    assert (owner == sim.owner).all() and g == sim.g
+    occ = owner >= 0
+    assert (stamp[occ] == sim.stamp[occ]).all()
+    cache.close()
 
 
 def test_prefill_seeds_decode_and_reads_resident_experts_in_place():

@@ -331,3 +331,34 @@ def test_prefill_carves_buffers_and_logs_evictions():
     assert sim.map[0] == 0
     with pytest.raises(lru.CapacityError):
         lru.CacheSim(L, E, 3).prefill(0, 1)
+
+
+@pytest.mark.parametrize("seed", range(20))
+def test_on_demand_prefill_matches_list_lru_in_chunks(seed):
+    rng = random.Random(seed)
+    L, E = 3, 6
+    C = rng.randint(1, 2 * E - 1)
+    a, b = lru.CacheSim(L, E, C), ListLRU(L, E, C)
+    for _ in range(6):
+        layer = rng.randrange(L)
+        if rng.random() < 0.5:  # a prefill layer: many tokens routed
+            ids = np.array([[rng.randrange(E) for _ in range(2)] for _ in range(rng.randint(1, 8))])
+            ev, slot_of = a.prefill_on_demand(layer, ids)
+            U = sorted(set(ids.reshape(-1).tolist()))
+            evb = []
+            for c0 in range(0, len(U), C):  # the list LRU, chunk by chunk
+                evb += b.access(layer, np.array([U[c0:c0 + C]]))
+            assert [e.as_tuple() for e in ev] == evb
+            assert set(slot_of) == set(U)
+        else:
+            ids = np.array([[rng.randrange(E)]])
+            assert [e.as_tuple() for e in a.access(layer, ids)[0]] == b.access(layer, ids)
+
+
+def test_on_demand_prefill_is_one_call_when_the_layer_fits():
+    sim, ref = lru.CacheSim(2, 8, 10), lru.CacheSim(2, 8, 10)
+    ids = np.array([[3, 1], [1, 7], [5, 3]])
+    ev, slot_of = sim.prefill_on_demand(1, ids)
+    ev2, _ = ref.access(1, ids)
+    assert [e.as_tuple() for e in ev] == [e.as_tuple() for e in ev2] and sim.calls == 1
+    assert sorted(slot_of) == [1, 3, 5, 7]
