@@ -237,6 +237,7 @@ struct moe_cache {
   std::vector<Timed> pending;
   int inject_after = -1;
   int fill_mode = MOE_FILL_COPY;
+  int prefill_prec = MOE_PREFILL_W4A16;
   // phase timeline (profiling level 2): ring of [kTlRing][12] GPU timestamps
   int profile_level = 0;
   unsigned long long* d_tl = nullptr;
@@ -1123,6 +1124,29 @@ extern "C" moe_status moe_cache_set_fill_mode(moe_cache_t c, int32_t mode) {
   return MOE_OK;
 }
 
+extern "C" moe_status moe_cache_set_prefill_precision(moe_cache_t c, int32_t mode) {
+  if (!c) return fail(MOE_ERR_INVALID_ARG, "cache is NULL");
+  if (mode != MOE_PREFILL_W4A16 && mode != MOE_PREFILL_W4A4)
+    return fail(MOE_ERR_INVALID_ARG, "unknown prefill precision %d", mode);
+  if (mode == MOE_PREFILL_W4A4 && c->d.wdtype != MOE_FP4)
+    return fail(MOE_ERR_INVALID_ARG, "FP4 x FP4 prefill needs a MOE_FP4 model");
+  c->prefill_prec = mode;
+  return MOE_OK;
+}
+
+extern "C" moe_status moe_quantize_fp4(const void* x, int32_t x_dtype, int64_t rows, int32_t K, uint8_t* codes,
+                                       uint8_t* scales, void* stream) {
+  g_err.clear();
+  if (x_dtype != MOE_BF16 && x_dtype != MOE_FP32) return fail(MOE_ERR_INVALID_ARG, "x_dtype must be MOE_BF16 or MOE_FP32");
+  if (rows < 0 || K <= 0 || K % 16) return fail(MOE_ERR_INVALID_ARG, "need rows >= 0 and K a positive multiple of 16");
+  if (rows == 0) return MOE_OK;
+  if (!x || !codes || !scales) return fail(MOE_ERR_INVALID_ARG, "x, codes and scales must be device pointers");
+  if (((uintptr_t)codes & 7) || ((uintptr_t)x & (x_dtype == MOE_FP32 ? 3 : 1)))
+    return fail(MOE_ERR_INVALID_ARG, "codes must be 8-byte aligned and x aligned to its element size");
+  CU_TRY(quantize_rows(x, x_dtype == MOE_FP32, rows, K, codes, scales, (cudaStream_t)stream));
+  return MOE_OK;
+}
+
 extern "C" moe_status moe_cache_inject_fill_failure(moe_cache_t c, int32_t after) {
   if (!c) return fail(MOE_ERR_INVALID_ARG, "cache is NULL");
   c->inject_after = after;
@@ -1188,6 +1212,40 @@ static moe_status map_fp4_layer(Fp4Maps* m, const uint8_t* base, int n, int H, i
   if (moe_status e = map_fp4_scales(&m->gu_s, base + HI, n, 2 * I, H, S)) return e;
   if (moe_status e = map_fp4_codes(&m->dn_c, base + HI + HI / 8, n, H, I, S)) return e;
   return map_fp4_scales(&m->dn_s, base + HI + HI / 8 + HI / 2, n, H, I, S);
+}
+
+// FP4 x FP4 maps: packed codes with 128-byte boxes (one 256-element K stage)
+// in the 128-byte swizzle the MMA reads, block scales with 16-byte boxes.
+// Activations [rows][K/2] and [rows][K/16], boxes of 128 rows; weights
+// [n][rows][K/2] and [n][rows][K/16], boxes of 64 rows.
+static moe_status map_act_codes(CUtensorMap* m, const void* base, int64_t rows, int K) {
+  const uint64_t dims[2] = {(uint64_t)K / 2, (uint64_t)rows}, strides[1] = {(uint64_t)K / 2};
+  const uint32_t box[2] = {128, 128};
+  return encode_map(m, base, 2, dims, strides, box, CU_TENSOR_MAP_DATA_TYPE_UINT8, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+static moe_status map_act_scales(CUtensorMap* m, const void* base, int64_t rows, int K) {
+  const uint64_t dims[2] = {(uint64_t)K / 16, (uint64_t)rows}, strides[1] = {(uint64_t)K / 16};
+  const uint32_t box[2] = {16, 128};
+  return encode_map(m, base, 2, dims, strides, box, CU_TENSOR_MAP_DATA_TYPE_UINT8, CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+static moe_status map_w_codes64(CUtensorMap* m, const void* base, int n, int rows, int K, int64_t rec_stride) {
+  const uint64_t dims[3] = {(uint64_t)K / 2, (uint64_t)rows, (uint64_t)n};
+  const uint64_t strides[2] = {(uint64_t)K / 2, (uint64_t)rec_stride};
+  const uint32_t box[3] = {128, 64, 1};
+  return encode_map(m, base, 3, dims, strides, box, CU_TENSOR_MAP_DATA_TYPE_UINT8, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+static moe_status map_w_scales64(CUtensorMap* m, const void* base, int n, int rows, int K, int64_t rec_stride) {
+  const uint64_t dims[3] = {(uint64_t)K / 16, (uint64_t)rows, (uint64_t)n};
+  const uint64_t strides[2] = {(uint64_t)K / 16, (uint64_t)rec_stride};
+  const uint32_t box[3] = {16, 64, 1};
+  return encode_map(m, base, 3, dims, strides, box, CU_TENSOR_MAP_DATA_TYPE_UINT8, CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+static moe_status map_nvf4_layer(Fp4Maps* m, const uint8_t* base, int n, int H, int I, int64_t S) {
+  const int64_t HI = (int64_t)H * I;
+  if (moe_status e = map_w_codes64(&m->gu_c, base, n, 2 * I, H, S)) return e;
+  if (moe_status e = map_w_scales64(&m->gu_s, base + HI, n, 2 * I, H, S)) return e;
+  if (moe_status e = map_w_codes64(&m->dn_c, base + HI + HI / 8, n, H, I, S)) return e;
+  return map_w_scales64(&m->dn_s, base + HI + HI / 8 + HI / 2, n, H, I, S);
 }
 
 static constexpr int kPrefillChunk = 8192;  // tokens per pass over the layers (the pages' prefill chunk)
@@ -1422,14 +1480,30 @@ extern "C" moe_status moe_prefill_stream_ex(moe_cache_t c, int32_t layer_begin, 
   CU_TRY(cudaEventRecord(pf.start, s));
   CU_TRY(cudaStreamWaitEvent(c->copy, pf.start, 0));
   const int np_c = Tc * k + (sh ? Tc : 0);
-  CUtensorMap map_xp, map_hp;
-  if (moe_status e = map_rows(&map_xp, pf.xp, np_c, H)) return e;
-  if (moe_status e = map_rows(&map_hp, pf.hp, np_c, I)) return e;
+  // FP4 x FP4: the gathered rows and the SwiGLU output as codes then block
+  // scales in the same buffers
+  const bool w4a4 = d.wdtype == MOE_FP4 && c->prefill_prec == MOE_PREFILL_W4A4;
+  uint8_t* xq_c = (uint8_t*)pf.xp;
+  uint8_t* xq_s = xq_c + (int64_t)np_c * H / 2;
+  uint8_t* hq_c = (uint8_t*)pf.hp;
+  uint8_t* hq_s = hq_c + (int64_t)np_c * I / 2;
+  CUtensorMap map_xp, map_hp, map_xs, map_hs;
+  if (w4a4) {
+    if (moe_status e = map_act_codes(&map_xp, xq_c, np_c, H)) return e;
+    if (moe_status e = map_act_scales(&map_xs, xq_s, np_c, H)) return e;
+    if (moe_status e = map_act_codes(&map_hp, hq_c, np_c, I)) return e;
+    if (moe_status e = map_act_scales(&map_hs, hq_s, np_c, I)) return e;
+  } else {
+    if (moe_status e = map_rows(&map_xp, pf.xp, np_c, H)) return e;
+    if (moe_status e = map_rows(&map_hp, pf.hp, np_c, I)) return e;
+  }
   // weight maps over the whole slot pool (group e reads record tab[e]) and
   // over the shared expert's record of each layer
   Fp4Maps pool_fp4{}, sh_fp4{};
   CUtensorMap bgu{}, bdn{}, bsgu{}, bsdn{};
-  if (d.wdtype == MOE_FP4) {
+  if (w4a4) {
+    if (moe_status e = map_nvf4_layer(&pool_fp4, slots, (int)C, H, I, S)) return e;
+  } else if (d.wdtype == MOE_FP4) {
     if (moe_status e = map_fp4_layer(&pool_fp4, slots, (int)C, H, I, S)) return e;
   } else {
     if (moe_status e = map_weights(&bgu, slots, (int)C, 2 * I, H, S)) return e;
@@ -1451,7 +1525,10 @@ extern "C" moe_status moe_prefill_stream_ex(moe_cache_t c, int32_t layer_begin, 
     const uint8_t* xl = (const uint8_t*)x + ((int64_t)li * T + t0) * H * 2;
     CU_TRY(prefill_route(lg, Tn, (int)E, k, pf.ids, pf.w, s));
     CU_TRY(prefill_group(pf.ids, Tn, k, (int)E, sh, pf.cnt, pf.base, pf.offsets, pf.pos, pf.perm, s));
-    CU_TRY(prefill_gather(xl, Tn, k, H, n_pairs, pf.perm, pf.xp, d.wdtype == MOE_FP4, s));  // FP4: f16 rows
+    if (w4a4)
+      CU_TRY(prefill_gather_quant(xl, Tn, k, H, n_pairs, pf.perm, xq_c, xq_s, s));
+    else
+      CU_TRY(prefill_gather(xl, Tn, k, H, n_pairs, pf.perm, pf.xp, d.wdtype == MOE_FP4, s));  // FP4: f16 rows
     if (aux) {
       const int64_t at = ((int64_t)li * T + t0) * k, Tk = (int64_t)Tn * k;
       if (aux->ids) CU_TRY(cudaMemcpyAsync(aux->ids + at, pf.ids, sizeof(int32_t) * Tk, cudaMemcpyDeviceToDevice, s));
@@ -1470,7 +1547,20 @@ extern "C" moe_status moe_prefill_stream_ex(moe_cache_t c, int32_t layer_begin, 
   // shared, the shared expert of layer l)
   auto gemms = [&](const int32_t* tab_i, int l, int n_pairs, bool shared) -> moe_status {
     const uint8_t* srec = shared ? c->shared_dev + (int64_t)l * S : nullptr;
-    if (d.wdtype == MOE_FP4) {  // the GEMMs read the FP4 codes and scales where each expert sits
+    if (w4a4) {  // block-scaled FP4 x FP4 on the codes and scales where each expert sits
+      if (shared)
+        if (moe_status e = map_nvf4_layer(&sh_fp4, srec, 1, H, I, S)) return e;
+      CU_TRY(prefill_gemm_gate_up_nvf4(map_xp, map_xs, pool_fp4.gu_c, pool_fp4.gu_s, pf.offsets, tab_i, (int)E,
+                                       n_pairs, H, I, hq_c, hq_s, c->d_err, s));
+      if (shared)
+        CU_TRY(prefill_gemm_gate_up_nvf4(map_xp, map_xs, sh_fp4.gu_c, sh_fp4.gu_s, pf.offsets + E, pf.zero, 1,
+                                         n_pairs, H, I, hq_c, hq_s, c->d_err, s));
+      CU_TRY(prefill_gemm_down_nvf4(map_hp, map_hs, pool_fp4.dn_c, pool_fp4.dn_s, pf.offsets, tab_i, (int)E, n_pairs,
+                                    H, I, pf.op, c->d_err, s));
+      if (shared)
+        CU_TRY(prefill_gemm_down_nvf4(map_hp, map_hs, sh_fp4.dn_c, sh_fp4.dn_s, pf.offsets + E, pf.zero, 1, n_pairs,
+                                      H, I, pf.op, c->d_err, s));
+    } else if (d.wdtype == MOE_FP4) {  // the GEMMs read the FP4 codes and scales where each expert sits
       if (shared)
         if (moe_status e = map_fp4_layer(&sh_fp4, srec, 1, H, I, S)) return e;
       CU_TRY(prefill_gemm_gate_up_fp4(map_xp, pool_fp4.gu_c, pool_fp4.gu_s, pf.offsets, tab_i, (int)E, n_pairs, H, I,

@@ -88,6 +88,20 @@ cudaError_t prefill_gemm_gate_up_fp4(const CUtensorMap& a, const CUtensorMap& co
 cudaError_t prefill_gemm_down_fp4(const CUtensorMap& a, const CUtensorMap& codes, const CUtensorMap& scales,
                                   const int32_t* offsets, const int32_t* slot_of, int n_groups, int n_rows, int H,
                                   int I, float* op, int* err, cudaStream_t s);
+// FP4 x FP4 path: gathered rows quantised to codes [n_pairs][H/2] and block
+// scales [n_pairs][H/16]; block-scaled GEMMs (A and B maps of codes and scales)
+cudaError_t prefill_gather_quant(const void* x, int T, int k, int H, int n_pairs, const int32_t* perm, uint8_t* codes,
+                                 uint8_t* scales, cudaStream_t s);
+cudaError_t prefill_gemm_gate_up_nvf4(const CUtensorMap& ac, const CUtensorMap& as, const CUtensorMap& bc,
+                                      const CUtensorMap& bs, const int32_t* offsets, const int32_t* slot_of,
+                                      int n_groups, int n_rows, int H, int I, uint8_t* hc, uint8_t* hs, int* err,
+                                      cudaStream_t s);
+cudaError_t prefill_gemm_down_nvf4(const CUtensorMap& ac, const CUtensorMap& as, const CUtensorMap& bc,
+                                   const CUtensorMap& bs, const int32_t* offsets, const int32_t* slot_of, int n_groups,
+                                   int n_rows, int H, int I, float* op, int* err, cudaStream_t s);
+// rows of bf16 (fp32 = 0) or float32 values -> FP4 codes and block scales
+cudaError_t quantize_rows(const void* x, int fp32, int64_t rows, int K, uint8_t* codes, uint8_t* scales,
+                          cudaStream_t s);
 cudaError_t prefill_combine(const float* op, const int32_t* pos, const float* w, int T, int k, int H, int has_shared,
                             void* y, cudaStream_t s);
 

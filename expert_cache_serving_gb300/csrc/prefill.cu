@@ -11,6 +11,7 @@
 #include "expert_math.cuh"
 #include "params.cuh"
 #include "tc_gemm.cuh"
+#include "tc_nvf4.cuh"
 
 namespace moe {
 namespace pf {
@@ -156,6 +157,53 @@ __global__ void gather_kernel(const __nv_bfloat16* __restrict__ x, int Tk, int k
   }
 }
 
+// FP4 x FP4 path: the gathered rows quantised to e2m1 codes [n_pairs][H/2]
+// and e4m3 block scales [n_pairs][H/16]; one thread per 16-element block.
+__global__ void gather_quant_kernel(const __nv_bfloat16* __restrict__ x, int Tk, int k, int H, int n_pairs,
+                                    const int32_t* __restrict__ perm, uint8_t* __restrict__ codes,
+                                    uint8_t* __restrict__ scales) {
+  const int per = H / 16;
+  const int64_t total = (int64_t)n_pairs * per;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+    const int row = (int)(i / per), b = (int)(i % per);
+    const int p = perm[row];
+    const int t = p < Tk ? p / k : p - Tk;
+    const uint4* src = reinterpret_cast<const uint4*>(x + (int64_t)t * H + (int64_t)b * 16);
+    const uint4 v0 = src[0], v1 = src[1];
+    const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+    float f[16];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      f[2 * j] = bf16lo(w[j]);
+      f[2 * j + 1] = bf16hi(w[j]);
+    }
+    uint32_t c01[2];
+    scales[(int64_t)row * per + b] = (uint8_t)quant16(f, c01);
+    *reinterpret_cast<uint2*>(codes + (int64_t)row * (H / 2) + (int64_t)b * 8) = make_uint2(c01[0], c01[1]);
+  }
+}
+
+// Rows of bf16 or float32 values -> codes and scales (the library's quantiser).
+template <typename T>
+__global__ void quantize_kernel(const T* __restrict__ x, int64_t rows, int K, uint8_t* __restrict__ codes,
+                                uint8_t* __restrict__ scales) {
+  const int per = K / 16;
+  const int64_t total = rows * per;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t row = i / per;
+    const int b = (int)(i % per);
+    float f[16];
+    const T* src = x + row * K + (int64_t)b * 16;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      if constexpr (std::is_same<T, float>::value) f[j] = src[j];
+      else f[j] = __bfloat162float(src[j]);
+    }
+    uint32_t c01[2];
+    scales[row * per + b] = (uint8_t)quant16(f, c01);
+    *reinterpret_cast<uint2*>(codes + row * (K / 2) + (int64_t)b * 8) = make_uint2(c01[0], c01[1]);
+  }
+}
 
 // ---- 4/5. grouped GEMMs ----------------------------------------------------------------------
 struct BRowGateUp {
@@ -196,6 +244,34 @@ __global__ void __launch_bounds__(tc::fp4::kThreads, 1)
                          int n_groups, int H, int I, float* op, int* err) {
   tc::grouped_gemm_fp4_persistent(&map_a, &map_c, &map_s, offsets, slot_of, n_groups, H / 256, I,
                                   tc::EpiStoreF32{op, H}, BRowDown{}, err);
+}
+
+// FP4 x FP4 with block scales (activations quantised): 128-column blocks,
+// gate rows nb*64.. next to up rows I + nb*64..; down rows nb*128 + half*64..
+struct BRowGateUp64 {
+  int I;
+  __device__ int operator()(int nb, int half) const { return half ? I + nb * 64 : nb * 64; }
+};
+struct BRowDown64 {
+  __device__ int operator()(int nb, int half) const { return nb * 128 + half * 64; }
+};
+
+__global__ void __launch_bounds__(tc::nvf4::kThreads, 1)
+    gemm_gate_up_nvf4_kernel(const __grid_constant__ CUtensorMap map_ac, const __grid_constant__ CUtensorMap map_as,
+                             const __grid_constant__ CUtensorMap map_bc, const __grid_constant__ CUtensorMap map_bs,
+                             const int32_t* offsets, const int32_t* slot_of, int n_groups, int H, int I,
+                             uint8_t* hc, uint8_t* hs, int* err) {
+  tc::grouped_gemm_nvf4(&map_ac, &map_as, &map_bc, &map_bs, offsets, slot_of, n_groups, I / 64, H,
+                        tc::EpiSwiGLUQuant{hc, hs, I}, BRowGateUp64{I}, err);
+}
+
+__global__ void __launch_bounds__(tc::nvf4::kThreads, 1)
+    gemm_down_nvf4_kernel(const __grid_constant__ CUtensorMap map_ac, const __grid_constant__ CUtensorMap map_as,
+                          const __grid_constant__ CUtensorMap map_bc, const __grid_constant__ CUtensorMap map_bs,
+                          const int32_t* offsets, const int32_t* slot_of, int n_groups, int H, int I, float* op,
+                          int* err) {
+  tc::grouped_gemm_nvf4(&map_ac, &map_as, &map_bc, &map_bs, offsets, slot_of, n_groups, H / 128, I,
+                        tc::EpiStoreF32N128{op, H}, BRowDown64{}, err);
 }
 
 // ---- 6. combine ------------------------------------------------------------------------------
@@ -331,6 +407,59 @@ cudaError_t prefill_gemm_down_fp4(const CUtensorMap& a, const CUtensorMap& codes
   pf::gemm_down_fp4_kernel<<<persistent_grid(n_rows, n_groups, H / 256), tc::fp4::kThreads, tc::fp4::kSmemBytes,
                              s>>>(
       a, codes, scales, offsets, slot_of, n_groups, H, I, op, err);
+  return cudaGetLastError();
+}
+
+cudaError_t prefill_gather_quant(const void* x, int T, int k, int H, int n_pairs, const int32_t* perm, uint8_t* codes,
+                                 uint8_t* scales, cudaStream_t s) {
+  pf::gather_quant_kernel<<<sms() * 8, 256, 0, s>>>((const __nv_bfloat16*)x, T * k, k, H, n_pairs, perm, codes, scales);
+  return cudaGetLastError();
+}
+
+cudaError_t quantize_rows(const void* x, int fp32, int64_t rows, int K, uint8_t* codes, uint8_t* scales,
+                          cudaStream_t s) {
+  if (fp32)
+    pf::quantize_kernel<float><<<sms() * 8, 256, 0, s>>>((const float*)x, rows, K, codes, scales);
+  else
+    pf::quantize_kernel<__nv_bfloat16><<<sms() * 8, 256, 0, s>>>((const __nv_bfloat16*)x, rows, K, codes, scales);
+  return cudaGetLastError();
+}
+
+static bool g_gemm_nvf4_attr = false;
+static cudaError_t gemm_nvf4_attr() {
+  if (g_gemm_nvf4_attr) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(pf::gemm_gate_up_nvf4_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)tc::nvf4::kSmemBytes);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(pf::gemm_down_nvf4_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)tc::nvf4::kSmemBytes);
+  g_gemm_nvf4_attr = e == cudaSuccess;
+  return e;
+}
+
+// persistent grid for 128-row x 128-column tiles
+static int persistent_grid128(int n_rows, int n_groups, int nblocks_n) {
+  const int most = (n_rows / 128 + n_groups) * nblocks_n;
+  return most < sms() ? most : sms();
+}
+
+cudaError_t prefill_gemm_gate_up_nvf4(const CUtensorMap& ac, const CUtensorMap& as, const CUtensorMap& bc,
+                                      const CUtensorMap& bs, const int32_t* offsets, const int32_t* slot_of,
+                                      int n_groups, int n_rows, int H, int I, uint8_t* hc, uint8_t* hs, int* err,
+                                      cudaStream_t s) {
+  if (cudaError_t e = gemm_nvf4_attr()) return e;
+  pf::gemm_gate_up_nvf4_kernel<<<persistent_grid128(n_rows, n_groups, I / 64), tc::nvf4::kThreads,
+                                 tc::nvf4::kSmemBytes, s>>>(ac, as, bc, bs, offsets, slot_of, n_groups, H, I, hc, hs,
+                                                            err);
+  return cudaGetLastError();
+}
+
+cudaError_t prefill_gemm_down_nvf4(const CUtensorMap& ac, const CUtensorMap& as, const CUtensorMap& bc,
+                                   const CUtensorMap& bs, const int32_t* offsets, const int32_t* slot_of, int n_groups,
+                                   int n_rows, int H, int I, float* op, int* err, cudaStream_t s) {
+  if (cudaError_t e = gemm_nvf4_attr()) return e;
+  pf::gemm_down_nvf4_kernel<<<persistent_grid128(n_rows, n_groups, H / 128), tc::nvf4::kThreads,
+                              tc::nvf4::kSmemBytes, s>>>(ac, as, bc, bs, offsets, slot_of, n_groups, H, I, op, err);
   return cudaGetLastError();
 }
 

@@ -17,6 +17,7 @@ MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_OOM, MOE_ERR_CAPACITY, MOE_ERR_BUSY, MOE_ER
 MOE_FP32, MOE_BF16, MOE_FP4 = 0, 1, 2
 MOE_EV_HIT, MOE_EV_MISS, MOE_EV_RESIZE_EVICT, MOE_EV_PREFILL_EVICT = 0, 1, 2, 3
 MOE_FILL_COPY, MOE_FILL_DEVICE = 0, 1
+MOE_PREFILL_W4A16, MOE_PREFILL_W4A4 = 0, 1
 STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_OOM", 3: "MOE_ERR_CAPACITY",
                 4: "MOE_ERR_BUSY", 5: "MOE_ERR_CUDA", 6: "MOE_ERR_TIMEOUT"}
 
@@ -98,6 +99,8 @@ SIGNATURES = {
     "moe_cache_state": (_I32, [_P, _P, _P, _I64, ctypes.POINTER(_I64), ctypes.POINTER(ctypes.c_uint64)]),
     "moe_cache_slot_ptr": (_P, [_P, _I64]),
     "moe_cache_set_fill_mode": (_I32, [_P, _I32]),
+    "moe_cache_set_prefill_precision": (_I32, [_P, _I32]),
+    "moe_quantize_fp4": (_I32, [_P, _I32, _I64, _I32, _P, _P, _P]),
     "moe_cache_inject_fill_failure": (_I32, [_P, _I32]),
     "moe_layer_forward_resident_noalloc": (_I32, [ctypes.POINTER(moe_model_desc), _P, _P, _P, _P, _I32, _P, _P]),
     "moe_cache_destroy": (_I32, [_P]),
@@ -251,6 +254,15 @@ def moe_cache_slot_ptr(cache: int, s: int) -> int | None:
 
 def moe_cache_set_fill_mode(cache: int, mode: int) -> None:
     check(lib.moe_cache_set_fill_mode(cache, mode), "moe_cache_set_fill_mode")
+
+
+def moe_cache_set_prefill_precision(cache: int, mode: int) -> None:
+    check(lib.moe_cache_set_prefill_precision(cache, mode), "moe_cache_set_prefill_precision")
+
+
+def moe_quantize_fp4(x, x_dtype: int, rows: int, K: int, codes, scales, stream=None) -> None:
+    check(lib.moe_quantize_fp4(_ptr(x), x_dtype, rows, K, _ptr(codes), _ptr(scales), _stream(stream)),
+          "moe_quantize_fp4")
 
 
 def moe_cache_inject_fill_failure(cache: int, after: int) -> None:

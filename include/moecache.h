@@ -224,7 +224,8 @@ moe_status moe_layer_forward_ex(moe_cache_t cache, int32_t layer, const void* x,
  * models; prefill also needs I % 128 == 0 and H % 256 == 0.  The expert GEMMs
  * accumulate in float32; their operands are bf16 for MOE_BF16 models and f16
  * for MOE_FP4 models (the activations convert exactly for |x| <= 65504, the
- * FP4 weights expand exactly, the SwiGLU intermediate is rounded to f16).
+ * FP4 weights expand exactly, the SwiGLU intermediate is rounded to f16), or,
+ * after moe_cache_set_prefill_precision(MOE_PREFILL_W4A4), FP4 x FP4.
  * The host waits once at the start for the cache's earlier work (it plans the
  * copies from the residency table); the rest is asynchronous on `stream`.
  * When the pool has fewer than 2*E slots the experts are loaded on demand
@@ -336,6 +337,38 @@ const void* moe_cache_slot_ptr(moe_cache_t cache, int64_t s);
  * Errors: MOE_ERR_INVALID_ARG (unknown mode, pool not mapped). */
 enum { MOE_FILL_COPY = 0, MOE_FILL_DEVICE = 1 };
 moe_status moe_cache_set_fill_mode(moe_cache_t cache, int32_t mode);
+
+/* Arithmetic of moe_prefill_stream for MOE_FP4 models.
+ * MOE_PREFILL_W4A16 (default): the FP4 weights expand exactly to f16 and the
+ *   GEMMs run on f16 activations (see moe_prefill_stream).
+ * MOE_PREFILL_W4A4: the activations are quantised to the weights' own format
+ *   (the pages deploy MXFP4 / NVFP4 experts, FreeToken write-up, experimental
+ *   setup; they do not say how activations are treated, this is the reading
+ *   that lets both GEMM operands use the block-scaled FP4 tensor-core path):
+ *   the layer input x before the gate/up GEMM and the SwiGLU output h, rounded
+ *   to float32, before the down GEMM, each with moe_quantize_fp4's rule; the
+ *   GEMMs then run as block-scaled FP4 x FP4 products accumulating in float32.
+ *   Needs H and I multiples of 256 (the MOE_FP4 rule).
+ * The setting applies to later moe_prefill_stream calls; decode is unaffected.
+ * Errors: MOE_ERR_INVALID_ARG (unknown mode, or W4A4 for a model that is not
+ * MOE_FP4). */
+enum { MOE_PREFILL_W4A16 = 0, MOE_PREFILL_W4A4 = 1 };
+moe_status moe_cache_set_prefill_precision(moe_cache_t cache, int32_t mode);
+
+/* The FP4 quantiser of the W4A4 prefill, for rows of activations.
+ * Each block of 16 consecutive elements of a row gets one e4m3 scale
+ * s = e4m3(amax / 6) and each element the e2m1 code of v / s; both are
+ * rounded to nearest with ties to the even code and saturated to the largest
+ * finite value (448 and 6); amax / 6 and v / s are IEEE float32 divisions.
+ * A block whose scale rounds to 0 gets codes 0, and a value that rounds to
+ * magnitude 0 gets code 0 (never the negative zero 0x8).
+ * x: device [rows][K], bf16 (x_dtype MOE_BF16) or float32 (MOE_FP32), aligned
+ * to its element size; codes: device [rows][K/2], element 2c of a row in the
+ * low nibble of byte c, 8-byte aligned; scales: device [rows][K/16].  K a
+ * positive multiple of 16.  Asynchronous on `stream`; all buffers owned by
+ * the caller.  Errors: MOE_ERR_INVALID_ARG, MOE_ERR_CUDA (launch failure). */
+moe_status moe_quantize_fp4(const void* x, int32_t x_dtype, int64_t rows, int32_t K, uint8_t* codes,
+                            uint8_t* scales, void* stream);
 
 /* Test hook: the next fill copies of this cache fail after `after` successful
  * copies (-1 disables).  Used to check the rollback path without a GPU fault. */
