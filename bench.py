@@ -45,7 +45,8 @@ from synth import configs  # noqa: E402
 METRIC = "MoE decode tok/s + prefill tok/s; HBM GB/s (tensor %) vs peak; cache hit rate"
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
-ALL_LEGS = ("c2_device", "c3", "c4", "c5")
+ALL_LEGS = ("c2_device", "c3", "c4", "c4_w4a4", "c5")
+FP4_OVER_BF16 = 13.5 / 2.25  # nominal dense FP4 : bf16 tensor rate
 
 
 def load_peaks():
@@ -467,9 +468,10 @@ def decode_leg(inp, W, K, peak, b_p, fill_mode="copy", profile=True):
     return out, main
 
 
-def prefill_leg(w, pool, dev, W, K, peaks, peak_kind):
+def prefill_leg(w, pool, dev, W, K, peaks, peak_kind, w4a4=False, hbm_peak=FALLBACK_HBM_GBS):
     """Config 4: one T-token prompt through every layer of the FP4 model per
-    step, layer l+1's experts streamed host->device while layer l runs."""
+    step, layer l+1's experts streamed host->device while layer l runs.
+    w4a4: activations quantised to FP4 and block-scaled FP4 x FP4 GEMMs."""
     import torch
 
     from expert_cache_serving_gb300 import moecache as mc
@@ -482,6 +484,8 @@ def prefill_leg(w, pool, dev, W, K, peaks, peak_kind):
     logits = torch.from_numpy(synth.iid_logits(w.seed, L, T, w.E)).to(dev)
     y = torch.empty_like(x)
     cache = runner.Cache(w, pool, None, C=w.C, max_tokens=1)
+    if w4a4:
+        mc.moe_cache_set_prefill_precision(cache.handle, mc.MOE_PREFILL_W4A4)
     stream = torch.cuda.current_stream()
 
     def step():
@@ -515,18 +519,40 @@ def prefill_leg(w, pool, dev, W, K, peaks, peak_kind):
     gemm_tflops = st["prefill_gemm_flop"] / (st["prefill_gemm_ms"] / 1e3) / 1e12 if st["prefill_gemm_ms"] else None
     peak_tf = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops", FALLBACK_BF16_TFLOPS)))
     copy_bytes = L * w.E * S
+    roof = {"bound": "tensor", "achieved": gemm_tflops, "peak": peak_tf, "unit": "TFLOP/s",
+            "frac": gemm_tflops / peak_tf if gemm_tflops else None, "traffic": None,
+            "kernel": "grouped tcgen05 GEMMs (gate/up + down), weights resident in the layer buffer",
+            "peak_kind": peak_kind + " bf16 sustained (f16 dense rate is the same)",
+            "gemm_ms_per_step": st["prefill_gemm_ms"], "flop_per_step": st["prefill_gemm_flop"]}
+    dtype = "f16 operands (FP4 weights expanded exactly), fp32 accumulation"
+    if w4a4:
+        # per layer: every expert's weights once, the quantised activations and
+        # SwiGLU output once each way, the float32 down-GEMM rows written once
+        pairs = T * w.k + (T if w.shared else 0)
+        gemm_bytes = L * (w.E * S + pairs * (w.H + 2 * w.I) * 9 / 16 + pairs * w.H * 4)
+        fp4_peak = peak_tf * FP4_OVER_BF16
+        t = st["prefill_gemm_ms"] / 1e3 if st["prefill_gemm_ms"] else None
+        gbps = gemm_bytes / t / 1e9 if t else None
+        roof = {"bound": "hbm", "achieved": gbps, "peak": hbm_peak, "unit": "GB/s",
+                "frac": gbps / hbm_peak if gbps else None, "traffic": None,
+                "algorithmic_bytes_per_step": gemm_bytes,
+                "kernel": "block-scaled FP4 x FP4 tcgen05 GEMMs (kind::mxf4nvf4), weights resident in the layer buffer",
+                "peak_kind": peak_kind + " hbm_gbs (copy)",
+                "tensor": {"achieved_tflops": gemm_tflops, "peak_tflops": fp4_peak,
+                           "frac": gemm_tflops / fp4_peak if gemm_tflops else None,
+                           "peak_kind": peak_kind + " bf16 sustained x 6 (nominal FP4 : bf16 dense ratio)"},
+                "gemm_ms_per_step": st["prefill_gemm_ms"], "flop_per_step": st["prefill_gemm_flop"],
+                "note": "at ~96 rows per expert every weight byte feeds ~340 flop, below the FP4 ridge (~1,500 flop per byte): "
+                        "the GEMMs are bound by streaming the weights from HBM"}
+        dtype = "e2m1 x e2m1 with e4m3 block scales (activations quantised), fp32 accumulation"
     return {
         "value": value, "unit": "tok/s (prefill)", "ms_per_step": ms / K, "steps": K, "warmup": W,
-        "dtype": "f16 operands (FP4 weights expanded exactly), fp32 accumulation",
+        "dtype": dtype,
         "config": {"workload": w.name, "layers": L, "experts": w.E, "top_k": w.k, "hidden": w.H,
                    "intermediate": w.I, "prompt_tokens": T, "cache_slots": w.C, "record_bytes": S,
                    "step": "one prompt through all layers", "logits": "i.i.d. N(0,1) per (token, layer, expert)",
                    "l2": "each layer streams 3.6 GB of experts >> 129 MB L2; no flush"},
-        "roofline": {"bound": "tensor", "achieved": gemm_tflops, "peak": peak_tf, "unit": "TFLOP/s",
-                     "frac": gemm_tflops / peak_tf if gemm_tflops else None, "traffic": None,
-                     "kernel": "grouped tcgen05 GEMMs (gate/up + down), weights resident in the layer buffer",
-                     "peak_kind": peak_kind + " bf16 sustained (f16 dense rate is the same)",
-                     "gemm_ms_per_step": st["prefill_gemm_ms"], "flop_per_step": st["prefill_gemm_flop"]},
+        "roofline": roof,
         "link": {"copy_ms_per_step": st["prefill_copy_ms"], "compute_ms_per_step": st["prefill_compute_ms"],
                  "profiled_step_ms": pms,
                  "exposed_copy_ms_per_step": max(0.0, ms / K - st["prefill_compute_ms"]),
@@ -654,7 +680,7 @@ def run_native(args):
     torch.cuda.empty_cache()
 
     # ---- configs 3 and 4: the FP4 model -------------------------------------------
-    if "c3" in legs or "c4" in legs:
+    if "c3" in legs or "c4" in legs or "c4_w4a4" in legs:
         from expert_cache_serving_gb300 import runner
 
         pool3 = runner.build_pool(configs.C3)
@@ -676,6 +702,12 @@ def run_native(args):
             leg["config"]["weights"] = "the config-3 model's pool (seed 3); prompt activations and logits seed 4"
             leg["link"]["B_P_GBps"] = b_p3
             line["legs"]["prefill_c4"] = leg
+        if "c4_w4a4" in legs:
+            leg = prefill_leg(configs.C4, pool3, dev, args.prefill_warmup, args.prefill_steps, peaks, peak_kind,
+                              w4a4=True, hbm_peak=hbm_peak)
+            leg["config"]["weights"] = "the config-3 model's pool (seed 3); prompt activations and logits seed 4"
+            leg["link"]["B_P_GBps"] = b_p3
+            line["legs"]["prefill_c4_w4a4"] = leg
         del pool3
         torch.cuda.empty_cache()
 
@@ -701,10 +733,12 @@ def run_prefill_only(args):
     torch.cuda.set_device(0)
     dev = torch.device("cuda", 0)
     peaks, peak_kind = load_peaks()
-    w = configs.C4 if args.workload == "c4" else configs.C4.with_(name="small-fp4-prefill-256", L=2, E=16, C=32, B=256)
-    pool = runner.build_pool(configs.C3 if args.workload == "c4" else w)
+    full = args.workload.startswith("c4")
+    w = configs.C4 if full else configs.C4.with_(name="small-fp4-prefill-256", L=2, E=16, C=32, B=256)
+    pool = runner.build_pool(configs.C3 if full else w)
     touch_pool(dev, pool)
-    leg = prefill_leg(w, pool, dev, args.warmup, args.steps, peaks, peak_kind)
+    leg = prefill_leg(w, pool, dev, args.warmup, args.steps, peaks, peak_kind, w4a4=args.workload.endswith("w4a4"),
+                      hbm_peak=float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS)))
     line = dict(leg, metric=METRIC, n_gpus=1, higher_is_better=True, scaling="weak", vs_baseline=None,
                 data="synthetic")
     print(json.dumps(line), flush=True)
@@ -717,12 +751,13 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
-    ap.add_argument("--workload", default="c2", choices=["c2", "small", "c4", "small-prefill"],
+    ap.add_argument("--workload", default="c2",
+                    choices=["c2", "small", "c4", "small-prefill", "c4-w4a4", "small-prefill-w4a4"],
                     help="c2: the full benchmark (default); small: a 3-layer bf16 decode headline for profiler "
                          "captures; c4 / small-prefill: only the prefill leg, at full size or on 2 layers of "
-                         "16 experts with 256 tokens (profiler captures)")
+                         "16 experts with 256 tokens (profiler captures); -w4a4: the same with FP4 x FP4 GEMMs")
     ap.add_argument("--legs", default="all",
-                    help="comma list of extra legs: c2_device, c3, c4, c5 ('all' default, '' for none)")
+                    help="comma list of extra legs: c2_device, c3, c4, c4_w4a4, c5 ('all' default, '' for none)")
     ap.add_argument("--prefill-steps", type=int, default=3)
     ap.add_argument("--prefill-warmup", type=int, default=2)
     ap.add_argument("--elastic-batches", default="1,4")
@@ -734,7 +769,7 @@ def main():
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
         return run_reference(args, configs.C2)
-    if args.workload in ("c4", "small-prefill"):
+    if args.workload.startswith("c4") or args.workload.startswith("small-prefill"):
         return run_prefill_only(args)
     return run_native(args)
 

@@ -477,10 +477,12 @@ extern "C" moe_status moe_cache_create(const moe_model_desc* desc, const void* h
   const size_t obytes = (size_t)c->rows_per_cta_max * Bm * (k + 1) * 4;
   const size_t static_smem = layer_static_smem(desc->wdtype);
   const size_t budget = (size_t)smem_optin > static_smem + 1024 ? (size_t)smem_optin - static_smem - 1024 : 0;
-  const size_t need_h = (size_t)Bm * I * 4;  // one expert with every token
+  // staged h rows: I floats, or for FP4 36 floats per 32 (padded against bank conflicts)
+  const size_t hrow_f = desc->wdtype == MOE_FP4 ? (size_t)I / 32 * 36 : (size_t)I;
+  const size_t need_h = (size_t)Bm * hrow_f * 4;  // one expert with every token
   if (xbytes + obytes + need_h > budget)
     return bail(fail(MOE_ERR_INVALID_ARG, "max_tokens * (H, I) too large for the layer kernel's shared memory"));
-  c->smem_h_floats = (int)std::min<size_t>((budget - xbytes - obytes) / 4, (size_t)(Bm * k + Bm) * I);
+  c->smem_h_floats = (int)std::min<size_t>((budget - xbytes - obytes) / 4, (size_t)(Bm * k + Bm) * hrow_f);
   c->smem_h_floats &= ~3;
   // what is left holds this CTA's W_down rows of as many resident experts as fit
   const int64_t down_row_bytes = desc->wdtype == MOE_FP32   ? 4LL * I

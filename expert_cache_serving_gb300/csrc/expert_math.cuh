@@ -82,6 +82,14 @@ __device__ __forceinline__ float2 e4m3x2_to_float2(unsigned short two) {
   return __half22float2(hv);
 }
 
+// 16-byte chunks per lane and row in flight in the gate/up stream (a lane's
+// chunks are lane, lane + 32, ... in that order whatever the unroll).
+#ifndef MOE_P1_UNROLL_BF16
+#define MOE_P1_UNROLL_BF16 8
+#endif
+#ifndef MOE_P1_UNROLL_FP4
+#define MOE_P1_UNROLL_FP4 4
+#endif
 template <int WD>
 struct Fmt;
 template <>
@@ -93,13 +101,13 @@ struct Fmt<MOE_FP32> {
 template <>
 struct Fmt<MOE_BF16> {
   static constexpr int kElemsPerChunk = 8;
-  static constexpr int kUnroll = 4;
+  static constexpr int kUnroll = MOE_P1_UNROLL_BF16;
   __device__ static int64_t row_bytes(int K) { return (int64_t)K * 2; }
 };
 template <>
 struct Fmt<MOE_FP4> {
   static constexpr int kElemsPerChunk = 32;
-  static constexpr int kUnroll = 2;
+  static constexpr int kUnroll = MOE_P1_UNROLL_FP4;
   __device__ static int64_t row_bytes(int K) { return (int64_t)K / 2; }
 };
 
@@ -195,15 +203,20 @@ __device__ __forceinline__ float block16_dot<__nv_bfloat16>(uint32_t c0, uint32_
   return acc;
 }
 
+// xs 16-byte aligned: four 16-byte loads, the products in element order
 template <>
 __device__ __forceinline__ float block16_dot<float>(uint32_t c0, uint32_t c1, const float* xs) {
   float acc = 0.f;
 #pragma unroll
-  for (int b = 0; b < 8; ++b) {
-    const uint32_t byte = ((b < 4 ? c0 : c1) >> (8 * (b & 3))) & 0xFFu;
-    float2 w2 = e2m1x2_to_float2(byte);
-    acc = fmaf(w2.x, xs[2 * b], acc);
-    acc = fmaf(w2.y, xs[2 * b + 1], acc);
+  for (int q = 0; q < 4; ++q) {
+    const float4 v = reinterpret_cast<const float4*>(xs)[q];
+    const uint32_t word = q < 2 ? c0 : c1;
+    const float2 wa = e2m1x2_to_float2((word >> (16 * (q & 1))) & 0xFFu);
+    const float2 wb = e2m1x2_to_float2((word >> (16 * (q & 1) + 8)) & 0xFFu);
+    acc = fmaf(wa.x, v.x, acc);
+    acc = fmaf(wa.y, v.y, acc);
+    acc = fmaf(wb.x, v.z, acc);
+    acc = fmaf(wb.y, v.w, acc);
   }
   return acc;
 }

@@ -105,6 +105,24 @@ __device__ __forceinline__ const uint8_t* down_unit(const uint8_t* rec, int H, i
   return r.down_sc + (int64_t)n0 * (I / 16) + (int64_t)(v - nv) * 16;
 }
 
+// The CTA's mbarrier for the h rows phase 2 copies into shared memory, and
+// the parity of its current phase.
+__device__ __forceinline__ uint64_t* h_bar() {
+  __shared__ __align__(8) uint64_t b;
+  return &b;
+}
+__device__ __forceinline__ uint32_t* h_bar_phase() {
+  __shared__ uint32_t ph;
+  return &ph;
+}
+// Thread 0, before the kernel's first CTA barrier.
+__device__ __forceinline__ void h_bar_init() {
+  mbar_init(h_bar(), 1);
+  *h_bar_phase() = 0u;
+  fence_mbar_init();
+}
+__device__ __forceinline__ void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
+
 // Device-driven fill of this CTA's W_down rows [n0, n0 + nrows) of items
 // [ib, ie): copy them from the host pool into the items' slots, with eight
 // independent 16-byte loads in flight per thread (host-link latency bound).
@@ -154,7 +172,7 @@ template <int WD, int MAXT, bool FRESH, bool WB = false, typename XT>
 __device__ void phase1(const LayerParams& p, const ItemTable& tb, int ib, int ie, int cta0, int ncta, const XT* xs,
                        WarpGroup grp = whole_cta()) {
   using F = Fmt<WD>;
-  constexpr int EPC = F::kElemsPerChunk, UNR = F::kUnroll;
+  constexpr int EPC = F::kElemsPerChunk, UNR = MAXT >= 16 ? F::kUnroll / 2 : F::kUnroll;  // registers at 16 tokens
   const int rel = (int)blockIdx.x - cta0;
   if (rel < 0 || rel >= ncta || ie <= ib) return;
   const int H = p.H, I = p.I, lane = threadIdx.x & 31, warp = grp.tid() >> 5;
@@ -267,6 +285,13 @@ __device__ __forceinline__ unsigned short ld_down2(const uint8_t* q) {
   if constexpr (STAGED) return lds2(q); else return ld_w2<FRESH>(q);
 }
 
+// Floats between consecutive 16-byte weight chunks' activations in the
+// staged h rows: FP4 chunks cover 32 values (128 bytes, one pass over the 32
+// shared-memory banks), so eight lanes reading eight consecutive chunks would
+// all hit the same banks; 4 floats of padding per chunk spread them.
+template <int WD>
+__host__ __device__ constexpr int h_chunk_stride() { return WD == MOE_FP4 ? 36 : Fmt<WD>::kElemsPerChunk; }
+
 // W_down rows [n0, n0 + nrows) of items [ib, ie) -> os[row][t][j], by the
 // warp group grp.  STAGED: the rows of item i sit in shared memory at
 // stage + i * pitch (rows n0.., then their FP4 scales), copied there early.
@@ -280,17 +305,22 @@ __device__ void phase2(const LayerParams& p, const ItemTable& tb, int ib, int ie
   const int gt = grp.tid(), gn = grp.nthreads();
   const int ostride = B * (k + 1);
   const int nchunks = I / EPC;
+  constexpr int CS = h_chunk_stride<WD>();
+  const int hrow_f = nchunks * CS;  // floats per staged h row
   int g0 = ib;
   while (g0 < ie) {
     int g1 = g0, used = 0;
     while (g1 < ie) {
       const int nt = tb.ntok[g1];
-      if (used + nt * I > p.smem_h_floats && g1 > g0) break;
-      used += nt * I;
+      if (used + nt * hrow_f > p.smem_h_floats && g1 > g0) break;
+      used += nt * hrow_f;
       ++g1;
     }
     grp.sync();
-    {  // h rows of the group, item-major, in one flat pass (all loads in flight together)
+    const uint32_t par = *h_bar_phase();
+    if constexpr (CS != EPC) {
+      // padded layout (chunk c of a row at c * CS floats): plain loads and
+      // stores, four 16-byte loads in flight per thread
       __shared__ int s_hrow[kMaxPairs + kMaxB];
       const int rows = tb.hbase[g1] - tb.hbase[g0];
       for (int rr = gt; rr < rows; rr += gn) {
@@ -302,7 +332,7 @@ __device__ void phase2(const LayerParams& p, const ItemTable& tb, int ib, int ie
       }
       grp.sync();
       const int per = I / 4, n4 = rows * per;
-      for (int e0 = gt; e0 < n4; e0 += 4 * gn) {  // four loads in flight per thread
+      for (int e0 = gt; e0 < n4; e0 += 4 * gn) {
         float4 v[4];
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
@@ -312,11 +342,33 @@ __device__ void phase2(const LayerParams& p, const ItemTable& tb, int ib, int ie
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
           const int e = e0 + u * gn;
-          if (e < n4) reinterpret_cast<float4*>(hs + (int64_t)(e / per) * I)[e % per] = v[u];
+          if (e < n4) {
+            const int r = e / per, f = (e % per) * 4;  // float index within the row
+            *reinterpret_cast<float4*>(hs + (int64_t)r * hrow_f + (f / EPC) * CS + f % EPC) = v[u];
+          }
         }
+      }
+    } else {  // h rows of the group, item-major: one bulk copy per row, all in flight together
+      const int rows = tb.hbase[g1] - tb.hbase[g0];
+      if (gt < 32) {
+        fence_proxy_async_global();  // h was written through the generic proxy (ordered by a grid barrier)
+        if (gt == 0) mbar_expect_tx(h_bar(), (uint32_t)(rows * I * 4));
+        __syncwarp();
+        for (int rr = gt; rr < rows; rr += 32) {
+          int g = g0;
+          while (tb.hbase[g + 1] - tb.hbase[g0] <= rr) ++g;
+          int t, hr, j;
+          item_token(p, tb, g, rr - (tb.hbase[g] - tb.hbase[g0]), &t, &hr, &j);
+          bulk_g2s(hs + (int64_t)rr * I, p.h + (int64_t)hr * I, (uint32_t)(I * 4), h_bar());
+        }
+      }
+      if (!mbar_wait(h_bar(), par)) {  // L2 copies: only a broken context gets here
+        if (gt == 0) atomicExch(p.err, MOE_ERR_TIMEOUT);
+        mbar_wait(h_bar(), par);
       }
     }
     grp.sync();
+    if (gt == 0) *h_bar_phase() = par ^ 1u;
     // 8 lanes per row, 4 rows per warp: lane l of row group g reads chunks
     // l, l + 8, l + 16, ... of unit u0 + g in increasing order (8 in flight),
     // then the group's 8 partial sums reduce by a fixed butterfly
@@ -350,7 +402,7 @@ __device__ void phase2(const LayerParams& p, const ItemTable& tb, int ib, int ie
           if (live && c < nchunks) {
 #pragma unroll
             for (int q = 0; q < MAXT; ++q)
-              if (q < ntok) acc[q] += chunk_dot<WD, float>(w[u], sc[u], hs + (int64_t)(hbase + q) * I + (int64_t)c * EPC);
+              if (q < ntok) acc[q] += chunk_dot<WD, float>(w[u], sc[u], hs + (int64_t)(hbase + q) * hrow_f + (int64_t)c * CS);
           }
         }
       }
@@ -504,7 +556,10 @@ __global__ void __launch_bounds__(kThreads, 1) layer_kernel(LayerParams p) {
   grid_dep_wait();  // the previous call's commit and outputs are visible
   grid_dep_launch();
   if (rec) p.tl[0] = globaltimer_ns();
-  if (threadIdx.x == 0) s_flag = 0;  // read only after CTA barriers
+  if (threadIdx.x == 0) {
+    s_flag = 0;  // read only after CTA barriers
+    h_bar_init();
+  }
   if (threadIdx.x == kThreads - 64) {
     p.cst->part[blockIdx.x] = -1;
     if (ctrl) p.cst->gu_stop = 0;  // before the plan flag, which every later writer acquires
@@ -699,6 +754,7 @@ __global__ void __launch_bounds__(kThreads, 1) layer_finish_kernel(LayerParams p
   if (pl->err != MOE_OK) return;
   const int nf = pl->n_items[1];
   if (threadIdx.x == 0) {
+    h_bar_init();
     int failed = 0;
     for (int f = 0; f < nf; ++f)
       if (p.fill_flags[f] != p.seq || p.fill_flags[kMaxU + f] != p.seq) failed = 1;

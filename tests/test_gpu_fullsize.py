@@ -108,14 +108,16 @@ def _expert_outputs(args):
     import numpy as np
 
     import synth
-    from oracle import ffn, records
+    from oracle import ffn, nvfp4, records
 
-    seed, key, H, I, wdtype, x = args
+    seed, key, H, I, wdtype, x, w4a4 = args
     rec = synth.records_array(seed, key, 1, H, I, wdtype)[0]
+    if w4a4:
+        return key, nvfp4.expert(x.astype(np.float32), *records.parse(rec, H, I, wdtype))
     return key, ffn.expert(x, *records.parse(rec, H, I, wdtype))
 
 
-def sampled_prefill_reference(w, xs, lg, layers, tokens, workers=16):
+def sampled_prefill_reference(w, xs, lg, layers, tokens, workers=16, w4a4=False):
     """y [len(layers), len(tokens), H] from the oracle: routing and combine here,
     the expert FFNs of the distinct (layer, expert) pairs in a spawned pool."""
     import multiprocessing as mp
@@ -128,9 +130,9 @@ def sampled_prefill_reference(w, xs, lg, layers, tokens, workers=16):
         ids, wts = router.topk_softmax(lg[li][tokens].astype(np.float64), w.k)
         plan.append((x, ids, wts))
         for e in sorted(set(ids.reshape(-1).tolist())):
-            jobs.append((w.seed, l * w.E + e, w.H, w.I, w.wdtype, x))
+            jobs.append((w.seed, l * w.E + e, w.H, w.I, w.wdtype, x, w4a4))
         if w.shared:
-            jobs.append((w.seed, w.LE + l, w.H, w.I, w.wdtype, x))
+            jobs.append((w.seed, w.LE + l, w.H, w.I, w.wdtype, x, w4a4))
     with mp.get_context("spawn").Pool(min(workers, os.cpu_count() or 1)) as pool:
         outs = dict(pool.map(_expert_outputs, jobs, chunksize=1))
     ys = []
@@ -146,9 +148,10 @@ def sampled_prefill_reference(w, xs, lg, layers, tokens, workers=16):
     return ys
 
 
-@pytest.mark.parametrize("w", [configs.C4, configs.C2.with_(name="qwen3.6-shape-prefill-4096", B=4096)],
-                         ids=["dsv4-fp4-4096x43", "qwen36-bf16-4096x40"])
-def test_prefill_full_size_sampled(w):
+@pytest.mark.parametrize("w,w4a4", [(configs.C4, False), (configs.C2.with_(name="qwen3.6-shape-prefill-4096", B=4096),
+                                                         False), (configs.C4, True)],
+                         ids=["dsv4-fp4-4096x43", "qwen36-bf16-4096x40", "dsv4-fp4xfp4-4096x43"])
+def test_prefill_full_size_sampled(w, w4a4):
     from expert_cache_serving_gb300 import moecache as mc
     from expert_cache_serving_gb300 import runner
 
@@ -158,10 +161,12 @@ def test_prefill_full_size_sampled(w):
     tokens = np.sort(rng.choice(T, size=64, replace=False))
     xs = np.stack([synth.activations_bf16(w.seed, 0, l, T, w.H) for l in range(L)])
     lg = synth.iid_logits(w.seed, L, T, w.E)
-    ref = sampled_prefill_reference(w, xs[layers], lg[layers], layers, tokens)
+    ref = sampled_prefill_reference(w, xs[layers], lg[layers], layers, tokens, w4a4=w4a4)
     dev = torch.device("cuda")
     pool, shared = runner.build_pool(w), runner.build_shared(w)
     cache = runner.Cache(w, pool, shared, C=w.C, max_tokens=1)
+    if w4a4:
+        mc.moe_cache_set_prefill_precision(cache.handle, mc.MOE_PREFILL_W4A4)
     x = torch.from_numpy(xs.view(np.int16)).view(torch.bfloat16).to(dev)
     del xs
     y = torch.empty_like(x)

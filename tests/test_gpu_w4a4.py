@@ -138,9 +138,9 @@ def test_w4a4_experts_spanning_several_row_tiles():
 
 
 def test_w4a4_narrow_shape_with_shared_expert():
-    w = configs.SMALL_FP4_NARROW.with_(name="fp4-narrow-shared", shared=True, C=60)
+    w = configs.SMALL_FP4_NARROW.with_(name="fp4-narrow-shared", shared=True, C=48)
     layers = [0, 1]
-    cache, xs, lg, y = run_w4a4(w, 97, layers, C=60)
+    cache, xs, lg, y = run_w4a4(w, 97, layers, C=48)
     ref = oracle_w4a4(w, xs, lg, layers, H.ExpertBank(w))
     for li in range(len(layers)):
         H.assert_layer_close(y[li], ref[li], f"W4A4 prefill layer {layers[li]}")
