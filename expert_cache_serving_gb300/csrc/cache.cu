@@ -188,6 +188,11 @@ struct moe_cache {
   int o_part_floats = 0;
   unsigned long long* d_deferred = nullptr;
   unsigned* d_wave = nullptr;   // [2][kWaveCtrs] per-call counters of the layer kernel, by call parity
+  // graph mode: decode calls may be captured into CUDA graphs and replayed;
+  // each layer-kernel CTA adds 1 to d_seqctr per call and takes its sequence
+  // number from it, and the host reads the calls' summaries at moe_cache_sync
+  bool graph = false;
+  unsigned long long* d_seqctr = nullptr;
   unsigned long long deferred_base = 0;  // value of the device counter at the last statistics reset
   unsigned long long wait_gu_ns = 2000000, wait_dn_ns = 2000000;
   double split_bp = 0.0, split_bh = 0.0;  // bandwidths for q* (0: not set)
@@ -269,7 +274,7 @@ struct moe_cache {
 
 static constexpr int kTlRing = 1024;
 static constexpr int kTlStamps = 16;
-static constexpr int kRing = 256;  // call summaries in flight (device-fill calls the host has not read)
+static constexpr int kRing = kSummaryRing;  // call summaries in flight (device-fill calls the host has not read)
 
 static const char* kNotFound = "";
 
@@ -313,7 +318,7 @@ static void free_all(moe_cache* c) {
   for (void* p : {(void*)c->d_map, (void*)c->d_owner, (void*)c->d_stamp, (void*)c->d_g, (void*)c->d_plan,
                   (void*)c->d_h, (void*)c->d_logits, (void*)c->d_bar, (void*)c->d_flags, (void*)c->d_oldest,
                   (void*)c->d_oldest_n, (void*)c->d_moves, (void*)c->d_tl, (void*)c->d_cst, (void*)c->d_o_part,
-                  (void*)c->d_deferred, (void*)c->d_wave})
+                  (void*)c->d_deferred, (void*)c->d_wave, (void*)c->d_seqctr})
     if (p) cudaFree(p);
   if (c->h_work) cudaFreeHost(c->h_work);
   if (c->h_err) cudaFreeHost(c->h_err);
@@ -421,7 +426,8 @@ extern "C" moe_status moe_cache_create(const moe_model_desc* desc, const void* h
       (s = cu(cudaMalloc(&c->d_oldest_n, sizeof(int)), "victim order")) ||
       (s = cu(cudaMalloc(&c->d_cst, sizeof(CallState)), "call state")) ||
       (s = cu(cudaMalloc(&c->d_deferred, sizeof(unsigned long long)), "counter")) ||
-      (s = cu(cudaMalloc(&c->d_wave, sizeof(unsigned) * 2 * kWaveCtrs), "wave counters")))
+      (s = cu(cudaMalloc(&c->d_wave, sizeof(unsigned) * 2 * kWaveCtrs), "wave counters")) ||
+      (s = cu(cudaMalloc(&c->d_seqctr, sizeof(unsigned long long)), "sequence counter")))
     return bail(s);
   if ((s = cu(cudaMemset(c->d_map, 0xFF, sizeof(int32_t) * LE), "memset")) ||
       (s = cu(cudaMemset(c->d_owner, 0xFF, sizeof(int32_t) * nslot_alloc), "memset")) ||
@@ -432,7 +438,8 @@ extern "C" moe_status moe_cache_create(const moe_model_desc* desc, const void* h
       (s = cu(cudaMemset(c->d_oldest_n, 0xFF, sizeof(int)), "memset")) ||
       (s = cu(cudaMemset(c->d_cst, 0xFF, sizeof(CallState)), "memset")) ||
       (s = cu(cudaMemset(c->d_deferred, 0, sizeof(unsigned long long)), "memset")) ||
-      (s = cu(cudaMemset(c->d_wave, 0, sizeof(unsigned) * 2 * kWaveCtrs), "memset")))
+      (s = cu(cudaMemset(c->d_wave, 0, sizeof(unsigned) * 2 * kWaveCtrs), "memset")) ||
+      (s = cu(cudaMemset(c->d_seqctr, 0, sizeof(unsigned long long)), "memset")))
     return bail(s);
   if ((s = cu(cudaHostAlloc((void**)&c->h_work, sizeof(HostWork) * kRing, cudaHostAllocMapped), "pinned summary")) ||
       (s = cu(cudaHostAlloc((void**)&c->h_err, sizeof(int), cudaHostAllocMapped), "pinned error word")))
@@ -689,6 +696,128 @@ static cudaError_t launch_k1(moe_cache* c, const LayerParams& p, cudaStream_t s)
   return launch_layer(c->d.wdtype, p, c->grid, c->smem, false, s);
 }
 
+// The fields of one call's LayerParams that do not depend on its sequence number.
+static LayerParams call_params(moe_cache* c, int32_t layer, const void* x, const float* lg, int32_t B, void* y,
+                               const moe_layer_aux* aux) {
+  const moe_model_desc& d = c->d;
+  LayerParams p{};
+  p.L = d.L; p.E = d.E; p.k = d.k; p.B = B; p.layer = layer; p.H = d.H; p.I = d.I;
+  p.C = c->C;
+  p.logits = lg;
+  p.st = CacheDev{c->d_map, c->d_owner, c->d_stamp, c->d_g};
+  p.plan = c->d_plan;
+  p.plan_flag = c->d_flags;
+  p.fill_flags = c->d_flags + 1;
+  p.bar = c->d_bar;
+  p.err = c->d_err;
+  p.cst = c->d_cst;
+  p.o_part = c->d_o_part;
+  p.o_part_floats = c->o_part_floats;
+  p.wait_gu_ns = c->wait_gu_ns;
+  p.wait_dn_ns = c->wait_dn_ns;
+  p.deferred = c->d_deferred;
+  p.split_bp = c->split_bp;
+  p.split_bh = c->split_bh;
+  p.has_shared = d.has_shared;
+  p.device_fill = c->fill_mode == MOE_FILL_DEVICE;
+  p.pool = c->host_pool;  // pinned pages are mapped at the same address under unified addressing
+  p.slots = (const uint8_t*)c->slots.base;
+  p.S = c->S;
+  p.shared_rec = d.has_shared ? c->shared_dev + (int64_t)layer * c->S : nullptr;
+  p.x = x;
+  p.h = c->d_h;
+  p.h_shared_row0 = d.max_tokens * d.k;
+  p.y = y;
+  p.smem_h_floats = c->smem_h_floats;
+  p.rows_per_cta_max = c->rows_per_cta_max;
+  p.stage_items = c->stage_items;
+  p.stage_pitch = c->stage_pitch;
+  p.stage_off = c->stage_off;
+  p.oldest = c->d_oldest;
+  p.oldest_n = c->d_oldest_n;
+  if (aux) {
+    p.aux_ids = aux->ids; p.aux_w = aux->weights; p.aux_slots = aux->slots;
+    p.aux_perm = aux->perm; p.aux_offsets = aux->offsets; p.aux_logits = aux->logits;
+    p.aux_qstar = aux->qstar;
+  }
+  return p;
+}
+
+// A decode call in graph mode: nothing on the host depends on the call's
+// progress (no wait, no event, no host counter of its own), so the launch can
+// be captured into a CUDA graph and replayed; the kernel numbers the call from
+// the device counter and moe_cache_sync reads the summaries.
+static moe_status forward_graph(moe_cache* c, int32_t layer, const void* x, const float* logits,
+                                const float* router_w, int32_t B, void* y, cudaStream_t s,
+                                const moe_layer_aux* aux) {
+  const moe_model_desc& d = c->d;
+  if ((int64_t)B * d.k > c->C)
+    return fail(MOE_ERR_INVALID_ARG, "graph mode needs B*k <= n_slots (a capacity error could not be reported)");
+  // a stream being captured is ordered by whoever captures it (a wait on an
+  // event recorded outside the capture would break it)
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  CU_TRY(cudaStreamIsCapturing(s, &cap));
+  if (cap == cudaStreamCaptureStatusNone)
+    if (moe_status e = follow_stream(c, s)) return e;
+  const float* lg = logits;
+  if (!lg) {
+    CU_TRY(launch_router_logits(x, d.wdtype != MOE_FP32, router_w, B, d.E, d.H, c->d_logits, s));
+    lg = c->d_logits;
+  }
+  LayerParams p = call_params(c, layer, x, lg, B, y, aux);
+  p.seq_ctr = c->d_seqctr;
+  p.work = c->d_work;     // the ring's base: the kernel picks entry seq % ring
+  p.wave_ctr = c->d_wave;  // both counter sets: the kernel picks by seq parity
+  CU_TRY(launch_k1(c, p, s));
+  return MOE_OK;
+}
+
+// Graph mode: account every call whose summary the ring still holds, up to
+// the device counter; calls whose entry a later call overwrote are counted as
+// lost.  The stream must be idle.
+static moe_status drain_graph(moe_cache* c) {
+  unsigned long long ctr = 0;
+  CU_TRY(cudaMemcpy(&ctr, c->d_seqctr, sizeof(ctr), cudaMemcpyDeviceToHost));
+  const uint32_t last = (uint32_t)(ctr / (unsigned long long)c->grid);
+  for (uint32_t q = c->seq + 1; q != last + 1; ++q) {
+    const HostWork& w = c->h_work[q % kRing];
+    c->st.layer_launches += 1;
+    if (__atomic_load_n(&w.seq, __ATOMIC_ACQUIRE) != q) {
+      c->st.summaries_lost += 1;
+      continue;
+    }
+    if (w.err != MOE_OK) {
+      if (c->sticky == MOE_OK) {
+        c->sticky = MOE_ERR_CUDA;
+        c->sticky_msg = "internal error: victim selection found an inconsistent cache state";
+      }
+      continue;
+    }
+    account_call(c, w.layer, w.B, w, nullptr, nullptr, -1);
+  }
+  c->seq = last;
+  return MOE_OK;
+}
+
+extern "C" moe_status moe_cache_set_graph_mode(moe_cache_t c, int32_t on) {
+  g_err.clear();
+  if (!c) return fail(MOE_ERR_INVALID_ARG, "cache is NULL");
+  if (on && c->fill_mode != MOE_FILL_DEVICE)
+    return fail(MOE_ERR_INVALID_ARG, "graph mode needs device-driven fills (moe_cache_set_fill_mode)");
+  if ((bool)on == c->graph) return MOE_OK;
+  CU_TRY(cudaDeviceSynchronize());
+  if (on) {
+    if (moe_status e = drain_inflight(c, 0)) return e;
+    const unsigned long long ctr = (unsigned long long)c->seq * (unsigned long long)c->grid;
+    CU_TRY(cudaMemcpy(c->d_seqctr, &ctr, sizeof(ctr), cudaMemcpyHostToDevice));
+    c->graph = true;
+  } else {
+    if (moe_status e = drain_graph(c)) return e;
+    c->graph = false;
+  }
+  return MOE_OK;
+}
+
 extern "C" moe_status moe_layer_forward_ex(moe_cache_t c, int32_t layer, const void* x, const float* logits,
                                            const float* router_w, int32_t B, void* y, void* stream,
                                            const moe_layer_aux* aux) {
@@ -700,6 +829,7 @@ extern "C" moe_status moe_layer_forward_ex(moe_cache_t c, int32_t layer, const v
   if (!x || !y) return fail(MOE_ERR_INVALID_ARG, "x and y must be device pointers");
   if (!logits && !router_w) return fail(MOE_ERR_INVALID_ARG, "need logits or router_w");
   cudaStream_t s = (cudaStream_t)stream;
+  if (c->graph) return forward_graph(c, layer, x, logits, router_w, B, y, s, aux);
   if (*(volatile int*)c->h_err != 0) {
     drain_inflight(c, 0);
     return recover_after_timeout(c, s);
@@ -718,45 +848,11 @@ extern "C" moe_status moe_layer_forward_ex(moe_cache_t c, int32_t layer, const v
     lg = c->d_logits;
   }
   const uint32_t seq = ++c->seq;
-  LayerParams p{};
-  p.L = d.L; p.E = d.E; p.k = d.k; p.B = B; p.layer = layer; p.H = d.H; p.I = d.I;
-  p.C = c->C;
-  p.logits = lg;
-  p.st = CacheDev{c->d_map, c->d_owner, c->d_stamp, c->d_g};
-  p.plan = c->d_plan;
+  LayerParams p = call_params(c, layer, x, lg, B, y, aux);
   p.work = c->d_work + seq % kRing;
   p.seq = seq;
-  p.plan_flag = c->d_flags;
-  p.fill_flags = c->d_flags + 1;
-  p.bar = c->d_bar;
-  p.err = c->d_err;
-  p.cst = c->d_cst;
-  p.o_part = c->d_o_part;
-  p.o_part_floats = c->o_part_floats;
-  p.wait_gu_ns = c->wait_gu_ns;
-  p.wait_dn_ns = c->wait_dn_ns;
-  p.deferred = c->d_deferred;
-  p.split_bp = c->split_bp;
-  p.split_bh = c->split_bh;
   p.wave_ctr = c->d_wave + (seq & 1) * kWaveCtrs;
   p.wave_next = c->d_wave + ((seq + 1) & 1) * kWaveCtrs;
-  p.has_shared = d.has_shared;
-  p.device_fill = device;
-  p.pool = c->host_pool;  // pinned pages are mapped at the same address under unified addressing
-  p.slots = (const uint8_t*)c->slots.base;
-  p.S = c->S;
-  p.shared_rec = d.has_shared ? c->shared_dev + (int64_t)layer * c->S : nullptr;
-  p.x = x;
-  p.h = c->d_h;
-  p.h_shared_row0 = d.max_tokens * d.k;
-  p.y = y;
-  p.smem_h_floats = c->smem_h_floats;
-  p.rows_per_cta_max = c->rows_per_cta_max;
-  p.stage_items = c->stage_items;
-  p.stage_pitch = c->stage_pitch;
-  p.stage_off = c->stage_off;
-  p.oldest = c->d_oldest;
-  p.oldest_n = c->d_oldest_n;
   int tl_row = -1;
   if (c->profile_level >= 2 && c->d_tl) {
     if ((int)c->tl_calls.size() >= kTlRing / 2) {
@@ -767,11 +863,6 @@ extern "C" moe_status moe_layer_forward_ex(moe_cache_t c, int32_t layer, const v
     c->tl_next = (c->tl_next + 1) % kTlRing;
     p.tl = c->d_tl + (size_t)tl_row * kTlStamps;
     CU_TRY(cudaMemsetAsync(p.tl, 0, kTlStamps * sizeof(unsigned long long), s));
-  }
-  if (aux) {
-    p.aux_ids = aux->ids; p.aux_w = aux->weights; p.aux_slots = aux->slots;
-    p.aux_perm = aux->perm; p.aux_offsets = aux->offsets; p.aux_logits = aux->logits;
-    p.aux_qstar = aux->qstar;
   }
   cudaEvent_t ta = nullptr, tb = nullptr;
   if (c->profiling) {
@@ -1033,6 +1124,10 @@ extern "C" moe_status moe_cache_sync(moe_cache_t c, void* stream) {
   if (c->have_last && c->last_stream != s) CU_TRY(cudaStreamSynchronize(c->last_stream));
   CU_TRY(cudaStreamSynchronize(c->copy));
   CU_TRY(cudaStreamSynchronize(c->copy2));
+  if (c->graph) {
+    CU_TRY(cudaDeviceSynchronize());  // replays may run on any stream
+    if (moe_status e = drain_graph(c)) return e;
+  }
   if (moe_status e = drain_inflight(c, 0)) return e;
   if (*(volatile int*)c->h_err != 0) return recover_after_timeout(c, s);
   if (c->sticky != MOE_OK) {
@@ -1114,6 +1209,7 @@ extern "C" const void* moe_cache_slot_ptr(moe_cache_t c, int64_t s) {
 extern "C" moe_status moe_cache_set_fill_mode(moe_cache_t c, int32_t mode) {
   if (!c) return fail(MOE_ERR_INVALID_ARG, "cache is NULL");
   if (mode != MOE_FILL_COPY && mode != MOE_FILL_DEVICE) return fail(MOE_ERR_INVALID_ARG, "unknown fill mode %d", mode);
+  if (c->graph && mode != MOE_FILL_DEVICE) return fail(MOE_ERR_INVALID_ARG, "graph mode needs device-driven fills");
   if (moe_status e = drain_inflight(c, 0)) return e;
   if (mode == MOE_FILL_DEVICE) {
     cudaPointerAttributes a;

@@ -40,9 +40,11 @@ struct Plan {
 
 // Host-visible (pinned, mapped) summary of one call: the miss list the host
 // needs to issue the fills, the undo log, and a sequence number written last.
+constexpr int kSummaryRing = 256;  // host summaries in flight (one per call, by call sequence number)
 struct HostWork {
   volatile uint32_t seq;
   int32_t err;
+  int32_t layer, B;             // the call's layer and token count
   int32_t n_u, n_miss;
   uint64_t g_before;
   int32_t key[kMaxU];

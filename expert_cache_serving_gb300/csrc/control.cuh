@@ -237,6 +237,38 @@ static __device__ int select_oldest(CtrlSmem& cs, const CacheDev& st, int64_t C,
   return nsel == want ? want : -1;
 }
 
+// Sequence number of the current call and what derives from it, set once
+// per CTA before the first CTA barrier (call_seq_init) and read from shared
+// memory afterwards.  For a call launched from the host it is the launch's
+// own; for a call replayed from a captured graph it comes from a counter
+// every CTA adds 1 to per call, so consecutive replays get consecutive numbers.
+struct CallSeq {
+  uint32_t seq;
+  HostWork* work;     // this call's host summary
+  unsigned* wave_ctr;   // this call's counters
+  unsigned* wave_next;  // the next call's counters (cleared by this call)
+};
+__device__ __forceinline__ CallSeq& cseq() {
+  __shared__ CallSeq c;
+  return c;
+}
+// One thread per CTA.
+__device__ __forceinline__ void call_seq_init(const LayerParams& p) {
+  CallSeq& c = cseq();
+  if (p.seq_ctr) {
+    const uint32_t s = (uint32_t)(atomicAdd(p.seq_ctr, 1ull) / gridDim.x + 1ull);
+    c.seq = s;
+    c.work = p.work + s % kSummaryRing;
+    c.wave_ctr = p.wave_ctr + (s & 1u) * kWaveCtrs;
+    c.wave_next = p.wave_ctr + ((s + 1u) & 1u) * kWaveCtrs;
+  } else {
+    c.seq = p.seq;
+    c.work = p.work;
+    c.wave_ctr = p.wave_ctr;
+    c.wave_next = p.wave_next;
+  }
+}
+
 // Publish the host summary of the call (its fields are already written):
 // system-scope fences by every writer, then the sequence number last.
 __device__ __forceinline__ void publish_summary(const LayerParams& p) {
@@ -244,7 +276,7 @@ __device__ __forceinline__ void publish_summary(const LayerParams& p) {
   __syncthreads();
   if (threadIdx.x == 0) {
     __threadfence_system();
-    p.work->seq = p.seq;
+    cseq().work->seq = cseq().seq;
   }
 }
 
@@ -360,19 +392,21 @@ static __device__ int route_lookup(const LayerParams& p, CtrlSmem& cs, bool writ
 static __device__ void publish_error(const LayerParams& p, const CtrlSmem& cs, int err) {
   if (threadIdx.x != 0) return;
   Plan* plan = p.plan;
-  HostWork* work = p.work;
+  HostWork* work = cseq().work;
   plan->err = err;
   plan->n_u = cs.nu;
   plan->n_miss = 0;
   plan->n_items[0] = plan->n_items[1] = 0;
   work->err = err;
+  work->layer = p.layer;
+  work->B = p.B;
   work->n_u = cs.nu;
   work->n_miss = 0;
   work->g_before = *p.st.g;
   __threadfence_system();
-  work->seq = p.seq;
+  work->seq = cseq().seq;
   __threadfence();
-  st_release_u32(p.plan_flag, p.seq);
+  st_release_u32(p.plan_flag, cseq().seq);
 }
 
 // Fill count q* of the bandwidth split for m misses ("measured bandwidths
@@ -401,7 +435,7 @@ static __device__ int choose_victims(const LayerParams& p, CtrlSmem& cs) {
   const int E = p.E, k = p.k, B = p.B, npairs = B * k, n_u = cs.nu, nmiss = cs.nmiss;
   const int64_t C = p.C;
   Plan* plan = p.plan;
-  HostWork* work = p.work;
+  HostWork* work = cseq().work;
   const int my_listed = tid < kMaxU ? p.oldest[tid] : -1;
   if (tid == 0) {
     cs.err = MOE_OK;
@@ -504,6 +538,8 @@ static __device__ int choose_victims(const LayerParams& p, CtrlSmem& cs) {
     plan->n_items[1] = nmiss;
     plan->g_before = cs.g;
     work->err = MOE_OK;
+    work->layer = p.layer;
+    work->B = p.B;
     work->n_u = n_u;
     work->n_miss = nmiss;
     work->g_before = cs.g;
@@ -514,7 +550,7 @@ static __device__ int choose_victims(const LayerParams& p, CtrlSmem& cs) {
   // the CTA barrier orders every thread's plan writes before thread 0's
   // release store of the plan flag (GPU scope), which the other CTAs acquire
   __syncthreads();
-  if (tid == 0) st_release_u32(p.plan_flag, p.seq);
+  if (tid == 0) st_release_u32(p.plan_flag, cseq().seq);
   return MOE_OK;
 }
 

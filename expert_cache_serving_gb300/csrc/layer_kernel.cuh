@@ -560,12 +560,11 @@ __global__ void __launch_bounds__(kThreads, 1) layer_kernel(LayerParams p) {
     s_flag = 0;  // read only after CTA barriers
     h_bar_init();
   }
-  if (threadIdx.x == kThreads - 64) {
+  if (threadIdx.x == kThreads - 64) {  // a warp off the router's path (the counter add may take a while)
+    call_seq_init(p);
     p.cst->part[blockIdx.x] = -1;
     if (ctrl) p.cst->gu_stop = 0;  // before the plan flag, which every later writer acquires
   }
-  // counters of the next call (this call's were cleared by the previous one)
-  if (ctrl && threadIdx.x >= kThreads - kWaveCtrs) p.wave_next[threadIdx.x - (kThreads - kWaveCtrs)] = 0u;
   // activations into shared memory by one bulk copy (waited for before phase 1),
   // or by plain loads when the caller's pointer is not 16-byte aligned
   const uint32_t xbytes = (uint32_t)((size_t)B * H * sizeof(XT));
@@ -584,6 +583,9 @@ __global__ void __launch_bounds__(kThreads, 1) layer_kernel(LayerParams p) {
 
   // ---- 0. routing and lookup (every CTA); victims, plan, summary (control CTA)
   int err = route_lookup(p, cs, ctrl);
+  // counters of the next call (this call's were cleared by the previous one);
+  // on every path, errors included
+  if (ctrl && threadIdx.x >= kThreads - kWaveCtrs) cseq().wave_next[threadIdx.x - (kThreads - kWaveCtrs)] = 0u;
   if (ctrl) err = err == MOE_OK ? choose_victims(p, cs) : (publish_error(p, cs, err), err);
   if (err != MOE_OK) {  // capacity: every CTA; inconsistent victim list: the control CTA
     if (x_bulk) mbar_wait(&s_xin, 0);  // no bulk copy outlives its CTA
@@ -625,7 +627,7 @@ __global__ void __launch_bounds__(kThreads, 1) layer_kernel(LayerParams p) {
     return;
   }
   // this CTA has read the residency table: the control CTA may commit
-  if (threadIdx.x == 0) atomicAdd(&p.wave_ctr[kLookupCtr], 1u);
+  if (threadIdx.x == 0) atomicAdd(&cseq().wave_ctr[kLookupCtr], 1u);
 
   // ---- 1./2. gate/up rows of the resident experts and the shared expert (CTAs
   // 1..), one grid barrier, then every CTA's W_down rows; the control CTA
@@ -634,7 +636,7 @@ __global__ void __launch_bounds__(kThreads, 1) layer_kernel(LayerParams p) {
   if (rec) p.tl[2] = globaltimer_ns();
   bool bad = false;
   if (ctrl) {
-    bad = !wait_count(&p.wave_ctr[kLookupCtr], (unsigned)G, whole_cta(), p.err);
+    bad = !wait_count(&cseq().wave_ctr[kLookupCtr], (unsigned)G, whole_cta(), p.err);
     if (!bad) {
       control_commit(p, cs);
       compact_oldest(p, cs);
@@ -661,7 +663,7 @@ __global__ void __launch_bounds__(kThreads, 1) layer_kernel(LayerParams p) {
 
   // the fills' slots come from the control CTA's plan
   bool ok = true;
-  if (!ctrl && wait_flag(p.plan_flag, p.seq, nullptr, 5000000000ull, 32) != 0) {
+  if (!ctrl && wait_flag(p.plan_flag, cseq().seq, nullptr, 5000000000ull, 32) != 0) {
     if (threadIdx.x == 0) atomicExch(p.err, MOE_ERR_TIMEOUT);
     ok = false;
   }
@@ -691,7 +693,7 @@ __global__ void __launch_bounds__(kThreads, 1) layer_kernel(LayerParams p) {
     // copy mode: each fill as soon as its copy has landed
     load_items(p, pl, 1, tb);
     for (int f = 0; f < nf; ++f) {
-      if (wait_flag(&p.fill_flags[f], p.seq, &p.cst->gu_stop, p.wait_gu_ns) != 0) {
+      if (wait_flag(&p.fill_flags[f], cseq().seq, &p.cst->gu_stop, p.wait_gu_ns) != 0) {
         if (threadIdx.x == 0) atomicExch(&p.cst->gu_stop, 1);  // every CTA stops waiting
         break;
       }
@@ -707,7 +709,7 @@ __global__ void __launch_bounds__(kThreads, 1) layer_kernel(LayerParams p) {
     __syncthreads();
     int handed = s_flag ? 0 : -1;  // fills whose W_down rows os holds when handing over
     for (int f = 0; f < nf && handed < 0; ++f) {
-      if (wait_flag(&p.fill_flags[kMaxU + f], p.seq, nullptr, p.wait_dn_ns) != 0) {
+      if (wait_flag(&p.fill_flags[kMaxU + f], cseq().seq, nullptr, p.wait_dn_ns) != 0) {
         handed = f;
         break;
       }
@@ -755,6 +757,7 @@ __global__ void __launch_bounds__(kThreads, 1) layer_finish_kernel(LayerParams p
   const int nf = pl->n_items[1];
   if (threadIdx.x == 0) {
     h_bar_init();
+    call_seq_init(p);  // launched from the host only (copy-fill calls)
     int failed = 0;
     for (int f = 0; f < nf; ++f)
       if (p.fill_flags[f] != p.seq || p.fill_flags[kMaxU + f] != p.seq) failed = 1;

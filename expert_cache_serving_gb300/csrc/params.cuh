@@ -14,7 +14,9 @@ struct LayerParams {
   CacheDev st;
   Plan* plan;
   HostWork* work;             // device alias of the pinned host summary
-  uint32_t seq;               // call sequence number
+  uint32_t seq;               // call sequence number (when seq_ctr is null)
+  unsigned long long* seq_ctr;  // captured calls: every CTA adds 1 per call, seq = value / gridDim.x + 1, and
+                              // work / wave_ctr are then the bases of the summary ring and of the counter pairs
   unsigned* plan_flag;        // set to seq by the control CTA once the plan is written
   unsigned* fill_flags;       // [2][kMaxU]: first/second half of fill f landed (seq, or seq|kFlagError)
   unsigned long long* bar;    // grid barrier counter (only grows; see grid_barrier)

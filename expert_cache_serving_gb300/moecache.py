@@ -43,7 +43,8 @@ class moe_stats(ctypes.Structure):
                 ("prefill_gemm_ms", ctypes.c_double), ("prefill_gemm_flop", ctypes.c_double),
                 ("deferred_calls", ctypes.c_int64), ("finish_launches", ctypes.c_int64),
                 ("pdl_launches", ctypes.c_int64), ("prefill_records_streamed", ctypes.c_int64),
-                ("prefill_records_in_place", ctypes.c_int64), ("qstar_fills", ctypes.c_int64)]
+                ("prefill_records_in_place", ctypes.c_int64), ("qstar_fills", ctypes.c_int64),
+                ("summaries_lost", ctypes.c_int64)]
 
     def as_dict(self):
         return {name: getattr(self, name) for name, _ in self._fields_}
@@ -100,6 +101,7 @@ SIGNATURES = {
     "moe_cache_slot_ptr": (_P, [_P, _I64]),
     "moe_cache_set_fill_mode": (_I32, [_P, _I32]),
     "moe_cache_set_prefill_precision": (_I32, [_P, _I32]),
+    "moe_cache_set_graph_mode": (_I32, [_P, _I32]),
     "moe_quantize_fp4": (_I32, [_P, _I32, _I64, _I32, _P, _P, _P]),
     "moe_cache_inject_fill_failure": (_I32, [_P, _I32]),
     "moe_layer_forward_resident_noalloc": (_I32, [ctypes.POINTER(moe_model_desc), _P, _P, _P, _P, _I32, _P, _P]),
@@ -254,6 +256,10 @@ def moe_cache_slot_ptr(cache: int, s: int) -> int | None:
 
 def moe_cache_set_fill_mode(cache: int, mode: int) -> None:
     check(lib.moe_cache_set_fill_mode(cache, mode), "moe_cache_set_fill_mode")
+
+
+def moe_cache_set_graph_mode(cache: int, on: int) -> None:
+    check(lib.moe_cache_set_graph_mode(cache, on), "moe_cache_set_graph_mode")
 
 
 def moe_cache_set_prefill_precision(cache: int, mode: int) -> None:

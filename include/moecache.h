@@ -116,6 +116,8 @@ typedef struct {
   int64_t prefill_records_streamed;  /* expert records moe_prefill_stream copied into its buffers */
   int64_t prefill_records_in_place;  /* expert records it read where they were already resident */
   int64_t qstar_fills;       /* sum over calls of q*, the fill count of the bandwidth split */
+  int64_t summaries_lost;    /* graph mode: calls whose summary a later call overwrote before moe_cache_sync
+                                read it (more than 256 calls in between); not counted in the other fields */
 } moe_stats;
 
 typedef struct {
@@ -369,6 +371,23 @@ moe_status moe_cache_set_prefill_precision(moe_cache_t cache, int32_t mode);
  * the caller.  Errors: MOE_ERR_INVALID_ARG, MOE_ERR_CUDA (launch failure). */
 moe_status moe_quantize_fp4(const void* x, int32_t x_dtype, int64_t rows, int32_t K, uint8_t* codes,
                             uint8_t* scales, void* stream);
+
+/* Graph mode (on = 1): decode calls may be captured into CUDA graphs and
+ * replayed ("CUDA Graph와 공존하는 LRU 캐시" in the FreeToken write-up: the
+ * control step runs on the device so the whole decode step can be a graph).
+ * Needs MOE_FILL_DEVICE (a copy-mode call waits on the host).  In graph mode
+ * moe_layer_forward only enqueues the layer kernel (no host wait, event or
+ * allocation); the kernel numbers the call from a device counter, so every
+ * replay of a captured call is a new call with its own recency, fills and
+ * evictions, exactly as if it had been launched.  The host reads the calls'
+ * summaries (statistics, trace) at moe_cache_sync, or when graph mode is
+ * turned off; call moe_cache_sync at least every 256 calls or the oldest
+ * summaries are overwritten (counted in summaries_lost; the cache state
+ * itself is never affected).  Calls need B * k <= n_slots.  Profiling
+ * timestamps and per-launch events are not recorded in graph mode.
+ * Turning it on or off synchronises the device.
+ * Errors: MOE_ERR_INVALID_ARG (copy-fill mode). */
+moe_status moe_cache_set_graph_mode(moe_cache_t cache, int32_t on);
 
 /* Test hook: the next fill copies of this cache fail after `after` successful
  * copies (-1 disables).  Used to check the rollback path without a GPU fault. */
