@@ -260,6 +260,42 @@ __device__ void phase1(const LayerParams& p, const ItemTable& tb, int ib, int ie
   }
 }
 
+// Bytes of gate/up rows per CTA up to which phase 1's rows are requested into
+// L2 all at once before the warps stream them (0: never): with the whole
+// call's rows in flight the DRAM queue stays full while the warps work
+// through their rows; a call far larger than L2 streams without it.
+#ifndef MOE_P1_PREFETCH_MAX
+#define MOE_P1_PREFETCH_MAX (512 * 1024)
+#endif
+
+// The last warp requests this CTA's phase-1 rows of items [ib, ie) (the same
+// split as phase1) into L2, one bulk prefetch per item and matrix.
+template <int WD>
+__device__ void prefetch_gate_up(const LayerParams& p, const ItemTable& tb, int ib, int ie, int cta0, int ncta) {
+  using F = Fmt<WD>;
+  const int rel = (int)blockIdx.x - cta0;
+  if (MOE_P1_PREFETCH_MAX == 0 || rel < 0 || rel >= ncta || ie <= ib) return;
+  const int H = p.H, I = p.I;
+  const int64_t total = (int64_t)(ie - ib) * I;
+  const int64_t t0 = (int64_t)rel * total / ncta, t1 = (int64_t)(rel + 1) * total / ncta;
+  const int64_t rb = F::row_bytes(H), sb = WD == MOE_FP4 ? H / 16 : 0;
+  if ((t1 - t0) * 2 * (rb + sb) > MOE_P1_PREFETCH_MAX) return;
+  const int lane = (int)threadIdx.x - (int)(blockDim.x - 32);
+  if (lane < 0) return;
+  for (int it = ib + lane; it < ie; it += 32) {
+    const int64_t a = max(t0, (int64_t)(it - ib) * I), b = min(t1, (int64_t)(it - ib + 1) * I);
+    if (a >= b) continue;
+    const int i0 = (int)(a - (int64_t)(it - ib) * I), n = (int)(b - a);
+    const RecView v = rec_view<WD>(tb.rec[it], H, I);
+    prefetch_l2(v.gate + (int64_t)i0 * rb, (uint32_t)(n * rb));
+    prefetch_l2(v.up + (int64_t)i0 * rb, (uint32_t)(n * rb));
+    if (WD == MOE_FP4) {
+      prefetch_l2(v.gate_sc + (int64_t)i0 * sb, (uint32_t)(n * sb));
+      prefetch_l2(v.up_sc + (int64_t)i0 * sb, (uint32_t)(n * sb));
+    }
+  }
+}
+
 // Where W_down row `row` (and its FP4 scales) of item gi is read: its record,
 // or, when STAGED, staged item j of this CTA in shared memory.
 template <int WD, bool STAGED>
@@ -596,6 +632,7 @@ __global__ void __launch_bounds__(kThreads, 1) layer_kernel(LayerParams p) {
 
   // ---- 1. gate/up rows of the resident experts and the shared expert --------------
   const int n_res = local_items(p, cs, tb);
+  if (!ctrl) prefetch_gate_up<WD>(p, tb, 0, n_res, 1, G - 1);
   // this CTA's W_down rows of the resident experts: the first n_stage items
   // into shared memory by bulk copies completing on s_stage, the rest into L2
   const int n_stage = nrows > 0 ? min(n_res, p.stage_items) : 0;
