@@ -77,7 +77,8 @@ __device__ __forceinline__ float key_logit(unsigned key) {
 // min); only the winning lane rescans.  Weights = softmax over the k taken
 // logits, exp(l_r - l_0) / sum, in the order taken.
 template <int NQ>
-__device__ __forceinline__ void route_token(const float* lg, int E, int k, int lane, float* aux, int* ids, float* w) {
+__device__ __forceinline__ void route_token(const float* lg, int E, int k, int lane, float* aux, int* ids, float* w,
+                                            unsigned long long* stamp = nullptr) {
   unsigned key[NQ];
 #pragma unroll
   for (int q = 0; q < NQ; ++q) {
@@ -94,6 +95,7 @@ __device__ __forceinline__ void route_token(const float* lg, int E, int k, int l
 #pragma unroll
   for (int q = 0; q < NQ; ++q)
     if (key[q] > bk) { bk = key[q]; bq = q; }
+  if (stamp && lane == 0) *stamp = globaltimer_ns();  // profiling: the logits have landed
   float m0 = 0.f, sum = 0.f;
   for (int r = 0; r < k; ++r) {
     const unsigned m = __reduce_max_sync(0xFFFFFFFFu, bk);
@@ -310,12 +312,13 @@ static __device__ int route_lookup(const LayerParams& p, CtrlSmem& cs, bool writ
     float* aux = (write_aux && p.aux_logits) ? p.aux_logits + (size_t)t * E : nullptr;
     int* ids = cs.ids + t * k;
     float* w = cs.w + t * k;
-    if (nq <= 1) route_token<1>(lg, E, k, lane, aux, ids, w);
-    else if (nq <= 2) route_token<2>(lg, E, k, lane, aux, ids, w);
-    else if (nq <= 4) route_token<4>(lg, E, k, lane, aux, ids, w);
-    else if (nq <= 8) route_token<8>(lg, E, k, lane, aux, ids, w);
-    else if (nq <= 16) route_token<16>(lg, E, k, lane, aux, ids, w);
-    else route_token<32>(lg, E, k, lane, aux, ids, w);
+    unsigned long long* st = rec && t == 0 ? p.tl + 15 : nullptr;
+    if (nq <= 1) route_token<1>(lg, E, k, lane, aux, ids, w, st);
+    else if (nq <= 2) route_token<2>(lg, E, k, lane, aux, ids, w, st);
+    else if (nq <= 4) route_token<4>(lg, E, k, lane, aux, ids, w, st);
+    else if (nq <= 8) route_token<8>(lg, E, k, lane, aux, ids, w, st);
+    else if (nq <= 16) route_token<16>(lg, E, k, lane, aux, ids, w, st);
+    else route_token<32>(lg, E, k, lane, aux, ids, w, st);
   }
   if (rec) p.tl[12] = globaltimer_ns();
 #pragma unroll

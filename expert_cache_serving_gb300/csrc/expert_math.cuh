@@ -237,4 +237,60 @@ __device__ __forceinline__ float chunk_dot<MOE_FP4, float>(uint4 w, unsigned sho
   return fmaf(a1, s.y, a0 * s.x);
 }
 
+// One half (16 codes) of an FP4 chunk converted once for several tokens
+// (unscaled e2m1 values, exact), and its sum against one token's 16 values
+// with block16_dot's operations in block16_dot's order.
+__device__ __forceinline__ void fp4_half(uint32_t c0, uint32_t c1, float* v) {
+#pragma unroll
+  for (int b = 0; b < 8; ++b) {
+    const float2 w2 = e2m1x2_to_float2(((b < 4 ? c0 : c1) >> (8 * (b & 3))) & 0xFFu);
+    v[2 * b] = w2.x;
+    v[2 * b + 1] = w2.y;
+  }
+}
+__device__ __forceinline__ float block16_sum(const float* v, const __nv_bfloat16* xs) {
+  const uint4 xa = reinterpret_cast<const uint4*>(xs)[0], xb = reinterpret_cast<const uint4*>(xs)[1];
+  const uint32_t xw[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
+  float acc = 0.f;
+#pragma unroll
+  for (int b = 0; b < 8; ++b) {
+    acc = fmaf(v[2 * b], bf16lo(xw[b]), acc);
+    acc = fmaf(v[2 * b + 1], bf16hi(xw[b]), acc);
+  }
+  return acc;
+}
+__device__ __forceinline__ float block16_sum(const float* v, const float* xs) {
+  float acc = 0.f;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const float4 x4 = reinterpret_cast<const float4*>(xs)[q];
+    acc = fmaf(v[4 * q], x4.x, acc);
+    acc = fmaf(v[4 * q + 1], x4.y, acc);
+    acc = fmaf(v[4 * q + 2], x4.z, acc);
+    acc = fmaf(v[4 * q + 3], x4.w, acc);
+  }
+  return acc;
+}
+
+// acc[q] += chunk_dot<MOE_FP4>(w, sc2, xs(q)) for the first ntok tokens,
+// each half of the chunk converted once: the same operations in the same
+// order as chunk_dot, token by token.
+template <int MAXT, typename VT, typename XF>
+__device__ __forceinline__ void fp4_chunk_tokens(uint4 w, unsigned short sc2, int ntok, XF xs_of, float* acc) {
+  float v[16], a0[MAXT];
+  fp4_half(w.x, w.y, v);
+#pragma unroll
+  for (int q = 0; q < MAXT; ++q) {
+    if (q >= ntok) break;
+    a0[q] = block16_sum(v, (const VT*)xs_of(q));
+  }
+  fp4_half(w.z, w.w, v);
+  const float2 s = e4m3x2_to_float2(sc2);
+#pragma unroll
+  for (int q = 0; q < MAXT; ++q) {
+    if (q >= ntok) break;
+    acc[q] += fmaf(block16_sum(v, (const VT*)xs_of(q) + 16), s.y, a0[q] * s.x);
+  }
+}
+
 }  // namespace moe

@@ -172,7 +172,8 @@ template <int WD, int MAXT, bool FRESH, bool WB = false, typename XT>
 __device__ void phase1(const LayerParams& p, const ItemTable& tb, int ib, int ie, int cta0, int ncta, const XT* xs,
                        WarpGroup grp = whole_cta()) {
   using F = Fmt<WD>;
-  constexpr int EPC = F::kElemsPerChunk, UNR = MAXT >= 16 ? F::kUnroll / 2 : F::kUnroll;  // registers at 16 tokens
+  // fewer chunks in flight where the token registers grow (16 tokens; FP4 with converted chunks)
+  constexpr int EPC = F::kElemsPerChunk, UNR = (MAXT >= 16 || (WD == MOE_FP4 && MAXT > 1)) ? F::kUnroll / 2 : F::kUnroll;
   const int rel = (int)blockIdx.x - cta0;
   if (rel < 0 || rel >= ncta || ie <= ib) return;
   const int H = p.H, I = p.I, lane = threadIdx.x & 31, warp = grp.tid() >> 5;
@@ -234,12 +235,19 @@ __device__ void phase1(const LayerParams& p, const ItemTable& tb, int ib, int ie
       for (int u = 0; u < UNR; ++u) {
         const int c = c0 + lane + 32 * u;
         if (c < nchunks) {
+          if constexpr (WD == MOE_FP4 && MAXT > 1 && MAXT < 16) {
+            // several tokens: each chunk's codes converted once (same sums as chunk_dot)
+            auto x_of = [&](int q) { return xs + (size_t)tok[q] * H + (size_t)c * EPC; };
+            fp4_chunk_tokens<MAXT, XT>(wg[u], sg[u], ntok, x_of, ag);
+            fp4_chunk_tokens<MAXT, XT>(wu[u], su[u], ntok, x_of, au);
+          } else {
 #pragma unroll
-          for (int q = 0; q < MAXT; ++q) {
-            if (q < ntok) {
-              const XT* xr = xs + (size_t)tok[q] * H + (size_t)c * EPC;
-              ag[q] += chunk_dot<WD, XT>(wg[u], sg[u], xr);
-              au[q] += chunk_dot<WD, XT>(wu[u], su[u], xr);
+            for (int q = 0; q < MAXT; ++q) {
+              if (q < ntok) {
+                const XT* xr = xs + (size_t)tok[q] * H + (size_t)c * EPC;
+                ag[q] += chunk_dot<WD, XT>(wg[u], sg[u], xr);
+                au[q] += chunk_dot<WD, XT>(wu[u], su[u], xr);
+              }
             }
           }
         }
@@ -256,42 +264,6 @@ __device__ void phase1(const LayerParams& p, const ItemTable& tb, int ib, int ie
           p.h[(int64_t)hr * I + i] = g / (1.0f + expf(-g)) * u;
         }
       }
-    }
-  }
-}
-
-// Bytes of gate/up rows per CTA up to which phase 1's rows are requested into
-// L2 all at once before the warps stream them (0: never): with the whole
-// call's rows in flight the DRAM queue stays full while the warps work
-// through their rows; a call far larger than L2 streams without it.
-#ifndef MOE_P1_PREFETCH_MAX
-#define MOE_P1_PREFETCH_MAX (512 * 1024)
-#endif
-
-// The last warp requests this CTA's phase-1 rows of items [ib, ie) (the same
-// split as phase1) into L2, one bulk prefetch per item and matrix.
-template <int WD>
-__device__ void prefetch_gate_up(const LayerParams& p, const ItemTable& tb, int ib, int ie, int cta0, int ncta) {
-  using F = Fmt<WD>;
-  const int rel = (int)blockIdx.x - cta0;
-  if (MOE_P1_PREFETCH_MAX == 0 || rel < 0 || rel >= ncta || ie <= ib) return;
-  const int H = p.H, I = p.I;
-  const int64_t total = (int64_t)(ie - ib) * I;
-  const int64_t t0 = (int64_t)rel * total / ncta, t1 = (int64_t)(rel + 1) * total / ncta;
-  const int64_t rb = F::row_bytes(H), sb = WD == MOE_FP4 ? H / 16 : 0;
-  if ((t1 - t0) * 2 * (rb + sb) > MOE_P1_PREFETCH_MAX) return;
-  const int lane = (int)threadIdx.x - (int)(blockDim.x - 32);
-  if (lane < 0) return;
-  for (int it = ib + lane; it < ie; it += 32) {
-    const int64_t a = max(t0, (int64_t)(it - ib) * I), b = min(t1, (int64_t)(it - ib + 1) * I);
-    if (a >= b) continue;
-    const int i0 = (int)(a - (int64_t)(it - ib) * I), n = (int)(b - a);
-    const RecView v = rec_view<WD>(tb.rec[it], H, I);
-    prefetch_l2(v.gate + (int64_t)i0 * rb, (uint32_t)(n * rb));
-    prefetch_l2(v.up + (int64_t)i0 * rb, (uint32_t)(n * rb));
-    if (WD == MOE_FP4) {
-      prefetch_l2(v.gate_sc + (int64_t)i0 * sb, (uint32_t)(n * sb));
-      prefetch_l2(v.up_sc + (int64_t)i0 * sb, (uint32_t)(n * sb));
     }
   }
 }
@@ -336,7 +308,8 @@ __device__ void phase2(const LayerParams& p, const ItemTable& tb, int ib, int ie
                        float* os, const uint8_t* stage = nullptr, int pitch = 0, WarpGroup grp = whole_cta()) {
   using F = Fmt<WD>;
   constexpr int EPC = F::kElemsPerChunk;
-  constexpr int kLanesPerRow = 8, kRowsPerWarp = 32 / kLanesPerRow, kChunksPerLane = MAXT >= 16 ? 4 : 8;
+  constexpr int kLanesPerRow = 8, kRowsPerWarp = 32 / kLanesPerRow;
+  constexpr int kChunksPerLane = (MAXT >= 16 || (WD == MOE_FP4 && MAXT > 1)) ? 4 : 8;  // a lane still sums its chunks in order
   const int H = p.H, I = p.I, B = p.B, k = p.k, lane = threadIdx.x & 31, warp = grp.tid() >> 5;
   const int gt = grp.tid(), gn = grp.nthreads();
   const int ostride = B * (k + 1);
@@ -436,9 +409,14 @@ __device__ void phase2(const LayerParams& p, const ItemTable& tb, int ib, int ie
         for (int u = 0; u < kChunksPerLane; ++u) {
           const int c = c0 + gl + kLanesPerRow * u;
           if (live && c < nchunks) {
+            if constexpr (WD == MOE_FP4 && MAXT > 1 && MAXT < 16) {
+              auto h_of = [&](int q) { return hs + (int64_t)(hbase + q) * hrow_f + (int64_t)c * CS; };
+              fp4_chunk_tokens<MAXT, float>(w[u], sc[u], ntok, h_of, acc);
+            } else {
 #pragma unroll
-            for (int q = 0; q < MAXT; ++q)
-              if (q < ntok) acc[q] += chunk_dot<WD, float>(w[u], sc[u], hs + (int64_t)(hbase + q) * hrow_f + (int64_t)c * CS);
+              for (int q = 0; q < MAXT; ++q)
+                if (q < ntok) acc[q] += chunk_dot<WD, float>(w[u], sc[u], hs + (int64_t)(hbase + q) * hrow_f + (int64_t)c * CS);
+            }
           }
         }
       }
@@ -632,7 +610,6 @@ __global__ void __launch_bounds__(kThreads, 1) layer_kernel(LayerParams p) {
 
   // ---- 1. gate/up rows of the resident experts and the shared expert --------------
   const int n_res = local_items(p, cs, tb);
-  if (!ctrl) prefetch_gate_up<WD>(p, tb, 0, n_res, 1, G - 1);
   // this CTA's W_down rows of the resident experts: the first n_stage items
   // into shared memory by bulk copies completing on s_stage, the rest into L2
   const int n_stage = nrows > 0 ? min(n_res, p.stage_items) : 0;

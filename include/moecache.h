@@ -298,12 +298,13 @@ moe_status moe_cache_set_profiling(moe_cache_t cache, int32_t on);
  * reaches each phase, over the calls profiled at level 2 (split by whether
  * the call had fills), as seen by CTA 1 unless noted.  Stamps: 0 start, 1
  * routing and lookup done, 2 gate/up rows of the resident experts streamed, 3
- * first wave of W_down rows started, 4 W_down rows of the resident experts
+ * W_down rows started (after the grid barrier), 4 W_down rows of the resident experts
  * done, 5 first fill's first half landed, 6 gate/up rows of the fills done, 7
  * plan of the fills read, 8 last fill's second half landed, 9 end, 10 control
  * CTA: victims and plan written, 11 control CTA: recency committed, 12 router
  * done, 13 residency row in shared memory, 14 lookups and grouping done,
- * 15 unused.  A call that never reaches a stamp does not count towards it. */
+ * 15 the first token's router logits loaded.  A call that never reaches a
+ * stamp does not count towards it. */
 typedef struct {
   int64_t calls_hit_only, calls_with_fills;
   double hit_only_us[16];
