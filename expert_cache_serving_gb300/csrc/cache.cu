@@ -273,7 +273,7 @@ struct moe_cache {
 };
 
 static constexpr int kTlRing = 1024;
-static constexpr int kTlStamps = 16;
+static constexpr int kTlStamps = 20;
 static constexpr int kRing = kSummaryRing;  // call summaries in flight (device-fill calls the host has not read)
 
 static const char* kNotFound = "";
@@ -572,7 +572,8 @@ static void drain_timeline(moe_cache* c) {
     // running mean per stamp (stamps never reached stay 0 and are skipped)
     for (int i = 0; i < kTlStamps; ++i) {
       if (!t[i] || !t[0]) continue;
-      const double us = ((double)t[i] - (double)t[0]) / 1e3;
+      const unsigned long long ti = i == 16 ? ~t[i] : t[i];  // stamp 16 is kept as a complement (earliest)
+      const double us = ((double)ti - (double)t[0]) / 1e3;
       acc[i] += (us - acc[i]) / (double)(n + 1);
     }
     n += 1;

@@ -607,6 +607,7 @@ __global__ void __launch_bounds__(kThreads, 1) layer_kernel(LayerParams p) {
   }
   if (ctrl && p.tl) p.tl[10] = globaltimer_ns();
   if (rec) p.tl[1] = globaltimer_ns();
+  if (p.tl && threadIdx.x == 0) atomicMax(p.tl + 18, globaltimer_ns());
 
   // ---- 1. gate/up rows of the resident experts and the shared expert --------------
   const int n_res = local_items(p, cs, tb);
@@ -648,6 +649,11 @@ __global__ void __launch_bounds__(kThreads, 1) layer_kernel(LayerParams p) {
   // commits recency and residency meanwhile, once every CTA has done its lookups
   if (!ctrl) phase1<WD, MAXT, false>(p, tb, 0, n_res, 1, G - 1, xs);
   if (rec) p.tl[2] = globaltimer_ns();
+  if (p.tl && !ctrl && threadIdx.x == 0) {
+    const unsigned long long now = globaltimer_ns();
+    atomicMax(p.tl + 16, ~now);  // earliest, as a complement
+    atomicMax(p.tl + 17, now);
+  }
   bool bad = false;
   if (ctrl) {
     bad = !wait_count(&cseq().wave_ctr[kLookupCtr], (unsigned)G, whole_cta(), p.err);
@@ -742,6 +748,7 @@ __global__ void __launch_bounds__(kThreads, 1) layer_kernel(LayerParams p) {
   // ---- 4. weighted combine in rank order --------------------------------------------
   combine_rows<WD>(p, tb, os, n0, nrows);
   if (rec) p.tl[9] = globaltimer_ns();
+  if (p.tl && threadIdx.x == 0) atomicMax(p.tl + 19, globaltimer_ns());
 }
 
 // Completion kernel of a copy-fill call, launched on the compute stream after

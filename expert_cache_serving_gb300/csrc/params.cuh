@@ -48,7 +48,7 @@ struct LayerParams {
   int stage_off;              // byte offset of the staging area in dynamic shared memory
   int32_t* oldest;            // [kMaxU] oldest slots, ascending key
   int* oldest_n;              // entries in it, -1 if invalid
-  unsigned long long* tl;     // optional phase timestamps of this call [16] (profiling)
+  unsigned long long* tl;     // optional phase timestamps of this call [20] (profiling)
   // optional inspection outputs
   int32_t* aux_ids;
   float* aux_w;

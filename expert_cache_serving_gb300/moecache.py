@@ -69,7 +69,7 @@ class moe_prefill_aux(ctypes.Structure):
 
 class moe_phase_times(ctypes.Structure):
     _fields_ = [("calls_hit_only", ctypes.c_int64), ("calls_with_fills", ctypes.c_int64),
-                ("hit_only_us", ctypes.c_double * 16), ("with_fills_us", ctypes.c_double * 16)]
+                ("hit_only_us", ctypes.c_double * 20), ("with_fills_us", ctypes.c_double * 20)]
 
     def as_dict(self):
         return {"calls_hit_only": self.calls_hit_only, "calls_with_fills": self.calls_with_fills,

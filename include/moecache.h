@@ -303,12 +303,14 @@ moe_status moe_cache_set_profiling(moe_cache_t cache, int32_t on);
  * plan of the fills read, 8 last fill's second half landed, 9 end, 10 control
  * CTA: victims and plan written, 11 control CTA: recency committed, 12 router
  * done, 13 residency row in shared memory, 14 lookups and grouping done,
- * 15 the first token's router logits loaded.  A call that never reaches a
- * stamp does not count towards it. */
+ * 15 the first token's router logits loaded; over all CTAs: 16 the first and
+ * 17 the last to finish the gate/up rows of the resident experts, 18 the last
+ * to finish routing and lookup, 19 the last to end.  A call that never
+ * reaches a stamp does not count towards it. */
 typedef struct {
   int64_t calls_hit_only, calls_with_fills;
-  double hit_only_us[16];
-  double with_fills_us[16];
+  double hit_only_us[20];
+  double with_fills_us[20];
 } moe_phase_times;
 moe_status moe_cache_phase_times(moe_cache_t cache, moe_phase_times* out);
 
