@@ -595,11 +595,13 @@ __global__ void __launch_bounds__(kThreads, 1) layer_kernel(LayerParams p) {
   grid_dep_wait();  // the previous call's commit and outputs are visible
   grid_dep_launch();
   if (rec) p.tl[0] = globaltimer_ns();
-  if (threadIdx.x == 0) {
+  // warp 0 goes straight to the router (token 0): set-up with fences or
+  // long-latency operations runs in other warps
+  if (threadIdx.x == kThreads - 96) {
     s_flag = 0;  // read only after CTA barriers
     h_bar_init();
   }
-  if (threadIdx.x == kThreads - 64) {  // a warp off the router's path (the counter add may take a while)
+  if (threadIdx.x == kThreads - 64) {  // the counter add may take a while
     call_seq_init(p);
     p.cst->part[blockIdx.x] = -1;
     if (ctrl) p.cst->gu_stop = 0;  // before the plan flag, which every later writer acquires
