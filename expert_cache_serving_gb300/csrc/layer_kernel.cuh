@@ -168,18 +168,9 @@ __device__ __forceinline__ void item_token(const LayerParams& p, const ItemTable
 
 // Gate/up rows of items [ib, ie), spread over CTAs [cta0, cta0 + ncta).
 // WB: the rows are read from the host pool and also written to the slot.
-// dyn (non-null): the rows are not split in advance; each warp takes
-// kP1Grab consecutive rows at a time from this per-call counter (zero at the
-// start of the call), the next batch requested while it works on the current
-// one, so fast CTAs take more rows and all finish together.  Which warp
-// computes a row does not change its value.
-#ifndef MOE_P1_DYNAMIC
-#define MOE_P1_DYNAMIC 1
-#endif
-constexpr int kP1Grab = 2;
 template <int WD, int MAXT, bool FRESH, bool WB = false, typename XT>
 __device__ void phase1(const LayerParams& p, const ItemTable& tb, int ib, int ie, int cta0, int ncta, const XT* xs,
-                       WarpGroup grp = whole_cta(), unsigned* dyn = nullptr) {
+                       WarpGroup grp = whole_cta()) {
   using F = Fmt<WD>;
   // fewer chunks in flight where the token registers grow (16 tokens; FP4 with converted chunks)
   constexpr int EPC = F::kElemsPerChunk, UNR = (MAXT >= 16 || (WD == MOE_FP4 && MAXT > 1)) ? F::kUnroll / 2 : F::kUnroll;
@@ -275,20 +266,6 @@ __device__ void phase1(const LayerParams& p, const ItemTable& tb, int ib, int ie
       }
     }
   };
-  if (dyn) {
-    auto grab = [&]() -> int64_t {
-      unsigned v = 0;
-      if (lane == 0) v = atomicAdd(dyn, (unsigned)kP1Grab);
-      return (int64_t)__shfl_sync(0xFFFFFFFFu, v, 0);
-    };
-    int64_t cur = grab();
-    while (cur < total) {
-      const int64_t nxt = grab();
-      for (int64_t task = cur; task < cur + kP1Grab && task < total; ++task) row_task(task);
-      cur = nxt;
-    }
-    return;
-  }
   for (int64_t task = t0 + warp; task < t1; task += grp.nw) row_task(task);
 }
 
@@ -528,7 +505,6 @@ __device__ void poison_rows(const LayerParams& p, int n0, int nrows) {
 }
 
 constexpr int kLookupCtr = 0;  // per-call counter of CTAs done with the residency lookups
-constexpr int kP1Ctr = 1;      // per-call counter of the resident gate/up rows handed out
 
 // Wait (thread 0 of the group polls, the group waits on it) until *c >=
 // target; false after limit_ns (MOE_ERR_TIMEOUT is then recorded).
@@ -674,8 +650,7 @@ __global__ void __launch_bounds__(kThreads, 1) layer_kernel(LayerParams p) {
   // ---- 1./2. gate/up rows of the resident experts and the shared expert (CTAs
   // 1..), one grid barrier, then every CTA's W_down rows; the control CTA
   // commits recency and residency meanwhile, once every CTA has done its lookups
-  unsigned* p1_ctr = MOE_P1_DYNAMIC ? &cseq().wave_ctr[kP1Ctr] : nullptr;
-  if (!ctrl) phase1<WD, MAXT, false>(p, tb, 0, n_res, p1_ctr ? 0 : 1, p1_ctr ? G : G - 1, xs, whole_cta(), p1_ctr);
+  if (!ctrl) phase1<WD, MAXT, false>(p, tb, 0, n_res, 1, G - 1, xs);
   if (rec) p.tl[2] = globaltimer_ns();
   if (p.tl && !ctrl && threadIdx.x == 0) {
     const unsigned long long now = globaltimer_ns();
@@ -690,7 +665,6 @@ __global__ void __launch_bounds__(kThreads, 1) layer_kernel(LayerParams p) {
       compact_oldest(p, cs);
     }
     if (p.tl && threadIdx.x == 0) p.tl[11] = globaltimer_ns();
-    if (p1_ctr) phase1<WD, MAXT, false>(p, tb, 0, n_res, 0, G, xs, whole_cta(), p1_ctr);  // rows still left
   }
   bad = !grid_barrier(p.bar, p.err) || bad;
   if (n_stage > 0 && !mbar_wait(&s_stage, 0)) {  // the staging copies never leave this CTA in flight
