@@ -35,12 +35,15 @@
 
 namespace moe {
 
+constexpr int kEarlyItem = kMaxItems;
 struct ItemTable {
-  const uint8_t* rec[kMaxItems];  // where the record is read (slot, shared expert, or host pool)
-  uint8_t* dst[kMaxItems];        // slot a device-driven fill writes the record to (else null)
-  int ntok[kMaxItems];
-  int pair0[kMaxItems];      // -1 for the shared expert
-  int hbase[kMaxItems + 1];  // running token count in item order
+  // entries 0 .. kMaxItems-1 in item order; entry kEarlyItem holds the shared
+  // expert while its gate/up rows run alongside the routing
+  const uint8_t* rec[kMaxItems + 1];  // where the record is read (slot, shared expert, or host pool)
+  uint8_t* dst[kMaxItems + 1];        // slot a device-driven fill writes the record to (else null)
+  int ntok[kMaxItems + 1];
+  int pair0[kMaxItems + 1];  // -1 for the shared expert
+  int hbase[kMaxItems + 2];  // running token count in item order
   int perm[kMaxPairs];       // the plan's grouped pair order, copied once per call
   float pair_w[kMaxPairs];   // the plan's routing weights, copied once per call
 };
@@ -598,6 +601,21 @@ __global__ void __launch_bounds__(kThreads, 1) layer_kernel(LayerParams p) {
     for (int i = threadIdx.x; i < (int)(xbytes / 16); i += blockDim.x) dst[i] = src[i];
   }
 
+  // ---- the shared expert needs no routing: warps 1.. stream its gate/up rows
+  // (split over every CTA) while warp 0 routes the call
+  const bool early_shared = p.has_shared && x_bulk;
+  if (early_shared && threadIdx.x >= 32) {
+    const WarpGroup rest{1, kWarps - 1, 1};
+    if (threadIdx.x == 32) {
+      tb.rec[kEarlyItem] = p.shared_rec;
+      tb.dst[kEarlyItem] = nullptr;
+      tb.ntok[kEarlyItem] = B;
+      tb.pair0[kEarlyItem] = -1;
+    }
+    rest.sync();  // the entry and the activations' mbarrier are initialised
+    if (mbar_wait(&s_xin, 0)) phase1<WD, MAXT, false>(p, tb, kEarlyItem, kEarlyItem + 1, 0, G, xs, rest);
+  }
+
   // ---- 0. routing and lookup (every CTA); victims, plan, summary (control CTA)
   int err = route_lookup(p, cs, ctrl);
   // counters of the next call (this call's were cleared by the previous one);
@@ -650,7 +668,8 @@ __global__ void __launch_bounds__(kThreads, 1) layer_kernel(LayerParams p) {
   // ---- 1./2. gate/up rows of the resident experts and the shared expert (CTAs
   // 1..), one grid barrier, then every CTA's W_down rows; the control CTA
   // commits recency and residency meanwhile, once every CTA has done its lookups
-  if (!ctrl) phase1<WD, MAXT, false>(p, tb, 0, n_res, 1, G - 1, xs);
+  // (the shared expert, item n_res - 1, already done when early_shared)
+  if (!ctrl) phase1<WD, MAXT, false>(p, tb, 0, early_shared ? n_res - 1 : n_res, 1, G - 1, xs);
   if (rec) p.tl[2] = globaltimer_ns();
   if (p.tl && !ctrl && threadIdx.x == 0) {
     const unsigned long long now = globaltimer_ns();
