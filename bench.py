@@ -622,7 +622,8 @@ def run_native(args):
     t_all = time.perf_counter()
 
     # ---- headline: config 2, copy-mode fills ---------------------------------------
-    w = configs.C2 if args.workload == "c2" else configs.SMALL_BF16
+    w = {"c2": configs.C2, "small": configs.SMALL_BF16,
+         "small-fp4": configs.SMALL_FP4.with_(name="small-fp4-L2-E16-k6", C=16, steps=W + K)}[args.workload]
     inp = DecodeInputs(w, W + K, dev)
     first_touch = touch_pool(dev, inp.pool)
     b_p = measure_link(dev, inp.pool, inp.S)
@@ -758,9 +759,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--workload", default="c2",
-                    choices=["c2", "small", "c4", "small-prefill", "c4-w4a4", "small-prefill-w4a4"],
-                    help="c2: the full benchmark (default); small: a 3-layer bf16 decode headline for profiler "
-                         "captures; c4 / small-prefill: only the prefill leg, at full size or on 2 layers of "
+                    choices=["c2", "small", "small-fp4", "c4", "small-prefill", "c4-w4a4", "small-prefill-w4a4"],
+                    help="c2: the full benchmark (default); small / small-fp4: a 3-layer bf16 or 2-layer FP4 "
+                         "(config-3 shapes) decode headline for profiler captures; c4 / small-prefill: only the prefill leg, at full size or on 2 layers of "
                          "16 experts with 256 tokens (profiler captures); -w4a4: the same with FP4 x FP4 GEMMs")
     ap.add_argument("--legs", default="all",
                     help="comma list of extra legs: c2_device, c3, c4, c4_w4a4, c5 ('all' default, '' for none)")
