@@ -134,7 +134,8 @@ __global__ void __launch_bounds__(1024) group_place_kernel(const int32_t* ids, i
 
 // ---- 3. gather of the activations in group order -------------------------------------
 // TO_F16: rows are written as f16 (the FP4 GEMMs run on f16 operands); bf16 ->
-// f16 is exact for every bf16 value inside the f16 range.
+// f16 is exact for 2^-14 <= |x| <= 65504 and 0, smaller magnitudes round to
+// the f16 subnormal grid (absolute error <= 2^-25).
 template <bool TO_F16>
 __global__ void gather_kernel(const __nv_bfloat16* __restrict__ x, int Tk, int k, int H, int n_pairs,
                               const int32_t* __restrict__ perm, __nv_bfloat16* __restrict__ xp) {

@@ -225,8 +225,10 @@ moe_status moe_layer_forward_ex(moe_cache_t cache, int32_t layer, const void* x,
  * [n_layers][T][E], y: device [n_layers][T][H] bf16.  Only MOE_BF16 / MOE_FP4
  * models; prefill also needs I % 128 == 0 and H % 256 == 0.  The expert GEMMs
  * accumulate in float32; their operands are bf16 for MOE_BF16 models and f16
- * for MOE_FP4 models (the activations convert exactly for |x| <= 65504, the
- * FP4 weights expand exactly, the SwiGLU intermediate is rounded to f16), or,
+ * for MOE_FP4 models (an activation converts exactly when 2^-14 <= |x| <=
+ * 65504 or x = 0; smaller magnitudes round to the f16 subnormal grid, an
+ * absolute error of at most 2^-25; the FP4 weights expand exactly; the SwiGLU
+ * intermediate is rounded to f16), or,
  * after moe_cache_set_prefill_precision(MOE_PREFILL_W4A4), FP4 x FP4.
  * The host waits once at the start for the cache's earlier work (it plans the
  * copies from the residency table); the rest is asynchronous on `stream`.
