@@ -313,6 +313,7 @@ static __device__ int route_lookup(const LayerParams& p, CtrlSmem& cs, bool writ
     int* ids = cs.ids + t * k;
     float* w = cs.w + t * k;
     unsigned long long* st = rec && t == 0 ? p.tl + 15 : nullptr;
+    if (rec && t == 0) p.tl[13] = globaltimer_ns();  // profiling: the router starts loading
     if (nq <= 1) route_token<1>(lg, E, k, lane, aux, ids, w, st);
     else if (nq <= 2) route_token<2>(lg, E, k, lane, aux, ids, w, st);
     else if (nq <= 4) route_token<4>(lg, E, k, lane, aux, ids, w, st);
@@ -327,7 +328,7 @@ static __device__ int route_lookup(const LayerParams& p, CtrlSmem& cs, bool writ
     if (e < E) cs.maprow[e] = mrow[j];
   }
   __syncthreads();
-  if (rec) p.tl[13] = globaltimer_ns();
+
 
   // ---- dedup: U = sorted distinct routed experts ----------------------------------
   if (tid < npairs) atomicOr(&cs.bits[cs.ids[tid] >> 5], 1u << (cs.ids[tid] & 31));

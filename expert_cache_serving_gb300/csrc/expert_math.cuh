@@ -4,6 +4,8 @@
 #pragma once
 #include <cuda_fp16.h>
 
+#include <type_traits>
+
 #include "common.cuh"
 
 namespace moe {
@@ -221,6 +223,46 @@ __device__ __forceinline__ float block16_dot<float>(uint32_t c0, uint32_t c1, co
   return acc;
 }
 
+// Two e2m1 codes (low nibble = first element) -> two f16 in one word (exact).
+__device__ __forceinline__ uint32_t e2m1x2_to_h2(uint32_t byte) {
+  uint32_t h2;
+  asm("{ .reg .b8 t; cvt.u8.u32 t, %1; cvt.rn.f16x2.e2m1x2 %0, t; }" : "=r"(h2) : "r"(byte));
+  return h2;
+}
+// acc + a * b with f16 a, b (the halves of two words picked by HI) in one
+// float32 rounding: the product of two f16 values is exact in float32, so this
+// is fmaf((float)a, (float)b, acc) bit for bit, without the two conversions.
+template <int HI>
+__device__ __forceinline__ float fma_h(uint32_t a2, uint32_t b2, float acc) {
+  const unsigned short a = (unsigned short)(HI ? a2 >> 16 : a2), b = (unsigned short)(HI ? b2 >> 16 : b2);
+  asm("fma.rn.f32.f16 %0, %1, %2, %0;" : "+f"(acc) : "h"(a), "h"(b));
+  return acc;
+}
+
+// 16 e2m1 codes against 16 f16 activations (16-byte aligned), in element
+// order; the activations of FP4 decode are staged as f16 (see x_to_f16).
+template <>
+__device__ __forceinline__ float block16_dot<__half>(uint32_t c0, uint32_t c1, const __half* xs) {
+  const uint4 xa = reinterpret_cast<const uint4*>(xs)[0], xb = reinterpret_cast<const uint4*>(xs)[1];
+  const uint32_t xw[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
+  float acc = 0.f;
+#pragma unroll
+  for (int b = 0; b < 8; ++b) {
+    const uint32_t w2 = e2m1x2_to_h2(((b < 4 ? c0 : c1) >> (8 * (b & 3))) & 0xFFu);
+    acc = fma_h<0>(w2, xw[b], acc);
+    acc = fma_h<1>(w2, xw[b], acc);
+  }
+  return acc;
+}
+
+template <>
+__device__ __forceinline__ float chunk_dot<MOE_FP4, __half>(uint4 w, unsigned short sc2, const __half* xs) {
+  float2 s = e4m3x2_to_float2(sc2);
+  float a0 = block16_dot<__half>(w.x, w.y, xs);
+  float a1 = block16_dot<__half>(w.z, w.w, xs + 16);
+  return fmaf(a1, s.y, a0 * s.x);
+}
+
 template <>
 __device__ __forceinline__ float chunk_dot<MOE_FP4, __nv_bfloat16>(uint4 w, unsigned short sc2, const __nv_bfloat16* xs) {
   float2 s = e4m3x2_to_float2(sc2);
@@ -277,6 +319,38 @@ __device__ __forceinline__ float block16_sum(const float* v, const float* xs) {
 // order as chunk_dot, token by token.
 template <int MAXT, typename VT, typename XF>
 __device__ __forceinline__ void fp4_chunk_tokens(uint4 w, unsigned short sc2, int ntok, XF xs_of, float* acc) {
+  if constexpr (std::is_same<VT, __half>::value) {  // f16 activations: codes kept as f16 pairs
+    float a0[MAXT];
+    uint32_t h[8];
+#pragma unroll
+    for (int b = 0; b < 8; ++b) h[b] = e2m1x2_to_h2(((b < 4 ? w.x : w.y) >> (8 * (b & 3))) & 0xFFu);
+#pragma unroll
+    for (int q = 0; q < MAXT; ++q) {
+      if (q >= ntok) break;
+      const uint4* x4 = reinterpret_cast<const uint4*>(xs_of(q));
+      const uint4 xa = x4[0], xb = x4[1];
+      const uint32_t xw[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
+      float s0 = 0.f;
+#pragma unroll
+      for (int b = 0; b < 8; ++b) s0 = fma_h<1>(h[b], xw[b], fma_h<0>(h[b], xw[b], s0));
+      a0[q] = s0;
+    }
+#pragma unroll
+    for (int b = 0; b < 8; ++b) h[b] = e2m1x2_to_h2(((b < 4 ? w.z : w.w) >> (8 * (b & 3))) & 0xFFu);
+    const float2 s = e4m3x2_to_float2(sc2);
+#pragma unroll
+    for (int q = 0; q < MAXT; ++q) {
+      if (q >= ntok) break;
+      const uint4* x4 = reinterpret_cast<const uint4*>(xs_of(q)) + 2;
+      const uint4 xa = x4[0], xb = x4[1];
+      const uint32_t xw[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
+      float s1 = 0.f;
+#pragma unroll
+      for (int b = 0; b < 8; ++b) s1 = fma_h<1>(h[b], xw[b], fma_h<0>(h[b], xw[b], s1));
+      acc[q] += fmaf(s1, s.y, a0[q] * s.x);
+    }
+    return;
+  }
   float v[16], a0[MAXT];
   fp4_half(w.x, w.y, v);
 #pragma unroll

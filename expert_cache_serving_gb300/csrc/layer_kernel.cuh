@@ -126,6 +126,27 @@ __device__ __forceinline__ void h_bar_init() {
 }
 __device__ __forceinline__ void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
 
+// FP4 models: the staged bf16 activations become f16 in place (all threads;
+// a CTA barrier must follow), so the gate/up dot products run as
+// mixed-precision f16 FMAs; exact for 2^-14 <= |x| <= 65504 and 0, smaller
+// magnitudes round to the f16 subnormal grid (absolute error <= 2^-25).
+template <int WD, typename XT>
+__device__ __forceinline__ void x_to_f16(XT* xs, int n) {
+  if constexpr (WD == MOE_FP4) {
+    uint32_t* w = reinterpret_cast<uint32_t*>(xs);
+    for (int i = threadIdx.x; i < n / 2; i += blockDim.x) {
+      const __half2 h = __floats2half2_rn(bf16lo(w[i]), bf16hi(w[i]));
+      w[i] = *reinterpret_cast<const uint32_t*>(&h);
+    }
+  }
+}
+// The activations as the gate/up dot products read them.
+template <int WD, typename XT>
+__device__ __forceinline__ auto x_dot(const XT* xs) {
+  if constexpr (WD == MOE_FP4) return reinterpret_cast<const __half*>(xs);
+  else return xs;
+}
+
 // Device-driven fill of this CTA's W_down rows [n0, n0 + nrows) of items
 // [ib, ie): copy them from the host pool into the items' slots, with eight
 // independent 16-byte loads in flight per thread (host-link latency bound).
@@ -603,7 +624,7 @@ __global__ void __launch_bounds__(kThreads, 1) layer_kernel(LayerParams p) {
 
   // ---- the shared expert needs no routing: warps 1.. stream its gate/up rows
   // (split over every CTA) while warp 0 routes the call
-  const bool early_shared = p.has_shared && x_bulk;
+  const bool early_shared = p.has_shared && x_bulk && WD != MOE_FP4;  // FP4 converts x first
   if (early_shared && threadIdx.x >= 32) {
     const WarpGroup rest{1, kWarps - 1, 1};
     if (threadIdx.x == 32) {
@@ -613,7 +634,7 @@ __global__ void __launch_bounds__(kThreads, 1) layer_kernel(LayerParams p) {
       tb.pair0[kEarlyItem] = -1;
     }
     rest.sync();  // the entry and the activations' mbarrier are initialised
-    if (mbar_wait(&s_xin, 0)) phase1<WD, MAXT, false>(p, tb, kEarlyItem, kEarlyItem + 1, 0, G, xs, rest);
+    if (mbar_wait(&s_xin, 0)) phase1<WD, MAXT, false>(p, tb, kEarlyItem, kEarlyItem + 1, 0, G, x_dot<WD>(xs), rest);
   }
 
   // ---- 0. routing and lookup (every CTA); victims, plan, summary (control CTA)
@@ -662,6 +683,10 @@ __global__ void __launch_bounds__(kThreads, 1) layer_kernel(LayerParams p) {
     poison_rows<WD>(p, n0, nrows);
     return;
   }
+  if constexpr (WD == MOE_FP4) {
+    x_to_f16<WD>(xs, B * H);
+    __syncthreads();
+  }
   // this CTA has read the residency table: the control CTA may commit
   if (threadIdx.x == 0) atomicAdd(&cseq().wave_ctr[kLookupCtr], 1u);
 
@@ -669,7 +694,7 @@ __global__ void __launch_bounds__(kThreads, 1) layer_kernel(LayerParams p) {
   // 1..), one grid barrier, then every CTA's W_down rows; the control CTA
   // commits recency and residency meanwhile, once every CTA has done its lookups
   // (the shared expert, item n_res - 1, already done when early_shared)
-  if (!ctrl) phase1<WD, MAXT, false>(p, tb, 0, early_shared ? n_res - 1 : n_res, 1, G - 1, xs);
+  if (!ctrl) phase1<WD, MAXT, false>(p, tb, 0, early_shared ? n_res - 1 : n_res, 1, G - 1, x_dot<WD>(xs));
   if (rec) p.tl[2] = globaltimer_ns();
   if (p.tl && !ctrl && threadIdx.x == 0) {
     const unsigned long long now = globaltimer_ns();
@@ -723,7 +748,7 @@ __global__ void __launch_bounds__(kThreads, 1) layer_kernel(LayerParams p) {
     // the link
     const int n_all = load_items(p, pl, 1, tb, n_res, true);
     copy_down_rows<WD>(p, tb, n_res, n_all, n0, nrows);
-    if (!ctrl) phase1<WD, MAXT, false, true>(p, tb, n_res, n_all, 1, G - 1, xs);
+    if (!ctrl) phase1<WD, MAXT, false, true>(p, tb, n_res, n_all, 1, G - 1, x_dot<WD>(xs));
     if (!grid_barrier(p.bar, p.err)) {
       poison_rows<WD>(p, n0, nrows);
       return;
@@ -740,7 +765,7 @@ __global__ void __launch_bounds__(kThreads, 1) layer_kernel(LayerParams p) {
         break;
       }
       if (rec && f == 0) p.tl[5] = globaltimer_ns();
-      phase1<WD, MAXT, true>(p, tb, f, f + 1, 0, G, xs);
+      phase1<WD, MAXT, true>(p, tb, f, f + 1, 0, G, x_dot<WD>(xs));
     }
     if (rec) p.tl[6] = globaltimer_ns();
     if (!grid_barrier(p.bar, p.err)) {
@@ -826,7 +851,11 @@ __global__ void __launch_bounds__(kThreads, 1) layer_finish_kernel(LayerParams p
     uint4* dst = reinterpret_cast<uint4*>(xs);
     for (int i = threadIdx.x; i < nvec; i += blockDim.x) dst[i] = src[i];
     __syncthreads();
-    phase1<WD, MAXT, false>(p, tb, 0, nf, 0, G, xs);
+    if constexpr (WD == MOE_FP4) {
+      x_to_f16<WD>(xs, B * H);
+      __syncthreads();
+    }
+    phase1<WD, MAXT, false>(p, tb, 0, nf, 0, G, x_dot<WD>(xs));
     if (!grid_barrier(p.bar, p.err)) {
       poison_rows<WD>(p, n0, nrows);
       return;

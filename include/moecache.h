@@ -304,7 +304,7 @@ moe_status moe_cache_set_profiling(moe_cache_t cache, int32_t on);
  * done, 5 first fill's first half landed, 6 gate/up rows of the fills done, 7
  * plan of the fills read, 8 last fill's second half landed, 9 end, 10 control
  * CTA: victims and plan written, 11 control CTA: recency committed, 12 router
- * done, 13 residency row in shared memory, 14 lookups and grouping done,
+ * done, 13 the router starts loading the first token's logits, 14 lookups and grouping done,
  * 15 the first token's router logits loaded; over all CTAs: 16 the first and
  * 17 the last to finish the gate/up rows of the resident experts, 18 the last
  * to finish routing and lookup, 19 the last to end.  A call that never
