@@ -349,21 +349,21 @@ __device__ __forceinline__ void fp4_chunk_tokens(uint4 w, unsigned short sc2, in
       for (int b = 0; b < 8; ++b) s1 = fma_h<1>(h[b], xw[b], fma_h<0>(h[b], xw[b], s1));
       acc[q] += fmaf(s1, s.y, a0[q] * s.x);
     }
-    return;
-  }
-  float v[16], a0[MAXT];
-  fp4_half(w.x, w.y, v);
+  } else {
+    float v[16], a0[MAXT];
+    fp4_half(w.x, w.y, v);
 #pragma unroll
-  for (int q = 0; q < MAXT; ++q) {
-    if (q >= ntok) break;
-    a0[q] = block16_sum(v, (const VT*)xs_of(q));
-  }
-  fp4_half(w.z, w.w, v);
-  const float2 s = e4m3x2_to_float2(sc2);
+    for (int q = 0; q < MAXT; ++q) {
+      if (q >= ntok) break;
+      a0[q] = block16_sum(v, (const VT*)xs_of(q));
+    }
+    fp4_half(w.z, w.w, v);
+    const float2 s = e4m3x2_to_float2(sc2);
 #pragma unroll
-  for (int q = 0; q < MAXT; ++q) {
-    if (q >= ntok) break;
-    acc[q] += fmaf(block16_sum(v, (const VT*)xs_of(q) + 16), s.y, a0[q] * s.x);
+    for (int q = 0; q < MAXT; ++q) {
+      if (q >= ntok) break;
+      acc[q] += fmaf(block16_sum(v, (const VT*)xs_of(q) + 16), s.y, a0[q] * s.x);
+    }
   }
 }
 
