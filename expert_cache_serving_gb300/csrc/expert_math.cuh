@@ -170,12 +170,30 @@ __device__ __forceinline__ float dot8_bf16w(uint4 w, float4 a, float4 b) {
   return acc;
 }
 
+// acc + a * b with bf16 a, b (the halves of two words picked by HI) in one
+// float32 rounding: the product of two bf16 values is exact in float32, so
+// this is fmaf((float)a, (float)b, acc) bit for bit (acc = -0 gives a * b).
+template <int HI>
+__device__ __forceinline__ float fma_bf(uint32_t a2, uint32_t b2, float acc) {
+  const unsigned short a = (unsigned short)(HI ? a2 >> 16 : a2), b = (unsigned short)(HI ? b2 >> 16 : b2);
+  asm("fma.rn.f32.bf16 %0, %1, %2, %0;" : "+f"(acc) : "h"(a), "h"(b));
+  return acc;
+}
+
+// bf16 weights against bf16 activations: dot8_bf16w's operations in its order,
+// as mixed-precision FMAs on the bf16 pairs (no conversions).
 template <>
 __device__ __forceinline__ float chunk_dot<MOE_BF16, __nv_bfloat16>(uint4 w, unsigned short, const __nv_bfloat16* xs) {
-  uint4 xv = *reinterpret_cast<const uint4*>(xs);
-  float4 a = make_float4(bf16lo(xv.x), bf16hi(xv.x), bf16lo(xv.y), bf16hi(xv.y));
-  float4 b = make_float4(bf16lo(xv.z), bf16hi(xv.z), bf16lo(xv.w), bf16hi(xv.w));
-  return dot8_bf16w(w, a, b);
+  const uint4 xv = *reinterpret_cast<const uint4*>(xs);
+  float acc = fma_bf<0>(w.x, xv.x, -0.0f);
+  acc = fma_bf<1>(w.x, xv.x, acc);
+  acc = fma_bf<0>(w.y, xv.y, acc);
+  acc = fma_bf<1>(w.y, xv.y, acc);
+  acc = fma_bf<0>(w.z, xv.z, acc);
+  acc = fma_bf<1>(w.z, xv.z, acc);
+  acc = fma_bf<0>(w.w, xv.w, acc);
+  acc = fma_bf<1>(w.w, xv.w, acc);
+  return acc;
 }
 
 template <>
