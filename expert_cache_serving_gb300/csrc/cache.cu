@@ -863,7 +863,7 @@ extern "C" moe_status moe_layer_forward_ex(moe_cache_t c, int32_t layer, const v
     tl_row = c->tl_next;
     c->tl_next = (c->tl_next + 1) % kTlRing;
     p.tl = c->d_tl + (size_t)tl_row * kTlStamps;
-    CU_TRY(cudaMemsetAsync(p.tl, 0, kTlStamps * sizeof(unsigned long long), s));
+    p.tl_next = c->d_tl + (size_t)c->tl_next * kTlStamps;  // cleared by this call (no launch in between)
   }
   cudaEvent_t ta = nullptr, tb = nullptr;
   if (c->profiling) {
@@ -1163,6 +1163,10 @@ extern "C" moe_status moe_cache_set_profiling(moe_cache_t c, int32_t on) {
   c->profile_level = on;
   if (on >= 2 && !c->d_tl)
     CU_TRY(cudaMalloc(&c->d_tl, sizeof(unsigned long long) * kTlRing * kTlStamps));
+  if (on >= 2) {  // each call clears the row of the call after it; the first row starts clear
+    CU_TRY(cudaDeviceSynchronize());
+    CU_TRY(cudaMemset(c->d_tl + (size_t)c->tl_next * kTlStamps, 0, kTlStamps * sizeof(unsigned long long)));
+  }
   return MOE_OK;
 }
 

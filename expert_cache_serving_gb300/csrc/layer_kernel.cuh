@@ -529,6 +529,7 @@ __device__ void poison_rows(const LayerParams& p, int n0, int nrows) {
 }
 
 constexpr int kLookupCtr = 0;  // per-call counter of CTAs done with the residency lookups
+constexpr int kTlSlots = 20;   // phase timestamps per call (profiling)
 
 // Wait (thread 0 of the group polls, the group waits on it) until *c >=
 // target; false after limit_ns (MOE_ERR_TIMEOUT is then recorded).
@@ -595,6 +596,7 @@ __global__ void __launch_bounds__(kThreads, 1) layer_kernel(LayerParams p) {
   grid_dep_wait();  // the previous call's commit and outputs are visible
   grid_dep_launch();
   if (rec) p.tl[0] = globaltimer_ns();
+  if (p.tl_next && blockIdx.x == 0 && threadIdx.x >= 32 && threadIdx.x < 32 + kTlSlots) p.tl_next[threadIdx.x - 32] = 0ull;
   // warp 0 goes straight to the router (token 0): set-up with fences or
   // long-latency operations runs in other warps
   if (threadIdx.x == kThreads - 96) {

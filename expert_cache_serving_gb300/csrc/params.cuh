@@ -49,6 +49,7 @@ struct LayerParams {
   int32_t* oldest;            // [kMaxU] oldest slots, ascending key
   int* oldest_n;              // entries in it, -1 if invalid
   unsigned long long* tl;     // optional phase timestamps of this call [20] (profiling)
+  unsigned long long* tl_next;  // the next call's timestamp row, cleared by this call
   // optional inspection outputs
   int32_t* aux_ids;
   float* aux_w;
