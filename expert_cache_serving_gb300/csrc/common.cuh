@@ -187,11 +187,11 @@ __device__ __forceinline__ void fence_mbar_init() { asm volatile("fence.mbarrier
 __device__ __forceinline__ bool grid_barrier(unsigned long long* count, int* err,
                                              unsigned long long limit_ns = 2000000000ull) {
   __shared__ int s_ok;
-  __threadfence();  // publish this thread's global writes before arriving
-  __syncthreads();
+  __syncthreads();  // the CTA's global writes happen before thread 0's fence (cumulative)
   if (threadIdx.x == 0) {
     s_ok = 1;
     const unsigned long long G = gridDim.x;
+    __threadfence();  // publish the CTA's writes before arriving
     const unsigned long long target = (atomicAdd(count, 1ull) / G + 1) * G;
     const unsigned long long t0 = globaltimer_ns();
     while (ld_acquire_u64(count) < target) {

@@ -407,6 +407,63 @@ __device__ void phase2(const LayerParams& p, const ItemTable& tb, int ib, int ie
     // l, l + 8, l + 16, ... of unit u0 + g in increasing order (8 in flight),
     // then the group's 8 partial sums reduce by a fixed butterfly
     const int rg = lane / kLanesPerRow, gl = lane % kLanesPerRow;
+    if constexpr (MAXT == 1) {
+      // one token per item: a row group takes two rows of the same item at
+      // once, so each h chunk read from shared memory serves both (each row
+      // keeps the order above: same chunks, same butterfly)
+      const int npr = (nrows + 1) / 2;
+      const int nunits2 = (g1 - g0) * npr;
+      for (int u0 = warp * kRowsPerWarp; u0 < nunits2; u0 += grp.nw * kRowsPerWarp) {
+        const int unit = u0 + rg;
+        const bool live = unit < nunits2;
+        const int gi = live ? g0 + unit / npr : g0;
+        const int ra = live ? 2 * (unit % npr) : 0;
+        const bool live_b = live && ra + 1 < nrows;
+        const uint8_t *da = nullptr, *sa = nullptr, *db = nullptr, *sb = nullptr;
+        if (live) down_row<WD, STAGED>(tb, gi, gi, n0 + ra, n0, nrows, H, I, stage, pitch, &da, &sa);
+        if (live_b) down_row<WD, STAGED>(tb, gi, gi, n0 + ra + 1, n0, nrows, H, I, stage, pitch, &db, &sb);
+        const float* hrow = hs + (int64_t)(tb.hbase[gi] - tb.hbase[g0]) * hrow_f;
+        float acc_a = 0.f, acc_b = 0.f;
+        constexpr int CPL = 4;
+        for (int c0 = 0; c0 < nchunks; c0 += kLanesPerRow * CPL) {
+          uint4 wa[CPL], wb[CPL];
+          unsigned short ca[CPL], cb[CPL];
+#pragma unroll
+          for (int u = 0; u < CPL; ++u) {
+            const int c = c0 + gl + kLanesPerRow * u;
+            if (live && c < nchunks) {
+              wa[u] = ld_down16<FRESH, STAGED>(da + (int64_t)c * 16);
+              ca[u] = (WD == MOE_FP4) ? ld_down2<FRESH, STAGED>(sa + 2 * c) : (unsigned short)0;
+            }
+            if (live_b && c < nchunks) {
+              wb[u] = ld_down16<FRESH, STAGED>(db + (int64_t)c * 16);
+              cb[u] = (WD == MOE_FP4) ? ld_down2<FRESH, STAGED>(sb + 2 * c) : (unsigned short)0;
+            }
+          }
+#pragma unroll
+          for (int u = 0; u < CPL; ++u) {
+            const int c = c0 + gl + kLanesPerRow * u;
+            const float* hc = hrow + (int64_t)c * CS;
+            if (live && c < nchunks) acc_a += chunk_dot<WD, float>(wa[u], ca[u], hc);
+            if (live_b && c < nchunks) acc_b += chunk_dot<WD, float>(wb[u], cb[u], hc);
+          }
+        }
+        acc_a += __shfl_xor_sync(0xFFFFFFFFu, acc_a, 4);
+        acc_a += __shfl_xor_sync(0xFFFFFFFFu, acc_a, 2);
+        acc_a += __shfl_xor_sync(0xFFFFFFFFu, acc_a, 1);
+        acc_b += __shfl_xor_sync(0xFFFFFFFFu, acc_b, 4);
+        acc_b += __shfl_xor_sync(0xFFFFFFFFu, acc_b, 2);
+        acc_b += __shfl_xor_sync(0xFFFFFFFFu, acc_b, 1);
+        if (live && gl == 0) {
+          int t, hr, j;
+          item_token(p, tb, gi, 0, &t, &hr, &j);
+          os[ra * ostride + t * (k + 1) + j] = acc_a;
+          if (live_b) os[(ra + 1) * ostride + t * (k + 1) + j] = acc_b;
+        }
+      }
+      g0 = g1;
+      continue;
+    }
     const int nunits = (g1 - g0) * nrows;
     for (int u0 = warp * kRowsPerWarp; u0 < nunits; u0 += grp.nw * kRowsPerWarp) {
       const int unit = u0 + rg;
