@@ -202,7 +202,26 @@ __device__ void phase1(const LayerParams& p, const ItemTable& tb, int ib, int ie
   if (rel < 0 || rel >= ncta || ie <= ib) return;
   const int H = p.H, I = p.I, lane = threadIdx.x & 31, warp = grp.tid() >> 5;
   const int64_t total = (int64_t)(ie - ib) * I;
-  const int64_t t0 = (int64_t)rel * total / ncta, t1 = (int64_t)(rel + 1) * total / ncta;
+  int64_t t0 = (int64_t)rel * total / ncta, t1 = (int64_t)(rel + 1) * total / ncta;
+  if constexpr (MAXT > 1) {
+    // rows of experts with more tokens cost more: split the rows so that each
+    // CTA gets an equal share of rows x (tokens + 1) (the row's loads and
+    // conversions, then one pass per token); every CTA computes the same split
+    int64_t wtot = 0;
+    for (int it = ib; it < ie; ++it) wtot += (int64_t)I * (tb.ntok[it] + 1);
+    const int64_t w0 = rel * wtot / ncta, w1 = (rel + 1) * wtot / ncta;
+    auto row_at = [&](int64_t wq) -> int64_t {  // first row whose weight span ends after wq
+      int64_t acc = 0;
+      for (int it = ib; it < ie; ++it) {
+        const int64_t per = tb.ntok[it] + 1, span = (int64_t)I * per;
+        if (wq < acc + span) return (int64_t)(it - ib) * I + (wq - acc + per - 1) / per;
+        acc += span;
+      }
+      return total;
+    };
+    t0 = row_at(w0);
+    t1 = rel + 1 == ncta ? total : row_at(w1);
+  }
   const int nchunks = H / EPC;
   const int64_t rb = F::row_bytes(H);
   auto row_task = [&](int64_t task) {
