@@ -56,8 +56,16 @@ def build_synth(verbose=False) -> str:
     return SYNTH_LIB
 
 
-def build_cuda(verbose=False) -> str:
-    os.makedirs(OBJDIR, exist_ok=True)
+DEBUG_LIBDIR = os.path.join(PKG, "_lib_debug")
+DEBUG_LIB = os.path.join(DEBUG_LIBDIR, "libmoecache.so")
+
+
+def build_cuda(verbose=False, debug=False) -> str:
+    """debug: the bounds-checked build (-DMOE_DEBUG_BOUNDS) in _lib_debug/."""
+    objdir = os.path.join(DEBUG_LIBDIR, "obj") if debug else OBJDIR
+    lib = DEBUG_LIB if debug else LIB
+    extra = ["-DMOE_DEBUG_BOUNDS"] if debug else []
+    os.makedirs(objdir, exist_ok=True)
     nvcc = _nvcc()
     srcs = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
     if not srcs:
@@ -71,18 +79,18 @@ def build_cuda(verbose=False) -> str:
         if base == LAYER_INST:
             for fmt in (0, 1, 2):
                 for maxt in (1, 2, 4, 8, 16):
-                    units.append((s, [f"-DMOE_LAYER_FMT={fmt}", f"-DMOE_LAYER_MAXT={maxt}"],
-                                  os.path.join(OBJDIR, f"{base}.{fmt}.{maxt}.o")))
+                    units.append((s, extra + [f"-DMOE_LAYER_FMT={fmt}", f"-DMOE_LAYER_MAXT={maxt}"],
+                                  os.path.join(objdir, f"{base}.{fmt}.{maxt}.o")))
         else:
-            units.append((s, [], os.path.join(OBJDIR, base + ".o")))
+            units.append((s, extra, os.path.join(objdir, base + ".o")))
     objs = [o for _, _, o in units]
     workers = max(1, min(len(units), os.cpu_count() or 8))
     with cf.ThreadPoolExecutor(max_workers=workers) as ex:
         jobs = [ex.submit(_run, [nvcc] + ARCH + NVCC_FLAGS + defs + ["-c", s, "-o", o], verbose) for s, defs, o in units]
         for j in jobs:
             j.result()
-    _run([nvcc] + ARCH + ["-shared", "-cudart", "static", "-o", LIB] + objs + ["-lpthread", "-ldl", "-lrt"], verbose)
-    return LIB
+    _run([nvcc] + ARCH + ["-shared", "-cudart", "static", "-o", lib] + objs + ["-lpthread", "-ldl", "-lrt"], verbose)
+    return lib
 
 
 def build_all(verbose=False) -> None:

@@ -20,6 +20,7 @@
 #include <new>
 #include <string>
 #include <thread>
+#include <mutex>
 #include <vector>
 
 #include "params.cuh"
@@ -697,6 +698,42 @@ static cudaError_t launch_k1(moe_cache* c, const LayerParams& p, cudaStream_t s)
   return launch_layer(c->d.wdtype, p, c->grid, c->smem, false, s);
 }
 
+// Bounds-check counters of the debug build: one device pair per process
+// (current device at first use), zero at start.
+unsigned* moe::debug_counters() {
+  static unsigned* d = nullptr;
+  static std::mutex m;
+  std::lock_guard<std::mutex> lk(m);
+  if (!d) {
+    if (cudaMalloc(&d, 2 * sizeof(unsigned)) != cudaSuccess || cudaMemset(d, 0, 2 * sizeof(unsigned)) != cudaSuccess) {
+      cudaGetLastError();
+      d = nullptr;
+    }
+  }
+  return d;
+}
+
+extern "C" int32_t moe_debug_bounds_enabled(void) {
+#ifdef MOE_DEBUG_BOUNDS
+  return 1;
+#else
+  return 0;
+#endif
+}
+
+extern "C" moe_status moe_debug_violations(int64_t* count, int32_t* first_site) {
+  g_err.clear();
+  if (!count || !first_site) return fail(MOE_ERR_INVALID_ARG, "NULL argument");
+  unsigned h[2] = {0u, 0u};
+  if (unsigned* d = debug_counters()) {
+    CU_TRY(cudaDeviceSynchronize());
+    CU_TRY(cudaMemcpy(h, d, sizeof(h), cudaMemcpyDeviceToHost));
+  }
+  *count = h[0];
+  *first_site = (int32_t)h[1];
+  return MOE_OK;
+}
+
 // The fields of one call's LayerParams that do not depend on its sequence number.
 static LayerParams call_params(moe_cache* c, int32_t layer, const void* x, const float* lg, int32_t B, void* y,
                                const moe_layer_aux* aux) {
@@ -736,6 +773,7 @@ static LayerParams call_params(moe_cache* c, int32_t layer, const void* x, const
   p.stage_off = c->stage_off;
   p.oldest = c->d_oldest;
   p.oldest_n = c->d_oldest_n;
+  p.dbg = debug_counters();
   if (aux) {
     p.aux_ids = aux->ids; p.aux_w = aux->weights; p.aux_slots = aux->slots;
     p.aux_perm = aux->perm; p.aux_offsets = aux->offsets; p.aux_logits = aux->logits;

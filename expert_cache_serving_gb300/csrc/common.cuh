@@ -17,6 +17,29 @@ constexpr int kMaxItems = kMaxU + 1; // + shared expert
 constexpr int kThreads = 512;  // layer kernel CTA size
 constexpr int kWarps = kThreads / 32;
 constexpr unsigned kFlagError = 0x80000000u;  // fill flag: the copy was not issued
+// Bounds checks of the debug build (compiled with -DMOE_DEBUG_BOUNDS, the
+// stand-in for a memory checker): in_bounds(dbg, ok, site) is true when the
+// index it guards is valid; when it is not, the debug build counts the
+// violation in dbg[0], keeps the first site in dbg[1] and returns false so
+// the caller skips the access.  The release build checks nothing (always
+// true; the condition is dead code).
+__device__ __forceinline__ bool in_bounds(unsigned* dbg, bool ok, unsigned site) {
+#ifdef MOE_DEBUG_BOUNDS
+  if (!ok) {
+    if (dbg) {
+      atomicAdd(dbg, 1u);
+      atomicCAS(dbg + 1, 0u, site);
+    }
+    return false;
+  }
+#else
+  (void)dbg;
+  (void)ok;
+  (void)site;
+#endif
+  return true;
+}
+
 constexpr int kWaveCtrs = 16;  // per-call counters of the layer kernel (two sets, by call parity)
 
 // Per-call plan written by the control kernel into device memory and read by

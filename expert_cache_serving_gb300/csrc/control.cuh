@@ -331,7 +331,8 @@ static __device__ int route_lookup(const LayerParams& p, CtrlSmem& cs, bool writ
 
 
   // ---- dedup: U = sorted distinct routed experts ----------------------------------
-  if (tid < npairs) atomicOr(&cs.bits[cs.ids[tid] >> 5], 1u << (cs.ids[tid] & 31));
+  if (tid < npairs && in_bounds(p.dbg, cs.ids[tid] >= 0 && cs.ids[tid] < E, 8))
+    atomicOr(&cs.bits[cs.ids[tid] >> 5], 1u << (cs.ids[tid] & 31));
   __syncthreads();
   const int nwords = (E + 31) / 32;
   if (warp == 0) {
@@ -498,6 +499,7 @@ static __device__ int choose_victims(const LayerParams& p, CtrlSmem& cs) {
     const int key = p.layer * E + cs.U[tid];
     const int fill = cs.fill[tid];
     const int s = fill ? cs.victim[cs.mrank[tid]] : cs.slot[tid];
+    in_bounds(p.dbg, s >= 0 && s < C && (!fill || cs.mrank[tid] < kMaxU), 9);  // recorded; the host sees the count
     cs.slot[tid] = s;
     plan->u_key[tid] = key;
     plan->u_expert[tid] = cs.U[tid];

@@ -81,6 +81,9 @@ static __device__ int load_items(const LayerParams& p, const Plan* pl, int which
       tb.ntok[at + i] = p.B;
       tb.pair0[at + i] = -1;
     } else {
+      if (!in_bounds(p.dbg, r >= 0 && r < kMaxU && pl->u_slot[r] >= 0 && pl->u_slot[r] < p.C &&
+                                pl->u_key[r] >= 0 && pl->u_key[r] < p.L * p.E && at + i < kMaxItems, 2))
+        continue;
       uint8_t* slot = const_cast<uint8_t*>(p.slots) + (int64_t)pl->u_slot[r] * p.S;
       tb.rec[at + i] = from_pool ? p.pool + (int64_t)pl->u_key[r] * p.S : slot;
       tb.dst[at + i] = from_pool ? slot : nullptr;
@@ -167,9 +170,11 @@ __device__ void copy_down_rows(const LayerParams& p, const ItemTable& tb, int ib
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const int v = v0 + u * (int)blockDim.x;
-      if (v < total)
-        *reinterpret_cast<uint4*>(const_cast<uint8_t*>(down_unit<WD>(tb.dst[ib + v / per], H, I, n0, nv, v % per))) =
-            buf[u];
+      if (v < total) {
+        const uint8_t* d = tb.dst[ib + v / per];
+        if (in_bounds(p.dbg, d >= p.slots && d < p.slots + p.C * p.S, 7))
+          *reinterpret_cast<uint4*>(const_cast<uint8_t*>(down_unit<WD>(d, H, I, n0, nv, v % per))) = buf[u];
+      }
     }
   }
 }
@@ -187,6 +192,11 @@ __device__ __forceinline__ void item_token(const LayerParams& p, const ItemTable
     *t = pair / p.k;
     *hrow = pair;
     *j = pair % p.k;
+    if (!in_bounds(p.dbg, p0 + q >= 0 && p0 + q < p.B * p.k && pair >= 0 && pair < p.B * p.k, 3)) {
+      *t = 0;
+      *hrow = 0;
+      *j = 0;
+    }
   }
 }
 
@@ -350,6 +360,7 @@ __host__ __device__ constexpr int h_chunk_stride() { return WD == MOE_FP4 ? 36 :
 template <int WD, int MAXT, bool FRESH, bool STAGED = false>
 __device__ void phase2(const LayerParams& p, const ItemTable& tb, int ib, int ie, int n0, int nrows, float* hs,
                        float* os, const uint8_t* stage = nullptr, int pitch = 0, WarpGroup grp = whole_cta()) {
+  if (STAGED && !in_bounds(p.dbg, ie <= p.stage_items && nrows <= p.rows_per_cta_max, 5)) return;
   using F = Fmt<WD>;
   constexpr int EPC = F::kElemsPerChunk;
   constexpr int kLanesPerRow = 8, kRowsPerWarp = 32 / kLanesPerRow;
@@ -476,8 +487,9 @@ __device__ void phase2(const LayerParams& p, const ItemTable& tb, int ib, int ie
         if (live && gl == 0) {
           int t, hr, j;
           item_token(p, tb, gi, 0, &t, &hr, &j);
-          os[ra * ostride + t * (k + 1) + j] = acc_a;
-          if (live_b) os[(ra + 1) * ostride + t * (k + 1) + j] = acc_b;
+          const bool okr = in_bounds(p.dbg, ra + (live_b ? 1 : 0) < p.rows_per_cta_max && t < B && j <= k, 4);
+          if (okr) os[ra * ostride + t * (k + 1) + j] = acc_a;
+          if (okr && live_b) os[(ra + 1) * ostride + t * (k + 1) + j] = acc_b;
         }
       }
       g0 = g1;
@@ -530,7 +542,8 @@ __device__ void phase2(const LayerParams& p, const ItemTable& tb, int ib, int ie
         if (live && gl == 0 && q < ntok) {
           int t, hr, j;
           item_token(p, tb, gi, q, &t, &hr, &j);
-          os[(row - n0) * ostride + t * (k + 1) + j] = a;
+          if (in_bounds(p.dbg, row - n0 < p.rows_per_cta_max && t < B && j <= k, 4))
+            os[(row - n0) * ostride + t * (k + 1) + j] = a;
         }
       }
     }
@@ -551,6 +564,7 @@ static __device__ int local_items(const LayerParams& p, const CtrlSmem& cs, Item
   for (int r = threadIdx.x; r < n_u; r += blockDim.x) {
     if (cs.fill[r]) continue;
     const int i = r - cs.mrank[r];  // hits before rank r
+    if (!in_bounds(p.dbg, cs.slot[r] >= 0 && cs.slot[r] < p.C && i >= 0 && i < kMaxItems, 1)) continue;
     tb.rec[i] = p.slots + (int64_t)cs.slot[r] * p.S;
     tb.dst[i] = nullptr;
     tb.pair0[i] = cs.off[r];
@@ -580,6 +594,7 @@ __device__ __forceinline__ void combine_rows(const LayerParams& p, const ItemTab
   const int B = p.B, k = p.k, H = p.H, ostride = B * (k + 1);
   for (int e = threadIdx.x; e < nrows * B; e += blockDim.x) {
     const int nl = e / B, t = e % B, n = n0 + nl;
+    if (!in_bounds(p.dbg, n < H && nl < p.rows_per_cta_max, 6)) continue;
     const float* o = os + nl * ostride + t * (k + 1);
     float acc = 0.f;
     for (int j = 0; j < k; ++j) acc = fmaf(tb.pair_w[t * k + j], o[j], acc);

@@ -50,6 +50,7 @@ struct LayerParams {
   int* oldest_n;              // entries in it, -1 if invalid
   unsigned long long* tl;     // optional phase timestamps of this call [20] (profiling)
   unsigned long long* tl_next;  // the next call's timestamp row, cleared by this call
+  unsigned* dbg;              // bounds-check counters of the debug build ([0] count, [1] first site)
   // optional inspection outputs
   int32_t* aux_ids;
   float* aux_w;
@@ -71,6 +72,7 @@ cudaError_t launch_layer_finish(int wdtype, const LayerParams& p, int grid, size
 int layer_max_grid(int wdtype, size_t smem);
 cudaError_t launch_slot_moves(uint8_t* base, int64_t S, const int32_t* moves, int n_moves, cudaStream_t s);
 void set_last_error(const char* msg);  // message returned by moe_last_error() on this thread
+unsigned* debug_counters();  // the process's bounds-check counters (device, [2]); null if unavailable
 
 // prefill (prefill.cu)
 cudaError_t prefill_route(const float* logits, int T, int E, int k, int32_t* ids, float* w, cudaStream_t s);

@@ -109,7 +109,8 @@ __global__ void __launch_bounds__(1024) group_scan_kernel(const int32_t* cnt, in
 // place the chunk's pairs in order: warps one after the other, ranks within a
 // warp from the peer mask of equal groups
 __global__ void __launch_bounds__(1024) group_place_kernel(const int32_t* ids, int Tk, int n_pairs, int E, int G,
-                                                           const int32_t* base, int32_t* pos, int32_t* perm) {
+                                                           const int32_t* base, int32_t* pos, int32_t* perm,
+                                                           unsigned* dbg) {
   extern __shared__ int32_t run[];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   for (int g = threadIdx.x; g < G; g += blockDim.x) run[g] = base[(size_t)blockIdx.x * G + g];
@@ -124,7 +125,7 @@ __global__ void __launch_bounds__(1024) group_place_kernel(const int32_t* ids, i
     if (warp == w && valid) {
       const int at = run[g] + rank;
       pos[p] = at;
-      perm[at] = p;
+      if (in_bounds(dbg, at >= 0 && at < n_pairs, 101)) perm[at] = p;
       __syncwarp(peers);
       if (leader) run[g] += __popc(peers);
     }
@@ -138,13 +139,14 @@ __global__ void __launch_bounds__(1024) group_place_kernel(const int32_t* ids, i
 // the f16 subnormal grid (absolute error <= 2^-25).
 template <bool TO_F16>
 __global__ void gather_kernel(const __nv_bfloat16* __restrict__ x, int Tk, int k, int H, int n_pairs,
-                              const int32_t* __restrict__ perm, __nv_bfloat16* __restrict__ xp) {
+                              const int32_t* __restrict__ perm, __nv_bfloat16* __restrict__ xp, unsigned* dbg) {
   const int per = H / 8;  // 16-byte vectors per row
   const int64_t total = (int64_t)n_pairs * per;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
     const int row = (int)(i / per), v = (int)(i % per);
     const int p = perm[row];
     const int t = p < Tk ? p / k : p - Tk;
+    if (!in_bounds(dbg, p >= 0 && p < n_pairs && t < (Tk / k), 102)) continue;
     uint4 val = reinterpret_cast<const uint4*>(x + (int64_t)t * H)[v];
     if constexpr (TO_F16) {
       uint32_t* w = reinterpret_cast<uint32_t*>(&val);
@@ -162,13 +164,14 @@ __global__ void gather_kernel(const __nv_bfloat16* __restrict__ x, int Tk, int k
 // and e4m3 block scales [n_pairs][H/16]; one thread per 16-element block.
 __global__ void gather_quant_kernel(const __nv_bfloat16* __restrict__ x, int Tk, int k, int H, int n_pairs,
                                     const int32_t* __restrict__ perm, uint8_t* __restrict__ codes,
-                                    uint8_t* __restrict__ scales) {
+                                    uint8_t* __restrict__ scales, unsigned* dbg) {
   const int per = H / 16;
   const int64_t total = (int64_t)n_pairs * per;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
     const int row = (int)(i / per), b = (int)(i % per);
     const int p = perm[row];
     const int t = p < Tk ? p / k : p - Tk;
+    if (!in_bounds(dbg, p >= 0 && p < n_pairs && t < (Tk / k), 103)) continue;
     const uint4* src = reinterpret_cast<const uint4*>(x + (int64_t)t * H + (int64_t)b * 16);
     const uint4 v0 = src[0], v1 = src[1];
     const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
@@ -277,16 +280,19 @@ __global__ void __launch_bounds__(tc::nvf4::kThreads, 1)
 
 // ---- 6. combine ------------------------------------------------------------------------------
 __global__ void combine_kernel(const float* __restrict__ op, const int32_t* __restrict__ pos, const float* __restrict__ w,
-                               int T, int k, int H, int has_shared, __nv_bfloat16* __restrict__ y) {
+                               int T, int k, int H, int has_shared, __nv_bfloat16* __restrict__ y, unsigned* dbg) {
   const int per = H / 4;
   const int64_t total = (int64_t)T * per;
   const int Tk = T * k;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
     const int t = (int)(i / per), v = (int)(i % per);
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    const int n_pairs = Tk + (has_shared ? T : 0);
     for (int j = 0; j < k; ++j) {
       const float wj = w[(int64_t)t * k + j];
-      const float4 o = reinterpret_cast<const float4*>(op + (int64_t)pos[(int64_t)t * k + j] * H)[v];
+      const int at = pos[(int64_t)t * k + j];
+      if (!in_bounds(dbg, at >= 0 && at < n_pairs, 104)) continue;
+      const float4 o = reinterpret_cast<const float4*>(op + (int64_t)at * H)[v];
       acc.x = fmaf(wj, o.x, acc.x);
       acc.y = fmaf(wj, o.y, acc.y);
       acc.z = fmaf(wj, o.z, acc.z);
@@ -327,7 +333,8 @@ cudaError_t prefill_group(const int32_t* ids, int T, int k, int E, int has_share
   const int n_chunks = (n_pairs + 1023) / 1024;
   pf::group_count_kernel<<<n_chunks, 1024, G * sizeof(int32_t), s>>>(ids, Tk, n_pairs, E, G, cnt);
   pf::group_scan_kernel<<<1, 1024, 0, s>>>(cnt, n_chunks, G, base, offsets);
-  pf::group_place_kernel<<<n_chunks, 1024, G * sizeof(int32_t), s>>>(ids, Tk, n_pairs, E, G, base, pos, perm);
+  pf::group_place_kernel<<<n_chunks, 1024, G * sizeof(int32_t), s>>>(ids, Tk, n_pairs, E, G, base, pos, perm,
+                                                                       debug_counters());
   return cudaGetLastError();
 }
 
@@ -335,10 +342,10 @@ cudaError_t prefill_gather(const void* x, int T, int k, int H, int n_pairs, cons
                            int to_f16, cudaStream_t s) {
   if (to_f16)
     pf::gather_kernel<true><<<sms() * 8, 256, 0, s>>>((const __nv_bfloat16*)x, T * k, k, H, n_pairs, perm,
-                                                      (__nv_bfloat16*)xp);
+                                                      (__nv_bfloat16*)xp, debug_counters());
   else
     pf::gather_kernel<false><<<sms() * 8, 256, 0, s>>>((const __nv_bfloat16*)x, T * k, k, H, n_pairs, perm,
-                                                       (__nv_bfloat16*)xp);
+                                                       (__nv_bfloat16*)xp, debug_counters());
   return cudaGetLastError();
 }
 
@@ -413,7 +420,8 @@ cudaError_t prefill_gemm_down_fp4(const CUtensorMap& a, const CUtensorMap& codes
 
 cudaError_t prefill_gather_quant(const void* x, int T, int k, int H, int n_pairs, const int32_t* perm, uint8_t* codes,
                                  uint8_t* scales, cudaStream_t s) {
-  pf::gather_quant_kernel<<<sms() * 8, 256, 0, s>>>((const __nv_bfloat16*)x, T * k, k, H, n_pairs, perm, codes, scales);
+  pf::gather_quant_kernel<<<sms() * 8, 256, 0, s>>>((const __nv_bfloat16*)x, T * k, k, H, n_pairs, perm, codes, scales,
+                                                    debug_counters());
   return cudaGetLastError();
 }
 
@@ -466,7 +474,7 @@ cudaError_t prefill_gemm_down_nvf4(const CUtensorMap& ac, const CUtensorMap& as,
 
 cudaError_t prefill_combine(const float* op, const int32_t* pos, const float* w, int T, int k, int H, int has_shared,
                             void* y, cudaStream_t s) {
-  pf::combine_kernel<<<sms() * 8, 256, 0, s>>>(op, pos, w, T, k, H, has_shared, (__nv_bfloat16*)y);
+  pf::combine_kernel<<<sms() * 8, 256, 0, s>>>(op, pos, w, T, k, H, has_shared, (__nv_bfloat16*)y, debug_counters());
   return cudaGetLastError();
 }
 

@@ -11,7 +11,9 @@ from __future__ import annotations
 import ctypes
 import os
 
-_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib", "libmoecache.so")
+# MOECACHE_LIB selects another build of the library (the bounds-checked one)
+_LIB_PATH = os.environ.get("MOECACHE_LIB") or os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib",
+                                                           "libmoecache.so")
 
 MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_OOM, MOE_ERR_CAPACITY, MOE_ERR_BUSY, MOE_ERR_CUDA, MOE_ERR_TIMEOUT = range(7)
 MOE_FP32, MOE_BF16, MOE_FP4 = 0, 1, 2
@@ -106,6 +108,8 @@ SIGNATURES = {
     "moe_cache_inject_fill_failure": (_I32, [_P, _I32]),
     "moe_layer_forward_resident_noalloc": (_I32, [ctypes.POINTER(moe_model_desc), _P, _P, _P, _P, _I32, _P, _P]),
     "moe_cache_destroy": (_I32, [_P]),
+    "moe_debug_bounds_enabled": (_I32, []),
+    "moe_debug_violations": (_I32, [ctypes.POINTER(_I64), ctypes.POINTER(_I32)]),
     "moe_last_error": (ctypes.c_char_p, []),
     "moe_version": (_I32, []),
 }
@@ -256,6 +260,13 @@ def moe_cache_slot_ptr(cache: int, s: int) -> int | None:
 
 def moe_cache_set_fill_mode(cache: int, mode: int) -> None:
     check(lib.moe_cache_set_fill_mode(cache, mode), "moe_cache_set_fill_mode")
+
+
+def moe_debug_violations() -> tuple[int, int]:
+    """(count, first site) of the bounds checks of a debug build (0, 0 otherwise)."""
+    n, site = _I64(), _I32()
+    check(lib.moe_debug_violations(ctypes.byref(n), ctypes.byref(site)), "moe_debug_violations")
+    return n.value, site.value
 
 
 def moe_cache_set_graph_mode(cache: int, on: int) -> None:

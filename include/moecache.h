@@ -423,6 +423,19 @@ moe_status moe_layer_forward_resident_noalloc(const moe_model_desc* desc, const 
 /* Free everything the library allocated.  Synchronises. */
 moe_status moe_cache_destroy(moe_cache_t cache);
 
+/* Bounds checks of the debug build (the library compiled with
+ * -DMOE_DEBUG_BOUNDS, a stand-in for a device memory checker): every index
+ * the kernels derive from the cache state or the routing (slots, keys, pair
+ * positions, h rows, output rows) is checked before use; a bad one is
+ * counted and its access skipped.  moe_debug_bounds_enabled: 1 when this
+ * library has the checks, 0 otherwise. */
+int32_t moe_debug_bounds_enabled(void);
+
+/* Violations the checks counted in this process so far and the site of the
+ * first (0 if none).  Synchronises the device.  A release build reports 0.
+ * Errors: MOE_ERR_INVALID_ARG (NULL argument), MOE_ERR_CUDA. */
+moe_status moe_debug_violations(int64_t* count, int32_t* first_site);
+
 /* Message of the last error on this thread ("" if none). */
 const char* moe_last_error(void);
 

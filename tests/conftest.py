@@ -16,3 +16,16 @@ def pytest_configure(config):
 @pytest.fixture(scope="session")
 def root():
     return ROOT
+
+
+@pytest.fixture(autouse=True)
+def _no_bounds_violations():
+    """Under the bounds-checked build (MOE_EXPECT_DEBUG set by
+    test_gpu_debug_bounds), every test must leave the violation count at 0."""
+    yield
+    if os.environ.get("MOE_EXPECT_DEBUG"):
+        from expert_cache_serving_gb300 import moecache as mc
+
+        assert mc.lib.moe_debug_bounds_enabled() == 1, "MOECACHE_LIB is not the bounds-checked build"
+        count, site = mc.moe_debug_violations()
+        assert count == 0, f"{count} bounds violations, first at check site {site}"
