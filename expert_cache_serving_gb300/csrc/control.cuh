@@ -78,14 +78,14 @@ __device__ __forceinline__ float key_logit(unsigned key) {
 // logits, exp(l_r - l_0) / sum, in the order taken.
 template <int NQ>
 __device__ __forceinline__ void route_token(const float* lg, int E, int k, int lane, float* aux, int* ids, float* w,
-                                            unsigned long long* stamp = nullptr) {
+                                            unsigned long long* stamp = nullptr, const float* pre = nullptr) {
   unsigned key[NQ];
 #pragma unroll
   for (int q = 0; q < NQ; ++q) {
     const int e = lane + 32 * q;
     key[q] = 0u;
     if (e < E) {
-      const float x = lg[e];
+      const float x = pre ? pre[q] : lg[e];
       if (aux) aux[e] = x;
       key[q] = logit_key(x);
     }
@@ -291,7 +291,7 @@ __device__ __forceinline__ void publish_summary(const LayerParams& p) {
 // is only read here; the control CTA writes it after a grid barrier that every
 // CTA reaches after this lookup.  Returns MOE_ERR_CAPACITY (|U| > C) or MOE_OK
 // to every thread.
-static __device__ int route_lookup(const LayerParams& p, CtrlSmem& cs, bool write_aux) {
+static __device__ int route_lookup(const LayerParams& p, CtrlSmem& cs, bool write_aux, const float* pre = nullptr) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarp = blockDim.x >> 5;
   const bool rec = p.tl && blockIdx.x == 1 && tid == 0;
   const int E = p.E, k = p.k, B = p.B, npairs = B * k;
@@ -317,7 +317,7 @@ static __device__ int route_lookup(const LayerParams& p, CtrlSmem& cs, bool writ
     if (nq <= 1) route_token<1>(lg, E, k, lane, aux, ids, w, st);
     else if (nq <= 2) route_token<2>(lg, E, k, lane, aux, ids, w, st);
     else if (nq <= 4) route_token<4>(lg, E, k, lane, aux, ids, w, st);
-    else if (nq <= 8) route_token<8>(lg, E, k, lane, aux, ids, w, st);
+    else if (nq <= 8) route_token<8>(lg, E, k, lane, aux, ids, w, st, t == warp ? pre : nullptr);
     else if (nq <= 16) route_token<16>(lg, E, k, lane, aux, ids, w, st);
     else route_token<32>(lg, E, k, lane, aux, ids, w, st);
   }
