@@ -291,18 +291,23 @@ __device__ __forceinline__ void publish_summary(const LayerParams& p) {
 // is only read here; the control CTA writes it after a grid barrier that every
 // CTA reaches after this lookup.  Returns MOE_ERR_CAPACITY (|U| > C) or MOE_OK
 // to every thread.
-static __device__ int route_lookup(const LayerParams& p, CtrlSmem& cs, bool write_aux, const float* pre = nullptr) {
+// The layer's residency row as route_lookup reads it: entry tid + j * kThreads
+// in mrow[j] (issued at the kernel's start, next to the router's logits).
+__device__ __forceinline__ void load_map_row(const LayerParams& p, int* mrow) {
+#pragma unroll
+  for (int j = 0; j < kMaxE / kThreads; ++j) {
+    const int e = (int)threadIdx.x + j * kThreads;
+    mrow[j] = e < p.E ? p.st.map[p.layer * p.E + e] : -1;
+  }
+}
+
+// pre: the calling warp's first token's logits already in registers (E <= 256), or null.
+// mrow: the layer's residency row from load_map_row.
+static __device__ int route_lookup(const LayerParams& p, CtrlSmem& cs, bool write_aux, const int* mrow,
+                                   const float* pre = nullptr) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarp = blockDim.x >> 5;
   const bool rec = p.tl && blockIdx.x == 1 && tid == 0;
   const int E = p.E, k = p.k, B = p.B, npairs = B * k;
-  // the layer's residency row is loaded while the router's logits load (the
-  // two latencies overlap); stored to shared memory after the router
-  int mrow[kMaxE / kThreads];
-#pragma unroll
-  for (int j = 0; j < kMaxE / kThreads; ++j) {
-    const int e = tid + j * kThreads;
-    mrow[j] = e < E ? p.st.map[p.layer * E + e] : -1;
-  }
   for (int i = tid; i < kMaxE / 32; i += blockDim.x) cs.bits[i] = 0u;
 
   // ---- router: one warp per token ------------------------------------------------
@@ -314,10 +319,11 @@ static __device__ int route_lookup(const LayerParams& p, CtrlSmem& cs, bool writ
     float* w = cs.w + t * k;
     unsigned long long* st = rec && t == 0 ? p.tl + 15 : nullptr;
     if (rec && t == 0) p.tl[13] = globaltimer_ns();  // profiling: the router starts loading
-    if (nq <= 1) route_token<1>(lg, E, k, lane, aux, ids, w, st);
-    else if (nq <= 2) route_token<2>(lg, E, k, lane, aux, ids, w, st);
-    else if (nq <= 4) route_token<4>(lg, E, k, lane, aux, ids, w, st);
-    else if (nq <= 8) route_token<8>(lg, E, k, lane, aux, ids, w, st, t == warp ? pre : nullptr);
+    const float* tp = t == warp ? pre : nullptr;  // this warp's first token may be preloaded
+    if (nq <= 1) route_token<1>(lg, E, k, lane, aux, ids, w, st, tp);
+    else if (nq <= 2) route_token<2>(lg, E, k, lane, aux, ids, w, st, tp);
+    else if (nq <= 4) route_token<4>(lg, E, k, lane, aux, ids, w, st, tp);
+    else if (nq <= 8) route_token<8>(lg, E, k, lane, aux, ids, w, st, tp);
     else if (nq <= 16) route_token<16>(lg, E, k, lane, aux, ids, w, st);
     else route_token<32>(lg, E, k, lane, aux, ids, w, st);
   }

@@ -686,13 +686,11 @@ __global__ void __launch_bounds__(kThreads, 1) layer_kernel(LayerParams p) {
 
   grid_dep_wait();  // the previous call's commit and outputs are visible
   grid_dep_launch();
-#ifndef MOE_PRELOAD_LOGITS
-#define MOE_PRELOAD_LOGITS 0
-#endif
-  // the router warps' first token's logits, loaded before anything else
-  // (E <= 256: eight per lane)
+  // the router warps' first token's logits, requested before anything else
+  // (E <= 256: up to eight per lane): issued later, behind the CTA's other
+  // start-up traffic, they landed 3.5 us after the kernel started instead of 1.5
   float lg_pre[8];
-  const bool use_pre = MOE_PRELOAD_LOGITS && p.E > 128 && p.E <= 256 && (int)(threadIdx.x >> 5) < B;
+  const bool use_pre = p.E <= 256 && (int)(threadIdx.x >> 5) < B;
   if (use_pre) {
     const float* lg = p.logits + (size_t)(threadIdx.x >> 5) * p.E;
 #pragma unroll
@@ -701,6 +699,8 @@ __global__ void __launch_bounds__(kThreads, 1) layer_kernel(LayerParams p) {
       lg_pre[q] = e < p.E ? lg[e] : 0.f;
     }
   }
+  int mrow[kMaxE / kThreads];  // the layer's residency row, read in route_lookup
+  load_map_row(p, mrow);
   if (rec) p.tl[0] = globaltimer_ns();
   if (p.tl_next && blockIdx.x == 0 && threadIdx.x >= 32 && threadIdx.x < 32 + kTlSlots) p.tl_next[threadIdx.x - 32] = 0ull;
   // warp 0 goes straight to the router (token 0): set-up with fences or
@@ -746,7 +746,7 @@ __global__ void __launch_bounds__(kThreads, 1) layer_kernel(LayerParams p) {
   }
 
   // ---- 0. routing and lookup (every CTA); victims, plan, summary (control CTA)
-  int err = route_lookup(p, cs, ctrl, use_pre ? lg_pre : nullptr);
+  int err = route_lookup(p, cs, ctrl, mrow, use_pre ? lg_pre : nullptr);
   // counters of the next call (this call's were cleared by the previous one);
   // on every path, errors included
   if (ctrl && threadIdx.x >= kThreads - kWaveCtrs) cseq().wave_next[threadIdx.x - (kThreads - kWaveCtrs)] = 0u;
