@@ -836,16 +836,20 @@ __global__ void __launch_bounds__(kThreads, 1) layer_kernel(LayerParams p) {
   phase2<WD, MAXT, false>(p, tb, n_stage, n_res, n0, nrows, hs, os);
   if (rec) p.tl[4] = globaltimer_ns();
 
-  // the fills' slots come from the control CTA's plan
-  bool ok = true;
-  if (!ctrl && wait_flag(p.plan_flag, cseq().seq, nullptr, 5000000000ull, 32) != 0) {
-    if (threadIdx.x == 0) atomicExch(p.err, MOE_ERR_TIMEOUT);
-    ok = false;
-  }
+  // the fills' slots come from the control CTA's plan (a call without misses,
+  // which this CTA's own lookup shows, has no fills and needs no plan)
   const Plan* pl = p.plan;
-  if (ok && pl->err != MOE_OK) ok = false;
-  if (!ok) return;
-  const int nf = pl->n_items[1];
+  int nf = 0;
+  if (cs.nmiss > 0) {
+    bool ok = true;
+    if (!ctrl && wait_flag(p.plan_flag, cseq().seq, nullptr, 5000000000ull, 32) != 0) {
+      if (threadIdx.x == 0) atomicExch(p.err, MOE_ERR_TIMEOUT);
+      ok = false;
+    }
+    if (ok && pl->err != MOE_OK) ok = false;
+    if (!ok) return;
+    nf = pl->n_items[1];
+  }
   if (rec) p.tl[7] = globaltimer_ns();
 
   // ---- 3. fills ----------------------------------------------------------------------
