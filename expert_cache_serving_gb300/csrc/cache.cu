@@ -485,8 +485,9 @@ extern "C" moe_status moe_cache_create(const moe_model_desc* desc, const void* h
   const size_t obytes = (size_t)c->rows_per_cta_max * Bm * (k + 1) * 4;
   const size_t static_smem = layer_static_smem(desc->wdtype);
   const size_t budget = (size_t)smem_optin > static_smem + 1024 ? (size_t)smem_optin - static_smem - 1024 : 0;
-  // staged h rows: I floats, or for FP4 36 floats per 32 (padded against bank conflicts)
-  const size_t hrow_f = desc->wdtype == MOE_FP4 ? (size_t)I / 32 * 36 : (size_t)I;
+  // staged h rows, float32 units: I floats, or for FP4 f16 values padded to
+  // 40 per 32 (against bank conflicts), 20 float32 units per 32 values
+  const size_t hrow_f = desc->wdtype == MOE_FP4 ? (size_t)I / 32 * 20 : (size_t)I;
   const size_t need_h = (size_t)Bm * hrow_f * 4;  // one expert with every token
   if (xbytes + obytes + need_h > budget)
     return bail(fail(MOE_ERR_INVALID_ARG, "max_tokens * (H, I) too large for the layer kernel's shared memory"));

@@ -347,12 +347,19 @@ __device__ __forceinline__ unsigned short ld_down2(const uint8_t* q) {
   if constexpr (STAGED) return lds2(q); else return ld_w2<FRESH>(q);
 }
 
-// Floats between consecutive 16-byte weight chunks' activations in the
-// staged h rows: FP4 chunks cover 32 values (128 bytes, one pass over the 32
-// shared-memory banks), so eight lanes reading eight consecutive chunks would
-// all hit the same banks; 4 floats of padding per chunk spread them.
+// Staged h for the W_down phase.  bf16 / float32 models: float32 rows, the
+// chunks contiguous.  FP4 models: f16 values (the SwiGLU intermediate
+// rounded to f16, as in the FP4 prefill GEMMs), so the W_down dots run as
+// mixed-precision f16 FMAs; each 32-value chunk (64 bytes) padded to 80
+// bytes so that eight lanes reading eight consecutive chunks with 16-byte
+// loads hit distinct banks.  h_chunk_stride: values of the staged type from
+// one chunk to the next; h_row_floats: the staged row in float32 units.
 template <int WD>
-__host__ __device__ constexpr int h_chunk_stride() { return WD == MOE_FP4 ? 36 : Fmt<WD>::kElemsPerChunk; }
+__host__ __device__ constexpr int h_chunk_stride() { return WD == MOE_FP4 ? 40 : Fmt<WD>::kElemsPerChunk; }
+template <int WD>
+__host__ __device__ constexpr int h_chunk_floats() { return WD == MOE_FP4 ? 20 : Fmt<WD>::kElemsPerChunk; }
+template <int WD>
+using HStage = typename std::conditional<WD == MOE_FP4, __half, float>::type;
 
 // W_down rows [n0, n0 + nrows) of items [ib, ie) -> os[row][t][j], by the
 // warp group grp.  STAGED: the rows of item i sit in shared memory at
@@ -369,8 +376,11 @@ __device__ void phase2(const LayerParams& p, const ItemTable& tb, int ib, int ie
   const int gt = grp.tid(), gn = grp.nthreads();
   const int ostride = B * (k + 1);
   const int nchunks = I / EPC;
-  constexpr int CS = h_chunk_stride<WD>();
-  const int hrow_f = nchunks * CS;  // floats per staged h row
+  using HT = HStage<WD>;
+  constexpr int CS = h_chunk_stride<WD>();     // in HT values
+  const int hrow_f = nchunks * h_chunk_floats<WD>();  // staged row, float32 units
+  const int hrow_h = nchunks * CS;                    // staged row, HT values
+  const HT* hsv = reinterpret_cast<const HT*>(hs);
   int g0 = ib;
   while (g0 < ie) {
     int g1 = g0, used = 0;
@@ -382,9 +392,9 @@ __device__ void phase2(const LayerParams& p, const ItemTable& tb, int ib, int ie
     }
     grp.sync();
     const uint32_t par = *h_bar_phase();
-    if constexpr (CS != EPC) {
-      // padded layout (chunk c of a row at c * CS floats): plain loads and
-      // stores, four 16-byte loads in flight per thread
+    if constexpr (WD == MOE_FP4) {
+      // f16 padded layout (chunk c of a row at c * CS values): plain loads,
+      // conversion, stores; four 16-byte loads in flight per thread
       __shared__ int s_hrow[kMaxPairs + kMaxB];
       const int rows = tb.hbase[g1] - tb.hbase[g0];
       for (int rr = gt; rr < rows; rr += gn) {
@@ -407,8 +417,10 @@ __device__ void phase2(const LayerParams& p, const ItemTable& tb, int ib, int ie
         for (int u = 0; u < 4; ++u) {
           const int e = e0 + u * gn;
           if (e < n4) {
-            const int r = e / per, f = (e % per) * 4;  // float index within the row
-            *reinterpret_cast<float4*>(hs + (int64_t)r * hrow_f + (f / EPC) * CS + f % EPC) = v[u];
+            const int r = e / per, f = (e % per) * 4;  // value index within the row
+            const __half2 a = __floats2half2_rn(v[u].x, v[u].y), b = __floats2half2_rn(v[u].z, v[u].w);
+            *reinterpret_cast<uint2*>(reinterpret_cast<__half*>(hs) + (int64_t)r * hrow_h + (f / EPC) * CS + f % EPC) =
+                make_uint2(*reinterpret_cast<const uint32_t*>(&a), *reinterpret_cast<const uint32_t*>(&b));
           }
         }
       }
@@ -452,7 +464,7 @@ __device__ void phase2(const LayerParams& p, const ItemTable& tb, int ib, int ie
         const uint8_t *da = nullptr, *sa = nullptr, *db = nullptr, *sb = nullptr;
         if (live) down_row<WD, STAGED>(tb, gi, gi, n0 + ra, n0, nrows, H, I, stage, pitch, &da, &sa);
         if (live_b) down_row<WD, STAGED>(tb, gi, gi, n0 + ra + 1, n0, nrows, H, I, stage, pitch, &db, &sb);
-        const float* hrow = hs + (int64_t)(tb.hbase[gi] - tb.hbase[g0]) * hrow_f;
+        const HT* hrow = hsv + (int64_t)(tb.hbase[gi] - tb.hbase[g0]) * hrow_h;
         float acc_a = 0.f, acc_b = 0.f;
         constexpr int CPL = 4;
         for (int c0 = 0; c0 < nchunks; c0 += kLanesPerRow * CPL) {
@@ -473,9 +485,9 @@ __device__ void phase2(const LayerParams& p, const ItemTable& tb, int ib, int ie
 #pragma unroll
           for (int u = 0; u < CPL; ++u) {
             const int c = c0 + gl + kLanesPerRow * u;
-            const float* hc = hrow + (int64_t)c * CS;
-            if (live && c < nchunks) acc_a += chunk_dot<WD, float>(wa[u], ca[u], hc);
-            if (live_b && c < nchunks) acc_b += chunk_dot<WD, float>(wb[u], cb[u], hc);
+            const HT* hc = hrow + (int64_t)c * CS;
+            if (live && c < nchunks) acc_a += chunk_dot<WD, HT>(wa[u], ca[u], hc);
+            if (live_b && c < nchunks) acc_b += chunk_dot<WD, HT>(wb[u], cb[u], hc);
           }
         }
         acc_a += __shfl_xor_sync(0xFFFFFFFFu, acc_a, 4);
@@ -523,12 +535,12 @@ __device__ void phase2(const LayerParams& p, const ItemTable& tb, int ib, int ie
           const int c = c0 + gl + kLanesPerRow * u;
           if (live && c < nchunks) {
             if constexpr (WD == MOE_FP4 && MAXT > 1 && MAXT < 16) {
-              auto h_of = [&](int q) { return hs + (int64_t)(hbase + q) * hrow_f + (int64_t)c * CS; };
-              fp4_chunk_tokens<MAXT, float>(w[u], sc[u], ntok, h_of, acc);
+              auto h_of = [&](int q) { return hsv + (int64_t)(hbase + q) * hrow_h + (int64_t)c * CS; };
+              fp4_chunk_tokens<MAXT, HT>(w[u], sc[u], ntok, h_of, acc);
             } else {
 #pragma unroll
               for (int q = 0; q < MAXT; ++q)
-                if (q < ntok) acc[q] += chunk_dot<WD, float>(w[u], sc[u], hs + (int64_t)(hbase + q) * hrow_f + (int64_t)c * CS);
+                if (q < ntok) acc[q] += chunk_dot<WD, HT>(w[u], sc[u], hsv + (int64_t)(hbase + q) * hrow_h + (int64_t)c * CS);
             }
           }
         }
