@@ -186,6 +186,11 @@ moe_status moe_cache_resize(moe_cache_t cache, int64_t n_slots, void* stream);
  * with cudaMemcpyAsync on the copy streams while the resident experts already
  * run, evaluates every selected expert (and the shared expert) straight from
  * the cache slots, and writes y_t = sum_j w_tj * o_tj (+ shared) in rank order.
+ * Arithmetic: products exact, sums in float32; for MOE_FP4 models x is read as
+ * f16 (exact for 2^-14 <= |x| <= 65504 and 0) and the SwiGLU intermediate is
+ * rounded to f16 before the down projection (float32 otherwise).  Every dot
+ * product has a fixed summation order, so y is bitwise the same whatever the
+ * residency, fill mode or cache size.
  * Copy-fill mode (default): the host waits once per call for the layer
  * kernel's miss list (it issues the copies), then enqueues a small completion
  * kernel on `stream` after the call's copies; the layer kernel consumes each
