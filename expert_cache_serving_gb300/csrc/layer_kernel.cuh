@@ -319,23 +319,7 @@ __device__ void phase1(const LayerParams& p, const ItemTable& tb, int ib, int ie
       }
     }
   };
-#ifndef MOE_P1_PREFETCH_NEXT
-#define MOE_P1_PREFETCH_NEXT 0
-#endif
-  for (int64_t task = t0 + warp; task < t1; task += grp.nw) {
-    if (MOE_P1_PREFETCH_NEXT && task + grp.nw < t1) {
-      // the warp's next rows into L2 while it works on these (one line per lane)
-      const int64_t nt = task + grp.nw;
-      const int it = ib + (int)(nt / I), i = (int)(nt % I);
-      const RecView v = rec_view<WD>(tb.rec[it], H, I);
-      const int lines = (int)(rb / 128);
-      for (int l = lane; l < 2 * lines; l += 32) {
-        const uint8_t* a = (l < lines ? v.gate : v.up) + (int64_t)i * rb + (int64_t)(l % lines) * 128;
-        asm volatile("prefetch.global.L2 [%0];" ::"l"(a));
-      }
-    }
-    row_task(task);
-  }
+  for (int64_t task = t0 + warp; task < t1; task += grp.nw) row_task(task);
 }
 
 // Where W_down row `row` (and its FP4 scales) of item gi is read: its record,
