@@ -423,6 +423,26 @@ def hit_rate(st):
     return st["hits"] / (st["hits"] + st["misses"]) if st["hits"] + st["misses"] else None
 
 
+def read_ceiling(nbytes, peak):
+    """HBM read rate of a kernel that does nothing but read the same bytes per
+    launch (moe_measure_read_rate: the layer kernel's 16-byte evict-first
+    loads on every SM, buffers rotated so that no launch finds its bytes in
+    L2): the practical ceiling for one layer call of that size."""
+    import torch
+
+    from expert_cache_serving_gb300 import moecache as mc
+
+    nbytes = int(nbytes) // 16 * 16
+    n_bufs = max(2, min(16, (2 << 30) // max(nbytes, 1)))
+    buf = torch.empty(n_bufs * nbytes, dtype=torch.uint8, device="cuda")
+    buf.fill_(1)
+    reps = 3 * n_bufs
+    gbps = mc.moe_measure_read_rate(buf, nbytes, n_bufs, reps, torch.cuda.current_stream())
+    del buf
+    return {"GBps": gbps, "frac_of_peak": gbps / peak, "bytes_per_launch": nbytes, "launches": reps,
+            "kernel": "reads only (moe_measure_read_rate), one 512-thread CTA per SM, rotating buffers"}
+
+
 def kernel_roofline(inp, W, K, peak, prof_stats=None):
     """Layer-kernel HBM roofline: algorithmic bytes per launch (records
     streamed x record bytes) over the average launch time of calls without
@@ -435,6 +455,9 @@ def kernel_roofline(inp, W, K, peak, prof_stats=None):
            "traffic": None, "algorithmic_bytes_per_launch": recs * inp.S, "avg_launch_us": ms * 1e3,
            "launches": K * inp.w.L,
            "kernel": "layer_kernel, calls without fills: one warmed step replayed K times, device-fill mode"}
+    ceil = read_ceiling(recs * inp.S, peak)
+    out["read_ceiling"] = ceil
+    out["frac_of_read_ceiling"] = achieved / ceil["GBps"] if ceil["GBps"] else None
     if prof_stats is not None:
         n = prof_stats["hit_only_timed"]
         out["profiled_hit_only_avg_us"] = prof_stats["hit_only_ms"] * 1e3 / n if n else None

@@ -1289,6 +1289,17 @@ extern "C" moe_status moe_quantize_fp4(const void* x, int32_t x_dtype, int64_t r
   return MOE_OK;
 }
 
+extern "C" moe_status moe_measure_read_rate(const void* bufs, int64_t bytes, int32_t n_bufs, int32_t reps,
+                                            void* stream, double* gbps) {
+  g_err.clear();
+  if (!bufs || !gbps) return fail(MOE_ERR_INVALID_ARG, "bufs and gbps must not be NULL");
+  if (bytes <= 0 || bytes % 16 || ((uintptr_t)bufs & 15))
+    return fail(MOE_ERR_INVALID_ARG, "bytes must be a positive multiple of 16 and bufs 16-byte aligned");
+  if (n_bufs < 1 || reps < 1) return fail(MOE_ERR_INVALID_ARG, "need n_bufs >= 1 and reps >= 1");
+  CU_TRY(read_rate(static_cast<const uint8_t*>(bufs), (size_t)bytes, n_bufs, reps, (cudaStream_t)stream, gbps));
+  return MOE_OK;
+}
+
 extern "C" moe_status moe_cache_inject_fill_failure(moe_cache_t c, int32_t after) {
   if (!c) return fail(MOE_ERR_INVALID_ARG, "cache is NULL");
   c->inject_after = after;

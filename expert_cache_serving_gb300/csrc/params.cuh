@@ -63,6 +63,8 @@ struct LayerParams {
 cudaError_t launch_router_logits(const void* x, bool x_bf16, const float* wr, int B, int E, int H, float* logits,
                                  cudaStream_t s);
 size_t layer_smem_bytes(int wdtype, int B, int H, int k, int smem_h_floats, int rows_per_cta_max);
+// Read rate of a kernel that only reads `bytes` per launch (calib.cu).
+cudaError_t read_rate(const uint8_t* bufs, size_t bytes, int n_bufs, int reps, cudaStream_t s, double* gbps);
 size_t layer_static_smem(int wdtype);
 // The layer kernel of one call (pdl: launched as a programmatic dependent of
 // the previous launch on the stream), and its completion kernel, which runs

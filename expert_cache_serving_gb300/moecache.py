@@ -110,6 +110,7 @@ SIGNATURES = {
     "moe_cache_destroy": (_I32, [_P]),
     "moe_debug_bounds_enabled": (_I32, []),
     "moe_debug_violations": (_I32, [ctypes.POINTER(_I64), ctypes.POINTER(_I32)]),
+    "moe_measure_read_rate": (_I32, [_P, _I64, _I32, _I32, _P, ctypes.POINTER(ctypes.c_double)]),
     "moe_last_error": (ctypes.c_char_p, []),
     "moe_version": (_I32, []),
 }
@@ -267,6 +268,14 @@ def moe_debug_violations() -> tuple[int, int]:
     n, site = _I64(), _I32()
     check(lib.moe_debug_violations(ctypes.byref(n), ctypes.byref(site)), "moe_debug_violations")
     return n.value, site.value
+
+
+def moe_measure_read_rate(bufs, nbytes: int, n_bufs: int, reps: int, stream=None) -> float:
+    """GB/s of a kernel that only reads nbytes per launch, over n_bufs rotating buffers."""
+    g = ctypes.c_double()
+    check(lib.moe_measure_read_rate(_ptr(bufs), nbytes, n_bufs, reps, _stream(stream), ctypes.byref(g)),
+          "moe_measure_read_rate")
+    return g.value
 
 
 def moe_cache_set_graph_mode(cache: int, on: int) -> None:

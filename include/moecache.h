@@ -441,6 +441,20 @@ int32_t moe_debug_bounds_enabled(void);
  * Errors: MOE_ERR_INVALID_ARG (NULL argument), MOE_ERR_CUDA. */
 moe_status moe_debug_violations(int64_t* count, int32_t* first_site);
 
+/* Measurement aid (no counterpart on the pages): the HBM read rate, in GB/s,
+ * of a kernel that does nothing but read `bytes` per launch with the decode
+ * layer kernel's weight loads (16-byte, L2 evict-first, every SM).  bufs:
+ * device memory of n_bufs * bytes, caller-owned; launch r reads buffer
+ * r % n_bufs, so with n_bufs * bytes well above the 129 MB L2 no launch finds
+ * its bytes in L2.  One untimed pass over every buffer, then reps launches
+ * back to back timed with events on `stream`; blocks until they end.  It is
+ * the practical ceiling for a layer call that streams the same bytes (a
+ * launch's ramp-up and drain included).  Errors: MOE_ERR_INVALID_ARG (NULL,
+ * bytes not a positive multiple of 16, bufs not 16-byte aligned, n_bufs or
+ * reps < 1), MOE_ERR_CUDA. */
+moe_status moe_measure_read_rate(const void* bufs, int64_t bytes, int32_t n_bufs, int32_t reps, void* stream,
+                                 double* gbps);
+
 /* Message of the last error on this thread ("" if none). */
 const char* moe_last_error(void);
 
