@@ -59,3 +59,19 @@ def test_router_ties_nan_and_signed_zero():
     first = ref.calls[0]
     assert first.ids[0].tolist() == list(range(w.k))
     assert first.ids[1].tolist()[:4] == [1, 3, 5, 9]
+
+
+@pytest.mark.parametrize("E,k", [(256, 8), (100, 6), (64, 8)])
+def test_router_edges_wide_expert_counts(E, k):
+    """The same crafted cases with 64..256 experts (several logits per lane)."""
+    w = configs.SMALL_BF16.with_(name=f"edge-e{E}-k{k}", L=2, E=E, k=k, H=256, I=64, B=3, C=100, steps=5)
+    calls = H.decode_calls(w)
+    lg = edge_logits(w)
+    ref = H.run_oracle(w, calls, logits=lg)
+    gpu, _, _ = H.run_gpu(w, calls, logits=lg)
+    for ci, (g, r) in enumerate(zip(gpu.calls, ref.calls)):
+        assert g.status == r.status == 0, f"call {ci}"
+        assert (g.ids == r.ids).all(), f"call {ci}: ids {g.ids.tolist()} vs {r.ids.tolist()}"
+        assert np.allclose(g.w, r.w, rtol=0, atol=2e-6), f"call {ci}: weights"
+        H.assert_layer_close(g.y, r.y, f"call {ci}")
+    assert [tuple(e) for e in gpu.events] == [tuple(e) for e in ref.events]
