@@ -347,8 +347,9 @@ __device__ __forceinline__ unsigned short ld_down2(const uint8_t* q) {
   if constexpr (STAGED) return lds2(q); else return ld_w2<FRESH>(q);
 }
 
-// Staged h for the W_down phase.  bf16 / float32 models: float32 rows, the
-// chunks contiguous.  FP4 models: f16 values (the SwiGLU intermediate
+// Staged h for the W_down phase.  float32 models: float32 rows, the chunks
+// contiguous; bf16 models: float32 rows in two halves (see h_dot).  FP4
+// models: f16 values (the SwiGLU intermediate
 // rounded to f16, as in the FP4 prefill GEMMs), so the W_down dots run as
 // mixed-precision f16 FMAs; each 32-value chunk (64 bytes) padded to 80
 // bytes so that eight lanes reading eight consecutive chunks with 16-byte
@@ -360,6 +361,21 @@ template <int WD>
 __host__ __device__ constexpr int h_chunk_floats() { return WD == MOE_FP4 ? 20 : Fmt<WD>::kElemsPerChunk; }
 template <int WD>
 using HStage = typename std::conditional<WD == MOE_FP4, __half, float>::type;
+
+// W_down chunk c of a row against the staged h row `hrow`.  bf16 models stage
+// a row as two halves, floats 0-3 of every 8-value chunk and then floats 4-7,
+// so the 16-byte loads of eight lanes reading eight consecutive chunks are
+// contiguous (with whole 32-byte chunks they would be two-way bank
+// conflicts); the products and their order are chunk_dot's.
+template <int WD, typename HT>
+__device__ __forceinline__ float h_dot(uint4 w, unsigned short sc, const HT* hrow, int c, int I) {
+  if constexpr (WD == MOE_BF16) {
+    const float* r = reinterpret_cast<const float*>(hrow);
+    return dot8_bf16w(w, *reinterpret_cast<const float4*>(r + 4 * c), *reinterpret_cast<const float4*>(r + I / 2 + 4 * c));
+  } else {
+    return chunk_dot<WD, HT>(w, sc, hrow + (int64_t)c * h_chunk_stride<WD>());
+  }
+}
 
 // W_down rows [n0, n0 + nrows) of items [ib, ie) -> os[row][t][j], by the
 // warp group grp.  STAGED: the rows of item i sit in shared memory at
@@ -392,9 +408,11 @@ __device__ void phase2(const LayerParams& p, const ItemTable& tb, int ib, int ie
     }
     grp.sync();
     const uint32_t par = *h_bar_phase();
-    if constexpr (WD == MOE_FP4) {
-      // f16 padded layout (chunk c of a row at c * CS values): plain loads,
-      // conversion, stores; four 16-byte loads in flight per thread
+    if constexpr (WD == MOE_FP4 || WD == MOE_BF16) {
+      // plain loads, four 16-byte loads in flight per thread, then stores:
+      // FP4 models in the f16 padded layout (chunk c of a row at c * CS
+      // values); bf16 models as two halves, floats 0-3 of every chunk, then
+      // floats 4-7 (see h_dot)
       __shared__ int s_hrow[kMaxPairs + kMaxB];
       const int rows = tb.hbase[g1] - tb.hbase[g0];
       for (int rr = gt; rr < rows; rr += gn) {
@@ -418,13 +436,17 @@ __device__ void phase2(const LayerParams& p, const ItemTable& tb, int ib, int ie
           const int e = e0 + u * gn;
           if (e < n4) {
             const int r = e / per, f = (e % per) * 4;  // value index within the row
-            const __half2 a = __floats2half2_rn(v[u].x, v[u].y), b = __floats2half2_rn(v[u].z, v[u].w);
-            *reinterpret_cast<uint2*>(reinterpret_cast<__half*>(hs) + (int64_t)r * hrow_h + (f / EPC) * CS + f % EPC) =
-                make_uint2(*reinterpret_cast<const uint32_t*>(&a), *reinterpret_cast<const uint32_t*>(&b));
+            if constexpr (WD == MOE_FP4) {
+              const __half2 a = __floats2half2_rn(v[u].x, v[u].y), b = __floats2half2_rn(v[u].z, v[u].w);
+              *reinterpret_cast<uint2*>(reinterpret_cast<__half*>(hs) + (int64_t)r * hrow_h + (f / EPC) * CS + f % EPC) =
+                  make_uint2(*reinterpret_cast<const uint32_t*>(&a), *reinterpret_cast<const uint32_t*>(&b));
+            } else {
+              *reinterpret_cast<float4*>(hs + (int64_t)r * hrow_h + ((f % EPC) ? I / 2 : 0) + (f / EPC) * 4) = v[u];
+            }
           }
         }
       }
-    } else {  // h rows of the group, item-major: one bulk copy per row, all in flight together
+    } else {  // float32 models: h rows of the group, item-major, one bulk copy per row, all in flight together
       const int rows = tb.hbase[g1] - tb.hbase[g0];
       if (gt < 32) {
         fence_proxy_async_global();  // h was written through the generic proxy (ordered by a grid barrier)
@@ -485,9 +507,8 @@ __device__ void phase2(const LayerParams& p, const ItemTable& tb, int ib, int ie
 #pragma unroll
           for (int u = 0; u < CPL; ++u) {
             const int c = c0 + gl + kLanesPerRow * u;
-            const HT* hc = hrow + (int64_t)c * CS;
-            if (live && c < nchunks) acc_a += chunk_dot<WD, HT>(wa[u], ca[u], hc);
-            if (live_b && c < nchunks) acc_b += chunk_dot<WD, HT>(wb[u], cb[u], hc);
+            if (live && c < nchunks) acc_a += h_dot<WD, HT>(wa[u], ca[u], hrow, c, I);
+            if (live_b && c < nchunks) acc_b += h_dot<WD, HT>(wb[u], cb[u], hrow, c, I);
           }
         }
         acc_a += __shfl_xor_sync(0xFFFFFFFFu, acc_a, 4);
@@ -540,7 +561,7 @@ __device__ void phase2(const LayerParams& p, const ItemTable& tb, int ib, int ie
             } else {
 #pragma unroll
               for (int q = 0; q < MAXT; ++q)
-                if (q < ntok) acc[q] += chunk_dot<WD, HT>(w[u], sc[u], hsv + (int64_t)(hbase + q) * hrow_h + (int64_t)c * CS);
+                if (q < ntok) acc[q] += h_dot<WD, HT>(w[u], sc[u], hsv + (int64_t)(hbase + q) * hrow_h, c, I);
             }
           }
         }
