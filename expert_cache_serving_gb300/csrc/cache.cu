@@ -299,6 +299,8 @@ static moe_status check_desc(const moe_model_desc* d) {
   const int m = d->wdtype == MOE_FP4 ? 256 : 64;
   if (d->H < m || d->I < m || d->H % m || d->I % m)
     return fail(MOE_ERR_INVALID_ARG, "H and I must be positive multiples of %d for this format", m);
+  if (d->wdtype == MOE_FP4 && d->H > 16384)  // the decode kernel rearranges an activation row in registers
+    return fail(MOE_ERR_INVALID_ARG, "FP4 models need H <= 16384");
   if (d->has_shared != 0 && d->has_shared != 1) return fail(MOE_ERR_INVALID_ARG, "has_shared must be 0 or 1");
   if ((int64_t)d->L * d->E > (int64_t)1 << 30) return fail(MOE_ERR_INVALID_ARG, "L*E too large");
   return MOE_OK;

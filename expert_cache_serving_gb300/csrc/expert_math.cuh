@@ -259,9 +259,9 @@ __device__ __forceinline__ float fma_h(uint32_t a2, uint32_t b2, float acc) {
 
 // 16 e2m1 codes against 16 f16 activations (16-byte aligned), in element
 // order; the activations of FP4 decode are staged as f16 (see x_to_f16).
-template <>
-__device__ __forceinline__ float block16_dot<__half>(uint32_t c0, uint32_t c1, const __half* xs) {
-  const uint4 xa = reinterpret_cast<const uint4*>(xs)[0], xb = reinterpret_cast<const uint4*>(xs)[1];
+// The same with the block's two 8-value quarters at xa and xb (16-byte aligned).
+__device__ __forceinline__ float block16_dot_q(uint32_t c0, uint32_t c1, const __half* xa_p, const __half* xb_p) {
+  const uint4 xa = *reinterpret_cast<const uint4*>(xa_p), xb = *reinterpret_cast<const uint4*>(xb_p);
   const uint32_t xw[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
   float acc = 0.f;
 #pragma unroll
@@ -272,12 +272,25 @@ __device__ __forceinline__ float block16_dot<__half>(uint32_t c0, uint32_t c1, c
   }
   return acc;
 }
+template <>
+__device__ __forceinline__ float block16_dot<__half>(uint32_t c0, uint32_t c1, const __half* xs) {
+  return block16_dot_q(c0, c1, xs, xs + 8);
+}
 
 template <>
 __device__ __forceinline__ float chunk_dot<MOE_FP4, __half>(uint4 w, unsigned short sc2, const __half* xs) {
   float2 s = e4m3x2_to_float2(sc2);
   float a0 = block16_dot<__half>(w.x, w.y, xs);
   float a1 = block16_dot<__half>(w.z, w.w, xs + 16);
+  return fmaf(a1, s.y, a0 * s.x);
+}
+
+// chunk_dot<MOE_FP4, __half> with the chunk's four 8-value quarters qs values
+// apart (x + k * qs for quarter k): the same operations in the same order.
+__device__ __forceinline__ float chunk_dot_fp4q(uint4 w, unsigned short sc2, const __half* x, int qs) {
+  float2 s = e4m3x2_to_float2(sc2);
+  float a0 = block16_dot_q(w.x, w.y, x, x + qs);
+  float a1 = block16_dot_q(w.z, w.w, x + 2 * qs, x + 3 * qs);
   return fmaf(a1, s.y, a0 * s.x);
 }
 
@@ -334,9 +347,11 @@ __device__ __forceinline__ float block16_sum(const float* v, const float* xs) {
 
 // acc[q] += chunk_dot<MOE_FP4>(w, sc2, xs(q)) for the first ntok tokens,
 // each half of the chunk converted once: the same operations in the same
-// order as chunk_dot, token by token.
+// order as chunk_dot, token by token.  f16 values: the chunk's quarter k at
+// xs(q) + k * qs (qs = 8 for a contiguous chunk).
 template <int MAXT, typename VT, typename XF>
-__device__ __forceinline__ void fp4_chunk_tokens(uint4 w, unsigned short sc2, int ntok, XF xs_of, float* acc) {
+__device__ __forceinline__ void fp4_chunk_tokens(uint4 w, unsigned short sc2, int ntok, XF xs_of, float* acc,
+                                                 int qs = 8) {
   if constexpr (std::is_same<VT, __half>::value) {  // f16 activations: codes kept as f16 pairs
     float a0[MAXT];
     uint32_t h[8];
@@ -345,8 +360,8 @@ __device__ __forceinline__ void fp4_chunk_tokens(uint4 w, unsigned short sc2, in
 #pragma unroll
     for (int q = 0; q < MAXT; ++q) {
       if (q >= ntok) break;
-      const uint4* x4 = reinterpret_cast<const uint4*>(xs_of(q));
-      const uint4 xa = x4[0], xb = x4[1];
+      const __half* xq = xs_of(q);
+      const uint4 xa = *reinterpret_cast<const uint4*>(xq), xb = *reinterpret_cast<const uint4*>(xq + qs);
       const uint32_t xw[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
       float s0 = 0.f;
 #pragma unroll
@@ -359,8 +374,8 @@ __device__ __forceinline__ void fp4_chunk_tokens(uint4 w, unsigned short sc2, in
 #pragma unroll
     for (int q = 0; q < MAXT; ++q) {
       if (q >= ntok) break;
-      const uint4* x4 = reinterpret_cast<const uint4*>(xs_of(q)) + 2;
-      const uint4 xa = x4[0], xb = x4[1];
+      const __half* xq = xs_of(q) + 2 * qs;
+      const uint4 xa = *reinterpret_cast<const uint4*>(xq), xb = *reinterpret_cast<const uint4*>(xq + qs);
       const uint32_t xw[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
       float s1 = 0.f;
 #pragma unroll

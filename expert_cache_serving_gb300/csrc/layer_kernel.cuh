@@ -129,17 +129,41 @@ __device__ __forceinline__ void h_bar_init() {
 }
 __device__ __forceinline__ void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
 
-// FP4 models: the staged bf16 activations become f16 in place (all threads;
-// a CTA barrier must follow), so the gate/up dot products run as
-// mixed-precision f16 FMAs; exact for 2^-14 <= |x| <= 65504 and 0, smaller
-// magnitudes round to the f16 subnormal grid (absolute error <= 2^-25).
+// FP4 models: the staged bf16 activations become f16 in place (all threads),
+// so the gate/up dot products run as mixed-precision f16 FMAs; exact for
+// 2^-14 <= |x| <= 65504 and 0, smaller magnitudes round to the f16 subnormal
+// grid (absolute error <= 2^-25).  Each token's row is also rearranged so
+// that quarter q (values 8q .. 8q + 7) of every 32-value chunk c sits at
+// q * H / 4 + 8c: a lane reads its chunk as four 16-byte loads from four
+// contiguous runs, and eight lanes on eight consecutive chunks hit distinct
+// banks (with whole chunks, 64 bytes apart, they shared two bank groups).
+// H <= 16 * 2 * blockDim.x (16384 at 512 threads; the cache rejects larger).
 template <int WD, typename XT>
-__device__ __forceinline__ void x_to_f16(XT* xs, int n) {
+__device__ __forceinline__ void x_to_f16(XT* xs, int B, int H) {
   if constexpr (WD == MOE_FP4) {
-    uint32_t* w = reinterpret_cast<uint32_t*>(xs);
-    for (int i = threadIdx.x; i < n / 2; i += blockDim.x) {
-      const __half2 h = __floats2half2_rn(bf16lo(w[i]), bf16hi(w[i]));
-      w[i] = *reinterpret_cast<const uint32_t*>(&h);
+    constexpr int kPer = 16;  // words of one row per thread
+    const int nw = H / 2;
+    for (int t = 0; t < B; ++t) {
+      uint32_t* w = reinterpret_cast<uint32_t*>(xs) + (size_t)t * nw;
+      uint32_t v[kPer];
+#pragma unroll
+      for (int k = 0; k < kPer; ++k) {
+        const int i = (int)threadIdx.x + k * (int)blockDim.x;
+        if (i < nw) {
+          const __half2 h = __floats2half2_rn(bf16lo(w[i]), bf16hi(w[i]));
+          v[k] = *reinterpret_cast<const uint32_t*>(&h);
+        }
+      }
+      __syncthreads();
+#pragma unroll
+      for (int k = 0; k < kPer; ++k) {
+        const int i = (int)threadIdx.x + k * (int)blockDim.x;
+        if (i < nw) {
+          const int e = 2 * i, c = e >> 5, q = (e >> 3) & 3, r = e & 7;
+          w[(q * (H >> 2) + 8 * c + r) >> 1] = v[k];
+        }
+      }
+      __syncthreads();
     }
   }
 }
@@ -290,16 +314,23 @@ __device__ void phase1(const LayerParams& p, const ItemTable& tb, int ib, int ie
         if (c < nchunks) {
           if constexpr (WD == MOE_FP4 && MAXT > 1 && MAXT < 16) {
             // several tokens: each chunk's codes converted once (same sums as chunk_dot)
-            auto x_of = [&](int q) { return xs + (size_t)tok[q] * H + (size_t)c * EPC; };
-            fp4_chunk_tokens<MAXT, XT>(wg[u], sg[u], ntok, x_of, ag);
-            fp4_chunk_tokens<MAXT, XT>(wu[u], su[u], ntok, x_of, au);
+            // (activations in the quarter layout of x_to_f16)
+            auto x_of = [&](int q) { return xs + (size_t)tok[q] * H + (size_t)c * 8; };
+            fp4_chunk_tokens<MAXT, XT>(wg[u], sg[u], ntok, x_of, ag, H / 4);
+            fp4_chunk_tokens<MAXT, XT>(wu[u], su[u], ntok, x_of, au, H / 4);
           } else {
 #pragma unroll
             for (int q = 0; q < MAXT; ++q) {
               if (q < ntok) {
-                const XT* xr = xs + (size_t)tok[q] * H + (size_t)c * EPC;
-                ag[q] += chunk_dot<WD, XT>(wg[u], sg[u], xr);
-                au[q] += chunk_dot<WD, XT>(wu[u], su[u], xr);
+                if constexpr (WD == MOE_FP4) {  // activations in the quarter layout of x_to_f16
+                  const XT* xr = xs + (size_t)tok[q] * H + (size_t)c * 8;
+                  ag[q] += chunk_dot_fp4q(wg[u], sg[u], xr, H / 4);
+                  au[q] += chunk_dot_fp4q(wu[u], su[u], xr, H / 4);
+                } else {
+                  const XT* xr = xs + (size_t)tok[q] * H + (size_t)c * EPC;
+                  ag[q] += chunk_dot<WD, XT>(wg[u], sg[u], xr);
+                  au[q] += chunk_dot<WD, XT>(wu[u], su[u], xr);
+                }
               }
             }
           }
@@ -825,7 +856,7 @@ __global__ void __launch_bounds__(kThreads, 1) layer_kernel(LayerParams p) {
     return;
   }
   if constexpr (WD == MOE_FP4) {
-    x_to_f16<WD>(xs, B * H);
+    x_to_f16<WD>(xs, B, H);
     __syncthreads();
   }
   // this CTA has read the residency table: the control CTA may commit
@@ -997,7 +1028,7 @@ __global__ void __launch_bounds__(kThreads, 1) layer_finish_kernel(LayerParams p
     for (int i = threadIdx.x; i < nvec; i += blockDim.x) dst[i] = src[i];
     __syncthreads();
     if constexpr (WD == MOE_FP4) {
-      x_to_f16<WD>(xs, B * H);
+      x_to_f16<WD>(xs, B, H);
       __syncthreads();
     }
     phase1<WD, MAXT, false>(p, tb, 0, nf, 0, G, x_dot<WD>(xs));

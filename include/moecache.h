@@ -82,7 +82,7 @@ typedef struct {
   int32_t max_tokens; /* largest B passed to moe_layer_forward (1 .. 16) */
 } moe_model_desc;
 /* Shape rules: MOE_FP32/MOE_BF16 need H and I multiples of 64; MOE_FP4 needs
- * multiples of 256.  Activations x and outputs y are float32 for MOE_FP32
+ * multiples of 256 and H <= 16384.  Activations x and outputs y are float32 for MOE_FP32
  * models and bf16 otherwise. */
 
 typedef struct {
